@@ -1,0 +1,235 @@
+/*
+ * rkv.h - C ABI of librkv, the ResidualKV cache codec for one GB300 (sm_103a).
+ *
+ * Method: "ResidualKV:基于参考向量与残差的 KV Cache 压缩" (study notes on
+ * arXiv 2602.08005v2), cited as "ResidualKV notes §x".  The cache keeps a
+ * sparse pool of reference tokens in FP8 and, for every other token, a short
+ * quantised latent residual.  Writing a token retrieves its k nearest
+ * references, averages them and stores z = f_c(kv) - f_c(mean) quantised per
+ * group; reading a token restores KV_hat = dequant(z) W_d + mean, splits it
+ * into K and V and applies RoPE to K at the token's own position.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Pointers marked (device) are CUDA device pointers on the current device;
+ *   pointers marked (host) are ordinary host memory read before the call
+ *   returns.  No signature uses a framework type.
+ * - Ownership: the caller allocates and frees the weights, the storage
+ *   tensors (rkv_storage), all inputs and all outputs.  The library owns only
+ *   the context, its repacked weight copies, RoPE tables, scratch and a
+ *   pinned staging buffer; rkv_free releases exactly those.
+ * - Streams: `stream` is a cudaStream_t passed as void* (NULL = legacy
+ *   default stream).  Every call enqueues its work on that stream and returns
+ *   without synchronising, except rkv_create and rkv_get_status.
+ * - Errors: a negative rkv_status means nothing was launched (the message is
+ *   available from rkv_last_error).  Problems only the device can see (an
+ *   out-of-range selected position, a never-written token, a timed-out wait,
+ *   an FP16 overflow of a group extreme) never trap: the kernel clamps or
+ *   skips the row, writes zeros for it, and ORs a bit into the context's
+ *   device status word, read by rkv_get_status.
+ * - All dimensions are in elements unless a name ends in _bytes.
+ */
+#ifndef RKV_H
+#define RKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  RKV_OK = 0,
+  RKV_EINVAL = -1,      /* bad argument: shape, dtype, range, ordering       */
+  RKV_EALIGN = -2,      /* a pointer is not 16-byte aligned                  */
+  RKV_ECAPACITY = -3,   /* more tokens / references than the config allows   */
+  RKV_EEMPTYPOOL = -4,  /* a non-reference token whose pool has no reference */
+  RKV_ECUDA = -5,       /* a CUDA runtime call or kernel launch failed       */
+  RKV_EDEVICE = -6,     /* rkv_get_status: the device status word is set     */
+  RKV_ETIMEOUT = -7     /* rkv_get_status: a kernel wait gave up             */
+} rkv_status;
+
+/* element types */
+enum { RKV_F32 = 0, RKV_BF16 = 1 };
+
+/* bits of the device status word (rkv_get_status) */
+enum {
+  RKV_FLAG_TIMEOUT = 1,      /* a bounded spin-wait expired; the CTA stopped  */
+  RKV_FLAG_BAD_INDEX = 2,    /* a selected (seq, pos) was out of range        */
+  RKV_FLAG_UNWRITTEN = 4,    /* a selected token was never written            */
+  RKV_FLAG_FP16_SAT = 8,     /* a group extreme saturated at +-65504          */
+  RKV_FLAG_BAD_SLOT = 16     /* a pool slot outside [0, max_refs)             */
+};
+
+/*
+ * Codec configuration.  Shapes follow ResidualKV notes §2.1 (d_k = N*D, the
+ * joint vector kv_i has 2*d_k entries), §2.3 (d_c, d_ff), §2.4 (g, b) and §2.6
+ * (fixed reference stride s).  Limits of this build: head_dim in {64, 128,
+ * 256}; 2*d_k, d_c multiples of 64 and 2*d_k a multiple of 256; d_ff a
+ * multiple of 128; topk in 1..4; group = 32; bits in {4, 2, 16} (16 =
+ * quantisation off, z kept as bf16).
+ */
+typedef struct {
+  int32_t n_kv_heads;        /* N                                              */
+  int32_t head_dim;          /* D                                              */
+  int32_t d_c;               /* latent code width                              */
+  int32_t d_ff;              /* SwiGLU hidden width                            */
+  int32_t topk;              /* k (the page's default is 4)                    */
+  int32_t group;             /* g = 32                                         */
+  int32_t bits;              /* 4, 2 or 16                                     */
+  int32_t ref_stride;        /* s: token pos is a reference iff pos % s == 0   */
+  int32_t kv_dtype;          /* RKV_F32 or RKV_BF16: input kv rows             */
+  int32_t out_dtype;         /* RKV_F32 or RKV_BF16: restored K and V          */
+  double rope_base;          /* theta_j = rope_base^(-2j/D)                    */
+  int32_t batch;             /* number of sequences B                          */
+  int32_t max_tokens;        /* T_cap: positions per sequence                  */
+  int32_t max_refs;          /* R_cap: pool slots per sequence (>= ceil(T_cap/s)) */
+  int32_t max_rows;          /* rows one compress pass handles (0 = 32768);
+                                larger calls are processed in passes          */
+} rkv_config;
+
+/*
+ * Cache storage, allocated by the caller on the device and zero-filled or
+ * not (rkv_create initialises what needs it).  Sizes in bytes are given by
+ * rkv_storage_bytes.  All row-major; "row" = seq * T_cap + pos for token
+ * tables and seq * R_cap + slot for pool tables.
+ *   pool_fp8   [B, R_cap, 2d_k]  E4M3 references (ResidualKV notes §2.4, §3.3)
+ *   pool_bf16  [B, R_cap, 2d_k]  the same values in bf16: the tensor-core
+ *                                operand of retrieval (a compute copy)
+ *   pool_norm2 [B, R_cap]  fp32  squared norm of each decoded reference
+ *   pool_pos   [B, R_cap]  int32 position of each reference, INT32_MAX = empty
+ *   codes      [B, T_cap, code_bytes]  packed codes (d_c*b/8 bytes; 2*d_c
+ *                                for bits = 16)
+ *   meta       [B, T_cap, d_c/g, 2]  FP16 (min, max) of each group
+ *   ref_idx    [B, T_cap, topk] int32  retrieved pool slots, nearest first,
+ *                                -1 padded; a reference token stores
+ *                                [its slot, -1, ...]
+ */
+typedef struct {
+  void* pool_fp8;
+  void* pool_bf16;
+  float* pool_norm2;
+  int32_t* pool_pos;
+  void* codes;
+  void* meta;
+  int32_t* ref_idx;
+} rkv_storage;
+
+/* Byte sizes of the seven storage tensors, in the order of rkv_storage. */
+rkv_status rkv_storage_bytes(const rkv_config* cfg, size_t sizes[7]);
+
+typedef struct rkv_ctx rkv_ctx;
+
+/*
+ * Create a codec context on the current device.
+ *   Wc1, Wc2 (device, bf16) [2d_k, d_ff]; Wc3 (device, bf16) [d_ff, d_c];
+ *   Wd (device, bf16) [d_c, 2d_k] - row-major, the row-vector convention of
+ *   ResidualKV notes §2.3 (f_c) and §2.5 (f_d(z) = z W_d).  The library keeps
+ *   its own repacked copies; the caller's weights may be freed afterwards.
+ *   st: device storage (see rkv_storage); pointers must stay valid for the
+ *   context's lifetime.  rkv_create marks every pool slot empty, every token
+ *   row unwritten (ref_idx = -1) and synchronises `stream`.
+ * Returns RKV_EINVAL for an unsupported config, RKV_EALIGN for a pointer not
+ * 16-byte aligned, RKV_ECUDA if allocation or a launch fails.
+ */
+rkv_status rkv_create(const rkv_config* cfg, const void* Wc1, const void* Wc2,
+                      const void* Wc3, const void* Wd, const rkv_storage* st,
+                      void* stream, rkv_ctx** out);
+
+/*
+ * Append reference tokens to their sequences' pools (ResidualKV notes §2.6
+ * fixed stride; §2.4 and §3.3: references are stored directly, in FP8).
+ *   kv (device) rows of 2*d_k elements of cfg.kv_dtype; row r of the call
+ *     reads kv + src_rows[r] * kv_row_stride (src_rows NULL: row r).
+ *   src_rows, seq, pos (host) [n]; every pos must satisfy pos % s == 0, and
+ *     per sequence the positions must continue the sequence's references in
+ *     order (slot = pos / s).
+ * Writes pool_fp8/pool_bf16/pool_norm2/pool_pos at slot pos/s and the
+ * token's own row: ref_idx = [slot, -1, ...], codes = 0, meta = 0.
+ * Errors (nothing launched): RKV_EINVAL (range, not a reference position,
+ * out of order), RKV_ECAPACITY (slot >= R_cap).
+ */
+rkv_status rkv_pool_append(rkv_ctx* ctx, const void* kv, int64_t kv_row_stride,
+                           const int32_t* src_rows, const int32_t* seq,
+                           const int32_t* pos, int32_t n, void* stream);
+
+/*
+ * Encode non-reference tokens (ResidualKV notes §2.2 retrieval and mean,
+ * §2.3 z = f_c(kv) - f_c(mean), §2.4 group quantisation).
+ *   kv, kv_row_stride, src_rows, seq, pos: as for rkv_pool_append; every pos
+ *     must NOT be a reference position, and every reference of the sequence
+ *     before pos must already have been appended (stream order).
+ * Token i uses the references with position < pos_i, k_i = min(k, count),
+ * ties to the smaller slot.  Writes ref_idx, codes and meta of each token.
+ * Errors: RKV_EINVAL, RKV_EEMPTYPOOL (no reference before pos), RKV_ECAPACITY.
+ */
+rkv_status rkv_compress(rkv_ctx* ctx, const void* kv, int64_t kv_row_stride,
+                        const int32_t* src_rows, const int32_t* seq,
+                        const int32_t* pos, int32_t n, void* stream);
+
+/*
+ * Restore selected tokens (ResidualKV notes §2.5 KV_hat = z~ W_d + mean,
+ * §2.1 K/V split and RoPE at the token's own position, §2.7 sparse read).
+ *   seq, pos (device, int32) [n_sel]: the selected tokens, any order,
+ *     duplicates allowed.
+ *   k_out, v_out (device) [n_sel, N, D] of cfg.out_dtype: K (rotated) and V.
+ * An out-of-range (seq, pos) or a never-written token yields zero rows and a
+ * status bit (RKV_FLAG_BAD_INDEX / RKV_FLAG_UNWRITTEN).  n_sel = 0 is a no-op.
+ */
+rkv_status rkv_reconstruct(rkv_ctx* ctx, const int32_t* seq, const int32_t* pos,
+                           int32_t n_sel, void* k_out, void* v_out, void* stream);
+
+/*
+ * Forget everything written for one sequence (seq >= 0) or for all (seq = -1):
+ * its pool slots become empty and its token rows unwritten, so the slot can
+ * hold a new sequence (stream-ordered; codes and extremes are overwritten by
+ * later writes).  Errors: RKV_EINVAL for seq out of range.
+ */
+rkv_status rkv_reset(rkv_ctx* ctx, int32_t seq, void* stream);
+
+/*
+ * Read and clear the device status word (stream-ordered copy, then the
+ * stream is synchronised).  *flags receives the RKV_FLAG_* bits.  Returns
+ * RKV_OK if no bit was set, RKV_ETIMEOUT if RKV_FLAG_TIMEOUT was set,
+ * RKV_EDEVICE for any other bit, RKV_ECUDA if the copy failed.
+ */
+rkv_status rkv_get_status(rkv_ctx* ctx, int32_t* flags, void* stream);
+
+/* Message of the last non-OK status returned on this thread. */
+const char* rkv_last_error(void);
+
+/* Release the context; NULL is allowed.  Never frees caller storage. */
+void rkv_free(rkv_ctx* ctx);
+
+/* ---------------------------------------------------------------------------
+ * Instrumentation (not part of the method).
+ * rkv_set_timing(ctx, 1) records CUDA events around every kernel launch on
+ * the launching stream; rkv_get_timing returns, per kernel name, the number
+ * of launches and the summed event time since the last reset (it
+ * synchronises on the recorded events).  rkv_launch_count counts every
+ * kernel the context has launched.
+ * ------------------------------------------------------------------------- */
+typedef struct {
+  char name[48];
+  int64_t launches;
+  double total_ms;
+} rkv_kernel_timing;
+
+rkv_status rkv_set_timing(rkv_ctx* ctx, int32_t enable);
+int32_t rkv_get_timing(rkv_ctx* ctx, rkv_kernel_timing* out, int32_t max_entries,
+                       int32_t reset);
+int64_t rkv_launch_count(rkv_ctx* ctx);
+
+/*
+ * Test hook: device address and size of a scratch tensor of the last
+ * compress pass (0 = the bf16 [2*rows, 2d_k] operand rows kv/mean
+ * interleaved, 1 = the bf16 [2*rows, d_ff] SwiGLU hidden rows, the mean row
+ * negated).  Valid until the next call on the context.
+ */
+rkv_status rkv_debug_scratch(rkv_ctx* ctx, int32_t which, void** ptr, size_t* bytes);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RKV_H */

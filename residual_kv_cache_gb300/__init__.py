@@ -1,0 +1,274 @@
+"""Python binding of librkv (the ResidualKV cache codec for GB300, sm_103a).
+
+Argument marshalling only: every step of the codec runs in the CUDA library behind
+the C ABI declared in ``include/rkv.h``.  PyTorch provides device memory and streams.
+If ``librkv.so`` has not been built, importing works but any use raises
+``RkvLibraryMissing``: there is no CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+__all__ = ["RkvError", "RkvLibraryMissing", "Config", "Codec", "lib", "LIB_PATH",
+           "FLAG_TIMEOUT", "FLAG_BAD_INDEX", "FLAG_UNWRITTEN", "FLAG_FP16_SAT", "FLAG_BAD_SLOT",
+           "ABI_FUNCTIONS"]
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "librkv.so")
+
+RKV_F32, RKV_BF16 = 0, 1
+FLAG_TIMEOUT, FLAG_BAD_INDEX, FLAG_UNWRITTEN, FLAG_FP16_SAT, FLAG_BAD_SLOT = 1, 2, 4, 8, 16
+STATUS_NAMES = {0: "RKV_OK", -1: "RKV_EINVAL", -2: "RKV_EALIGN", -3: "RKV_ECAPACITY",
+                -4: "RKV_EEMPTYPOOL", -5: "RKV_ECUDA", -6: "RKV_EDEVICE", -7: "RKV_ETIMEOUT"}
+
+
+class RkvLibraryMissing(RuntimeError):
+    pass
+
+
+class RkvError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class _Config(ctypes.Structure):
+    _fields_ = [("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32),
+                ("d_c", ctypes.c_int32), ("d_ff", ctypes.c_int32), ("topk", ctypes.c_int32),
+                ("group", ctypes.c_int32), ("bits", ctypes.c_int32),
+                ("ref_stride", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
+                ("out_dtype", ctypes.c_int32), ("rope_base", ctypes.c_double),
+                ("batch", ctypes.c_int32), ("max_tokens", ctypes.c_int32),
+                ("max_refs", ctypes.c_int32), ("max_rows", ctypes.c_int32)]
+
+
+class _Storage(ctypes.Structure):
+    _fields_ = [("pool_fp8", ctypes.c_void_p), ("pool_bf16", ctypes.c_void_p),
+                ("pool_norm2", ctypes.c_void_p), ("pool_pos", ctypes.c_void_p),
+                ("codes", ctypes.c_void_p), ("meta", ctypes.c_void_p),
+                ("ref_idx", ctypes.c_void_p)]
+
+
+class _Timing(ctypes.Structure):
+    _fields_ = [("name", ctypes.c_char * 48), ("launches", ctypes.c_int64),
+                ("total_ms", ctypes.c_double)]
+
+
+# name -> (restype, argtypes); the entry points of include/rkv.h
+_P, _I32, _I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
+ABI_FUNCTIONS = {
+    "rkv_storage_bytes": (_I32, [ctypes.POINTER(_Config), ctypes.POINTER(ctypes.c_size_t)]),
+    "rkv_create": (_I32, [ctypes.POINTER(_Config), _P, _P, _P, _P, ctypes.POINTER(_Storage), _P,
+                          ctypes.POINTER(_P)]),
+    "rkv_pool_append": (_I32, [_P, _P, _I64, _P, _P, _P, _I32, _P]),
+    "rkv_compress": (_I32, [_P, _P, _I64, _P, _P, _P, _I32, _P]),
+    "rkv_reconstruct": (_I32, [_P, _P, _P, _I32, _P, _P, _P]),
+    "rkv_get_status": (_I32, [_P, ctypes.POINTER(_I32), _P]),
+    "rkv_reset": (_I32, [_P, _I32, _P]),
+    "rkv_last_error": (ctypes.c_char_p, []),
+    "rkv_free": (None, [_P]),
+    "rkv_set_timing": (_I32, [_P, _I32]),
+    "rkv_get_timing": (_I32, [_P, ctypes.POINTER(_Timing), _I32, _I32]),
+    "rkv_launch_count": (_I64, [_P]),
+    "rkv_debug_scratch": (_I32, [_P, _I32, ctypes.POINTER(_P), ctypes.POINTER(ctypes.c_size_t)]),
+}
+
+_lib = None
+
+
+def lib() -> ctypes.CDLL:
+    """Load librkv.so from this package's directory (built in-tree)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RkvLibraryMissing(
+                f"{LIB_PATH} is missing: build it with `python -m residual_kv_cache_gb300.build`")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in ABI_FUNCTIONS.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def _check(status: int):
+    if status != 0:
+        raise RkvError(status, lib().rkv_last_error().decode(errors="replace"))
+
+
+def _dtype_code(dt) -> int:
+    if dt in ("fp32", torch.float32):
+        return RKV_F32
+    if dt in ("bf16", torch.bfloat16):
+        return RKV_BF16
+    raise ValueError(f"unsupported dtype {dt}")
+
+
+def _host_i32(a):
+    """Host int32 contiguous array (numpy) and its address; None passes NULL."""
+    if a is None:
+        return None, None
+    if isinstance(a, torch.Tensor):
+        a = a.detach().cpu().numpy()
+    arr = np.ascontiguousarray(np.asarray(a, dtype=np.int32))
+    return arr, arr.ctypes.data
+
+
+def _stream_ptr(stream) -> int:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return s.cuda_stream
+
+
+@dataclass
+class Config:
+    n_kv_heads: int
+    head_dim: int
+    d_c: int
+    d_ff: int
+    topk: int = 4
+    group: int = 32
+    bits: int = 4
+    ref_stride: int = 16
+    kv_dtype: str = "bf16"
+    out_dtype: str = "bf16"
+    rope_base: float = 10000.0
+    batch: int = 1
+    max_tokens: int = 32768
+    max_refs: int = 0          # 0 -> ceil(max_tokens / ref_stride)
+    max_rows: int = 0
+
+    def to_c(self) -> _Config:
+        max_refs = self.max_refs or -(-self.max_tokens // self.ref_stride)
+        return _Config(self.n_kv_heads, self.head_dim, self.d_c, self.d_ff, self.topk,
+                       self.group, self.bits, self.ref_stride, _dtype_code(self.kv_dtype),
+                       _dtype_code(self.out_dtype), float(self.rope_base), self.batch,
+                       self.max_tokens, max_refs, self.max_rows)
+
+    @property
+    def d_kv(self) -> int:
+        return 2 * self.n_kv_heads * self.head_dim
+
+
+def storage_bytes(cfg: Config):
+    sizes = (ctypes.c_size_t * 7)()
+    c = cfg.to_c()
+    _check(lib().rkv_storage_bytes(ctypes.byref(c), sizes))
+    return list(sizes)
+
+
+class Codec:
+    """One codec layer: caller-side storage tensors plus the library context."""
+
+    STORAGE = ("pool_fp8", "pool_bf16", "pool_norm2", "pool_pos", "codes", "meta", "ref_idx")
+
+    def __init__(self, cfg: Config, weights: dict, device=None, stream=None):
+        self.cfg = cfg
+        self.device = torch.device(device or "cuda")
+        c = cfg.to_c()
+        self._c = c
+        sizes = (ctypes.c_size_t * 7)()
+        _check(lib().rkv_storage_bytes(ctypes.byref(c), sizes))
+        B, R, T = c.batch, c.max_refs, c.max_tokens
+        dkv, G = cfg.d_kv, cfg.d_c // cfg.group
+        cb = sizes[4] // (B * T)
+        dev = self.device
+        self.pool_fp8 = torch.empty((B, R, dkv), dtype=torch.uint8, device=dev)
+        self.pool_bf16 = torch.empty((B, R, dkv), dtype=torch.bfloat16, device=dev)
+        self.pool_norm2 = torch.empty((B, R), dtype=torch.float32, device=dev)
+        self.pool_pos = torch.empty((B, R), dtype=torch.int32, device=dev)
+        self.codes = torch.zeros((B, T, cb), dtype=torch.uint8, device=dev)
+        self.meta = torch.zeros((B, T, G, 2), dtype=torch.float16, device=dev)
+        self.ref_idx = torch.empty((B, T, cfg.topk), dtype=torch.int32, device=dev)
+        st = _Storage(*(getattr(self, n).data_ptr() for n in self.STORAGE))
+        w = [weights[k] for k in ("Wc1", "Wc2", "Wc3", "Wd")]
+        for t in w:
+            if t.dtype != torch.bfloat16 or not t.is_cuda or not t.is_contiguous():
+                raise ValueError("weights must be contiguous bf16 CUDA tensors")
+        ctx = ctypes.c_void_p()
+        _check(lib().rkv_create(ctypes.byref(c), *(t.data_ptr() for t in w), ctypes.byref(st),
+                                _stream_ptr(stream), ctypes.byref(ctx)))
+        self._ctx = ctx
+
+    # -- ABI calls -------------------------------------------------------------------
+    def _rows_call(self, fn, kv, seq, pos, src_rows, stream):
+        if kv.dim() != 2 or kv.shape[1] != self.cfg.d_kv or not kv.is_cuda:
+            raise ValueError("kv must be a [rows, 2*d_k] CUDA tensor")
+        seq_a, seq_p = _host_i32(seq)
+        pos_a, pos_p = _host_i32(pos)
+        src_a, src_p = _host_i32(src_rows)
+        n = len(pos_a)
+        if len(seq_a) != n or (src_a is not None and len(src_a) != n):
+            raise ValueError("seq, pos and src_rows must have the same length")
+        _check(fn(self._ctx, kv.data_ptr(), kv.stride(0), src_p, seq_p, pos_p, n,
+                  _stream_ptr(stream)))
+
+    def pool_append(self, kv, seq, pos, src_rows=None, stream=None):
+        """Append reference rows (seq, pos: host int arrays)."""
+        self._rows_call(lib().rkv_pool_append, kv, seq, pos, src_rows, stream)
+
+    def compress(self, kv, seq, pos, src_rows=None, stream=None):
+        """Encode non-reference rows (seq, pos: host int arrays)."""
+        self._rows_call(lib().rkv_compress, kv, seq, pos, src_rows, stream)
+
+    def reconstruct(self, seq, pos, k_out=None, v_out=None, stream=None):
+        """Restore selected tokens; seq, pos are int32 CUDA tensors.  Returns (K, V)."""
+        n = int(pos.numel())
+        N, D = self.cfg.n_kv_heads, self.cfg.head_dim
+        odt = torch.float32 if self.cfg.out_dtype == "fp32" else torch.bfloat16
+        if k_out is None:
+            k_out = torch.empty((n, N, D), dtype=odt, device=self.device)
+        if v_out is None:
+            v_out = torch.empty((n, N, D), dtype=odt, device=self.device)
+        for t in (seq, pos):
+            if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+                raise ValueError("seq and pos must be contiguous int32 CUDA tensors")
+        _check(lib().rkv_reconstruct(self._ctx, seq.data_ptr(), pos.data_ptr(), n,
+                                     k_out.data_ptr(), v_out.data_ptr(), _stream_ptr(stream)))
+        return k_out, v_out
+
+    def reset(self, seq: int = -1, stream=None):
+        """Empty one sequence's pool and token rows (seq = -1: all sequences)."""
+        _check(lib().rkv_reset(self._ctx, seq, _stream_ptr(stream)))
+
+    def get_status(self, stream=None) -> int:
+        flags = ctypes.c_int32(0)
+        st = lib().rkv_get_status(self._ctx, ctypes.byref(flags), _stream_ptr(stream))
+        if st not in (0, -6, -7):
+            _check(st)
+        return int(flags.value)
+
+    # -- instrumentation ---------------------------------------------------------------
+    def set_timing(self, enable: bool):
+        _check(lib().rkv_set_timing(self._ctx, 1 if enable else 0))
+
+    def get_timing(self, reset: bool = False) -> dict:
+        n = lib().rkv_get_timing(self._ctx, None, 0, 0)
+        buf = (_Timing * max(n, 1))()
+        n = lib().rkv_get_timing(self._ctx, buf, n, 1 if reset else 0)
+        return {buf[i].name.decode(): (int(buf[i].launches), float(buf[i].total_ms))
+                for i in range(n)}
+
+    def launch_count(self) -> int:
+        return int(lib().rkv_launch_count(self._ctx))
+
+    def debug_scratch(self, which: int):
+        """(device address, bytes) of a scratch tensor of the last compress pass."""
+        p, b = ctypes.c_void_p(), ctypes.c_size_t()
+        _check(lib().rkv_debug_scratch(self._ctx, which, ctypes.byref(p), ctypes.byref(b)))
+        return p.value, b.value
+
+    def free(self):
+        if getattr(self, "_ctx", None):
+            lib().rkv_free(self._ctx)
+            self._ctx = None
+
+    def __del__(self):
+        try:
+            self.free()
+        except Exception:
+            pass

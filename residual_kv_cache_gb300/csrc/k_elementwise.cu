@@ -1,0 +1,308 @@
+// k_elementwise.cu - the memory-bound kernels of the codec: storage initialisation,
+// weight repacking, reference-pool append (FP8 storage), query preparation for the
+// tensor-core retrieval, and the reference-mean rows of the encoder operand.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
+#include <stdint.h>
+
+#include <climits>
+
+#include "rkv_internal.h"
+
+namespace rkv {
+namespace {
+
+__device__ __forceinline__ float fp8_to_float(uint8_t b) {
+  __half_raw h = __nv_cvt_fp8_to_halfraw(static_cast<__nv_fp8_storage_t>(b), __NV_E4M3);
+  return __half2float(__half(h));
+}
+
+// Decode 8 E4M3 bytes (little-endian in a uint2) to floats; exact.
+__device__ __forceinline__ void fp8x8_to_float(uint2 v, float* f) {
+  const uint32_t w[2] = {v.x, v.y};
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      __nv_fp8x2_storage_t pair = static_cast<__nv_fp8x2_storage_t>((w[i] >> (16 * j)) & 0xFFFFu);
+      __half2_raw h2 = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
+      __half2 hh(h2);
+      float2 ff = __half22float2(hh);
+      f[4 * i + 2 * j] = ff.x;
+      f[4 * i + 2 * j + 1] = ff.y;
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat16 lo = __float2bfloat16_rn(a), hi = __float2bfloat16_rn(b);
+  return static_cast<uint32_t>(__bfloat16_as_ushort(lo)) |
+         (static_cast<uint32_t>(__bfloat16_as_ushort(hi)) << 16);
+}
+
+// ---------------------------------------------------------------- init
+__global__ void init_storage_kernel(int32_t* pool_pos, int64_t n_pool, int32_t* ref_idx,
+                                    int64_t n_idx) {
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_pool;
+       i += (int64_t)gridDim.x * blockDim.x)
+    pool_pos[i] = INT_MAX;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_idx;
+       i += (int64_t)gridDim.x * blockDim.x)
+    ref_idx[i] = -1;
+}
+
+// out[r][k] = src[k][col(r)] for a [K, N] row-major source; the W_c1/W_c2 pair is
+// interleaved in 256-row tiles (128 rows of each) so one accumulator tile holds
+// matching gate and value columns.
+__global__ void repack_kernel(const __nv_bfloat16* __restrict__ a, const __nv_bfloat16* __restrict__ b,
+                              __nv_bfloat16* __restrict__ out, int K, int N_src, int rows,
+                              int interleave) {
+  const int64_t total = (int64_t)rows * K;
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < total;
+       i += (int64_t)gridDim.x * blockDim.x) {
+    const int r = (int)(i / K);
+    const int k = (int)(i % K);
+    const __nv_bfloat16* src = a;
+    int col = r;
+    if (interleave) {
+      const int j = r / kEncN, u = r % kEncN;
+      col = j * (kEncN / 2) + (u % (kEncN / 2));
+      src = (u < kEncN / 2) ? a : b;
+    }
+    out[i] = src[(int64_t)k * N_src + col];
+  }
+}
+
+// ---------------------------------------------------------------- pool append
+// One block per reference row.  plan row: {src row, pool row, pos, token row}.
+__global__ void pool_append_kernel(const void* __restrict__ kv, int64_t stride, int kv_f32,
+                                   const int32_t* __restrict__ plan, int dkv, int R_cap,
+                                   uint8_t* __restrict__ pool8, __nv_bfloat16* __restrict__ poolb,
+                                   float* __restrict__ norm2, int32_t* __restrict__ pool_pos,
+                                   int32_t* __restrict__ ref_idx, int topk,
+                                   uint8_t* __restrict__ codes, int code_bytes,
+                                   uint32_t* __restrict__ meta, int G) {
+  const int r = blockIdx.x;
+  const int64_t src = plan[4 * r + 0];
+  const int64_t prow = plan[4 * r + 1];
+  const int32_t pos = plan[4 * r + 2];
+  const int64_t tok = plan[4 * r + 3];
+  double acc = 0.0;
+  for (int e = threadIdx.x * 4; e < dkv; e += blockDim.x * 4) {
+    float v[4];
+    if (kv_f32) {
+      const float4 x = *reinterpret_cast<const float4*>(
+          static_cast<const float*>(kv) + src * stride + e);
+      v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
+    } else {
+      const uint2 x = *reinterpret_cast<const uint2*>(
+          static_cast<const __nv_bfloat16*>(kv) + src * stride + e);
+      v[0] = __uint_as_float(x.x << 16);
+      v[1] = __uint_as_float(x.x & 0xFFFF0000u);
+      v[2] = __uint_as_float(x.y << 16);
+      v[3] = __uint_as_float(x.y & 0xFFFF0000u);
+    }
+    uint32_t packed = 0;
+    float d[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_fp8_storage_t q = __nv_cvt_float_to_fp8(v[i], __NV_SATFINITE, __NV_E4M3);
+      packed |= static_cast<uint32_t>(q) << (8 * i);
+      d[i] = fp8_to_float(q);
+      acc += (double)d[i] * (double)d[i];   // exact: squares of E4M3 values
+    }
+    *reinterpret_cast<uint32_t*>(pool8 + prow * dkv + e) = packed;
+    uint2 bv;
+    bv.x = pack_bf16x2(d[0], d[1]);
+    bv.y = pack_bf16x2(d[2], d[3]);
+    *reinterpret_cast<uint2*>(poolb + prow * dkv + e) = bv;
+  }
+  // block sum of the squared norm (float64, exact in any order)
+  __shared__ double red[32];
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double s = 0.0;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += red[w];
+    norm2[prow] = (float)s;
+    pool_pos[prow] = pos;
+    const int32_t slot = (int32_t)(prow % R_cap);
+    ref_idx[tok * topk] = slot;
+    for (int t = 1; t < topk; ++t) ref_idx[tok * topk + t] = -1;
+  }
+  for (int i = threadIdx.x; i < code_bytes; i += blockDim.x) codes[tok * code_bytes + i] = 0;
+  for (int i = threadIdx.x; i < G; i += blockDim.x) meta[tok * G + i] = 0u;
+}
+
+// ---------------------------------------------------------------- queries
+// One block per retrieval-order row: bf16 copy of kv, or for fp32 kv the three bf16
+// pieces hi, mid, lo with hi + mid + lo == x exactly (each piece takes the next 8
+// significant bits), laid out [hi | mid | lo] along the row.
+__global__ void prep_queries_kernel(const void* __restrict__ kv, int64_t stride, int kv_f32,
+                                    const int32_t* __restrict__ q_src, int dkv, int parts,
+                                    __nv_bfloat16* __restrict__ Q) {
+  const int64_t row = blockIdx.x;
+  const int64_t src = q_src[row];
+  __nv_bfloat16* out = Q + row * (int64_t)parts * dkv;
+  for (int e = threadIdx.x * 4; e < dkv; e += blockDim.x * 4) {
+    if (src < 0) {
+      for (int p = 0; p < parts; ++p)
+        *reinterpret_cast<uint2*>(out + p * dkv + e) = make_uint2(0u, 0u);
+      continue;
+    }
+    if (!kv_f32) {
+      *reinterpret_cast<uint2*>(out + e) = *reinterpret_cast<const uint2*>(
+          static_cast<const __nv_bfloat16*>(kv) + src * stride + e);
+      continue;
+    }
+    const float4 x4 = *reinterpret_cast<const float4*>(
+        static_cast<const float*>(kv) + src * stride + e);
+    const float x[4] = {x4.x, x4.y, x4.z, x4.w};
+    float pc[3][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float rem = x[i];
+#pragma unroll
+      for (int p = 0; p < 3; ++p) {
+        const float h = __bfloat162float(__float2bfloat16_rn(rem));
+        pc[p][i] = h;
+        rem = __fsub_rn(rem, h);   // exact
+      }
+    }
+    for (int p = 0; p < parts; ++p) {
+      uint2 v;
+      v.x = pack_bf16x2(pc[p][0], pc[p][1]);
+      v.y = pack_bf16x2(pc[p][2], pc[p][3]);
+      *reinterpret_cast<uint2*>(out + p * dkv + e) = v;
+    }
+  }
+}
+
+// ---------------------------------------------------------------- mean rows
+// One block per compact row r: X[2r] = bf16 kv (the hi piece of the query row),
+// X[2r+1] = bf16(mean of the retrieved FP8 references).  The sum of at most four
+// E4M3 values is exact in fp32; it is divided by k_i once (IEEE division).
+__global__ void mean_rows_kernel(const int32_t* __restrict__ c_q, const int32_t* __restrict__ c_dst,
+                                 const __nv_bfloat16* __restrict__ Q, int parts,
+                                 const uint8_t* __restrict__ pool8,
+                                 const int32_t* __restrict__ ref_idx, int topk, int dkv,
+                                 int T_cap, int R_cap, __nv_bfloat16* __restrict__ X,
+                                 int* __restrict__ status) {
+  const int64_t r = blockIdx.x;
+  const int64_t qrow = c_q[r];
+  const int64_t dst = c_dst[r];
+  const int64_t seq = dst / T_cap;
+  int64_t prow[4];
+  int k_i = 0;
+  for (int t = 0; t < topk; ++t) {
+    const int32_t s = ref_idx[dst * topk + t];
+    if (s >= 0 && s < R_cap) prow[k_i++] = seq * R_cap + s;
+  }
+  if (k_i == 0 && threadIdx.x == 0) atomicOr(status, RKV_FLAG_UNWRITTEN);
+  const __nv_bfloat16* q = Q + qrow * (int64_t)parts * dkv;
+  __nv_bfloat16* xk = X + (2 * r) * (int64_t)dkv;
+  __nv_bfloat16* xm = X + (2 * r + 1) * (int64_t)dkv;
+  const float kf = (float)(k_i > 0 ? k_i : 1);
+  for (int e = threadIdx.x * 8; e < dkv; e += blockDim.x * 8) {
+    *reinterpret_cast<uint4*>(xk + e) = *reinterpret_cast<const uint4*>(q + e);
+    float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int t = 0; t < k_i; ++t) {
+      float f[8];
+      fp8x8_to_float(*reinterpret_cast<const uint2*>(pool8 + prow[t] * dkv + e), f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) s[i] = __fadd_rn(s[i], f[i]);
+    }
+    uint4 o;
+    o.x = pack_bf16x2(__fdiv_rn(s[0], kf), __fdiv_rn(s[1], kf));
+    o.y = pack_bf16x2(__fdiv_rn(s[2], kf), __fdiv_rn(s[3], kf));
+    o.z = pack_bf16x2(__fdiv_rn(s[4], kf), __fdiv_rn(s[5], kf));
+    o.w = pack_bf16x2(__fdiv_rn(s[6], kf), __fdiv_rn(s[7], kf));
+    *reinterpret_cast<uint4*>(xm + e) = o;
+  }
+}
+
+int grid_for(int64_t n, int threads, int cap) {
+  int64_t g = (n + threads - 1) / threads;
+  if (g < 1) g = 1;
+  if (g > cap) g = cap;
+  return (int)g;
+}
+
+}  // namespace
+
+cudaError_t launch_init_storage(rkv_ctx* c, cudaStream_t s, int seq) {
+  int64_t n_pool = (int64_t)c->d.B * c->d.R_cap;
+  int64_t n_idx = (int64_t)c->d.B * c->d.T_cap * c->d.topk;
+  int32_t* pool_pos = c->st.pool_pos;
+  int32_t* ref_idx = c->st.ref_idx;
+  if (seq >= 0) {
+    n_pool = c->d.R_cap;
+    n_idx = (int64_t)c->d.T_cap * c->d.topk;
+    pool_pos += (int64_t)seq * n_pool;
+    ref_idx += (int64_t)seq * n_idx;
+  }
+  cudaEvent_t ev;
+  timing_begin(c, "rkv_init_storage_kernel", s, &ev);
+  init_storage_kernel<<<grid_for(n_idx > n_pool ? n_idx : n_pool, 256, 4096), 256, 0, s>>>(
+      pool_pos, n_pool, ref_idx, n_idx);
+  cudaError_t e = cudaGetLastError();
+  timing_end(c, "rkv_init_storage_kernel", s, ev);
+  return e;
+}
+
+cudaError_t launch_repack_weights(rkv_ctx* c, const __nv_bfloat16* Wc1, const __nv_bfloat16* Wc2,
+                                  const __nv_bfloat16* Wc3, const __nv_bfloat16* Wd,
+                                  cudaStream_t s) {
+  const Dims& d = c->d;
+  repack_kernel<<<grid_for((int64_t)2 * d.dff * d.dkv, 256, 8192), 256, 0, s>>>(
+      Wc1, Wc2, c->w12, d.dkv, d.dff, 2 * d.dff, 1);
+  repack_kernel<<<grid_for((int64_t)d.dc * d.dff, 256, 8192), 256, 0, s>>>(
+      Wc3, nullptr, c->w3, d.dff, d.dc, d.dc, 0);
+  repack_kernel<<<grid_for((int64_t)d.dkv * d.dc, 256, 8192), 256, 0, s>>>(
+      Wd, nullptr, c->wd, d.dc, d.dkv, d.dkv, 0);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_pool_append(rkv_ctx* c, const void* kv, int64_t stride, const int32_t* plan,
+                               int n, cudaStream_t s) {
+  const Dims& d = c->d;
+  cudaEvent_t ev;
+  timing_begin(c, "rkv_pool_append_kernel", s, &ev);
+  pool_append_kernel<<<n, 256, 0, s>>>(kv, stride, d.kv_f32, plan, d.dkv, d.R_cap,
+                                       static_cast<uint8_t*>(c->st.pool_fp8),
+                                       static_cast<__nv_bfloat16*>(c->st.pool_bf16),
+                                       c->st.pool_norm2, c->st.pool_pos, c->st.ref_idx, d.topk,
+                                       static_cast<uint8_t*>(c->st.codes), d.code_bytes,
+                                       static_cast<uint32_t*>(c->st.meta), d.G);
+  cudaError_t e = cudaGetLastError();
+  timing_end(c, "rkv_pool_append_kernel", s, ev);
+  return e;
+}
+
+cudaError_t launch_prep_queries(rkv_ctx* c, const void* kv, int64_t stride, const int32_t* q_src,
+                                int m_pad, cudaStream_t s) {
+  const Dims& d = c->d;
+  cudaEvent_t ev;
+  timing_begin(c, "rkv_prep_queries_kernel", s, &ev);
+  prep_queries_kernel<<<m_pad, 256, 0, s>>>(kv, stride, d.kv_f32, q_src, d.dkv, d.parts, c->Q);
+  cudaError_t e = cudaGetLastError();
+  timing_end(c, "rkv_prep_queries_kernel", s, ev);
+  return e;
+}
+
+cudaError_t launch_mean_rows(rkv_ctx* c, const PassPlan& p, const int32_t* plan, cudaStream_t s) {
+  const Dims& d = c->d;
+  cudaEvent_t ev;
+  timing_begin(c, "rkv_mean_rows_kernel", s, &ev);
+  mean_rows_kernel<<<p.n_rows, 256, 0, s>>>(plan + p.off_c_q, plan + p.off_c_dst, c->Q, d.parts,
+                                            static_cast<const uint8_t*>(c->st.pool_fp8),
+                                            c->st.ref_idx, d.topk, d.dkv, d.T_cap, d.R_cap, c->X,
+                                            c->status);
+  cudaError_t e = cudaGetLastError();
+  timing_end(c, "rkv_mean_rows_kernel", s, ev);
+  return e;
+}
+
+}  // namespace rkv

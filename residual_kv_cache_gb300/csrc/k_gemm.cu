@@ -1,0 +1,392 @@
+// k_gemm.cu - the encoder's two tensor-core GEMMs (ResidualKV notes §2.3, §2.4).
+//
+//   GEMM-1/2:  [kv; mean] rows x [W_c1 | W_c2]  ->  H = Swish(a1) * a2   (bf16)
+//              A = X [2n, 2d_k] (row 2r = bf16 kv_r, row 2r+1 = bf16 mean_r),
+//              B = W12 [2 d_ff, 2d_k] with gate and value columns interleaved per
+//              256-row tile so that one 128x256 accumulator holds a1 and a2 of the same
+//              128 hidden units.  The epilogue applies the SwiGLU gate and stores the
+//              mean rows negated (an exact bf16 sign flip).
+//   GEMM-3:    H viewed as [n, 2 d_ff] (row r = [h(kv_r) | -h(mean_r)]) x W_c3^T
+//              -> z_r = h(kv_r) W_c3 - h(mean_r) W_c3 in one fp32 accumulator: both f_c
+//              outputs are mapped before the subtraction, never f_c of a difference.
+//              The epilogue quantises each 32-column group in the thread that owns the
+//              token row (min/max, FP16 extremes rounded outward, Delta, round-half-
+//              even, clamp, nibble/crumb packing) and writes codes and extremes.
+//
+// Both run one persistent CTA per SM: a 4..6-stage TMA ring feeds tcgen05.mma (M=128,
+// K=16 per instruction, fp32 accumulators in TMEM), two TMEM accumulators let the
+// epilogue of tile t overlap the main loop of tile t+1.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "tc_common.cuh"
+
+namespace rkv {
+namespace {
+
+struct GemmShape {
+  int m_tiles, n_tiles, nkb;  // tiles of 128 rows, tiles of BN columns, 64-wide k-blocks
+  int b_kwrap;                // B's k-block coordinate is kb % b_kwrap
+  int* status;
+};
+
+struct Epi12Args {
+  __nv_bfloat16* H;
+  int dff;
+  int rows;  // valid A rows (2 n)
+};
+
+struct Epi3Args {
+  const int32_t* c_dst;
+  int rows;  // valid token rows
+  uint8_t* codes;
+  uint32_t* meta;
+  int code_bytes, G, bits, BN;
+};
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  __nv_bfloat16 lo = __float2bfloat16_rn(a), hi = __float2bfloat16_rn(b);
+  return static_cast<uint32_t>(__bfloat16_as_ushort(lo)) |
+         (static_cast<uint32_t>(__bfloat16_as_ushort(hi)) << 16);
+}
+
+// ---------------------------------------------------------------- epilogues
+struct Epi12 {
+  using Args = Epi12Args;
+  static constexpr int BN = kEncN;
+  __device__ static void run(const Args& a, uint32_t tacc, int m, int n, int row_in_tile,
+                             int* status) {
+    const int64_t row = (int64_t)m * kTileM + row_in_tile;
+    const bool valid = row < a.rows;
+    const float sign = (row & 1) ? -1.0f : 1.0f;
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      uint32_t g[32], v[32];
+      tmem_ld32(tacc + c * 32, g);
+      tmem_ld32(tacc + 128 + c * 32, v);
+      tmem_ld_wait();
+      if (!valid) continue;
+      uint32_t w[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        float h[2];
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+          const float a1 = __uint_as_float(g[2 * i + j]);
+          const float a2 = __uint_as_float(v[2 * i + j]);
+          const float sw = a1 / (1.0f + expf(-a1));   // Swish, beta = 1
+          h[j] = sign * (sw * a2);
+        }
+        w[i] = pack_bf16x2(h[0], h[1]);
+      }
+      uint4* dst = reinterpret_cast<uint4*>(a.H + row * a.dff + (int64_t)n * 128 + c * 32);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    }
+  }
+};
+
+// Quantise one 32-value group held by this thread and write its code bytes and extremes.
+__device__ __forceinline__ void quant_group(const float* z, int bits, uint8_t* code, uint32_t* meta,
+                                            int* status) {
+  if (bits == 16) {
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) w[i] = pack_bf16x2(z[2 * i], z[2 * i + 1]);
+    uint4* d = reinterpret_cast<uint4*>(code);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) d[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+    *meta = 0u;
+    return;
+  }
+  float zmin = z[0], zmax = z[0];
+#pragma unroll
+  for (int i = 1; i < 32; ++i) {
+    zmin = fminf(zmin, z[i]);
+    zmax = fmaxf(zmax, z[i]);
+  }
+  const bool sat = (fabsf(zmin) > 65504.0f) || (fabsf(zmax) > 65504.0f);
+  if (sat) atomicOr(status, RKV_FLAG_FP16_SAT);
+  __half lo16, hi16;
+  const bool constant = (zmin == zmax);
+  if (constant) {
+    lo16 = __float2half_rn(fminf(fmaxf(zmin, -65504.0f), 65504.0f));
+    hi16 = lo16;
+  } else {
+    lo16 = __float2half_rd(fmaxf(zmin, -65504.0f));
+    hi16 = __float2half_ru(fminf(zmax, 65504.0f));
+  }
+  const float lo = __half2float(lo16), hi = __half2float(hi16);
+  const int levels = (1 << bits) - 1;
+  const float delta = __fdiv_rn(__fsub_rn(hi, lo), (float)levels);
+  const bool zero = constant || (delta == 0.0f);
+  int q[32];
+#pragma unroll
+  for (int i = 0; i < 32; ++i) {
+    int v = zero ? 0 : __float2int_rn(__fdiv_rn(__fsub_rn(z[i], lo), delta));
+    q[i] = v < 0 ? 0 : (v > levels ? levels : v);
+  }
+  if (bits == 4) {
+    uint32_t w[4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      uint32_t x = 0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) x |= (uint32_t)q[8 * k + i] << (4 * i);
+      w[k] = x;
+    }
+    *reinterpret_cast<uint4*>(code) = make_uint4(w[0], w[1], w[2], w[3]);
+  } else {  // bits == 2
+    uint32_t w[2];
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+      uint32_t x = 0;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) x |= (uint32_t)q[16 * k + i] << (2 * i);
+      w[k] = x;
+    }
+    *reinterpret_cast<uint2*>(code) = make_uint2(w[0], w[1]);
+  }
+  *meta = (uint32_t)__half_as_ushort(lo16) | ((uint32_t)__half_as_ushort(hi16) << 16);
+}
+
+struct Epi3 {
+  using Args = Epi3Args;
+  __device__ static void run(const Args& a, uint32_t tacc, int m, int n, int row_in_tile,
+                             int* status) {
+    const int64_t row = (int64_t)m * kTileM + row_in_tile;
+    const bool valid = row < a.rows;
+    const int64_t dst = valid ? (int64_t)a.c_dst[row] : 0;
+    const int groups = a.BN / 32;
+#pragma unroll 1
+    for (int gi = 0; gi < groups; ++gi) {
+      uint32_t r[32];
+      tmem_ld32(tacc + gi * 32, r);
+      tmem_ld_wait();
+      if (!valid) continue;
+      float z[32];
+#pragma unroll
+      for (int i = 0; i < 32; ++i) z[i] = __uint_as_float(r[i]);
+      const int g = n * groups + gi;   // group index within the token
+      uint8_t* code = a.codes + dst * a.code_bytes + (int64_t)g * (a.bits * 32 / 8);
+      uint32_t* meta = a.meta + dst * a.G + g;
+      quant_group(z, a.bits, code, meta, status);
+    }
+  }
+};
+
+// ---------------------------------------------------------------- kernel
+template <int BN, int STAGES, typename Epi>
+__global__ void __launch_bounds__(kThreads, 1)
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                   GemmShape g, typename Epi::Args ea) {
+  constexpr uint32_t kBBytes = BN * 128;
+  constexpr uint32_t kTmemCols = 2 * BN;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * kTileABytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * kBBytes);
+  uint64_t* empty = full + STAGES;
+  uint64_t* tfull = empty + STAGES;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int n_tiles_total = g.m_tiles * g.n_tiles;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 128);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch(&tmA);
+    tma_prefetch(&tmB);
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    // ------------------------------------------------ TMA producer
+    if (elect_one()) {
+      Ring ring;
+      int issued[STAGES];
+      uint32_t issued_phase[STAGES];
+      for (int s = 0; s < STAGES; ++s) issued[s] = 0, issued_phase[s] = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < n_tiles_total && ok; t += gridDim.x) {
+        const int m = t / g.n_tiles, n = t % g.n_tiles;
+        for (int kb = 0; kb < g.nkb; ++kb) {
+          if (!mbar_wait(&empty[ring.stage], ring.phase ^ 1u, abort_flag, g.status)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(&full[ring.stage], kTileABytes + kBBytes);
+          tma_load_2d(sA + ring.stage * kTileABytes, &tmA, &full[ring.stage], kb * kTileK,
+                      m * kTileM);
+          const int kbB = kb % g.b_kwrap;
+          for (int h = 0; h < BN; h += 256)
+            tma_load_2d(sB + ring.stage * kBBytes + h * 128, &tmB, &full[ring.stage],
+                        kbB * kTileK, n * BN + h);
+          issued[ring.stage] = 1;
+          issued_phase[ring.stage] = ring.phase;
+          ring.next(STAGES);
+        }
+      }
+      if (!ok) {
+        for (int s = 0; s < STAGES; ++s)
+          if (issued[s]) drain_wait(&full[s], issued_phase[s]);
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------ MMA issuer
+    if (elect_one()) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kTileM, BN > 256 ? 256 : BN);
+      Ring ring;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true;
+      bool any = false;
+      int last_stage = 0;
+      uint32_t last_phase = 0;
+      for (int t = blockIdx.x; t < n_tiles_total && ok; t += gridDim.x) {
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, g.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d = tmem + acc * BN;
+        for (int kb = 0; kb < g.nkb; ++kb) {
+          if (!mbar_wait(&full[ring.stage], ring.phase, abort_flag, g.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a0 = smem_u32(sA + ring.stage * kTileABytes);
+          const uint32_t b0 = smem_u32(sB + ring.stage * kBBytes);
+#pragma unroll
+          for (int k = 0; k < kTileK / 16; ++k) {
+            for (int h = 0; h < BN; h += 256)
+              umma_bf16(d + h, sdesc_sw128(a0 + k * 32), sdesc_sw128(b0 + h * 128 + k * 32),
+                        idesc, (kb | k) != 0 ? 1u : 0u);
+          }
+          umma_commit(&empty[ring.stage]);
+          any = true;
+          last_stage = ring.stage;
+          last_phase = ring.phase;
+          ring.next(STAGES);
+        }
+        if (!ok) break;
+        umma_commit(&tfull[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok && any) drain_wait(&empty[last_stage], last_phase);
+    }
+  } else if (warp >= kEpiWarp0) {
+    // ------------------------------------------------ epilogue
+    const int ew = warp - kEpiWarp0;
+    const int row_in_tile = ew * 32 + (int)lane_id();
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int t = blockIdx.x; t < n_tiles_total; t += gridDim.x) {
+      const int m = t / g.n_tiles, n = t % g.n_tiles;
+      if (!warp_wait(&tfull[acc], acc_phase, abort_flag, g.status)) break;
+      tc_fence_after();
+      const uint32_t tacc = tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)(acc * BN);
+      Epi::run(ea, tacc, m, n, row_in_tile, g.status);
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+template <int BN, int STAGES>
+constexpr size_t gemm_smem_bytes() {
+  return 1024 + (size_t)STAGES * (kTileABytes + BN * 128) + 8 * (2 * STAGES + 4) + 16;
+}
+
+template <int BN, int STAGES, typename Epi>
+cudaError_t run_gemm(rkv_ctx* c, const CUtensorMap& tA, const CUtensorMap& tB, GemmShape g,
+                     typename Epi::Args ea, const char* name, cudaStream_t s) {
+  const size_t smem = gemm_smem_bytes<BN, STAGES>();
+  auto kern = tc_gemm_kernel<BN, STAGES, Epi>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  const int tiles = g.m_tiles * g.n_tiles;
+  if (tiles == 0) return cudaSuccess;
+  const int grid = tiles < c->num_sms ? tiles : c->num_sms;
+  cudaEvent_t ev;
+  timing_begin(c, name, s, &ev);
+  kern<<<grid, kThreads, smem, s>>>(tA, tB, g, ea);
+  e = cudaGetLastError();
+  timing_end(c, name, s, ev);
+  return e;
+}
+
+}  // namespace
+
+cudaError_t launch_gemm12(rkv_ctx* c, int n_rows, cudaStream_t s) {
+  const Dims& d = c->d;
+  GemmShape g;
+  g.m_tiles = (2 * n_rows + kTileM - 1) / kTileM;
+  g.n_tiles = (2 * d.dff) / kEncN;
+  g.nkb = d.dkv / kTileK;
+  g.b_kwrap = g.nkb;
+  g.status = c->status;
+  Epi12Args ea{c->H, d.dff, 2 * n_rows};
+  return run_gemm<kEncN, 4, Epi12>(c, c->tm_x, c->tm_w12, g, ea, "rkv_gemm12_swiglu_kernel", s);
+}
+
+cudaError_t launch_gemm3_quant(rkv_ctx* c, const PassPlan& p, const int32_t* plan,
+                               cudaStream_t s) {
+  const Dims& d = c->d;
+  GemmShape g;
+  g.m_tiles = (p.n_rows + kTileM - 1) / kTileM;
+  g.nkb = (2 * d.dff) / kTileK;
+  g.b_kwrap = d.dff / kTileK;
+  g.status = c->status;
+  Epi3Args ea{plan + p.off_c_dst, p.n_rows, static_cast<uint8_t*>(c->st.codes),
+              static_cast<uint32_t*>(c->st.meta), d.code_bytes, d.G, d.bits, 0};
+  const char* name = "rkv_gemm3_quant_kernel";
+  if (d.dc % 256 == 0) {
+    g.n_tiles = d.dc / 256;
+    ea.BN = 256;
+    return run_gemm<256, 4, Epi3>(c, c->tm_h3, c->tm_w3, g, ea, name, s);
+  } else if (d.dc % 128 == 0) {
+    g.n_tiles = d.dc / 128;
+    ea.BN = 128;
+    return run_gemm<128, 6, Epi3>(c, c->tm_h3, c->tm_w3, g, ea, name, s);
+  }
+  g.n_tiles = d.dc / 64;
+  ea.BN = 64;
+  return run_gemm<64, 6, Epi3>(c, c->tm_h3, c->tm_w3, g, ea, name, s);
+}
+
+}  // namespace rkv

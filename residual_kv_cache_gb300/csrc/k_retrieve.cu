@@ -1,0 +1,277 @@
+// k_retrieve.cu - global top-k L2 retrieval of references (ResidualKV notes §2.2, the
+// arg top-k_i equation; k_i = min(k, |T_ref,i|), T_ref,i = references before token i).
+//
+// For a tile of 128 query tokens of one sequence and a tile of 256 pool slots the
+// tensor cores compute the dot products a_i . r_j (bf16 operands, exact products, fp32
+// accumulation in TMEM).  The epilogue thread that owns query row i (one TMEM lane)
+// turns each into the ranking score ||r_j||^2 - 2 a_i . r_j (= ||a_i - r_j||^2 minus a
+// per-row constant), masks slots whose reference is not strictly before the token,
+// and keeps a sorted running top-4 in registers across the pool tiles; equal scores
+// keep the smaller slot because slots are visited in increasing order with a strict
+// comparison.  fp32 queries are split into three bf16 pieces (hi + mid + lo == x), so
+// the products stay exact and the three partial dots accumulate into one fp32 sum.
+//
+// Work unit = one 128-query tile; its pool tiles are the causal prefix only, so tiles
+// late in the sequence do more work; the host plan orders units heaviest first.
+#include <cuda_bf16.h>
+#include <float.h>
+
+#include "tc_common.cuh"
+
+namespace rkv {
+namespace {
+
+struct RetrieveArgs {
+  const int32_t* t_seq;
+  const int32_t* t_row0;
+  const int32_t* t_nrt;
+  const int32_t* q_pos;
+  const int32_t* q_dst;
+  int n_units;
+  int nkb;      // k-blocks per piece (2d_k / 64)
+  int parts;    // 1 or 3
+  int R_cap, topk;
+  const float* norm2;
+  const int32_t* pool_pos;
+  int32_t* ref_idx;
+  int* status;
+};
+
+constexpr int kStages = 4;
+constexpr uint32_t kBBytes = kRefTile * 128;
+constexpr uint32_t kTmemCols = 2 * kRefTile;
+
+__device__ __forceinline__ void topk_insert(float d, int j, float* bd, int* bj) {
+  if (!(d < bd[3])) return;
+  if (d < bd[2]) {
+    bd[3] = bd[2];
+    bj[3] = bj[2];
+    if (d < bd[1]) {
+      bd[2] = bd[1];
+      bj[2] = bj[1];
+      if (d < bd[0]) {
+        bd[1] = bd[0];
+        bj[1] = bj[0];
+        bd[0] = d;
+        bj[0] = j;
+      } else {
+        bd[1] = d;
+        bj[1] = j;
+      }
+    } else {
+      bd[2] = d;
+      bj[2] = j;
+    }
+  } else {
+    bd[3] = d;
+    bj[3] = j;
+  }
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    retrieve_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmP,
+                    RetrieveArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = align1024(smem_raw);
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + kStages * kTileABytes;
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kStages * kBBytes);
+  uint64_t* empty = full + kStages;
+  uint64_t* tfull = empty + kStages;
+  uint64_t* tempty = tfull + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 128);
+    }
+    *abort_flag = 0;
+    fence_barrier_init();
+    tma_prefetch(&tmQ);
+    tma_prefetch(&tmP);
+  }
+  if (warp == 2) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const int kb_total = a.parts * a.nkb;
+
+  if (warp == 0) {
+    if (elect_one()) {
+      Ring ring;
+      int issued[kStages];
+      uint32_t issued_phase[kStages];
+      for (int s = 0; s < kStages; ++s) issued[s] = 0, issued_phase[s] = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x) {
+        const int seq = a.t_seq[u], row0 = a.t_row0[u], nrt = a.t_nrt[u];
+        for (int rt = 0; rt < nrt && ok; ++rt) {
+          for (int kb = 0; kb < kb_total; ++kb) {
+            if (!mbar_wait(&empty[ring.stage], ring.phase ^ 1u, abort_flag, a.status)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&full[ring.stage], kTileABytes + kBBytes);
+            tma_load_2d(sA + ring.stage * kTileABytes, &tmQ, &full[ring.stage], kb * kTileK, row0);
+            tma_load_2d(sB + ring.stage * kBBytes, &tmP, &full[ring.stage], (kb % a.nkb) * kTileK,
+                        seq * a.R_cap + rt * kRefTile);
+            issued[ring.stage] = 1;
+            issued_phase[ring.stage] = ring.phase;
+            ring.next(kStages);
+          }
+        }
+      }
+      if (!ok)
+        for (int s = 0; s < kStages; ++s)
+          if (issued[s]) drain_wait(&full[s], issued_phase[s]);
+    }
+  } else if (warp == 1) {
+    if (elect_one()) {
+      constexpr uint32_t idesc = idesc_bf16_f32(kTileM, kRefTile);
+      Ring ring;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      bool ok = true, any = false;
+      int last_stage = 0;
+      uint32_t last_phase = 0;
+      for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x) {
+        const int nrt = a.t_nrt[u];
+        for (int rt = 0; rt < nrt && ok; ++rt) {
+          if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, a.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t d = tmem + acc * kRefTile;
+          for (int kb = 0; kb < kb_total; ++kb) {
+            if (!mbar_wait(&full[ring.stage], ring.phase, abort_flag, a.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a0 = smem_u32(sA + ring.stage * kTileABytes);
+            const uint32_t b0 = smem_u32(sB + ring.stage * kBBytes);
+#pragma unroll
+            for (int k = 0; k < kTileK / 16; ++k)
+              umma_bf16(d, sdesc_sw128(a0 + k * 32), sdesc_sw128(b0 + k * 32), idesc,
+                        (kb | k) != 0 ? 1u : 0u);
+            umma_commit(&empty[ring.stage]);
+            any = true;
+            last_stage = ring.stage;
+            last_phase = ring.phase;
+            ring.next(kStages);
+          }
+          if (!ok) break;
+          umma_commit(&tfull[acc]);
+          if (++acc == 2) {
+            acc = 0;
+            acc_phase ^= 1u;
+          }
+        }
+      }
+      if (!ok && any) drain_wait(&empty[last_stage], last_phase);
+    }
+  } else if (warp >= kEpiWarp0) {
+    const int ew = warp - kEpiWarp0;
+    const int row_in_tile = ew * 32 + (int)lane_id();
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x) {
+      const int seq = a.t_seq[u], row0 = a.t_row0[u], nrt = a.t_nrt[u];
+      const int qrow = row0 + row_in_tile;
+      const int pos = a.q_pos[qrow];
+      const int64_t pbase = (int64_t)seq * a.R_cap;
+      float bd[4] = {FLT_MAX, FLT_MAX, FLT_MAX, FLT_MAX};
+      int bj[4] = {-1, -1, -1, -1};
+      for (int rt = 0; rt < nrt; ++rt) {
+        if (!warp_wait(&tfull[acc], acc_phase, abort_flag, a.status)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t tacc = tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)(acc * kRefTile);
+#pragma unroll 1
+        for (int c = 0; c < kRefTile / 32; ++c) {
+          uint32_t r[32];
+          tmem_ld32(tacc + c * 32, r);
+          tmem_ld_wait();
+          const int j0 = rt * kRefTile + c * 32;
+#pragma unroll 4
+          for (int i = 0; i < 32; ++i) {
+            const int j = j0 + i;
+            if (j >= a.R_cap) break;
+            const int32_t pj = __ldg(a.pool_pos + pbase + j);
+            if (pos >= 0 && pj < pos) {
+              const float dist = fmaf(-2.0f, __uint_as_float(r[i]), __ldg(a.norm2 + pbase + j));
+              topk_insert(dist, j, bd, bj);
+            }
+          }
+        }
+        tc_fence_before();
+        mbar_arrive(&tempty[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1u;
+        }
+      }
+      if (!ok) break;
+      if (pos >= 0) {
+        const int64_t dst = a.q_dst[qrow];
+        for (int t = 0; t < a.topk; ++t) a.ref_idx[dst * a.topk + t] = bj[t];
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_retrieve(rkv_ctx* c, const PassPlan& p, const int32_t* plan, cudaStream_t s) {
+  if (p.n_tiles == 0) return cudaSuccess;
+  const size_t smem = 1024 + (size_t)kStages * (kTileABytes + kBBytes) + 8 * (2 * kStages + 4) + 16;
+  cudaError_t e =
+      cudaFuncSetAttribute(retrieve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  RetrieveArgs a;
+  a.t_seq = plan + p.off_t_seq;
+  a.t_row0 = plan + p.off_t_row0;
+  a.t_nrt = plan + p.off_t_nrt;
+  a.q_pos = plan + p.off_q_pos;
+  a.q_dst = plan + p.off_q_dst;
+  a.n_units = p.n_tiles;
+  a.nkb = c->d.dkv / kTileK;
+  a.parts = c->d.parts;
+  a.R_cap = c->d.R_cap;
+  a.topk = c->d.topk;
+  a.norm2 = c->st.pool_norm2;
+  a.pool_pos = c->st.pool_pos;
+  a.ref_idx = c->st.ref_idx;
+  a.status = c->status;
+  const int grid = p.n_tiles < c->num_sms ? p.n_tiles : c->num_sms;
+  cudaEvent_t ev;
+  timing_begin(c, "rkv_retrieve_kernel", s, &ev);
+  retrieve_kernel<<<grid, kThreads, smem, s>>>(c->tm_q, c->tm_pool, a);
+  e = cudaGetLastError();
+  timing_end(c, "rkv_retrieve_kernel", s, ev);
+  return e;
+}
+
+}  // namespace rkv

@@ -1,0 +1,569 @@
+// rkv_api.cu - host side of the C ABI declared in include/rkv.h: validation, planning
+// of compress passes, storage initialisation, tensor maps, RoPE tables, launches and
+// instrumentation.  No method arithmetic happens here except the float64 RoPE tables.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <climits>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "rkv_internal.h"
+
+using namespace rkv;
+
+namespace {
+
+thread_local std::string g_err;
+
+rkv_status fail(rkv_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_err = buf;
+  return s;
+}
+
+#define CUDA_OK(call)                                                                    \
+  do {                                                                                  \
+    cudaError_t e_ = (call);                                                            \
+    if (e_ != cudaSuccess)                                                              \
+      return fail(RKV_ECUDA, "%s failed: %s", #call, cudaGetErrorString(e_));          \
+  } while (0)
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+bool get_encoder() {
+  if (g_encode) return true;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || fn == nullptr)
+    return false;
+  g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  return true;
+}
+
+// 2-D bf16 tensor map with the 128-byte swizzle, box = {64 elements, box_rows}.
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
+              uint64_t row_stride_bytes, uint32_t box_rows) {
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {row_stride_bytes};
+  cuuint32_t box[2] = {64u, box_rows};
+  cuuint32_t es[2] = {1u, 1u};
+  CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+rkv_status derive(const rkv_config* c, Dims* d) {
+  if (!c) return fail(RKV_EINVAL, "config is NULL");
+  d->N = c->n_kv_heads;
+  d->D = c->head_dim;
+  d->dk = c->n_kv_heads * c->head_dim;
+  d->dkv = 2 * d->dk;
+  d->dc = c->d_c;
+  d->dff = c->d_ff;
+  d->topk = c->topk;
+  d->group = c->group;
+  d->bits = c->bits;
+  d->stride = c->ref_stride;
+  d->B = c->batch;
+  d->T_cap = c->max_tokens;
+  d->R_cap = c->max_refs;
+  d->kv_f32 = c->kv_dtype == RKV_F32;
+  d->out_f32 = c->out_dtype == RKV_F32;
+  d->parts = d->kv_f32 ? 3 : 1;
+  if (d->N <= 0 || !(d->D == 64 || d->D == 128 || d->D == 256))
+    return fail(RKV_EINVAL, "head_dim must be 64, 128 or 256 and n_kv_heads > 0");
+  if (d->dkv % 256 != 0) return fail(RKV_EINVAL, "2*N*D must be a multiple of 256");
+  if (d->dc <= 0 || d->dc % 64 != 0) return fail(RKV_EINVAL, "d_c must be a positive multiple of 64");
+  if (d->dff <= 0 || d->dff % 128 != 0) return fail(RKV_EINVAL, "d_ff must be a positive multiple of 128");
+  if (d->topk < 1 || d->topk > 4) return fail(RKV_EINVAL, "topk must be in 1..4");
+  if (d->group != 32) return fail(RKV_EINVAL, "group must be 32");
+  if (!(d->bits == 4 || d->bits == 2 || d->bits == 16)) return fail(RKV_EINVAL, "bits must be 4, 2 or 16");
+  if (d->stride < 1) return fail(RKV_EINVAL, "ref_stride must be >= 1");
+  if (!(c->kv_dtype == RKV_F32 || c->kv_dtype == RKV_BF16) ||
+      !(c->out_dtype == RKV_F32 || c->out_dtype == RKV_BF16))
+    return fail(RKV_EINVAL, "kv_dtype / out_dtype must be RKV_F32 or RKV_BF16");
+  if (!(c->rope_base > 1.0)) return fail(RKV_EINVAL, "rope_base must be > 1");
+  if (d->B < 1 || d->T_cap < 1 || d->R_cap < 1) return fail(RKV_EINVAL, "batch, max_tokens, max_refs must be >= 1");
+  if ((int64_t)d->R_cap < ((int64_t)d->T_cap + d->stride - 1) / d->stride)
+    return fail(RKV_EINVAL, "max_refs must be >= ceil(max_tokens / ref_stride)");
+  if ((int64_t)d->B * d->T_cap > INT32_MAX || (int64_t)d->B * d->R_cap > INT32_MAX)
+    return fail(RKV_EINVAL, "batch * max_tokens too large");
+  d->G = d->dc / d->group;
+  d->code_bytes = d->bits == 16 ? 2 * d->dc : d->dc * d->bits / 8;
+  d->n_hi = (d->T_cap + kRopeLo - 1) / kRopeLo;
+  return RKV_OK;
+}
+
+// ------------------------------------------------------------------ staging
+// Double-buffered pinned staging: before rewriting buffer b, wait for the copy that
+// last read it (normally long finished).
+int32_t* staging_acquire(rkv_ctx* c, int* which) {
+  const int b = c->plan_flip;
+  c->plan_flip ^= 1;
+  cudaEventSynchronize(c->plan_copied[b]);
+  *which = b;
+  return c->plan_host[b];
+}
+
+cudaError_t staging_upload(rkv_ctx* c, int b, int n_ints, cudaStream_t s) {
+  cudaError_t e = cudaMemcpyAsync(c->plan_dev[b], c->plan_host[b], sizeof(int32_t) * n_ints,
+                                  cudaMemcpyHostToDevice, s);
+  if (e != cudaSuccess) return e;
+  return cudaEventRecord(c->plan_copied[b], s);
+}
+
+inline int visible_refs(int pos, int stride) { return (pos - 1) / stride + 1; }
+
+}  // namespace
+
+namespace rkv {
+
+void timing_begin(rkv_ctx* c, const char* name, cudaStream_t s, cudaEvent_t* start) {
+  c->launches++;
+  *start = nullptr;
+  if (!c->timing) return;
+  if (cudaEventCreate(start) != cudaSuccess) {
+    *start = nullptr;
+    return;
+  }
+  cudaEventRecord(*start, s);
+}
+
+void timing_end(rkv_ctx* c, const char* name, cudaStream_t s, cudaEvent_t start) {
+  if (!c->timing || !start) return;
+  cudaEvent_t stop;
+  if (cudaEventCreate(&stop) != cudaSuccess) return;
+  cudaEventRecord(stop, s);
+  TimingSlot* slot = nullptr;
+  for (auto& t : c->timings)
+    if (t.name == name) slot = &t;
+  if (!slot) {
+    c->timings.emplace_back();
+    slot = &c->timings.back();
+    slot->name = name;
+  }
+  slot->launches++;
+  slot->pending.push_back(start);
+  slot->pending.push_back(stop);
+}
+
+}  // namespace rkv
+
+extern "C" {
+
+const char* rkv_last_error(void) { return g_err.c_str(); }
+
+rkv_status rkv_storage_bytes(const rkv_config* cfg, size_t sizes[7]) {
+  Dims d;
+  rkv_status st = derive(cfg, &d);
+  if (st != RKV_OK) return st;
+  const size_t pool_rows = (size_t)d.B * d.R_cap, tok_rows = (size_t)d.B * d.T_cap;
+  sizes[0] = pool_rows * d.dkv;                 // pool_fp8
+  sizes[1] = pool_rows * d.dkv * 2;             // pool_bf16
+  sizes[2] = pool_rows * 4;                     // pool_norm2
+  sizes[3] = pool_rows * 4;                     // pool_pos
+  sizes[4] = tok_rows * d.code_bytes;           // codes
+  sizes[5] = tok_rows * d.G * 4;                // meta
+  sizes[6] = tok_rows * d.topk * 4;             // ref_idx
+  return RKV_OK;
+}
+
+rkv_status rkv_create(const rkv_config* cfg, const void* Wc1, const void* Wc2, const void* Wc3,
+                      const void* Wd, const rkv_storage* st, void* stream, rkv_ctx** out) {
+  if (!out) return fail(RKV_EINVAL, "out is NULL");
+  *out = nullptr;
+  Dims d;
+  rkv_status r = derive(cfg, &d);
+  if (r != RKV_OK) return r;
+  if (!st || !Wc1 || !Wc2 || !Wc3 || !Wd) return fail(RKV_EINVAL, "NULL weight or storage");
+  const void* ptrs[] = {Wc1, Wc2, Wc3, Wd, st->pool_fp8, st->pool_bf16, st->pool_norm2,
+                        st->pool_pos, st->codes, st->meta, st->ref_idx};
+  for (const void* p : ptrs) {
+    if (!p) return fail(RKV_EINVAL, "NULL storage pointer");
+    if (!aligned16(p)) return fail(RKV_EALIGN, "weights and storage must be 16-byte aligned");
+  }
+  if (!get_encoder()) return fail(RKV_ECUDA, "cuTensorMapEncodeTiled is unavailable");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+
+  rkv_ctx* c = new rkv_ctx();
+  c->cfg = *cfg;
+  c->d = d;
+  c->st = *st;
+  CUDA_OK(cudaGetDevice(&c->device));
+  CUDA_OK(cudaDeviceGetAttribute(&c->num_sms, cudaDevAttrMultiProcessorCount, c->device));
+  c->max_rows = cfg->max_rows > 0 ? cfg->max_rows : 32768;
+  c->max_rows = (c->max_rows + kTileM - 1) / kTileM * kTileM;
+  c->m_cap = c->max_rows + kTileM * std::min(d.B, c->max_rows);
+  c->tiles_cap = c->m_cap / kTileM;
+  c->plan_ints = std::max(3 * c->m_cap + 3 * c->tiles_cap + 2 * c->max_rows, 4 * c->max_rows);
+  c->pool_count.assign(d.B, 0);
+
+  auto alloc = [&](void** p, size_t bytes) -> cudaError_t { return cudaMalloc(p, bytes); };
+  rkv_status fail_status = RKV_OK;
+#define ALLOC(ptr, bytes)                                                                 \
+  if (fail_status == RKV_OK && alloc(reinterpret_cast<void**>(&(ptr)), (bytes)) != cudaSuccess) \
+    fail_status = fail(RKV_ECUDA, "cudaMalloc of %zu bytes failed", (size_t)(bytes));
+  ALLOC(c->w12, (size_t)2 * d.dff * d.dkv * 2);
+  ALLOC(c->w3, (size_t)d.dc * d.dff * 2);
+  ALLOC(c->wd, (size_t)d.dkv * d.dc * 2);
+  ALLOC(c->rope_lo, (size_t)kRopeLo * (d.D / 2) * sizeof(float2));
+  ALLOC(c->rope_hi, (size_t)d.n_hi * (d.D / 2) * sizeof(float2));
+  ALLOC(c->Q, (size_t)c->m_cap * d.parts * d.dkv * 2);
+  ALLOC(c->X, (size_t)2 * c->max_rows * d.dkv * 2);
+  ALLOC(c->H, (size_t)2 * c->max_rows * d.dff * 2);
+  ALLOC(c->plan_dev[0], (size_t)c->plan_ints * 4);
+  ALLOC(c->plan_dev[1], (size_t)c->plan_ints * 4);
+  ALLOC(c->status, 64);
+#undef ALLOC
+  if (fail_status != RKV_OK) {
+    rkv_free(c);
+    return fail_status;
+  }
+  for (int b = 0; b < 2; ++b) {
+    if (cudaHostAlloc(reinterpret_cast<void**>(&c->plan_host[b]), (size_t)c->plan_ints * 4,
+                      cudaHostAllocDefault) != cudaSuccess ||
+        cudaEventCreateWithFlags(&c->plan_copied[b], cudaEventDisableTiming) != cudaSuccess) {
+      rkv_free(c);
+      return fail(RKV_ECUDA, "pinned staging allocation failed");
+    }
+  }
+
+  // RoPE tables in float64, rounded once to fp32: (cos, sin) of l*theta_j and of
+  // h*512*theta_j with theta_j = base^(-2j/D).
+  {
+    const int half = d.D / 2;
+    std::vector<float2> lo((size_t)kRopeLo * half), hi((size_t)d.n_hi * half);
+    for (int j = 0; j < half; ++j) {
+      const double theta = std::pow(cfg->rope_base, -2.0 * j / d.D);
+      for (int l = 0; l < kRopeLo; ++l) {
+        const double a = (double)l * theta;
+        lo[(size_t)l * half + j] = make_float2((float)std::cos(a), (float)std::sin(a));
+      }
+      for (int h = 0; h < d.n_hi; ++h) {
+        const double a = (double)h * kRopeLo * theta;
+        hi[(size_t)h * half + j] = make_float2((float)std::cos(a), (float)std::sin(a));
+      }
+    }
+    if (cudaMemcpy(c->rope_lo, lo.data(), lo.size() * sizeof(float2), cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMemcpy(c->rope_hi, hi.data(), hi.size() * sizeof(float2), cudaMemcpyHostToDevice) != cudaSuccess) {
+      rkv_free(c);
+      return fail(RKV_ECUDA, "RoPE table upload failed");
+    }
+  }
+
+  // Tensor maps over fixed addresses.
+  const uint64_t dkv = d.dkv;
+  bool ok = true;
+  ok &= make_map(&c->tm_q, c->Q, (uint64_t)d.parts * dkv, c->m_cap, (uint64_t)d.parts * dkv * 2, kTileM);
+  ok &= make_map(&c->tm_pool, st->pool_bf16, dkv, (uint64_t)d.B * d.R_cap, dkv * 2, kRefTile);
+  ok &= make_map(&c->tm_x, c->X, dkv, (uint64_t)2 * c->max_rows, dkv * 2, kTileM);
+  ok &= make_map(&c->tm_w12, c->w12, dkv, (uint64_t)2 * d.dff, dkv * 2, kEncN);
+  ok &= make_map(&c->tm_h3, c->H, (uint64_t)2 * d.dff, c->max_rows, (uint64_t)2 * d.dff * 2, kTileM);
+  const uint32_t bn3 = d.dc % 256 == 0 ? 256u : (d.dc % 128 == 0 ? 128u : 64u);
+  ok &= make_map(&c->tm_w3, c->w3, d.dff, d.dc, (uint64_t)d.dff * 2, bn3);
+  ok &= make_map(&c->tm_wd, c->wd, d.dc, dkv, (uint64_t)d.dc * 2, kDecN);
+  if (!ok) {
+    rkv_free(c);
+    return fail(RKV_ECUDA, "cuTensorMapEncodeTiled rejected a tensor map");
+  }
+
+  cudaError_t e = cudaMemsetAsync(c->status, 0, 64, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(c->Q, 0, (size_t)c->m_cap * d.parts * d.dkv * 2, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(c->X, 0, (size_t)2 * c->max_rows * d.dkv * 2, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(c->H, 0, (size_t)2 * c->max_rows * d.dff * 2, s);
+  if (e == cudaSuccess) e = launch_init_storage(c, s);
+  if (e == cudaSuccess)
+    e = launch_repack_weights(c, static_cast<const __nv_bfloat16*>(Wc1),
+                              static_cast<const __nv_bfloat16*>(Wc2),
+                              static_cast<const __nv_bfloat16*>(Wc3),
+                              static_cast<const __nv_bfloat16*>(Wd), s);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) {
+    rkv_free(c);
+    return fail(RKV_ECUDA, "initialisation failed: %s", cudaGetErrorString(e));
+  }
+  *out = c;
+  return RKV_OK;
+}
+
+rkv_status rkv_pool_append(rkv_ctx* c, const void* kv, int64_t kv_row_stride,
+                           const int32_t* src_rows, const int32_t* seq, const int32_t* pos,
+                           int32_t n, void* stream) {
+  if (!c) return fail(RKV_EINVAL, "ctx is NULL");
+  if (n < 0) return fail(RKV_EINVAL, "n < 0");
+  if (n == 0) return RKV_OK;
+  if (!kv || !seq || !pos) return fail(RKV_EINVAL, "NULL kv, seq or pos");
+  if (!aligned16(kv)) return fail(RKV_EALIGN, "kv must be 16-byte aligned");
+  const Dims& d = c->d;
+  if (kv_row_stride < d.dkv || kv_row_stride % 8 != 0)
+    return fail(RKV_EINVAL, "kv_row_stride must be >= 2*d_k and a multiple of 8");
+  // validate everything before touching the host mirror
+  std::vector<int32_t> next(c->pool_count);
+  for (int i = 0; i < n; ++i) {
+    const int s = seq[i], p = pos[i];
+    const int src = src_rows ? src_rows[i] : i;
+    if (s < 0 || s >= d.B) return fail(RKV_EINVAL, "row %d: seq %d out of range", i, s);
+    if (p < 0 || p >= d.T_cap) return fail(RKV_EINVAL, "row %d: pos %d out of range", i, p);
+    if (src < 0) return fail(RKV_EINVAL, "row %d: negative source row", i);
+    if (p % d.stride != 0) return fail(RKV_EINVAL, "row %d: pos %d is not a reference position", i, p);
+    const int slot = p / d.stride;
+    if (slot >= d.R_cap) return fail(RKV_ECAPACITY, "row %d: slot %d >= max_refs", i, slot);
+    if (slot != next[s])
+      return fail(RKV_EINVAL, "row %d: seq %d expects the reference at pos %d next, got %d", i, s,
+                  next[s] * d.stride, p);
+    next[s] = slot + 1;
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  for (int r0 = 0; r0 < n; r0 += c->max_rows) {
+    const int m = std::min(c->max_rows, n - r0);
+    int b;
+    int32_t* h = staging_acquire(c, &b);
+    for (int i = 0; i < m; ++i) {
+      const int k = r0 + i;
+      const int s = seq[k], p = pos[k];
+      h[4 * i + 0] = src_rows ? src_rows[k] : k;
+      h[4 * i + 1] = s * d.R_cap + p / d.stride;
+      h[4 * i + 2] = p;
+      h[4 * i + 3] = s * d.T_cap + p;
+    }
+    CUDA_OK(staging_upload(c, b, 4 * m, st));
+    CUDA_OK(launch_pool_append(c, kv, kv_row_stride, c->plan_dev[b], m, st));
+  }
+  c->pool_count = next;
+  return RKV_OK;
+}
+
+rkv_status rkv_compress(rkv_ctx* c, const void* kv, int64_t kv_row_stride, const int32_t* src_rows,
+                        const int32_t* seq, const int32_t* pos, int32_t n, void* stream) {
+  if (!c) return fail(RKV_EINVAL, "ctx is NULL");
+  if (n < 0) return fail(RKV_EINVAL, "n < 0");
+  if (n == 0) return RKV_OK;
+  if (!kv || !seq || !pos) return fail(RKV_EINVAL, "NULL kv, seq or pos");
+  if (!aligned16(kv)) return fail(RKV_EALIGN, "kv must be 16-byte aligned");
+  const Dims& d = c->d;
+  if (kv_row_stride < d.dkv || kv_row_stride % 8 != 0)
+    return fail(RKV_EINVAL, "kv_row_stride must be >= 2*d_k and a multiple of 8");
+  for (int i = 0; i < n; ++i) {
+    const int s = seq[i], p = pos[i];
+    const int src = src_rows ? src_rows[i] : i;
+    if (s < 0 || s >= d.B) return fail(RKV_EINVAL, "row %d: seq %d out of range", i, s);
+    if (p < 0 || p >= d.T_cap) return fail(RKV_EINVAL, "row %d: pos %d out of range", i, p);
+    if (src < 0) return fail(RKV_EINVAL, "row %d: negative source row", i);
+    if (p % d.stride == 0) return fail(RKV_EINVAL, "row %d: pos %d is a reference position", i, p);
+    if (c->pool_count[s] == 0) return fail(RKV_EEMPTYPOOL, "row %d: seq %d has no reference", i, s);
+    if (visible_refs(p, d.stride) > c->pool_count[s])
+      return fail(RKV_EINVAL, "row %d: references of seq %d before pos %d are not all appended", i,
+                  s, p);
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  std::vector<int> order;
+  std::vector<std::pair<int, int>> tiles;   // (nrt, tile index)
+  for (int r0 = 0; r0 < n; r0 += c->max_rows) {
+    const int m = std::min(c->max_rows, n - r0);
+    // ---- plan: rows grouped by sequence (stable), each group padded to 128 rows
+    order.resize(m);
+    for (int i = 0; i < m; ++i) order[i] = r0 + i;
+    std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return seq[a] < seq[b]; });
+    PassPlan p;
+    p.n_rows = m;
+    int m_pad = 0, ntiles = 0;
+    for (int i = 0; i < m;) {
+      int j = i;
+      while (j < m && seq[order[j]] == seq[order[i]]) ++j;
+      const int cnt = j - i;
+      const int padded = (cnt + kTileM - 1) / kTileM * kTileM;
+      m_pad += padded;
+      ntiles += padded / kTileM;
+      i = j;
+    }
+    p.m_pad = m_pad;
+    p.n_tiles = ntiles;
+    p.off_q_src = 0;
+    p.off_q_pos = m_pad;
+    p.off_q_dst = 2 * m_pad;
+    p.off_t_seq = 3 * m_pad;
+    p.off_t_row0 = 3 * m_pad + ntiles;
+    p.off_t_nrt = 3 * m_pad + 2 * ntiles;
+    p.off_c_q = 3 * m_pad + 3 * ntiles;
+    p.off_c_dst = p.off_c_q + m;
+    p.total_ints = p.off_c_dst + m;
+    if (m_pad > c->m_cap || p.total_ints > c->plan_ints)
+      return fail(RKV_ECAPACITY, "compress pass exceeds the planned scratch");
+    int b;
+    int32_t* h = staging_acquire(c, &b);
+    int q = 0, t = 0;
+    tiles.clear();
+    std::vector<int32_t> tseq, trow0, tnrt;
+    for (int i = 0; i < m;) {
+      int j = i;
+      const int s = seq[order[i]];
+      while (j < m && seq[order[j]] == s) ++j;
+      for (int k = i; k < j; k += kTileM) {
+        int maxvis = 1;
+        for (int r = k; r < std::min(j, k + kTileM); ++r)
+          maxvis = std::max(maxvis, visible_refs(pos[order[r]], d.stride));
+        tseq.push_back(s);
+        trow0.push_back(q + (k - i));
+        tnrt.push_back((maxvis + kRefTile - 1) / kRefTile);
+      }
+      for (int k = i; k < j; ++k) {
+        const int row = order[k];
+        const int qr = q + (k - i);
+        h[p.off_q_src + qr] = src_rows ? src_rows[row] : row;
+        h[p.off_q_pos + qr] = pos[row];
+        h[p.off_q_dst + qr] = seq[row] * d.T_cap + pos[row];
+        h[p.off_c_q + (row - r0)] = qr;
+        h[p.off_c_dst + (row - r0)] = seq[row] * d.T_cap + pos[row];
+      }
+      const int padded = (j - i + kTileM - 1) / kTileM * kTileM;
+      for (int k = j - i; k < padded; ++k) {
+        h[p.off_q_src + q + k] = -1;
+        h[p.off_q_pos + q + k] = -1;
+        h[p.off_q_dst + q + k] = -1;
+      }
+      q += padded;
+      i = j;
+    }
+    // heaviest tiles first
+    std::vector<int> tord(ntiles);
+    for (int i = 0; i < ntiles; ++i) tord[i] = i;
+    std::stable_sort(tord.begin(), tord.end(), [&](int a, int b2) { return tnrt[a] > tnrt[b2]; });
+    for (int i = 0; i < ntiles; ++i) {
+      h[p.off_t_seq + i] = tseq[tord[i]];
+      h[p.off_t_row0 + i] = trow0[tord[i]];
+      h[p.off_t_nrt + i] = tnrt[tord[i]];
+    }
+    (void)t;
+    CUDA_OK(staging_upload(c, b, p.total_ints, st));
+    const int32_t* plan = c->plan_dev[b];
+    CUDA_OK(launch_prep_queries(c, kv, kv_row_stride, plan + p.off_q_src, p.m_pad, st));
+    CUDA_OK(launch_retrieve(c, p, plan, st));
+    CUDA_OK(launch_mean_rows(c, p, plan, st));
+    CUDA_OK(launch_gemm12(c, p.n_rows, st));
+    CUDA_OK(launch_gemm3_quant(c, p, plan, st));
+  }
+  return RKV_OK;
+}
+
+rkv_status rkv_reconstruct(rkv_ctx* c, const int32_t* seq, const int32_t* pos, int32_t n_sel,
+                           void* k_out, void* v_out, void* stream) {
+  if (!c) return fail(RKV_EINVAL, "ctx is NULL");
+  if (n_sel < 0) return fail(RKV_EINVAL, "n_sel < 0");
+  if (n_sel == 0) return RKV_OK;
+  if (!seq || !pos || !k_out || !v_out) return fail(RKV_EINVAL, "NULL seq, pos or output");
+  if (!aligned16(k_out) || !aligned16(v_out) || (reinterpret_cast<uintptr_t>(seq) & 3u) ||
+      (reinterpret_cast<uintptr_t>(pos) & 3u))
+    return fail(RKV_EALIGN, "outputs must be 16-byte aligned, seq/pos 4-byte aligned");
+  CUDA_OK(launch_reconstruct(c, seq, pos, n_sel, k_out, v_out, static_cast<cudaStream_t>(stream)));
+  return RKV_OK;
+}
+
+rkv_status rkv_reset(rkv_ctx* c, int32_t seq, void* stream) {
+  if (!c) return fail(RKV_EINVAL, "ctx is NULL");
+  if (seq < -1 || seq >= c->d.B) return fail(RKV_EINVAL, "seq %d out of range", seq);
+  CUDA_OK(launch_init_storage(c, static_cast<cudaStream_t>(stream), seq));
+  if (seq < 0)
+    std::fill(c->pool_count.begin(), c->pool_count.end(), 0);
+  else
+    c->pool_count[seq] = 0;
+  return RKV_OK;
+}
+
+rkv_status rkv_get_status(rkv_ctx* c, int32_t* flags, void* stream) {
+  if (!c || !flags) return fail(RKV_EINVAL, "NULL ctx or flags");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  CUDA_OK(cudaMemcpyAsync(&v, c->status, 4, cudaMemcpyDeviceToHost, s));
+  CUDA_OK(cudaMemsetAsync(c->status, 0, 4, s));
+  CUDA_OK(cudaStreamSynchronize(s));
+  *flags = v;
+  if (v == 0) return RKV_OK;
+  if (v & RKV_FLAG_TIMEOUT) return fail(RKV_ETIMEOUT, "a kernel wait timed out (flags 0x%x)", v);
+  return fail(RKV_EDEVICE, "device status flags 0x%x", v);
+}
+
+void rkv_free(rkv_ctx* c) {
+  if (!c) return;
+  cudaFree(c->w12);
+  cudaFree(c->w3);
+  cudaFree(c->wd);
+  cudaFree(c->rope_lo);
+  cudaFree(c->rope_hi);
+  cudaFree(c->Q);
+  cudaFree(c->X);
+  cudaFree(c->H);
+  cudaFree(c->status);
+  for (int b = 0; b < 2; ++b) {
+    cudaFree(c->plan_dev[b]);
+    if (c->plan_host[b]) cudaFreeHost(c->plan_host[b]);
+    if (c->plan_copied[b]) cudaEventDestroy(c->plan_copied[b]);
+  }
+  for (auto& t : c->timings)
+    for (cudaEvent_t e : t.pending) cudaEventDestroy(e);
+  delete c;
+}
+
+rkv_status rkv_set_timing(rkv_ctx* c, int32_t enable) {
+  if (!c) return fail(RKV_EINVAL, "ctx is NULL");
+  c->timing = enable != 0;
+  return RKV_OK;
+}
+
+int32_t rkv_get_timing(rkv_ctx* c, rkv_kernel_timing* out, int32_t max_entries, int32_t reset) {
+  if (!c) return 0;
+  int32_t n = 0;
+  for (auto& t : c->timings) {
+    for (size_t i = 0; i + 1 < t.pending.size(); i += 2) {
+      float ms = 0.f;
+      cudaEventSynchronize(t.pending[i + 1]);
+      if (cudaEventElapsedTime(&ms, t.pending[i], t.pending[i + 1]) == cudaSuccess) t.total_ms += ms;
+      cudaEventDestroy(t.pending[i]);
+      cudaEventDestroy(t.pending[i + 1]);
+    }
+    t.pending.clear();
+    if (out && n < max_entries) {
+      std::memset(&out[n], 0, sizeof(rkv_kernel_timing));
+      std::snprintf(out[n].name, sizeof(out[n].name), "%s", t.name.c_str());
+      out[n].launches = t.launches;
+      out[n].total_ms = t.total_ms;
+    }
+    ++n;
+  }
+  if (reset) c->timings.clear();
+  return n;
+}
+
+int64_t rkv_launch_count(rkv_ctx* c) { return c ? c->launches : 0; }
+
+rkv_status rkv_debug_scratch(rkv_ctx* c, int32_t which, void** ptr, size_t* bytes) {
+  if (!c || !ptr || !bytes) return fail(RKV_EINVAL, "NULL argument");
+  if (which == 0) {
+    *ptr = c->X;
+    *bytes = (size_t)2 * c->max_rows * c->d.dkv * 2;
+  } else if (which == 1) {
+    *ptr = c->H;
+    *bytes = (size_t)2 * c->max_rows * c->d.dff * 2;
+  } else {
+    return fail(RKV_EINVAL, "which must be 0 or 1");
+  }
+  return RKV_OK;
+}
+
+}  // extern "C"

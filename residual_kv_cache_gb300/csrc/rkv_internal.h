@@ -1,0 +1,115 @@
+// rkv_internal.h - context layout and the launchers shared by the host API and kernels.
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+#include <vector>
+
+#include "../../include/rkv.h"
+
+namespace rkv {
+
+constexpr int kTileM = 128;        // rows per tensor-core tile (one TMEM lane per row)
+constexpr int kTileK = 64;         // bf16 elements per 128-byte swizzled row
+constexpr int kRefTile = 256;      // references per retrieval tile
+constexpr int kEncN = 256;         // GEMM-1/2 N tile: 128 W_c1 + 128 W_c2 columns
+constexpr int kDecN = 256;         // decoder N tile
+constexpr int kRopeLo = 512;       // positions per low RoPE table
+
+// Derived sizes of a configuration.
+struct Dims {
+  int N, D, dk, dkv, dc, dff, topk, group, bits, stride;
+  int G;           // groups per token
+  int code_bytes;  // bytes of one packed code row
+  int B, T_cap, R_cap;
+  int kv_f32, out_f32;
+  int parts;       // 3 bf16 pieces per fp32 query element, 1 for bf16
+  int n_hi;        // rows of the high RoPE table
+};
+
+// One kernel's accumulated event time (instrumentation).
+struct TimingSlot {
+  std::string name;
+  int64_t launches = 0;
+  double total_ms = 0.0;
+  std::vector<cudaEvent_t> pending;  // start/stop pairs not yet read
+};
+
+// Device plan of one compress pass (int32 arrays inside one buffer).
+struct PassPlan {
+  int n_rows = 0;      // compact rows (this pass)
+  int m_pad = 0;       // retrieval-order rows, padded per sequence to 128
+  int n_tiles = 0;     // retrieval tiles
+  // offsets (in int32 elements) inside the plan buffer
+  int off_q_src, off_q_pos, off_q_dst, off_t_seq, off_t_row0, off_t_nrt, off_c_q, off_c_dst;
+  int total_ints = 0;
+};
+
+}  // namespace rkv
+
+struct rkv_ctx {
+  rkv_config cfg;
+  rkv::Dims d;
+  rkv_storage st;
+  int device = 0;
+  int num_sms = 0;
+  int max_rows = 0;    // compact rows per pass
+  int m_cap = 0;       // retrieval-order rows per pass (with padding)
+  int tiles_cap = 0;
+
+  // library-owned device memory
+  __nv_bfloat16* w12 = nullptr;   // [2 d_ff, 2d_k]: per 256-row tile, 128 W_c1^T rows then 128 W_c2^T rows
+  __nv_bfloat16* w3 = nullptr;    // [d_c, d_ff] = W_c3^T
+  __nv_bfloat16* wd = nullptr;    // [2d_k, d_c] = W_d^T
+  float2* rope_lo = nullptr;      // [512][D/2] (cos, sin)(l * theta_j)
+  float2* rope_hi = nullptr;      // [n_hi][D/2] (cos, sin)(h * 512 * theta_j)
+  __nv_bfloat16* Q = nullptr;     // [m_cap, parts * 2d_k] retrieval-order queries
+  __nv_bfloat16* X = nullptr;     // [2 max_rows, 2d_k] kv / mean rows interleaved
+  __nv_bfloat16* H = nullptr;     // [2 max_rows, d_ff] SwiGLU rows (mean rows negated)
+  int32_t* plan_dev[2] = {nullptr, nullptr};
+  int32_t* plan_host[2] = {nullptr, nullptr};   // pinned staging
+  cudaEvent_t plan_copied[2] = {nullptr, nullptr};
+  int plan_ints = 0;
+  int plan_flip = 0;
+  int* status = nullptr;          // device status word
+
+  // TMA descriptors (fixed addresses, built once)
+  CUtensorMap tm_q, tm_pool, tm_x, tm_w12, tm_h3, tm_w3, tm_wd;
+
+  // host mirror of each sequence's pool fill
+  std::vector<int32_t> pool_count;
+
+  // instrumentation
+  bool timing = false;
+  std::vector<rkv::TimingSlot> timings;
+  int64_t launches = 0;
+};
+
+namespace rkv {
+
+// ---- launchers (defined in the kernel translation units) ----
+// Each returns cudaGetLastError() of its launch.
+cudaError_t launch_init_storage(rkv_ctx* c, cudaStream_t s, int seq = -1);
+cudaError_t launch_repack_weights(rkv_ctx* c, const __nv_bfloat16* Wc1, const __nv_bfloat16* Wc2,
+                                  const __nv_bfloat16* Wc3, const __nv_bfloat16* Wd,
+                                  cudaStream_t s);
+cudaError_t launch_pool_append(rkv_ctx* c, const void* kv, int64_t stride, const int32_t* plan,
+                               int n, cudaStream_t s);
+cudaError_t launch_prep_queries(rkv_ctx* c, const void* kv, int64_t stride, const int32_t* q_src,
+                                int m_pad, cudaStream_t s);
+cudaError_t launch_retrieve(rkv_ctx* c, const PassPlan& p, const int32_t* plan, cudaStream_t s);
+cudaError_t launch_mean_rows(rkv_ctx* c, const PassPlan& p, const int32_t* plan, cudaStream_t s);
+cudaError_t launch_gemm12(rkv_ctx* c, int n_rows, cudaStream_t s);
+cudaError_t launch_gemm3_quant(rkv_ctx* c, const PassPlan& p, const int32_t* plan,
+                               cudaStream_t s);
+cudaError_t launch_reconstruct(rkv_ctx* c, const int32_t* seq, const int32_t* pos, int n_sel,
+                               void* k_out, void* v_out, cudaStream_t s);
+
+// Instrumentation helpers used around every launch.
+void timing_begin(rkv_ctx* c, const char* name, cudaStream_t s, cudaEvent_t* start);
+void timing_end(rkv_ctx* c, const char* name, cudaStream_t s, cudaEvent_t start);
+
+}  // namespace rkv

@@ -1,0 +1,66 @@
+"""The C-ABI library builds, loads and exports every entry point the header declares;
+host-only entry points validate configurations (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def built():
+    from residual_kv_cache_gb300 import build
+    return build.build()
+
+
+def _header_functions():
+    text = open(os.path.join(ROOT, "include", "rkv.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(rkv_[a-z_]+)\s*\(", text)))
+
+
+def test_header_functions_are_exported(built):
+    import residual_kv_cache_gb300 as rkv
+    names = _header_functions()
+    assert len(names) >= 12
+    handle = ctypes.CDLL(built)
+    for n in names:
+        assert hasattr(handle, n), f"{n} missing from librkv.so"
+    assert set(names) == set(rkv.ABI_FUNCTIONS), "binding and header disagree"
+
+
+def test_library_has_sm103a_code(built):
+    data = open(built, "rb").read()
+    assert b"sm_103a" in data or b"sm_103" in data
+
+
+def test_storage_bytes_and_config_validation(built):
+    import residual_kv_cache_gb300 as rkv
+    cfg = rkv.Config(n_kv_heads=8, head_dim=128, d_c=512, d_ff=1536, bits=4, ref_stride=16,
+                     max_tokens=32768)
+    s = rkv.storage_bytes(cfg)
+    assert s[0] == 2048 * 2048 and s[1] == 2048 * 2048 * 2
+    assert s[4] == 32768 * 256 and s[5] == 32768 * 16 * 4 and s[6] == 32768 * 4 * 4
+    for bad in (dict(head_dim=96), dict(d_c=100), dict(bits=3), dict(topk=5), dict(d_ff=200),
+                dict(group=16), dict(max_refs=10)):
+        with pytest.raises(rkv.RkvError) as e:
+            rkv.storage_bytes(rkv.Config(**{**cfg.__dict__, **bad}))
+        assert e.value.status == -1
+
+
+def test_null_context_is_rejected(built):
+    import residual_kv_cache_gb300 as rkv
+    L = rkv.lib()
+    assert L.rkv_reconstruct(None, None, None, 0, None, None, None) == -1
+    assert b"ctx" in L.rkv_last_error()
+    L.rkv_free(None)
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    import residual_kv_cache_gb300 as rkv
+    monkeypatch.setattr(rkv, "LIB_PATH", str(tmp_path / "absent.so"))
+    monkeypatch.setattr(rkv, "_lib", None)
+    with pytest.raises(rkv.RkvLibraryMissing):
+        rkv.lib()

@@ -1,0 +1,369 @@
+"""GPU parity of the CUDA library against the oracle on the same seeded inputs.
+
+Tolerances (from the method's requirements):
+* reference pool bytes, squared norms, positions: bit-exact;
+* retrieved slots: bit-exact except swaps whose relative distance gap is < 1e-4;
+* encoder operand rows (bf16 kv, bf16 mean): bit-exact;
+* integer codes: >= 99.9 % identical, a differing code only +-1 where the oracle's
+  pre-round value is within 1e-3 of a .5 boundary;
+* restored K/V: relative Frobenius error <= 1e-2 against the operand-mode oracle
+  (bf16 GEMM operands), and <= 1e-5 when fed the oracle's own codes with fp32 output.
+"""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import codec as C
+from oracle import formats as F
+
+from _common import (code_parity, device_bytes, gpu_prefill, idx_parity, make_codec, np64,
+                     oracle_shape, rel_fro)
+
+pytestmark = pytest.mark.gpu
+
+cuda = pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")
+
+
+def _weights64(W):
+    return {k: np64(v) for k, v in W.items()}
+
+
+def _run(name, T, seed_kv=11, seed_w=12, **kw):
+    w = synth.workload(name)
+    kv = synth.gen_kv(w, seed_kv, T=T)
+    W = synth.gen_weights(w, seed_w)
+    codec = make_codec(w, W, T=T, **kw)
+    kv_dev = kv.cuda()
+    ref, non = gpu_prefill(codec, kv_dev, w.stride)
+    torch.cuda.synchronize()
+    assert codec.get_status() == 0
+    sh = oracle_shape(w)
+    if "bits" in kw and kw["bits"] is not None:
+        sh = C.Shape(**{**sh.__dict__, "bits": kw["bits"]})
+    kv64 = np64(kv)
+    W64 = _weights64(W)
+    store = C.compress_sequence(kv64, W64, sh, "operand")
+    return dict(w=w, kv=kv, kv64=kv64, W=W, W64=W64, codec=codec, store=store, sh=sh,
+                ref=ref, non=non, T=T)
+
+
+@pytest.fixture(scope="module")
+def tiny():
+    return _run("tiny", 256)
+
+
+@pytest.fixture(scope="module")
+def llama():
+    return _run("llama8b", 4096)
+
+
+def _check_pool(r):
+    c, st = r["codec"], r["store"]
+    R = len(st.pool.pos)
+    assert np.array_equal(c.pool_fp8[0, :R].cpu().numpy(), st.pool.codes)
+    assert np.array_equal(np64(c.pool_bf16[0, :R]), st.pool.vals)
+    assert np.array_equal(c.pool_norm2[0, :R].cpu().numpy().astype(np.float64), st.pool.norm2)
+    assert np.array_equal(c.pool_pos[0, :R].cpu().numpy(), st.pool.pos)
+    idx = c.ref_idx[0].cpu().numpy()
+    ref = r["ref"]
+    assert np.array_equal(idx[ref, 0], np.arange(R))
+    assert np.all(idx[ref, 1:] == -1)
+    assert np.all(c.codes[0, ref].cpu().numpy() == 0)
+    assert np.all(c.meta[0, ref].cpu().numpy() == 0)
+
+
+@cuda
+@pytest.mark.parametrize("name", ["tiny", "llama"])
+def test_pool_append_bit_exact(name, request):
+    _check_pool(request.getfixturevalue(name))
+
+
+def _check_idx(r):
+    c, st = r["codec"], r["store"]
+    non = r["non"]
+    gidx = c.ref_idx[0].cpu().numpy().astype(np.int64)[non]
+    oidx = st.idx[non]
+    n_exact, n_swap, bad = idx_parity(gidx, oidx, r["kv64"][non], st.pool.vals, st.pool.pos, non)
+    assert not bad, f"{len(bad)} rows differ beyond near-ties, e.g. row {non[bad[0]]}: " \
+                    f"gpu {gidx[bad[0]]} oracle {oidx[bad[0]]}"
+    return n_exact, n_swap
+
+
+@cuda
+@pytest.mark.parametrize("name", ["tiny", "llama"])
+def test_retrieval_parity(name, request):
+    n_exact, n_swap = _check_idx(request.getfixturevalue(name))
+    assert n_swap <= max(2, 0.001 * (n_exact + n_swap))
+
+
+def _same_idx_rows(r):
+    c, st = r["codec"], r["store"]
+    non = r["non"]
+    gidx = c.ref_idx[0].cpu().numpy().astype(np.int64)
+    return non[np.all(gidx[non] == st.idx[non], axis=1)]
+
+
+@cuda
+@pytest.mark.parametrize("name", ["tiny", "llama"])
+def test_encoder_operand_rows_bit_exact(name, request):
+    r = request.getfixturevalue(name)
+    c, st, w = r["codec"], r["store"], r["w"]
+    non = r["non"]
+    ptr, nbytes = c.debug_scratch(0)
+    X = device_bytes(ptr, 2 * len(non) * w.d_kv * 2).view(torch.bfloat16).view(2 * len(non), w.d_kv)
+    X = np64(X)
+    assert np.array_equal(X[0::2], F.bf16(r["kv64"][non]))
+    ok = set(_same_idx_rows(r).tolist())
+    rows = [i for i, p in enumerate(non) if p in ok]
+    means = np.stack([C.reference_mean(st.pool.vals, st.idx[non[i]][st.idx[non[i]] >= 0])
+                      for i in rows])
+    assert np.array_equal(X[1::2][rows], F.bf16(means))
+
+
+@cuda
+@pytest.mark.parametrize("name", ["tiny", "llama"])
+def test_swiglu_hidden_rows(name, request):
+    r = request.getfixturevalue(name)
+    c, st, w = r["codec"], r["store"], r["w"]
+    non = r["non"]
+    ptr, _ = c.debug_scratch(1)
+    H = np64(device_bytes(ptr, 2 * len(non) * w.d_ff * 2).view(torch.bfloat16).view(2 * len(non), w.d_ff))
+    # the oracle's own operand rows (kv, mean) for tokens whose retrieval matched
+    ok = set(_same_idx_rows(r).tolist())
+    rows = [i for i, p in enumerate(non) if p in ok][:256]
+    means = np.stack([C.reference_mean(st.pool.vals, st.idx[non[i]][st.idx[non[i]] >= 0])
+                      for i in rows])
+    Xo = np.empty((2 * len(rows), w.d_kv))
+    Xo[0::2] = F.bf16(r["kv64"][non[rows]])
+    Xo[1::2] = F.bf16(means)
+    sub = np.stack([2 * np.array(rows), 2 * np.array(rows) + 1], axis=1).ravel()
+    ref = C.swiglu_hidden(Xo, r["W64"]["Wc1"], r["W64"]["Wc2"], "operand")
+    ref[1::2] *= -1.0                                  # the kernel stores -h(mean)
+    got = H[sub]
+    rel = np.abs(got - ref) / np.maximum(np.abs(ref), 1e-30)
+    # identical except rare last-bit flips of the bf16 rounding (fp32 accumulation order)
+    assert np.mean(got == ref) > 0.99
+    assert np.max(rel[got != ref]) <= 2 ** -7 if np.any(got != ref) else True
+
+
+@cuda
+@pytest.mark.parametrize("name", ["tiny", "llama"])
+def test_codes_parity(name, request):
+    r = request.getfixturevalue(name)
+    c, st, sh = r["codec"], r["store"], r["sh"]
+    rows = _same_idx_rows(r)
+    packed = c.codes[0].cpu().numpy()[rows]
+    gq = C.unpack_codes(packed, sh.bits, sh.d_c)
+    gmeta = c.meta[0].cpu().numpy().astype(np.float64)[rows]
+    frac, viol = code_parity(gq, gmeta, st.q[rows], st.meta[rows], st.z[rows], sh.bits, sh.group)
+    assert frac >= 0.999, f"only {frac:.5f} of codes identical"
+    assert not viol, f"{len(viol)} code violations, first {viol[:3]}"
+
+
+@cuda
+@pytest.mark.parametrize("name", ["tiny", "llama"])
+def test_reconstruct_end_to_end(name, request):
+    r = request.getfixturevalue(name)
+    c, st, w = r["codec"], r["store"], r["w"]
+    T = r["T"]
+    sel = synth.gen_selection(T, int(round(0.3 * T)), 21)
+    K, V = c.reconstruct(torch.zeros_like(sel).cuda(), sel.cuda())
+    torch.cuda.synchronize()
+    assert c.get_status() == 0
+    Ko, Vo, _ = C.reconstruct(st, sel.numpy().astype(np.int64), r["W64"], "operand")
+    assert rel_fro(np64(K), Ko) <= 1e-2
+    assert rel_fro(np64(V), Vo) <= 1e-2
+
+
+@cuda
+def test_reconstruct_from_oracle_codes_fp32():
+    """Read path alone: storage written from the oracle, fp32 output."""
+    w = synth.workload("llama8b")
+    T = 2048
+    kv64 = np64(synth.gen_kv(w, 31, T=T))
+    W = synth.gen_weights(w, 32)
+    W64 = _weights64(W)
+    sh = oracle_shape(w)
+    st = C.compress_sequence(kv64, W64, sh, "operand")
+    c = make_codec(w, W, T=T, out_dtype="fp32")
+    R = len(st.pool.pos)
+    c.pool_fp8[0, :R] = torch.from_numpy(st.pool.codes).cuda()
+    c.ref_idx[0] = torch.from_numpy(st.idx.astype(np.int32)).cuda()
+    c.codes[0] = torch.from_numpy(st.packed).cuda()
+    c.meta[0] = torch.from_numpy(st.meta.astype(np.float16)).cuda()
+    sel = synth.gen_selection(T, 700, 33)
+    K, V = c.reconstruct(torch.zeros_like(sel).cuda(), sel.cuda())
+    torch.cuda.synchronize()
+    assert c.get_status() == 0
+    Ko, Vo, _ = C.reconstruct(st, sel.numpy().astype(np.int64), W64, "operand")
+    assert rel_fro(np64(K), Ko) <= 1e-5
+    assert rel_fro(np64(V), Vo) <= 1e-5
+
+
+@cuda
+def test_zero_decoder_returns_mean_and_refs_exact():
+    w = synth.workload("tiny")
+    T = w.T
+    kv = synth.gen_kv(w, 41)
+    W = synth.gen_weights(w, 42)
+    W["Wd"] = torch.zeros_like(W["Wd"])
+    c = make_codec(w, W, T=T)
+    gpu_prefill(c, kv.cuda(), w.stride)
+    pos = torch.arange(T, dtype=torch.int32)
+    K, V = c.reconstruct(torch.zeros_like(pos).cuda(), pos.cuda())
+    torch.cuda.synchronize()
+    st = C.compress_sequence(np64(kv), _weights64(W), oracle_shape(w), "operand")
+    gidx = c.ref_idx[0].cpu().numpy()
+    same = np.all(gidx == st.idx, axis=1)                # compare where retrieval matched
+    assert same.mean() > 0.99
+    means = np.stack([C.reference_mean(st.pool.vals, st.idx[p][st.idx[p] >= 0]) for p in range(T)])
+    Km, Vm = C.split_kv(means, w.n_kv_heads, w.head_dim)
+    assert np.array_equal(np64(V)[same], Vm[same])      # fp32 output: exactly the mean
+    assert np.array_equal(np64(K)[0], Km[0])            # position 0: no rotation
+    # reference tokens: their FP8 value, exactly
+    refs = np.arange(0, T, w.stride)
+    fp8 = F.e4m3_decode(F.e4m3_encode(np64(kv)[refs]))
+    Kr, Vr = C.split_kv(fp8, w.n_kv_heads, w.head_dim)
+    assert np.array_equal(np64(V)[refs], Vr)
+
+
+@cuda
+def test_device_errors_flag_and_zero_rows():
+    w = synth.workload("tiny")
+    T = w.T
+    kv = synth.gen_kv(w, 51)
+    W = synth.gen_weights(w, 52)
+    c = make_codec(w, W, T=T + 64)            # positions >= T never written
+    gpu_prefill(c, kv.cuda(), w.stride)
+    torch.cuda.synchronize()
+    assert c.get_status() == 0
+    seq = torch.tensor([0, 0, 5, 0], dtype=torch.int32).cuda()
+    pos = torch.tensor([3, T + 10, 3, 100000], dtype=torch.int32).cuda()
+    K, V = c.reconstruct(seq, pos)
+    torch.cuda.synchronize()
+    flags = c.get_status()
+    from residual_kv_cache_gb300 import FLAG_BAD_INDEX, FLAG_UNWRITTEN
+    assert flags & FLAG_BAD_INDEX and flags & FLAG_UNWRITTEN
+    Kc = K.cpu()
+    assert torch.all(Kc[1:] == 0) and torch.all(V.cpu()[1:] == 0)
+    assert torch.any(Kc[0] != 0)
+    assert c.get_status() == 0                 # cleared by the previous read
+
+
+@cuda
+def test_host_errors():
+    from residual_kv_cache_gb300 import RkvError
+    w = synth.workload("tiny")
+    kv = synth.gen_kv(w, 61).cuda()
+    W = synth.gen_weights(w, 62)
+    c = make_codec(w, W, T=w.T)
+    with pytest.raises(RkvError) as e:            # compress before any reference
+        c.compress(kv, [0], [3])
+    assert e.value.status == -4
+    with pytest.raises(RkvError) as e:            # not a reference position
+        c.pool_append(kv, [0], [3])
+    assert e.value.status == -1
+    with pytest.raises(RkvError) as e:            # out of order
+        c.pool_append(kv, [0], [8])
+    assert e.value.status == -1
+    c.pool_append(kv, [0], [0])
+    with pytest.raises(RkvError) as e:            # needs the reference at 8 first
+        c.compress(kv, [0], [9])
+    assert e.value.status == -1
+    with pytest.raises(RkvError) as e:            # reference position passed to compress
+        c.compress(kv, [0], [0])
+    assert e.value.status == -1
+    with pytest.raises(RkvError) as e:            # sequence out of range
+        c.compress(kv, [1], [3])
+    assert e.value.status == -1
+    big = make_codec(w, W, T=64)
+    with pytest.raises(RkvError):
+        big.pool_append(kv, [0], [64])
+    with pytest.raises(RkvError) as e:            # misaligned kv
+        c.compress(kv.view(-1)[1:1 + 255 * 256].view(255, 256), [0], [3])
+    assert e.value.status == -2
+    c.compress(kv, [0], [3])
+    torch.cuda.synchronize()
+    assert c.get_status() == 0
+
+
+@cuda
+def test_multi_sequence_ragged():
+    """Three sequences of ragged lengths written in interleaved calls; each token only
+    sees its own sequence's pool."""
+    w = synth.workload("llama8b")
+    lens = [300, 515, 1000]
+    Tcap = 1024
+    W = synth.gen_weights(w, 72)
+    W64 = _weights64(W)
+    c = make_codec(w, W, T=Tcap, batch=3)
+    kvs = [synth.gen_kv(w, 70 + b, T=L) for b, L in enumerate(lens)]
+    flat = torch.cat(kvs).cuda()
+    offs = np.cumsum([0] + lens)
+    seq = np.concatenate([np.full(L, b) for b, L in enumerate(lens)]).astype(np.int32)
+    pos = np.concatenate([np.arange(L) for L in lens]).astype(np.int32)
+    rows = np.arange(len(seq), dtype=np.int32)
+    isref = pos % w.stride == 0
+    # append all references (ordered per sequence), then compress interleaved rows
+    c.pool_append(flat, seq[isref], pos[isref], src_rows=rows[isref])
+    rng = np.random.default_rng(0)
+    perm = rng.permutation(np.nonzero(~isref)[0])
+    c.compress(flat, seq[perm], pos[perm], src_rows=rows[perm].astype(np.int32))
+    torch.cuda.synchronize()
+    assert c.get_status() == 0
+    sh = oracle_shape(w)
+    for b, L in enumerate(lens):
+        st = C.compress_sequence(np64(kvs[b]), W64, sh, "operand")
+        non = np.nonzero(np.arange(L) % w.stride)[0]
+        gidx = c.ref_idx[b].cpu().numpy().astype(np.int64)[:L]
+        _, _, bad = idx_parity(gidx[non], st.idx[non], np64(kvs[b])[non], st.pool.vals,
+                               st.pool.pos, non)
+        assert not bad
+        same = non[np.all(gidx[non] == st.idx[non], axis=1)]
+        gq = C.unpack_codes(c.codes[b].cpu().numpy()[same], sh.bits, sh.d_c)
+        frac, viol = code_parity(gq, c.meta[b].cpu().numpy().astype(np.float64)[same],
+                                 st.q[same], st.meta[same], st.z[same], sh.bits)
+        assert frac >= 0.999 and not viol
+        sel = torch.arange(L, dtype=torch.int32)
+        K, V = c.reconstruct(torch.full_like(sel, b).cuda(), sel.cuda())
+        Ko, Vo, _ = C.reconstruct(st, np.arange(L), W64, "operand")
+        assert rel_fro(np64(K), Ko) <= 1e-2 and rel_fro(np64(V), Vo) <= 1e-2
+
+
+@cuda
+@pytest.mark.parametrize("bits", [2, 16])
+def test_int2_and_quant_off(bits):
+    r = _run("llama8b", 2048, seed_kv=81, seed_w=82, bits=bits)
+    _check_pool(r)
+    _check_idx(r)
+    c, st, sh = r["codec"], r["store"], r["sh"]
+    rows = _same_idx_rows(r)
+    if bits == 16:
+        got = C.unpack_codes(c.codes[0].cpu().numpy()[rows], 16, sh.d_c)
+        assert np.mean(got == st.q[rows]) >= 0.999
+    else:
+        gq = C.unpack_codes(c.codes[0].cpu().numpy()[rows], bits, sh.d_c)
+        frac, viol = code_parity(gq, c.meta[0].cpu().numpy().astype(np.float64)[rows],
+                                 st.q[rows], st.meta[rows], st.z[rows], bits)
+        assert frac >= 0.999 and not viol
+    sel = synth.gen_selection(2048, 600, 83)
+    K, V = c.reconstruct(torch.zeros_like(sel).cuda(), sel.cuda())
+    Ko, Vo, _ = C.reconstruct(st, sel.numpy().astype(np.int64), r["W64"], "operand")
+    assert rel_fro(np64(K), Ko) <= 1e-2 and rel_fro(np64(V), Vo) <= 1e-2
+
+
+@cuda
+def test_multi_pass_equals_single_pass():
+    w = synth.workload("llama8b")
+    T = 2048
+    kv = synth.gen_kv(w, 91, T=T).cuda()
+    W = synth.gen_weights(w, 92)
+    a = make_codec(w, W, T=T)
+    b = make_codec(w, W, T=T, max_rows=384)      # five passes of at most 384 rows
+    gpu_prefill(a, kv, w.stride)
+    gpu_prefill(b, kv, w.stride)
+    torch.cuda.synchronize()
+    assert torch.equal(a.ref_idx, b.ref_idx)
+    assert torch.equal(a.codes, b.codes)
+    assert torch.equal(a.meta, b.meta)
