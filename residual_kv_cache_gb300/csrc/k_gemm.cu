@@ -375,14 +375,22 @@ cudaError_t launch_gemm3_quant(rkv_ctx* c, const PassPlan& p, const int32_t* pla
   Epi3Args ea{plan + p.off_c_dst, p.n_rows, static_cast<uint8_t*>(c->st.codes),
               static_cast<uint32_t*>(c->st.meta), d.code_bytes, d.G, d.bits, 0};
   const char* name = "rkv_gemm3_quant_kernel";
-  if (d.dc % 256 == 0) {
+  // Tile width: the one whose whole waves of one-tile-per-SM finish first (a tile's
+  // main loop costs in proportion to its width).
+  auto waves = [&](int bn) {
+    const int64_t tiles = (int64_t)g.m_tiles * (d.dc / bn);
+    return ((tiles + c->num_sms - 1) / c->num_sms) * bn;
+  };
+  if (d.dc % 256 == 0 && waves(256) <= waves(128)) {
     g.n_tiles = d.dc / 256;
     ea.BN = 256;
     return run_gemm<256, 4, Epi3>(c, c->tm_h3, c->tm_w3, g, ea, name, s);
-  } else if (d.dc % 128 == 0) {
+  }
+  if (d.dc % 128 == 0) {
     g.n_tiles = d.dc / 128;
     ea.BN = 128;
-    return run_gemm<128, 6, Epi3>(c, c->tm_h3, c->tm_w3, g, ea, name, s);
+    return run_gemm<128, 6, Epi3>(c, c->tm_h3, d.dc % 256 == 0 ? c->tm_w3_128 : c->tm_w3, g, ea,
+                                  name, s);
   }
   g.n_tiles = d.dc / 64;
   ea.BN = 64;

@@ -11,10 +11,13 @@
 // comparison.  fp32 queries are split into three bf16 pieces (hi + mid + lo == x), so
 // the products stay exact and the three partial dots accumulate into one fp32 sum.
 //
-// Work unit = one 128-query tile; its pool tiles are the causal prefix only, so tiles
-// late in the sequence do more work; the host plan orders units heaviest first.
+// Work unit = (128-query tile, 256-slot pool tile): all units cost the same, so a
+// persistent grid balances them.  Each unit leaves a sorted partial top-4 per query
+// row; a merge kernel combines a row's partials in increasing slot order with the same
+// strict comparison, which yields exactly the 4 smallest (distance, slot) pairs.
 #include <cuda_bf16.h>
 #include <float.h>
+#include <climits>
 
 #include "tc_common.cuh"
 
@@ -25,8 +28,12 @@ struct RetrieveArgs {
   const int32_t* t_seq;
   const int32_t* t_row0;
   const int32_t* t_nrt;
+  const int32_t* t_u0;
+  const int32_t* u_tile;
+  const int32_t* u_rt;
   const int32_t* q_pos;
   const int32_t* q_dst;
+  int2* part;
   int n_units;
   int nkb;      // k-blocks per piece (2d_k / 64)
   int parts;    // 1 or 3
@@ -115,8 +122,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < kStages; ++s) issued[s] = 0, issued_phase[s] = 0;
       bool ok = true;
       for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x) {
-        const int seq = a.t_seq[u], row0 = a.t_row0[u], nrt = a.t_nrt[u];
-        for (int rt = 0; rt < nrt && ok; ++rt) {
+        const int t = a.u_tile[u], rt = a.u_rt[u];
+        const int seq = a.t_seq[t], row0 = a.t_row0[t];
+        {
           for (int kb = 0; kb < kb_total; ++kb) {
             if (!mbar_wait(&empty[ring.stage], ring.phase ^ 1u, abort_flag, a.status)) {
               ok = false;
@@ -146,8 +154,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int last_stage = 0;
       uint32_t last_phase = 0;
       for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x) {
-        const int nrt = a.t_nrt[u];
-        for (int rt = 0; rt < nrt && ok; ++rt) {
+        {
           if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag, a.status)) {
             ok = false;
             break;
@@ -189,48 +196,51 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x) {
-      const int seq = a.t_seq[u], row0 = a.t_row0[u], nrt = a.t_nrt[u];
+      const int t = a.u_tile[u], rt = a.u_rt[u];
+      const int seq = a.t_seq[t], row0 = a.t_row0[t];
       const int qrow = row0 + row_in_tile;
       const int pos = a.q_pos[qrow];
       const int64_t pbase = (int64_t)seq * a.R_cap;
       float bd[4] = {FLT_MAX, FLT_MAX, FLT_MAX, FLT_MAX};
       int bj[4] = {-1, -1, -1, -1};
-      for (int rt = 0; rt < nrt; ++rt) {
-        if (!warp_wait(&tfull[acc], acc_phase, abort_flag, a.status)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        const uint32_t tacc = tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)(acc * kRefTile);
+      if (!warp_wait(&tfull[acc], acc_phase, abort_flag, a.status)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const uint32_t tacc = tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)(acc * kRefTile);
 #pragma unroll 1
-        for (int c = 0; c < kRefTile / 32; ++c) {
-          uint32_t r[32];
-          tmem_ld32(tacc + c * 32, r);
-          tmem_ld_wait();
-          const int j0 = rt * kRefTile + c * 32;
-#pragma unroll 4
-          for (int i = 0; i < 32; ++i) {
-            const int j = j0 + i;
-            if (j >= a.R_cap) break;
-            const int32_t pj = __ldg(a.pool_pos + pbase + j);
-            if (pos >= 0 && pj < pos) {
-              const float dist = fmaf(-2.0f, __uint_as_float(r[i]), __ldg(a.norm2 + pbase + j));
-              topk_insert(dist, j, bd, bj);
-            }
-          }
+      for (int c = 0; c < kRefTile / 32; ++c) {
+        // lane i fetches column j0+i's position and squared norm once; the warp then
+        // broadcasts them with shuffles, so the drain below has no memory latency.
+        const int j0 = rt * kRefTile + c * 32;
+        const int jl = j0 + (int)lane_id();
+        int32_t pl = INT_MAX;
+        float nl = 0.f;
+        if (jl < a.R_cap) {
+          pl = __ldg(a.pool_pos + pbase + jl);
+          nl = __ldg(a.norm2 + pbase + jl);
         }
-        tc_fence_before();
-        mbar_arrive(&tempty[acc]);
-        if (++acc == 2) {
-          acc = 0;
-          acc_phase ^= 1u;
+        uint32_t r[32];
+        tmem_ld32(tacc + c * 32, r);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          const int32_t pj = __shfl_sync(0xffffffffu, pl, i);
+          const float nj = __shfl_sync(0xffffffffu, nl, i);
+          const float dist = fmaf(-2.0f, __uint_as_float(r[i]), nj);
+          if (pj < pos) topk_insert(dist, j0 + i, bd, bj);
         }
       }
-      if (!ok) break;
-      if (pos >= 0) {
-        const int64_t dst = a.q_dst[qrow];
-        for (int t = 0; t < a.topk; ++t) a.ref_idx[dst * a.topk + t] = bj[t];
+      tc_fence_before();
+      mbar_arrive(&tempty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
       }
+      int4* dp = reinterpret_cast<int4*>(a.part + ((int64_t)u * kTileM + row_in_tile) * 4);
+      dp[0] = make_int4(__float_as_int(bd[0]), bj[0], __float_as_int(bd[1]), bj[1]);
+      dp[1] = make_int4(__float_as_int(bd[2]), bj[2], __float_as_int(bd[3]), bj[3]);
     }
   }
 
@@ -242,10 +252,49 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// One thread per retrieval-order row: merge the row's partial top-4 lists of its pool
+// tiles (increasing slots) and write the final slots of real rows.
+__global__ void retrieve_merge_kernel(const int2* __restrict__ part, const int32_t* __restrict__ t_nrt,
+                                      const int32_t* __restrict__ t_u0,
+                                      const int32_t* __restrict__ q_pos,
+                                      const int32_t* __restrict__ q_dst, int m_pad, int topk,
+                                      int32_t* __restrict__ ref_idx) {
+  const int q = blockIdx.x * blockDim.x + threadIdx.x;
+  if (q >= m_pad || q_pos[q] < 0) return;
+  const int t = q / kTileM, r = q % kTileM;
+  float bd[4] = {FLT_MAX, FLT_MAX, FLT_MAX, FLT_MAX};
+  int bj[4] = {-1, -1, -1, -1};
+  const int u0 = t_u0[t], nrt = t_nrt[t];
+  for (int k = 0; k < nrt; ++k) {
+    const int4* sp = reinterpret_cast<const int4*>(part + ((int64_t)(u0 + k) * kTileM + r) * 4);
+    const int4 e0 = sp[0], e1 = sp[1];
+    const float d[4] = {__int_as_float(e0.x), __int_as_float(e0.z), __int_as_float(e1.x), __int_as_float(e1.z)};
+    const int j[4] = {e0.y, e0.w, e1.y, e1.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+      if (j[i] >= 0) topk_insert(d[i], j[i], bd, bj);
+  }
+  const int64_t dst = q_dst[q];
+  for (int i = 0; i < topk; ++i) ref_idx[dst * topk + i] = bj[i];
+}
+
 }  // namespace
 
+cudaError_t launch_retrieve_merge(rkv_ctx* c, const PassPlan& p, const int32_t* plan,
+                                  cudaStream_t s) {
+  if (p.m_pad == 0) return cudaSuccess;
+  cudaEvent_t ev;
+  timing_begin(c, "rkv_retrieve_merge_kernel", s, &ev);
+  retrieve_merge_kernel<<<(p.m_pad + 127) / 128, 128, 0, s>>>(
+      c->part, plan + p.off_t_nrt, plan + p.off_t_u0, plan + p.off_q_pos, plan + p.off_q_dst,
+      p.m_pad, c->d.topk, c->st.ref_idx);
+  cudaError_t e = cudaGetLastError();
+  timing_end(c, "rkv_retrieve_merge_kernel", s, ev);
+  return e;
+}
+
 cudaError_t launch_retrieve(rkv_ctx* c, const PassPlan& p, const int32_t* plan, cudaStream_t s) {
-  if (p.n_tiles == 0) return cudaSuccess;
+  if (p.n_units == 0) return cudaSuccess;
   const size_t smem = 1024 + (size_t)kStages * (kTileABytes + kBBytes) + 8 * (2 * kStages + 4) + 16;
   cudaError_t e =
       cudaFuncSetAttribute(retrieve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -254,9 +303,13 @@ cudaError_t launch_retrieve(rkv_ctx* c, const PassPlan& p, const int32_t* plan, 
   a.t_seq = plan + p.off_t_seq;
   a.t_row0 = plan + p.off_t_row0;
   a.t_nrt = plan + p.off_t_nrt;
+  a.t_u0 = plan + p.off_t_u0;
+  a.u_tile = plan + p.off_u_tile;
+  a.u_rt = plan + p.off_u_rt;
   a.q_pos = plan + p.off_q_pos;
   a.q_dst = plan + p.off_q_dst;
-  a.n_units = p.n_tiles;
+  a.part = c->part;
+  a.n_units = p.n_units;
   a.nkb = c->d.dkv / kTileK;
   a.parts = c->d.parts;
   a.R_cap = c->d.R_cap;
@@ -265,7 +318,7 @@ cudaError_t launch_retrieve(rkv_ctx* c, const PassPlan& p, const int32_t* plan, 
   a.pool_pos = c->st.pool_pos;
   a.ref_idx = c->st.ref_idx;
   a.status = c->status;
-  const int grid = p.n_tiles < c->num_sms ? p.n_tiles : c->num_sms;
+  const int grid = p.n_units < c->num_sms ? p.n_units : c->num_sms;
   cudaEvent_t ev;
   timing_begin(c, "rkv_retrieve_kernel", s, &ev);
   retrieve_kernel<<<grid, kThreads, smem, s>>>(c->tm_q, c->tm_pool, a);

@@ -87,8 +87,8 @@ rkv_status derive(const rkv_config* c, Dims* d) {
   d->kv_f32 = c->kv_dtype == RKV_F32;
   d->out_f32 = c->out_dtype == RKV_F32;
   d->parts = d->kv_f32 ? 3 : 1;
-  if (d->N <= 0 || !(d->D == 64 || d->D == 128 || d->D == 256))
-    return fail(RKV_EINVAL, "head_dim must be 64, 128 or 256 and n_kv_heads > 0");
+  if (d->N <= 0 || !(d->D == 64 || d->D == 128))
+    return fail(RKV_EINVAL, "head_dim must be 64 or 128 and n_kv_heads > 0");
   if (d->dkv % 256 != 0) return fail(RKV_EINVAL, "2*N*D must be a multiple of 256");
   if (d->dc <= 0 || d->dc % 64 != 0) return fail(RKV_EINVAL, "d_c must be a positive multiple of 64");
   if (d->dff <= 0 || d->dff % 128 != 0) return fail(RKV_EINVAL, "d_ff must be a positive multiple of 128");
@@ -212,7 +212,9 @@ rkv_status rkv_create(const rkv_config* cfg, const void* Wc1, const void* Wc2, c
   c->max_rows = (c->max_rows + kTileM - 1) / kTileM * kTileM;
   c->m_cap = c->max_rows + kTileM * std::min(d.B, c->max_rows);
   c->tiles_cap = c->m_cap / kTileM;
-  c->plan_ints = std::max(3 * c->m_cap + 3 * c->tiles_cap + 2 * c->max_rows, 4 * c->max_rows);
+  c->units_cap = c->tiles_cap * ((d.R_cap + kRefTile - 1) / kRefTile);
+  c->plan_ints = std::max(3 * c->m_cap + 4 * c->tiles_cap + 2 * c->units_cap + 2 * c->max_rows,
+                          4 * c->max_rows);
   c->pool_count.assign(d.B, 0);
 
   auto alloc = [&](void** p, size_t bytes) -> cudaError_t { return cudaMalloc(p, bytes); };
@@ -228,6 +230,7 @@ rkv_status rkv_create(const rkv_config* cfg, const void* Wc1, const void* Wc2, c
   ALLOC(c->Q, (size_t)c->m_cap * d.parts * d.dkv * 2);
   ALLOC(c->X, (size_t)2 * c->max_rows * d.dkv * 2);
   ALLOC(c->H, (size_t)2 * c->max_rows * d.dff * 2);
+  ALLOC(c->part, (size_t)c->units_cap * kTileM * 4 * sizeof(int2));
   ALLOC(c->plan_dev[0], (size_t)c->plan_ints * 4);
   ALLOC(c->plan_dev[1], (size_t)c->plan_ints * 4);
   ALLOC(c->status, 64);
@@ -278,6 +281,8 @@ rkv_status rkv_create(const rkv_config* cfg, const void* Wc1, const void* Wc2, c
   ok &= make_map(&c->tm_h3, c->H, (uint64_t)2 * d.dff, c->max_rows, (uint64_t)2 * d.dff * 2, kTileM);
   const uint32_t bn3 = d.dc % 256 == 0 ? 256u : (d.dc % 128 == 0 ? 128u : 64u);
   ok &= make_map(&c->tm_w3, c->w3, d.dff, d.dc, (uint64_t)d.dff * 2, bn3);
+  if (d.dc % 128 == 0)
+    ok &= make_map(&c->tm_w3_128, c->w3, d.dff, d.dc, (uint64_t)d.dff * 2, 128u);
   ok &= make_map(&c->tm_wd, c->wd, d.dc, dkv, (uint64_t)d.dc * 2, kDecN);
   if (!ok) {
     rkv_free(c);
@@ -374,7 +379,6 @@ rkv_status rkv_compress(rkv_ctx* c, const void* kv, int64_t kv_row_stride, const
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   std::vector<int> order;
-  std::vector<std::pair<int, int>> tiles;   // (nrt, tile index)
   for (int r0 = 0; r0 < n; r0 += c->max_rows) {
     const int m = std::min(c->max_rows, n - r0);
     // ---- plan: rows grouped by sequence (stable), each group padded to 128 rows
@@ -395,21 +399,39 @@ rkv_status rkv_compress(rkv_ctx* c, const void* kv, int64_t kv_row_stride, const
     }
     p.m_pad = m_pad;
     p.n_tiles = ntiles;
+    // units: every (tile, pool tile) of the causal prefix; counted below
+    int n_units = 0;
+    for (int i = 0; i < m;) {
+      int j = i;
+      while (j < m && seq[order[j]] == seq[order[i]]) ++j;
+      for (int k = i; k < j; k += kTileM) {
+        int maxvis = 1;
+        for (int r = k; r < std::min(j, k + kTileM); ++r)
+          maxvis = std::max(maxvis, visible_refs(pos[order[r]], d.stride));
+        n_units += (maxvis + kRefTile - 1) / kRefTile;
+      }
+      i = j;
+    }
+    p.n_units = n_units;
     p.off_q_src = 0;
     p.off_q_pos = m_pad;
     p.off_q_dst = 2 * m_pad;
     p.off_t_seq = 3 * m_pad;
-    p.off_t_row0 = 3 * m_pad + ntiles;
-    p.off_t_nrt = 3 * m_pad + 2 * ntiles;
-    p.off_c_q = 3 * m_pad + 3 * ntiles;
+    p.off_t_row0 = p.off_t_seq + ntiles;
+    p.off_t_nrt = p.off_t_row0 + ntiles;
+    p.off_t_u0 = p.off_t_nrt + ntiles;
+    p.off_u_tile = p.off_t_u0 + ntiles;
+    p.off_u_rt = p.off_u_tile + n_units;
+    p.off_c_q = p.off_u_rt + n_units;
     p.off_c_dst = p.off_c_q + m;
     p.total_ints = p.off_c_dst + m;
+    if (n_units > c->units_cap)
+      return fail(RKV_ECAPACITY, "compress pass exceeds the planned retrieval scratch");
     if (m_pad > c->m_cap || p.total_ints > c->plan_ints)
       return fail(RKV_ECAPACITY, "compress pass exceeds the planned scratch");
     int b;
     int32_t* h = staging_acquire(c, &b);
-    int q = 0, t = 0;
-    tiles.clear();
+    int q = 0;
     std::vector<int32_t> tseq, trow0, tnrt;
     for (int i = 0; i < m;) {
       int j = i;
@@ -441,20 +463,23 @@ rkv_status rkv_compress(rkv_ctx* c, const void* kv, int64_t kv_row_stride, const
       q += padded;
       i = j;
     }
-    // heaviest tiles first
-    std::vector<int> tord(ntiles);
-    for (int i = 0; i < ntiles; ++i) tord[i] = i;
-    std::stable_sort(tord.begin(), tord.end(), [&](int a, int b2) { return tnrt[a] > tnrt[b2]; });
+    // tiles in order; units tile-major, pool tiles in increasing slot order
+    int u = 0;
     for (int i = 0; i < ntiles; ++i) {
-      h[p.off_t_seq + i] = tseq[tord[i]];
-      h[p.off_t_row0 + i] = trow0[tord[i]];
-      h[p.off_t_nrt + i] = tnrt[tord[i]];
+      h[p.off_t_seq + i] = tseq[i];
+      h[p.off_t_row0 + i] = trow0[i];
+      h[p.off_t_nrt + i] = tnrt[i];
+      h[p.off_t_u0 + i] = u;
+      for (int rt = 0; rt < tnrt[i]; ++rt, ++u) {
+        h[p.off_u_tile + u] = i;
+        h[p.off_u_rt + u] = rt;
+      }
     }
-    (void)t;
     CUDA_OK(staging_upload(c, b, p.total_ints, st));
     const int32_t* plan = c->plan_dev[b];
     CUDA_OK(launch_prep_queries(c, kv, kv_row_stride, plan + p.off_q_src, p.m_pad, st));
     CUDA_OK(launch_retrieve(c, p, plan, st));
+    CUDA_OK(launch_retrieve_merge(c, p, plan, st));
     CUDA_OK(launch_mean_rows(c, p, plan, st));
     CUDA_OK(launch_gemm12(c, p.n_rows, st));
     CUDA_OK(launch_gemm3_quant(c, p, plan, st));
@@ -509,6 +534,7 @@ void rkv_free(rkv_ctx* c) {
   cudaFree(c->Q);
   cudaFree(c->X);
   cudaFree(c->H);
+  cudaFree(c->part);
   cudaFree(c->status);
   for (int b = 0; b < 2; ++b) {
     cudaFree(c->plan_dev[b]);

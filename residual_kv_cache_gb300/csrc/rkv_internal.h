@@ -16,7 +16,7 @@ constexpr int kTileM = 128;        // rows per tensor-core tile (one TMEM lane p
 constexpr int kTileK = 64;         // bf16 elements per 128-byte swizzled row
 constexpr int kRefTile = 256;      // references per retrieval tile
 constexpr int kEncN = 256;         // GEMM-1/2 N tile: 128 W_c1 + 128 W_c2 columns
-constexpr int kDecN = 256;         // decoder N tile
+constexpr int kDecN = 128;         // decoder N tile (one head of D = 128)
 constexpr int kRopeLo = 512;       // positions per low RoPE table
 
 // Derived sizes of a configuration.
@@ -42,9 +42,11 @@ struct TimingSlot {
 struct PassPlan {
   int n_rows = 0;      // compact rows (this pass)
   int m_pad = 0;       // retrieval-order rows, padded per sequence to 128
-  int n_tiles = 0;     // retrieval tiles
+  int n_tiles = 0;     // retrieval tiles (128 query rows of one sequence)
+  int n_units = 0;     // retrieval units: (tile, 256-reference pool tile)
   // offsets (in int32 elements) inside the plan buffer
-  int off_q_src, off_q_pos, off_q_dst, off_t_seq, off_t_row0, off_t_nrt, off_c_q, off_c_dst;
+  int off_q_src, off_q_pos, off_q_dst, off_t_seq, off_t_row0, off_t_nrt, off_t_u0, off_u_tile,
+      off_u_rt, off_c_q, off_c_dst;
   int total_ints = 0;
 };
 
@@ -69,6 +71,8 @@ struct rkv_ctx {
   __nv_bfloat16* Q = nullptr;     // [m_cap, parts * 2d_k] retrieval-order queries
   __nv_bfloat16* X = nullptr;     // [2 max_rows, 2d_k] kv / mean rows interleaved
   __nv_bfloat16* H = nullptr;     // [2 max_rows, d_ff] SwiGLU rows (mean rows negated)
+  int2* part = nullptr;           // [units_cap, 128, 4] partial top-k (distance bits, slot)
+  int units_cap = 0;
   int32_t* plan_dev[2] = {nullptr, nullptr};
   int32_t* plan_host[2] = {nullptr, nullptr};   // pinned staging
   cudaEvent_t plan_copied[2] = {nullptr, nullptr};
@@ -77,7 +81,7 @@ struct rkv_ctx {
   int* status = nullptr;          // device status word
 
   // TMA descriptors (fixed addresses, built once)
-  CUtensorMap tm_q, tm_pool, tm_x, tm_w12, tm_h3, tm_w3, tm_wd;
+  CUtensorMap tm_q, tm_pool, tm_x, tm_w12, tm_h3, tm_w3, tm_w3_128, tm_wd;
 
   // host mirror of each sequence's pool fill
   std::vector<int32_t> pool_count;
@@ -101,6 +105,8 @@ cudaError_t launch_pool_append(rkv_ctx* c, const void* kv, int64_t stride, const
 cudaError_t launch_prep_queries(rkv_ctx* c, const void* kv, int64_t stride, const int32_t* q_src,
                                 int m_pad, cudaStream_t s);
 cudaError_t launch_retrieve(rkv_ctx* c, const PassPlan& p, const int32_t* plan, cudaStream_t s);
+cudaError_t launch_retrieve_merge(rkv_ctx* c, const PassPlan& p, const int32_t* plan,
+                                  cudaStream_t s);
 cudaError_t launch_mean_rows(rkv_ctx* c, const PassPlan& p, const int32_t* plan, cudaStream_t s);
 cudaError_t launch_gemm12(rkv_ctx* c, int n_rows, cudaStream_t s);
 cudaError_t launch_gemm3_quant(rkv_ctx* c, const PassPlan& p, const int32_t* plan,

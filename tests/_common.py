@@ -128,3 +128,121 @@ def code_parity(gq: np.ndarray, gmeta: np.ndarray, oq: np.ndarray, ometa: np.nda
 
 def rel_fro(a: np.ndarray, b: np.ndarray) -> float:
     return float(np.linalg.norm((a - b).ravel()) / max(np.linalg.norm(b.ravel()), 1e-300))
+
+
+# ---------------------------------------------------------------------------------
+# Ambiguity bounds.  The kernels multiply bf16 operands on the tensor cores and
+# accumulate in fp32, 16 products per instruction, instructions issued in K order;
+# then H is rounded to bf16.  Where the exact value lies within the fp32 evaluation
+# error of a rounding boundary, both neighbouring results are correct.  These helpers
+# compute, from the oracle's own values only, the interval every correct evaluation
+# lands in, and check that the GPU's values are valid roundings inside it.
+# Accumulation bound (first order, rigorous for that order): each addition into the
+# running sum S_m rounds once, so |err| <= (u/2) sum_m (|S_m| + sum_chunk |x w|), with
+# the second term covering the rounding inside one 16-product instruction.
+# ---------------------------------------------------------------------------------
+U32 = 2.0 ** -24
+
+
+def fp32_chunked_bound(X: np.ndarray, W: np.ndarray, chunk: int = 16) -> np.ndarray:
+    """Bound on |fl32(X W) - X W| for a K-ordered accumulation in 16-wide chunks."""
+    n, K = X.shape
+    S = np.zeros((n, W.shape[1]))
+    acc = np.zeros_like(S)
+    for k0 in range(0, K, chunk):
+        xs, ws = X[:, k0:k0 + chunk], W[k0:k0 + chunk]
+        S += xs @ ws
+        acc += np.abs(S) + np.abs(xs) @ np.abs(ws)
+    return 0.5 * U32 * acc
+
+
+def hidden_bounds(X: np.ndarray, Wc1: np.ndarray, Wc2: np.ndarray):
+    """For operand rows X (bf16 values): exact h = Swish(X Wc1) * (X Wc2), a bound dh on
+    a fp32 evaluation's error, and the bf16 roundings of h - dh and h + dh."""
+    a1, a2 = X @ Wc1, X @ Wc2
+    da1 = fp32_chunked_bound(X, Wc1)
+    da2 = fp32_chunked_bound(X, Wc2)
+    with np.errstate(over="ignore"):
+        sig = 1.0 / (1.0 + np.exp(-a1))
+    sw = a1 * sig
+    dsw = np.abs(sig * (1.0 + a1 * (1.0 - sig)))
+    h = sw * a2
+    # Swish and the product in fp32: expf, add, divide, multiply (a few ulps)
+    dh = dsw * da1 * np.abs(a2) + np.abs(sw) * da2 + 8 * U32 * np.abs(h) + da1 * da2
+    return h, dh, F.bf16(h - dh), F.bf16(h + dh)
+
+
+def z_bounds(Hk, Hk_lo, Hk_hi, Hm, Hm_lo, Hm_hi, Wc3):
+    """z = Hk W3 - Hm W3 for the oracle's bf16 H, and a half-width covering every
+    valid rounding of H plus the fp32 accumulation of the 2 d_ff products (h(kv) half
+    first, then the -h(mean) half, as the kernel issues them)."""
+    aw = np.abs(Wc3)
+    z = Hk @ Wc3 - Hm @ Wc3
+    dk = np.maximum(Hk_hi - Hk, Hk - Hk_lo)
+    dm = np.maximum(Hm_hi - Hm, Hm - Hm_lo)
+    Xcat = np.concatenate([Hk, -Hm], axis=1)
+    Wcat = np.concatenate([Wc3, Wc3], axis=0)
+    w = dk @ aw + dm @ aw + fp32_chunked_bound(Xcat, Wcat) \
+        + fp32_chunked_bound(np.concatenate([dk, dm], axis=1), np.abs(Wcat))
+    return z, w
+
+
+def check_codes_interval(gq, gmeta, z, w, bits, g=32, window=1e-3):
+    """Every GPU extreme must be the directed FP16 rounding of the extreme of some z' in
+    [z - w, z + w]; every GPU code must be the rounding (in binary32, the kernel's
+    precision) of (z' - min)/Delta under the GPU's own extremes for such a z', widened
+    by `window` quantisation steps.  Returns a list of violations."""
+    viol = []
+    n, d_c = z.shape
+    levels = 2 ** bits - 1
+    for gi, a in enumerate(range(0, d_c, g)):
+        zl, zh = z[:, a:a + g] - w[:, a:a + g], z[:, a:a + g] + w[:, a:a + g]
+        lo_min, lo_max = F.fp16_rd(zl.min(1)), F.fp16_rd(zh.min(1))
+        hi_min, hi_max = F.fp16_ru(zl.max(1)), F.fp16_ru(zh.max(1))
+        glo, ghi = gmeta[:, gi, 0], gmeta[:, gi, 1]
+        # a constant group stores the nearest FP16 of its value
+        exact_const = (w[:, a:a + g].max(1) == 0) & (z[:, a:a + g].min(1) == z[:, a:a + g].max(1))
+        okm = ((glo >= lo_min) & (glo <= lo_max) & (ghi >= hi_min) & (ghi <= hi_max)) | exact_const
+        for r in np.nonzero(~okm)[0]:
+            viol.append(("meta", int(r), gi, float(glo[r]), float(ghi[r]), float(lo_min[r]),
+                         float(lo_max[r]), float(hi_min[r]), float(hi_max[r])))
+        lo32 = glo.astype(np.float32)[:, None]
+        delta = (ghi.astype(np.float32)[:, None] - lo32) / np.float32(levels)
+        with np.errstate(divide="ignore", invalid="ignore"):
+            ul = ((zl.astype(np.float32) - lo32) / delta).astype(np.float64) - window
+            uh = ((zh.astype(np.float32) - lo32) / delta).astype(np.float64) + window
+        qmin = np.clip(np.rint(ul), 0, levels)
+        qmax = np.clip(np.rint(uh), 0, levels)
+        zero = (delta[:, 0] == 0)
+        qmin[zero] = 0
+        qmax[zero] = 0
+        q = gq[:, a:a + g]
+        bad = (q < qmin) | (q > qmax)
+        for r, c in zip(*np.nonzero(bad)):
+            viol.append(("code", int(r), int(a + c), int(q[r, c]), float(ul[r, c]), float(uh[r, c])))
+    return viol
+
+
+def oracle_operand_rows(kv64_rows: np.ndarray, pool_vals: np.ndarray, idx_rows: np.ndarray):
+    """bf16 kv rows and bf16 mean rows exactly as the oracle forms them."""
+    means = np.stack([C.reference_mean(pool_vals, i[i >= 0]) for i in idx_rows])
+    return F.bf16(kv64_rows), F.bf16(means)
+
+
+def encoder_intervals(kv64_rows, pool_vals, idx_rows, W64):
+    """Hidden and code intervals of the oracle for the given tokens."""
+    xk, xm = oracle_operand_rows(kv64_rows, pool_vals, idx_rows)
+    hk, dhk, hk_lo, hk_hi = hidden_bounds(xk, W64["Wc1"], W64["Wc2"])
+    hm, dhm, hm_lo, hm_hi = hidden_bounds(xm, W64["Wc1"], W64["Wc2"])
+    Hk, Hm = F.bf16(hk), F.bf16(hm)
+    z, w = z_bounds(Hk, hk_lo, hk_hi, Hm, hm_lo, hm_hi, W64["Wc3"])
+    return dict(Hk=Hk, Hk_lo=hk_lo, Hk_hi=hk_hi, Hm=Hm, Hm_lo=hm_lo, Hm_hi=hm_hi, z=z, w=w)
+
+
+def codes_identical_fraction(gq, gmeta, oq, ometa, g=32):
+    """Fraction of identical codes over the groups whose FP16 extremes agree (where the
+    extremes differ - a validated rounding ambiguity - the codes are not comparable)."""
+    n, d_c = gq.shape
+    same_meta = np.all(gmeta == ometa, axis=2)                     # [n, G]
+    mask = np.repeat(same_meta, g, axis=1)[:, :d_c]
+    return float(np.mean((gq == oq)[mask])) if mask.any() else 1.0

@@ -17,8 +17,8 @@ import synth
 from oracle import codec as C
 from oracle import formats as F
 
-from _common import (code_parity, device_bytes, gpu_prefill, idx_parity, make_codec, np64,
-                     oracle_shape, rel_fro)
+from _common import (codes_identical_fraction, check_codes_interval, device_bytes, encoder_intervals, gpu_prefill,
+                     idx_parity, make_codec, np64, oracle_shape, rel_fro)
 
 pytestmark = pytest.mark.gpu
 
@@ -131,20 +131,33 @@ def test_swiglu_hidden_rows(name, request):
     H = np64(device_bytes(ptr, 2 * len(non) * w.d_ff * 2).view(torch.bfloat16).view(2 * len(non), w.d_ff))
     # the oracle's own operand rows (kv, mean) for tokens whose retrieval matched
     ok = set(_same_idx_rows(r).tolist())
-    rows = [i for i, p in enumerate(non) if p in ok][:256]
-    means = np.stack([C.reference_mean(st.pool.vals, st.idx[non[i]][st.idx[non[i]] >= 0])
-                      for i in rows])
-    Xo = np.empty((2 * len(rows), w.d_kv))
-    Xo[0::2] = F.bf16(r["kv64"][non[rows]])
-    Xo[1::2] = F.bf16(means)
-    sub = np.stack([2 * np.array(rows), 2 * np.array(rows) + 1], axis=1).ravel()
-    ref = C.swiglu_hidden(Xo, r["W64"]["Wc1"], r["W64"]["Wc2"], "operand")
-    ref[1::2] *= -1.0                                  # the kernel stores -h(mean)
-    got = H[sub]
-    rel = np.abs(got - ref) / np.maximum(np.abs(ref), 1e-30)
-    # identical except rare last-bit flips of the bf16 rounding (fp32 accumulation order)
-    assert np.mean(got == ref) > 0.99
-    assert np.max(rel[got != ref]) <= 2 ** -7 if np.any(got != ref) else True
+    rows = np.array([i for i, p in enumerate(non) if p in ok][:512])
+    iv = encoder_intervals(r["kv64"][non[rows]], st.pool.vals, st.idx[non[rows]], r["W64"])
+    gk, gm = H[2 * rows], -H[2 * rows + 1]            # the kernel stores -h(mean)
+    assert np.mean(gk == iv["Hk"]) > 0.99 and np.mean(gm == iv["Hm"]) > 0.99
+    # every value is a correct bf16 rounding of some fp32 evaluation of h
+    assert np.all((gk >= iv["Hk_lo"]) & (gk <= iv["Hk_hi"]))
+    assert np.all((gm >= iv["Hm_lo"]) & (gm <= iv["Hm_hi"]))
+
+
+def _codes_check(r, rows, bits=None):
+    c, st, sh = r["codec"], r["store"], r["sh"]
+    bits = sh.bits if bits is None else bits
+    rows = rows[:1024]
+    iv = encoder_intervals(r["kv64"][rows], st.pool.vals, st.idx[rows], r["W64"])
+    packed = c.codes[0].cpu().numpy()[rows]
+    if bits == 16:
+        got = C.unpack_codes(packed, 16, sh.d_c)
+        assert np.mean(got == st.q[rows]) >= 0.9
+        lo, hi = F.bf16(iv["z"] - iv["w"]), F.bf16(iv["z"] + iv["w"])
+        assert np.all((got >= lo) & (got <= hi))
+        return
+    gq = C.unpack_codes(packed, bits, sh.d_c)
+    gmeta = c.meta[0].cpu().numpy().astype(np.float64)[rows]
+    frac = codes_identical_fraction(gq, gmeta, st.q[rows], st.meta[rows])
+    assert frac >= 0.999, f"only {frac:.5f} of codes identical"
+    viol = check_codes_interval(gq, gmeta, iv["z"], iv["w"], bits, sh.group)
+    assert not viol, f"{len(viol)} violations, first {viol[:3]}"
 
 
 @cuda
@@ -152,13 +165,7 @@ def test_swiglu_hidden_rows(name, request):
 def test_codes_parity(name, request):
     r = request.getfixturevalue(name)
     c, st, sh = r["codec"], r["store"], r["sh"]
-    rows = _same_idx_rows(r)
-    packed = c.codes[0].cpu().numpy()[rows]
-    gq = C.unpack_codes(packed, sh.bits, sh.d_c)
-    gmeta = c.meta[0].cpu().numpy().astype(np.float64)[rows]
-    frac, viol = code_parity(gq, gmeta, st.q[rows], st.meta[rows], st.z[rows], sh.bits, sh.group)
-    assert frac >= 0.999, f"only {frac:.5f} of codes identical"
-    assert not viol, f"{len(viol)} code violations, first {viol[:3]}"
+    _codes_check(r, _same_idx_rows(r))
 
 
 @cuda
@@ -172,8 +179,11 @@ def test_reconstruct_end_to_end(name, request):
     torch.cuda.synchronize()
     assert c.get_status() == 0
     Ko, Vo, _ = C.reconstruct(st, sel.numpy().astype(np.int64), r["W64"], "operand")
-    assert rel_fro(np64(K), Ko) <= 1e-2
-    assert rel_fro(np64(V), Vo) <= 1e-2
+    # tokens whose retrieval is a validated near-tie swap have no unique oracle answer
+    same = np.all(c.ref_idx[0].cpu().numpy()[sel.numpy()] == st.idx[sel.numpy()], axis=1)
+    assert same.mean() > 0.9
+    assert rel_fro(np64(K)[same], Ko[same]) <= 1e-2
+    assert rel_fro(np64(V)[same], Vo[same]) <= 1e-2
 
 
 @cuda
@@ -321,14 +331,17 @@ def test_multi_sequence_ragged():
                                st.pool.pos, non)
         assert not bad
         same = non[np.all(gidx[non] == st.idx[non], axis=1)]
+        iv = encoder_intervals(np64(kvs[b])[same], st.pool.vals, st.idx[same], W64)
         gq = C.unpack_codes(c.codes[b].cpu().numpy()[same], sh.bits, sh.d_c)
-        frac, viol = code_parity(gq, c.meta[b].cpu().numpy().astype(np.float64)[same],
-                                 st.q[same], st.meta[same], st.z[same], sh.bits)
-        assert frac >= 0.999 and not viol
+        gm = c.meta[b].cpu().numpy().astype(np.float64)[same]
+        assert codes_identical_fraction(gq, gm, st.q[same], st.meta[same]) >= 0.999
+        viol = check_codes_interval(gq, gm, iv["z"], iv["w"], sh.bits)
+        assert not viol, viol[:3]
         sel = torch.arange(L, dtype=torch.int32)
         K, V = c.reconstruct(torch.full_like(sel, b).cuda(), sel.cuda())
         Ko, Vo, _ = C.reconstruct(st, np.arange(L), W64, "operand")
-        assert rel_fro(np64(K), Ko) <= 1e-2 and rel_fro(np64(V), Vo) <= 1e-2
+        ok = np.all(gidx == st.idx, axis=1)
+        assert rel_fro(np64(K)[ok], Ko[ok]) <= 1e-2 and rel_fro(np64(V)[ok], Vo[ok]) <= 1e-2
 
 
 @cuda
@@ -337,20 +350,13 @@ def test_int2_and_quant_off(bits):
     r = _run("llama8b", 2048, seed_kv=81, seed_w=82, bits=bits)
     _check_pool(r)
     _check_idx(r)
-    c, st, sh = r["codec"], r["store"], r["sh"]
-    rows = _same_idx_rows(r)
-    if bits == 16:
-        got = C.unpack_codes(c.codes[0].cpu().numpy()[rows], 16, sh.d_c)
-        assert np.mean(got == st.q[rows]) >= 0.999
-    else:
-        gq = C.unpack_codes(c.codes[0].cpu().numpy()[rows], bits, sh.d_c)
-        frac, viol = code_parity(gq, c.meta[0].cpu().numpy().astype(np.float64)[rows],
-                                 st.q[rows], st.meta[rows], st.z[rows], bits)
-        assert frac >= 0.999 and not viol
+    c, st = r["codec"], r["store"]
+    _codes_check(r, _same_idx_rows(r), bits)
     sel = synth.gen_selection(2048, 600, 83)
     K, V = c.reconstruct(torch.zeros_like(sel).cuda(), sel.cuda())
     Ko, Vo, _ = C.reconstruct(st, sel.numpy().astype(np.int64), r["W64"], "operand")
-    assert rel_fro(np64(K), Ko) <= 1e-2 and rel_fro(np64(V), Vo) <= 1e-2
+    ok = np.all(c.ref_idx[0].cpu().numpy()[sel.numpy()] == st.idx[sel.numpy()], axis=1)
+    assert rel_fro(np64(K)[ok], Ko[ok]) <= 1e-2 and rel_fro(np64(V)[ok], Vo[ok]) <= 1e-2
 
 
 @cuda
