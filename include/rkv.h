@@ -201,6 +201,40 @@ const char* rkv_last_error(void);
 /* Release the context; NULL is allowed.  Never frees caller storage. */
 void rkv_free(rkv_ctx* ctx);
 
+/*
+ * Retrieval that allocates nothing.  The page has no counterpart to this entry point:
+ * it exists for callers that must not call the CUDA allocator - a serving runtime that
+ * reserves all device memory up front in its own arena, or a step that must not pay
+ * cudaMalloc's implicit device synchronisation.  Such callers cannot create a context
+ * (rkv_create allocates), yet can run the retrieval step on buffers they own.
+ *
+ * Computes, for one sequence, what the retrieval of rkv_compress computes (ResidualKV
+ * notes §2.2): for each query row i, the topk pool slots j with pool_pos[j] < q_pos[i]
+ * nearest in squared L2 distance, nearest first, ties to the smaller slot, -1 padded.
+ *   queries    (device, bf16)  [n, d]   the query rows (bf16 joint K/V rows)
+ *   q_pos      (device, int32) [n]      their positions
+ *   pool       (device, bf16)  [R, d]   the decoded reference rows (rkv_storage.pool_bf16)
+ *   pool_norm2 (device, fp32)  [R]      their squared norms (rkv_storage.pool_norm2)
+ *   pool_pos   (device, int32) [R]      their positions; INT32_MAX marks an empty slot
+ *   out_idx    (device, int32) [n, topk]  output
+ *   flags      (device, int32) or NULL: RKV_FLAG_* bits are ORed into it (the caller
+ *              clears it); a set RKV_FLAG_TIMEOUT means out_idx is not valid.
+ * d must be a multiple of 64, topk in 1..4, queries and pool 16-byte aligned.
+ * Scratch: a fixed 4 MiB device array inside the library (every GPU that loads the
+ * library holds it until the process exits), enough for ceil(n/128)*ceil(R/256) <= 1024
+ * tiles, e.g. n <= 2048 queries against R <= 16384 references; larger calls return
+ * RKV_ECAPACITY before any launch.  Nothing in the array needs to start at zero: each
+ * call writes every entry it later reads.  All calls share the array, so calls whose
+ * kernels overlap on the GPU (different streams, no ordering) race and must not be made.
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress
+ * with that device current); make that first call before any stream capture.  No call
+ * allocates or frees memory.
+ */
+rkv_status rkv_retrieve_noalloc(const void* queries, const int32_t* q_pos, int32_t n,
+                                const void* pool, const float* pool_norm2,
+                                const int32_t* pool_pos, int32_t R, int32_t d, int32_t topk,
+                                int32_t* out_idx, int32_t* flags, void* stream);
+
 /* ---------------------------------------------------------------------------
  * Instrumentation (not part of the method).
  * rkv_set_timing(ctx, 1) records CUDA events around every kernel launch on

@@ -14,7 +14,7 @@ from dataclasses import dataclass
 import numpy as np
 import torch
 
-__all__ = ["RkvError", "RkvLibraryMissing", "Config", "Codec", "lib", "LIB_PATH",
+__all__ = ["RkvError", "RkvLibraryMissing", "Config", "Codec", "lib", "LIB_PATH", "retrieve_noalloc",
            "FLAG_TIMEOUT", "FLAG_BAD_INDEX", "FLAG_UNWRITTEN", "FLAG_FP16_SAT", "FLAG_BAD_SLOT",
            "ABI_FUNCTIONS"]
 
@@ -75,6 +75,7 @@ ABI_FUNCTIONS = {
     "rkv_get_timing": (_I32, [_P, ctypes.POINTER(_Timing), _I32, _I32]),
     "rkv_launch_count": (_I64, [_P]),
     "rkv_debug_scratch": (_I32, [_P, _I32, ctypes.POINTER(_P), ctypes.POINTER(ctypes.c_size_t)]),
+    "rkv_retrieve_noalloc": (_I32, [_P, _P, _I32, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P]),
 }
 
 _lib = None
@@ -159,6 +160,23 @@ def storage_bytes(cfg: Config):
     c = cfg.to_c()
     _check(lib().rkv_storage_bytes(ctypes.byref(c), sizes))
     return list(sizes)
+
+
+def retrieve_noalloc(queries, q_pos, pool, pool_norm2, pool_pos, topk: int = 4, out=None,
+                     flags=None, stream=None):
+    """Top-k retrieval of one sequence through rkv_retrieve_noalloc (no allocation in the
+    library; scratch is a fixed device array).  queries [n, d] bf16, q_pos [n] int32,
+    pool [R, d] bf16, pool_norm2 [R] fp32, pool_pos [R] int32, all CUDA tensors.
+    Returns out [n, topk] int32 (allocated here by torch if not given)."""
+    n, d = queries.shape
+    R = pool.shape[0]
+    if out is None:
+        out = torch.empty((n, topk), dtype=torch.int32, device=queries.device)
+    fp = flags.data_ptr() if flags is not None else None
+    _check(lib().rkv_retrieve_noalloc(queries.data_ptr(), q_pos.data_ptr(), n, pool.data_ptr(),
+                                      pool_norm2.data_ptr(), pool_pos.data_ptr(), R, d, topk,
+                                      out.data_ptr(), fp, _stream_ptr(stream)))
+    return out
 
 
 class Codec:

@@ -16,7 +16,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "librkv.so")
-SOURCES = ["rkv_api.cu", "k_elementwise.cu", "k_gemm.cu", "k_retrieve.cu", "k_reconstruct.cu"]
+SOURCES = ["rkv_api.cu", "k_elementwise.cu", "k_gemm.cu", "k_retrieve.cu", "k_reconstruct.cu",
+           "k_noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
          "--expt-relaxed-constexpr", "-Xptxas", "-v"]

@@ -135,6 +135,8 @@ inline int visible_refs(int pos, int stride) { return (pos - 1) / stride + 1; }
 
 namespace rkv {
 
+void set_error(const char* msg) { g_err = msg ? msg : ""; }
+
 void timing_begin(rkv_ctx* c, const char* name, cudaStream_t s, cudaEvent_t* start) {
   c->launches++;
   *start = nullptr;

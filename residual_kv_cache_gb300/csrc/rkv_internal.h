@@ -114,6 +114,9 @@ cudaError_t launch_gemm3_quant(rkv_ctx* c, const PassPlan& p, const int32_t* pla
 cudaError_t launch_reconstruct(rkv_ctx* c, const int32_t* seq, const int32_t* pos, int n_sel,
                                void* k_out, void* v_out, cudaStream_t s);
 
+// Record the message rkv_last_error returns on this thread.
+void set_error(const char* msg);
+
 // Instrumentation helpers used around every launch.
 void timing_begin(rkv_ctx* c, const char* name, cudaStream_t s, cudaEvent_t* start);
 void timing_end(rkv_ctx* c, const char* name, cudaStream_t s, cudaEvent_t start);
