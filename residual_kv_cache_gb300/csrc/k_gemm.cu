@@ -203,7 +203,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull[a], 1);
-      mbar_init(&tempty[a], 128);
+      mbar_init(&tempty[a], 4);                        // one arrival per epilogue warp
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -311,7 +311,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t tacc = tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)(acc * BN);
       Epi::run(ea, tacc, m, n, row_in_tile, g.status);
       tc_fence_before();
-      mbar_arrive(&tempty[acc]);
+      __syncwarp();
+      if (lane_id() == 0) mbar_arrive(&tempty[acc]);
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;

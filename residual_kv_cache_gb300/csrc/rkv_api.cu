@@ -495,9 +495,10 @@ rkv_status rkv_reconstruct(rkv_ctx* c, const int32_t* seq, const int32_t* pos, i
   if (n_sel < 0) return fail(RKV_EINVAL, "n_sel < 0");
   if (n_sel == 0) return RKV_OK;
   if (!seq || !pos || !k_out || !v_out) return fail(RKV_EINVAL, "NULL seq, pos or output");
-  if (!aligned16(k_out) || !aligned16(v_out) || (reinterpret_cast<uintptr_t>(seq) & 3u) ||
-      (reinterpret_cast<uintptr_t>(pos) & 3u))
-    return fail(RKV_EALIGN, "outputs must be 16-byte aligned, seq/pos 4-byte aligned");
+  // the kernel writes whole 32-byte sectors
+  if ((reinterpret_cast<uintptr_t>(k_out) & 31u) || (reinterpret_cast<uintptr_t>(v_out) & 31u) ||
+      (reinterpret_cast<uintptr_t>(seq) & 3u) || (reinterpret_cast<uintptr_t>(pos) & 3u))
+    return fail(RKV_EALIGN, "outputs must be 32-byte aligned, seq/pos 4-byte aligned");
   CUDA_OK(launch_reconstruct(c, seq, pos, n_sel, k_out, v_out, static_cast<cudaStream_t>(stream)));
   return RKV_OK;
 }

@@ -296,6 +296,14 @@ def test_host_errors():
     c.compress(kv, [0], [3])
     torch.cuda.synchronize()
     assert c.get_status() == 0
+    # outputs must be 32-byte aligned (checked on the host before any launch)
+    from residual_kv_cache_gb300 import lib
+    buf = torch.empty(4 * 256 + 64, dtype=torch.float32, device="cuda")
+    sp = torch.tensor([0, 0], dtype=torch.int32, device="cuda")
+    pp = torch.tensor([3, 5], dtype=torch.int32, device="cuda")
+    st = lib().rkv_reconstruct(c._ctx, sp.data_ptr(), pp.data_ptr(), 2, buf.data_ptr() + 16,
+                               buf.data_ptr() + 16 + 2 * 128 * 4, torch.cuda.current_stream().cuda_stream)
+    assert st == -2
 
 
 @cuda
