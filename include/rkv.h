@@ -65,8 +65,9 @@ enum {
 /*
  * Codec configuration.  Shapes follow ResidualKV notes §2.1 (d_k = N*D, the
  * joint vector kv_i has 2*d_k entries), §2.3 (d_c, d_ff), §2.4 (g, b) and §2.6
- * (fixed reference stride s).  Limits of this build: head_dim in {64, 128}; 2*d_k, d_c multiples of 64 and 2*d_k a multiple of 256; d_ff a
- * multiple of 128; topk in 1..4; group = 32; bits in {4, 2, 16} (16 =
+ * (fixed reference stride s).  Limits of this build: head_dim in {64, 128}; 2*d_k a
+ * multiple of 256; d_c a multiple of 64 and at most 512 (the decoder keeps a token
+ * tile's z~ in tensor memory); d_ff a multiple of 128; topk in 1..4; group = 32; bits in {4, 2, 16} (16 =
  * quantisation off, z kept as bf16).
  */
 typedef struct {

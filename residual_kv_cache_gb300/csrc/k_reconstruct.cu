@@ -5,20 +5,23 @@
 //
 // Work unit = (tile of 128 selected tokens, 128 output columns = one head for D = 128,
 // two for D = 64).  A CTA owns a contiguous range of units, so consecutive units share
-// the token tile.  Two warpgroup pairs alternate units, each owning one TMEM
-// accumulator, so two units' epilogues are in flight while the tensor core runs ahead.
-// Per token tile, the 512 epilogue threads (four warpgroups; the threads of TMEM lane r
-// own token row r):
-//   1. gather the row's codes and FP16 extremes and dequantise them in fp32
-//      (z~ = q * Delta + min, Delta = (max - min) / (2^b - 1)) into bf16 z~ in shared
-//      memory, in the 128-byte-swizzled K-major layout the tensor core reads;
-//   2. build the row's RoPE cos/sin for the group's 32 column pairs (float64-built
-//      two-level tables, angle-addition in fp32) once, and park them in TMEM.
-// Per unit, a TMA ring streams W_d^T tiles, one thread issues tcgen05.mma into one of
-// two TMEM accumulators, and each epilogue thread reads its accumulator row, adds the
-// mean of its <= 4 FP8 references (exact fp32 sum, one division by k_i; every gather
-// is a whole 32-byte sector), rotates K columns with the cached cos/sin and stores K
-// or V in whole sectors.
+// the token tile.  Per token tile, the 512 epilogue threads (four warpgroups; the
+// threads of TMEM lane r own token row r):
+//   1. dequantise the row's codes in fp32 (z~ = q * Delta + min, Delta = (max - min) /
+//      (2^b - 1)) and store bf16 z~ straight into tensor memory, where the tensor core
+//      reads the A operand (two bf16 per 32-bit column);
+//   2. build the row's RoPE cos/sin for its 16 column pairs (float64-built two-level
+//      tables, angle addition in fp32) into shared memory.
+// Per unit, a TMA ring streams W_d^T tiles (the B operand) and one thread issues
+// tcgen05.mma into one of two TMEM accumulators.  Each epilogue warp prefetches, one
+// unit ahead, exactly the reference bytes it will read (its 32 rows x its 16 column
+// pairs x <= 4 references, 16-byte cp.async copies into a private shared-memory slot
+// per reference), so the reference gathers need no cross-warp synchronisation.  Each
+// epilogue thread then sums its row's references (exact in fp32), divides by k_i, adds
+// its accumulator row, rotates the K columns and stores K or V in whole 32-byte sectors.
+//
+// The kernel is bound by the bytes each SM pulls from L2 per unit (128 KB of W_d^T plus
+// 64 KB of reference rows), not by the tensor core.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <cuda_fp8.h>
@@ -28,16 +31,19 @@
 namespace rkv {
 namespace {
 
-// 20 warps: TMA + TMEM, MMA, two idle, 4 x 4 epilogue.  The register file is split
-// over the four SM sub-partitions, so 18 or 20 warps both cap a thread at 96 registers.
+// 20 warps: 0 TMEM + W_d^T producer, 1 MMA, 2..3 idle, 4..19 epilogue.
+// The register file is split over the four SM sub-partitions, so 18 or 20 warps both
+// cap a thread at 96 registers.
 constexpr int kReconThreads = 640;
-constexpr int kEpiGroups = 4;
-constexpr int kEpiWarpR = 4;               // first epilogue warp
-constexpr int kNT = 128;                    // output columns per unit
-constexpr uint32_t kBBytes = kNT * 128;     // one 64-wide k-block of W_d^T rows
+constexpr int kEpiWarpR = 4;                 // first epilogue warp
+constexpr int kNT = 128;                     // output columns per unit
+constexpr uint32_t kBBytes = kNT * 128;      // one 64-wide k-block of W_d^T rows
+constexpr uint32_t kGBytes = 4 * 4 * 2 * kTileM * 16;   // [group][ref][x|y][row] x 16 B
+constexpr uint32_t kCSBytes = 4 * 8 * kTileM * 16;   // cos/sin: 4 groups x 8 float4 x 128 rows
+constexpr uint32_t kBarBytes = 512;
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kRopeCol = 2 * kNT;      // per-group cos/sin caches after the accumulators
-constexpr int kMaxStages = 4;
+constexpr uint32_t kACol = 2 * kNT;          // z~ after the two accumulators
+constexpr int kMaxStages = 8;
 
 struct ReconArgs {
   const int32_t* seq;
@@ -45,7 +51,7 @@ struct ReconArgs {
   int n_sel;
   int n_tiles;   // 2d_k / 128
   int units;
-  int stages;
+  int b_stages;
   const uint8_t* codes;
   const uint32_t* meta;
   const int32_t* ref_idx;
@@ -80,19 +86,34 @@ __device__ __forceinline__ void fp8x16_add2(uint4 v, uint64_t* s) {
   }
 }
 
+// Pool rows (or -1) of the references whose chunks one lane copies: [row half i][ref t].
+struct GatherRows {
+  int r[8];
+};
+
+// Per-tile state of one epilogue thread's token row.
+struct RowState {
+  int valid;    // the row has a readable code and a first reference
+  int vmask;    // bit t: reference t is a valid slot
+  int kcnt;     // number of valid references (k_i)
+  int in_sel;   // the row is one of the n_sel selected tokens
+  int pos;      // the token's position (RoPE)
+};
+
 __global__ void __launch_bounds__(kReconThreads, 1)
     reconstruct_kernel(const __grid_constant__ CUtensorMap tmW, ReconArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int nkb = a.dc / kTileK;
-  uint8_t* sA = smem;                                  // nkb x [128 rows x 128 B]
-  uint8_t* sB = smem + nkb * kTileABytes;              // stages x [128 rows x 128 B]
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + a.stages * kBBytes);
-  uint64_t* empty = full + a.stages;
-  uint64_t* tfull = empty + a.stages;
+  uint8_t* sB = smem;                                       // b_stages x W_d^T k-block
+  uint8_t* sG = sB + a.b_stages * kBBytes;                  // per-warp reference slots
+  float4* sCS = reinterpret_cast<float4*>(sG + kGBytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sCS) + kCSBytes);
+  uint64_t* empty = full + a.b_stages;
+  uint64_t* tfull = empty + a.b_stages;
   uint64_t* tempty = tfull + 2;
-  uint64_t* afull = tempty + 2;
-  uint64_t* afree = afull + 1;                         // the MMAs of a token tile are done
+  uint64_t* afull = tempty + 2;                             // z~ of a tile is in TMEM
+  uint64_t* afree = afull + 1;                              // the MMAs of a tile are done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(afree + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -101,15 +122,15 @@ __global__ void __launch_bounds__(kReconThreads, 1)
   const int u_end = (int)(((int64_t)(blockIdx.x + 1) * a.units) / gridDim.x);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < a.stages; ++s) {
+    for (int s = 0; s < a.b_stages; ++s) {
       mbar_init(&full[s], 1);
       mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 8);                        // the owning pair's eight warps
+      mbar_init(&tempty[b], 16);
     }
-    mbar_init(afull, kEpiGroups * 4);                   // one arrival per epilogue warp
+    mbar_init(afull, 16);
     mbar_init(afree, 1);
     *abort_flag = 0;
     fence_barrier_init();
@@ -128,9 +149,7 @@ __global__ void __launch_bounds__(kReconThreads, 1)
     // ------------------------------------------------ TMA producer: W_d^T tiles
     if (elect_one()) {
       Ring ring;
-      int issued[kMaxStages];
-      uint32_t issued_phase[kMaxStages];
-      for (int s = 0; s < kMaxStages; ++s) issued[s] = 0, issued_phase[s] = 0;
+      uint32_t issued = 0, issued_phase = 0;             // bit s: stage s used / its phase
       bool ok = true;
       for (int u = u_begin; u < u_end && ok; ++u) {
         const int n = u % a.n_tiles;
@@ -141,17 +160,17 @@ __global__ void __launch_bounds__(kReconThreads, 1)
           }
           mbar_arrive_expect_tx(&full[ring.stage], kBBytes);
           tma_load_2d(sB + ring.stage * kBBytes, &tmW, &full[ring.stage], kb * kTileK, n * kNT);
-          issued[ring.stage] = 1;
-          issued_phase[ring.stage] = ring.phase;
-          ring.next(a.stages);
+          issued |= 1u << ring.stage;
+          issued_phase = (issued_phase & ~(1u << ring.stage)) | (ring.phase << ring.stage);
+          ring.next(a.b_stages);
         }
       }
       if (!ok)
-        for (int s = 0; s < a.stages; ++s)
-          if (issued[s]) drain_wait(&full[s], issued_phase[s]);
+        for (int s = 0; s < a.b_stages; ++s)
+          if ((issued >> s) & 1u) drain_wait(&full[s], (issued_phase >> s) & 1u);
     }
   } else if (warp == 1) {
-    // ------------------------------------------------ MMA issuer
+    // ------------------------------------------------ MMA issuer (A from TMEM)
     if (elect_one()) {
       constexpr uint32_t idesc = idesc_bf16_f32(kTileM, kNT);
       Ring ring;
@@ -164,7 +183,7 @@ __global__ void __launch_bounds__(kReconThreads, 1)
       for (int u = u_begin; u < u_end && ok; ++u) {
         const int m = u / a.n_tiles;
         if (m != cur_m) {
-          // the previous tile's A may be overwritten once its MMAs are done
+          // the previous tile's z~ may be overwritten once its MMAs are done
           if (cur_m >= 0) umma_commit(afree);
           if (!mbar_wait(afull, a_phase, abort_flag, a.status)) {
             ok = false;
@@ -185,17 +204,16 @@ __global__ void __launch_bounds__(kReconThreads, 1)
             break;
           }
           tc_fence_after();
-          const uint32_t a0 = smem_u32(sA + kb * kTileABytes);
           const uint32_t b0 = smem_u32(sB + ring.stage * kBBytes);
 #pragma unroll
           for (int k = 0; k < kTileK / 16; ++k)
-            umma_bf16(d, sdesc_sw128(a0 + k * 32), sdesc_sw128(b0 + k * 32), idesc,
-                      (kb | k) != 0 ? 1u : 0u);
+            umma_bf16_ta(d, tmem + kACol + (uint32_t)(kb * (kTileK / 2) + k * 8),
+                         sdesc_sw128(b0 + k * 32), idesc, (kb | k) != 0 ? 1u : 0u);
           umma_commit(&empty[ring.stage]);
           any = true;
           last_stage = ring.stage;
           last_phase = ring.phase;
-          ring.next(a.stages);
+          ring.next(a.b_stages);
         }
         if (!ok) break;
         umma_commit(&tfull[acc]);
@@ -208,300 +226,321 @@ __global__ void __launch_bounds__(kReconThreads, 1)
     }
   } else if (warp >= kEpiWarpR) {
     // Four groups of four consecutive warps (warps 4..19).  Warp w reads TMEM lanes
-    // [32 (w % 4), +32), so every group owns the same 128 rows.  Groups 2p and 2p+1 form
-    // pair p, which handles the CTA's units of parity p with accumulator p; within a
-    // unit, group 2p+h takes column pairs [32h, 32h+32) in two chunks of 16.  Every
-    // group dequantises a quarter of each row's code groups.
+    // [32 (w % 4), +32), so every group owns the same 128 rows; group g takes 16 of each
+    // unit's 64 column pairs and a quarter of each row's code groups.
     const int ew = warp & 3;
     const int wg = (warp - kEpiWarpR) >> 2;
-    const int pr = wg >> 1, hw = wg & 1;
     const int row = ew * 32 + (int)lane_id();        // TMEM lane = tile row
     const uint32_t lane_base = (uint32_t)(ew * 32) << 16;
     const int levels = (1 << a.bits) - 1;
     const int P = a.D / 2;                           // pairs per head
-    const int jbase = (32 * hw) % P;                 // first pair index of the group
-    const uint32_t rope_col = kRopeCol + 64u * (uint32_t)wg;
-    const int g0 = wg * a.G / kEpiGroups;            // this group's code groups [g0, g1)
-    const int g_per = (wg + 1) * a.G / kEpiGroups - g0;
+    const int slot0 = 16 * wg;                       // first of this group's 16 pair slots
+    const int hl = slot0 / P, j0 = slot0 % P;        // head within the unit, first pair
+    const int xcol = hl * a.D + j0, ycol = xcol + P; // unit-local columns of x and y
+    // Reference slots of this group: plane (ref t, x|y) holds 16 bytes per tile row.
+    // Lane l copies, per reference, the x or y chunk (l & 1) of rows 32 ew + (l >> 1) and
+    // 32 ew + 16 + (l >> 1); lane l reads both chunks of its own row.
+    uint8_t* slots = sG + (uint32_t)wg * (4 * 2 * kTileM * 16);
+    const int cp_row0 = ew * 32 + ((int)lane_id() >> 1);
+    const int cp_chunk = (lane_id() & 1) ? (ycol >> 4) : (xcol >> 4);
+    const int g0 = wg * a.G / 4;                     // this group's code groups [g0, g0+g_per)
+    const int g_per = (wg + 1) * a.G / 4 - g0;
+    float4* cs_row = sCS + wg * 8 * kTileM + row;    // entry i at cs_row[i * kTileM]
+
+    int nx_m = -1, nx_s = -1, nx_p = -1;             // prefetched seq/pos of the next tile
+
+    // z~ of tile m into TMEM (the caller has made sure the tensor core is done with the
+    // previous tile), then one arrival per warp on afull.
+    auto setup_a = [&](int m, RowState& st, GatherRows& gr) {
+      const int64_t gi = (int64_t)m * kTileM + row;
+      int s_, p_;
+      if (nx_m == m) {
+        s_ = nx_s;
+        p_ = nx_p;
+      } else {
+        s_ = gi < a.n_sel ? a.seq[gi] : -1;
+        p_ = gi < a.n_sel ? a.pos[gi] : -1;
+      }
+      st.valid = 0;
+      st.vmask = 0;
+      st.kcnt = 0;
+      st.in_sel = gi < a.n_sel;
+      st.pos = 0;
+      bool in_range = false;
+      int64_t dst = 0;
+      if (st.in_sel) {
+        if (s_ < 0 || s_ >= a.B || p_ < 0 || p_ >= a.T_cap) {
+          if (wg == 0) atomicOr(a.status, RKV_FLAG_BAD_INDEX);
+        } else {
+          in_range = true;
+          dst = (int64_t)s_ * a.T_cap + p_;
+          st.pos = p_;
+        }
+      }
+      // one round trip: slots, extremes and codes together
+      int32_t sl[4] = {-1, -1, -1, -1};
+      uint32_t mt[4] = {0u, 0u, 0u, 0u};
+      uint4 cw[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) cw[i] = make_uint4(0u, 0u, 0u, 0u);
+      const uint8_t* crow = a.codes + dst * a.code_bytes;
+      if (in_range) {
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+          if (t < a.topk) sl[t] = a.ref_idx[dst * a.topk + t];
+        if (a.bits != 16) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            if (i < g_per) {
+              const int g = g0 + i;
+              mt[i] = a.meta[dst * a.G + g];
+              if (a.bits == 4) {
+                cw[i] = *reinterpret_cast<const uint4*>(crow + (int64_t)g * 16);
+              } else {
+                const uint2 v = *reinterpret_cast<const uint2*>(crow + (int64_t)g * 8);
+                cw[i] = make_uint4(v.x, v.y, 0u, 0u);
+              }
+            }
+          }
+        }
+      }
+      // the next tile's row metadata, for the next tile change
+      {
+        const int u_next = (m + 1) * a.n_tiles;
+        nx_m = -1;
+        if (u_next < u_end) {
+          const int64_t gn = (int64_t)(m + 1) * kTileM + row;
+          nx_m = m + 1;
+          nx_s = gn < a.n_sel ? a.seq[gn] : -1;
+          nx_p = gn < a.n_sel ? a.pos[gn] : -1;
+        }
+      }
+      if (in_range) {
+        if (sl[0] < 0 && wg == 0) atomicOr(a.status, RKV_FLAG_UNWRITTEN);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          if (sl[t] >= a.R_cap && wg == 0) atomicOr(a.status, RKV_FLAG_BAD_SLOT);
+          if (sl[t] >= 0 && sl[t] < a.R_cap) {
+            st.vmask |= 1 << t;
+            ++st.kcnt;
+          }
+        }
+        st.valid = (st.vmask & 1) && st.kcnt > 0;
+      }
+      // pool rows of the references of the two rows whose chunks this lane copies
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const int mine = ((st.vmask >> t) & 1) ? s_ * a.R_cap + sl[t] : -1;
+        gr.r[t] = __shfl_sync(0xffffffffu, mine, (int)(lane_id() >> 1));
+        gr.r[4 + t] = __shfl_sync(0xffffffffu, mine, 16 + (int)(lane_id() >> 1));
+      }
+      // dequantise this row's share of code groups straight into TMEM
+      if (a.bits == 16) {
+        for (int g = g0; g < g0 + g_per; ++g) {
+          uint32_t o[16];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            const uint4 v = st.valid ? reinterpret_cast<const uint4*>(crow + (int64_t)g * 64)[q]
+                                     : make_uint4(0u, 0u, 0u, 0u);
+            o[4 * q] = v.x, o[4 * q + 1] = v.y, o[4 * q + 2] = v.z, o[4 * q + 3] = v.w;
+          }
+          tmem_st16(tmem + lane_base + kACol + 16u * (uint32_t)g, o);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          if (i >= g_per) break;
+          const int g = g0 + i;
+          const float lo = __half2float(__ushort_as_half((unsigned short)(mt[i] & 0xFFFFu)));
+          const float hi = __half2float(__ushort_as_half((unsigned short)(mt[i] >> 16)));
+          const float delta = __fdiv_rn(__fsub_rn(hi, lo), (float)levels);
+          const uint32_t w4[4] = {cw[i].x, cw[i].y, cw[i].z, cw[i].w};
+          uint32_t o[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int k = 2 * e;                       // first of two coordinates
+            uint32_t q0, q1;
+            if (a.bits == 4) {
+              q0 = (w4[k >> 3] >> (4 * (k & 7))) & 15u;
+              q1 = (w4[k >> 3] >> (4 * (k & 7) + 4)) & 15u;
+            } else {
+              q0 = (w4[k >> 4] >> (2 * (k & 15))) & 3u;
+              q1 = (w4[k >> 4] >> (2 * (k & 15) + 2)) & 3u;
+            }
+            o[e] = st.valid ? pack_bf16x2(__fadd_rn(__fmul_rn((float)q0, delta), lo),
+                                          __fadd_rn(__fmul_rn((float)q1, delta), lo))
+                            : 0u;
+          }
+          tmem_st16(tmem + lane_base + kACol + 16u * (uint32_t)g, o);
+        }
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane_id() == 0) mbar_arrive(afull);
+    };
+
+    // cos/sin of the row's 16 pairs at its own position, into shared memory
+    auto setup_cs = [&](int p) {
+      const float4* th = reinterpret_cast<const float4*>(a.rope_hi + (int64_t)(p >> 9) * P + j0);
+      const float4* tl = reinterpret_cast<const float4*>(a.rope_lo + (int64_t)(p & (kRopeLo - 1)) * P + j0);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 hv = __ldg(th + i), lv = __ldg(tl + i);
+        float4 o;
+        o.x = hv.x * lv.x - hv.y * lv.y;    // cos(A + B), pair 2i
+        o.y = hv.y * lv.x + hv.x * lv.y;    // sin(A + B)
+        o.z = hv.z * lv.z - hv.w * lv.w;    // pair 2i + 1
+        o.w = hv.w * lv.z + hv.z * lv.w;
+        cs_row[i * kTileM] = o;
+      }
+    };
+
+    // One commit group per (unit, reference): copy reference t of unit column block
+    // n_next into its slot (nothing when `active` is false; the group is still committed
+    // so that exactly three groups are always younger than the one waited for).
+    auto issue_ref = [&](const GatherRows& gr, int n_next, bool active, int t) {
+      if (active) {
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+          const int prow = gr.r[4 * i + t];
+          if (prow >= 0) {
+            const uint8_t* src = a.pool8 + (int64_t)prow * a.dkv + n_next * kNT + cp_chunk * 16;
+            uint8_t* dst = slots + ((t * 2 + (int)(lane_id() & 1)) * kTileM + cp_row0 + 16 * i) * 16;
+            cp_async16(dst, src);
+          }
+        }
+      }
+      cp_async_commit();
+    };
+
+    RowState cur, nxt;
+    GatherRows grows;                                  // rows of the tile of the next copies
+    int acc = 0;
     uint32_t acc_phase = 0, afree_phase = 0;
     int cur_m = -1;
-    bool valid = false;
-    int k_i = 0;
-    int32_t rrow[4] = {0, 0, 0, 0};                // pool rows of the references
-    int my_pos = 0;
-    bool have_next = false;
-    int next_m = -1, next_s = -1, next_p = -1;
     bool ok = true;
     for (int u = u_begin; u < u_end && ok; ++u) {
       const int m = u / a.n_tiles, n = u % a.n_tiles;
-      const int64_t gi = (int64_t)m * kTileM + row;
       if (m != cur_m) {
-        // wait until the tensor core is done with the previous tile's A
-        if (cur_m >= 0) {
-          if (!warp_wait(afree, afree_phase, abort_flag, a.status)) break;
-          afree_phase ^= 1u;
+        if (cur_m < 0) {
+          setup_a(m, cur, grows);
+#pragma unroll
+          for (int t = 0; t < 4; ++t) issue_ref(grows, n, true, t);   // the first unit's copies
+        } else {
+          cur = nxt;                                   // z~ already staged before the last unit
         }
         cur_m = m;
-        // ---- this row's metadata (prefetched while the previous tile was processed)
-        int s_, p_;
-        if (have_next && next_m == m) {
-          s_ = next_s;
-          p_ = next_p;
-        } else {
-          s_ = gi < a.n_sel ? a.seq[gi] : -1;
-          p_ = gi < a.n_sel ? a.pos[gi] : -1;
-        }
-        valid = false;
-        k_i = 0;
-        bool in_range = false;
-        int64_t dst = 0;
-        my_pos = 0;
-        if (gi < a.n_sel) {
-          if (s_ < 0 || s_ >= a.B || p_ < 0 || p_ >= a.T_cap) {
-            if (wg == 0) atomicOr(a.status, RKV_FLAG_BAD_INDEX);
-          } else {
-            in_range = true;
-            dst = (int64_t)s_ * a.T_cap + p_;
-            my_pos = p_;
-          }
-        }
-        // one round trip: slots, extremes and codes together
-        int32_t sl[4] = {-1, -1, -1, -1};
-        uint32_t mt[4] = {0u, 0u, 0u, 0u};
-        uint4 cw[4];
+        setup_cs(cur.pos);
+      }
+      // Last unit of its tile: as soon as the tensor core is done with this tile, stage
+      // the next tile's z~ so the MMAs resume while this unit's epilogue runs; from here
+      // on every copy this thread issues is for the next tile.
+      if (u + 1 < u_end && (u + 1) / a.n_tiles != m) {
+        if (!warp_wait(afree, afree_phase, abort_flag, a.status)) break;
+        afree_phase ^= 1u;
+        setup_a(m + 1, nxt, grows);
+      }
+      const bool more = u + 1 < u_end;
+      const int n_next = (u + 1) % a.n_tiles;
+      const int c0 = n * kNT + hl * a.D;               // first KV_hat column of the head
+      const bool is_k = c0 < a.dk;
+      // ---- mean of the references: wait for this unit's copy of reference t, read it,
+      // then reuse its slot for the next unit's copy
+      uint64_t mx2[8], my2[8];                          // packed fp32 pairs
 #pragma unroll
-        for (int i = 0; i < 4; ++i) cw[i] = make_uint4(0u, 0u, 0u, 0u);
-        const uint8_t* crow = a.codes + dst * a.code_bytes;
-        if (in_range) {
+      for (int i = 0; i < 8; ++i) mx2[i] = 0ull, my2[i] = 0ull;
 #pragma unroll
-          for (int t = 0; t < 4; ++t)
-            if (t < a.topk) sl[t] = a.ref_idx[dst * a.topk + t];
-          if (a.bits != 16) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              if (i < g_per) {
-                const int g = g0 + i;
-                mt[i] = a.meta[dst * a.G + g];
-                if (a.bits == 4) {
-                  cw[i] = *reinterpret_cast<const uint4*>(crow + (int64_t)g * 16);
-                } else {
-                  const uint2 v = *reinterpret_cast<const uint2*>(crow + (int64_t)g * 8);
-                  cw[i] = make_uint4(v.x, v.y, 0u, 0u);
-                }
-              }
-            }
-          }
-        }
-        // the next tile's row metadata, for the next tile change
-        have_next = false;
-        {
-          const int u_next = (m + 1) * a.n_tiles;
-          if (u_next < u_end) {
-            const int64_t gn = (int64_t)(m + 1) * kTileM + row;
-            next_m = m + 1;
-            next_s = gn < a.n_sel ? a.seq[gn] : -1;
-            next_p = gn < a.n_sel ? a.pos[gn] : -1;
-            have_next = true;
-          }
-        }
-        if (in_range) {
-          if (sl[0] < 0 && wg == 0) atomicOr(a.status, RKV_FLAG_UNWRITTEN);
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            if (sl[t] >= a.R_cap && wg == 0) atomicOr(a.status, RKV_FLAG_BAD_SLOT);
-            if (sl[t] >= 0 && sl[t] < a.R_cap) {
-              const int32_t q = s_ * a.R_cap + sl[t];
-              if (k_i == 0) rrow[0] = q;
-              else if (k_i == 1) rrow[1] = q;
-              else if (k_i == 2) rrow[2] = q;
-              else rrow[3] = q;
-              ++k_i;
-            }
-          }
-          valid = (sl[0] >= 0 && sl[0] < a.R_cap) && k_i > 0;
-        }
-        // ---- dequantise this row's share of code groups into the swizzled A tile
-        if (a.bits == 16) {
-          for (int g = g0; g < g0 + g_per; ++g) {
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              const int ch = g * 4 + q;
-              const uint4 v = valid ? reinterpret_cast<const uint4*>(crow + (int64_t)g * 64)[q]
-                                    : make_uint4(0u, 0u, 0u, 0u);
-              *reinterpret_cast<uint4*>(sA + (ch >> 3) * kTileABytes + sw128_offset(row, ch & 7)) = v;
-            }
-          }
-        } else {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            if (i >= g_per) break;
-            const int g = g0 + i;
-            const float lo = __half2float(__ushort_as_half((unsigned short)(mt[i] & 0xFFFFu)));
-            const float hi = __half2float(__ushort_as_half((unsigned short)(mt[i] >> 16)));
-            const float delta = __fdiv_rn(__fsub_rn(hi, lo), (float)levels);
-            const uint32_t w4[4] = {cw[i].x, cw[i].y, cw[i].z, cw[i].w};
-            // group g = coordinates [32g, 32g+32) = four 16-byte chunks of 8 values
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-              uint32_t o[4];
-#pragma unroll
-              for (int e = 0; e < 4; ++e) {
-                const int k = 8 * q + 2 * e;           // first of two coordinates
-                uint32_t q0, q1;
-                if (a.bits == 4) {
-                  q0 = (w4[k >> 3] >> (4 * (k & 7))) & 15u;
-                  q1 = (w4[k >> 3] >> (4 * (k & 7) + 4)) & 15u;
-                } else {
-                  q0 = (w4[k >> 4] >> (2 * (k & 15))) & 3u;
-                  q1 = (w4[k >> 4] >> (2 * (k & 15) + 2)) & 3u;
-                }
-                o[e] = valid ? pack_bf16x2(__fadd_rn(__fmul_rn((float)q0, delta), lo),
-                                           __fadd_rn(__fmul_rn((float)q1, delta), lo))
-                             : 0u;
-              }
-              const int ch = g * 4 + q;
-              *reinterpret_cast<uint4*>(sA + (ch >> 3) * kTileABytes + sw128_offset(row, ch & 7)) =
-                  make_uint4(o[0], o[1], o[2], o[3]);
-            }
-          }
-        }
-        // A is ready for the tensor core (each thread publishes its shared-memory writes
-        // to the async proxy; one lane per warp arrives); the RoPE cache below is only
-        // needed later
-        fence_proxy_async_smem();
+      for (int t = 0; t < 4; ++t) {
+        cp_async_wait<3>();
         __syncwarp();
-        if (lane_id() == 0) mbar_arrive(afull);
-        // ---- cos/sin of the group's 32 pairs at the row's own position, into TMEM
-        {
-          const float4* th = reinterpret_cast<const float4*>(a.rope_hi + (int64_t)(my_pos >> 9) * P + jbase);
-          const float4* tl = reinterpret_cast<const float4*>(a.rope_lo + (int64_t)(my_pos & (kRopeLo - 1)) * P + jbase);
-#pragma unroll 1
-          for (int hb = 0; hb < 4; ++hb) {             // 8 pairs at a time
-            float4 hv[4], lv[4];
+        if ((cur.vmask >> t) & 1) {
+          const uint4 rx = *reinterpret_cast<const uint4*>(slots + ((t * 2) * kTileM + row) * 16);
+          const uint4 ry = *reinterpret_cast<const uint4*>(slots + ((t * 2 + 1) * kTileM + row) * 16);
+          fp8x16_add2(rx, mx2);
+          fp8x16_add2(ry, my2);
+        }
+        __syncwarp();
+        issue_ref(grows, n_next, more && t < a.topk, t);
+      }
+      float mx[16], my[16];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) hv[i] = __ldg(th + 4 * hb + i), lv[i] = __ldg(tl + 4 * hb + i);
-            uint32_t cs[16];
+      for (int i = 0; i < 8; ++i) {
+        f32x2_unpack(mx2[i], mx[2 * i], mx[2 * i + 1]);
+        f32x2_unpack(my2[i], my[2 * i], my[2 * i + 1]);
+      }
+      if (cur.valid) {
+        if (cur.kcnt == 3) {
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
+          for (int i = 0; i < 16; ++i) mx[i] = __fdiv_rn(mx[i], 3.0f), my[i] = __fdiv_rn(my[i], 3.0f);
+        } else {
+          const float kinv = 1.0f / (float)cur.kcnt;   // exact for k_i = 1, 2, 4
 #pragma unroll
-              for (int e = 0; e < 2; ++e) {
-                const float hc = e ? hv[i].z : hv[i].x, hs = e ? hv[i].w : hv[i].y;
-                const float lc = e ? lv[i].z : lv[i].x, ls = e ? lv[i].w : lv[i].y;
-                cs[4 * i + 2 * e] = __float_as_uint(hc * lc - hs * ls);       // cos(A + B)
-                cs[4 * i + 2 * e + 1] = __float_as_uint(hs * lc + hc * ls);   // sin(A + B)
-              }
-            }
-            tmem_st16(tmem + lane_base + rope_col + 16u * hb, cs);
-          }
-          tmem_st_wait();
+          for (int i = 0; i < 16; ++i) mx[i] = __fmul_rn(mx[i], kinv), my[i] = __fmul_rn(my[i], kinv);
         }
       }
-      if (((u - u_begin) & 1) != pr) continue;         // the other pair's unit
-      // ---- this group's 32 pairs of the unit, 16 at a time
-      bool have_acc = false;
-      const uint32_t tacc = tmem + lane_base + (uint32_t)(pr * kNT);
-#pragma unroll 1
-      for (int c = 0; c < 2; ++c) {
-        const int slot = 32 * hw + 16 * c;             // pair slot within the unit
-        const int hl = slot / P, j0 = slot % P;        // head within the unit, first pair
-        const int xcol = hl * a.D + j0, ycol = xcol + P;
-        const int c0 = n * kNT + hl * a.D;             // first KV_hat column of the head
-        const bool is_k = c0 < a.dk;
-        // mean of the references first (no TMEM dependency)
-        uint64_t mx2[8], my2[8];                        // packed fp32 pairs
+      // ---- accumulator row
+      if (!warp_wait(&tfull[acc], acc_phase, abort_flag, a.status)) break;
+      tc_fence_after();
+      {
+        const uint32_t tacc = tmem + lane_base + (uint32_t)(acc * kNT);
+        uint32_t xr[16], yr[16];
+        tmem_ld16(tacc + xcol, xr);
+        tmem_ld16(tacc + ycol, yr);
+        tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 8; ++i) mx2[i] = 0ull, my2[i] = 0ull;
-        if (valid) {
-#pragma unroll
-          for (int t = 0; t < 4; ++t) {
-            if (t < k_i) {
-              const uint8_t* rp = a.pool8 + (int64_t)rrow[t] * a.dkv + c0 + j0;
-              const uint4 rx = __ldg(reinterpret_cast<const uint4*>(rp));
-              const uint4 ry = __ldg(reinterpret_cast<const uint4*>(rp + P));
-              fp8x16_add2(rx, mx2);
-              fp8x16_add2(ry, my2);
-            }
-          }
-        }
-        float mx[16], my[16];
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-          f32x2_unpack(mx2[i], mx[2 * i], mx[2 * i + 1]);
-          f32x2_unpack(my2[i], my[2 * i], my[2 * i + 1]);
-        }
-        if (valid) {
-          if (k_i == 3) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) mx[i] = __fdiv_rn(mx[i], 3.0f), my[i] = __fdiv_rn(my[i], 3.0f);
-          } else {
-            const float kinv = 1.0f / (float)k_i;     // exact for k_i = 1, 2, 4
-#pragma unroll
-            for (int i = 0; i < 16; ++i) mx[i] = __fmul_rn(mx[i], kinv), my[i] = __fmul_rn(my[i], kinv);
-          }
-        }
-        if (!have_acc) {
-          if (!warp_wait(&tfull[pr], acc_phase, abort_flag, a.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          have_acc = true;
-        }
-        {
-          uint32_t xr[16], yr[16];
-          tmem_ld16(tacc + xcol, xr);
-          tmem_ld16(tacc + ycol, yr);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            mx[i] = __fadd_rn(__uint_as_float(xr[i]), mx[i]);
-            my[i] = __fadd_rn(__uint_as_float(yr[i]), my[i]);
-          }
-        }
-        if (is_k) {
-          uint32_t cs[32];
-          tmem_ld32(tmem + lane_base + rope_col + 32u * c, cs);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            const float cc = __uint_as_float(cs[2 * i]), sn = __uint_as_float(cs[2 * i + 1]);
-            const float xv = mx[i], yv = my[i];
-            mx[i] = xv * cc - yv * sn;
-            my[i] = yv * cc + xv * sn;
-          }
-        }
-        if (!valid) {
-#pragma unroll
-          for (int i = 0; i < 16; ++i) mx[i] = 0.f, my[i] = 0.f;
-        }
-        if (gi < a.n_sel) {
-          void* out = is_k ? a.k_out : a.v_out;
-          const int64_t rowoff = gi * (int64_t)a.dk + (is_k ? c0 : c0 - a.dk) + j0;
-          if (a.out_f32) {
-            float* o = static_cast<float*>(out) + rowoff;
-            st_global_v8(o, reinterpret_cast<const uint32_t*>(mx));
-            st_global_v8(o + 8, reinterpret_cast<const uint32_t*>(mx + 8));
-            st_global_v8(o + P, reinterpret_cast<const uint32_t*>(my));
-            st_global_v8(o + P + 8, reinterpret_cast<const uint32_t*>(my + 8));
-          } else {
-            uint32_t wx[8], wy[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              wx[i] = pack_bf16x2(mx[2 * i], mx[2 * i + 1]);
-              wy[i] = pack_bf16x2(my[2 * i], my[2 * i + 1]);
-            }
-            __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out) + rowoff;
-            st_global_v8(o, wx);                        // 16 bf16 = one 32-byte sector
-            st_global_v8(o + P, wy);
-          }
+        for (int i = 0; i < 16; ++i) {
+          mx[i] = __fadd_rn(__uint_as_float(xr[i]), mx[i]);
+          my[i] = __fadd_rn(__uint_as_float(yr[i]), my[i]);
         }
       }
-      if (!ok) break;
+      // the accumulator is free as soon as it has been read
       tc_fence_before();
       __syncwarp();
-      if (lane_id() == 0) mbar_arrive(&tempty[pr]);
-      acc_phase ^= 1u;
+      if (lane_id() == 0) mbar_arrive(&tempty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1u;
+      }
+      if (is_k) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float4 cs = cs_row[i * kTileM];
+          const float x0 = mx[2 * i], y0 = my[2 * i], x1 = mx[2 * i + 1], y1 = my[2 * i + 1];
+          mx[2 * i] = x0 * cs.x - y0 * cs.y;
+          my[2 * i] = y0 * cs.x + x0 * cs.y;
+          mx[2 * i + 1] = x1 * cs.z - y1 * cs.w;
+          my[2 * i + 1] = y1 * cs.z + x1 * cs.w;
+        }
+      }
+      if (!cur.valid) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) mx[i] = 0.f, my[i] = 0.f;
+      }
+      if (cur.in_sel) {
+        const int64_t gi = (int64_t)m * kTileM + row;
+        void* out = is_k ? a.k_out : a.v_out;
+        const int64_t rowoff = gi * (int64_t)a.dk + (is_k ? c0 : c0 - a.dk) + j0;
+        if (a.out_f32) {
+          float* o = static_cast<float*>(out) + rowoff;
+          st_global_v8(o, reinterpret_cast<const uint32_t*>(mx));
+          st_global_v8(o + 8, reinterpret_cast<const uint32_t*>(mx + 8));
+          st_global_v8(o + P, reinterpret_cast<const uint32_t*>(my));
+          st_global_v8(o + P + 8, reinterpret_cast<const uint32_t*>(my + 8));
+        } else {
+          uint32_t wx[8], wy[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            wx[i] = pack_bf16x2(mx[2 * i], mx[2 * i + 1]);
+            wy[i] = pack_bf16x2(my[2 * i], my[2 * i + 1]);
+          }
+          __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out) + rowoff;
+          st_global_v8(o, wx);                          // 16 bf16 = one 32-byte sector
+          st_global_v8(o + P, wy);
+        }
+      }
     }
+    cp_async_wait<0>();                                // no copy may outlive the CTA
   }
 
   tc_fence_before();
@@ -518,11 +557,11 @@ cudaError_t launch_reconstruct(rkv_ctx* c, const int32_t* seq, const int32_t* po
                                void* k_out, void* v_out, cudaStream_t s) {
   const Dims& d = c->d;
   if (n_sel <= 0) return cudaSuccess;
-  const size_t fixed = 1024 + (size_t)(d.dc / kTileK) * kTileABytes + 256;
-  int stages = (int)((232448 - fixed) / kBBytes);
-  if (stages > kMaxStages) stages = kMaxStages;
-  if (stages < 2) return cudaErrorInvalidConfiguration;
-  const size_t smem = fixed + (size_t)stages * kBBytes;
+  const size_t fixed = 1024 + kCSBytes + kGBytes + kBarBytes;
+  int b_stages = (int)((232448 - fixed) / kBBytes);
+  if (b_stages > kMaxStages) b_stages = kMaxStages;
+  if (b_stages < 2) return cudaErrorInvalidConfiguration;
+  const size_t smem = fixed + (size_t)b_stages * kBBytes;
   cudaError_t e = cudaFuncSetAttribute(reconstruct_kernel,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -533,7 +572,7 @@ cudaError_t launch_reconstruct(rkv_ctx* c, const int32_t* seq, const int32_t* po
   a.n_tiles = d.dkv / kNT;
   const int m_tiles = (n_sel + kTileM - 1) / kTileM;
   a.units = m_tiles * a.n_tiles;
-  a.stages = stages;
+  a.b_stages = b_stages;
   a.codes = static_cast<const uint8_t*>(c->st.codes);
   a.meta = static_cast<const uint32_t*>(c->st.meta);
   a.ref_idx = c->st.ref_idx;

@@ -90,7 +90,8 @@ rkv_status derive(const rkv_config* c, Dims* d) {
   if (d->N <= 0 || !(d->D == 64 || d->D == 128))
     return fail(RKV_EINVAL, "head_dim must be 64 or 128 and n_kv_heads > 0");
   if (d->dkv % 256 != 0) return fail(RKV_EINVAL, "2*N*D must be a multiple of 256");
-  if (d->dc <= 0 || d->dc % 64 != 0) return fail(RKV_EINVAL, "d_c must be a positive multiple of 64");
+  if (d->dc <= 0 || d->dc % 64 != 0 || d->dc > 512)
+    return fail(RKV_EINVAL, "d_c must be a positive multiple of 64, at most 512");
   if (d->dff <= 0 || d->dff % 128 != 0) return fail(RKV_EINVAL, "d_ff must be a positive multiple of 128");
   if (d->topk < 1 || d->topk > 4) return fail(RKV_EINVAL, "topk must be in 1..4");
   if (d->group != 32) return fail(RKV_EINVAL, "group must be 32");

@@ -43,7 +43,7 @@ def test_storage_bytes_and_config_validation(built):
     s = rkv.storage_bytes(cfg)
     assert s[0] == 2048 * 2048 and s[1] == 2048 * 2048 * 2
     assert s[4] == 32768 * 256 and s[5] == 32768 * 16 * 4 and s[6] == 32768 * 4 * 4
-    for bad in (dict(head_dim=96), dict(d_c=100), dict(bits=3), dict(topk=5), dict(d_ff=200),
+    for bad in (dict(head_dim=96), dict(d_c=100), dict(d_c=576), dict(bits=3), dict(topk=5), dict(d_ff=200),
                 dict(group=16), dict(max_refs=10)):
         with pytest.raises(rkv.RkvError) as e:
             rkv.storage_bytes(rkv.Config(**{**cfg.__dict__, **bad}))
