@@ -20,6 +20,12 @@
 // epilogue thread then sums its row's references (exact in fp32), divides by k_i, adds
 // its accumulator row, rotates the K columns and stores K or V in whole 32-byte sectors.
 //
+// Back-to-back launches overlap: every CTA lets the next launch of the stream start its
+// CTAs as SMs free up, and a thread waits for the previous grid to complete only before
+// its first output store, so one launch's setup (dependent loads of selections, slots
+// and codes, dequantisation) hides behind the previous launch's last CTAs.  Nothing else
+// this kernel reads is written by it.
+//
 // The kernel is bound by the bytes each SM pulls from L2 per unit (128 KB of W_d^T plus
 // 64 KB of reference rows), not by the tensor core.
 #include <cuda_bf16.h>
@@ -118,6 +124,7 @@ __global__ void __launch_bounds__(kReconThreads, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
+  pdl_launch_dependents();
   const int u_begin = (int)(((int64_t)blockIdx.x * a.units) / gridDim.x);
   const int u_end = (int)(((int64_t)(blockIdx.x + 1) * a.units) / gridDim.x);
 
@@ -416,6 +423,7 @@ __global__ void __launch_bounds__(kReconThreads, 1)
 
     RowState cur, nxt;
     GatherRows grows;                                  // rows of the tile of the next copies
+    bool waited = false;                               // previous grid complete (first store)
     int acc = 0;
     uint32_t acc_phase = 0, afree_phase = 0;
     int cur_m = -1;
@@ -518,6 +526,10 @@ __global__ void __launch_bounds__(kReconThreads, 1)
         for (int i = 0; i < 16; ++i) mx[i] = 0.f, my[i] = 0.f;
       }
       if (cur.in_sel) {
+        if (!waited) {
+          pdl_wait_previous_grid();                    // K/V may be the previous launch's outputs
+          waited = true;
+        }
         const int64_t gi = (int64_t)m * kTileM + row;
         void* out = is_k ? a.k_out : a.v_out;
         const int64_t rowoff = gi * (int64_t)a.dk + (is_k ? c0 : c0 - a.dk) + j0;
@@ -597,8 +609,18 @@ cudaError_t launch_reconstruct(rkv_ctx* c, const int32_t* seq, const int32_t* po
   const int grid = a.units < c->num_sms ? a.units : c->num_sms;
   cudaEvent_t ev;
   timing_begin(c, "rkv_reconstruct_kernel", s, &ev);
-  reconstruct_kernel<<<grid, kReconThreads, smem, s>>>(c->tm_wd, a);
-  e = cudaGetLastError();
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(grid);
+  lc.blockDim = dim3(kReconThreads);
+  lc.dynamicSmemBytes = smem;
+  lc.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  e = cudaLaunchKernelEx(&lc, reconstruct_kernel, c->tm_wd, a);
+  if (e == cudaSuccess) e = cudaGetLastError();
   timing_end(c, "rkv_reconstruct_kernel", s, ev);
   return e;
 }

@@ -138,6 +138,19 @@ namespace rkv {
 
 void set_error(const char* msg) { g_err = msg ? msg : ""; }
 
+bool make_out_map(CUtensorMap* m, void* base, int64_t cols, int64_t rows, bool f32) {
+  const uint32_t es = f32 ? 4u : 2u;
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * es};
+  cuuint32_t box[2] = {128u / es, (cuuint32_t)kTileM};
+  cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = g_encode(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                        2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 void timing_begin(rkv_ctx* c, const char* name, cudaStream_t s, cudaEvent_t* start) {
   c->launches++;
   *start = nullptr;
@@ -236,7 +249,7 @@ rkv_status rkv_create(const rkv_config* cfg, const void* Wc1, const void* Wc2, c
   ALLOC(c->part, (size_t)c->units_cap * kTileM * 4 * sizeof(int2));
   ALLOC(c->plan_dev[0], (size_t)c->plan_ints * 4);
   ALLOC(c->plan_dev[1], (size_t)c->plan_ints * 4);
-  ALLOC(c->status, 64);
+  ALLOC(c->status, 512);
 #undef ALLOC
   if (fail_status != RKV_OK) {
     rkv_free(c);
@@ -292,7 +305,8 @@ rkv_status rkv_create(const rkv_config* cfg, const void* Wc1, const void* Wc2, c
     return fail(RKV_ECUDA, "cuTensorMapEncodeTiled rejected a tensor map");
   }
 
-  cudaError_t e = cudaMemsetAsync(c->status, 0, 64, s);
+  c->zero_line = reinterpret_cast<const uint8_t*>(c->status) + 256;
+  cudaError_t e = cudaMemsetAsync(c->status, 0, 512, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(c->Q, 0, (size_t)c->m_cap * d.parts * d.dkv * 2, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(c->X, 0, (size_t)2 * c->max_rows * d.dkv * 2, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(c->H, 0, (size_t)2 * c->max_rows * d.dff * 2, s);

@@ -78,7 +78,8 @@ struct rkv_ctx {
   cudaEvent_t plan_copied[2] = {nullptr, nullptr};
   int plan_ints = 0;
   int plan_flip = 0;
-  int* status = nullptr;          // device status word
+  int* status = nullptr;          // device status word (first 64 bytes of a 512-byte block)
+  const uint8_t* zero_line = nullptr;   // 256 zero bytes in the same block (gather source)
 
   // TMA descriptors (fixed addresses, built once)
   CUtensorMap tm_q, tm_pool, tm_x, tm_w12, tm_h3, tm_w3, tm_w3_128, tm_wd;
@@ -113,6 +114,10 @@ cudaError_t launch_gemm3_quant(rkv_ctx* c, const PassPlan& p, const int32_t* pla
                                cudaStream_t s);
 cudaError_t launch_reconstruct(rkv_ctx* c, const int32_t* seq, const int32_t* pos, int n_sel,
                                void* k_out, void* v_out, cudaStream_t s);
+
+// Tensor map of a row-major [rows, cols] output matrix (bf16 or fp32) for 2-D tiled
+// stores: box = {128 bytes of columns, 128 rows}, 128-byte swizzle.
+bool make_out_map(CUtensorMap* m, void* base, int64_t cols, int64_t rows, bool f32);
 
 // Record the message rkv_last_error returns on this thread.
 void set_error(const char* msg);
