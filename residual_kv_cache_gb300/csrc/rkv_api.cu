@@ -390,86 +390,87 @@ rkv_status rkv_compress(rkv_ctx* c, const void* kv, int64_t kv_row_stride, const
     if (src < 0) return fail(RKV_EINVAL, "row %d: negative source row", i);
     if (p % d.stride == 0) return fail(RKV_EINVAL, "row %d: pos %d is a reference position", i, p);
     if (c->pool_count[s] == 0) return fail(RKV_EEMPTYPOOL, "row %d: seq %d has no reference", i, s);
-    if (visible_refs(p, d.stride) > c->pool_count[s])
+    // the references before p are the ceil(p / s) positions 0, s, 2s, ... < p
+    if ((int64_t)p > (int64_t)c->pool_count[s] * d.stride)
       return fail(RKV_EINVAL, "row %d: references of seq %d before pos %d are not all appended", i,
                   s, p);
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  std::vector<int> order;
+  std::vector<int> order, gbeg;
+  std::vector<int32_t> tseq, trow0, tnrt;
   for (int r0 = 0; r0 < n; r0 += c->max_rows) {
     const int m = std::min(c->max_rows, n - r0);
-    // ---- plan: rows grouped by sequence (stable), each group padded to 128 rows
+    // ---- plan: rows grouped by sequence (stable), each group padded to 128 rows.  A
+    // counting sort by sequence id (O(m + B)); nothing to do when the ids never decrease.
     order.resize(m);
-    for (int i = 0; i < m; ++i) order[i] = r0 + i;
-    std::stable_sort(order.begin(), order.end(), [&](int a, int b) { return seq[a] < seq[b]; });
-    PassPlan p;
-    p.n_rows = m;
+    bool grouped = true;
+    for (int i = 1; i < m && grouped; ++i) grouped = seq[r0 + i] >= seq[r0 + i - 1];
+    if (grouped) {
+      for (int i = 0; i < m; ++i) order[i] = r0 + i;
+    } else {
+      std::vector<int> start(d.B + 1, 0);
+      for (int i = 0; i < m; ++i) ++start[seq[r0 + i] + 1];
+      for (int b2 = 0; b2 < d.B; ++b2) start[b2 + 1] += start[b2];
+      for (int i = 0; i < m; ++i) order[start[seq[r0 + i]]++] = r0 + i;
+    }
+    // group boundaries in `order`, padded sizes
+    gbeg.clear();
     int m_pad = 0, ntiles = 0;
     for (int i = 0; i < m;) {
-      int j = i;
+      int j = i + 1;
       while (j < m && seq[order[j]] == seq[order[i]]) ++j;
-      const int cnt = j - i;
-      const int padded = (cnt + kTileM - 1) / kTileM * kTileM;
+      gbeg.push_back(i);
+      const int padded = (j - i + kTileM - 1) / kTileM * kTileM;
       m_pad += padded;
       ntiles += padded / kTileM;
       i = j;
     }
+    gbeg.push_back(m);
+    // plan layout: per-row arrays first, then tiles, then units (counted while filling)
+    PassPlan p;
+    p.n_rows = m;
     p.m_pad = m_pad;
     p.n_tiles = ntiles;
-    // units: every (tile, pool tile) of the causal prefix; counted below
-    int n_units = 0;
-    for (int i = 0; i < m;) {
-      int j = i;
-      while (j < m && seq[order[j]] == seq[order[i]]) ++j;
-      for (int k = i; k < j; k += kTileM) {
-        int maxvis = 1;
-        for (int r = k; r < std::min(j, k + kTileM); ++r)
-          maxvis = std::max(maxvis, visible_refs(pos[order[r]], d.stride));
-        n_units += (maxvis + kRefTile - 1) / kRefTile;
-      }
-      i = j;
-    }
-    p.n_units = n_units;
     p.off_q_src = 0;
     p.off_q_pos = m_pad;
     p.off_q_dst = 2 * m_pad;
-    p.off_t_seq = 3 * m_pad;
+    p.off_c_q = 3 * m_pad;
+    p.off_c_dst = p.off_c_q + m;
+    p.off_t_seq = p.off_c_dst + m;
     p.off_t_row0 = p.off_t_seq + ntiles;
     p.off_t_nrt = p.off_t_row0 + ntiles;
     p.off_t_u0 = p.off_t_nrt + ntiles;
     p.off_u_tile = p.off_t_u0 + ntiles;
-    p.off_u_rt = p.off_u_tile + n_units;
-    p.off_c_q = p.off_u_rt + n_units;
-    p.off_c_dst = p.off_c_q + m;
-    p.total_ints = p.off_c_dst + m;
-    if (n_units > c->units_cap)
-      return fail(RKV_ECAPACITY, "compress pass exceeds the planned retrieval scratch");
-    if (m_pad > c->m_cap || p.total_ints > c->plan_ints)
+    if (m_pad > c->m_cap || p.off_u_tile > c->plan_ints)
       return fail(RKV_ECAPACITY, "compress pass exceeds the planned scratch");
     int b;
     int32_t* h = staging_acquire(c, &b);
-    int q = 0;
-    std::vector<int32_t> tseq, trow0, tnrt;
-    for (int i = 0; i < m;) {
-      int j = i;
+    tseq.clear();
+    trow0.clear();
+    tnrt.clear();
+    int q = 0, n_units = 0;
+    for (size_t g = 0; g + 1 < gbeg.size(); ++g) {
+      const int i = gbeg[g], j = gbeg[g + 1];
       const int s = seq[order[i]];
-      while (j < m && seq[order[j]] == s) ++j;
       for (int k = i; k < j; k += kTileM) {
-        int maxvis = 1;
-        for (int r = k; r < std::min(j, k + kTileM); ++r)
-          maxvis = std::max(maxvis, visible_refs(pos[order[r]], d.stride));
+        const int kend = std::min(j, k + kTileM);
+        int maxpos = 1;
+        for (int r = k; r < kend; ++r) {
+          const int row = order[r];
+          const int qr = q + (r - i);
+          const int pr = pos[row];
+          maxpos = std::max(maxpos, pr);
+          h[p.off_q_src + qr] = src_rows ? src_rows[row] : row;
+          h[p.off_q_pos + qr] = pr;
+          h[p.off_q_dst + qr] = s * d.T_cap + pr;
+          h[p.off_c_q + (row - r0)] = qr;
+          h[p.off_c_dst + (row - r0)] = s * d.T_cap + pr;
+        }
+        const int nrt = (visible_refs(maxpos, d.stride) + kRefTile - 1) / kRefTile;
         tseq.push_back(s);
         trow0.push_back(q + (k - i));
-        tnrt.push_back((maxvis + kRefTile - 1) / kRefTile);
-      }
-      for (int k = i; k < j; ++k) {
-        const int row = order[k];
-        const int qr = q + (k - i);
-        h[p.off_q_src + qr] = src_rows ? src_rows[row] : row;
-        h[p.off_q_pos + qr] = pos[row];
-        h[p.off_q_dst + qr] = seq[row] * d.T_cap + pos[row];
-        h[p.off_c_q + (row - r0)] = qr;
-        h[p.off_c_dst + (row - r0)] = seq[row] * d.T_cap + pos[row];
+        tnrt.push_back(nrt);
+        n_units += nrt;
       }
       const int padded = (j - i + kTileM - 1) / kTileM * kTileM;
       for (int k = j - i; k < padded; ++k) {
@@ -478,8 +479,12 @@ rkv_status rkv_compress(rkv_ctx* c, const void* kv, int64_t kv_row_stride, const
         h[p.off_q_dst + q + k] = -1;
       }
       q += padded;
-      i = j;
     }
+    p.n_units = n_units;
+    p.off_u_rt = p.off_u_tile + n_units;
+    p.total_ints = p.off_u_rt + n_units;
+    if (n_units > c->units_cap || p.total_ints > c->plan_ints)
+      return fail(RKV_ECAPACITY, "compress pass exceeds the planned retrieval scratch");
     // tiles in order; units tile-major, pool tiles in increasing slot order
     int u = 0;
     for (int i = 0; i < ntiles; ++i) {
