@@ -264,6 +264,16 @@ int64_t rkv_launch_count(rkv_ctx* ctx);
  */
 rkv_status rkv_debug_scratch(rkv_ctx* ctx, int32_t which, void** ptr, size_t* bytes);
 
+/*
+ * Test hook for failure detection: launches one block that waits on an
+ * mbarrier nothing ever arrives at.  The wait is bounded like every pipeline
+ * wait in this library; after about a second it sets RKV_FLAG_TIMEOUT in the
+ * device status word and the kernel returns.  No fault, no hang: the context
+ * stays usable.  rkv_get_status then reports RKV_ETIMEOUT.  The page has no
+ * counterpart.
+ */
+rkv_status rkv_debug_timeout_probe(rkv_ctx* ctx, void* stream);
+
 #ifdef __cplusplus
 }
 #endif

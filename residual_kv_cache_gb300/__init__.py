@@ -75,6 +75,7 @@ ABI_FUNCTIONS = {
     "rkv_get_timing": (_I32, [_P, ctypes.POINTER(_Timing), _I32, _I32]),
     "rkv_launch_count": (_I64, [_P]),
     "rkv_debug_scratch": (_I32, [_P, _I32, ctypes.POINTER(_P), ctypes.POINTER(ctypes.c_size_t)]),
+    "rkv_debug_timeout_probe": (_I32, [_P, _P]),
     "rkv_retrieve_noalloc": (_I32, [_P, _P, _I32, _P, _P, _P, _I32, _I32, _I32, _P, _P, _P]),
 }
 
@@ -279,6 +280,10 @@ class Codec:
         p, b = ctypes.c_void_p(), ctypes.c_size_t()
         _check(lib().rkv_debug_scratch(self._ctx, which, ctypes.byref(p), ctypes.byref(b)))
         return p.value, b.value
+
+    def debug_timeout_probe(self, stream=None):
+        """Launch one block whose bounded wait must expire (failure-detection test)."""
+        _check(lib().rkv_debug_timeout_probe(self._ctx, _stream_ptr(stream)))
 
     def free(self):
         if getattr(self, "_ctx", None):

@@ -8,6 +8,7 @@
 
 #include <climits>
 
+#include "ptx.cuh"
 #include "rkv_internal.h"
 
 namespace rkv {
@@ -303,6 +304,27 @@ cudaError_t launch_mean_rows(rkv_ctx* c, const PassPlan& p, const int32_t* plan,
   cudaError_t e = cudaGetLastError();
   timing_end(c, "rkv_mean_rows_kernel", s, ev);
   return e;
+}
+
+// One block whose wait is never satisfied: the same bounded mbarrier wait as every
+// pipeline here, so it must expire (about a second), raise RKV_FLAG_TIMEOUT and return.
+// Exercises the failure-detection path without faulting or hanging the GPU.
+__global__ void timeout_probe_kernel(int* status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    abort_flag = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) (void)mbar_wait(&bar, 0, &abort_flag, status);  // nothing arrives
+  __syncthreads();
+}
+
+cudaError_t launch_timeout_probe(rkv_ctx* c, cudaStream_t s) {
+  timeout_probe_kernel<<<1, 32, 0, s>>>(c->status);
+  return cudaGetLastError();
 }
 
 }  // namespace rkv

@@ -601,6 +601,12 @@ int32_t rkv_get_timing(rkv_ctx* c, rkv_kernel_timing* out, int32_t max_entries, 
 
 int64_t rkv_launch_count(rkv_ctx* c) { return c ? c->launches : 0; }
 
+rkv_status rkv_debug_timeout_probe(rkv_ctx* c, void* stream) {
+  if (!c) return fail(RKV_EINVAL, "ctx is NULL");
+  CUDA_OK(launch_timeout_probe(c, static_cast<cudaStream_t>(stream)));
+  return RKV_OK;
+}
+
 rkv_status rkv_debug_scratch(rkv_ctx* c, int32_t which, void** ptr, size_t* bytes) {
   if (!c || !ptr || !bytes) return fail(RKV_EINVAL, "NULL argument");
   if (which == 0) {

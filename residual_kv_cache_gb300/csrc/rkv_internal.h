@@ -115,6 +115,8 @@ cudaError_t launch_gemm3_quant(rkv_ctx* c, const PassPlan& p, const int32_t* pla
 cudaError_t launch_reconstruct(rkv_ctx* c, const int32_t* seq, const int32_t* pos, int n_sel,
                                void* k_out, void* v_out, cudaStream_t s);
 
+cudaError_t launch_timeout_probe(rkv_ctx* c, cudaStream_t s);
+
 // Tensor map of a row-major [rows, cols] output matrix (bf16 or fp32) for 2-D tiled
 // stores: box = {128 bytes of columns, 128 rows}, 128-byte swizzle.
 bool make_out_map(CUtensorMap* m, void* base, int64_t cols, int64_t rows, bool f32);

@@ -262,6 +262,32 @@ def test_device_errors_flag_and_zero_rows():
 
 
 @cuda
+def test_wait_timeout_is_reported_and_context_survives():
+    """Failure detection without a fault: a wait nothing satisfies expires (~1 s), the
+    status word says so, and the same context restores tokens correctly afterwards."""
+    w = synth.workload("tiny")
+    kv = synth.gen_kv(w, 61)
+    W = synth.gen_weights(w, 62)
+    c = make_codec(w, W, T=w.T)
+    gpu_prefill(c, kv.cuda(), w.stride)
+    torch.cuda.synchronize()
+    assert c.get_status() == 0
+    sel = synth.gen_selection(w.T, w.n_sel, 63).cuda()
+    seq = torch.zeros_like(sel)
+    K0, V0 = c.reconstruct(seq, sel)
+    torch.cuda.synchronize()
+    c.debug_timeout_probe()
+    torch.cuda.synchronize()
+    from residual_kv_cache_gb300 import FLAG_TIMEOUT
+    flags = c.get_status()
+    assert flags == FLAG_TIMEOUT
+    K1, V1 = c.reconstruct(seq, sel)
+    torch.cuda.synchronize()
+    assert c.get_status() == 0
+    assert torch.equal(K0, K1) and torch.equal(V0, V1)
+
+
+@cuda
 def test_host_errors():
     from residual_kv_cache_gb300 import RkvError
     w = synth.workload("tiny")
