@@ -92,11 +92,6 @@ __device__ __forceinline__ void fp8x16_add2(uint4 v, uint64_t* s) {
   }
 }
 
-// Pool rows (or -1) of the references whose chunks one lane copies: [row half i][ref t].
-struct GatherRows {
-  int r[8];
-};
-
 // Correctly rounded s / 3 for every fp32 s that is a sum of at most three E4M3 values:
 // q = RN(s * RN(1/3)), r = s - 3 q (exact), RN(q + r * RN(1/3)).  Checked against the
 // exact quotient for all 256317 such sums.
@@ -107,17 +102,155 @@ __device__ __forceinline__ float div3_rn(float s) {
   return __fmaf_rn(r, c, q);
 }
 
-// Per-tile state of one epilogue thread's token row.
+// Per-tile state of one epilogue thread's token row, packed into two registers.
 struct RowState {
-  int valid;    // the row has a readable code and a first reference
-  int vmask;    // bit t: reference t is a valid slot
-  int kcnt;     // number of valid references (k_i)
-  int in_sel;   // the row is one of the n_sel selected tokens
+  int flags;    // bit 0: the row has a readable code and a first reference; bit 1: the
+                // row is one of the n_sel selected tokens; bits 2..5: reference t is a
+                // valid slot; bits 6..: k_i
   int pos;      // the token's position (RoPE)
+  __device__ __forceinline__ bool valid() const { return flags & 1; }
+  __device__ __forceinline__ bool in_sel() const { return (flags >> 1) & 1; }
+  __device__ __forceinline__ bool has_ref(int t) const { return (flags >> (2 + t)) & 1; }
+  __device__ __forceinline__ int kcnt() const { return flags >> 6; }
 };
 
+// A row's state, the pool rows of its references 0..3 (-1 where there is none) and the
+// sequence and position of the same row of the next tile (-1 past the selection).
+struct TileRow {
+  RowState st;
+  int r[4];
+  int nx_s, nx_p;
+};
+
+// The row `row` of token tile m, whose sequence and position s_, p_ the caller has
+// already loaded: its metadata and references, and its share of code groups
+// [g0, g0 + g_per) dequantised (z~ = q * Delta + min in fp32, bf16 into TMEM at
+// zaddr + 16 g; zeros for an invalid row).  Raises the device flags for bad selections.
+// With `next`, also loads the next tile's sequence and position of the row, so that the
+// next call starts with independent loads.
+__device__ __forceinline__ TileRow tile_setup(const ReconArgs& a, int m, int row, int wg,
+                                              int g0, int g_per, uint32_t zaddr, int s_,
+                                              int p_, bool next) {
+  TileRow tr;
+  RowState& st = tr.st;
+  const int64_t gi = (int64_t)m * kTileM + row;
+  const bool in_sel = gi < a.n_sel;
+  st.pos = 0;
+  bool in_range = false;
+  int64_t dst = 0;
+  if (in_sel) {
+    if (s_ < 0 || s_ >= a.B || p_ < 0 || p_ >= a.T_cap) {
+      if (wg == 0) atomicOr(a.status, RKV_FLAG_BAD_INDEX);
+    } else {
+      in_range = true;
+      dst = (int64_t)s_ * a.T_cap + p_;
+      st.pos = p_;
+    }
+  }
+  // one round trip: slots, extremes and codes together
+  int32_t sl[4] = {-1, -1, -1, -1};
+  uint32_t mt[4] = {0u, 0u, 0u, 0u};
+  uint4 cw[4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) cw[i] = make_uint4(0u, 0u, 0u, 0u);
+  const uint8_t* crow = a.codes + dst * a.code_bytes;
+  if (in_range) {
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+      if (t < a.topk) sl[t] = a.ref_idx[dst * a.topk + t];
+    if (a.bits != 16) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        if (i < g_per) {
+          const int g = g0 + i;
+          mt[i] = a.meta[dst * a.G + g];
+          if (a.bits == 4) {
+            cw[i] = *reinterpret_cast<const uint4*>(crow + (int64_t)g * 16);
+          } else {
+            const uint2 v = *reinterpret_cast<const uint2*>(crow + (int64_t)g * 8);
+            cw[i] = make_uint4(v.x, v.y, 0u, 0u);
+          }
+        }
+      }
+    }
+  }
+  {
+    const int64_t gn = gi + kTileM;
+    const bool nx = next && gn < a.n_sel;
+    tr.nx_s = nx ? a.seq[gn] : -1;
+    tr.nx_p = nx ? a.pos[gn] : -1;
+  }
+  int kcnt = 0;
+  bool valid = false;
+#pragma unroll
+  for (int t = 0; t < 4; ++t) tr.r[t] = -1;
+  if (in_range) {
+    if (sl[0] < 0 && wg == 0) atomicOr(a.status, RKV_FLAG_UNWRITTEN);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      if (sl[t] >= a.R_cap && wg == 0) atomicOr(a.status, RKV_FLAG_BAD_SLOT);
+      if (sl[t] >= 0 && sl[t] < a.R_cap) {
+        tr.r[t] = s_ * a.R_cap + sl[t];
+        ++kcnt;
+      }
+    }
+    valid = tr.r[0] >= 0 && kcnt > 0;
+  }
+  if (!valid) {
+    kcnt = 0;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) tr.r[t] = -1;
+  }
+  st.flags = (valid ? 1 : 0) | (in_sel ? 2 : 0) | (kcnt << 6);
+#pragma unroll
+  for (int t = 0; t < 4; ++t) st.flags |= (tr.r[t] >= 0 ? 1 : 0) << (2 + t);
+  // dequantise this row's share of code groups straight into TMEM
+  if (a.bits == 16) {
+    for (int g = g0; g < g0 + g_per; ++g) {
+      uint32_t o[16];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 v = valid ? reinterpret_cast<const uint4*>(crow + (int64_t)g * 64)[q]
+                              : make_uint4(0u, 0u, 0u, 0u);
+        o[4 * q] = v.x, o[4 * q + 1] = v.y, o[4 * q + 2] = v.z, o[4 * q + 3] = v.w;
+      }
+      tmem_st16(zaddr + 16u * (uint32_t)g, o);
+    }
+  } else {
+    const int levels = (1 << a.bits) - 1;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      if (i >= g_per) break;
+      const int g = g0 + i;
+      const float lo = __half2float(__ushort_as_half((unsigned short)(mt[i] & 0xFFFFu)));
+      const float hi = __half2float(__ushort_as_half((unsigned short)(mt[i] >> 16)));
+      const float delta = __fdiv_rn(__fsub_rn(hi, lo), (float)levels);
+      const uint32_t w4[4] = {cw[i].x, cw[i].y, cw[i].z, cw[i].w};
+      uint32_t o[16];
+#pragma unroll
+      for (int e = 0; e < 16; ++e) {
+        const int k = 2 * e;                           // first of two coordinates
+        uint32_t q0, q1;
+        if (a.bits == 4) {
+          q0 = (w4[k >> 3] >> (4 * (k & 7))) & 15u;
+          q1 = (w4[k >> 3] >> (4 * (k & 7) + 4)) & 15u;
+        } else {
+          q0 = (w4[k >> 4] >> (2 * (k & 15))) & 3u;
+          q1 = (w4[k >> 4] >> (2 * (k & 15) + 2)) & 3u;
+        }
+        o[e] = valid ? pack_bf16x2(__fadd_rn(__fmul_rn((float)q0, delta), lo),
+                                   __fadd_rn(__fmul_rn((float)q1, delta), lo))
+                     : 0u;
+      }
+      tmem_st16(zaddr + 16u * (uint32_t)g, o);
+    }
+  }
+  tmem_st_wait();
+  return tr;
+}
+
 __global__ void __launch_bounds__(kReconThreads, 1)
-    reconstruct_kernel(const __grid_constant__ CUtensorMap tmW, ReconArgs a) {
+    reconstruct_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ ReconArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int nkb = a.dc / kTileK;
@@ -249,152 +382,37 @@ __global__ void __launch_bounds__(kReconThreads, 1)
     const int wg = (warp - kEpiWarpR) >> 2;
     const int row = ew * 32 + (int)lane_id();        // TMEM lane = tile row
     const uint32_t lane_base = (uint32_t)(ew * 32) << 16;
-    const int levels = (1 << a.bits) - 1;
     const int P = a.D / 2;                           // pairs per head
     const int slot0 = 16 * wg;                       // first of this group's 16 pair slots
     const int hl = slot0 / P, j0 = slot0 % P;        // head within the unit, first pair
     const int xcol = hl * a.D + j0, ycol = xcol + P; // unit-local columns of x and y
-    // Reference slots of this group: plane (ref t, x|y) holds 16 bytes per tile row.
-    // Lane l copies, per reference, the x or y chunk (l & 1) of rows 32 ew + (l >> 1) and
-    // 32 ew + 16 + (l >> 1); lane l reads both chunks of its own row.
+    // Reference slots of this group: plane (ref t, x|y) holds 16 bytes per tile row.  Each
+    // thread copies and reads only its own row's two chunks, so no other thread is
+    // involved.
     uint8_t* slots = sG + (uint32_t)wg * (4 * 2 * kTileM * 16);
-    const int cp_row0 = ew * 32 + ((int)lane_id() >> 1);
-    const int cp_chunk = (lane_id() & 1) ? (ycol >> 4) : (xcol >> 4);
+    const uint8_t* xsrc0 = a.pool8 + xcol;             // + pool row * d_kv + unit column base
+    const uint8_t* ysrc0 = a.pool8 + ycol;
+    uint8_t* xdst0 = slots + (uint32_t)row * 16;
+    const uint32_t zaddr = tmem + lane_base + kACol;  // this thread's z~ columns
     const int g0 = wg * a.G / 4;                     // this group's code groups [g0, g0+g_per)
     const int g_per = (wg + 1) * a.G / 4 - g0;
     float4* cs_row = sCS + wg * 8 * kTileM + row;    // entry i at cs_row[i * kTileM]
 
-    int nx_m = -1, nx_s = -1, nx_p = -1;             // prefetched seq/pos of the next tile
-
     // z~ of tile m into TMEM (the caller has made sure the tensor core is done with the
     // previous tile), then one arrival per warp on afull.
-    auto setup_a = [&](int m, RowState& st, GatherRows& gr) {
-      const int64_t gi = (int64_t)m * kTileM + row;
-      int s_, p_;
-      if (nx_m == m) {
-        s_ = nx_s;
-        p_ = nx_p;
-      } else {
-        s_ = gi < a.n_sel ? a.seq[gi] : -1;
-        p_ = gi < a.n_sel ? a.pos[gi] : -1;
-      }
-      st.valid = 0;
-      st.vmask = 0;
-      st.kcnt = 0;
-      st.in_sel = gi < a.n_sel;
-      st.pos = 0;
-      bool in_range = false;
-      int64_t dst = 0;
-      if (st.in_sel) {
-        if (s_ < 0 || s_ >= a.B || p_ < 0 || p_ >= a.T_cap) {
-          if (wg == 0) atomicOr(a.status, RKV_FLAG_BAD_INDEX);
-        } else {
-          in_range = true;
-          dst = (int64_t)s_ * a.T_cap + p_;
-          st.pos = p_;
-        }
-      }
-      // one round trip: slots, extremes and codes together
-      int32_t sl[4] = {-1, -1, -1, -1};
-      uint32_t mt[4] = {0u, 0u, 0u, 0u};
-      uint4 cw[4];
-#pragma unroll
-      for (int i = 0; i < 4; ++i) cw[i] = make_uint4(0u, 0u, 0u, 0u);
-      const uint8_t* crow = a.codes + dst * a.code_bytes;
-      if (in_range) {
-#pragma unroll
-        for (int t = 0; t < 4; ++t)
-          if (t < a.topk) sl[t] = a.ref_idx[dst * a.topk + t];
-        if (a.bits != 16) {
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            if (i < g_per) {
-              const int g = g0 + i;
-              mt[i] = a.meta[dst * a.G + g];
-              if (a.bits == 4) {
-                cw[i] = *reinterpret_cast<const uint4*>(crow + (int64_t)g * 16);
-              } else {
-                const uint2 v = *reinterpret_cast<const uint2*>(crow + (int64_t)g * 8);
-                cw[i] = make_uint4(v.x, v.y, 0u, 0u);
-              }
-            }
-          }
-        }
-      }
-      // the next tile's row metadata, for the next tile change
-      {
-        const int u_next = (m + 1) * a.n_tiles;
-        nx_m = -1;
-        if (u_next < u_end) {
-          const int64_t gn = (int64_t)(m + 1) * kTileM + row;
-          nx_m = m + 1;
-          nx_s = gn < a.n_sel ? a.seq[gn] : -1;
-          nx_p = gn < a.n_sel ? a.pos[gn] : -1;
-        }
-      }
-      if (in_range) {
-        if (sl[0] < 0 && wg == 0) atomicOr(a.status, RKV_FLAG_UNWRITTEN);
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          if (sl[t] >= a.R_cap && wg == 0) atomicOr(a.status, RKV_FLAG_BAD_SLOT);
-          if (sl[t] >= 0 && sl[t] < a.R_cap) {
-            st.vmask |= 1 << t;
-            ++st.kcnt;
-          }
-        }
-        st.valid = (st.vmask & 1) && st.kcnt > 0;
-      }
-      // pool rows of the references of the two rows whose chunks this lane copies
-#pragma unroll
-      for (int t = 0; t < 4; ++t) {
-        const int mine = ((st.vmask >> t) & 1) ? s_ * a.R_cap + sl[t] : -1;
-        gr.r[t] = __shfl_sync(0xffffffffu, mine, (int)(lane_id() >> 1));
-        gr.r[4 + t] = __shfl_sync(0xffffffffu, mine, 16 + (int)(lane_id() >> 1));
-      }
-      // dequantise this row's share of code groups straight into TMEM
-      if (a.bits == 16) {
-        for (int g = g0; g < g0 + g_per; ++g) {
-          uint32_t o[16];
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const uint4 v = st.valid ? reinterpret_cast<const uint4*>(crow + (int64_t)g * 64)[q]
-                                     : make_uint4(0u, 0u, 0u, 0u);
-            o[4 * q] = v.x, o[4 * q + 1] = v.y, o[4 * q + 2] = v.z, o[4 * q + 3] = v.w;
-          }
-          tmem_st16(tmem + lane_base + kACol + 16u * (uint32_t)g, o);
-        }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          if (i >= g_per) break;
-          const int g = g0 + i;
-          const float lo = __half2float(__ushort_as_half((unsigned short)(mt[i] & 0xFFFFu)));
-          const float hi = __half2float(__ushort_as_half((unsigned short)(mt[i] >> 16)));
-          const float delta = __fdiv_rn(__fsub_rn(hi, lo), (float)levels);
-          const uint32_t w4[4] = {cw[i].x, cw[i].y, cw[i].z, cw[i].w};
-          uint32_t o[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int k = 2 * e;                       // first of two coordinates
-            uint32_t q0, q1;
-            if (a.bits == 4) {
-              q0 = (w4[k >> 3] >> (4 * (k & 7))) & 15u;
-              q1 = (w4[k >> 3] >> (4 * (k & 7) + 4)) & 15u;
-            } else {
-              q0 = (w4[k >> 4] >> (2 * (k & 15))) & 3u;
-              q1 = (w4[k >> 4] >> (2 * (k & 15) + 2)) & 3u;
-            }
-            o[e] = st.valid ? pack_bf16x2(__fadd_rn(__fmul_rn((float)q0, delta), lo),
-                                          __fadd_rn(__fmul_rn((float)q1, delta), lo))
-                            : 0u;
-          }
-          tmem_st16(tmem + lane_base + kACol + 16u * (uint32_t)g, o);
-        }
-      }
-      tmem_st_wait();
+    int gr[4];                                        // pool rows of the next copies
+    int nx_s = -1, nx_p = -1;                         // the row of the next tile
+    auto setup_a = [&](int m) -> RowState {
+      const TileRow tr = tile_setup(a, m, row, wg, g0, g_per, zaddr, nx_s, nx_p,
+                                    (m + 1) * a.n_tiles < u_end);
+      nx_s = tr.nx_s;
+      nx_p = tr.nx_p;
       tc_fence_before();
       __syncwarp();
       if (lane_id() == 0) mbar_arrive(afull);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) gr[t] = tr.r[t];
+      return tr.st;
     };
 
     // cos/sin of the row's 16 pairs at its own position, into shared memory
@@ -414,25 +432,20 @@ __global__ void __launch_bounds__(kReconThreads, 1)
     };
 
     // One commit group per (unit, reference): copy reference t of unit column block
-    // n_next into its slot (nothing when `active` is false; the group is still committed
-    // so that exactly three groups are always younger than the one waited for).
-    auto issue_ref = [&](const GatherRows& gr, int n_next, bool active, int t) {
-      if (active) {
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-          const int prow = gr.r[4 * i + t];
-          if (prow >= 0) {
-            const uint8_t* src = a.pool8 + (int64_t)prow * a.dkv + n_next * kNT + cp_chunk * 16;
-            uint8_t* dst = slots + ((t * 2 + (int)(lane_id() & 1)) * kTileM + cp_row0 + 16 * i) * 16;
-            cp_async16(dst, src);
-          }
-        }
+    // n_next (this row's x and y chunks) into its slot; nothing when `active` is false or
+    // the row has no such reference (the group is still committed, so that exactly three
+    // groups are always younger than the one waited for).
+    auto issue_ref = [&](int n_next, bool active, int t) {
+      const int prow = gr[t];
+      if (active && prow >= 0) {
+        const int64_t off = (int64_t)prow * a.dkv + n_next * kNT;
+        cp_async16(xdst0 + (t * 2) * (kTileM * 16), xsrc0 + off);
+        cp_async16(xdst0 + (t * 2 + 1) * (kTileM * 16), ysrc0 + off);
       }
       cp_async_commit();
     };
 
     RowState cur, nxt;
-    GatherRows grows;                                  // rows of the tile of the next copies
     bool waited = false;                               // previous grid complete (first store)
     int acc = 0;
     uint32_t acc_phase = 0, afree_phase = 0;
@@ -442,9 +455,12 @@ __global__ void __launch_bounds__(kReconThreads, 1)
       const int m = u / a.n_tiles, n = u % a.n_tiles;
       if (m != cur_m) {
         if (cur_m < 0) {
-          setup_a(m, cur, grows);
+          const int64_t gi = (int64_t)m * kTileM + row;
+          nx_s = gi < a.n_sel ? a.seq[gi] : -1;
+          nx_p = gi < a.n_sel ? a.pos[gi] : -1;
+          cur = setup_a(m);
 #pragma unroll
-          for (int t = 0; t < 4; ++t) issue_ref(grows, n, true, t);   // the first unit's copies
+          for (int t = 0; t < 4; ++t) issue_ref(n, true, t);   // the first unit's copies
         } else {
           cur = nxt;                                   // z~ already staged before the last unit
         }
@@ -457,7 +473,7 @@ __global__ void __launch_bounds__(kReconThreads, 1)
       if (u + 1 < u_end && (u + 1) / a.n_tiles != m) {
         if (!warp_wait(afree, afree_phase, abort_flag, a.status)) break;
         afree_phase ^= 1u;
-        setup_a(m + 1, nxt, grows);
+        nxt = setup_a(m + 1);
       }
       const bool more = u + 1 < u_end;
       const int n_next = (u + 1) % a.n_tiles;
@@ -472,14 +488,14 @@ __global__ void __launch_bounds__(kReconThreads, 1)
       for (int t = 0; t < 4; ++t) {
         cp_async_wait<3>();
         __syncwarp();
-        if ((cur.vmask >> t) & 1) {
+        if (cur.has_ref(t)) {
           const uint4 rx = *reinterpret_cast<const uint4*>(slots + ((t * 2) * kTileM + row) * 16);
           const uint4 ry = *reinterpret_cast<const uint4*>(slots + ((t * 2 + 1) * kTileM + row) * 16);
           fp8x16_add2(rx, mx2);
           fp8x16_add2(ry, my2);
         }
         __syncwarp();
-        issue_ref(grows, n_next, more && t < a.topk, t);
+        issue_ref(n_next, more && t < a.topk, t);
       }
       float mx[16], my[16];
 #pragma unroll
@@ -487,12 +503,12 @@ __global__ void __launch_bounds__(kReconThreads, 1)
         f32x2_unpack(mx2[i], mx[2 * i], mx[2 * i + 1]);
         f32x2_unpack(my2[i], my[2 * i], my[2 * i + 1]);
       }
-      if (cur.valid) {
-        if (cur.kcnt == 3) {
+      if (cur.valid()) {
+        if (cur.kcnt() == 3) {
 #pragma unroll
           for (int i = 0; i < 16; ++i) mx[i] = div3_rn(mx[i]), my[i] = div3_rn(my[i]);
         } else {
-          const float kinv = 1.0f / (float)cur.kcnt;   // exact for k_i = 1, 2, 4
+          const float kinv = 1.0f / (float)cur.kcnt();   // exact for k_i = 1, 2, 4
 #pragma unroll
           for (int i = 0; i < 16; ++i) mx[i] = __fmul_rn(mx[i], kinv), my[i] = __fmul_rn(my[i], kinv);
         }
@@ -531,11 +547,11 @@ __global__ void __launch_bounds__(kReconThreads, 1)
           my[2 * i + 1] = y1 * cs.z + x1 * cs.w;
         }
       }
-      if (!cur.valid) {
+      if (!cur.valid()) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) mx[i] = 0.f, my[i] = 0.f;
       }
-      if (cur.in_sel) {
+      if (cur.in_sel()) {
         if (!waited) {
           pdl_wait_previous_grid();                    // K/V may be the previous launch's outputs
           waited = true;
