@@ -44,7 +44,8 @@ constexpr int kReconThreads = 640;
 constexpr int kEpiWarpR = 4;                 // first epilogue warp
 constexpr int kNT = 128;                     // output columns per unit
 constexpr uint32_t kBBytes = kNT * 128;      // one 64-wide k-block of W_d^T rows
-constexpr uint32_t kGBytes = 4 * 4 * 2 * kTileM * 16;   // [group][ref][x|y][row] x 16 B
+constexpr uint32_t kPlaneBytes = kTileM * 32;            // one 32-byte sector per tile row
+constexpr uint32_t kGBytes = 2 * 4 * 2 * kPlaneBytes;    // [group pair][ref][x|y] planes
 constexpr uint32_t kCSBytes = 4 * 8 * kTileM * 16;   // cos/sin: 4 groups x 8 float4 x 128 rows
 constexpr uint32_t kBarBytes = 512;
 constexpr uint32_t kTmemCols = 512;
@@ -386,13 +387,23 @@ __global__ void __launch_bounds__(kReconThreads, 1)
     const int slot0 = 16 * wg;                       // first of this group's 16 pair slots
     const int hl = slot0 / P, j0 = slot0 % P;        // head within the unit, first pair
     const int xcol = hl * a.D + j0, ycol = xcol + P; // unit-local columns of x and y
-    // Reference slots of this group: plane (ref t, x|y) holds 16 bytes per tile row.  Each
-    // thread copies and reads only its own row's two chunks, so no other thread is
-    // involved.
-    uint8_t* slots = sG + (uint32_t)wg * (4 * 2 * kTileM * 16);
-    const uint8_t* xsrc0 = a.pool8 + xcol;             // + pool row * d_kv + unit column base
-    const uint8_t* ysrc0 = a.pool8 + ycol;
-    uint8_t* xdst0 = slots + (uint32_t)row * 16;
+    // Groups 2p and 2p+1 read the two 16-byte halves of the same 32-byte sectors of each
+    // reference row (x columns, and y columns), so they share reference slots: plane
+    // (ref t, x|y) of pair p holds one whole sector per tile row, the halves swapped on
+    // every other group of four rows so that a warp's 16-byte reads hit distinct banks.
+    // Per reference, the warp of group 2p copies the x sectors and the warp of group 2p+1
+    // the y sectors of their 32 rows (two lanes per row, one instruction per 16 rows, so
+    // each sector is fetched once); the two warps meet at named barrier 1 + ew + 4p.
+    const int half = wg & 1;                           // this group's half of a sector
+    const int bar_id = 1 + ew + 4 * (wg >> 1);
+    const int xsec = xcol - 16 * half;                 // the pair's sectors (32-aligned)
+    uint8_t* pslots = sG + (uint32_t)(wg >> 1) * (4 * 2 * kPlaneBytes);
+    const uint32_t rd_off = (uint32_t)row * 32 + (uint32_t)((half ^ ((row >> 2) & 1)) * 16);
+    const int cl = (int)lane_id();
+    const int cp_r0 = ew * 32 + (cl >> 1);             // copies rows cp_r0 and cp_r0 + 16
+    uint8_t* cp_dst0 = pslots + half * kPlaneBytes + (uint32_t)cp_r0 * 32 +
+                       (uint32_t)(((cl & 1) ^ ((cp_r0 >> 2) & 1)) * 16);
+    const uint8_t* cp_src0 = a.pool8 + (half ? xsec + P : xsec) + 16 * (cl & 1);
     const uint32_t zaddr = tmem + lane_base + kACol;  // this thread's z~ columns
     const int g0 = wg * a.G / 4;                     // this group's code groups [g0, g0+g_per)
     const int g_per = (wg + 1) * a.G / 4 - g0;
@@ -431,16 +442,18 @@ __global__ void __launch_bounds__(kReconThreads, 1)
       }
     };
 
-    // One commit group per (unit, reference): copy reference t of unit column block
-    // n_next (this row's x and y chunks) into its slot; nothing when `active` is false or
-    // the row has no such reference (the group is still committed, so that exactly three
-    // groups are always younger than the one waited for).
+    // One commit group per (unit, reference) and one empty group per unit: copy this
+    // warp's sectors of reference t of unit column block n_next into its plane; nothing
+    // when `active` is false or a row has no such reference.  Five groups per unit, so
+    // that exactly three are always younger than the one waited for.
     auto issue_ref = [&](int n_next, bool active, int t) {
-      const int prow = gr[t];
-      if (active && prow >= 0) {
-        const int64_t off = (int64_t)prow * a.dkv + n_next * kNT;
-        cp_async16(xdst0 + (t * 2) * (kTileM * 16), xsrc0 + off);
-        cp_async16(xdst0 + (t * 2 + 1) * (kTileM * 16), ysrc0 + off);
+      if (active) {
+        const int p0 = __shfl_sync(0xffffffffu, gr[t], cl >> 1);
+        const int p1 = __shfl_sync(0xffffffffu, gr[t], (cl >> 1) + 16);
+        uint8_t* dst = cp_dst0 + (uint32_t)(t * 2) * kPlaneBytes;
+        const uint8_t* src = cp_src0 + n_next * kNT;
+        if (p0 >= 0) cp_async16(dst, src + (int64_t)p0 * a.dkv);
+        if (p1 >= 0) cp_async16(dst + 16 * 32, src + (int64_t)p1 * a.dkv);
       }
       cp_async_commit();
     };
@@ -471,7 +484,8 @@ __global__ void __launch_bounds__(kReconThreads, 1)
       // the next tile's z~ so the MMAs resume while this unit's epilogue runs; from here
       // on every copy this thread issues is for the next tile.
       if (u + 1 < u_end && (u + 1) / a.n_tiles != m) {
-        if (!warp_wait(afree, afree_phase, abort_flag, a.status)) break;
+        // both warps of the pair leave together, so neither waits at a barrier alone
+        if (!bar_red_and(bar_id, 64, warp_wait(afree, afree_phase, abort_flag, a.status))) break;
         afree_phase ^= 1u;
         nxt = setup_a(m + 1);
       }
@@ -479,23 +493,25 @@ __global__ void __launch_bounds__(kReconThreads, 1)
       const int n_next = (u + 1) % a.n_tiles;
       const int c0 = n * kNT + hl * a.D;               // first KV_hat column of the head
       const bool is_k = c0 < a.dk;
-      // ---- mean of the references: wait for this unit's copy of reference t, read it,
-      // then reuse its slot for the next unit's copy
+      // ---- mean of the references: wait for this unit's copies of reference t (both
+      // warps' halves), read it; reference t-1 has then been read by both warps, so its
+      // plane takes the next unit's copy
       uint64_t mx2[8], my2[8];                          // packed fp32 pairs
 #pragma unroll
       for (int i = 0; i < 8; ++i) mx2[i] = 0ull, my2[i] = 0ull;
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
         cp_async_wait<3>();
-        __syncwarp();
+        bar_sync(bar_id, 64);
         if (cur.has_ref(t)) {
-          const uint4 rx = *reinterpret_cast<const uint4*>(slots + ((t * 2) * kTileM + row) * 16);
-          const uint4 ry = *reinterpret_cast<const uint4*>(slots + ((t * 2 + 1) * kTileM + row) * 16);
-          fp8x16_add2(rx, mx2);
-          fp8x16_add2(ry, my2);
+          const uint8_t* pt = pslots + (uint32_t)(t * 2) * kPlaneBytes + rd_off;
+          fp8x16_add2(*reinterpret_cast<const uint4*>(pt), mx2);
+          fp8x16_add2(*reinterpret_cast<const uint4*>(pt + kPlaneBytes), my2);
         }
-        __syncwarp();
-        issue_ref(n_next, more && t < a.topk, t);
+        if (t > 0)
+          issue_ref(n_next, more && t - 1 < a.topk, t - 1);
+        else
+          cp_async_commit();
       }
       float mx[16], my[16];
 #pragma unroll
@@ -513,8 +529,10 @@ __global__ void __launch_bounds__(kReconThreads, 1)
           for (int i = 0; i < 16; ++i) mx[i] = __fmul_rn(mx[i], kinv), my[i] = __fmul_rn(my[i], kinv);
         }
       }
-      // ---- accumulator row
-      if (!warp_wait(&tfull[acc], acc_phase, abort_flag, a.status)) break;
+      // ---- accumulator row; the pair's vote also tells that both warps have read
+      // reference 3, whose plane then takes the next unit's copy
+      if (!bar_red_and(bar_id, 64, warp_wait(&tfull[acc], acc_phase, abort_flag, a.status))) break;
+      issue_ref(n_next, more && 3 < a.topk, 3);
       tc_fence_after();
       {
         const uint32_t tacc = tmem + lane_base + (uint32_t)(acc * kNT);

@@ -144,6 +144,28 @@ __device__ __forceinline__ void pdl_wait_previous_grid() {
   asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
+// Named barrier `id` (1..15; 0 is __syncthreads) over `count` threads, a multiple of 32.
+// Orders the participants' earlier shared-memory accesses before their later ones.
+__device__ __forceinline__ void bar_sync(int id, int count) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
+// bar_sync that also returns whether `pred` holds in every participating thread.
+__device__ __forceinline__ bool bar_red_and(int id, int count, bool pred) {
+  int r;
+  asm volatile(
+      "{\n"
+      ".reg .pred p, q;\n"
+      "setp.ne.s32 p, %1, 0;\n"
+      "bar.red.and.pred q, %2, %3, p;\n"
+      "selp.s32 %0, 1, 0, q;\n"
+      "}"
+      : "=r"(r)
+      : "r"(pred ? 1 : 0), "r"(id), "r"(count)
+      : "memory");
+  return r != 0;
+}
+
 // Hint: bring the line holding `p` into L1.
 __device__ __forceinline__ void prefetch_l1(const void* p) {
   asm volatile("prefetch.global.L1 [%0];" ::"l"(p));
