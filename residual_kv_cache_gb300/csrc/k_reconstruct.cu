@@ -30,7 +30,6 @@
 // 64 KB of reference rows), not by the tensor core.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
-#include <cuda_fp8.h>
 
 #include "tc_common.cuh"
 
@@ -78,19 +77,35 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
          (static_cast<uint32_t>(__bfloat16_as_ushort(hi)) << 16);
 }
 
-// s[i] += value of FP8 byte i of v (16 bytes), s held as 8 packed fp32 pairs; exact in
-// fp32 for <= 4 addends (their bits span 2^-9 .. 2^11).
-__device__ __forceinline__ void fp8x16_add2(uint4 v, uint64_t* s) {
-  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      __nv_fp8x2_storage_t pair = static_cast<__nv_fp8x2_storage_t>((w[i] >> (16 * j)) & 0xFFFFu);
-      const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3)));
-      s[2 * i + j] = f32x2_add(s[2 * i + j], f32x2_pack(f.x, f.y));
-    }
-  }
+// s[4i .. 4i+3] += values of the four E4M3 bytes of w (byte 0 first): two bytes at a
+// time to f16 (exact: every E4M3 value is an f16), then each f16 added to its fp32
+// accumulator in one mixed-precision add.
+__device__ __forceinline__ void fp8x4_add(uint32_t w, float& s0, float& s1, float& s2, float& s3) {
+  asm("{\n"
+      ".reg .b16 lo, hi;\n"
+      ".reg .b32 h0, h1;\n"
+      ".reg .f16 a, b, c, d;\n"
+      "mov.b32 {lo, hi}, %4;\n"
+      "cvt.rn.f16x2.e4m3x2 h0, lo;\n"
+      "cvt.rn.f16x2.e4m3x2 h1, hi;\n"
+      "mov.b32 {a, b}, h0;\n"
+      "mov.b32 {c, d}, h1;\n"
+      "add.rn.f32.f16 %0, a, %0;\n"
+      "add.rn.f32.f16 %1, b, %1;\n"
+      "add.rn.f32.f16 %2, c, %2;\n"
+      "add.rn.f32.f16 %3, d, %3;\n"
+      "}"
+      : "+f"(s0), "+f"(s1), "+f"(s2), "+f"(s3)
+      : "r"(w));
+}
+
+// s[i] += value of FP8 byte i of v (16 bytes); exact in fp32 for <= 4 addends (their
+// bits span 2^-9 .. 2^11).
+__device__ __forceinline__ void fp8x16_add(uint4 v, float* s) {
+  fp8x4_add(v.x, s[0], s[1], s[2], s[3]);
+  fp8x4_add(v.y, s[4], s[5], s[6], s[7]);
+  fp8x4_add(v.z, s[8], s[9], s[10], s[11]);
+  fp8x4_add(v.w, s[12], s[13], s[14], s[15]);
 }
 
 // Correctly rounded s / 3 for every fp32 s that is a sum of at most three E4M3 values:
@@ -496,28 +511,22 @@ __global__ void __launch_bounds__(kReconThreads, 1)
       // ---- mean of the references: wait for this unit's copies of reference t (both
       // warps' halves), read it; reference t-1 has then been read by both warps, so its
       // plane takes the next unit's copy
-      uint64_t mx2[8], my2[8];                          // packed fp32 pairs
+      float mx[16], my[16];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) mx2[i] = 0ull, my2[i] = 0ull;
+      for (int i = 0; i < 16; ++i) mx[i] = 0.f, my[i] = 0.f;
 #pragma unroll
       for (int t = 0; t < 4; ++t) {
         cp_async_wait<3>();
         bar_sync(bar_id, 64);
         if (cur.has_ref(t)) {
           const uint8_t* pt = pslots + (uint32_t)(t * 2) * kPlaneBytes + rd_off;
-          fp8x16_add2(*reinterpret_cast<const uint4*>(pt), mx2);
-          fp8x16_add2(*reinterpret_cast<const uint4*>(pt + kPlaneBytes), my2);
+          fp8x16_add(*reinterpret_cast<const uint4*>(pt), mx);
+          fp8x16_add(*reinterpret_cast<const uint4*>(pt + kPlaneBytes), my);
         }
         if (t > 0)
           issue_ref(n_next, more && t - 1 < a.topk, t - 1);
         else
           cp_async_commit();
-      }
-      float mx[16], my[16];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        f32x2_unpack(mx2[i], mx[2 * i], mx[2 * i + 1]);
-        f32x2_unpack(my2[i], my[2 * i], my[2 * i + 1]);
       }
       if (cur.valid()) {
         if (cur.kcnt() == 3) {
