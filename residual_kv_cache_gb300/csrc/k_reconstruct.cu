@@ -233,30 +233,43 @@ __device__ __forceinline__ TileRow tile_setup(const ReconArgs& a, int m, int row
       tmem_st16(zaddr + 16u * (uint32_t)g, o);
     }
   } else {
+    // Codes become floats without integer-to-float conversions: a code q placed in the
+    // low mantissa bits under the exponent of 2^23 reads as the float 2^23 + q exactly,
+    // and one subtraction leaves q.  z~ = RN(RN(q * Delta) + min), two columns at a time.
     const int levels = (1 << a.bits) - 1;
+    const uint64_t two23 = f32x2_pack(8388608.0f, 8388608.0f);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       if (i >= g_per) break;
       const int g = g0 + i;
-      const float lo = __half2float(__ushort_as_half((unsigned short)(mt[i] & 0xFFFFu)));
+      float lo = __half2float(__ushort_as_half((unsigned short)(mt[i] & 0xFFFFu)));
       const float hi = __half2float(__ushort_as_half((unsigned short)(mt[i] >> 16)));
-      const float delta = __fdiv_rn(__fsub_rn(hi, lo), (float)levels);
+      float delta = __fdiv_rn(__fsub_rn(hi, lo), (float)levels);
+      if (!valid) lo = 0.f, delta = 0.f;              // an invalid row decodes to zeros
+      const uint64_t dd = f32x2_pack(delta, delta);
       const uint32_t w4[4] = {cw[i].x, cw[i].y, cw[i].z, cw[i].w};
       uint32_t o[16];
 #pragma unroll
       for (int e = 0; e < 16; ++e) {
-        const int k = 2 * e;                           // first of two coordinates
-        uint32_t q0, q1;
+        uint32_t t0, t1;                               // 2^23 + q of coordinates 2e, 2e + 1
         if (a.bits == 4) {
-          q0 = (w4[k >> 3] >> (4 * (k & 7))) & 15u;
-          q1 = (w4[k >> 3] >> (4 * (k & 7) + 4)) & 15u;
+          // word e/4 holds coordinates 8 (e/4) + n in nibble n: the even nibbles of a
+          // word are its bytes' low halves, the odd nibbles their high halves
+          const uint32_t w = w4[e >> 2];
+          const uint32_t sel = 0x7650u + (uint32_t)(e & 3);
+          t0 = __byte_perm(w & 0x0F0F0F0Fu, 0x4B000000u, sel);
+          t1 = __byte_perm((w >> 4) & 0x0F0F0F0Fu, 0x4B000000u, sel);
         } else {
-          q0 = (w4[k >> 4] >> (2 * (k & 15))) & 3u;
-          q1 = (w4[k >> 4] >> (2 * (k & 15) + 2)) & 3u;
+          const int k = 2 * e;
+          t0 = ((w4[k >> 4] >> (2 * (k & 15))) & 3u) | 0x4B000000u;
+          t1 = ((w4[k >> 4] >> (2 * (k & 15) + 2)) & 3u) | 0x4B000000u;
         }
-        o[e] = valid ? pack_bf16x2(__fadd_rn(__fmul_rn((float)q0, delta), lo),
-                                   __fadd_rn(__fmul_rn((float)q1, delta), lo))
-                     : 0u;
+        const uint64_t q = f32x2_sub(f32x2_pack(__uint_as_float(t0), __uint_as_float(t1)), two23);
+        // the addition stays scalar: ptxas contracts a packed multiply followed by a
+        // packed add into one fused multiply-add, which rounds once instead of twice
+        float m0, m1;
+        f32x2_unpack(f32x2_mul(q, dd), m0, m1);
+        o[e] = pack_bf16x2(__fadd_rn(m0, lo), __fadd_rn(m1, lo));
       }
       tmem_st16(zaddr + 16u * (uint32_t)g, o);
     }
