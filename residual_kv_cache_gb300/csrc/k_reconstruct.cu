@@ -50,6 +50,12 @@ constexpr uint32_t kBarBytes = 512;
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kACol = 2 * kNT;          // z~ after the two accumulators
 constexpr int kMaxStages = 8;
+// Extra cost of a token-tile change inside a CTA's range (staging the next tile's z~ and
+// cos/sin while the tensor core drains), in quarter units.
+#ifndef RKV_TILE_CHANGE_COST4
+#define RKV_TILE_CHANGE_COST4 8
+#endif
+constexpr int kTileChangeCost4 = RKV_TILE_CHANGE_COST4;
 
 struct ReconArgs {
   const int32_t* seq;
@@ -278,6 +284,20 @@ __device__ __forceinline__ TileRow tile_setup(const ReconArgs& a, int m, int row
   return tr;
 }
 
+// First unit of CTA b's contiguous range (b = grid gives `units`).  The ranges split a
+// cost of one per unit plus kTileChangeCost4 / 4 per token-tile boundary crossed inside
+// a range evenly over the grid: each tile after the first carries that extra cost ahead
+// of its first unit, and a cut falling there starts the next range on the tile.
+__device__ __forceinline__ int range_start(int b, int grid, int units, int n_tiles) {
+  const int64_t tc = 4 * (int64_t)n_tiles + kTileChangeCost4;
+  const int64_t total = (int64_t)(units / n_tiles) * tc - kTileChangeCost4;
+  const int64_t c = (int64_t)b * total / grid + kTileChangeCost4;
+  const int64_t t = c / tc;
+  const int64_t off4 = c - t * tc - kTileChangeCost4;
+  const int64_t u = t * n_tiles + (off4 <= 0 ? 0 : off4 / 4);
+  return (int)(u < units ? u : units);
+}
+
 __global__ void __launch_bounds__(kReconThreads, 1)
     reconstruct_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ ReconArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -297,8 +317,8 @@ __global__ void __launch_bounds__(kReconThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   pdl_launch_dependents();
-  const int u_begin = (int)(((int64_t)blockIdx.x * a.units) / gridDim.x);
-  const int u_end = (int)(((int64_t)(blockIdx.x + 1) * a.units) / gridDim.x);
+  const int u_begin = range_start(blockIdx.x, gridDim.x, a.units, a.n_tiles);
+  const int u_end = range_start(blockIdx.x + 1, gridDim.x, a.units, a.n_tiles);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < a.b_stages; ++s) {
