@@ -182,6 +182,93 @@ void timing_end(rkv_ctx* c, const char* name, cudaStream_t s, cudaEvent_t start)
 
 }  // namespace rkv
 
+namespace {
+
+// Whether any row breaks a precondition of rkv_compress (see compress_row_error).
+template <bool kPow2Stride>
+bool compress_rows_bad(const rkv_ctx* c, const int32_t* src_rows, const int32_t* seq,
+                       const int32_t* pos, int n) {
+  const rkv::Dims& d = c->d;
+  const int32_t* pc = c->pool_count.data();
+  const unsigned smask = (unsigned)d.stride - 1u;
+  int bad = 0;
+  for (int i = 0; i < n; ++i) {
+    const int s = seq[i], p = pos[i];
+    const int s_ok = (unsigned)s < (unsigned)d.B;
+    const int64_t cnt = pc[s_ok ? s : 0];
+    const int off = kPow2Stride ? (int)((unsigned)p & smask) : p % d.stride;
+    bad |= !s_ok | ((unsigned)p >= (unsigned)d.T_cap) | (off == 0) | (cnt == 0) |
+           ((int64_t)p > cnt * d.stride);
+  }
+  if (src_rows)
+    for (int i = 0; i < n; ++i) bad |= src_rows[i] < 0;
+  return bad != 0;
+}
+
+// The first row that breaks a precondition of rkv_compress, as an error.
+rkv_status compress_row_error(const rkv_ctx* c, const int32_t* src_rows, const int32_t* seq,
+                              const int32_t* pos, int n) {
+  const rkv::Dims& d = c->d;
+  for (int i = 0; i < n; ++i) {
+    const int s = seq[i], p = pos[i];
+    const int src = src_rows ? src_rows[i] : i;
+    if (s < 0 || s >= d.B) return fail(RKV_EINVAL, "row %d: seq %d out of range", i, s);
+    if (p < 0 || p >= d.T_cap) return fail(RKV_EINVAL, "row %d: pos %d out of range", i, p);
+    if (src < 0) return fail(RKV_EINVAL, "row %d: negative source row", i);
+    if (p % d.stride == 0) return fail(RKV_EINVAL, "row %d: pos %d is a reference position", i, p);
+    if (c->pool_count[s] == 0) return fail(RKV_EEMPTYPOOL, "row %d: seq %d has no reference", i, s);
+    // the references before p are the ceil(p / s) positions 0, s, 2s, ... < p
+    if ((int64_t)p > (int64_t)c->pool_count[s] * d.stride)
+      return fail(RKV_EINVAL, "row %d: references of seq %d before pos %d are not all appended", i,
+                  s, p);
+  }
+  return fail(RKV_EINVAL, "invalid rows");
+}
+
+// Per-row plan entries of one tile's rows (retrieval slots q0 .. q0 + cnt - 1, compact
+// rows given by `rows`, or r_first .. r_first + cnt - 1 when `rows` is null) of sequence
+// s; returns the largest position among them (at least 1).
+int fill_tile_rows(int32_t* h, const rkv::PassPlan& p, const rkv::Dims& d, const int32_t* src_rows,
+                   const int32_t* pos, const int* rows, int r_first, int r0, int cnt, int q0,
+                   int s) {
+  int32_t* __restrict__ qsrc = h + p.off_q_src + q0;
+  int32_t* __restrict__ qpos = h + p.off_q_pos + q0;
+  int32_t* __restrict__ qdst = h + p.off_q_dst + q0;
+  const int64_t sT = (int64_t)s * d.T_cap;
+  int maxpos = 1;
+  if (!rows) {
+    const int32_t* __restrict__ pp = pos + r_first;
+    int32_t* __restrict__ cq = h + p.off_c_q + (r_first - r0);
+    int32_t* __restrict__ cdst = h + p.off_c_dst + (r_first - r0);
+    for (int r = 0; r < cnt; ++r) {
+      const int pr = pp[r];
+      maxpos = pr > maxpos ? pr : maxpos;
+      qpos[r] = pr;
+      qdst[r] = (int32_t)(sT + pr);
+      cdst[r] = (int32_t)(sT + pr);
+      cq[r] = q0 + r;
+    }
+    if (src_rows)
+      std::memcpy(qsrc, src_rows + r_first, sizeof(int32_t) * cnt);
+    else
+      for (int r = 0; r < cnt; ++r) qsrc[r] = r_first + r;
+  } else {
+    for (int r = 0; r < cnt; ++r) {
+      const int row = rows[r];
+      const int pr = pos[row];
+      maxpos = pr > maxpos ? pr : maxpos;
+      qsrc[r] = src_rows ? src_rows[row] : row;
+      qpos[r] = pr;
+      qdst[r] = (int32_t)(sT + pr);
+      h[p.off_c_q + (row - r0)] = q0 + r;
+      h[p.off_c_dst + (row - r0)] = (int32_t)(sT + pr);
+    }
+  }
+  return maxpos;
+}
+
+}  // namespace
+
 extern "C" {
 
 const char* rkv_last_error(void) { return g_err.c_str(); }
@@ -382,19 +469,12 @@ rkv_status rkv_compress(rkv_ctx* c, const void* kv, int64_t kv_row_stride, const
   const Dims& d = c->d;
   if (kv_row_stride < d.dkv || kv_row_stride % 8 != 0)
     return fail(RKV_EINVAL, "kv_row_stride must be >= 2*d_k and a multiple of 8");
-  for (int i = 0; i < n; ++i) {
-    const int s = seq[i], p = pos[i];
-    const int src = src_rows ? src_rows[i] : i;
-    if (s < 0 || s >= d.B) return fail(RKV_EINVAL, "row %d: seq %d out of range", i, s);
-    if (p < 0 || p >= d.T_cap) return fail(RKV_EINVAL, "row %d: pos %d out of range", i, p);
-    if (src < 0) return fail(RKV_EINVAL, "row %d: negative source row", i);
-    if (p % d.stride == 0) return fail(RKV_EINVAL, "row %d: pos %d is a reference position", i, p);
-    if (c->pool_count[s] == 0) return fail(RKV_EEMPTYPOOL, "row %d: seq %d has no reference", i, s);
-    // the references before p are the ceil(p / s) positions 0, s, 2s, ... < p
-    if ((int64_t)p > (int64_t)c->pool_count[s] * d.stride)
-      return fail(RKV_EINVAL, "row %d: references of seq %d before pos %d are not all appended", i,
-                  s, p);
-  }
+  // one branch-free pass over the rows; the row-by-row pass that names the first bad
+  // row runs only when it found one
+  const bool any_bad = (d.stride & (d.stride - 1)) == 0
+                           ? compress_rows_bad<true>(c, src_rows, seq, pos, n)
+                           : compress_rows_bad<false>(c, src_rows, seq, pos, n);
+  if (any_bad) return compress_row_error(c, src_rows, seq, pos, n);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   std::vector<int> order, gbeg;
   std::vector<int32_t> tseq, trow0, tnrt;
@@ -402,28 +482,33 @@ rkv_status rkv_compress(rkv_ctx* c, const void* kv, int64_t kv_row_stride, const
     const int m = std::min(c->max_rows, n - r0);
     // ---- plan: rows grouped by sequence (stable), each group padded to 128 rows.  A
     // counting sort by sequence id (O(m + B)); nothing to do when the ids never decrease.
-    order.resize(m);
     bool grouped = true;
-    for (int i = 1; i < m && grouped; ++i) grouped = seq[r0 + i] >= seq[r0 + i - 1];
-    if (grouped) {
-      for (int i = 0; i < m; ++i) order[i] = r0 + i;
-    } else {
+    for (int i = 1; i < m; ++i) grouped &= seq[r0 + i] >= seq[r0 + i - 1];
+    const int* ord = nullptr;                          // group order; null: rows as given
+    if (!grouped) {
+      order.resize(m);
       std::vector<int> start(d.B + 1, 0);
       for (int i = 0; i < m; ++i) ++start[seq[r0 + i] + 1];
       for (int b2 = 0; b2 < d.B; ++b2) start[b2 + 1] += start[b2];
       for (int i = 0; i < m; ++i) order[start[seq[r0 + i]]++] = r0 + i;
+      ord = order.data();
     }
-    // group boundaries in `order`, padded sizes
+    // group boundaries (positions in group order), padded sizes
     gbeg.clear();
     int m_pad = 0, ntiles = 0;
-    for (int i = 0; i < m;) {
-      int j = i + 1;
-      while (j < m && seq[order[j]] == seq[order[i]]) ++j;
-      gbeg.push_back(i);
-      const int padded = (j - i + kTileM - 1) / kTileM * kTileM;
-      m_pad += padded;
-      ntiles += padded / kTileM;
-      i = j;
+    {
+      int i = 0;
+      int si = seq[ord ? ord[0] : r0];
+      for (int j = 1; j <= m; ++j) {
+        const int sj = j < m ? seq[ord ? ord[j] : r0 + j] : -1;
+        if (sj == si) continue;
+        gbeg.push_back(i);
+        const int padded = (j - i + kTileM - 1) / kTileM * kTileM;
+        m_pad += padded;
+        ntiles += padded / kTileM;
+        i = j;
+        si = sj;
+      }
     }
     gbeg.push_back(m);
     // plan layout: per-row arrays first, then tiles, then units (counted while filling)
@@ -451,21 +536,11 @@ rkv_status rkv_compress(rkv_ctx* c, const void* kv, int64_t kv_row_stride, const
     int q = 0, n_units = 0;
     for (size_t g = 0; g + 1 < gbeg.size(); ++g) {
       const int i = gbeg[g], j = gbeg[g + 1];
-      const int s = seq[order[i]];
+      const int s = seq[ord ? ord[i] : r0 + i];
       for (int k = i; k < j; k += kTileM) {
         const int kend = std::min(j, k + kTileM);
-        int maxpos = 1;
-        for (int r = k; r < kend; ++r) {
-          const int row = order[r];
-          const int qr = q + (r - i);
-          const int pr = pos[row];
-          maxpos = std::max(maxpos, pr);
-          h[p.off_q_src + qr] = src_rows ? src_rows[row] : row;
-          h[p.off_q_pos + qr] = pr;
-          h[p.off_q_dst + qr] = s * d.T_cap + pr;
-          h[p.off_c_q + (row - r0)] = qr;
-          h[p.off_c_dst + (row - r0)] = s * d.T_cap + pr;
-        }
+        const int maxpos = fill_tile_rows(h, p, d, src_rows, pos, ord ? ord + k : nullptr, r0 + k,
+                                          r0, kend - k, q + (k - i), s);
         const int nrt = (visible_refs(maxpos, d.stride) + kRefTile - 1) / kRefTile;
         tseq.push_back(s);
         trow0.push_back(q + (k - i));
