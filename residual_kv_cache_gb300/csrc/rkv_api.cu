@@ -184,25 +184,51 @@ void timing_end(rkv_ctx* c, const char* name, cudaStream_t s, cudaEvent_t start)
 
 namespace {
 
-// Whether any row breaks a precondition of rkv_compress (see compress_row_error).
+// One pass over the rows of an rkv_compress call (branch-free, so that it vectorises):
+// the checks that need no per-sequence state, and the shape of the sequence ids.
+struct RowScan {
+  bool bad;       // a row breaks a per-row precondition
+  bool grouped;   // the sequence ids never decrease
+  int runs;       // runs of equal sequence ids
+  int max_pos;    // largest position (meaningful when runs == 1)
+};
+
 template <bool kPow2Stride>
-bool compress_rows_bad(const rkv_ctx* c, const int32_t* src_rows, const int32_t* seq,
-                       const int32_t* pos, int n) {
-  const rkv::Dims& d = c->d;
-  const int32_t* pc = c->pool_count.data();
+RowScan scan_compress_rows(const rkv::Dims& d, const int32_t* src_rows, const int32_t* seq,
+                           const int32_t* pos, int n) {
   const unsigned smask = (unsigned)d.stride - 1u;
-  int bad = 0;
+  unsigned bad = 0, dec = 0;
+  int changes = 0, max_pos = 0;
   for (int i = 0; i < n; ++i) {
     const int s = seq[i], p = pos[i];
-    const int s_ok = (unsigned)s < (unsigned)d.B;
-    const int64_t cnt = pc[s_ok ? s : 0];
     const int off = kPow2Stride ? (int)((unsigned)p & smask) : p % d.stride;
-    bad |= !s_ok | ((unsigned)p >= (unsigned)d.T_cap) | (off == 0) | (cnt == 0) |
-           ((int64_t)p > cnt * d.stride);
+    bad |= (unsigned)((unsigned)s >= (unsigned)d.B) | (unsigned)((unsigned)p >= (unsigned)d.T_cap) |
+           (unsigned)(off == 0);
+    max_pos = p > max_pos ? p : max_pos;
+  }
+  for (int i = 1; i < n; ++i) {
+    dec |= (unsigned)(seq[i] < seq[i - 1]);
+    changes += seq[i] != seq[i - 1];
   }
   if (src_rows)
-    for (int i = 0; i < n; ++i) bad |= src_rows[i] < 0;
-  return bad != 0;
+    for (int i = 0; i < n; ++i) bad |= (unsigned)src_rows[i] >> 31;
+  return {bad != 0, dec == 0, changes + 1, max_pos};
+}
+
+// Whether some row's sequence has no reference, or lacks references before the row's
+// position (the references before p are the ceil(p / stride) positions 0, stride, ...).
+bool compress_pools_bad(const rkv_ctx* c, const RowScan& r, const int32_t* seq,
+                        const int32_t* pos, int n) {
+  const rkv::Dims& d = c->d;
+  if (r.runs == 1) {
+    const int64_t cnt = c->pool_count[seq[0]];
+    return cnt == 0 || (int64_t)r.max_pos > cnt * d.stride;
+  }
+  for (int i = 0; i < n; ++i) {
+    const int64_t cnt = c->pool_count[seq[i]];
+    if (cnt == 0 || (int64_t)pos[i] > cnt * d.stride) return true;
+  }
+  return false;
 }
 
 // The first row that breaks a precondition of rkv_compress, as an error.
@@ -471,10 +497,11 @@ rkv_status rkv_compress(rkv_ctx* c, const void* kv, int64_t kv_row_stride, const
     return fail(RKV_EINVAL, "kv_row_stride must be >= 2*d_k and a multiple of 8");
   // one branch-free pass over the rows; the row-by-row pass that names the first bad
   // row runs only when it found one
-  const bool any_bad = (d.stride & (d.stride - 1)) == 0
-                           ? compress_rows_bad<true>(c, src_rows, seq, pos, n)
-                           : compress_rows_bad<false>(c, src_rows, seq, pos, n);
-  if (any_bad) return compress_row_error(c, src_rows, seq, pos, n);
+  const RowScan scan = (d.stride & (d.stride - 1)) == 0
+                           ? scan_compress_rows<true>(d, src_rows, seq, pos, n)
+                           : scan_compress_rows<false>(d, src_rows, seq, pos, n);
+  if (scan.bad || compress_pools_bad(c, scan, seq, pos, n))
+    return compress_row_error(c, src_rows, seq, pos, n);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   std::vector<int> order, gbeg;
   std::vector<int32_t> tseq, trow0, tnrt;
@@ -482,8 +509,12 @@ rkv_status rkv_compress(rkv_ctx* c, const void* kv, int64_t kv_row_stride, const
     const int m = std::min(c->max_rows, n - r0);
     // ---- plan: rows grouped by sequence (stable), each group padded to 128 rows.  A
     // counting sort by sequence id (O(m + B)); nothing to do when the ids never decrease.
-    bool grouped = true;
-    for (int i = 1; i < m; ++i) grouped &= seq[r0 + i] >= seq[r0 + i - 1];
+    bool grouped = scan.grouped;
+    if (!grouped) {
+      unsigned dec = 0;
+      for (int i = 1; i < m; ++i) dec |= (unsigned)(seq[r0 + i] < seq[r0 + i - 1]);
+      grouped = dec == 0;
+    }
     const int* ord = nullptr;                          // group order; null: rows as given
     if (!grouped) {
       order.resize(m);
@@ -496,7 +527,11 @@ rkv_status rkv_compress(rkv_ctx* c, const void* kv, int64_t kv_row_stride, const
     // group boundaries (positions in group order), padded sizes
     gbeg.clear();
     int m_pad = 0, ntiles = 0;
-    {
+    if (scan.runs == 1) {
+      gbeg.push_back(0);
+      m_pad = (m + kTileM - 1) / kTileM * kTileM;
+      ntiles = m_pad / kTileM;
+    } else {
       int i = 0;
       int si = seq[ord ? ord[0] : r0];
       for (int j = 1; j <= m; ++j) {
