@@ -23,7 +23,9 @@ Two arithmetic modes
 
 Readings of points the page leaves open (each one is also listed in the
 design notes of the repository):
-* the reference schedule is fixed stride with position 0 a reference;
+* the reference schedule starts at position 0 (fixed stride) or, for the
+  dynamic schedule, at p_0 = n_sink with the n_sink sink tokens before it kept
+  as references too; floor(alpha (p - n_sink)) is taken of one binary64 product;
 * token i may retrieve references with position < i, ties broken by the
   smaller pool slot;
 * "Swish" is x*sigmoid(x) (beta = 1), no biases;
@@ -39,6 +41,8 @@ from __future__ import annotations
 
 from dataclasses import dataclass
 
+import math
+
 import numpy as np
 
 from . import formats as F
@@ -47,6 +51,7 @@ __all__ = [
     "Shape",
     "reference_positions",
     "is_reference",
+    "reference_count_estimate",
     "store_references",
     "visible_slots",
     "retrieve",
@@ -88,6 +93,8 @@ class Shape:
     bits: int = 4          # 4, 2, or 16 = quantisation off (z kept as bf16)
     stride: int = 16
     rope_base: float = 1e4
+    ref_alpha: float = 0.0  # dynamic schedule growth (0: fixed stride)
+    ref_sink: int = 0       # sink tokens, kept as references ahead of the schedule
 
     @property
     def d_k(self) -> int:
@@ -110,15 +117,39 @@ class Shape:
 
 
 # --------------------------------------------------------------------------
-# Reference schedule (ResidualKV notes, section 2.6, fixed stride)
+# Reference schedule (ResidualKV notes, section 2.6: fixed and dynamic stride)
 # --------------------------------------------------------------------------
-def reference_positions(T: int, stride: int) -> np.ndarray:
-    """Positions kept as references: every ``stride``-th token, starting at 0."""
-    return np.arange(0, T, stride, dtype=np.int64)
+def reference_positions(T: int, stride: int, alpha: float = 0.0, sink: int = 0) -> np.ndarray:
+    """Positions below T kept as references.
+
+    Section 2.6: the gaps grow with the position, p_{m+1} = p_m + s_0 +
+    floor(alpha (p_m - n_sink)), with s_0 = ``stride``; alpha = 0 is the fixed
+    stride.  Readings: the schedule starts at p_0 = n_sink, and the n_sink sink
+    tokens before it are references too (so every token has one before it);
+    alpha (p_m - n_sink) is one binary64 product, then floored.
+    """
+    out = list(range(min(sink, T)))
+    p = sink
+    while p < T:
+        out.append(p)
+        p = p + stride + math.floor(alpha * (p - sink))
+    return np.array(out, dtype=np.int64)
 
 
-def is_reference(pos, stride: int):
-    return np.asarray(pos) % stride == 0
+def is_reference(pos, stride: int, alpha: float = 0.0, sink: int = 0):
+    pos = np.asarray(pos)
+    if pos.size == 0:
+        return np.zeros(pos.shape, dtype=bool)
+    return np.isin(pos, reference_positions(int(pos.max()) + 1, stride, alpha, sink))
+
+
+def reference_count_estimate(T: int, stride: int, alpha: float, sink: int = 0) -> float:
+    """The page's closed-form estimate of the scheduled references (section 2.6),
+    from the recurrence without the floor: log_{1+alpha}(1 + alpha (T - n_sink) / s_0);
+    its alpha -> 0 limit is (T - n_sink) / s_0."""
+    if alpha == 0.0:
+        return (T - sink) / stride
+    return math.log1p(alpha * (T - sink) / stride) / math.log1p(alpha)
 
 
 # --------------------------------------------------------------------------
@@ -378,8 +409,8 @@ class Pool:
     pos: np.ndarray        # [R] token positions
 
 
-def build_pool(kv, T: int, stride: int) -> Pool:
-    rp = reference_positions(T, stride)
+def build_pool(kv, T: int, stride: int, alpha: float = 0.0, sink: int = 0) -> Pool:
+    rp = reference_positions(T, stride, alpha, sink)
     codes, vals, norm2 = store_references(np.asarray(kv, np.float64)[rp])
     return Pool(codes, vals, norm2, rp)
 
@@ -444,14 +475,15 @@ def compress_sequence(kv, W, shape: Shape, mode: str = "operand") -> Store:
     """
     kv = np.asarray(kv, np.float64)
     T = kv.shape[0]
-    pool = build_pool(kv, T, shape.stride)
+    pool = build_pool(kv, T, shape.stride, shape.ref_alpha, shape.ref_sink)
     idx = np.full((T, shape.topk), -1, dtype=np.int64)
     q = np.zeros((T, shape.d_c))
     meta = np.zeros((T, shape.n_groups, 2))
     z = np.zeros((T, shape.d_c))
     dist = np.full((T, shape.topk), np.nan)
     idx[pool.pos, 0] = np.arange(len(pool.pos))
-    nonref = np.nonzero(~is_reference(np.arange(T), shape.stride))[0]
+    nonref = np.nonzero(~is_reference(np.arange(T), shape.stride, shape.ref_alpha,
+                                      shape.ref_sink))[0]
     enc = encode_tokens(kv[nonref], nonref, pool, W, shape, mode)
     idx[nonref] = enc["idx"]
     q[nonref] = enc["q"]

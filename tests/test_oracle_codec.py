@@ -40,6 +40,85 @@ def test_reference_count_is_ceil_T_over_s():
     assert C.reference_positions(40, 16).tolist() == [0, 16, 32]
 
 
+def test_dynamic_schedule_with_alpha_zero_is_the_fixed_stride():
+    """Section 2.6: alpha = 0 is the fixed stride, p_m = n_sink + m s_0."""
+    for T, s in ((256, 8), (1000, 16), (4099, 10), (17, 32)):
+        assert C.reference_positions(T, s, 0.0, 0).tolist() == list(range(0, T, s))
+    # with sinks: 0 .. n_sink - 1, then n_sink, n_sink + s, ...
+    assert C.reference_positions(40, 10, 0.0, 4).tolist() == [0, 1, 2, 3, 4, 14, 24, 34]
+
+
+def test_dynamic_schedule_first_terms_by_hand():
+    """p_{m+1} = p_m + s_0 + floor(alpha (p_m - n_sink)) with s_0 = 10,
+    alpha = 0.1, n_sink = 4: 4, 4+10+0 = 14, 14+10+1 = 25, 25+10+2 = 37,
+    37+10+3 = 50, 50+10+4 = 64, 64+10+6 = 80."""
+    got = C.reference_positions(81, 10, 0.1, 4).tolist()
+    assert got == [0, 1, 2, 3, 4, 14, 25, 37, 50, 64, 80]
+    assert C.is_reference([3, 4, 5, 14, 24, 25], 10, 0.1, 4).tolist() == [
+        True, True, False, True, False, True]
+
+
+def test_dynamic_schedule_reproduces_table_vi_counts():
+    """Table VI (section 4.6) counts at a 262K context with s_0 = 10.  The five
+    counts are reproduced together, with no sink tokens, for an effective
+    length T in [261881, 261890] (the page does not state the exact length);
+    alpha = 0 there is ceil(T / 10)."""
+    rows = [(float(a), int(n)) for a, n in _golden("table6_reference_counts.txt")]
+    for T in (261881, 261885, 261890):
+        for alpha, n in rows:
+            assert len(C.reference_positions(T, 10, alpha, 0)) == n, (T, alpha)
+    assert -(-261885 // 10) == 26189
+    # just outside the window the alpha = 0 count moves
+    assert len(C.reference_positions(261880, 10, 0.0, 0)) == 26188
+    assert len(C.reference_positions(261891, 10, 0.0, 0)) == 26190
+
+
+def test_dynamic_schedule_against_the_page_estimate():
+    """Section 2.6's estimate log_{1+alpha}(1 + alpha (T - n_sink) / s_0) drops
+    the floor.  The floor shortens each gap by less than one token, so the gaps
+    lie between those of the real-valued recurrence with s_0 - 1 and with s_0,
+    and the count between the two estimates (+1 for the last partial gap)."""
+    for alpha in (0.001, 0.02, 0.05, 0.1):
+        for T, sink in ((262144, 0), (98304, 0), (32768, 4)):
+            n = len(C.reference_positions(T, 10, alpha, sink)) - sink
+            lo = C.reference_count_estimate(T, 10, alpha, sink)
+            hi = C.reference_count_estimate(T, 9, alpha, sink) + 1
+            assert lo <= n <= hi, (alpha, T, n, lo, hi)
+
+
+def test_dynamic_schedule_every_token_has_an_earlier_reference():
+    """With the sinks kept as references, position 0 is always a reference, so
+    no non-reference token has an empty pool; gaps never shrink."""
+    for alpha, sink in ((0.02, 0), (0.05, 4), (0.1, 16)):
+        rp = C.reference_positions(5000, 8, alpha, sink)
+        assert rp[0] == 0 and np.all(np.diff(rp) >= 1)
+        gaps = np.diff(rp[sink:])
+        assert np.all(np.diff(gaps) >= 0) and gaps[0] == 8
+
+
+def test_compress_with_dynamic_schedule_retrieves_only_earlier_references():
+    """The write path over a dynamic schedule: every token's slots point at
+    references strictly before it, k_i = min(k, references before it), and a
+    reference's own row is [slot, -1, ...]."""
+    rng = np.random.default_rng(7)
+    sh = C.Shape(n_kv_heads=1, head_dim=16, d_c=16, d_ff=32, topk=4, group=16, bits=4,
+                 stride=4, ref_alpha=0.25, ref_sink=2)
+    T = 96
+    kv = rng.normal(size=(T, sh.d_kv))
+    st = C.compress_sequence(kv, _weights(rng, sh.d_kv, sh.d_ff, sh.d_c), sh, "fp64")
+    rp = C.reference_positions(T, sh.stride, sh.ref_alpha, sh.ref_sink)
+    assert st.pool.pos.tolist() == rp.tolist()
+    for p in range(T):
+        row = st.idx[p]
+        if p in set(rp.tolist()):
+            assert row[0] == rp.tolist().index(p) and np.all(row[1:] == -1)
+            continue
+        before = int(np.sum(rp < p))
+        valid = row[row >= 0]
+        assert len(valid) == min(sh.topk, before)
+        assert np.all(st.pool.pos[valid] < p)
+
+
 # ---------------------------------------------------------------- retrieval
 def test_retrieval_equals_brute_force_over_subsets():
     rng = np.random.default_rng(10)
