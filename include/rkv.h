@@ -65,7 +65,7 @@ enum {
 /*
  * Codec configuration.  Shapes follow ResidualKV notes §2.1 (d_k = N*D, the
  * joint vector kv_i has 2*d_k entries), §2.3 (d_c, d_ff), §2.4 (g, b) and §2.6
- * (fixed reference stride s).  Limits of this build: head_dim in {64, 128}; 2*d_k a
+ * (the reference schedule, fixed or dynamic stride).  Limits of this build: head_dim in {64, 128}; 2*d_k a
  * multiple of 256; d_c a multiple of 64 and at most 512 (the decoder keeps a token
  * tile's z~ in tensor memory); d_ff a multiple of 128; topk in 1..4; group = 32; bits in {4, 2, 16} (16 =
  * quantisation off, z kept as bf16).
@@ -78,16 +78,28 @@ typedef struct {
   int32_t topk;              /* k (the page's default is 4)                    */
   int32_t group;             /* g = 32                                         */
   int32_t bits;              /* 4, 2 or 16                                     */
-  int32_t ref_stride;        /* s: token pos is a reference iff pos % s == 0   */
+  int32_t ref_stride;        /* s_0: the stride of the reference schedule      */
   int32_t kv_dtype;          /* RKV_F32 or RKV_BF16: input kv rows             */
   int32_t out_dtype;         /* RKV_F32 or RKV_BF16: restored K and V          */
   double rope_base;          /* theta_j = rope_base^(-2j/D)                    */
   int32_t batch;             /* number of sequences B                          */
   int32_t max_tokens;        /* T_cap: positions per sequence                  */
-  int32_t max_refs;          /* R_cap: pool slots per sequence (>= ceil(T_cap/s)) */
+  int32_t max_refs;          /* R_cap: pool slots per sequence, at least the
+                                schedule's positions below T_cap (0 = exactly
+                                that many)                                    */
   int32_t max_rows;          /* rows one compress pass handles (0 = 32768);
                                 larger calls are processed in passes          */
+  double ref_alpha;          /* alpha >= 0: growth of the dynamic stride (0 =
+                                fixed stride)                                 */
+  int32_t ref_sink;          /* n_sink >= 0: sink tokens                       */
 } rkv_config;
+/*
+ * Reference schedule (ResidualKV notes §2.6): a position is a reference iff it
+ * is one of the sink tokens 0 .. n_sink-1 or one of p_0 = n_sink,
+ * p_{m+1} = p_m + s_0 + floor(alpha * (p_m - n_sink)) (the product in binary64).
+ * alpha = 0, n_sink = 0 is the fixed stride: pos % s_0 == 0.  Pool slot m of a
+ * sequence holds its m-th reference position.
+ */
 
 /*
  * Cache storage, allocated by the caller on the device and zero-filled or
@@ -139,13 +151,13 @@ rkv_status rkv_create(const rkv_config* cfg, const void* Wc1, const void* Wc2,
 
 /*
  * Append reference tokens to their sequences' pools (ResidualKV notes §2.6
- * fixed stride; §2.4 and §3.3: references are stored directly, in FP8).
+ * reference schedule; §2.4 and §3.3: references are stored directly, in FP8).
  *   kv (device) rows of 2*d_k elements of cfg.kv_dtype; row r of the call
  *     reads kv + src_rows[r] * kv_row_stride (src_rows NULL: row r).
- *   src_rows, seq, pos (host) [n]; every pos must satisfy pos % s == 0, and
- *     per sequence the positions must continue the sequence's references in
- *     order (slot = pos / s).
- * Writes pool_fp8/pool_bf16/pool_norm2/pool_pos at slot pos/s and the
+ *   src_rows, seq, pos (host) [n]; every pos must be a position of the
+ *     schedule (see rkv_config), and per sequence the positions must continue
+ *     the sequence's references in order (slot m = the m-th schedule position).
+ * Writes pool_fp8/pool_bf16/pool_norm2/pool_pos at the position's slot and the
  * token's own row: ref_idx = [slot, -1, ...], codes = 0, meta = 0.
  * Errors (nothing launched): RKV_EINVAL (range, not a reference position,
  * out of order), RKV_ECAPACITY (slot >= R_cap).

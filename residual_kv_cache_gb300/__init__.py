@@ -43,7 +43,8 @@ class _Config(ctypes.Structure):
                 ("ref_stride", ctypes.c_int32), ("kv_dtype", ctypes.c_int32),
                 ("out_dtype", ctypes.c_int32), ("rope_base", ctypes.c_double),
                 ("batch", ctypes.c_int32), ("max_tokens", ctypes.c_int32),
-                ("max_refs", ctypes.c_int32), ("max_rows", ctypes.c_int32)]
+                ("max_refs", ctypes.c_int32), ("max_rows", ctypes.c_int32),
+                ("ref_alpha", ctypes.c_double), ("ref_sink", ctypes.c_int32)]
 
 
 class _Storage(ctypes.Structure):
@@ -141,15 +142,17 @@ class Config:
     rope_base: float = 10000.0
     batch: int = 1
     max_tokens: int = 32768
-    max_refs: int = 0          # 0 -> ceil(max_tokens / ref_stride)
+    max_refs: int = 0          # 0 -> the schedule's positions below max_tokens
     max_rows: int = 0
+    ref_alpha: float = 0.0     # dynamic-stride growth; 0 = fixed stride
+    ref_sink: int = 0          # sink tokens kept as references ahead of the schedule
 
     def to_c(self) -> _Config:
-        max_refs = self.max_refs or -(-self.max_tokens // self.ref_stride)
         return _Config(self.n_kv_heads, self.head_dim, self.d_c, self.d_ff, self.topk,
                        self.group, self.bits, self.ref_stride, _dtype_code(self.kv_dtype),
                        _dtype_code(self.out_dtype), float(self.rope_base), self.batch,
-                       self.max_tokens, max_refs, self.max_rows)
+                       self.max_tokens, self.max_refs, self.max_rows, float(self.ref_alpha),
+                       self.ref_sink)
 
     @property
     def d_kv(self) -> int:
@@ -192,8 +195,9 @@ class Codec:
         self._c = c
         sizes = (ctypes.c_size_t * 7)()
         _check(lib().rkv_storage_bytes(ctypes.byref(c), sizes))
-        B, R, T = c.batch, c.max_refs, c.max_tokens
+        B, T = c.batch, c.max_tokens
         dkv, G = cfg.d_kv, cfg.d_c // cfg.group
+        R = sizes[0] // (B * dkv)                      # pool slots per sequence
         cb = sizes[4] // (B * T)
         dev = self.device
         self.pool_fp8 = torch.empty((B, R, dkv), dtype=torch.uint8, device=dev)

@@ -69,6 +69,20 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
   return r == CUDA_SUCCESS;
 }
 
+// Calls fn(p) for every reference position p < T, in increasing order, and returns
+// their number (ResidualKV notes §2.6): the sink tokens 0 .. sink-1, then p_0 = sink,
+// p_{m+1} = p_m + s0 + floor(alpha * (p_m - sink)), the product taken in binary64.
+template <class F>
+int64_t walk_schedule(int T, int s0, double alpha, int sink, F fn) {
+  int64_t n = 0;
+  for (int p = 0; p < sink && p < T; ++p, ++n) fn(p);
+  for (int64_t p = sink; p < T; ++n) {
+    fn((int)p);
+    p = p + s0 + (int64_t)std::floor(alpha * (double)(p - sink));
+  }
+  return n;
+}
+
 rkv_status derive(const rkv_config* c, Dims* d) {
   if (!c) return fail(RKV_EINVAL, "config is NULL");
   d->N = c->n_kv_heads;
@@ -97,13 +111,23 @@ rkv_status derive(const rkv_config* c, Dims* d) {
   if (d->group != 32) return fail(RKV_EINVAL, "group must be 32");
   if (!(d->bits == 4 || d->bits == 2 || d->bits == 16)) return fail(RKV_EINVAL, "bits must be 4, 2 or 16");
   if (d->stride < 1) return fail(RKV_EINVAL, "ref_stride must be >= 1");
+  if (!(c->ref_alpha >= 0.0 && c->ref_alpha <= 1e6))
+    return fail(RKV_EINVAL, "ref_alpha must be in [0, 1e6]");
+  if (c->ref_sink < 0) return fail(RKV_EINVAL, "ref_sink must be >= 0");
+  d->alpha = c->ref_alpha;
+  d->sink = c->ref_sink;
+  d->fixed = c->ref_alpha == 0.0 && c->ref_sink == 0;
   if (!(c->kv_dtype == RKV_F32 || c->kv_dtype == RKV_BF16) ||
       !(c->out_dtype == RKV_F32 || c->out_dtype == RKV_BF16))
     return fail(RKV_EINVAL, "kv_dtype / out_dtype must be RKV_F32 or RKV_BF16");
   if (!(c->rope_base > 1.0)) return fail(RKV_EINVAL, "rope_base must be > 1");
-  if (d->B < 1 || d->T_cap < 1 || d->R_cap < 1) return fail(RKV_EINVAL, "batch, max_tokens, max_refs must be >= 1");
-  if ((int64_t)d->R_cap < ((int64_t)d->T_cap + d->stride - 1) / d->stride)
-    return fail(RKV_EINVAL, "max_refs must be >= ceil(max_tokens / ref_stride)");
+  if (d->B < 1 || d->T_cap < 1 || d->R_cap < 0)
+    return fail(RKV_EINVAL, "batch and max_tokens must be >= 1, max_refs >= 0");
+  d->n_sched = (int)walk_schedule(d->T_cap, d->stride, d->alpha, d->sink, [](int) {});
+  if (d->R_cap == 0) d->R_cap = d->n_sched;
+  if (d->R_cap < d->n_sched)
+    return fail(RKV_EINVAL, "max_refs %d is below the %d reference positions under max_tokens",
+                d->R_cap, d->n_sched);
   if ((int64_t)d->B * d->T_cap > INT32_MAX || (int64_t)d->B * d->R_cap > INT32_MAX)
     return fail(RKV_EINVAL, "batch * max_tokens too large");
   d->G = d->dc / d->group;
@@ -130,7 +154,6 @@ cudaError_t staging_upload(rkv_ctx* c, int b, int n_ints, cudaStream_t s) {
   return cudaEventRecord(c->plan_copied[b], s);
 }
 
-inline int visible_refs(int pos, int stride) { return (pos - 1) / stride + 1; }
 
 }  // namespace
 
@@ -193,17 +216,26 @@ struct RowScan {
   int max_pos;    // largest position (meaningful when runs == 1)
 };
 
-template <bool kPow2Stride>
-RowScan scan_compress_rows(const rkv::Dims& d, const int32_t* src_rows, const int32_t* seq,
-                           const int32_t* pos, int n) {
+// kSchedule: 0 fixed power-of-two stride, 1 fixed stride, 2 any schedule (ref_before).
+template <int kSchedule>
+RowScan scan_compress_rows(const rkv::Dims& d, const int32_t* ref_before, const int32_t* src_rows,
+                           const int32_t* seq, const int32_t* pos, int n) {
   const unsigned smask = (unsigned)d.stride - 1u;
   unsigned bad = 0, dec = 0;
   int changes = 0, max_pos = 0;
   for (int i = 0; i < n; ++i) {
     const int s = seq[i], p = pos[i];
-    const int off = kPow2Stride ? (int)((unsigned)p & smask) : p % d.stride;
-    bad |= (unsigned)((unsigned)s >= (unsigned)d.B) | (unsigned)((unsigned)p >= (unsigned)d.T_cap) |
-           (unsigned)(off == 0);
+    const unsigned p_bad = (unsigned)p >= (unsigned)d.T_cap;
+    unsigned is_ref;
+    if (kSchedule == 0) {
+      is_ref = ((unsigned)p & smask) == 0;
+    } else if (kSchedule == 1) {
+      is_ref = p % d.stride == 0;
+    } else {
+      const int pc = p_bad ? 0 : p;
+      is_ref = ref_before[pc + 1] != ref_before[pc];
+    }
+    bad |= (unsigned)((unsigned)s >= (unsigned)d.B) | p_bad | is_ref;
     max_pos = p > max_pos ? p : max_pos;
   }
   for (int i = 1; i < n; ++i) {
@@ -220,13 +252,14 @@ RowScan scan_compress_rows(const rkv::Dims& d, const int32_t* src_rows, const in
 bool compress_pools_bad(const rkv_ctx* c, const RowScan& r, const int32_t* seq,
                         const int32_t* pos, int n) {
   const rkv::Dims& d = c->d;
+  // ref_before is non-decreasing, so one sequence needs only its largest position
   if (r.runs == 1) {
-    const int64_t cnt = c->pool_count[seq[0]];
-    return cnt == 0 || (int64_t)r.max_pos > cnt * d.stride;
+    const int cnt = c->pool_count[seq[0]];
+    return cnt == 0 || c->ref_before[r.max_pos] > cnt;
   }
   for (int i = 0; i < n; ++i) {
-    const int64_t cnt = c->pool_count[seq[i]];
-    if (cnt == 0 || (int64_t)pos[i] > cnt * d.stride) return true;
+    const int cnt = c->pool_count[seq[i]];
+    if (cnt == 0 || c->ref_before[pos[i]] > cnt) return true;
   }
   return false;
 }
@@ -241,10 +274,11 @@ rkv_status compress_row_error(const rkv_ctx* c, const int32_t* src_rows, const i
     if (s < 0 || s >= d.B) return fail(RKV_EINVAL, "row %d: seq %d out of range", i, s);
     if (p < 0 || p >= d.T_cap) return fail(RKV_EINVAL, "row %d: pos %d out of range", i, p);
     if (src < 0) return fail(RKV_EINVAL, "row %d: negative source row", i);
-    if (p % d.stride == 0) return fail(RKV_EINVAL, "row %d: pos %d is a reference position", i, p);
+    if (c->ref_before[p + 1] != c->ref_before[p])
+      return fail(RKV_EINVAL, "row %d: pos %d is a reference position", i, p);
     if (c->pool_count[s] == 0) return fail(RKV_EEMPTYPOOL, "row %d: seq %d has no reference", i, s);
-    // the references before p are the ceil(p / s) positions 0, s, 2s, ... < p
-    if ((int64_t)p > (int64_t)c->pool_count[s] * d.stride)
+    // every reference position below p must be in the pool
+    if (c->ref_before[p] > c->pool_count[s])
       return fail(RKV_EINVAL, "row %d: references of seq %d before pos %d are not all appended", i,
                   s, p);
   }
@@ -345,6 +379,9 @@ rkv_status rkv_create(const rkv_config* cfg, const void* Wc1, const void* Wc2, c
   c->plan_ints = std::max(3 * c->m_cap + 4 * c->tiles_cap + 2 * c->units_cap + 2 * c->max_rows,
                           4 * c->max_rows);
   c->pool_count.assign(d.B, 0);
+  c->ref_before.assign((size_t)d.T_cap + 1, 0);
+  walk_schedule(d.T_cap, d.stride, d.alpha, d.sink, [&](int p) { c->ref_before[p + 1] = 1; });
+  for (int p = 0; p < d.T_cap; ++p) c->ref_before[p + 1] += c->ref_before[p];
 
   auto alloc = [&](void** p, size_t bytes) -> cudaError_t { return cudaMalloc(p, bytes); };
   rkv_status fail_status = RKV_OK;
@@ -457,12 +494,13 @@ rkv_status rkv_pool_append(rkv_ctx* c, const void* kv, int64_t kv_row_stride,
     if (s < 0 || s >= d.B) return fail(RKV_EINVAL, "row %d: seq %d out of range", i, s);
     if (p < 0 || p >= d.T_cap) return fail(RKV_EINVAL, "row %d: pos %d out of range", i, p);
     if (src < 0) return fail(RKV_EINVAL, "row %d: negative source row", i);
-    if (p % d.stride != 0) return fail(RKV_EINVAL, "row %d: pos %d is not a reference position", i, p);
-    const int slot = p / d.stride;
+    const int slot = c->ref_before[p];
+    if (c->ref_before[p + 1] == slot)
+      return fail(RKV_EINVAL, "row %d: pos %d is not a reference position", i, p);
     if (slot >= d.R_cap) return fail(RKV_ECAPACITY, "row %d: slot %d >= max_refs", i, slot);
     if (slot != next[s])
-      return fail(RKV_EINVAL, "row %d: seq %d expects the reference at pos %d next, got %d", i, s,
-                  next[s] * d.stride, p);
+      return fail(RKV_EINVAL, "row %d: seq %d expects its reference slot %d next, got pos %d (slot %d)",
+                  i, s, next[s], p, slot);
     next[s] = slot + 1;
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -474,7 +512,7 @@ rkv_status rkv_pool_append(rkv_ctx* c, const void* kv, int64_t kv_row_stride,
       const int k = r0 + i;
       const int s = seq[k], p = pos[k];
       h[4 * i + 0] = src_rows ? src_rows[k] : k;
-      h[4 * i + 1] = s * d.R_cap + p / d.stride;
+      h[4 * i + 1] = s * d.R_cap + c->ref_before[p];
       h[4 * i + 2] = p;
       h[4 * i + 3] = s * d.T_cap + p;
     }
@@ -497,9 +535,10 @@ rkv_status rkv_compress(rkv_ctx* c, const void* kv, int64_t kv_row_stride, const
     return fail(RKV_EINVAL, "kv_row_stride must be >= 2*d_k and a multiple of 8");
   // one branch-free pass over the rows; the row-by-row pass that names the first bad
   // row runs only when it found one
-  const RowScan scan = (d.stride & (d.stride - 1)) == 0
-                           ? scan_compress_rows<true>(d, src_rows, seq, pos, n)
-                           : scan_compress_rows<false>(d, src_rows, seq, pos, n);
+  const int32_t* rb = c->ref_before.data();
+  const RowScan scan = !d.fixed                          ? scan_compress_rows<2>(d, rb, src_rows, seq, pos, n)
+                       : (d.stride & (d.stride - 1)) == 0 ? scan_compress_rows<0>(d, rb, src_rows, seq, pos, n)
+                                                          : scan_compress_rows<1>(d, rb, src_rows, seq, pos, n);
   if (scan.bad || compress_pools_bad(c, scan, seq, pos, n))
     return compress_row_error(c, src_rows, seq, pos, n);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -576,7 +615,7 @@ rkv_status rkv_compress(rkv_ctx* c, const void* kv, int64_t kv_row_stride, const
         const int kend = std::min(j, k + kTileM);
         const int maxpos = fill_tile_rows(h, p, d, src_rows, pos, ord ? ord + k : nullptr, r0 + k,
                                           r0, kend - k, q + (k - i), s);
-        const int nrt = (visible_refs(maxpos, d.stride) + kRefTile - 1) / kRefTile;
+        const int nrt = (c->ref_before[maxpos] + kRefTile - 1) / kRefTile;
         tseq.push_back(s);
         trow0.push_back(q + (k - i));
         tnrt.push_back(nrt);

@@ -25,6 +25,10 @@ struct Dims {
   int G;           // groups per token
   int code_bytes;  // bytes of one packed code row
   int B, T_cap, R_cap;
+  double alpha;    // dynamic schedule growth (0: fixed stride)
+  int sink;        // sink tokens
+  int fixed;       // the schedule is pos % stride == 0
+  int n_sched;     // schedule positions below T_cap
   int kv_f32, out_f32;
   int parts;       // 3 bf16 pieces per fp32 query element, 1 for bf16
   int n_hi;        // rows of the high RoPE table
@@ -86,6 +90,7 @@ struct rkv_ctx {
 
   // host mirror of each sequence's pool fill
   std::vector<int32_t> pool_count;
+  std::vector<int32_t> ref_before;   // [T_cap + 1]: schedule positions below p
 
   // instrumentation
   bool timing = false;

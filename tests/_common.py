@@ -10,9 +10,9 @@ from oracle import codec as C
 from oracle import formats as F
 
 
-def oracle_shape(w: synth.Workload) -> C.Shape:
+def oracle_shape(w: synth.Workload, alpha: float = 0.0, sink: int = 0) -> C.Shape:
     return C.Shape(w.n_kv_heads, w.head_dim, w.d_c, w.d_ff, w.topk, w.group, w.bits, w.stride,
-                   w.rope_base)
+                   w.rope_base, alpha, sink)
 
 
 def np64(t: torch.Tensor) -> np.ndarray:
@@ -31,23 +31,27 @@ def device_bytes(ptr: int, nbytes: int) -> torch.Tensor:
 
 
 def make_codec(w: synth.Workload, W: dict, T: int, batch: int = 1, max_rows: int = 0,
-               out_dtype: str | None = None, bits: int | None = None):
+               out_dtype: str | None = None, bits: int | None = None, alpha: float = 0.0,
+               sink: int = 0):
     from residual_kv_cache_gb300 import Codec, Config
     cfg = Config(n_kv_heads=w.n_kv_heads, head_dim=w.head_dim, d_c=w.d_c, d_ff=w.d_ff,
                  topk=w.topk, group=w.group, bits=w.bits if bits is None else bits,
                  ref_stride=w.stride, kv_dtype=w.kv_dtype,
                  out_dtype=out_dtype or w.out_dtype, rope_base=w.rope_base, batch=batch,
-                 max_tokens=T, max_rows=max_rows)
+                 max_tokens=T, max_rows=max_rows, ref_alpha=alpha, ref_sink=sink)
     Wd = {k: v.cuda().contiguous() for k, v in W.items()}
     return Codec(cfg, Wd)
 
 
-def gpu_prefill(codec, kv_dev: torch.Tensor, stride: int, seq_id: int = 0):
-    """Write every position of one sequence: references to the pool, the rest encoded."""
+def gpu_prefill(codec, kv_dev: torch.Tensor, stride: int, seq_id: int = 0, alpha: float = 0.0,
+                sink: int = 0):
+    """Write every position of one sequence: references (the schedule's positions) to
+    the pool, the rest encoded."""
     T = kv_dev.shape[0]
     pos = np.arange(T, dtype=np.int32)
-    ref = pos[pos % stride == 0]
-    non = pos[pos % stride != 0]
+    isref = C.is_reference(pos, stride, alpha, sink)
+    ref = pos[isref]
+    non = pos[~isref]
     codec.pool_append(kv_dev, np.full(len(ref), seq_id, np.int32), ref, src_rows=ref)
     codec.compress(kv_dev, np.full(len(non), seq_id, np.int32), non, src_rows=non)
     return ref, non

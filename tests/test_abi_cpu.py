@@ -44,10 +44,27 @@ def test_storage_bytes_and_config_validation(built):
     assert s[0] == 2048 * 2048 and s[1] == 2048 * 2048 * 2
     assert s[4] == 32768 * 256 and s[5] == 32768 * 16 * 4 and s[6] == 32768 * 4 * 4
     for bad in (dict(head_dim=96), dict(d_c=100), dict(d_c=576), dict(bits=3), dict(topk=5), dict(d_ff=200),
-                dict(group=16), dict(max_refs=10)):
+                dict(group=16), dict(max_refs=10), dict(ref_alpha=-0.1), dict(ref_sink=-1),
+                dict(ref_alpha=float("nan")), dict(ref_alpha=0.02, ref_sink=4, max_refs=100)):
         with pytest.raises(rkv.RkvError) as e:
             rkv.storage_bytes(rkv.Config(**{**cfg.__dict__, **bad}))
         assert e.value.status == -1
+
+
+def test_pool_size_follows_the_reference_schedule(built):
+    """max_refs = 0 sizes the pool to the schedule's positions below max_tokens
+    (ResidualKV notes §2.6), the count the oracle's schedule gives."""
+    import residual_kv_cache_gb300 as rkv
+    from oracle import codec as C
+    for T, s, alpha, sink in ((32768, 16, 0.0, 0), (1000, 10, 0.0, 0), (262144, 10, 0.02, 0),
+                              (262144, 10, 0.001, 4), (4096, 16, 0.02, 4), (300, 8, 5.0, 16)):
+        cfg = rkv.Config(n_kv_heads=8, head_dim=128, d_c=512, d_ff=1536, ref_stride=s,
+                         max_tokens=T, ref_alpha=alpha, ref_sink=sink)
+        R = len(C.reference_positions(T, s, alpha, sink))
+        assert rkv.storage_bytes(cfg)[0] == R * 2048, (T, s, alpha, sink)
+        # an explicit capacity at least that large is kept as given
+        big = rkv.Config(**{**cfg.__dict__, "max_refs": R + 7})
+        assert rkv.storage_bytes(big)[0] == (R + 7) * 2048
 
 
 def test_null_context_is_rejected(built):

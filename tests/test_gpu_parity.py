@@ -29,16 +29,16 @@ def _weights64(W):
     return {k: np64(v) for k, v in W.items()}
 
 
-def _run(name, T, seed_kv=11, seed_w=12, **kw):
+def _run(name, T, seed_kv=11, seed_w=12, alpha=0.0, sink=0, **kw):
     w = synth.workload(name)
     kv = synth.gen_kv(w, seed_kv, T=T)
     W = synth.gen_weights(w, seed_w)
-    codec = make_codec(w, W, T=T, **kw)
+    codec = make_codec(w, W, T=T, alpha=alpha, sink=sink, **kw)
     kv_dev = kv.cuda()
-    ref, non = gpu_prefill(codec, kv_dev, w.stride)
+    ref, non = gpu_prefill(codec, kv_dev, w.stride, alpha=alpha, sink=sink)
     torch.cuda.synchronize()
     assert codec.get_status() == 0
-    sh = oracle_shape(w)
+    sh = oracle_shape(w, alpha, sink)
     if "bits" in kw and kw["bits"] is not None:
         sh = C.Shape(**{**sh.__dict__, "bits": kw["bits"]})
     kv64 = np64(kv)
@@ -58,6 +58,18 @@ def llama():
     return _run("llama8b", 4096)
 
 
+# the dynamic-stride schedule of ResidualKV notes §2.6 (gaps growing with the
+# position, sink tokens kept as references)
+@pytest.fixture(scope="module")
+def tiny_dyn():
+    return _run("tiny", 256, alpha=0.1, sink=2)
+
+
+@pytest.fixture(scope="module")
+def llama_dyn():
+    return _run("llama8b", 4096, alpha=0.02, sink=4)
+
+
 def _check_pool(r):
     c, st = r["codec"], r["store"]
     R = len(st.pool.pos)
@@ -74,7 +86,7 @@ def _check_pool(r):
 
 
 @cuda
-@pytest.mark.parametrize("name", ["tiny", "llama"])
+@pytest.mark.parametrize("name", ["tiny", "llama", "tiny_dyn", "llama_dyn"])
 def test_pool_append_bit_exact(name, request):
     _check_pool(request.getfixturevalue(name))
 
@@ -91,7 +103,7 @@ def _check_idx(r):
 
 
 @cuda
-@pytest.mark.parametrize("name", ["tiny", "llama"])
+@pytest.mark.parametrize("name", ["tiny", "llama", "tiny_dyn", "llama_dyn"])
 def test_retrieval_parity(name, request):
     n_exact, n_swap = _check_idx(request.getfixturevalue(name))
     assert n_swap <= max(2, 0.001 * (n_exact + n_swap))
@@ -105,7 +117,7 @@ def _same_idx_rows(r):
 
 
 @cuda
-@pytest.mark.parametrize("name", ["tiny", "llama"])
+@pytest.mark.parametrize("name", ["tiny", "llama", "tiny_dyn", "llama_dyn"])
 def test_encoder_operand_rows_bit_exact(name, request):
     r = request.getfixturevalue(name)
     c, st, w = r["codec"], r["store"], r["w"]
@@ -122,7 +134,7 @@ def test_encoder_operand_rows_bit_exact(name, request):
 
 
 @cuda
-@pytest.mark.parametrize("name", ["tiny", "llama"])
+@pytest.mark.parametrize("name", ["tiny", "llama", "tiny_dyn", "llama_dyn"])
 def test_swiglu_hidden_rows(name, request):
     r = request.getfixturevalue(name)
     c, st, w = r["codec"], r["store"], r["w"]
@@ -161,7 +173,7 @@ def _codes_check(r, rows, bits=None):
 
 
 @cuda
-@pytest.mark.parametrize("name", ["tiny", "llama"])
+@pytest.mark.parametrize("name", ["tiny", "llama", "tiny_dyn", "llama_dyn"])
 def test_codes_parity(name, request):
     r = request.getfixturevalue(name)
     c, st, sh = r["codec"], r["store"], r["sh"]
@@ -169,7 +181,7 @@ def test_codes_parity(name, request):
 
 
 @cuda
-@pytest.mark.parametrize("name", ["tiny", "llama"])
+@pytest.mark.parametrize("name", ["tiny", "llama", "tiny_dyn", "llama_dyn"])
 def test_reconstruct_end_to_end(name, request):
     r = request.getfixturevalue(name)
     c, st, w = r["codec"], r["store"], r["w"]
