@@ -35,6 +35,31 @@ WORKLOAD = "llama8b"
 METRIC = "KV tokens compressed/s + selected tokens reconstructed/s"
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# reference schedule (ResidualKV notes section 2.6): alpha = 0, n_sink = 0 is the fixed
+# stride of the workload; --alpha / --sink time the dynamic stride instead
+SCHEDULE = {"alpha": 0.0, "sink": 0}
+
+
+def schedule_note(w) -> str:
+    if SCHEDULE["alpha"] == 0.0 and SCHEDULE["sink"] == 0:
+        return f"stride {w.stride}"
+    return (f"dynamic stride s_0={w.stride}, alpha={SCHEDULE['alpha']}, "
+            f"n_sink={SCHEDULE['sink']}")
+
+
+def codec_config(rkv, w, T):
+    return rkv.Config(n_kv_heads=w.n_kv_heads, head_dim=w.head_dim, d_c=w.d_c, d_ff=w.d_ff,
+                      topk=w.topk, group=w.group, bits=w.bits, ref_stride=w.stride,
+                      kv_dtype=w.kv_dtype, out_dtype=w.out_dtype, rope_base=w.rope_base,
+                      max_tokens=T, ref_alpha=SCHEDULE["alpha"], ref_sink=SCHEDULE["sink"])
+
+
+def split_positions(ref_pos, T):
+    """Reference positions (from the schedule) and all the other positions below T."""
+    pos = np.arange(T, dtype=np.int32)
+    isref = np.zeros(T, dtype=bool)
+    isref[ref_pos] = True
+    return pos[isref], pos[~isref]
 
 
 def load_peaks():
@@ -75,16 +100,21 @@ def reduce_sum(value: float, world: int, device=None) -> float:
 
 
 # ------------------------------------------------------------------ work accounting
-def algorithmic_work(w, n_comp: int, n_sel: int) -> dict:
+def algorithmic_work(w, n_comp: int, n_sel: int, ref_pos) -> dict:
     """Flops and bytes the method itself needs, per kernel launch of one step."""
     dkv, dff, dc = w.d_kv, w.d_ff, w.d_c
-    n_ref = -(-w.T // w.stride)
+    ref_pos = np.asarray(ref_pos, dtype=np.int64)
+    n_ref = len(ref_pos)
     n_non = n_comp - n_ref
     code_b = dc * w.bits // 8 if w.bits != 16 else 2 * dc
     meta_b = 0 if w.bits == 16 else 4 * (dc // 32)
     idx_b = 4 * w.topk
     out_b = 4 if w.out_dtype == "fp32" else 2
-    avg_pool = sum((p - 1) // w.stride + 1 for p in range(w.T) if p % w.stride) / max(n_non, 1)
+    # references visible to each non-reference token (those at earlier positions)
+    before = np.searchsorted(ref_pos, np.arange(w.T), side="left")
+    isref = np.zeros(w.T, dtype=bool)
+    isref[ref_pos] = True
+    avg_pool = float(before[~isref].sum()) / max(n_non, 1)
     return {
         "rkv_gemm12_swiglu_kernel": {"flops": 2.0 * (2 * n_non) * (2 * dff) * dkv,
                                      "bytes": 2 * n_non * dkv * 2 + 2 * dff * dkv * 2
@@ -198,13 +228,10 @@ def run_cuda(args):
     seed = 1000 * (rank + 1)
     kv = synth.gen_kv(w, seed).to(dev)
     W = {k: v.to(dev) for k, v in synth.gen_weights(w, seed + 1).items()}
-    cfg = rkv.Config(n_kv_heads=w.n_kv_heads, head_dim=w.head_dim, d_c=w.d_c, d_ff=w.d_ff,
-                     topk=w.topk, group=w.group, bits=w.bits, ref_stride=w.stride,
-                     kv_dtype=w.kv_dtype, out_dtype=w.out_dtype, rope_base=w.rope_base,
-                     max_tokens=T)
+    cfg = codec_config(rkv, w, T)
     codec = rkv.Codec(cfg, W, device=dev)
-    pos = np.arange(T, dtype=np.int32)
-    ref, non = pos[pos % w.stride == 0], pos[pos % w.stride != 0]
+    ref_pos = rkv.reference_positions(cfg)
+    ref, non = split_positions(ref_pos, T)
     zeros_ref, zeros_non = np.zeros_like(ref), np.zeros_like(non)
     sels = [synth.gen_selection(T, n_sel, seed + 10 + s).to(dev) for s in range(steps_dec)]
     seq0 = torch.zeros(n_sel, dtype=torch.int32, device=dev)
@@ -276,7 +303,7 @@ def run_cuda(args):
 
     # ---- roofline of the dominant kernel
     peaks, peaks_kind = load_peaks()
-    work = algorithmic_work(w, T, n_sel)
+    work = algorithmic_work(w, T, n_sel, ref_pos)
     rows = {}
     for k, (n, ms) in per_k.items():
         if k not in work or n == 0:
@@ -306,7 +333,7 @@ def run_cuda(args):
                         "traffic": measured_traffic(dom), "peak_kind": f"{peaks_kind} copy"}
 
     # ---- end-to-end through the public API with host buffers
-    e2e = run_e2e(args, codec, kv, sels, w, dev, stream, barrier, world)
+    e2e = run_e2e(args, codec, kv, sels, w, dev, stream, barrier, world, ref, non)
 
     out = {
         "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
@@ -314,7 +341,7 @@ def run_cuda(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
         "config": {"workload": f"{WORKLOAD}: Llama-3.1-8B-shaped layer, T={T}, 2d_k={w.d_kv}, "
-                               f"d_c={w.d_c}, d_ff={w.d_ff}, stride {w.stride}, INT{w.bits}, "
+                               f"d_c={w.d_c}, d_ff={w.d_ff}, {schedule_note(w)}, INT{w.bits}, "
                                f"prefill write + {steps_dec} decode steps x {n_sel} restored",
                    "tokens_per_step": tokens_step, "l2": "flushed before every timed step",
                    "parallelism": f"replicas x{world} (independent sequences)"},
@@ -336,7 +363,7 @@ def run_cuda(args):
         dist.destroy_process_group()
 
 
-def run_e2e(args, codec, kv_dev, sels_dev, w, dev, stream, barrier, world):
+def run_e2e(args, codec, kv_dev, sels_dev, w, dev, stream, barrier, world, ref, non):
     """Public-API path with host buffers: H2D of the step's inputs, D2H of its result."""
     import torch
     T, n_sel = w.T, w.n_sel
@@ -347,8 +374,6 @@ def run_e2e(args, codec, kv_dev, sels_dev, w, dev, stream, barrier, world):
     k_host = torch.empty((n_sel, w.n_kv_heads, w.head_dim), dtype=torch.bfloat16).pin_memory()
     v_host = torch.empty_like(k_host).pin_memory()
     seq0 = torch.zeros(n_sel, dtype=torch.int32, device=dev)
-    pos = np.arange(T, dtype=np.int32)
-    ref, non = pos[pos % w.stride == 0], pos[pos % w.stride != 0]
 
     def step():
         kv_buf.copy_(kv_host, non_blocking=True)
@@ -393,12 +418,12 @@ def cpu_baseline(budget_s: float = 15.0) -> dict:
     kv = synth.gen_kv(w, 1000).to(torch.float64).numpy()
     W = {k: v.to(torch.float64).numpy() for k, v in synth.gen_weights(w, 1001).items()}
     sh = C.Shape(w.n_kv_heads, w.head_dim, w.d_c, w.d_ff, w.topk, w.group, w.bits, w.stride,
-                 w.rope_base)
+                 w.rope_base, SCHEDULE["alpha"], SCHEDULE["sink"])
     t0 = time.perf_counter()
-    pool = C.build_pool(kv, w.T, w.stride)
+    pool = C.build_pool(kv, w.T, w.stride, sh.ref_alpha, sh.ref_sink)
     t_pool = time.perf_counter() - t0
     rng = np.random.default_rng(0)
-    nonref = np.nonzero(np.arange(w.T) % w.stride)[0]
+    nonref = np.nonzero(~C.is_reference(np.arange(w.T), w.stride, sh.ref_alpha, sh.ref_sink))[0]
     # compress sample: batches of 64 tokens until half the budget is used
     n_c, t_c = 0, 0.0
     enc_q, enc_meta, enc_idx, enc_pos = [], [], [], []
@@ -427,11 +452,17 @@ def cpu_baseline(budget_s: float = 15.0) -> dict:
     tokens = w.T + w.steps * w.n_sel
     t_step = per_c * w.T + per_r * w.steps * w.n_sel
     return {"value": round(tokens / t_step, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{n_c} compressed tokens (random non-reference positions, full 2048-reference "
-                      f"pool) and {n_r} restored tokens of the {WORKLOAD} workload, scaled to the "
+            "sample": f"{n_c} compressed tokens (random non-reference positions, full "
+                      f"{len(pool.pos)}-reference pool, {schedule_note(w)}) and {n_r} restored "
+                      f"tokens of the {WORKLOAD} workload, scaled to the "
                       f"step mix ({w.T} written + {w.steps}x{w.n_sel} restored)",
             "compress_tok_s": round(1 / per_c, 2), "reconstruct_tok_s": round(1 / per_r, 2),
             "seconds": round(t_c + t_r + t_pool, 2)}
+
+
+def _workload():
+    import synth
+    return synth.workload(WORKLOAD)
 
 
 def run_reference(args):
@@ -450,7 +481,9 @@ def run_reference(args):
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tokens / v * 1e3, 1),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic", "impl": "reference",
-           "config": {"workload": f"{WORKLOAD} (oracle on bounded samples)"},
+           "config": {"workload": f"{WORKLOAD} (oracle on bounded samples)"
+                                  + ("" if SCHEDULE == {"alpha": 0.0, "sink": 0}
+                                     else f", {schedule_note(_workload())}")},
            "cpu_baseline": {"value": round(v, 2), "unit": UNIT, "cores": last["cores"],
                             "kind": "oracle", "sample": last["sample"]},
            "e2e": {"value": round(v, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -473,12 +506,9 @@ def run_kernel_case(args):
     dev = torch.device("cuda", 0)
     kv = synth.gen_kv(w, 1000).to(dev)
     W = {k: v.to(dev) for k, v in synth.gen_weights(w, 1001).items()}
-    cfg = rkv.Config(n_kv_heads=w.n_kv_heads, head_dim=w.head_dim, d_c=w.d_c, d_ff=w.d_ff,
-                     bits=w.bits, ref_stride=w.stride, kv_dtype=w.kv_dtype,
-                     out_dtype=w.out_dtype, rope_base=w.rope_base, max_tokens=w.T)
+    cfg = codec_config(rkv, w, w.T)
     codec = rkv.Codec(cfg, W, device=dev)
-    pos = np.arange(w.T, dtype=np.int32)
-    ref, non = pos[pos % w.stride == 0], pos[pos % w.stride != 0]
+    ref, non = split_positions(rkv.reference_positions(cfg), w.T)
     codec.pool_append(kv, np.zeros_like(ref), ref, src_rows=ref)
     codec.compress(kv, np.zeros_like(non), non, src_rows=non)
     zero = torch.zeros(w.n_sel, dtype=torch.int32, device=dev)
@@ -498,12 +528,18 @@ def main():
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
+    ap.add_argument("--alpha", type=float, default=0.0,
+                    help="dynamic-stride growth of the reference schedule (0: fixed stride)")
+    ap.add_argument("--sink", type=int, default=0, help="sink tokens of the reference schedule")
     ap.add_argument("--cpu-seconds", type=float, default=16.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel-case", action="store_true",
                     help="run one prefill and two restores, for kernel captures")
     ap.add_argument("--tokens", type=int, default=0, help="override T for --kernel-case")
     args = ap.parse_args()
+    if args.alpha < 0 or args.sink < 0:
+        ap.error("--alpha and --sink must be >= 0")
+    SCHEDULE.update(alpha=float(args.alpha), sink=int(args.sink))
     if args.kernel_case:
         run_kernel_case(args)
     elif args.impl == "reference":

@@ -131,6 +131,18 @@ typedef struct {
 /* Byte sizes of the seven storage tensors, in the order of rkv_storage. */
 rkv_status rkv_storage_bytes(const rkv_config* cfg, size_t sizes[7]);
 
+/*
+ * The reference positions of cfg's schedule below max_tokens (ResidualKV notes
+ * §2.6; see rkv_config), in increasing order: the positions a caller passes to
+ * rkv_pool_append, every other position going to rkv_compress.
+ *   pos (host, caller-owned) receives the first min(capacity, count) positions;
+ *   it may be NULL when capacity is 0.  *count (host) receives their number.
+ * Errors: RKV_EINVAL (invalid cfg, capacity < 0, NULL count or NULL pos with
+ * capacity > 0).  No device work.
+ */
+rkv_status rkv_reference_positions(const rkv_config* cfg, int32_t* pos, int32_t capacity,
+                                   int32_t* count);
+
 typedef struct rkv_ctx rkv_ctx;
 
 /*

@@ -63,6 +63,8 @@ class _Timing(ctypes.Structure):
 _P, _I32, _I64 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64
 ABI_FUNCTIONS = {
     "rkv_storage_bytes": (_I32, [ctypes.POINTER(_Config), ctypes.POINTER(ctypes.c_size_t)]),
+    "rkv_reference_positions": (_I32, [ctypes.POINTER(_Config), ctypes.POINTER(_I32), _I32,
+                                       ctypes.POINTER(_I32)]),
     "rkv_create": (_I32, [ctypes.POINTER(_Config), _P, _P, _P, _P, ctypes.POINTER(_Storage), _P,
                           ctypes.POINTER(_P)]),
     "rkv_pool_append": (_I32, [_P, _P, _I64, _P, _P, _P, _I32, _P]),
@@ -164,6 +166,18 @@ def storage_bytes(cfg: Config):
     c = cfg.to_c()
     _check(lib().rkv_storage_bytes(ctypes.byref(c), sizes))
     return list(sizes)
+
+
+def reference_positions(cfg: Config) -> np.ndarray:
+    """The schedule's reference positions below cfg.max_tokens (int32, increasing)."""
+    c = cfg.to_c()
+    n = _I32(0)
+    _check(lib().rkv_reference_positions(ctypes.byref(c), None, 0, ctypes.byref(n)))
+    out = np.empty(n.value, dtype=np.int32)
+    _check(lib().rkv_reference_positions(ctypes.byref(c),
+                                         out.ctypes.data_as(ctypes.POINTER(_I32)), n.value,
+                                         ctypes.byref(n)))
+    return out
 
 
 def retrieve_noalloc(queries, q_pos, pool, pool_norm2, pool_pos, topk: int = 4, out=None,

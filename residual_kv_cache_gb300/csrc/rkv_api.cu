@@ -333,6 +333,22 @@ extern "C" {
 
 const char* rkv_last_error(void) { return g_err.c_str(); }
 
+rkv_status rkv_reference_positions(const rkv_config* cfg, int32_t* pos, int32_t capacity,
+                                   int32_t* count) {
+  if (!count) return fail(RKV_EINVAL, "count is NULL");
+  if (capacity < 0 || (capacity > 0 && !pos)) return fail(RKV_EINVAL, "bad pos / capacity");
+  Dims d;
+  const rkv_status st = derive(cfg, &d);
+  if (st != RKV_OK) return st;
+  int32_t n = 0;
+  walk_schedule(d.T_cap, d.stride, d.alpha, d.sink, [&](int p) {
+    if (n < capacity) pos[n] = p;
+    ++n;
+  });
+  *count = n;
+  return RKV_OK;
+}
+
 rkv_status rkv_storage_bytes(const rkv_config* cfg, size_t sizes[7]) {
   Dims d;
   rkv_status st = derive(cfg, &d);

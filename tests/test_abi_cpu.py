@@ -67,6 +67,24 @@ def test_pool_size_follows_the_reference_schedule(built):
         assert rkv.storage_bytes(big)[0] == (R + 7) * 2048
 
 
+def test_library_schedule_equals_the_oracle_schedule(built):
+    """The positions the library tells callers to append as references are the
+    oracle's schedule (ResidualKV notes §2.6), fixed and dynamic."""
+    import residual_kv_cache_gb300 as rkv
+    from oracle import codec as C
+    for T, s, alpha, sink in ((256, 8, 0.0, 0), (32768, 16, 0.0, 0), (1000, 10, 0.1, 4),
+                              (261885, 10, 0.02, 0), (261885, 10, 0.001, 0), (4096, 16, 0.02, 4),
+                              (50, 7, 0.0, 60), (10000, 3, 0.7, 1)):
+        cfg = rkv.Config(n_kv_heads=8, head_dim=128, d_c=512, d_ff=1536, ref_stride=s,
+                         max_tokens=T, ref_alpha=alpha, ref_sink=sink)
+        got = rkv.reference_positions(cfg)
+        assert got.tolist() == C.reference_positions(T, s, alpha, sink).tolist(), (T, s, alpha, sink)
+    L = rkv.lib()
+    n = rkv._I32(0)
+    assert L.rkv_reference_positions(None, None, 0, rkv.ctypes.byref(n)) == -1
+    assert L.rkv_reference_positions(rkv.ctypes.byref(cfg.to_c()), None, 5, rkv.ctypes.byref(n)) == -1
+
+
 def test_null_context_is_rejected(built):
     import residual_kv_cache_gb300 as rkv
     L = rkv.lib()
