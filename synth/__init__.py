@@ -20,6 +20,9 @@ Workloads (the synthetic stand-ins for the page's model KV caches):
                 sequence per step, 30 % of each history read per step.
 * ``long_int2`` Llama layer shape, T=262144, INT2; ``long_bf16z`` the same
                 distribution at T=65536 with quantisation off (bf16 z).
+* ``t1_*``      the codec shapes of Table I (section 3.1): Qwen2.5-7B (2d_k=1024,
+                d_c=384, d_ff=3072), Qwen3-VL-8B (2048, 384, 3072), Qwen2.5-32B
+                (2048, 512, 4096); llama8b's input distribution, T=8192.
 """
 from __future__ import annotations
 
@@ -78,6 +81,14 @@ WORKLOADS = {
                           "bf16", 64, 0.25, True, 5e5, steps=16),
     "long_bf16z": Workload("long_bf16z", 8, 128, 512, 1536, 65536, 16, 16, "bf16",
                            "bf16", 64, 0.25, True, 5e5, steps=16),
+    # the codec shapes of the page's Table I (2d_k, d_c, d_ff), with the llama8b
+    # input distribution
+    "t1_qwen25_7b": Workload("t1_qwen25_7b", 4, 128, 384, 3072, 8192, 16, 4, "bf16", "bf16",
+                             64, 0.25, True, 1e6),
+    "t1_qwen3vl_8b": Workload("t1_qwen3vl_8b", 8, 128, 384, 3072, 8192, 16, 4, "bf16", "bf16",
+                              64, 0.25, True, 5e6),
+    "t1_qwen25_32b": Workload("t1_qwen25_32b", 8, 128, 512, 4096, 8192, 16, 4, "bf16", "bf16",
+                              64, 0.25, True, 1e6),
 }
 
 

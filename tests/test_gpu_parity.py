@@ -58,6 +58,38 @@ def llama():
     return _run("llama8b", 4096)
 
 
+# the codec shapes of the page's Table I (d_c = 384 / 512, d_ff = 3072 / 4096)
+@pytest.fixture(scope="module")
+def t1_qwen25_7b():
+    return _run("t1_qwen25_7b", 2048)
+
+
+@pytest.fixture(scope="module")
+def t1_qwen25_32b():
+    return _run("t1_qwen25_32b", 2048)
+
+
+@cuda
+@pytest.mark.parametrize("name", ["t1_qwen25_7b", "t1_qwen25_32b"])
+def test_table1_shapes_parity(name, request):
+    """Pool, retrieval, codes and the end-to-end restore at Table I's codec shapes."""
+    r = request.getfixturevalue(name)
+    _check_pool(r)
+    n_exact, n_swap = _check_idx(r)
+    assert n_swap <= max(2, 0.001 * (n_exact + n_swap))
+    _codes_check(r, _same_idx_rows(r))
+    c, st, T = r["codec"], r["store"], r["T"]
+    sel = synth.gen_selection(T, int(round(0.3 * T)), 23)
+    K, V = c.reconstruct(torch.zeros_like(sel).cuda(), sel.cuda())
+    torch.cuda.synchronize()
+    assert c.get_status() == 0
+    Ko, Vo, _ = C.reconstruct(st, sel.numpy().astype(np.int64), r["W64"], "operand")
+    same = np.all(c.ref_idx[0].cpu().numpy()[sel.numpy()] == st.idx[sel.numpy()], axis=1)
+    assert same.mean() > 0.9
+    assert rel_fro(np64(K)[same], Ko[same]) <= 1e-2
+    assert rel_fro(np64(V)[same], Vo[same]) <= 1e-2
+
+
 # the dynamic-stride schedule of ResidualKV notes §2.6 (gaps growing with the
 # position, sink tokens kept as references)
 @pytest.fixture(scope="module")
