@@ -1,0 +1,50 @@
+"""Sparse attention over restored K/V, written out in float64.
+
+Test infrastructure, like the rest of ``oracle/``: only ``tests/``,
+``__graft_entry__.smoke()`` and the CPU legs of ``bench.py`` may import it.  It
+shares no code with the CUDA library.
+
+ResidualKV notes, section 2.7 (the OmniKV combination): a sparse layer restores
+only the selected tokens I_t and computes
+
+    o = softmax(q K_hat[I_t]^T / sqrt(D)) V_hat[I_t]
+
+for the current query q.  Readings of what the section leaves open:
+* grouped-query attention as in the Llama / Qwen models the page uses: with H_q
+  query heads and N key/value heads, query head h reads key/value head
+  h // (H_q / N);
+* q arrives already rotated at the decode position (the restored K_hat is rotated
+  at each token's own position);
+* the softmax runs over exactly the selected tokens, with no mask or sink beyond
+  them.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+__all__ = ["sparse_attention"]
+
+
+def sparse_attention(q, K, V):
+    """q [H_q, D]; K, V [n, N, D] (the restored rows of the selected tokens).
+
+    Returns o [H_q, D] in float64.  An empty selection (n = 0) has no softmax and
+    is rejected.
+    """
+    q = np.asarray(q, np.float64)
+    K = np.asarray(K, np.float64)
+    V = np.asarray(V, np.float64)
+    n, N, D = K.shape
+    Hq = q.shape[0]
+    if n == 0:
+        raise ValueError("softmax over an empty selection")
+    if q.shape[1] != D or Hq % N != 0:
+        raise ValueError("q must be [H_q, D] with H_q a multiple of N")
+    group = Hq // N
+    out = np.empty((Hq, D))
+    for h in range(Hq):
+        g = h // group
+        s = K[:, g, :] @ q[h] / np.sqrt(D)           # [n] scores
+        w = np.exp(s - s.max())
+        out[h] = (w / w.sum()) @ V[:, g, :]
+    return out
