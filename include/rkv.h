@@ -206,6 +206,23 @@ rkv_status rkv_reconstruct(rkv_ctx* ctx, const int32_t* seq, const int32_t* pos,
                            int32_t n_sel, void* k_out, void* v_out, void* stream);
 
 /*
+ * Sparse-layer attention over restored K/V (ResidualKV notes §2.7, the output
+ * equation o = softmax(q K_hat^T / sqrt(D)) V_hat over the selected tokens I_t).
+ *   q (device, fp32) [n_q_heads, D]: the decode query, already rotated at its own
+ *     position; query head h reads key/value head h / (n_q_heads / N).
+ *   k, v (device, cfg.out_dtype) [n, N, D]: rows of rkv_reconstruct's outputs
+ *     (the selected tokens of one sequence), 16-byte aligned.
+ *   out (device, fp32) [n_q_heads, D].
+ *   n_q_heads: a multiple of N, at most 8 N;  n in [1, 262144].
+ * The softmax is fp32 with a per-chunk maximum; the library's workspace holds the
+ * chunk partials, so calls on one context must not run concurrently.
+ * Errors (nothing launched): RKV_EINVAL (sizes, NULL), RKV_EALIGN; RKV_ECUDA.
+ */
+rkv_status rkv_sparse_attention(rkv_ctx* ctx, const float* q, int32_t n_q_heads,
+                                const void* k, const void* v, int32_t n, float* out,
+                                void* stream);
+
+/*
  * Forget everything written for one sequence (seq >= 0) or for all (seq = -1):
  * its pool slots become empty and its token rows unwritten, so the slot can
  * hold a new sequence (stream-ordered; codes and extremes are overwritten by

@@ -70,6 +70,7 @@ ABI_FUNCTIONS = {
     "rkv_pool_append": (_I32, [_P, _P, _I64, _P, _P, _P, _I32, _P]),
     "rkv_compress": (_I32, [_P, _P, _I64, _P, _P, _P, _I32, _P]),
     "rkv_reconstruct": (_I32, [_P, _P, _P, _I32, _P, _P, _P]),
+    "rkv_sparse_attention": (_I32, [_P, _P, _I32, _P, _P, _I32, _P, _P]),
     "rkv_get_status": (_I32, [_P, ctypes.POINTER(_I32), _P]),
     "rkv_reset": (_I32, [_P, _I32, _P]),
     "rkv_last_error": (ctypes.c_char_p, []),
@@ -267,6 +268,26 @@ class Codec:
         _check(lib().rkv_reconstruct(self._ctx, seq.data_ptr(), pos.data_ptr(), n,
                                      k_out.data_ptr(), v_out.data_ptr(), _stream_ptr(stream)))
         return k_out, v_out
+
+    def sparse_attention(self, q, k, v, out=None, stream=None):
+        """softmax(q K^T / sqrt(D)) V over the rows of k, v (a restore's outputs).
+        q: [H_q, D] fp32 CUDA tensor; returns out [H_q, D] fp32."""
+        N, D = self.cfg.n_kv_heads, self.cfg.head_dim
+        odt = torch.float32 if self.cfg.out_dtype == "fp32" else torch.bfloat16
+        if q.dtype != torch.float32 or not q.is_cuda or not q.is_contiguous() or q.dim() != 2 \
+                or q.shape[1] != D:
+            raise ValueError("q must be a contiguous [H_q, D] fp32 CUDA tensor")
+        for t in (k, v):
+            if t.dtype != odt or not t.is_cuda or not t.is_contiguous() or tuple(t.shape[1:]) != (N, D):
+                raise ValueError("k and v must be contiguous [n, N, D] CUDA tensors of out_dtype")
+        if k.shape[0] != v.shape[0]:
+            raise ValueError("k and v must have the same rows")
+        if out is None:
+            out = torch.empty((q.shape[0], D), dtype=torch.float32, device=q.device)
+        _check(lib().rkv_sparse_attention(self._ctx, q.data_ptr(), q.shape[0], k.data_ptr(),
+                                          v.data_ptr(), k.shape[0], out.data_ptr(),
+                                          _stream_ptr(stream)))
+        return out
 
     def reset(self, seq: int = -1, stream=None):
         """Empty one sequence's pool and token rows (seq = -1: all sequences)."""

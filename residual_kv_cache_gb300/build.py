@@ -17,7 +17,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "librkv.so")
 SOURCES = ["rkv_api.cu", "k_elementwise.cu", "k_gemm.cu", "k_retrieve.cu", "k_reconstruct.cu",
-           "k_noalloc.cu"]
+           "k_noalloc.cu", "k_attention.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O3",
          "--expt-relaxed-constexpr", "-Xptxas", "-v"]

@@ -413,6 +413,7 @@ rkv_status rkv_create(const rkv_config* cfg, const void* Wc1, const void* Wc2, c
   ALLOC(c->X, (size_t)2 * c->max_rows * d.dkv * 2);
   ALLOC(c->H, (size_t)2 * c->max_rows * d.dff * 2);
   ALLOC(c->part, (size_t)c->units_cap * kTileM * 4 * sizeof(int2));
+  ALLOC(c->attn_ws, sizeof(float) * kAttnMaxChunks * kAttnMaxGroup * d.N * (2 + d.D));
   ALLOC(c->plan_dev[0], (size_t)c->plan_ints * 4);
   ALLOC(c->plan_dev[1], (size_t)c->plan_ints * 4);
   ALLOC(c->status, 512);
@@ -688,6 +689,24 @@ rkv_status rkv_reconstruct(rkv_ctx* c, const int32_t* seq, const int32_t* pos, i
   return RKV_OK;
 }
 
+rkv_status rkv_sparse_attention(rkv_ctx* c, const float* q, int32_t n_q_heads, const void* k,
+                                const void* v, int32_t n, float* out, void* stream) {
+  if (!c) return fail(RKV_EINVAL, "ctx is NULL");
+  if (!q || !k || !v || !out) return fail(RKV_EINVAL, "NULL q, k, v or out");
+  const Dims& d = c->d;
+  if (n_q_heads < d.N || n_q_heads % d.N != 0 || n_q_heads / d.N > kAttnMaxGroup)
+    return fail(RKV_EINVAL, "n_q_heads must be a multiple of n_kv_heads, at most %d times it",
+                kAttnMaxGroup);
+  if (n < 1 || n > kAttnMaxTokens)
+    return fail(RKV_EINVAL, "n must be in [1, %d] (softmax over the selected tokens)",
+                kAttnMaxTokens);
+  if ((reinterpret_cast<uintptr_t>(k) & 15u) || (reinterpret_cast<uintptr_t>(v) & 15u) ||
+      (reinterpret_cast<uintptr_t>(q) & 3u) || (reinterpret_cast<uintptr_t>(out) & 3u))
+    return fail(RKV_EALIGN, "k and v must be 16-byte aligned, q and out 4-byte aligned");
+  CUDA_OK(launch_attention(c, q, n_q_heads, k, v, n, out, static_cast<cudaStream_t>(stream)));
+  return RKV_OK;
+}
+
 rkv_status rkv_reset(rkv_ctx* c, int32_t seq, void* stream) {
   if (!c) return fail(RKV_EINVAL, "ctx is NULL");
   if (seq < -1 || seq >= c->d.B) return fail(RKV_EINVAL, "seq %d out of range", seq);
@@ -715,6 +734,7 @@ rkv_status rkv_get_status(rkv_ctx* c, int32_t* flags, void* stream) {
 void rkv_free(rkv_ctx* c) {
   if (!c) return;
   cudaFree(c->w12);
+  cudaFree(c->attn_ws);
   cudaFree(c->w3);
   cudaFree(c->wd);
   cudaFree(c->rope_lo);

@@ -76,6 +76,8 @@ struct rkv_ctx {
   __nv_bfloat16* X = nullptr;     // [2 max_rows, 2d_k] kv / mean rows interleaved
   __nv_bfloat16* H = nullptr;     // [2 max_rows, d_ff] SwiGLU rows (mean rows negated)
   int2* part = nullptr;           // [units_cap, 128, 4] partial top-k (distance bits, slot)
+  float* attn_ws = nullptr;       // sparse attention chunk partials (m, l, acc), kAttnMaxChunks
+                                  // x kAttnMaxGroup N query heads
   int units_cap = 0;
   int32_t* plan_dev[2] = {nullptr, nullptr};
   int32_t* plan_host[2] = {nullptr, nullptr};   // pinned staging
@@ -121,6 +123,15 @@ cudaError_t launch_reconstruct(rkv_ctx* c, const int32_t* seq, const int32_t* po
                                void* k_out, void* v_out, cudaStream_t s);
 
 cudaError_t launch_timeout_probe(rkv_ctx* c, cudaStream_t s);
+
+// Sparse attention over restored K/V: at most kAttnMaxChunks chunks of selected tokens
+// (of attention_chunk(n) tokens each), query heads per key/value head <= kAttnMaxGroup.
+constexpr int kAttnMaxChunks = 256;
+constexpr int kAttnMaxGroup = 8;
+constexpr int kAttnMaxTokens = kAttnMaxChunks * 1024;
+int attention_chunk(int n);
+cudaError_t launch_attention(rkv_ctx* c, const float* q, int n_q_heads, const void* k,
+                             const void* v, int n, float* out, cudaStream_t s);
 
 // Tensor map of a row-major [rows, cols] output matrix (bf16 or fp32) for 2-D tiled
 // stores: box = {128 bytes of columns, 128 rows}, 128-byte swizzle.
