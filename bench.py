@@ -292,6 +292,11 @@ def run_cuda(args):
     codec.set_timing(False)
     status |= codec.get_status()
 
+    # ---- sparse-layer attention over each decode step's restored rows (not part of the
+    # step above): 32 query heads of the Llama-3.1-8B layer on its 8 key/value heads
+    attn = measure_attention(codec, sels, seq0, k_out, v_out, w, dev, args.steps, flush, barrier)
+    status |= codec.get_status()
+
     t_step_ms = reduce_max(sum(times) / len(times), world, dev)
     tokens_step = T + steps_dec * n_sel
     value = reduce_sum(tokens_step, world, dev) / (t_step_ms / 1e3)
@@ -350,6 +355,7 @@ def run_cuda(args):
         "roofline": roofline,
         "kernels": {k: {kk: round(vv, 4) for kk, vv in v.items()} for k, v in rows.items()},
         "e2e": e2e,
+        "sparse_attention": attn,
         "gpu_launches": int(launches),
         "clocks": clk,
         "device_status": int(status),
@@ -361,6 +367,37 @@ def run_cuda(args):
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()
+
+
+def measure_attention(codec, sels, seq0, k_out, v_out, w, dev, steps, flush, barrier):
+    """Time rkv_sparse_attention after each decode step's restore (event pairs around
+    its two launches).  Bytes: the K and V rows it reads, q in, o out."""
+    import torch
+    hq = 4 * w.n_kv_heads
+    g = torch.Generator().manual_seed(4242)
+    q = torch.randn(hq, w.head_dim, generator=g).to(dev)
+    out = torch.empty(hq, w.head_dim, dtype=torch.float32, device=dev)
+    codec.set_timing(True)
+    codec.get_timing(reset=True)
+    for _ in range(steps):
+        flush.fill_(1.0)
+        barrier()
+        for s in range(len(sels)):
+            codec.reconstruct(seq0, sels[s], k_out, v_out)
+            codec.sparse_attention(q, k_out, v_out, out)
+        barrier()
+    t = codec.get_timing(reset=True)
+    codec.set_timing(False)
+    calls, ms = t["rkv_attention_kernel"]
+    us = ms / calls * 1e3
+    n = w.n_sel
+    kv_bytes = 2 * n * w.n_kv_heads * w.head_dim * 2
+    peaks, kind = load_peaks()
+    gbs = (kv_bytes + 2 * hq * w.head_dim * 4) / (us * 1e-6) / 1e9
+    return {"tokens": n, "q_heads": hq, "kv_heads": w.n_kv_heads, "us_per_call": round(us, 2),
+            "gbs": round(gbs, 1), "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
+            "peak_kind": f"{kind} copy",
+            "note": "K/V read right after their restore (L2-resident); o is fp32"}
 
 
 def run_e2e(args, codec, kv_dev, sels_dev, w, dev, stream, barrier, world, ref, non):
@@ -493,7 +530,8 @@ def run_reference(args):
 
 def run_kernel_case(args):
     """Minimal case for kernel captures under ncu: one prefill write and two decode-step
-    restores of the workload (no timing, no CPU work)."""
+    restores of the workload, each followed by the sparse attention over its rows (no
+    timing, no CPU work)."""
     import torch
     import residual_kv_cache_gb300 as rkv
     from residual_kv_cache_gb300 import build as _build
@@ -512,8 +550,11 @@ def run_kernel_case(args):
     codec.pool_append(kv, np.zeros_like(ref), ref, src_rows=ref)
     codec.compress(kv, np.zeros_like(non), non, src_rows=non)
     zero = torch.zeros(w.n_sel, dtype=torch.int32, device=dev)
+    g = torch.Generator().manual_seed(4242)
+    q = torch.randn(4 * w.n_kv_heads, w.head_dim, generator=g).to(dev)
     for s in range(2):
-        codec.reconstruct(zero, synth.gen_selection(w.T, w.n_sel, 1010 + s).to(dev))
+        K, V = codec.reconstruct(zero, synth.gen_selection(w.T, w.n_sel, 1010 + s).to(dev))
+        codec.sparse_attention(q, K, V)             # the sparse layer's attention over them
     torch.cuda.synchronize()
     flags = codec.get_status()
     print(json.dumps({"kernel_case": WORKLOAD, "T": w.T, "launches": codec.launch_count(),

@@ -5,9 +5,10 @@
 // just written (they are still in L2), so the work is split over the tokens, not over
 // the heads: a CTA takes one chunk of selected tokens and one key/value head, scores
 // the chunk against every query head of that head's group, and keeps a chunk-local
-// softmax (its maximum m, its sum l of exp(s - m), and sum exp(s - m) v).  A second
-// launch merges the chunks of each query head: M = max m_c, L = sum l_c e^(m_c - M),
-// o = sum acc_c e^(m_c - M) / L.  Everything is fp32; exp is the library expf.
+// softmax (its maximum m, its sum l of exp(s - m), and sum exp(s - m) v).  The last CTA
+// of each key/value head to finish (a counter after a fence) merges that head's chunks:
+// M = max m_c, L = sum l_c e^(m_c - M), o = sum acc_c e^(m_c - M) / L, and puts the
+// counter back to zero for the next call.  Everything is fp32; exp is the library expf.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -20,6 +21,8 @@ namespace rkv {
 namespace {
 
 constexpr int kAttnThreads = 256;
+constexpr int kWarps = kAttnThreads / 32;
+constexpr int kAttnCtasPerSm = 3;             // resident CTAs per SM (registers <= 85)
 
 __device__ __forceinline__ float block_max(float v, float* red) {
 #pragma unroll
@@ -29,7 +32,7 @@ __device__ __forceinline__ float block_max(float v, float* red) {
   if (l == 0) red[w] = v;
   __syncthreads();
   v = red[0];
-  for (int i = 1; i < kAttnThreads / 32; ++i) v = fmaxf(v, red[i]);
+  for (int i = 1; i < kWarps; ++i) v = fmaxf(v, red[i]);
   return v;
 }
 
@@ -41,10 +44,11 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   if (l == 0) red[w] = v;
   __syncthreads();
   v = 0.f;
-  for (int i = 0; i < kAttnThreads / 32; ++i) v += red[i];
+  for (int i = 0; i < kWarps; ++i) v += red[i];
   return v;
 }
 
+// Eight consecutive elements as floats (16-byte or 32-byte aligned).
 __device__ __forceinline__ void load8(const __nv_bfloat16* p, float* f) {
   const uint4 u = *reinterpret_cast<const uint4*>(p);
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -61,50 +65,99 @@ __device__ __forceinline__ void load8(const float* p, float* f) {
   f[0] = a.x, f[1] = a.y, f[2] = a.z, f[3] = a.w, f[4] = b.x, f[5] = b.y, f[6] = b.z, f[7] = b.w;
 }
 
-__device__ __forceinline__ float load1(const __nv_bfloat16* p) { return __bfloat162float(*p); }
-__device__ __forceinline__ float load1(const float* p) { return *p; }
+// Four consecutive elements (D = 128: one lane's share of a row) or two (D = 64).
+__device__ __forceinline__ void load_lane(const __nv_bfloat16* p, int n, float* f) {
+  if (n == 4) {
+    const uint2 u = *reinterpret_cast<const uint2*>(p);
+    f[0] = __uint_as_float(u.x << 16), f[1] = __uint_as_float(u.x & 0xFFFF0000u);
+    f[2] = __uint_as_float(u.y << 16), f[3] = __uint_as_float(u.y & 0xFFFF0000u);
+  } else {
+    const uint32_t u = *reinterpret_cast<const uint32_t*>(p);
+    f[0] = __uint_as_float(u << 16), f[1] = __uint_as_float(u & 0xFFFF0000u);
+  }
+}
+__device__ __forceinline__ void load_lane(const float* p, int n, float* f) {
+  if (n == 4) {
+    const float4 a = *reinterpret_cast<const float4*>(p);
+    f[0] = a.x, f[1] = a.y, f[2] = a.z, f[3] = a.w;
+  } else {
+    const float2 a = *reinterpret_cast<const float2*>(p);
+    f[0] = a.x, f[1] = a.y;
+  }
+}
 
-// Grid (chunks, N).  Dynamic shared memory: q [G][D] (scaled by 1/sqrt(D)), then the
-// scores / weights [G][chunk].  part_m, part_l: [chunks][Hq]; part_acc: [chunks][Hq][D].
-template <typename T>
-__global__ void __launch_bounds__(kAttnThreads)
-    attn_partial_kernel(const float* __restrict__ q, const T* __restrict__ k,
-                        const T* __restrict__ v, int n, int N, int D, int G, int chunk,
-                        float* __restrict__ part_m, float* __restrict__ part_l,
-                        float* __restrict__ part_acc) {
+}  // namespace
+
+// Shared memory of one CTA, in floats: q [G][4][D/4 + 4] (quarters padded apart),
+// the weights [G][chunk] and the warp sums [8][G][D].
+static size_t attention_smem_floats(int G, int D, int chunk) {
+  return (size_t)G * (D + 16) + (size_t)G * chunk + (size_t)kWarps * G * D;
+}
+
+namespace {
+
+// Grid (chunks, N).  part_m, part_l: [chunks][Hq]; part_acc: [chunks][Hq][D];
+// count [N]: finished chunks of each key/value head (zero between calls).
+template <typename T, int D>
+__global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
+    attn_kernel(const float* __restrict__ q, const T* __restrict__ k, const T* __restrict__ v,
+                int n, int N, int G, int chunk, float* __restrict__ part_m,
+                float* __restrict__ part_l, float* __restrict__ part_acc, int* __restrict__ count,
+                float* __restrict__ out) {
   extern __shared__ float sm[];
-  __shared__ float red[kAttnThreads / 32];
-  float* qs = sm;                     // [G][D]
-  float* ss = sm + G * D;             // [G][chunk]
+  __shared__ float red[kWarps];
+  __shared__ int is_last;
+  __shared__ float Ls[kAttnMaxGroup];
+  constexpr int dq = D / 4;                   // dimensions per quarter row
+  constexpr int qstride = dq + 4;             // padded so the four quarters hit distinct banks
+  float* qs = sm;                             // [G][4][qstride]
+  float* ss = sm + G * 4 * qstride;           // [G][chunk]
+  float* wsum = ss + G * chunk;               // [8][G][D]
   const int c = blockIdx.x, g = blockIdx.y;
   const int Hq = G * N;
   const int j0 = c * chunk;
   const int cn = min(chunk, n - j0);
   const float scale = rsqrtf((float)D);
-  for (int i = threadIdx.x; i < G * D; i += kAttnThreads)
-    qs[i] = q[(size_t)(g * G + i / D) * D + (i % D)] * scale;
+  for (int i = threadIdx.x; i < G * D; i += kAttnThreads) {
+    const int h = i / D, d = i % D;
+    qs[(h * 4 + d / dq) * qstride + d % dq] = q[(size_t)(g * G + h) * D + d] * scale;
+  }
   __syncthreads();
 
-  // scores: one token per thread, its whole row against every query head of the group
-  for (int j = threadIdx.x; j < cn; j += kAttnThreads) {
-    const T* kr = k + ((size_t)(j0 + j) * N + g) * D;
-    float s[8];
+  // scores: four threads per token, each a quarter of the row, so that a warp
+  // instruction reads contiguous quarter rows of eight tokens
+  {
+    const int quarter = threadIdx.x & 3;
+    const float* qq = qs + quarter * qstride;
+    const int cn_pad = (cn + kAttnThreads / 4 - 1) / (kAttnThreads / 4) * (kAttnThreads / 4);
+    for (int j = threadIdx.x >> 2; j < cn_pad; j += kAttnThreads / 4) {
+      float s[8];
 #pragma unroll
-    for (int h = 0; h < 8; ++h) s[h] = 0.f;
-    for (int d = 0; d < D; d += 8) {
-      float kf[8];
-      load8(kr + d, kf);
+      for (int h = 0; h < 8; ++h) s[h] = 0.f;
+      if (j < cn) {
+        const T* kr = k + ((size_t)(j0 + j) * N + g) * D + quarter * dq;
+#pragma unroll
+        for (int d = 0; d < dq; d += 8) {
+          float kf[8];
+          load8(kr + d, kf);
+#pragma unroll
+          for (int h = 0; h < 8; ++h) {
+            if (h < G) {
+#pragma unroll
+              for (int e = 0; e < 8; ++e) s[h] = fmaf(qq[h * 4 * qstride + d + e], kf[e], s[h]);
+            }
+          }
+        }
+      }
 #pragma unroll
       for (int h = 0; h < 8; ++h) {
         if (h < G) {
-#pragma unroll
-          for (int e = 0; e < 8; ++e) s[h] = fmaf(qs[h * D + d + e], kf[e], s[h]);
+          s[h] += __shfl_xor_sync(0xffffffffu, s[h], 1);
+          s[h] += __shfl_xor_sync(0xffffffffu, s[h], 2);
+          if (j < cn && quarter == 0) ss[h * chunk + j] = s[h];
         }
       }
     }
-#pragma unroll
-    for (int h = 0; h < 8; ++h)
-      if (h < G) ss[h * chunk + j] = s[h];
   }
   __syncthreads();
 
@@ -127,81 +180,154 @@ __global__ void __launch_bounds__(kAttnThreads)
   }
   __syncthreads();
 
-  // sum_j exp(s - m) v_j: thread t owns dimension t % D of heads t / D, t / D + slots, ...
-  const int slots = kAttnThreads / D;
-  const int d = threadIdx.x % D, h0 = threadIdx.x / D;
-  float acc[8];
+  // sum_j exp(s - m) v_j: warp w takes tokens w, w + 8, ...; lane l the dimensions
+  // [l * D / 32, (l + 1) * D / 32), so that a warp reads a whole V row per token
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  constexpr int dpl = D / 32;                      // 4 or 2 dimensions per lane
+  float acc[8][4];
 #pragma unroll
-  for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-  for (int j = 0; j < cn; ++j) {
-    const float vv = load1(v + ((size_t)(j0 + j) * N + g) * D + d);
+  for (int h = 0; h < 8; ++h)
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-      const int h = h0 + i * slots;
-      if (h < G) acc[i] = fmaf(ss[h * chunk + j], vv, acc[i]);
+    for (int e = 0; e < 4; ++e) acc[h][e] = 0.f;
+#pragma unroll 8
+  for (int j = warp; j < cn; j += kWarps) {
+    float vf[4] = {0.f, 0.f, 0.f, 0.f};
+    load_lane(v + ((size_t)(j0 + j) * N + g) * D + lane * dpl, dpl, vf);
+#pragma unroll
+    for (int h = 0; h < 8; ++h) {
+      if (h < G) {
+        const float w = ss[h * chunk + j];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) acc[h][e] = fmaf(w, vf[e], acc[h][e]);
+      }
     }
   }
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const int h = h0 + i * slots;
-    if (h < G) part_acc[((size_t)c * Hq + g * G + h) * D + d] = acc[i];
+  for (int h = 0; h < 8; ++h) {
+    if (h < G) {
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        if (e < dpl) wsum[(warp * G + h) * D + lane * dpl + e] = acc[h][e];
+    }
   }
-}
+  __syncthreads();
+  for (int i = threadIdx.x; i < G * D; i += kAttnThreads) {
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) t += wsum[w * G * D + i];
+    part_acc[((size_t)c * Hq + g * G) * D + i] = t;
+  }
 
-// Grid Hq, block D threads.
-__global__ void attn_merge_kernel(const float* __restrict__ part_m, const float* __restrict__ part_l,
-                                  const float* __restrict__ part_acc, int chunks, int Hq, int D,
-                                  float* __restrict__ out) {
-  const int h = blockIdx.x, d = threadIdx.x;
-  float M = -FLT_MAX;
-  for (int c = 0; c < chunks; ++c) M = fmaxf(M, part_m[(size_t)c * Hq + h]);
-  float L = 0.f, o = 0.f;
-  for (int c = 0; c < chunks; ++c) {
-    const float f = expf(part_m[(size_t)c * Hq + h] - M);
-    L = fmaf(part_l[(size_t)c * Hq + h], f, L);
-    o = fmaf(part_acc[((size_t)c * Hq + h) * D + d], f, o);
+  // the last CTA of this key/value head merges its chunks
+  __threadfence();
+  __syncthreads();
+  if (threadIdx.x == 0) is_last = atomicAdd(&count[g], 1) == (int)gridDim.x - 1;
+  __syncthreads();
+  if (!is_last) return;
+  __threadfence();
+  const int C = gridDim.x;
+  // every chunk's (m, l) of the group's heads in one pass, into the warp-sum area
+  // ([2][G][kAttnMaxChunks] <= 8 G D floats); then M_h, the factors e^(m_c - M_h) in
+  // place of m, and L_h into Ls
+  float* fac = wsum;                               // [G][kAttnMaxChunks]: m, then factors
+  float* lc = wsum + G * kAttnMaxChunks;           // [G][kAttnMaxChunks]: l
+  for (int i = threadIdx.x; i < G * C; i += kAttnThreads) {
+    const int h = i / C, cc = i % C;
+    fac[h * kAttnMaxChunks + cc] = __ldcg(part_m + (size_t)cc * Hq + g * G + h);
+    lc[h * kAttnMaxChunks + cc] = __ldcg(part_l + (size_t)cc * Hq + g * G + h);
   }
-  out[(size_t)h * D + d] = o / L;
+  __syncthreads();
+  // warp h (< G <= 8) reduces head h
+  if (warp < G) {
+    float mx = -FLT_MAX;
+    for (int cc = lane; cc < C; cc += 32) mx = fmaxf(mx, fac[warp * kAttnMaxChunks + cc]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    float L = 0.f;
+    for (int cc = lane; cc < C; cc += 32) {
+      const float f = expf(fac[warp * kAttnMaxChunks + cc] - mx);
+      fac[warp * kAttnMaxChunks + cc] = f;
+      L = fmaf(lc[warp * kAttnMaxChunks + cc], f, L);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+    if (lane == 0) Ls[warp] = L;
+  }
+  __syncthreads();
+  for (int i = threadIdx.x; i < G * D; i += kAttnThreads) {
+    const int h = i / D;
+    const float* pa = part_acc + (size_t)(g * G) * D + i;
+    float o = 0.f;
+#pragma unroll 16
+    for (int cc = 0; cc < C; ++cc)
+      o = fmaf(__ldcg(pa + (size_t)cc * Hq * D), fac[h * kAttnMaxChunks + cc], o);
+    out[(size_t)(g * G) * D + i] = o / Ls[h];
+  }
+  if (threadIdx.x == 0) count[g] = 0;                // ready for the next call
 }
 
 }  // namespace
 
-// Tokens per chunk: at least 128, and few enough chunks for the workspace.
-int attention_chunk(int n) {
-  int chunk = (n + kAttnMaxChunks - 1) / kAttnMaxChunks;
+// Tokens per chunk: enough chunks for one resident wave of CTAs over the N key/value
+// heads (kAttnCtasPerSm per SM), at most 1024 tokens (the weights' shared memory) and
+// at most kAttnMaxChunks chunks (the workspace).
+int attention_chunk(int n, int N, int num_sms) {
+  int target = kAttnCtasPerSm * num_sms / N;
+  target = target < 1 ? 1 : (target > kAttnMaxChunks ? kAttnMaxChunks : target);
+  int chunk = (n + target - 1) / target;
   chunk = (chunk + 31) / 32 * 32;
-  return chunk < 128 ? 128 : chunk;
+  if (chunk > 1024) chunk = 1024;
+  const int floor_chunk = (n + kAttnMaxChunks - 1) / kAttnMaxChunks;
+  return chunk < floor_chunk ? (floor_chunk + 31) / 32 * 32 : chunk;
+}
+
+template <typename T, int D>
+cudaError_t launch_attn(const float* q, const void* k, const void* v, int n, int N, int G,
+                        int chunk, int chunks, float* pm, float* pl, float* pa, int* count,
+                        float* out, size_t smem, int maxb, cudaStream_t s) {
+  // the shared-memory opt-in is a per-device function attribute: set it once per device
+  static unsigned set_on = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 32 && !((set_on >> dev) & 1u)) {
+    e = cudaFuncSetAttribute(attn_kernel<T, D>, cudaFuncAttributeMaxDynamicSharedMemorySize, maxb);
+    if (e != cudaSuccess) return e;
+    set_on |= 1u << dev;
+  }
+  attn_kernel<T, D><<<dim3(chunks, N), kAttnThreads, smem, s>>>(
+      q, static_cast<const T*>(k), static_cast<const T*>(v), n, N, G, chunk, pm, pl, pa, count,
+      out);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_attention(rkv_ctx* c, const float* q, int n_q_heads, const void* k,
                              const void* v, int n, float* out, cudaStream_t s) {
   const Dims& d = c->d;
   const int G = n_q_heads / d.N;
-  const int chunk = attention_chunk(n);
+  const int chunk = attention_chunk(n, d.N, c->num_sms);
   const int chunks = (n + chunk - 1) / chunk;
   float* pm = c->attn_ws;
   float* pl = pm + (size_t)kAttnMaxChunks * n_q_heads;
   float* pa = pl + (size_t)kAttnMaxChunks * n_q_heads;
-  // q [G][D] and the weights [G][chunk]: at most 8 x (128 + 1024) floats = 36 KB
-  const size_t smem = sizeof(float) * ((size_t)G * d.D + (size_t)G * chunk);
+  // at most 8 x (144 + 1024 + 8 x 128) floats = 68.5 KB
+  const size_t smem = sizeof(float) * attention_smem_floats(G, d.D, chunk);
+  const int maxb = (int)(sizeof(float) * attention_smem_floats(kAttnMaxGroup, 128, 1024));
   cudaEvent_t ev;
-  timing_begin(c, "rkv_attention_partial_kernel", s, &ev);
-  if (d.out_f32) {
-    attn_partial_kernel<float><<<dim3(chunks, d.N), kAttnThreads, smem, s>>>(
-        q, static_cast<const float*>(k), static_cast<const float*>(v), n, d.N, d.D, G, chunk, pm,
-        pl, pa);
-  } else {
-    attn_partial_kernel<__nv_bfloat16><<<dim3(chunks, d.N), kAttnThreads, smem, s>>>(
-        q, static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v), n, d.N,
-        d.D, G, chunk, pm, pl, pa);
-  }
-  timing_end(c, "rkv_attention_partial_kernel", s, ev);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  timing_begin(c, "rkv_attention_merge_kernel", s, &ev);
-  attn_merge_kernel<<<n_q_heads, d.D, 0, s>>>(pm, pl, pa, chunks, n_q_heads, d.D, out);
-  timing_end(c, "rkv_attention_merge_kernel", s, ev);
-  return cudaGetLastError();
+  timing_begin(c, "rkv_attention_kernel", s, &ev);
+  cudaError_t e;
+  if (d.out_f32)
+    e = d.D == 128 ? launch_attn<float, 128>(q, k, v, n, d.N, G, chunk, chunks, pm, pl, pa,
+                                             c->attn_count, out, smem, maxb, s)
+                   : launch_attn<float, 64>(q, k, v, n, d.N, G, chunk, chunks, pm, pl, pa,
+                                            c->attn_count, out, smem, maxb, s);
+  else
+    e = d.D == 128 ? launch_attn<__nv_bfloat16, 128>(q, k, v, n, d.N, G, chunk, chunks, pm, pl,
+                                                     pa, c->attn_count, out, smem, maxb, s)
+                   : launch_attn<__nv_bfloat16, 64>(q, k, v, n, d.N, G, chunk, chunks, pm, pl,
+                                                    pa, c->attn_count, out, smem, maxb, s);
+  timing_end(c, "rkv_attention_kernel", s, ev);
+  return e;
 }
 
 }  // namespace rkv

@@ -414,6 +414,7 @@ rkv_status rkv_create(const rkv_config* cfg, const void* Wc1, const void* Wc2, c
   ALLOC(c->H, (size_t)2 * c->max_rows * d.dff * 2);
   ALLOC(c->part, (size_t)c->units_cap * kTileM * 4 * sizeof(int2));
   ALLOC(c->attn_ws, sizeof(float) * kAttnMaxChunks * kAttnMaxGroup * d.N * (2 + d.D));
+  ALLOC(c->attn_count, sizeof(int) * d.N);
   ALLOC(c->plan_dev[0], (size_t)c->plan_ints * 4);
   ALLOC(c->plan_dev[1], (size_t)c->plan_ints * 4);
   ALLOC(c->status, 512);
@@ -477,6 +478,7 @@ rkv_status rkv_create(const rkv_config* cfg, const void* Wc1, const void* Wc2, c
   if (e == cudaSuccess) e = cudaMemsetAsync(c->Q, 0, (size_t)c->m_cap * d.parts * d.dkv * 2, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(c->X, 0, (size_t)2 * c->max_rows * d.dkv * 2, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(c->H, 0, (size_t)2 * c->max_rows * d.dff * 2, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(c->attn_count, 0, sizeof(int) * d.N, s);
   if (e == cudaSuccess) e = launch_init_storage(c, s);
   if (e == cudaSuccess)
     e = launch_repack_weights(c, static_cast<const __nv_bfloat16*>(Wc1),
@@ -735,6 +737,7 @@ void rkv_free(rkv_ctx* c) {
   if (!c) return;
   cudaFree(c->w12);
   cudaFree(c->attn_ws);
+  cudaFree(c->attn_count);
   cudaFree(c->w3);
   cudaFree(c->wd);
   cudaFree(c->rope_lo);

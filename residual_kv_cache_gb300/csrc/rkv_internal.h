@@ -78,6 +78,7 @@ struct rkv_ctx {
   int2* part = nullptr;           // [units_cap, 128, 4] partial top-k (distance bits, slot)
   float* attn_ws = nullptr;       // sparse attention chunk partials (m, l, acc), kAttnMaxChunks
                                   // x kAttnMaxGroup N query heads
+  int* attn_count = nullptr;      // [N] finished chunks per key/value head (zero between calls)
   int units_cap = 0;
   int32_t* plan_dev[2] = {nullptr, nullptr};
   int32_t* plan_host[2] = {nullptr, nullptr};   // pinned staging
@@ -129,7 +130,7 @@ cudaError_t launch_timeout_probe(rkv_ctx* c, cudaStream_t s);
 constexpr int kAttnMaxChunks = 256;
 constexpr int kAttnMaxGroup = 8;
 constexpr int kAttnMaxTokens = kAttnMaxChunks * 1024;
-int attention_chunk(int n);
+int attention_chunk(int n, int N, int num_sms);
 cudaError_t launch_attention(rkv_ctx* c, const float* q, int n_q_heads, const void* k,
                              const void* v, int n, float* out, cudaStream_t s);
 

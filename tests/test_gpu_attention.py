@@ -79,7 +79,7 @@ def test_attention_end_to_end_against_the_oracle_restore(llama_small):
 
 
 @cuda
-@pytest.mark.parametrize("n", [1, 127, 128, 129, 1000, 33000, 100000])
+@pytest.mark.parametrize("n", [1, 127, 128, 129, 1000, 20000, 33000, 100000])
 def test_attention_token_counts(llama_small, n):
     """Seeded random K/V rows: one token (o = v exactly), chunk edges, many chunks."""
     c = llama_small["codec"]
