@@ -19,23 +19,6 @@ __device__ __forceinline__ float fp8_to_float(uint8_t b) {
   return __half2float(__half(h));
 }
 
-// Decode 8 E4M3 bytes (little-endian in a uint2) to floats; exact.
-__device__ __forceinline__ void fp8x8_to_float(uint2 v, float* f) {
-  const uint32_t w[2] = {v.x, v.y};
-#pragma unroll
-  for (int i = 0; i < 2; ++i) {
-#pragma unroll
-    for (int j = 0; j < 2; ++j) {
-      __nv_fp8x2_storage_t pair = static_cast<__nv_fp8x2_storage_t>((w[i] >> (16 * j)) & 0xFFFFu);
-      __half2_raw h2 = __nv_cvt_fp8x2_to_halfraw2(pair, __NV_E4M3);
-      __half2 hh(h2);
-      float2 ff = __half22float2(hh);
-      f[4 * i + 2 * j] = ff.x;
-      f[4 * i + 2 * j + 1] = ff.y;
-    }
-  }
-}
-
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   __nv_bfloat16 lo = __float2bfloat16_rn(a), hi = __float2bfloat16_rn(b);
   return static_cast<uint32_t>(__bfloat16_as_ushort(lo)) |
@@ -181,46 +164,104 @@ __global__ void prep_queries_kernel(const void* __restrict__ kv, int64_t stride,
   }
 }
 
-// ---------------------------------------------------------------- mean rows
-// One block per compact row r: X[2r] = bf16 kv (the hi piece of the query row),
-// X[2r+1] = bf16(mean of the retrieved FP8 references).  The sum of at most four
-// E4M3 values is exact in fp32; it is divided by k_i once (IEEE division).
-__global__ void mean_rows_kernel(const int32_t* __restrict__ c_q, const int32_t* __restrict__ c_dst,
-                                 const __nv_bfloat16* __restrict__ Q, int parts,
-                                 const uint8_t* __restrict__ pool8,
-                                 const int32_t* __restrict__ ref_idx, int topk, int dkv,
-                                 int T_cap, int R_cap, __nv_bfloat16* __restrict__ X,
-                                 int* __restrict__ status) {
-  const int64_t r = blockIdx.x;
-  const int64_t qrow = c_q[r];
-  const int64_t dst = c_dst[r];
-  const int64_t seq = dst / T_cap;
-  int64_t prow[4];
-  int k_i = 0;
-  for (int t = 0; t < topk; ++t) {
-    const int32_t s = ref_idx[dst * topk + t];
-    if (s >= 0 && s < R_cap) prow[k_i++] = seq * R_cap + s;
-  }
-  if (k_i == 0 && threadIdx.x == 0) atomicOr(status, RKV_FLAG_UNWRITTEN);
-  const __nv_bfloat16* q = Q + qrow * (int64_t)parts * dkv;
-  __nv_bfloat16* xk = X + (2 * r) * (int64_t)dkv;
-  __nv_bfloat16* xm = X + (2 * r + 1) * (int64_t)dkv;
-  const float kf = (float)(k_i > 0 ? k_i : 1);
-  for (int e = threadIdx.x * 8; e < dkv; e += blockDim.x * 8) {
-    *reinterpret_cast<uint4*>(xk + e) = *reinterpret_cast<const uint4*>(q + e);
-    float s[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int t = 0; t < k_i; ++t) {
-      float f[8];
-      fp8x8_to_float(*reinterpret_cast<const uint2*>(pool8 + prow[t] * dkv + e), f);
+// bf16 kv rows: a plain copy into retrieval order.  One warp per row, each lane moving
+// 16-byte pieces with eight loads in flight before the stores (the copy is bound by how
+// many bytes are in flight, not by arithmetic).
+__global__ void __launch_bounds__(256)
+    prep_queries_bf16_kernel(const __nv_bfloat16* __restrict__ kv, int64_t stride,
+                             const int32_t* __restrict__ q_src, int dkv, int m_pad,
+                             __nv_bfloat16* __restrict__ Q) {
+  const int lane = threadIdx.x & 31;
+  const int pieces = dkv / 256;                       // 16-byte pieces per lane
+  for (int64_t row = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); row < m_pad;
+       row += (int64_t)gridDim.x * 8) {
+    const int64_t src = q_src[row];
+    uint4* out = reinterpret_cast<uint4*>(Q + row * (int64_t)dkv);
+    const uint4* in = reinterpret_cast<const uint4*>(kv + (src < 0 ? 0 : src) * stride);
+    for (int p0 = 0; p0 < pieces; p0 += 8) {
+      uint4 buf[8];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) s[i] = __fadd_rn(s[i], f[i]);
+      for (int p = 0; p < 8; ++p)
+        buf[p] = (src >= 0 && p0 + p < pieces) ? in[(p0 + p) * 32 + lane] : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+      for (int p = 0; p < 8; ++p)
+        if (p0 + p < pieces) out[(p0 + p) * 32 + lane] = buf[p];
     }
-    uint4 o;
-    o.x = pack_bf16x2(__fdiv_rn(s[0], kf), __fdiv_rn(s[1], kf));
-    o.y = pack_bf16x2(__fdiv_rn(s[2], kf), __fdiv_rn(s[3], kf));
-    o.z = pack_bf16x2(__fdiv_rn(s[4], kf), __fdiv_rn(s[5], kf));
-    o.w = pack_bf16x2(__fdiv_rn(s[6], kf), __fdiv_rn(s[7], kf));
-    *reinterpret_cast<uint4*>(xm + e) = o;
+  }
+}
+
+// ---------------------------------------------------------------- mean rows
+// One warp per compact row r: X[2r] = bf16 kv (the hi piece of the query row),
+// X[2r+1] = bf16(mean of the retrieved FP8 references).  The sum of at most four
+// E4M3 values is exact in fp32; it is divided by k_i once, correctly rounded.  Each lane
+// takes 8-element pieces e = (32 u + lane) * 8, four pieces in flight at a time.
+__global__ void __launch_bounds__(256)
+    mean_rows_kernel(const int32_t* __restrict__ c_q, const int32_t* __restrict__ c_dst,
+                     const __nv_bfloat16* __restrict__ Q, int parts,
+                     const uint8_t* __restrict__ pool8, const int32_t* __restrict__ ref_idx,
+                     int topk, int dkv, int T_cap, int R_cap, int n_rows,
+                     __nv_bfloat16* __restrict__ X, int* __restrict__ status) {
+  const int lane = threadIdx.x & 31;
+  for (int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); r < n_rows;
+       r += (int64_t)gridDim.x * 8) {
+    const int64_t qrow = c_q[r];
+    const int64_t dst = c_dst[r];
+    const int64_t seq = dst / T_cap;
+    const int32_t my = lane < topk ? ref_idx[dst * topk + lane] : -1;
+    int64_t prow[4];
+    bool ok[4];
+    int k_i = 0;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const int32_t sl = __shfl_sync(0xffffffffu, my, t);
+      ok[t] = t < topk && sl >= 0 && sl < R_cap;
+      prow[t] = ok[t] ? seq * R_cap + sl : 0;
+      k_i += ok[t] ? 1 : 0;
+    }
+    if (k_i == 0 && lane == 0) atomicOr(status, RKV_FLAG_UNWRITTEN);
+    // the sum divided by k_i, correctly rounded: a multiply by the exact reciprocal for
+    // k_i = 1, 2, 4, and the FMA-corrected division for k_i = 3
+    const float kinv = 1.0f / (float)(k_i == 2 ? 2 : (k_i == 4 ? 4 : 1));
+    const __nv_bfloat16* q = Q + qrow * (int64_t)parts * dkv;
+    __nv_bfloat16* xk = X + (2 * r) * (int64_t)dkv;
+    __nv_bfloat16* xm = X + (2 * r + 1) * (int64_t)dkv;
+    for (int e0 = 0; e0 < dkv; e0 += 4 * 256) {
+      uint4 qv[4];
+      uint2 rv[4][4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = e0 + (u * 32 + lane) * 8;
+        if (e < dkv) {
+          qv[u] = *reinterpret_cast<const uint4*>(q + e);
+#pragma unroll
+          for (int t = 0; t < 4; ++t)
+            rv[t][u] = ok[t] ? *reinterpret_cast<const uint2*>(pool8 + prow[t] * dkv + e)
+                             : make_uint2(0u, 0u);
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const int e = e0 + (u * 32 + lane) * 8;
+        if (e >= dkv) continue;
+        *reinterpret_cast<uint4*>(xk + e) = qv[u];
+        // exact sums of the E4M3 values (in any order: at most four of them)
+        float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          if (!ok[t]) continue;
+          fp8x4_add(rv[t][u].x, s8[0], s8[1], s8[2], s8[3]);
+          fp8x4_add(rv[t][u].y, s8[4], s8[5], s8[6], s8[7]);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) s8[i] = k_i == 3 ? div3_rn(s8[i]) : __fmul_rn(s8[i], kinv);
+        uint4 o;
+        o.x = pack_bf16x2(s8[0], s8[1]);
+        o.y = pack_bf16x2(s8[2], s8[3]);
+        o.z = pack_bf16x2(s8[4], s8[5]);
+        o.w = pack_bf16x2(s8[6], s8[7]);
+        *reinterpret_cast<uint4*>(xm + e) = o;
+      }
+    }
   }
 }
 
@@ -287,7 +328,11 @@ cudaError_t launch_prep_queries(rkv_ctx* c, const void* kv, int64_t stride, cons
   const Dims& d = c->d;
   cudaEvent_t ev;
   timing_begin(c, "rkv_prep_queries_kernel", s, &ev);
-  prep_queries_kernel<<<m_pad, 256, 0, s>>>(kv, stride, d.kv_f32, q_src, d.dkv, d.parts, c->Q);
+  if (d.kv_f32)
+    prep_queries_kernel<<<m_pad, 256, 0, s>>>(kv, stride, d.kv_f32, q_src, d.dkv, d.parts, c->Q);
+  else
+    prep_queries_bf16_kernel<<<grid_for(m_pad, 8, 16 * c->num_sms), 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(kv), stride, q_src, d.dkv, m_pad, c->Q);
   cudaError_t e = cudaGetLastError();
   timing_end(c, "rkv_prep_queries_kernel", s, ev);
   return e;
@@ -297,10 +342,10 @@ cudaError_t launch_mean_rows(rkv_ctx* c, const PassPlan& p, const int32_t* plan,
   const Dims& d = c->d;
   cudaEvent_t ev;
   timing_begin(c, "rkv_mean_rows_kernel", s, &ev);
-  mean_rows_kernel<<<p.n_rows, 256, 0, s>>>(plan + p.off_c_q, plan + p.off_c_dst, c->Q, d.parts,
-                                            static_cast<const uint8_t*>(c->st.pool_fp8),
-                                            c->st.ref_idx, d.topk, d.dkv, d.T_cap, d.R_cap, c->X,
-                                            c->status);
+  mean_rows_kernel<<<grid_for(p.n_rows, 8, 16 * c->num_sms), 256, 0, s>>>(
+      plan + p.off_c_q, plan + p.off_c_dst, c->Q, d.parts,
+      static_cast<const uint8_t*>(c->st.pool_fp8), c->st.ref_idx, d.topk, d.dkv, d.T_cap, d.R_cap,
+      p.n_rows, c->X, c->status);
   cudaError_t e = cudaGetLastError();
   timing_end(c, "rkv_mean_rows_kernel", s, ev);
   return e;

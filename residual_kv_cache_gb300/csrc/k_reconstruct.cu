@@ -83,28 +83,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
          (static_cast<uint32_t>(__bfloat16_as_ushort(hi)) << 16);
 }
 
-// s[4i .. 4i+3] += values of the four E4M3 bytes of w (byte 0 first): two bytes at a
-// time to f16 (exact: every E4M3 value is an f16), then each f16 added to its fp32
-// accumulator in one mixed-precision add.
-__device__ __forceinline__ void fp8x4_add(uint32_t w, float& s0, float& s1, float& s2, float& s3) {
-  asm("{\n"
-      ".reg .b16 lo, hi;\n"
-      ".reg .b32 h0, h1;\n"
-      ".reg .f16 a, b, c, d;\n"
-      "mov.b32 {lo, hi}, %4;\n"
-      "cvt.rn.f16x2.e4m3x2 h0, lo;\n"
-      "cvt.rn.f16x2.e4m3x2 h1, hi;\n"
-      "mov.b32 {a, b}, h0;\n"
-      "mov.b32 {c, d}, h1;\n"
-      "add.rn.f32.f16 %0, a, %0;\n"
-      "add.rn.f32.f16 %1, b, %1;\n"
-      "add.rn.f32.f16 %2, c, %2;\n"
-      "add.rn.f32.f16 %3, d, %3;\n"
-      "}"
-      : "+f"(s0), "+f"(s1), "+f"(s2), "+f"(s3)
-      : "r"(w));
-}
-
 // s[i] += value of FP8 byte i of v (16 bytes); exact in fp32 for <= 4 addends (their
 // bits span 2^-9 .. 2^11).
 __device__ __forceinline__ void fp8x16_add(uint4 v, float* s) {
@@ -112,16 +90,6 @@ __device__ __forceinline__ void fp8x16_add(uint4 v, float* s) {
   fp8x4_add(v.y, s[4], s[5], s[6], s[7]);
   fp8x4_add(v.z, s[8], s[9], s[10], s[11]);
   fp8x4_add(v.w, s[12], s[13], s[14], s[15]);
-}
-
-// Correctly rounded s / 3 for every fp32 s that is a sum of at most three E4M3 values:
-// q = RN(s * RN(1/3)), r = s - 3 q (exact), RN(q + r * RN(1/3)).  Checked against the
-// exact quotient for all 256317 such sums.
-__device__ __forceinline__ float div3_rn(float s) {
-  const float c = __uint_as_float(0x3EAAAAABu);       // RN(1/3)
-  const float q = __fmul_rn(s, c);
-  const float r = __fmaf_rn(-q, 3.0f, s);
-  return __fmaf_rn(r, c, q);
 }
 
 // Per-tile state of one epilogue thread's token row, packed into two registers.
