@@ -377,22 +377,23 @@ def test_host_errors():
 
 
 @cuda
-def test_multi_sequence_ragged():
+@pytest.mark.parametrize("alpha,sink", [(0.0, 0), (0.05, 3)])
+def test_multi_sequence_ragged(alpha, sink):
     """Three sequences of ragged lengths written in interleaved calls; each token only
-    sees its own sequence's pool."""
+    sees its own sequence's pool (fixed stride, and a dynamic-stride schedule)."""
     w = synth.workload("llama8b")
     lens = [300, 515, 1000]
     Tcap = 1024
     W = synth.gen_weights(w, 72)
     W64 = _weights64(W)
-    c = make_codec(w, W, T=Tcap, batch=3)
+    c = make_codec(w, W, T=Tcap, batch=3, alpha=alpha, sink=sink)
     kvs = [synth.gen_kv(w, 70 + b, T=L) for b, L in enumerate(lens)]
     flat = torch.cat(kvs).cuda()
     offs = np.cumsum([0] + lens)
     seq = np.concatenate([np.full(L, b) for b, L in enumerate(lens)]).astype(np.int32)
     pos = np.concatenate([np.arange(L) for L in lens]).astype(np.int32)
     rows = np.arange(len(seq), dtype=np.int32)
-    isref = pos % w.stride == 0
+    isref = C.is_reference(pos, w.stride, alpha, sink)
     # append all references (ordered per sequence), then compress interleaved rows
     c.pool_append(flat, seq[isref], pos[isref], src_rows=rows[isref])
     rng = np.random.default_rng(0)
@@ -400,10 +401,10 @@ def test_multi_sequence_ragged():
     c.compress(flat, seq[perm], pos[perm], src_rows=rows[perm].astype(np.int32))
     torch.cuda.synchronize()
     assert c.get_status() == 0
-    sh = oracle_shape(w)
+    sh = oracle_shape(w, alpha, sink)
     for b, L in enumerate(lens):
         st = C.compress_sequence(np64(kvs[b]), W64, sh, "operand")
-        non = np.nonzero(np.arange(L) % w.stride)[0]
+        non = np.nonzero(~C.is_reference(np.arange(L), w.stride, alpha, sink))[0]
         gidx = c.ref_idx[b].cpu().numpy().astype(np.int64)[:L]
         _, _, bad = idx_parity(gidx[non], st.idx[non], np64(kvs[b])[non], st.pool.vals,
                                st.pool.pos, non)
