@@ -299,9 +299,15 @@ int64_t rkv_launch_count(rkv_ctx* ctx);
 
 /*
  * Test hook: device address and size of a scratch tensor of the last
- * compress pass (0 = the bf16 [2*rows, 2d_k] operand rows kv/mean
- * interleaved, 1 = the bf16 [2*rows, d_ff] SwiGLU hidden rows, the mean row
- * negated).  Valid until the next call on the context.
+ * compress pass, whose rows are in retrieval order (the pass's rows grouped by
+ * sequence, each group padded to a multiple of 128; for a pass over one
+ * sequence, row q is the pass's row q):
+ *   0 = M, bf16 [rows, 2d_k]: the mean of each row's retrieved references;
+ *   1 = H, bf16 [2*rows, d_ff]: SwiGLU hidden rows, 2q of kv_q and 2q+1 of
+ *       the mean (negated);
+ *   2 = Q, bf16 [rows, parts*2d_k]: the query rows, whose first 2d_k columns
+ *       are bf16(kv) (parts = 1 for bf16 kv, 3 for fp32: hi, mid, lo pieces).
+ * Valid until the next call on the context.
  */
 rkv_status rkv_debug_scratch(rkv_ctx* ctx, int32_t which, void** ptr, size_t* bytes);
 

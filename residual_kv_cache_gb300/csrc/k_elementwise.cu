@@ -191,21 +191,26 @@ __global__ void __launch_bounds__(256)
 }
 
 // ---------------------------------------------------------------- mean rows
-// One warp per compact row r: X[2r] = bf16 kv (the hi piece of the query row),
-// X[2r+1] = bf16(mean of the retrieved FP8 references).  The sum of at most four
-// E4M3 values is exact in fp32; it is divided by k_i once, correctly rounded.  Each lane
-// takes 8-element pieces e = (32 u + lane) * 8, four pieces in flight at a time.
+// One warp per retrieval-order row q: M[q] = bf16(mean of the row's retrieved FP8
+// references), zeros for a padding row.  The sum of at most four E4M3 values is exact
+// in fp32; it is divided by k_i once, correctly rounded.  Each lane takes 8-element
+// pieces e = (32 u + lane) * 8, four pieces in flight at a time.  (The row's kv operand
+// is read by the encoder GEMM straight from the query rows.)
 __global__ void __launch_bounds__(256)
-    mean_rows_kernel(const int32_t* __restrict__ c_q, const int32_t* __restrict__ c_dst,
-                     const __nv_bfloat16* __restrict__ Q, int parts,
-                     const uint8_t* __restrict__ pool8, const int32_t* __restrict__ ref_idx,
-                     int topk, int dkv, int T_cap, int R_cap, int n_rows,
-                     __nv_bfloat16* __restrict__ X, int* __restrict__ status) {
+    mean_rows_kernel(const int32_t* __restrict__ q_dst, const uint8_t* __restrict__ pool8,
+                     const int32_t* __restrict__ ref_idx, int topk, int dkv, int T_cap,
+                     int R_cap, int m_pad, __nv_bfloat16* __restrict__ M,
+                     int* __restrict__ status) {
   const int lane = threadIdx.x & 31;
-  for (int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); r < n_rows;
-       r += (int64_t)gridDim.x * 8) {
-    const int64_t qrow = c_q[r];
-    const int64_t dst = c_dst[r];
+  for (int64_t q = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); q < m_pad;
+       q += (int64_t)gridDim.x * 8) {
+    const int64_t dst = q_dst[q];
+    __nv_bfloat16* xm = M + q * (int64_t)dkv;
+    if (dst < 0) {
+      for (int e = lane * 8; e < dkv; e += 256)
+        *reinterpret_cast<uint4*>(xm + e) = make_uint4(0u, 0u, 0u, 0u);
+      continue;
+    }
     const int64_t seq = dst / T_cap;
     const int32_t my = lane < topk ? ref_idx[dst * topk + lane] : -1;
     int64_t prow[4];
@@ -222,17 +227,12 @@ __global__ void __launch_bounds__(256)
     // the sum divided by k_i, correctly rounded: a multiply by the exact reciprocal for
     // k_i = 1, 2, 4, and the FMA-corrected division for k_i = 3
     const float kinv = 1.0f / (float)(k_i == 2 ? 2 : (k_i == 4 ? 4 : 1));
-    const __nv_bfloat16* q = Q + qrow * (int64_t)parts * dkv;
-    __nv_bfloat16* xk = X + (2 * r) * (int64_t)dkv;
-    __nv_bfloat16* xm = X + (2 * r + 1) * (int64_t)dkv;
     for (int e0 = 0; e0 < dkv; e0 += 4 * 256) {
-      uint4 qv[4];
       uint2 rv[4][4];
 #pragma unroll
       for (int u = 0; u < 4; ++u) {
         const int e = e0 + (u * 32 + lane) * 8;
         if (e < dkv) {
-          qv[u] = *reinterpret_cast<const uint4*>(q + e);
 #pragma unroll
           for (int t = 0; t < 4; ++t)
             rv[t][u] = ok[t] ? *reinterpret_cast<const uint2*>(pool8 + prow[t] * dkv + e)
@@ -243,7 +243,6 @@ __global__ void __launch_bounds__(256)
       for (int u = 0; u < 4; ++u) {
         const int e = e0 + (u * 32 + lane) * 8;
         if (e >= dkv) continue;
-        *reinterpret_cast<uint4*>(xk + e) = qv[u];
         // exact sums of the E4M3 values (in any order: at most four of them)
         float s8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -342,10 +341,9 @@ cudaError_t launch_mean_rows(rkv_ctx* c, const PassPlan& p, const int32_t* plan,
   const Dims& d = c->d;
   cudaEvent_t ev;
   timing_begin(c, "rkv_mean_rows_kernel", s, &ev);
-  mean_rows_kernel<<<grid_for(p.n_rows, 8, 16 * c->num_sms), 256, 0, s>>>(
-      plan + p.off_c_q, plan + p.off_c_dst, c->Q, d.parts,
-      static_cast<const uint8_t*>(c->st.pool_fp8), c->st.ref_idx, d.topk, d.dkv, d.T_cap, d.R_cap,
-      p.n_rows, c->X, c->status);
+  mean_rows_kernel<<<grid_for(p.m_pad, 8, 16 * c->num_sms), 256, 0, s>>>(
+      plan + p.off_q_dst, static_cast<const uint8_t*>(c->st.pool_fp8), c->st.ref_idx, d.topk,
+      d.dkv, d.T_cap, d.R_cap, p.m_pad, c->M, c->status);
   cudaError_t e = cudaGetLastError();
   timing_end(c, "rkv_mean_rows_kernel", s, ev);
   return e;

@@ -1,13 +1,15 @@
 // k_gemm.cu - the encoder's two tensor-core GEMMs (ResidualKV notes §2.3, §2.4).
 //
 //   GEMM-1/2:  [kv; mean] rows x [W_c1 | W_c2]  ->  H = Swish(a1) * a2   (bf16)
-//              A = X [2n, 2d_k] (row 2r = bf16 kv_r, row 2r+1 = bf16 mean_r),
+//              A tile m (128 rows) = the bf16 kv rows of retrieval rows q = 64 m .. 64 m
+//              + 63 (the first 2d_k columns of the query rows Q) over their bf16 mean rows
+//              (M), two 64-row TMA boxes into one swizzled stage;
 //              B = W12 [2 d_ff, 2d_k] with gate and value columns interleaved per
 //              256-row tile so that one 128x256 accumulator holds a1 and a2 of the same
-//              128 hidden units.  The epilogue applies the SwiGLU gate and stores the
-//              mean rows negated (an exact bf16 sign flip).
-//   GEMM-3:    H viewed as [n, 2 d_ff] (row r = [h(kv_r) | -h(mean_r)]) x W_c3^T
-//              -> z_r = h(kv_r) W_c3 - h(mean_r) W_c3 in one fp32 accumulator: both f_c
+//              128 hidden units.  The epilogue applies the SwiGLU gate and stores
+//              h(kv_q) as H row 2q and -h(mean_q) as row 2q + 1 (an exact bf16 sign flip).
+//   GEMM-3:    H viewed as [m, 2 d_ff] (row q = [h(kv_q) | -h(mean_q)]) x W_c3^T
+//              -> z_q = h(kv_q) W_c3 - h(mean_q) W_c3 in one fp32 accumulator: both f_c
 //              outputs are mapped before the subtraction, never f_c of a difference.
 //              The epilogue quantises each 32-column group in the thread that owns the
 //              token row (min/max, FP16 extremes rounded outward, Delta, round-half-
@@ -33,12 +35,12 @@ struct GemmShape {
 struct Epi12Args {
   __nv_bfloat16* H;
   int dff;
-  int rows;  // valid A rows (2 n)
+  int rows;  // retrieval-order rows (kv and mean row pairs)
 };
 
 struct Epi3Args {
-  const int32_t* c_dst;
-  int rows;  // valid token rows
+  const int32_t* q_dst;  // per retrieval row: storage row, -1 for padding
+  int rows;              // retrieval-order rows
   uint8_t* codes;
   uint32_t* meta;
   int code_bytes, G, bits, BN;
@@ -54,11 +56,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 struct Epi12 {
   using Args = Epi12Args;
   static constexpr int BN = kEncN;
+  static constexpr bool kSplitA = true;
   __device__ static void run(const Args& a, uint32_t tacc, int m, int n, int row_in_tile,
                              int* status) {
-    const int64_t row = (int64_t)m * kTileM + row_in_tile;
-    const bool valid = row < a.rows;
-    const float sign = (row & 1) ? -1.0f : 1.0f;
+    // tile row i holds the kv (i < 64) or mean (i >= 64) row of retrieval row 64 m + i % 64
+    const int half = row_in_tile >= kTileM / 2 ? 1 : 0;
+    const int64_t q = (int64_t)m * (kTileM / 2) + (row_in_tile & (kTileM / 2 - 1));
+    const int64_t row = 2 * q + half;
+    const bool valid = q < a.rows;
+    const float sign = half ? -1.0f : 1.0f;
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
       uint32_t g[32], v[32];
@@ -152,11 +158,12 @@ __device__ __forceinline__ void quant_group(const float* z, int bits, uint8_t* c
 
 struct Epi3 {
   using Args = Epi3Args;
+  static constexpr bool kSplitA = false;
   __device__ static void run(const Args& a, uint32_t tacc, int m, int n, int row_in_tile,
                              int* status) {
     const int64_t row = (int64_t)m * kTileM + row_in_tile;
-    const bool valid = row < a.rows;
-    const int64_t dst = valid ? (int64_t)a.c_dst[row] : 0;
+    const int64_t dst = row < a.rows ? (int64_t)a.q_dst[row] : -1;
+    const bool valid = dst >= 0;                     // padding rows are not stored
     const int groups = a.BN / 32;
 #pragma unroll 1
     for (int gi = 0; gi < groups; ++gi) {
@@ -178,8 +185,8 @@ struct Epi3 {
 // ---------------------------------------------------------------- kernel
 template <int BN, int STAGES, typename Epi>
 __global__ void __launch_bounds__(kThreads, 1)
-    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                   GemmShape g, typename Epi::Args ea) {
+    tc_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA2,
+                   const __grid_constant__ CUtensorMap tmB, GemmShape g, typename Epi::Args ea) {
   constexpr uint32_t kBBytes = BN * 128;
   constexpr uint32_t kTmemCols = 2 * BN;
   extern __shared__ uint8_t smem_raw[];
@@ -208,6 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     *abort_flag = 0;
     fence_barrier_init();
     tma_prefetch(&tmA);
+    if (Epi::kSplitA) tma_prefetch(&tmA2);
     tma_prefetch(&tmB);
   }
   if (warp == 2) {
@@ -235,8 +243,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           mbar_arrive_expect_tx(&full[ring.stage], kTileABytes + kBBytes);
-          tma_load_2d(sA + ring.stage * kTileABytes, &tmA, &full[ring.stage], kb * kTileK,
-                      m * kTileM);
+          if (Epi::kSplitA) {
+            // rows 0..63 from tmA, rows 64..127 from tmA2 (the same 64 retrieval rows)
+            tma_load_2d(sA + ring.stage * kTileABytes, &tmA, &full[ring.stage], kb * kTileK,
+                        m * (kTileM / 2));
+            tma_load_2d(sA + ring.stage * kTileABytes + kTileABytes / 2, &tmA2, &full[ring.stage],
+                        kb * kTileK, m * (kTileM / 2));
+          } else {
+            tma_load_2d(sA + ring.stage * kTileABytes, &tmA, &full[ring.stage], kb * kTileK,
+                        m * kTileM);
+          }
           const int kbB = kb % g.b_kwrap;
           for (int h = 0; h < BN; h += 256)
             tma_load_2d(sB + ring.stage * kBBytes + h * 128, &tmB, &full[ring.stage],
@@ -334,8 +350,8 @@ constexpr size_t gemm_smem_bytes() {
 }
 
 template <int BN, int STAGES, typename Epi>
-cudaError_t run_gemm(rkv_ctx* c, const CUtensorMap& tA, const CUtensorMap& tB, GemmShape g,
-                     typename Epi::Args ea, const char* name, cudaStream_t s) {
+cudaError_t run_gemm(rkv_ctx* c, const CUtensorMap& tA, const CUtensorMap& tA2, const CUtensorMap& tB,
+                     GemmShape g, typename Epi::Args ea, const char* name, cudaStream_t s) {
   const size_t smem = gemm_smem_bytes<BN, STAGES>();
   auto kern = tc_gemm_kernel<BN, STAGES, Epi>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -345,7 +361,7 @@ cudaError_t run_gemm(rkv_ctx* c, const CUtensorMap& tA, const CUtensorMap& tB, G
   const int grid = tiles < c->num_sms ? tiles : c->num_sms;
   cudaEvent_t ev;
   timing_begin(c, name, s, &ev);
-  kern<<<grid, kThreads, smem, s>>>(tA, tB, g, ea);
+  kern<<<grid, kThreads, smem, s>>>(tA, tA2, tB, g, ea);
   e = cudaGetLastError();
   timing_end(c, name, s, ev);
   return e;
@@ -353,27 +369,28 @@ cudaError_t run_gemm(rkv_ctx* c, const CUtensorMap& tA, const CUtensorMap& tB, G
 
 }  // namespace
 
-cudaError_t launch_gemm12(rkv_ctx* c, int n_rows, cudaStream_t s) {
+cudaError_t launch_gemm12(rkv_ctx* c, int m_pad, cudaStream_t s) {
   const Dims& d = c->d;
   GemmShape g;
-  g.m_tiles = (2 * n_rows + kTileM - 1) / kTileM;
+  g.m_tiles = (m_pad + kTileM / 2 - 1) / (kTileM / 2);
   g.n_tiles = (2 * d.dff) / kEncN;
   g.nkb = d.dkv / kTileK;
   g.b_kwrap = g.nkb;
   g.status = c->status;
-  Epi12Args ea{c->H, d.dff, 2 * n_rows};
-  return run_gemm<kEncN, 4, Epi12>(c, c->tm_x, c->tm_w12, g, ea, "rkv_gemm12_swiglu_kernel", s);
+  Epi12Args ea{c->H, d.dff, m_pad};
+  return run_gemm<kEncN, 4, Epi12>(c, c->tm_qa, c->tm_m, c->tm_w12, g, ea,
+                                   "rkv_gemm12_swiglu_kernel", s);
 }
 
 cudaError_t launch_gemm3_quant(rkv_ctx* c, const PassPlan& p, const int32_t* plan,
                                cudaStream_t s) {
   const Dims& d = c->d;
   GemmShape g;
-  g.m_tiles = (p.n_rows + kTileM - 1) / kTileM;
+  g.m_tiles = (p.m_pad + kTileM - 1) / kTileM;
   g.nkb = (2 * d.dff) / kTileK;
   g.b_kwrap = d.dff / kTileK;
   g.status = c->status;
-  Epi3Args ea{plan + p.off_c_dst, p.n_rows, static_cast<uint8_t*>(c->st.codes),
+  Epi3Args ea{plan + p.off_q_dst, p.m_pad, static_cast<uint8_t*>(c->st.codes),
               static_cast<uint32_t*>(c->st.meta), d.code_bytes, d.G, d.bits, 0};
   const char* name = "rkv_gemm3_quant_kernel";
   // Tile width: the one whose whole waves of one-tile-per-SM finish first (a tile's
@@ -385,17 +402,17 @@ cudaError_t launch_gemm3_quant(rkv_ctx* c, const PassPlan& p, const int32_t* pla
   if (d.dc % 256 == 0 && waves(256) <= waves(128)) {
     g.n_tiles = d.dc / 256;
     ea.BN = 256;
-    return run_gemm<256, 4, Epi3>(c, c->tm_h3, c->tm_w3, g, ea, name, s);
+    return run_gemm<256, 4, Epi3>(c, c->tm_h3, c->tm_h3, c->tm_w3, g, ea, name, s);
   }
   if (d.dc % 128 == 0) {
     g.n_tiles = d.dc / 128;
     ea.BN = 128;
-    return run_gemm<128, 6, Epi3>(c, c->tm_h3, d.dc % 256 == 0 ? c->tm_w3_128 : c->tm_w3, g, ea,
-                                  name, s);
+    return run_gemm<128, 6, Epi3>(c, c->tm_h3, c->tm_h3,
+                                  d.dc % 256 == 0 ? c->tm_w3_128 : c->tm_w3, g, ea, name, s);
   }
   g.n_tiles = d.dc / 64;
   ea.BN = 64;
-  return run_gemm<64, 6, Epi3>(c, c->tm_h3, c->tm_w3, g, ea, name, s);
+  return run_gemm<64, 6, Epi3>(c, c->tm_h3, c->tm_h3, c->tm_w3, g, ea, name, s);
 }
 
 }  // namespace rkv

@@ -18,7 +18,9 @@
 // pairs x <= 4 references, 16-byte cp.async copies into a private shared-memory slot
 // per reference), so the reference gathers need no cross-warp synchronisation.  Each
 // epilogue thread then sums its row's references (exact in fp32), divides by k_i, adds
-// its accumulator row, rotates the K columns and stores K or V in whole 32-byte sectors.
+// its accumulator row, rotates the K columns and writes its 16 + 16 K or V values into
+// its warp's two shared-memory boxes (32 rows x 16 columns each), which one lane of the
+// warp stores by TMA; the tensor map clips the rows past the selection.
 //
 // Back-to-back launches overlap: every CTA lets the next launch of the stream start its
 // CTAs as SMs free up, and a thread waits for the previous grid to complete only before
@@ -26,8 +28,10 @@
 // and codes, dequantisation) hides behind the previous launch's last CTAs.  Nothing else
 // this kernel reads is written by it.
 //
-// The kernel is bound by the bytes each SM pulls from L2 per unit (128 KB of W_d^T plus
-// 64 KB of reference rows), not by the tensor core.
+// Per unit an SM pulls 128 KB of W_d^T and up to 64 KB of reference rows from L2; the
+// tensor core finishes a unit's MMAs well within the epilogue's time, so the kernel is
+// bound by the epilogue's dependent chains and the per-tile setup, not by the tensor
+// core or by HBM.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -41,6 +45,7 @@ namespace {
 // cap a thread at 96 registers.
 constexpr int kReconThreads = 640;
 constexpr int kEpiWarpR = 4;                 // first epilogue warp
+constexpr int kEpiWarps = 16;
 constexpr int kNT = 128;                     // output columns per unit
 constexpr uint32_t kBBytes = kNT * 128;      // one 64-wide k-block of W_d^T rows
 constexpr uint32_t kPlaneBytes = kTileM * 32;            // one 32-byte sector per tile row
@@ -94,14 +99,12 @@ __device__ __forceinline__ void fp8x16_add(uint4 v, float* s) {
 
 // Per-tile state of one epilogue thread's token row, packed into two registers.
 struct RowState {
-  int flags;    // bit 0: the row has a readable code and a first reference; bit 1: the
-                // row is one of the n_sel selected tokens; bits 2..5: reference t is a
-                // valid slot; bits 6..: k_i
+  int flags;    // bit 0: the row has a readable code and a first reference; bits 1..4:
+                // reference t is a valid slot; bits 5..: k_i
   int pos;      // the token's position (RoPE)
   __device__ __forceinline__ bool valid() const { return flags & 1; }
-  __device__ __forceinline__ bool in_sel() const { return (flags >> 1) & 1; }
-  __device__ __forceinline__ bool has_ref(int t) const { return (flags >> (2 + t)) & 1; }
-  __device__ __forceinline__ int kcnt() const { return flags >> 6; }
+  __device__ __forceinline__ bool has_ref(int t) const { return (flags >> (1 + t)) & 1; }
+  __device__ __forceinline__ int kcnt() const { return flags >> 5; }
 };
 
 // A row's state, the pool rows of its references 0..3 (-1 where there is none) and the
@@ -191,9 +194,9 @@ __device__ __forceinline__ TileRow tile_setup(const ReconArgs& a, int m, int row
 #pragma unroll
     for (int t = 0; t < 4; ++t) tr.r[t] = -1;
   }
-  st.flags = (valid ? 1 : 0) | (in_sel ? 2 : 0) | (kcnt << 6);
+  st.flags = (valid ? 1 : 0) | (kcnt << 5);
 #pragma unroll
-  for (int t = 0; t < 4; ++t) st.flags |= (tr.r[t] >= 0 ? 1 : 0) << (2 + t);
+  for (int t = 0; t < 4; ++t) st.flags |= (tr.r[t] >= 0 ? 1 : 0) << (1 + t);
   // dequantise this row's share of code groups straight into TMEM
   if (a.bits == 16) {
     for (int g = g0; g < g0 + g_per; ++g) {
@@ -267,14 +270,17 @@ __device__ __forceinline__ int range_start(int b, int grid, int units, int n_til
 }
 
 __global__ void __launch_bounds__(kReconThreads, 1)
-    reconstruct_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ ReconArgs a) {
+    reconstruct_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ ReconArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int nkb = a.dc / kTileK;
   uint8_t* sB = smem;                                       // b_stages x W_d^T k-block
   uint8_t* sG = sB + a.b_stages * kBBytes;                  // per-warp reference slots
   float4* sCS = reinterpret_cast<float4*>(sG + kGBytes);
-  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sCS) + kCSBytes);
+  const uint32_t ob = a.out_f32 ? 64u : 32u;                // bytes of one output box row
+  uint8_t* sO = reinterpret_cast<uint8_t*>(sCS) + kCSBytes; // per-warp output boxes
+  uint64_t* full = reinterpret_cast<uint64_t*>(sO + kEpiWarps * 2 * 32 * ob);
   uint64_t* empty = full + a.b_stages;
   uint64_t* tfull = empty + a.b_stages;
   uint64_t* tempty = tfull + 2;
@@ -302,6 +308,8 @@ __global__ void __launch_bounds__(kReconThreads, 1)
     *abort_flag = 0;
     fence_barrier_init();
     tma_prefetch(&tmW);
+    tma_prefetch(&tmK);
+    tma_prefetch(&tmV);
   }
   if (warp == 0) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -579,34 +587,58 @@ __global__ void __launch_bounds__(kReconThreads, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i) mx[i] = 0.f, my[i] = 0.f;
       }
-      if (cur.in_sel()) {
+      // ---- output: stage this warp's two boxes, then one lane stores them by TMA (rows
+      // past the selection are clipped by the tensor map)
+      if (lane_id() == 0) bulk_wait_read0();           // the previous boxes have been read
+      __syncwarp();
+      // this warp's boxes (32 rows x 16 columns of x, then of y); lane r writes box row r,
+      // its 16-byte chunk c at chunk c ^ (bits of r), the tensor map's swizzle
+      uint8_t* so = sO + (uint32_t)(warp - kEpiWarpR) * (2 * 32 * ob);
+      const uint32_t so_row = (uint32_t)lane_id() * ob;
+      const uint32_t so_sw = a.out_f32 ? ((lane_id() >> 1) & 3u) : ((lane_id() >> 2) & 1u);
+      if (a.out_f32) {
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint32_t off = so_row + (((uint32_t)c ^ so_sw) << 4);
+          *reinterpret_cast<float4*>(so + off) =
+              make_float4(mx[4 * c], mx[4 * c + 1], mx[4 * c + 2], mx[4 * c + 3]);
+          *reinterpret_cast<float4*>(so + 32 * ob + off) =
+              make_float4(my[4 * c], my[4 * c + 1], my[4 * c + 2], my[4 * c + 3]);
+        }
+      } else {
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+          const uint32_t off = so_row + (((uint32_t)c ^ so_sw) << 4);
+          uint4 vx, vy;
+          vx.x = pack_bf16x2(mx[8 * c], mx[8 * c + 1]);
+          vx.y = pack_bf16x2(mx[8 * c + 2], mx[8 * c + 3]);
+          vx.z = pack_bf16x2(mx[8 * c + 4], mx[8 * c + 5]);
+          vx.w = pack_bf16x2(mx[8 * c + 6], mx[8 * c + 7]);
+          vy.x = pack_bf16x2(my[8 * c], my[8 * c + 1]);
+          vy.y = pack_bf16x2(my[8 * c + 2], my[8 * c + 3]);
+          vy.z = pack_bf16x2(my[8 * c + 4], my[8 * c + 5]);
+          vy.w = pack_bf16x2(my[8 * c + 6], my[8 * c + 7]);
+          *reinterpret_cast<uint4*>(so + off) = vx;
+          *reinterpret_cast<uint4*>(so + 32 * ob + off) = vy;
+        }
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      const int y0 = m * kTileM + ew * 32;
+      if (lane_id() == 0 && y0 < a.n_sel) {
         if (!waited) {
           pdl_wait_previous_grid();                    // K/V may be the previous launch's outputs
           waited = true;
         }
-        const int64_t gi = (int64_t)m * kTileM + row;
-        void* out = is_k ? a.k_out : a.v_out;
-        const int64_t rowoff = gi * (int64_t)a.dk + (is_k ? c0 : c0 - a.dk) + j0;
-        if (a.out_f32) {
-          float* o = static_cast<float*>(out) + rowoff;
-          st_global_v8(o, reinterpret_cast<const uint32_t*>(mx));
-          st_global_v8(o + 8, reinterpret_cast<const uint32_t*>(mx + 8));
-          st_global_v8(o + P, reinterpret_cast<const uint32_t*>(my));
-          st_global_v8(o + P + 8, reinterpret_cast<const uint32_t*>(my + 8));
-        } else {
-          uint32_t wx[8], wy[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            wx[i] = pack_bf16x2(mx[2 * i], mx[2 * i + 1]);
-            wy[i] = pack_bf16x2(my[2 * i], my[2 * i + 1]);
-          }
-          __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out) + rowoff;
-          st_global_v8(o, wx);                          // 16 bf16 = one 32-byte sector
-          st_global_v8(o + P, wy);
-        }
+        const CUtensorMap* om = is_k ? &tmK : &tmV;
+        const int x0 = (is_k ? c0 : c0 - a.dk) + j0;
+        tma_store_2d(om, so, x0, y0);
+        tma_store_2d(om, so + 32 * ob, x0 + P, y0);
+        bulk_commit();
       }
     }
     cp_async_wait<0>();                                // no copy may outlive the CTA
+    if (lane_id() == 0) bulk_wait0();                  // nor any output store
   }
 
   tc_fence_before();
@@ -623,7 +655,8 @@ cudaError_t launch_reconstruct(rkv_ctx* c, const int32_t* seq, const int32_t* po
                                void* k_out, void* v_out, cudaStream_t s) {
   const Dims& d = c->d;
   if (n_sel <= 0) return cudaSuccess;
-  const size_t fixed = 1024 + kCSBytes + kGBytes + kBarBytes;
+  const size_t obytes = (size_t)kEpiWarps * 2 * 32 * (d.out_f32 ? 64 : 32);
+  const size_t fixed = 1024 + kCSBytes + kGBytes + obytes + kBarBytes;
   int b_stages = (int)((232448 - fixed) / kBBytes);
   if (b_stages > kMaxStages) b_stages = kMaxStages;
   if (b_stages < 2) return cudaErrorInvalidConfiguration;
@@ -660,6 +693,10 @@ cudaError_t launch_reconstruct(rkv_ctx* c, const int32_t* seq, const int32_t* po
   a.bits = d.bits;
   a.code_bytes = d.code_bytes;
   a.status = c->status;
+  CUtensorMap tmK, tmV;
+  if (!make_out_map(&tmK, k_out, d.dk, n_sel, d.out_f32) ||
+      !make_out_map(&tmV, v_out, d.dk, n_sel, d.out_f32))
+    return cudaErrorInvalidValue;
   const int grid = a.units < c->num_sms ? a.units : c->num_sms;
   cudaEvent_t ev;
   timing_begin(c, "rkv_reconstruct_kernel", s, &ev);
@@ -673,7 +710,7 @@ cudaError_t launch_reconstruct(rkv_ctx* c, const int32_t* seq, const int32_t* po
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  e = cudaLaunchKernelEx(&lc, reconstruct_kernel, c->tm_wd, a);
+  e = cudaLaunchKernelEx(&lc, reconstruct_kernel, c->tm_wd, tmK, tmV, a);
   if (e == cudaSuccess) e = cudaGetLastError();
   timing_end(c, "rkv_reconstruct_kernel", s, ev);
   return e;

@@ -406,17 +406,4 @@ __device__ __forceinline__ float div3_rn(float s) {
   return __fmaf_rn(r, c, q);
 }
 
-// 32-byte store of eight 32-bit words (one whole sector); the address must be 32-byte aligned.
-__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* r) {
-  asm volatile("st.global.v8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"l"(p), "r"(r[0]), "r"(r[1]),
-               "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-               : "memory");
-}
-
-// Byte offset of 16-byte chunk `c` (0..7) of row `r` inside a 128-byte-swizzled tile
-// whose rows are 128 bytes: chunk index XOR (row mod 8).
-__host__ __device__ __forceinline__ uint32_t sw128_offset(uint32_t r, uint32_t c) {
-  return r * 128u + ((c ^ (r & 7u)) << 4);
-}
-
 }  // namespace rkv

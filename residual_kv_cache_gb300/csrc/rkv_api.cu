@@ -165,12 +165,12 @@ bool make_out_map(CUtensorMap* m, void* base, int64_t cols, int64_t rows, bool f
   const uint32_t es = f32 ? 4u : 2u;
   cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
   cuuint64_t strides[1] = {(cuuint64_t)cols * es};
-  cuuint32_t box[2] = {128u / es, (cuuint32_t)kTileM};
+  cuuint32_t box[2] = {16u, 32u};
   cuuint32_t estr[2] = {1u, 1u};
   CUresult r = g_encode(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
                         2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                        f32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
@@ -285,12 +285,11 @@ rkv_status compress_row_error(const rkv_ctx* c, const int32_t* src_rows, const i
   return fail(RKV_EINVAL, "invalid rows");
 }
 
-// Per-row plan entries of one tile's rows (retrieval slots q0 .. q0 + cnt - 1, compact
-// rows given by `rows`, or r_first .. r_first + cnt - 1 when `rows` is null) of sequence
-// s; returns the largest position among them (at least 1).
+// Per-row plan entries of one tile's rows (retrieval slots q0 .. q0 + cnt - 1, taking the
+// pass's rows given by `rows`, or r_first .. r_first + cnt - 1 when `rows` is null) of
+// sequence s; returns the largest position among them (at least 1).
 int fill_tile_rows(int32_t* h, const rkv::PassPlan& p, const rkv::Dims& d, const int32_t* src_rows,
-                   const int32_t* pos, const int* rows, int r_first, int r0, int cnt, int q0,
-                   int s) {
+                   const int32_t* pos, const int* rows, int r_first, int cnt, int q0, int s) {
   int32_t* __restrict__ qsrc = h + p.off_q_src + q0;
   int32_t* __restrict__ qpos = h + p.off_q_pos + q0;
   int32_t* __restrict__ qdst = h + p.off_q_dst + q0;
@@ -298,15 +297,11 @@ int fill_tile_rows(int32_t* h, const rkv::PassPlan& p, const rkv::Dims& d, const
   int maxpos = 1;
   if (!rows) {
     const int32_t* __restrict__ pp = pos + r_first;
-    int32_t* __restrict__ cq = h + p.off_c_q + (r_first - r0);
-    int32_t* __restrict__ cdst = h + p.off_c_dst + (r_first - r0);
     for (int r = 0; r < cnt; ++r) {
       const int pr = pp[r];
       maxpos = pr > maxpos ? pr : maxpos;
       qpos[r] = pr;
       qdst[r] = (int32_t)(sT + pr);
-      cdst[r] = (int32_t)(sT + pr);
-      cq[r] = q0 + r;
     }
     if (src_rows)
       std::memcpy(qsrc, src_rows + r_first, sizeof(int32_t) * cnt);
@@ -320,8 +315,6 @@ int fill_tile_rows(int32_t* h, const rkv::PassPlan& p, const rkv::Dims& d, const
       qsrc[r] = src_rows ? src_rows[row] : row;
       qpos[r] = pr;
       qdst[r] = (int32_t)(sT + pr);
-      h[p.off_c_q + (row - r0)] = q0 + r;
-      h[p.off_c_dst + (row - r0)] = (int32_t)(sT + pr);
     }
   }
   return maxpos;
@@ -392,8 +385,7 @@ rkv_status rkv_create(const rkv_config* cfg, const void* Wc1, const void* Wc2, c
   c->m_cap = c->max_rows + kTileM * std::min(d.B, c->max_rows);
   c->tiles_cap = c->m_cap / kTileM;
   c->units_cap = c->tiles_cap * ((d.R_cap + kRefTile - 1) / kRefTile);
-  c->plan_ints = std::max(3 * c->m_cap + 4 * c->tiles_cap + 2 * c->units_cap + 2 * c->max_rows,
-                          4 * c->max_rows);
+  c->plan_ints = std::max(3 * c->m_cap + 4 * c->tiles_cap + 2 * c->units_cap, 4 * c->max_rows);
   c->pool_count.assign(d.B, 0);
   c->ref_before.assign((size_t)d.T_cap + 1, 0);
   walk_schedule(d.T_cap, d.stride, d.alpha, d.sink, [&](int p) { c->ref_before[p + 1] = 1; });
@@ -410,8 +402,8 @@ rkv_status rkv_create(const rkv_config* cfg, const void* Wc1, const void* Wc2, c
   ALLOC(c->rope_lo, (size_t)kRopeLo * (d.D / 2) * sizeof(float2));
   ALLOC(c->rope_hi, (size_t)d.n_hi * (d.D / 2) * sizeof(float2));
   ALLOC(c->Q, (size_t)c->m_cap * d.parts * d.dkv * 2);
-  ALLOC(c->X, (size_t)2 * c->max_rows * d.dkv * 2);
-  ALLOC(c->H, (size_t)2 * c->max_rows * d.dff * 2);
+  ALLOC(c->M, (size_t)c->m_cap * d.dkv * 2);
+  ALLOC(c->H, (size_t)2 * c->m_cap * d.dff * 2);
   ALLOC(c->part, (size_t)c->units_cap * kTileM * 4 * sizeof(int2));
   ALLOC(c->attn_ws, sizeof(float) * kAttnMaxChunks * kAttnMaxGroup * d.N * (2 + d.D));
   ALLOC(c->attn_count, sizeof(int) * d.N);
@@ -460,9 +452,10 @@ rkv_status rkv_create(const rkv_config* cfg, const void* Wc1, const void* Wc2, c
   bool ok = true;
   ok &= make_map(&c->tm_q, c->Q, (uint64_t)d.parts * dkv, c->m_cap, (uint64_t)d.parts * dkv * 2, kTileM);
   ok &= make_map(&c->tm_pool, st->pool_bf16, dkv, (uint64_t)d.B * d.R_cap, dkv * 2, kRefTile);
-  ok &= make_map(&c->tm_x, c->X, dkv, (uint64_t)2 * c->max_rows, dkv * 2, kTileM);
+  ok &= make_map(&c->tm_qa, c->Q, dkv, c->m_cap, (uint64_t)d.parts * dkv * 2, kTileM / 2);
+  ok &= make_map(&c->tm_m, c->M, dkv, c->m_cap, dkv * 2, kTileM / 2);
   ok &= make_map(&c->tm_w12, c->w12, dkv, (uint64_t)2 * d.dff, dkv * 2, kEncN);
-  ok &= make_map(&c->tm_h3, c->H, (uint64_t)2 * d.dff, c->max_rows, (uint64_t)2 * d.dff * 2, kTileM);
+  ok &= make_map(&c->tm_h3, c->H, (uint64_t)2 * d.dff, c->m_cap, (uint64_t)2 * d.dff * 2, kTileM);
   const uint32_t bn3 = d.dc % 256 == 0 ? 256u : (d.dc % 128 == 0 ? 128u : 64u);
   ok &= make_map(&c->tm_w3, c->w3, d.dff, d.dc, (uint64_t)d.dff * 2, bn3);
   if (d.dc % 128 == 0)
@@ -476,8 +469,8 @@ rkv_status rkv_create(const rkv_config* cfg, const void* Wc1, const void* Wc2, c
   c->zero_line = reinterpret_cast<const uint8_t*>(c->status) + 256;
   cudaError_t e = cudaMemsetAsync(c->status, 0, 512, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(c->Q, 0, (size_t)c->m_cap * d.parts * d.dkv * 2, s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(c->X, 0, (size_t)2 * c->max_rows * d.dkv * 2, s);
-  if (e == cudaSuccess) e = cudaMemsetAsync(c->H, 0, (size_t)2 * c->max_rows * d.dff * 2, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(c->M, 0, (size_t)c->m_cap * d.dkv * 2, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(c->H, 0, (size_t)2 * c->m_cap * d.dff * 2, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(c->attn_count, 0, sizeof(int) * d.N, s);
   if (e == cudaSuccess) e = launch_init_storage(c, s);
   if (e == cudaSuccess)
@@ -612,9 +605,7 @@ rkv_status rkv_compress(rkv_ctx* c, const void* kv, int64_t kv_row_stride, const
     p.off_q_src = 0;
     p.off_q_pos = m_pad;
     p.off_q_dst = 2 * m_pad;
-    p.off_c_q = 3 * m_pad;
-    p.off_c_dst = p.off_c_q + m;
-    p.off_t_seq = p.off_c_dst + m;
+    p.off_t_seq = 3 * m_pad;
     p.off_t_row0 = p.off_t_seq + ntiles;
     p.off_t_nrt = p.off_t_row0 + ntiles;
     p.off_t_u0 = p.off_t_nrt + ntiles;
@@ -633,7 +624,7 @@ rkv_status rkv_compress(rkv_ctx* c, const void* kv, int64_t kv_row_stride, const
       for (int k = i; k < j; k += kTileM) {
         const int kend = std::min(j, k + kTileM);
         const int maxpos = fill_tile_rows(h, p, d, src_rows, pos, ord ? ord + k : nullptr, r0 + k,
-                                          r0, kend - k, q + (k - i), s);
+                                          kend - k, q + (k - i), s);
         const int nrt = (c->ref_before[maxpos] + kRefTile - 1) / kRefTile;
         tseq.push_back(s);
         trow0.push_back(q + (k - i));
@@ -671,7 +662,7 @@ rkv_status rkv_compress(rkv_ctx* c, const void* kv, int64_t kv_row_stride, const
     CUDA_OK(launch_retrieve(c, p, plan, st));
     CUDA_OK(launch_retrieve_merge(c, p, plan, st));
     CUDA_OK(launch_mean_rows(c, p, plan, st));
-    CUDA_OK(launch_gemm12(c, p.n_rows, st));
+    CUDA_OK(launch_gemm12(c, p.m_pad, st));
     CUDA_OK(launch_gemm3_quant(c, p, plan, st));
   }
   return RKV_OK;
@@ -743,7 +734,7 @@ void rkv_free(rkv_ctx* c) {
   cudaFree(c->rope_lo);
   cudaFree(c->rope_hi);
   cudaFree(c->Q);
-  cudaFree(c->X);
+  cudaFree(c->M);
   cudaFree(c->H);
   cudaFree(c->part);
   cudaFree(c->status);
@@ -798,13 +789,16 @@ rkv_status rkv_debug_timeout_probe(rkv_ctx* c, void* stream) {
 rkv_status rkv_debug_scratch(rkv_ctx* c, int32_t which, void** ptr, size_t* bytes) {
   if (!c || !ptr || !bytes) return fail(RKV_EINVAL, "NULL argument");
   if (which == 0) {
-    *ptr = c->X;
-    *bytes = (size_t)2 * c->max_rows * c->d.dkv * 2;
+    *ptr = c->M;
+    *bytes = (size_t)c->m_cap * c->d.dkv * 2;
   } else if (which == 1) {
     *ptr = c->H;
-    *bytes = (size_t)2 * c->max_rows * c->d.dff * 2;
+    *bytes = (size_t)2 * c->m_cap * c->d.dff * 2;
+  } else if (which == 2) {
+    *ptr = c->Q;
+    *bytes = (size_t)c->m_cap * c->d.parts * c->d.dkv * 2;
   } else {
-    return fail(RKV_EINVAL, "which must be 0 or 1");
+    return fail(RKV_EINVAL, "which must be 0, 1 or 2");
   }
   return RKV_OK;
 }

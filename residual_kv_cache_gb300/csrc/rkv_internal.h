@@ -50,7 +50,7 @@ struct PassPlan {
   int n_units = 0;     // retrieval units: (tile, 256-reference pool tile)
   // offsets (in int32 elements) inside the plan buffer
   int off_q_src, off_q_pos, off_q_dst, off_t_seq, off_t_row0, off_t_nrt, off_t_u0, off_u_tile,
-      off_u_rt, off_c_q, off_c_dst;
+      off_u_rt;
   int total_ints = 0;
 };
 
@@ -73,8 +73,9 @@ struct rkv_ctx {
   float2* rope_lo = nullptr;      // [512][D/2] (cos, sin)(l * theta_j)
   float2* rope_hi = nullptr;      // [n_hi][D/2] (cos, sin)(h * 512 * theta_j)
   __nv_bfloat16* Q = nullptr;     // [m_cap, parts * 2d_k] retrieval-order queries
-  __nv_bfloat16* X = nullptr;     // [2 max_rows, 2d_k] kv / mean rows interleaved
-  __nv_bfloat16* H = nullptr;     // [2 max_rows, d_ff] SwiGLU rows (mean rows negated)
+  __nv_bfloat16* M = nullptr;     // [m_cap, 2d_k] bf16 reference means, retrieval order
+  __nv_bfloat16* H = nullptr;     // [2 m_cap, d_ff] SwiGLU rows: 2q from kv, 2q + 1 from the
+                                  // mean (negated)
   int2* part = nullptr;           // [units_cap, 128, 4] partial top-k (distance bits, slot)
   float* attn_ws = nullptr;       // sparse attention chunk partials (m, l, acc), kAttnMaxChunks
                                   // x kAttnMaxGroup N query heads
@@ -89,7 +90,8 @@ struct rkv_ctx {
   const uint8_t* zero_line = nullptr;   // 256 zero bytes in the same block (gather source)
 
   // TMA descriptors (fixed addresses, built once)
-  CUtensorMap tm_q, tm_pool, tm_x, tm_w12, tm_h3, tm_w3, tm_w3_128, tm_wd;
+  CUtensorMap tm_q, tm_pool, tm_w12, tm_h3, tm_w3, tm_w3_128, tm_wd;
+  CUtensorMap tm_qa, tm_m;        // GEMM-1/2 A halves: the bf16 kv piece of Q, and M (64 rows)
 
   // host mirror of each sequence's pool fill
   std::vector<int32_t> pool_count;
@@ -117,7 +119,7 @@ cudaError_t launch_retrieve(rkv_ctx* c, const PassPlan& p, const int32_t* plan, 
 cudaError_t launch_retrieve_merge(rkv_ctx* c, const PassPlan& p, const int32_t* plan,
                                   cudaStream_t s);
 cudaError_t launch_mean_rows(rkv_ctx* c, const PassPlan& p, const int32_t* plan, cudaStream_t s);
-cudaError_t launch_gemm12(rkv_ctx* c, int n_rows, cudaStream_t s);
+cudaError_t launch_gemm12(rkv_ctx* c, int m_pad, cudaStream_t s);
 cudaError_t launch_gemm3_quant(rkv_ctx* c, const PassPlan& p, const int32_t* plan,
                                cudaStream_t s);
 cudaError_t launch_reconstruct(rkv_ctx* c, const int32_t* seq, const int32_t* pos, int n_sel,
@@ -135,7 +137,8 @@ cudaError_t launch_attention(rkv_ctx* c, const float* q, int n_q_heads, const vo
                              const void* v, int n, float* out, cudaStream_t s);
 
 // Tensor map of a row-major [rows, cols] output matrix (bf16 or fp32) for 2-D tiled
-// stores: box = {128 bytes of columns, 128 rows}, 128-byte swizzle.
+// stores: box = {16 columns, 32 rows}, swizzled over the box's row bytes (32 or 64), so
+// that a warp writing one box row per lane in 16-byte chunks hits distinct banks.
 bool make_out_map(CUtensorMap* m, void* base, int64_t cols, int64_t rows, bool f32);
 
 // Record the message rkv_last_error returns on this thread.

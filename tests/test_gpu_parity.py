@@ -154,15 +154,20 @@ def test_encoder_operand_rows_bit_exact(name, request):
     r = request.getfixturevalue(name)
     c, st, w = r["codec"], r["store"], r["w"]
     non = r["non"]
-    ptr, nbytes = c.debug_scratch(0)
-    X = device_bytes(ptr, 2 * len(non) * w.d_kv * 2).view(torch.bfloat16).view(2 * len(non), w.d_kv)
-    X = np64(X)
-    assert np.array_equal(X[0::2], F.bf16(r["kv64"][non]))
+    # the kv operand: the first 2d_k columns of the query rows (one sequence: row q = row q)
+    parts = 3 if w.kv_dtype == "fp32" else 1
+    ptr, _ = c.debug_scratch(2)
+    Q = np64(device_bytes(ptr, len(non) * parts * w.d_kv * 2).view(torch.bfloat16)
+             .view(len(non), parts * w.d_kv))
+    assert np.array_equal(Q[:, :w.d_kv], F.bf16(r["kv64"][non]))
+    # the mean operand
+    ptr, _ = c.debug_scratch(0)
+    Mg = np64(device_bytes(ptr, len(non) * w.d_kv * 2).view(torch.bfloat16).view(len(non), w.d_kv))
     ok = set(_same_idx_rows(r).tolist())
     rows = [i for i, p in enumerate(non) if p in ok]
     means = np.stack([C.reference_mean(st.pool.vals, st.idx[non[i]][st.idx[non[i]] >= 0])
                       for i in rows])
-    assert np.array_equal(X[1::2][rows], F.bf16(means))
+    assert np.array_equal(Mg[rows], F.bf16(means))
 
 
 @cuda
