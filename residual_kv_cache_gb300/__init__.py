@@ -125,9 +125,18 @@ def _host_i32(a):
     return arr, arr.ctypes.data
 
 
+# The current stream's raw handle without building a Stream object (a few microseconds
+# per call on the host, which an idle GPU waits for); the public call is the fallback.
+_raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
+_cur_device = getattr(torch._C, "_cuda_getDevice", None)
+
+
 def _stream_ptr(stream) -> int:
-    s = stream if stream is not None else torch.cuda.current_stream()
-    return s.cuda_stream
+    if stream is not None:
+        return stream.cuda_stream
+    if _raw_stream is not None and _cur_device is not None:
+        return _raw_stream(_cur_device())
+    return torch.cuda.current_stream().cuda_stream
 
 
 @dataclass

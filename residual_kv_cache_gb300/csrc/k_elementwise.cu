@@ -59,65 +59,86 @@ __global__ void repack_kernel(const __nv_bfloat16* __restrict__ a, const __nv_bf
 }
 
 // ---------------------------------------------------------------- pool append
-// One block per reference row.  plan row: {src row, pool row, pos, token row}.
-__global__ void pool_append_kernel(const void* __restrict__ kv, int64_t stride, int kv_f32,
-                                   const int32_t* __restrict__ plan, int dkv, int R_cap,
-                                   uint8_t* __restrict__ pool8, __nv_bfloat16* __restrict__ poolb,
-                                   float* __restrict__ norm2, int32_t* __restrict__ pool_pos,
-                                   int32_t* __restrict__ ref_idx, int topk,
-                                   uint8_t* __restrict__ codes, int code_bytes,
-                                   uint32_t* __restrict__ meta, int G) {
-  const int r = blockIdx.x;
+// One warp per reference row (plan row: {src row, pool row, pos, token row}).  Lane l
+// takes the 8-element pieces e = (32 u + l) * 8: all of its loads are issued before any
+// conversion, and the FP8 and bf16 stores of a warp cover whole contiguous segments.
+// The squared norm of the FP8 row is summed in float64, exact in any order (squares of
+// E4M3 values span 2^-18 .. 2^18, at most 2^12 of them per row), then rounded once.
+template <bool F32>
+__global__ void __launch_bounds__(256)
+    pool_append_kernel(const void* __restrict__ kv, int64_t stride,
+                       const int32_t* __restrict__ plan, int n, int dkv, int R_cap,
+                       uint8_t* __restrict__ pool8, __nv_bfloat16* __restrict__ poolb,
+                       float* __restrict__ norm2, int32_t* __restrict__ pool_pos,
+                       int32_t* __restrict__ ref_idx, int topk, uint8_t* __restrict__ codes,
+                       int code_bytes, uint32_t* __restrict__ meta, int G) {
+  constexpr int kPieces = F32 ? 4 : 8;          // pieces per lane in flight (32 registers)
+  constexpr int kWords = F32 ? 2 : 1;           // 16-byte words per piece
+  const int lane = threadIdx.x & 31;
+  const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (r >= n) return;
   const int64_t src = plan[4 * r + 0];
   const int64_t prow = plan[4 * r + 1];
   const int32_t pos = plan[4 * r + 2];
   const int64_t tok = plan[4 * r + 3];
+  const uint4* in = reinterpret_cast<const uint4*>(
+      static_cast<const uint8_t*>(kv) + src * stride * (F32 ? 4 : 2));
   double acc = 0.0;
-  for (int e = threadIdx.x * 4; e < dkv; e += blockDim.x * 4) {
-    float v[4];
-    if (kv_f32) {
-      const float4 x = *reinterpret_cast<const float4*>(
-          static_cast<const float*>(kv) + src * stride + e);
-      v[0] = x.x; v[1] = x.y; v[2] = x.z; v[3] = x.w;
-    } else {
-      const uint2 x = *reinterpret_cast<const uint2*>(
-          static_cast<const __nv_bfloat16*>(kv) + src * stride + e);
-      v[0] = __uint_as_float(x.x << 16);
-      v[1] = __uint_as_float(x.x & 0xFFFF0000u);
-      v[2] = __uint_as_float(x.y << 16);
-      v[3] = __uint_as_float(x.y & 0xFFFF0000u);
-    }
-    uint32_t packed = 0;
-    float d[4];
+  for (int u0 = 0; u0 * 256 < dkv; u0 += kPieces) {
+    uint4 raw[kPieces][kWords];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const __nv_fp8_storage_t q = __nv_cvt_float_to_fp8(v[i], __NV_SATFINITE, __NV_E4M3);
-      packed |= static_cast<uint32_t>(q) << (8 * i);
-      d[i] = fp8_to_float(q);
-      acc += (double)d[i] * (double)d[i];   // exact: squares of E4M3 values
+    for (int u = 0; u < kPieces; ++u) {
+      const int e = ((u0 + u) * 32 + lane) * 8;
+      if (e < dkv) {
+#pragma unroll
+        for (int w = 0; w < kWords; ++w) raw[u][w] = in[e / (8 / kWords) + w];
+      }
     }
-    *reinterpret_cast<uint32_t*>(pool8 + prow * dkv + e) = packed;
-    uint2 bv;
-    bv.x = pack_bf16x2(d[0], d[1]);
-    bv.y = pack_bf16x2(d[2], d[3]);
-    *reinterpret_cast<uint2*>(poolb + prow * dkv + e) = bv;
+#pragma unroll
+    for (int u = 0; u < kPieces; ++u) {
+      const int e = ((u0 + u) * 32 + lane) * 8;
+      if (e >= dkv) continue;
+      float v[8];
+      if (F32) {
+#pragma unroll
+        for (int w = 0; w < kWords; ++w) {
+          v[4 * w] = __uint_as_float(raw[u][w].x), v[4 * w + 1] = __uint_as_float(raw[u][w].y);
+          v[4 * w + 2] = __uint_as_float(raw[u][w].z), v[4 * w + 3] = __uint_as_float(raw[u][w].w);
+        }
+      } else {
+        const uint32_t x[4] = {raw[u][0].x, raw[u][0].y, raw[u][0].z, raw[u][0].w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          v[2 * i] = __uint_as_float(x[i] << 16);
+          v[2 * i + 1] = __uint_as_float(x[i] & 0xFFFF0000u);
+        }
+      }
+      uint32_t packed[2] = {0u, 0u};
+      float d[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const __nv_fp8_storage_t q = __nv_cvt_float_to_fp8(v[i], __NV_SATFINITE, __NV_E4M3);
+        packed[i >> 2] |= static_cast<uint32_t>(q) << (8 * (i & 3));
+        d[i] = fp8_to_float(q);
+        acc += (double)d[i] * (double)d[i];   // exact: squares of E4M3 values
+      }
+      *reinterpret_cast<uint2*>(pool8 + prow * dkv + e) = make_uint2(packed[0], packed[1]);
+      *reinterpret_cast<uint4*>(poolb + prow * dkv + e) =
+          make_uint4(pack_bf16x2(d[0], d[1]), pack_bf16x2(d[2], d[3]), pack_bf16x2(d[4], d[5]),
+                     pack_bf16x2(d[6], d[7]));
+    }
   }
-  // block sum of the squared norm (float64, exact in any order)
-  __shared__ double red[32];
+#pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    double s = 0.0;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) s += red[w];
-    norm2[prow] = (float)s;
+  if (lane == 0) {
+    norm2[prow] = (float)acc;
     pool_pos[prow] = pos;
-    const int32_t slot = (int32_t)(prow % R_cap);
-    ref_idx[tok * topk] = slot;
-    for (int t = 1; t < topk; ++t) ref_idx[tok * topk + t] = -1;
   }
-  for (int i = threadIdx.x; i < code_bytes; i += blockDim.x) codes[tok * code_bytes + i] = 0;
-  for (int i = threadIdx.x; i < G; i += blockDim.x) meta[tok * G + i] = 0u;
+  // the reference token's own entry: itself as the first reference, no code
+  for (int t = lane; t < topk; t += 32) ref_idx[tok * topk + t] = t == 0 ? (int32_t)(prow % R_cap) : -1;
+  for (int i = lane; i < code_bytes / 16; i += 32)
+    reinterpret_cast<uint4*>(codes + tok * code_bytes)[i] = make_uint4(0u, 0u, 0u, 0u);
+  for (int i = lane; i < G; i += 32) meta[tok * G + i] = 0u;
 }
 
 // ---------------------------------------------------------------- queries
@@ -311,12 +332,13 @@ cudaError_t launch_pool_append(rkv_ctx* c, const void* kv, int64_t stride, const
   const Dims& d = c->d;
   cudaEvent_t ev;
   timing_begin(c, "rkv_pool_append_kernel", s, &ev);
-  pool_append_kernel<<<n, 256, 0, s>>>(kv, stride, d.kv_f32, plan, d.dkv, d.R_cap,
-                                       static_cast<uint8_t*>(c->st.pool_fp8),
-                                       static_cast<__nv_bfloat16*>(c->st.pool_bf16),
-                                       c->st.pool_norm2, c->st.pool_pos, c->st.ref_idx, d.topk,
-                                       static_cast<uint8_t*>(c->st.codes), d.code_bytes,
-                                       static_cast<uint32_t*>(c->st.meta), d.G);
+  auto kern = d.kv_f32 ? pool_append_kernel<true> : pool_append_kernel<false>;
+  kern<<<(n + 7) / 8, 256, 0, s>>>(kv, stride, plan, n, d.dkv, d.R_cap,
+                                   static_cast<uint8_t*>(c->st.pool_fp8),
+                                   static_cast<__nv_bfloat16*>(c->st.pool_bf16), c->st.pool_norm2,
+                                   c->st.pool_pos, c->st.ref_idx, d.topk,
+                                   static_cast<uint8_t*>(c->st.codes), d.code_bytes,
+                                   static_cast<uint32_t*>(c->st.meta), d.G);
   cudaError_t e = cudaGetLastError();
   timing_end(c, "rkv_pool_append_kernel", s, ev);
   return e;

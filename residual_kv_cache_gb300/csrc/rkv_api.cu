@@ -147,9 +147,11 @@ int32_t* staging_acquire(rkv_ctx* c, int* which) {
   return c->plan_host[b];
 }
 
-cudaError_t staging_upload(rkv_ctx* c, int b, int n_ints, cudaStream_t s) {
-  cudaError_t e = cudaMemcpyAsync(c->plan_dev[b], c->plan_host[b], sizeof(int32_t) * n_ints,
-                                  cudaMemcpyHostToDevice, s);
+// Upload ints [first, first + n_ints) of staging buffer b; the buffer is free again once
+// the event recorded after its last upload has completed.
+cudaError_t staging_upload(rkv_ctx* c, int b, int first, int n_ints, cudaStream_t s) {
+  cudaError_t e = cudaMemcpyAsync(c->plan_dev[b] + first, c->plan_host[b] + first,
+                                  sizeof(int32_t) * n_ints, cudaMemcpyHostToDevice, s);
   if (e != cudaSuccess) return e;
   return cudaEventRecord(c->plan_copied[b], s);
 }
@@ -247,11 +249,34 @@ RowScan scan_compress_rows(const rkv::Dims& d, const int32_t* ref_before, const 
   return {bad != 0, dec == 0, changes + 1, max_pos};
 }
 
+// Whether the rows of a pool append are one sequence's next n reference slots in order
+// (in range, reference positions, non-negative sources); branch-free over the rows.
+bool append_rows_ok_one_seq(const rkv_ctx* c, const int32_t* src_rows, const int32_t* seq,
+                            const int32_t* pos, int n) {
+  const rkv::Dims& d = c->d;
+  const int s = seq[0];
+  if ((unsigned)s >= (unsigned)d.B) return false;
+  const int base = c->pool_count[s];
+  if ((int64_t)base + n > d.R_cap) return false;
+  const int32_t* __restrict__ rb = c->ref_before.data();
+  unsigned bad = 0;
+  for (int i = 0; i < n; ++i) {
+    const int p = pos[i];
+    const unsigned p_bad = (unsigned)p >= (unsigned)d.T_cap;
+    const int pc = p_bad ? 0 : p;
+    const int slot = rb[pc];
+    bad |= (unsigned)(seq[i] != s) | p_bad | (unsigned)(rb[pc + 1] == slot) |
+           (unsigned)(slot != base + i);
+  }
+  if (src_rows)
+    for (int i = 0; i < n; ++i) bad |= (unsigned)src_rows[i] >> 31;
+  return bad == 0;
+}
+
 // Whether some row's sequence has no reference, or lacks references before the row's
 // position (the references before p are the ceil(p / stride) positions 0, stride, ...).
 bool compress_pools_bad(const rkv_ctx* c, const RowScan& r, const int32_t* seq,
                         const int32_t* pos, int n) {
-  const rkv::Dims& d = c->d;
   // ref_before is non-decreasing, so one sequence needs only its largest position
   if (r.runs == 1) {
     const int cnt = c->pool_count[seq[0]];
@@ -285,37 +310,36 @@ rkv_status compress_row_error(const rkv_ctx* c, const int32_t* src_rows, const i
   return fail(RKV_EINVAL, "invalid rows");
 }
 
-// Per-row plan entries of one tile's rows (retrieval slots q0 .. q0 + cnt - 1, taking the
-// pass's rows given by `rows`, or r_first .. r_first + cnt - 1 when `rows` is null) of
-// sequence s; returns the largest position among them (at least 1).
-int fill_tile_rows(int32_t* h, const rkv::PassPlan& p, const rkv::Dims& d, const int32_t* src_rows,
-                   const int32_t* pos, const int* rows, int r_first, int cnt, int q0, int s) {
+// Per-row plan entries of one tile's rows: retrieval slots q0 .. q0 + cnt - 1 take the
+// pass's rows given by `rows`, or r_first .. r_first + cnt - 1 when `rows` is null, of
+// sequence s.  The source rows (all the query gather needs) are filled first, so that
+// the gather can start while the rest of the plan is built.
+void fill_tile_src(int32_t* h, const rkv::PassPlan& p, const int32_t* src_rows, const int* rows,
+                   int r_first, int cnt, int q0) {
   int32_t* __restrict__ qsrc = h + p.off_q_src + q0;
-  int32_t* __restrict__ qpos = h + p.off_q_pos + q0;
-  int32_t* __restrict__ qdst = h + p.off_q_dst + q0;
-  const int64_t sT = (int64_t)s * d.T_cap;
-  int maxpos = 1;
   if (!rows) {
-    const int32_t* __restrict__ pp = pos + r_first;
-    for (int r = 0; r < cnt; ++r) {
-      const int pr = pp[r];
-      maxpos = pr > maxpos ? pr : maxpos;
-      qpos[r] = pr;
-      qdst[r] = (int32_t)(sT + pr);
-    }
     if (src_rows)
       std::memcpy(qsrc, src_rows + r_first, sizeof(int32_t) * cnt);
     else
       for (int r = 0; r < cnt; ++r) qsrc[r] = r_first + r;
   } else {
-    for (int r = 0; r < cnt; ++r) {
-      const int row = rows[r];
-      const int pr = pos[row];
-      maxpos = pr > maxpos ? pr : maxpos;
-      qsrc[r] = src_rows ? src_rows[row] : row;
-      qpos[r] = pr;
-      qdst[r] = (int32_t)(sT + pr);
-    }
+    for (int r = 0; r < cnt; ++r) qsrc[r] = src_rows ? src_rows[rows[r]] : rows[r];
+  }
+}
+
+// Positions and storage rows of the same tile rows; returns their largest position (at
+// least 1).
+int fill_tile_pos(int32_t* h, const rkv::PassPlan& p, const rkv::Dims& d, const int32_t* pos,
+                  const int* rows, int r_first, int cnt, int q0, int s) {
+  int32_t* __restrict__ qpos = h + p.off_q_pos + q0;
+  int32_t* __restrict__ qdst = h + p.off_q_dst + q0;
+  const int64_t sT = (int64_t)s * d.T_cap;
+  int maxpos = 1;
+  for (int r = 0; r < cnt; ++r) {
+    const int pr = rows ? pos[rows[r]] : pos[r_first + r];
+    maxpos = pr > maxpos ? pr : maxpos;
+    qpos[r] = pr;
+    qdst[r] = (int32_t)(sT + pr);
   }
   return maxpos;
 }
@@ -498,9 +522,12 @@ rkv_status rkv_pool_append(rkv_ctx* c, const void* kv, int64_t kv_row_stride,
   const Dims& d = c->d;
   if (kv_row_stride < d.dkv || kv_row_stride % 8 != 0)
     return fail(RKV_EINVAL, "kv_row_stride must be >= 2*d_k and a multiple of 8");
-  // validate everything before touching the host mirror
+  // validate everything before touching the host mirror: one branch-free pass for the
+  // usual call, the row-by-row pass (which names the first bad row) otherwise
   std::vector<int32_t> next(c->pool_count);
-  for (int i = 0; i < n; ++i) {
+  const bool fast = append_rows_ok_one_seq(c, src_rows, seq, pos, n);
+  if (fast) next[seq[0]] += n;
+  for (int i = 0; i < n && !fast; ++i) {
     const int s = seq[i], p = pos[i];
     const int src = src_rows ? src_rows[i] : i;
     if (s < 0 || s >= d.B) return fail(RKV_EINVAL, "row %d: seq %d out of range", i, s);
@@ -528,7 +555,7 @@ rkv_status rkv_pool_append(rkv_ctx* c, const void* kv, int64_t kv_row_stride,
       h[4 * i + 2] = p;
       h[4 * i + 3] = s * d.T_cap + p;
     }
-    CUDA_OK(staging_upload(c, b, 4 * m, st));
+    CUDA_OK(staging_upload(c, b, 0, 4 * m, st));
     CUDA_OK(launch_pool_append(c, kv, kv_row_stride, c->plan_dev[b], m, st));
   }
   c->pool_count = next;
@@ -614,6 +641,17 @@ rkv_status rkv_compress(rkv_ctx* c, const void* kv, int64_t kv_row_stride, const
       return fail(RKV_ECAPACITY, "compress pass exceeds the planned scratch");
     int b;
     int32_t* h = staging_acquire(c, &b);
+    // the query rows' sources first: upload them and start the query gather
+    for (size_t g = 0, q = 0; g + 1 < gbeg.size(); ++g) {
+      const int i = gbeg[g], j = gbeg[g + 1];
+      const int padded = (j - i + kTileM - 1) / kTileM * kTileM;
+      fill_tile_src(h, p, src_rows, ord ? ord + i : nullptr, r0 + i, j - i, (int)q);
+      for (int k = j - i; k < padded; ++k) h[p.off_q_src + q + k] = -1;
+      q += padded;
+    }
+    CUDA_OK(staging_upload(c, b, p.off_q_src, m_pad, st));
+    const int32_t* plan = c->plan_dev[b];
+    CUDA_OK(launch_prep_queries(c, kv, kv_row_stride, plan + p.off_q_src, p.m_pad, st));
     tseq.clear();
     trow0.clear();
     tnrt.clear();
@@ -623,8 +661,8 @@ rkv_status rkv_compress(rkv_ctx* c, const void* kv, int64_t kv_row_stride, const
       const int s = seq[ord ? ord[i] : r0 + i];
       for (int k = i; k < j; k += kTileM) {
         const int kend = std::min(j, k + kTileM);
-        const int maxpos = fill_tile_rows(h, p, d, src_rows, pos, ord ? ord + k : nullptr, r0 + k,
-                                          kend - k, q + (k - i), s);
+        const int maxpos = fill_tile_pos(h, p, d, pos, ord ? ord + k : nullptr, r0 + k, kend - k,
+                                         q + (k - i), s);
         const int nrt = (c->ref_before[maxpos] + kRefTile - 1) / kRefTile;
         tseq.push_back(s);
         trow0.push_back(q + (k - i));
@@ -633,7 +671,6 @@ rkv_status rkv_compress(rkv_ctx* c, const void* kv, int64_t kv_row_stride, const
       }
       const int padded = (j - i + kTileM - 1) / kTileM * kTileM;
       for (int k = j - i; k < padded; ++k) {
-        h[p.off_q_src + q + k] = -1;
         h[p.off_q_pos + q + k] = -1;
         h[p.off_q_dst + q + k] = -1;
       }
@@ -656,9 +693,7 @@ rkv_status rkv_compress(rkv_ctx* c, const void* kv, int64_t kv_row_stride, const
         h[p.off_u_rt + u] = rt;
       }
     }
-    CUDA_OK(staging_upload(c, b, p.total_ints, st));
-    const int32_t* plan = c->plan_dev[b];
-    CUDA_OK(launch_prep_queries(c, kv, kv_row_stride, plan + p.off_q_src, p.m_pad, st));
+    CUDA_OK(staging_upload(c, b, p.off_q_pos, p.total_ints - p.off_q_pos, st));
     CUDA_OK(launch_retrieve(c, p, plan, st));
     CUDA_OK(launch_retrieve_merge(c, p, plan, st));
     CUDA_OK(launch_mean_rows(c, p, plan, st));
