@@ -62,8 +62,10 @@ __global__ void repack_kernel(const __nv_bfloat16* __restrict__ a, const __nv_bf
 // One warp per reference row (plan row: {src row, pool row, pos, token row}).  Lane l
 // takes the 8-element pieces e = (32 u + l) * 8: all of its loads are issued before any
 // conversion, and the FP8 and bf16 stores of a warp cover whole contiguous segments.
-// The squared norm of the FP8 row is summed in float64, exact in any order (squares of
-// E4M3 values span 2^-18 .. 2^18, at most 2^12 of them per row), then rounded once.
+// The squared norm of the FP8 row is summed exactly in integers: every E4M3 value is
+// k * 2^-9 with |k| <= 448 * 2^9 < 2^18, so the row's sum of k^2 fits in int64 (2^36 per
+// square); it is rounded to fp32 once and scaled by 2^-18 (exact), the correctly
+// rounded squared norm.  (The float64 pipe would do the same, far more slowly.)
 template <bool F32>
 __global__ void __launch_bounds__(256)
     pool_append_kernel(const void* __restrict__ kv, int64_t stride,
@@ -83,7 +85,7 @@ __global__ void __launch_bounds__(256)
   const int64_t tok = plan[4 * r + 3];
   const uint4* in = reinterpret_cast<const uint4*>(
       static_cast<const uint8_t*>(kv) + src * stride * (F32 ? 4 : 2));
-  double acc = 0.0;
+  long long acc = 0;
   for (int u0 = 0; u0 * 256 < dkv; u0 += kPieces) {
     uint4 raw[kPieces][kWords];
 #pragma unroll
@@ -120,7 +122,8 @@ __global__ void __launch_bounds__(256)
         const __nv_fp8_storage_t q = __nv_cvt_float_to_fp8(v[i], __NV_SATFINITE, __NV_E4M3);
         packed[i >> 2] |= static_cast<uint32_t>(q) << (8 * (i & 3));
         d[i] = fp8_to_float(q);
-        acc += (double)d[i] * (double)d[i];   // exact: squares of E4M3 values
+        const int k = __float2int_rz(d[i] * 512.0f);   // exact: d = k * 2^-9
+        acc += (long long)k * k;
       }
       *reinterpret_cast<uint2*>(pool8 + prow * dkv + e) = make_uint2(packed[0], packed[1]);
       *reinterpret_cast<uint4*>(poolb + prow * dkv + e) =
@@ -131,7 +134,7 @@ __global__ void __launch_bounds__(256)
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
   if (lane == 0) {
-    norm2[prow] = (float)acc;
+    norm2[prow] = __ll2float_rn(acc) * 0x1p-18f;
     pool_pos[prow] = pos;
   }
   // the reference token's own entry: itself as the first reference, no code
