@@ -6,7 +6,11 @@
 // accumulation in TMEM).  The epilogue thread that owns query row i (one TMEM lane)
 // turns each into the ranking score ||r_j||^2 - 2 a_i . r_j (= ||a_i - r_j||^2 minus a
 // per-row constant), masks slots whose reference is not strictly before the token,
-// and keeps a sorted running top-4 in registers across the pool tiles; equal scores
+// and keeps a sorted running top-4 in registers across the pool tiles.  A sequence's
+// pool slots hold its reference positions in increasing order, so the references
+// before position p are exactly slots 0 .. ref_before[p] - 1: the mask is one compare
+// with a per-row bound.  The unit's 256 squared norms are staged once in shared memory
+// and read four at a time by broadcast loads.  Equal scores
 // keep the smaller slot because slots are visited in increasing order with a strict
 // comparison.  fp32 queries are split into three bf16 pieces (hi + mid + lo == x), so
 // the products stay exact and the three partial dots accumulate into one fp32 sum.
@@ -17,7 +21,6 @@
 // strict comparison, which yields exactly the 4 smallest (distance, slot) pairs.
 #include <cuda_bf16.h>
 #include <float.h>
-#include <climits>
 
 #include "tc_common.cuh"
 
@@ -39,7 +42,7 @@ struct RetrieveArgs {
   int parts;    // 1 or 3
   int R_cap, topk;
   const float* norm2;
-  const int32_t* pool_pos;
+  const int32_t* ref_before;   // [T_cap + 1] references below each position
   int32_t* ref_idx;
   int* status;
 };
@@ -82,7 +85,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kTileABytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + kStages * kBBytes);
+  float* sN = reinterpret_cast<float*>(sB + kStages * kBBytes);   // [2][kRefTile] norms
+  uint64_t* full = reinterpret_cast<uint64_t*>(sN + 2 * kRefTile);
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;
   uint64_t* tempty = tfull + 2;
@@ -194,42 +198,46 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row_in_tile = ew * 32 + (int)lane_id();
     int acc = 0;
     uint32_t acc_phase = 0;
-    bool ok = true;
-    for (int u = blockIdx.x; u < a.n_units && ok; u += gridDim.x) {
+    int k = 0;                                         // this CTA's unit count
+    for (int u = blockIdx.x; u < a.n_units; u += gridDim.x, ++k) {
       const int t = a.u_tile[u], rt = a.u_rt[u];
       const int seq = a.t_seq[t], row0 = a.t_row0[t];
       const int qrow = row0 + row_in_tile;
       const int pos = a.q_pos[qrow];
       const int64_t pbase = (int64_t)seq * a.R_cap;
+      // references strictly before the token: the first ref_before[pos] slots (none for
+      // a padding row, pos = -1)
+      const int nref = pos >= 0 ? __ldg(a.ref_before + pos) : 0;
+      // the unit's squared norms into buffer k & 1; the same 128-thread barrier, whose
+      // vote also makes every exit uniform, orders these writes before the reads and the
+      // reads of unit k - 1 (other buffer) before the writes of unit k + 1
+      float* nb = sN + (k & 1) * kRefTile;
+      for (int i = row_in_tile; i < kRefTile; i += 128) {
+        const int j = rt * kRefTile + i;
+        nb[i] = j < a.R_cap ? __ldg(a.norm2 + pbase + j) : 0.f;
+      }
       float bd[4] = {FLT_MAX, FLT_MAX, FLT_MAX, FLT_MAX};
       int bj[4] = {-1, -1, -1, -1};
-      if (!warp_wait(&tfull[acc], acc_phase, abort_flag, a.status)) {
-        ok = false;
-        break;
-      }
+      if (!bar_red_and(1, 128, warp_wait(&tfull[acc], acc_phase, abort_flag, a.status))) break;
       tc_fence_after();
       const uint32_t tacc = tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)(acc * kRefTile);
 #pragma unroll 1
       for (int c = 0; c < kRefTile / 32; ++c) {
-        // lane i fetches column j0+i's position and squared norm once; the warp then
-        // broadcasts them with shuffles, so the drain below has no memory latency.
         const int j0 = rt * kRefTile + c * 32;
-        const int jl = j0 + (int)lane_id();
-        int32_t pl = INT_MAX;
-        float nl = 0.f;
-        if (jl < a.R_cap) {
-          pl = __ldg(a.pool_pos + pbase + jl);
-          nl = __ldg(a.norm2 + pbase + jl);
-        }
         uint32_t r[32];
         tmem_ld32(tacc + c * 32, r);
         tmem_ld_wait();
+        const float4* n4 = reinterpret_cast<const float4*>(nb + c * 32);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const int32_t pj = __shfl_sync(0xffffffffu, pl, i);
-          const float nj = __shfl_sync(0xffffffffu, nl, i);
-          const float dist = fmaf(-2.0f, __uint_as_float(r[i]), nj);
-          if (pj < pos) topk_insert(dist, j0 + i, bd, bj);
+        for (int q = 0; q < 8; ++q) {
+          const float4 nv = n4[q];
+          const float nn[4] = {nv.x, nv.y, nv.z, nv.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int i = 4 * q + e;
+            const float dist = fmaf(-2.0f, __uint_as_float(r[i]), nn[e]);
+            if (j0 + i < nref) topk_insert(dist, j0 + i, bd, bj);
+          }
         }
       }
       tc_fence_before();
@@ -296,7 +304,8 @@ cudaError_t launch_retrieve_merge(rkv_ctx* c, const PassPlan& p, const int32_t* 
 
 cudaError_t launch_retrieve(rkv_ctx* c, const PassPlan& p, const int32_t* plan, cudaStream_t s) {
   if (p.n_units == 0) return cudaSuccess;
-  const size_t smem = 1024 + (size_t)kStages * (kTileABytes + kBBytes) + 8 * (2 * kStages + 4) + 16;
+  const size_t smem = 1024 + (size_t)kStages * (kTileABytes + kBBytes) + 2 * kRefTile * sizeof(float) +
+                      8 * (2 * kStages + 4) + 16;
   cudaError_t e =
       cudaFuncSetAttribute(retrieve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -316,7 +325,7 @@ cudaError_t launch_retrieve(rkv_ctx* c, const PassPlan& p, const int32_t* plan, 
   a.R_cap = c->d.R_cap;
   a.topk = c->d.topk;
   a.norm2 = c->st.pool_norm2;
-  a.pool_pos = c->st.pool_pos;
+  a.ref_before = c->ref_before_dev;
   a.ref_idx = c->st.ref_idx;
   a.status = c->status;
   const int grid = p.n_units < c->num_sms ? p.n_units : c->num_sms;

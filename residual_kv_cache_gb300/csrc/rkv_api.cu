@@ -425,6 +425,7 @@ rkv_status rkv_create(const rkv_config* cfg, const void* Wc1, const void* Wc2, c
   ALLOC(c->wd, (size_t)d.dkv * d.dc * 2);
   ALLOC(c->rope_lo, (size_t)kRopeLo * (d.D / 2) * sizeof(float2));
   ALLOC(c->rope_hi, (size_t)d.n_hi * (d.D / 2) * sizeof(float2));
+  ALLOC(c->ref_before_dev, ((size_t)d.T_cap + 1) * sizeof(int32_t));
   ALLOC(c->Q, (size_t)c->m_cap * d.parts * d.dkv * 2);
   ALLOC(c->M, (size_t)c->m_cap * d.dkv * 2);
   ALLOC(c->H, (size_t)2 * c->m_cap * d.dff * 2);
@@ -465,9 +466,11 @@ rkv_status rkv_create(const rkv_config* cfg, const void* Wc1, const void* Wc2, c
       }
     }
     if (cudaMemcpy(c->rope_lo, lo.data(), lo.size() * sizeof(float2), cudaMemcpyHostToDevice) != cudaSuccess ||
-        cudaMemcpy(c->rope_hi, hi.data(), hi.size() * sizeof(float2), cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaMemcpy(c->rope_hi, hi.data(), hi.size() * sizeof(float2), cudaMemcpyHostToDevice) != cudaSuccess ||
+        cudaMemcpy(c->ref_before_dev, c->ref_before.data(), c->ref_before.size() * sizeof(int32_t),
+                   cudaMemcpyHostToDevice) != cudaSuccess) {
       rkv_free(c);
-      return fail(RKV_ECUDA, "RoPE table upload failed");
+      return fail(RKV_ECUDA, "RoPE or schedule table upload failed");
     }
   }
 
@@ -768,6 +771,7 @@ void rkv_free(rkv_ctx* c) {
   cudaFree(c->wd);
   cudaFree(c->rope_lo);
   cudaFree(c->rope_hi);
+  cudaFree(c->ref_before_dev);
   cudaFree(c->Q);
   cudaFree(c->M);
   cudaFree(c->H);

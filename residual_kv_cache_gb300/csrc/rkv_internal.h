@@ -72,6 +72,7 @@ struct rkv_ctx {
   __nv_bfloat16* wd = nullptr;    // [2d_k, d_c] = W_d^T
   float2* rope_lo = nullptr;      // [512][D/2] (cos, sin)(l * theta_j)
   float2* rope_hi = nullptr;      // [n_hi][D/2] (cos, sin)(h * 512 * theta_j)
+  int32_t* ref_before_dev = nullptr;   // [T_cap + 1] device copy of ref_before
   __nv_bfloat16* Q = nullptr;     // [m_cap, parts * 2d_k] retrieval-order queries
   __nv_bfloat16* M = nullptr;     // [m_cap, 2d_k] bf16 reference means, retrieval order
   __nv_bfloat16* H = nullptr;     // [2 m_cap, d_ff] SwiGLU rows: 2q from kv, 2q + 1 from the
