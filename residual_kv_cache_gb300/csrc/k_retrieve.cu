@@ -48,6 +48,10 @@ struct RetrieveArgs {
 };
 
 constexpr int kStages = 4;
+// 12 warps: 0 TMA producer, 1 MMA issuer, 2 TMEM allocator, 3 idle, 4..11 epilogue in two
+// groups of four; group g scans columns [128 g, 128 g + 128) of each unit's 256 slots.
+constexpr int kRetrThreads = 384;
+constexpr int kEpiThreads = 256;
 constexpr uint32_t kBBytes = kRefTile * 128;
 constexpr uint32_t kTmemCols = 2 * kRefTile;
 
@@ -78,7 +82,7 @@ __device__ __forceinline__ void topk_insert(float d, int j, float* bd, int* bj) 
   }
 }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kRetrThreads, 1)
     retrieve_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmP,
                     RetrieveArgs a) {
   extern __shared__ uint8_t smem_raw[];
@@ -86,7 +90,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sA = smem;
   uint8_t* sB = smem + kStages * kTileABytes;
   float* sN = reinterpret_cast<float*>(sB + kStages * kBBytes);   // [2][kRefTile] norms
-  uint64_t* full = reinterpret_cast<uint64_t*>(sN + 2 * kRefTile);
+  int4* sM = reinterpret_cast<int4*>(sN + 2 * kRefTile);          // [kTileM][2] group 1's top-4
+  uint64_t* full = reinterpret_cast<uint64_t*>(sM + 2 * kTileM);
   uint64_t* empty = full + kStages;
   uint64_t* tfull = empty + kStages;
   uint64_t* tempty = tfull + 2;
@@ -101,7 +106,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
-      mbar_init(&tempty[b], 4);                        // one arrival per epilogue warp
+      mbar_init(&tempty[b], kEpiThreads / 32);         // one arrival per epilogue warp
     }
     *abort_flag = 0;
     fence_barrier_init();
@@ -194,8 +199,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok && any) drain_wait(&empty[last_stage], last_phase);
     }
   } else if (warp >= kEpiWarp0) {
-    const int ew = warp - kEpiWarp0;
-    const int row_in_tile = ew * 32 + (int)lane_id();
+    const int et = (int)threadIdx.x - kEpiWarp0 * 32;  // 0 .. kEpiThreads - 1
+    const int eg = et >> 7;                            // column group
+    const int row_in_tile = et & (kTileM - 1);         // TMEM lane = query row
+    const uint32_t lane_base = (uint32_t)(row_in_tile & ~31) << 16;
     int acc = 0;
     uint32_t acc_phase = 0;
     int k = 0;                                         // this CTA's unit count
@@ -208,21 +215,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       // references strictly before the token: the first ref_before[pos] slots (none for
       // a padding row, pos = -1)
       const int nref = pos >= 0 ? __ldg(a.ref_before + pos) : 0;
-      // the unit's squared norms into buffer k & 1; the same 128-thread barrier, whose
-      // vote also makes every exit uniform, orders these writes before the reads and the
-      // reads of unit k - 1 (other buffer) before the writes of unit k + 1
+      // the unit's squared norms into buffer k & 1; the same barrier, whose vote also
+      // makes every exit uniform, orders these writes before the reads and the reads of
+      // unit k - 1 (other buffer, and group 1's list) before the writes of unit k + 1
       float* nb = sN + (k & 1) * kRefTile;
-      for (int i = row_in_tile; i < kRefTile; i += 128) {
-        const int j = rt * kRefTile + i;
-        nb[i] = j < a.R_cap ? __ldg(a.norm2 + pbase + j) : 0.f;
+      {
+        const int j = rt * kRefTile + et;
+        nb[et] = j < a.R_cap ? __ldg(a.norm2 + pbase + j) : 0.f;
       }
       float bd[4] = {FLT_MAX, FLT_MAX, FLT_MAX, FLT_MAX};
       int bj[4] = {-1, -1, -1, -1};
-      if (!bar_red_and(1, 128, warp_wait(&tfull[acc], acc_phase, abort_flag, a.status))) break;
+      if (!bar_red_and(1, kEpiThreads, warp_wait(&tfull[acc], acc_phase, abort_flag, a.status)))
+        break;
       tc_fence_after();
-      const uint32_t tacc = tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)(acc * kRefTile);
+      const uint32_t tacc = tmem + lane_base + (uint32_t)(acc * kRefTile);
 #pragma unroll 1
-      for (int c = 0; c < kRefTile / 32; ++c) {
+      for (int c = 4 * eg; c < 4 * eg + 4; ++c) {
         const int j0 = rt * kRefTile + c * 32;
         uint32_t r[32];
         tmem_ld32(tacc + c * 32, r);
@@ -246,6 +254,24 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
+      }
+      // group 1 (the larger slots) hands its list to group 0, which inserts it in order
+      // with the same strict comparison, so equal scores still keep the smaller slot
+      if (eg == 1) {
+        sM[2 * row_in_tile] = make_int4(__float_as_int(bd[0]), bj[0], __float_as_int(bd[1]), bj[1]);
+        sM[2 * row_in_tile + 1] = make_int4(__float_as_int(bd[2]), bj[2], __float_as_int(bd[3]), bj[3]);
+        bar_arrive(2, kEpiThreads);
+        continue;
+      }
+      bar_sync(2, kEpiThreads);
+      {
+        const int4 e0 = sM[2 * row_in_tile], e1 = sM[2 * row_in_tile + 1];
+        const float od[4] = {__int_as_float(e0.x), __int_as_float(e0.z), __int_as_float(e1.x),
+                             __int_as_float(e1.z)};
+        const int oj[4] = {e0.y, e0.w, e1.y, e1.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          if (oj[i] >= 0) topk_insert(od[i], oj[i], bd, bj);
       }
       int4* dp = reinterpret_cast<int4*>(a.part + ((int64_t)u * kTileM + row_in_tile) * 4);
       dp[0] = make_int4(__float_as_int(bd[0]), bj[0], __float_as_int(bd[1]), bj[1]);
@@ -305,7 +331,7 @@ cudaError_t launch_retrieve_merge(rkv_ctx* c, const PassPlan& p, const int32_t* 
 cudaError_t launch_retrieve(rkv_ctx* c, const PassPlan& p, const int32_t* plan, cudaStream_t s) {
   if (p.n_units == 0) return cudaSuccess;
   const size_t smem = 1024 + (size_t)kStages * (kTileABytes + kBBytes) + 2 * kRefTile * sizeof(float) +
-                      8 * (2 * kStages + 4) + 16;
+                      2 * kTileM * sizeof(int4) + 8 * (2 * kStages + 4) + 16;
   cudaError_t e =
       cudaFuncSetAttribute(retrieve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -331,7 +357,7 @@ cudaError_t launch_retrieve(rkv_ctx* c, const PassPlan& p, const int32_t* plan, 
   const int grid = p.n_units < c->num_sms ? p.n_units : c->num_sms;
   cudaEvent_t ev;
   timing_begin(c, "rkv_retrieve_kernel", s, &ev);
-  retrieve_kernel<<<grid, kThreads, smem, s>>>(c->tm_q, c->tm_pool, a);
+  retrieve_kernel<<<grid, kRetrThreads, smem, s>>>(c->tm_q, c->tm_pool, a);
   e = cudaGetLastError();
   timing_end(c, "rkv_retrieve_kernel", s, ev);
   return e;

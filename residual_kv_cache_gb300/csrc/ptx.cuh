@@ -158,6 +158,11 @@ __device__ __forceinline__ void bar_sync(int id, int count) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(count) : "memory");
 }
 
+// Arrive at named barrier `id` without waiting (the producer side of bar_sync).
+__device__ __forceinline__ void bar_arrive(int id, int count) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(count) : "memory");
+}
+
 // bar_sync that also returns whether `pred` holds in every participating thread.
 __device__ __forceinline__ bool bar_red_and(int id, int count, bool pred) {
   int r;
