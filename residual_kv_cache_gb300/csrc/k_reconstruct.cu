@@ -435,7 +435,7 @@ __global__ void __launch_bounds__(kReconThreads, 1)
 
     // z~ of tile m into TMEM (the caller has made sure the tensor core is done with the
     // previous tile), then one arrival per warp on afull.
-    int gr[4];                                        // pool rows of the next copies
+    int cp0[4], cp1[4];                               // pool rows this lane copies (per tile)
     int nx_s = -1, nx_p = -1;                         // the row of the next tile
     auto setup_a = [&](int m) -> RowState {
       const TileRow tr = tile_setup(a, m, row, wg, g0, g_per, zaddr, nx_s, nx_p,
@@ -446,7 +446,10 @@ __global__ void __launch_bounds__(kReconThreads, 1)
       __syncwarp();
       if (lane_id() == 0) mbar_arrive(afull);
 #pragma unroll
-      for (int t = 0; t < 4; ++t) gr[t] = tr.r[t];
+      for (int t = 0; t < 4; ++t) {
+        cp0[t] = __shfl_sync(0xffffffffu, tr.r[t], cl >> 1);
+        cp1[t] = __shfl_sync(0xffffffffu, tr.r[t], (cl >> 1) + 16);
+      }
       return tr.st;
     };
 
@@ -472,8 +475,7 @@ __global__ void __launch_bounds__(kReconThreads, 1)
     // that exactly three are always younger than the one waited for.
     auto issue_ref = [&](int n_next, bool active, int t) {
       if (active) {
-        const int p0 = __shfl_sync(0xffffffffu, gr[t], cl >> 1);
-        const int p1 = __shfl_sync(0xffffffffu, gr[t], (cl >> 1) + 16);
+        const int p0 = cp0[t], p1 = cp1[t];
         uint8_t* dst = cp_dst0 + (uint32_t)(t * 2) * kPlaneBytes;
         const uint8_t* src = cp_src0 + n_next * kNT;
         if (p0 >= 0) cp_async16(dst, src + (int64_t)p0 * a.dkv);
@@ -537,15 +539,16 @@ __global__ void __launch_bounds__(kReconThreads, 1)
         else
           cp_async_commit();
       }
-      if (cur.valid()) {
-        if (cur.kcnt() == 3) {
+      // mean = sum / k_i.  For k_i = 1, 2, 4 the scaling is exact, so it folds into the
+      // accumulator add below: one fma, RN(acc + sum / k_i), the same value as rounding
+      // the exact mean's sum with acc.  For k_i = 3 the sum is divided here (correctly
+      // rounded) and added with scale 1.  Rows without references keep zeros.
+      float kinv = 1.0f;
+      if (cur.kcnt() == 3) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) mx[i] = div3_rn(mx[i]), my[i] = div3_rn(my[i]);
-        } else {
-          const float kinv = 1.0f / (float)cur.kcnt();   // exact for k_i = 1, 2, 4
-#pragma unroll
-          for (int i = 0; i < 16; ++i) mx[i] = __fmul_rn(mx[i], kinv), my[i] = __fmul_rn(my[i], kinv);
-        }
+        for (int i = 0; i < 16; ++i) mx[i] = div3_rn(mx[i]), my[i] = div3_rn(my[i]);
+      } else {
+        kinv = cur.kcnt() == 2 ? 0.5f : (cur.kcnt() == 4 ? 0.25f : 1.0f);
       }
       // ---- accumulator row; the pair's vote also tells that both warps have read
       // reference 3, whose plane then takes the next unit's copy
@@ -560,8 +563,8 @@ __global__ void __launch_bounds__(kReconThreads, 1)
         tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
-          mx[i] = __fadd_rn(__uint_as_float(xr[i]), mx[i]);
-          my[i] = __fadd_rn(__uint_as_float(yr[i]), my[i]);
+          mx[i] = __fmaf_rn(mx[i], kinv, __uint_as_float(xr[i]));
+          my[i] = __fmaf_rn(my[i], kinv, __uint_as_float(yr[i]));
         }
       }
       // the accumulator is free as soon as it has been read
