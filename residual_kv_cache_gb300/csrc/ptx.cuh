@@ -111,14 +111,6 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, u
       : "memory");
 }
 
-// L2 prefetch of the box at (x, y) of a tensor map (no shared memory, no completion).
-__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t x, int32_t y) {
-  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                   reinterpret_cast<uint64_t>(map)),
-               "r"(x), "r"(y)
-               : "memory");
-}
-
 // 2-D tiled store of a box from shared memory (bulk-group completion).  The box's
 // shared-memory contents must have been made visible to the async proxy first
 // (fence_proxy_async_smem by every writer, then a barrier).
