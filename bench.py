@@ -138,8 +138,8 @@ def algorithmic_work(w, n_comp: int, n_sel: int, ref_pos) -> dict:
 # only while the kernel's source file is unchanged since the capture (sha1 below).
 MEASURED_TRAFFIC = {
     "rkv_reconstruct_kernel": {"file": "k_reconstruct.cu",
-                               "sha1": "ae46d9c4ea6d7cd3341a8a1eaa75f53dc8d1f513",
-                               "bytes": 10437888 + 144128},
+                               "sha1": "f3519d7eec49f3d081cf5333710497f95a7bece2",
+                               "bytes": 10746880 + 238592},
     "rkv_retrieve_kernel": {"file": "k_retrieve.cu",
                             "sha1": "5af5f39bd571fc93b322c34dc26ffb40142a4a2d",
                             "bytes": 134437888 + 4264960},
@@ -164,22 +164,31 @@ def measured_traffic(kernel: str):
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples every 50 ms, started early (its start-up takes a while); only
+    the samples whose timestamps fall inside [mark_begin, mark_end] are reported."""
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int):
         self.proc = None
         self.gpu = gpu_index
+        self.t0 = self.t1 = None
 
     def start(self):
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (OSError, FileNotFoundError):
             self.proc = None
+
+    def mark_begin(self):
+        self.t0 = time.time()
+
+    def mark_end(self):
+        self.t1 = time.time()
 
     def stop(self) -> dict:
         if self.proc is None:
@@ -190,18 +199,22 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
             out, _ = self.proc.communicate()
+        import datetime
         sm, smax, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in out.strip().splitlines():
             f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
+            if len(f) < 10:
                 continue
             try:
-                sm.append(float(f[1]))
-                smax.append(float(f[2]))
+                ts = datetime.datetime.strptime(f[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                if self.t0 is not None and not (self.t0 <= ts <= (self.t1 or ts)):
+                    continue
+                sm.append(float(f[2]))
+                smax.append(float(f[3]))
             except ValueError:
                 continue
-            for n, v in zip(names, f[5:9]):
+            for n, v in zip(names, f[6:10]):
                 if v.lower() == "active":
                     reasons.add(n)
         return {"sm_mhz": statistics.median(sm) if sm else None,
@@ -254,6 +267,8 @@ def run_cuda(args):
             dist.barrier()
         torch.cuda.synchronize(dev)
 
+    clocks = ClockSampler(local)           # started now: nvidia-smi takes a while to start
+    clocks.start()
     for _ in range(args.warmup):
         step()
     barrier()
@@ -263,8 +278,7 @@ def run_cuda(args):
     # ---- timed region (device time, CUDA events on the launching stream only at the
     # step boundaries, so consecutive launches are free to overlap)
     launches0 = codec.launch_count()
-    clocks = ClockSampler(local)
-    clocks.start()
+    clocks.mark_begin()
     times = []
     for _ in range(args.steps):
         flush.fill_(1.0)                       # L2 flush, outside the timed interval
@@ -276,6 +290,7 @@ def run_cuda(args):
         e1.record(stream)
         barrier()
         times.append(e0.elapsed_time(e1))
+    clocks.mark_end()
     clk = clocks.stop()
     launches = codec.launch_count() - launches0
     status = codec.get_status()
@@ -599,7 +614,7 @@ def run_kernel_case(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
     ap.add_argument("--alpha", type=float, default=0.0,
