@@ -260,6 +260,49 @@ def test_reconstruct_from_oracle_codes_fp32():
     assert rel_fro(np64(V), Vo) <= 1e-5
 
 
+@pytest.fixture(scope="module")
+def oracle_store_2k():
+    """Oracle-written storage of a 2048-token llama8b-shaped sequence (the read path's
+    inputs exactly as the pages define them)."""
+    w = synth.workload("llama8b")
+    T = 2048
+    kv64 = np64(synth.gen_kv(w, 131, T=T))
+    W = synth.gen_weights(w, 132)
+    W64 = _weights64(W)
+    st = C.compress_sequence(kv64, W64, oracle_shape(w), "operand")
+    return dict(w=w, T=T, W=W, W64=W64, st=st)
+
+
+@cuda
+@pytest.mark.parametrize("out_dtype", ["bf16", "fp32"])
+def test_reconstruct_ragged_selection_sizes(oracle_store_2k, out_dtype):
+    """Selections that end inside a 32-row warp box or a 128-row tile, or fill a single
+    row: parity with the oracle, and no row past n_sel is written (the output tensor map
+    clips them)."""
+    r = oracle_store_2k
+    w, T, st = r["w"], r["T"], r["st"]
+    c = make_codec(w, r["W"], T=T, out_dtype=out_dtype)
+    R = len(st.pool.pos)
+    c.pool_fp8[0, :R] = torch.from_numpy(st.pool.codes).cuda()
+    c.ref_idx[0] = torch.from_numpy(st.idx.astype(np.int32)).cuda()
+    c.codes[0] = torch.from_numpy(st.packed).cuda()
+    c.meta[0] = torch.from_numpy(st.meta.astype(np.float16)).cuda()
+    odt = torch.float32 if out_dtype == "fp32" else torch.bfloat16
+    tol = 1e-5 if out_dtype == "fp32" else 5e-3     # bf16: one final rounding, <= 2^-9
+    for n in (1, 31, 33, 97, 129, 250):
+        sel = synth.gen_selection(T, n, 140 + n)
+        pad = 40
+        kb = torch.full((n + pad, w.n_kv_heads, w.head_dim), float("nan"), dtype=odt, device="cuda")
+        vb = torch.full_like(kb, float("nan"))
+        K, V = c.reconstruct(torch.zeros_like(sel).cuda(), sel.cuda(), kb[:n], vb[:n])
+        torch.cuda.synchronize()
+        assert c.get_status() == 0
+        Ko, Vo, _ = C.reconstruct(st, sel.numpy().astype(np.int64), r["W64"], "operand")
+        assert rel_fro(np64(kb[:n]), Ko) <= tol, n
+        assert rel_fro(np64(vb[:n]), Vo) <= tol, n
+        assert torch.isnan(kb[n:]).all() and torch.isnan(vb[n:]).all(), n
+
+
 @cuda
 def test_zero_decoder_returns_mean_and_refs_exact():
     w = synth.workload("tiny")
