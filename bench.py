@@ -361,11 +361,7 @@ def run_cuda(args):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_step_ms, 4),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic",
-        "config": {"workload": f"{WORKLOAD}: Llama-3.1-8B-shaped layer, T={T}, 2d_k={w.d_kv}, "
-                               f"d_c={w.d_c}, d_ff={w.d_ff}, {schedule_note(w)}, INT{w.bits}, "
-                               f"prefill write + {steps_dec} decode steps x {n_sel} restored",
-                   "tokens_per_step": tokens_step, "l2": "flushed before every timed step",
-                   "parallelism": f"replicas x{world} (independent sequences)"},
+        "config": step_config(w, world),
         "compress_tok_s": round(T / (write_ms / 1e3), 1) if write_ms else None,
         "reconstruct_tok_s": round(steps_dec * n_sel / (read_ms / 1e3), 1) if read_ms else None,
         "roofline": roofline,
@@ -550,6 +546,15 @@ def _workload():
     return synth.workload(WORKLOAD)
 
 
+def step_config(w, world: int) -> dict:
+    """The workload of one step, the same on both arms of the comparison."""
+    return {"workload": f"{WORKLOAD}: Llama-3.1-8B-shaped layer, T={w.T}, 2d_k={w.d_kv}, "
+                        f"d_c={w.d_c}, d_ff={w.d_ff}, {schedule_note(w)}, INT{w.bits}, "
+                        f"prefill write + {w.steps} decode steps x {w.n_sel} restored",
+            "tokens_per_step": w.T + w.steps * w.n_sel, "l2": "flushed before every timed step",
+            "parallelism": f"replicas x{world} (independent sequences)"}
+
+
 def run_reference(args):
     rank, world, local = dist_env()
     if rank != 0:
@@ -561,14 +566,13 @@ def run_reference(args):
         last = cpu_baseline(args.cpu_seconds)
         vals.append(last["value"])
     v = statistics.mean(vals)
-    tokens = 32768 + 64 * 9830
+    w = _workload()
+    tokens = w.T + w.steps * w.n_sel
     out = {"metric": METRIC, "value": round(v, 2), "unit": UNIT, "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tokens / v * 1e3, 1),
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic", "impl": "reference",
-           "config": {"workload": f"{WORKLOAD} (oracle on bounded samples)"
-                                  + ("" if SCHEDULE == {"alpha": 0.0, "sink": 0}
-                                     else f", {schedule_note(_workload())}")},
+           "config": step_config(w, 1),
            "cpu_baseline": {"value": round(v, 2), "unit": UNIT, "cores": last["cores"],
                             "kind": "oracle", "sample": last["sample"]},
            "e2e": {"value": round(v, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
