@@ -48,7 +48,8 @@ def _stamp() -> str:
     """Machine + hash of every source and of this script: a library built on another
     architecture or from other sources is rebuilt."""
     h = hashlib.sha1(platform.machine().encode())
-    paths = sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC))
+    paths = sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC)
+                   if f.endswith((".cu", ".cuh", ".h")))
     paths += [os.path.join(HERE, "..", "include", "rkv.h"), os.path.abspath(__file__)]
     for p in paths:
         with open(p, "rb") as f:
