@@ -141,8 +141,8 @@ MEASURED_TRAFFIC = {
                                "sha1": "f3519d7eec49f3d081cf5333710497f95a7bece2",
                                "bytes": 10746880 + 238592},
     "rkv_retrieve_kernel": {"file": "k_retrieve.cu",
-                            "sha1": "5af5f39bd571fc93b322c34dc26ffb40142a4a2d",
-                            "bytes": 134437888 + 4264960},
+                            "sha1": "4cb997c96225542b611a891b8a622e58c14b237b",
+                            "bytes": 134557184 + 3536128},
 }
 
 
