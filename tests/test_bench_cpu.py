@@ -1,0 +1,71 @@
+"""Host-side pieces of bench.py: the algorithmic work behind the roofline figures, and
+the clock record kept to the timed window.  No GPU."""
+import datetime
+import os
+import sys
+
+import numpy as np
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+import bench  # noqa: E402
+import synth  # noqa: E402
+
+
+def test_algorithmic_work_closed_forms():
+    """The llama8b step: fixed stride 16, 2048 references, 30720 compressed tokens."""
+    w = synth.workload("llama8b")
+    ref = np.arange(0, w.T, 16)
+    work = bench.algorithmic_work(w, w.T, w.n_sel, ref)
+    n_non = w.T - len(ref)
+    # a restore: one (d_c x 2d_k) product per selected token
+    assert work["rkv_reconstruct_kernel"]["flops"] == 2.0 * w.n_sel * w.d_c * w.d_kv
+    # GEMM-1/2 over kv and mean rows, gate and value columns
+    assert work["rkv_gemm12_swiglu_kernel"]["flops"] == 2.0 * (2 * n_non) * (2 * w.d_ff) * w.d_kv
+    # retrieval: token 16k + j (j = 1..15) sees the k + 1 references at 0, 16, ..., 16k,
+    # so the average pool is 15 * sum_{k<2048} (k + 1) / 30720 = 2049 / 2
+    assert work["rkv_retrieve_kernel"]["flops"] == 2.0 * n_non * (2049 / 2) * w.d_kv
+    # bytes of a restore: code, extremes and slots in, K and V out, W_d and the pool once
+    per_tok = w.d_c * w.bits // 8 + 4 * (w.d_c // 32) + 4 * w.topk + w.d_kv * 2
+    assert work["rkv_reconstruct_kernel"]["bytes"] == (
+        w.n_sel * per_tok + w.d_kv * w.d_c * 2 + len(ref) * w.d_kv)
+
+
+class _FakeSmi:
+    def __init__(self, text):
+        self.text = text
+
+    def terminate(self):
+        pass
+
+    def communicate(self, timeout=None):
+        return self.text, ""
+
+
+def _line(t, sm, reasons=("Not Active",) * 4):
+    ts = datetime.datetime.fromtimestamp(t).strftime("%Y/%m/%d %H:%M:%S.%f")[:-3]
+    return ", ".join([ts, "0", str(sm), "2070", "900.00", "0x0"] + list(reasons))
+
+
+def test_clock_record_keeps_only_the_timed_window():
+    t0 = 1_800_000_000.0
+    lines = [
+        _line(t0 - 0.5, 900, ("Not Active", "Not Active", "Not Active", "Active")),  # before
+        _line(t0 + 0.05, 2070),
+        _line(t0 + 0.10, 2055, ("Not Active", "Not Active", "Not Active", "Active")),
+        _line(t0 + 0.15, 2070),
+        _line(t0 + 0.9, 1200, ("Active", "Not Active", "Not Active", "Not Active")),  # after
+    ]
+    c = bench.ClockSampler(0)
+    c.proc = _FakeSmi("\n".join(lines) + "\n")
+    c.t0, c.t1 = t0, t0 + 0.2
+    rec = c.stop()
+    assert rec["samples"] == 3
+    assert rec["sm_mhz"] == 2070.0 and rec["sm_max_mhz"] == 2070.0
+    assert rec["reasons"] == ["sw_power_cap"]          # the hw_slowdown sample lies outside
+
+
+def test_step_config_names_the_bench_workload():
+    w = synth.workload("llama8b")
+    cfg = bench.step_config(w, 1)
+    assert cfg["tokens_per_step"] == w.T + w.steps * w.n_sel == 32768 + 64 * 9830
+    assert cfg["workload"].startswith("llama8b: ")
