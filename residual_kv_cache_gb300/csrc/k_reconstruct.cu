@@ -13,14 +13,17 @@
 //   2. build the row's RoPE cos/sin for its 16 column pairs (float64-built two-level
 //      tables, angle addition in fp32) into shared memory.
 // Per unit, a TMA ring streams W_d^T tiles (the B operand) and one thread issues
-// tcgen05.mma into one of two TMEM accumulators.  Each epilogue warp prefetches, one
-// unit ahead, exactly the reference bytes it will read (its 32 rows x its 16 column
-// pairs x <= 4 references, 16-byte cp.async copies into a private shared-memory slot
-// per reference), so the reference gathers need no cross-warp synchronisation.  Each
-// epilogue thread then sums its row's references (exact in fp32), divides by k_i, adds
-// its accumulator row, rotates the K columns and writes its 16 + 16 K or V values into
-// its warp's two shared-memory boxes (32 rows x 16 columns each), which one lane of the
-// warp stores by TMA; the tensor map clips the rows past the selection.
+// tcgen05.mma into one of two TMEM accumulators.  The epilogue warps prefetch, one unit
+// ahead, exactly the reference bytes they will read (32 rows x 16 column pairs x <= 4
+// references, 16-byte cp.async copies): the two warps that read the two halves of the
+// same 32-byte sectors share one shared-memory slot per reference, one copying the x
+// sectors and the other the y sectors, and meet at a named barrier per reference.  Each
+// epilogue thread then sums its row's references (exact in fp32), adds the sum / k_i to
+// its accumulator row (one fma for k_i = 1, 2, 4, where the scaling is exact; the
+// correctly rounded s / 3 for k_i = 3), rotates the K columns and writes its 16 + 16 K
+// or V values into its warp's two shared-memory boxes (32 rows x 16 columns each),
+// which one lane of the warp stores by TMA; the tensor map clips the rows past the
+// selection.
 //
 // Back-to-back launches overlap: every CTA lets the next launch of the stream start its
 // CTAs as SMs free up, and a thread waits for the previous grid to complete only before

@@ -69,3 +69,14 @@ def test_step_config_names_the_bench_workload():
     cfg = bench.step_config(w, 1)
     assert cfg["tokens_per_step"] == w.T + w.steps * w.n_sel == 32768 + 64 * 9830
     assert cfg["workload"].startswith("llama8b: ")
+
+
+def test_code_hash_ignores_comments_only(tmp_path):
+    a = tmp_path / "a.cu"
+    b = tmp_path / "b.cu"
+    c = tmp_path / "c.cu"
+    a.write_text("// header\nint f(int x) {\n  return x + 1;  // add one\n}\n")
+    b.write_text("// a different header\n\nint f(int x) {\n  return x + 1;\n}\n")
+    c.write_text("int f(int x) {\n  return x + 2;\n}\n")
+    assert bench.code_sha1(str(a)) == bench.code_sha1(str(b))
+    assert bench.code_sha1(str(a)) != bench.code_sha1(str(c))
