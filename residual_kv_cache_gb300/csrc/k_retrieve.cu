@@ -3,17 +3,18 @@
 //
 // For a tile of 128 query tokens of one sequence and a tile of 256 pool slots the
 // tensor cores compute the dot products a_i . r_j (bf16 operands, exact products, fp32
-// accumulation in TMEM).  The epilogue thread that owns query row i (one TMEM lane)
-// turns each into the ranking score ||r_j||^2 - 2 a_i . r_j (= ||a_i - r_j||^2 minus a
-// per-row constant), masks slots whose reference is not strictly before the token,
-// and keeps a sorted running top-4 in registers across the pool tiles.  A sequence's
-// pool slots hold its reference positions in increasing order, so the references
-// before position p are exactly slots 0 .. ref_before[p] - 1: the mask is one compare
-// with a per-row bound.  The unit's 256 squared norms are staged once in shared memory
-// and read four at a time by broadcast loads.  Equal scores
-// keep the smaller slot because slots are visited in increasing order with a strict
-// comparison.  fp32 queries are split into three bf16 pieces (hi + mid + lo == x), so
-// the products stay exact and the three partial dots accumulate into one fp32 sum.
+// accumulation in TMEM).  Two epilogue warpgroups split the 256 slots; the thread of
+// each that owns query row i (one TMEM lane) turns its dot products into the ranking
+// score ||r_j||^2 - 2 a_i . r_j (= ||a_i - r_j||^2 minus a per-row constant), masks
+// slots whose reference is not strictly before the token, and keeps a sorted top-4;
+// the second group hands its list to the first, which inserts it.  A sequence's pool
+// slots hold its reference positions in increasing order, so the references before
+// position p are exactly slots 0 .. ref_before[p] - 1: the mask is one compare with a
+// per-row bound.  The unit's 256 squared norms are staged once in shared memory and
+// read four at a time by broadcast loads.  Equal scores keep the smaller slot because
+// slots are visited in increasing order with a strict comparison.  fp32 queries are
+// split into three bf16 pieces (hi + mid + lo == x), so the products stay exact and the
+// three partial dots accumulate into one fp32 sum.
 //
 // Work unit = (128-query tile, 256-slot pool tile): all units cost the same, so a
 // persistent grid balances them.  Each unit leaves a sorted partial top-4 per query

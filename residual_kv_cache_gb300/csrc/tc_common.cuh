@@ -1,12 +1,15 @@
 // tc_common.cuh - pieces shared by the tcgen05 kernels: shared-memory carve-up, the
 // TMA producer / MMA issuer ring protocol, and the bounded teardown.
 //
-// Warp roles of every tensor-core kernel here (256 threads):
+// Warp roles of the encoder GEMMs (256 threads):
 //   warp 0      TMA producer (one elected lane)
 //   warp 1      MMA issuer (one elected lane)
 //   warp 2      TMEM allocator (whole warp), idle otherwise
 //   warp 3      idle
 //   warps 4..7  epilogue: warp 4+w owns TMEM lanes [32w, 32w+32), i.e. tile rows.
+// The retrieval (384 threads, two epilogue warpgroups) and the restore (640 threads,
+// four) keep warps 0 and 1 in these roles and add epilogue warps; a warp w reads TMEM
+// lanes [32 (w % 4), +32).
 #pragma once
 #include "ptx.cuh"
 #include "rkv_internal.h"
