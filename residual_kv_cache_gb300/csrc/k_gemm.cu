@@ -55,7 +55,6 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 // ---------------------------------------------------------------- epilogues
 struct Epi12 {
   using Args = Epi12Args;
-  static constexpr int BN = kEncN;
   static constexpr bool kSplitA = true;
   __device__ static void run(const Args& a, uint32_t tacc, int m, int n, int row_in_tile,
                              int* status) {
