@@ -61,7 +61,7 @@ constexpr int kMaxStages = 8;
 // Extra cost of a token-tile change inside a CTA's range (staging the next tile's z~ and
 // cos/sin while the tensor core drains), in quarter units.
 #ifndef RKV_TILE_CHANGE_COST4
-#define RKV_TILE_CHANGE_COST4 8
+#define RKV_TILE_CHANGE_COST4 10
 #endif
 constexpr int kTileChangeCost4 = RKV_TILE_CHANGE_COST4;
 
