@@ -198,7 +198,8 @@ rkv_status rkv_compress(rkv_ctx* ctx, const void* kv, int64_t kv_row_stride,
  *   seq, pos (device, int32) [n_sel]: the selected tokens, any order,
  *     duplicates allowed.
  *   k_out, v_out (device) [n_sel, N, D] of cfg.out_dtype: K (rotated) and V;
- *     32-byte aligned (RKV_EALIGN otherwise).
+ *     32-byte aligned (RKV_EALIGN otherwise).  Only their first n_sel rows are
+ *     written.
  * An out-of-range (seq, pos) or a never-written token yields zero rows and a
  * status bit (RKV_FLAG_BAD_INDEX / RKV_FLAG_UNWRITTEN).  n_sel = 0 is a no-op.
  */
