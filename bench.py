@@ -379,6 +379,7 @@ def run_cuda(args):
         "kernels": {k: {kk: round(vv, 4) for kk, vv in v.items()} for k, v in rows.items()},
         "e2e": e2e,
         "sparse_attention": attn,
+        "storage": storage_report(codec, w),
         "gpu_launches": int(launches),
         "clocks": clk,
         "device_status": int(status),
@@ -555,6 +556,20 @@ def cpu_baseline(budget_s: float = 15.0) -> dict:
 def _workload():
     import synth
     return synth.workload(WORKLOAD)
+
+
+def storage_report(codec, w) -> dict:
+    """Bytes the codec keeps per token (its storage tensors over B x T tokens) against FP16
+    K and V (2 bytes per value of the 2d_k-wide row).  The bf16 shadow of the FP8 pool is
+    the retrieval's tensor-core operand, shown separately."""
+    names = ["pool_fp8", "pool_bf16", "pool_norm2", "pool_pos", "codes", "meta", "ref_idx"]
+    nbytes = {n: getattr(codec, n).numel() * getattr(codec, n).element_size() for n in names}
+    tokens = codec.codes.shape[0] * codec.codes.shape[1]
+    fp16 = 2 * w.d_kv
+    total = sum(nbytes.values())
+    return {"bytes_per_token": round(total / tokens, 1),
+            "fraction_of_fp16_kv": round(total / tokens / fp16, 4),
+            "fraction_without_pool_shadow": round((total - nbytes["pool_bf16"]) / tokens / fp16, 4)}
 
 
 def step_config(w, world: int) -> dict:
