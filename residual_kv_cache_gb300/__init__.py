@@ -131,6 +131,15 @@ _raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 _cur_device = getattr(torch._C, "_cuda_getDevice", None)
 
 
+def _check_out(t, n_elems: int, dtype, what: str):
+    """A caller-supplied output: a contiguous CUDA tensor of `dtype` with room for
+    n_elems values (the library writes exactly that many, from its start)."""
+    if not isinstance(t, torch.Tensor) or t.dtype != dtype or not t.is_cuda \
+            or not t.is_contiguous() or t.numel() < n_elems:
+        raise ValueError(f"{what} must be a contiguous CUDA tensor of {dtype} with at least "
+                         f"{n_elems} elements")
+
+
 def _stream_ptr(stream) -> int:
     if stream is not None:
         return stream.cuda_stream
@@ -274,6 +283,10 @@ class Codec:
         for t in (seq, pos):
             if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
                 raise ValueError("seq and pos must be contiguous int32 CUDA tensors")
+        if int(seq.numel()) != n:
+            raise ValueError("seq and pos must have the same length")
+        _check_out(k_out, n * N * D, odt, "k_out")
+        _check_out(v_out, n * N * D, odt, "v_out")
         _check(lib().rkv_reconstruct(self._ctx, seq.data_ptr(), pos.data_ptr(), n,
                                      k_out.data_ptr(), v_out.data_ptr(), _stream_ptr(stream)))
         return k_out, v_out
@@ -293,6 +306,7 @@ class Codec:
             raise ValueError("k and v must have the same rows")
         if out is None:
             out = torch.empty((q.shape[0], D), dtype=torch.float32, device=q.device)
+        _check_out(out, q.shape[0] * D, torch.float32, "out")
         _check(lib().rkv_sparse_attention(self._ctx, q.data_ptr(), q.shape[0], k.data_ptr(),
                                           v.data_ptr(), k.shape[0], out.data_ptr(),
                                           _stream_ptr(stream)))

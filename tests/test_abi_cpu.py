@@ -99,3 +99,16 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(rkv, "_lib", None)
     with pytest.raises(rkv.RkvLibraryMissing):
         rkv.lib()
+
+
+def test_output_buffers_are_checked_before_any_call():
+    """A caller's output tensor must be CUDA, contiguous, of the output dtype and large
+    enough; anything else is refused on the host (no device write past its end)."""
+    import torch
+    from residual_kv_cache_gb300 import _check_out
+    with pytest.raises(ValueError):
+        _check_out(torch.empty(10, dtype=torch.bfloat16), 10, torch.bfloat16, "k_out")  # CPU
+    with pytest.raises(ValueError):
+        _check_out(None, 10, torch.bfloat16, "k_out")
+    with pytest.raises(ValueError):
+        _check_out(torch.empty(10, dtype=torch.float32), 10, torch.bfloat16, "k_out")
