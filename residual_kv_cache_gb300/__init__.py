@@ -131,6 +131,31 @@ _raw_stream = getattr(torch._C, "_cuda_getCurrentRawStream", None)
 _cur_device = getattr(torch._C, "_cuda_getDevice", None)
 
 
+def _torch_dtype(dt):
+    """torch dtype of a config dtype ("fp32" / "bf16" or the torch dtypes themselves)."""
+    return torch.float32 if _dtype_code(dt) == RKV_F32 else torch.bfloat16
+
+
+def _check_kv_rows(kv, d_kv: int, dtype, n: int, src, need_cuda: bool = True):
+    """The rows a write call reads: a [rows, 2d_k] tensor of the configured kv dtype with
+    unit element stride, and every row index it will read below `rows` (the library
+    knows only the row stride, not how many rows there are).  Negative indices are left
+    to the library's own check."""
+    if not isinstance(kv, torch.Tensor) or kv.dim() != 2 or kv.shape[1] != d_kv \
+            or (need_cuda and not kv.is_cuda):
+        raise ValueError("kv must be a [rows, 2*d_k] CUDA tensor")
+    if kv.dtype != dtype or kv.stride(1) != 1:
+        raise ValueError(f"kv must hold {dtype} values with unit element stride")
+    rows = kv.shape[0]
+    if n == 0:
+        return
+    if src is None:
+        if n > rows:
+            raise ValueError("kv has fewer rows than the call writes")
+    elif int(src.max()) >= rows:
+        raise ValueError("src_rows must index rows of kv")
+
+
 def _check_out(t, n_elems: int, dtype, what: str):
     """A caller-supplied output: a contiguous CUDA tensor of `dtype` with room for
     n_elems values (the library writes exactly that many, from its start)."""
@@ -252,14 +277,13 @@ class Codec:
 
     # -- ABI calls -------------------------------------------------------------------
     def _rows_call(self, fn, kv, seq, pos, src_rows, stream):
-        if kv.dim() != 2 or kv.shape[1] != self.cfg.d_kv or not kv.is_cuda:
-            raise ValueError("kv must be a [rows, 2*d_k] CUDA tensor")
         seq_a, seq_p = _host_i32(seq)
         pos_a, pos_p = _host_i32(pos)
         src_a, src_p = _host_i32(src_rows)
         n = len(pos_a)
         if len(seq_a) != n or (src_a is not None and len(src_a) != n):
             raise ValueError("seq, pos and src_rows must have the same length")
+        _check_kv_rows(kv, self.cfg.d_kv, _torch_dtype(self.cfg.kv_dtype), n, src_a)
         _check(fn(self._ctx, kv.data_ptr(), kv.stride(0), src_p, seq_p, pos_p, n,
                   _stream_ptr(stream)))
 
@@ -275,7 +299,7 @@ class Codec:
         """Restore selected tokens; seq, pos are int32 CUDA tensors.  Returns (K, V)."""
         n = int(pos.numel())
         N, D = self.cfg.n_kv_heads, self.cfg.head_dim
-        odt = torch.float32 if self.cfg.out_dtype == "fp32" else torch.bfloat16
+        odt = _torch_dtype(self.cfg.out_dtype)
         if k_out is None:
             k_out = torch.empty((n, N, D), dtype=odt, device=self.device)
         if v_out is None:
@@ -295,7 +319,7 @@ class Codec:
         """softmax(q K^T / sqrt(D)) V over the rows of k, v (a restore's outputs).
         q: [H_q, D] fp32 CUDA tensor; returns out [H_q, D] fp32."""
         N, D = self.cfg.n_kv_heads, self.cfg.head_dim
-        odt = torch.float32 if self.cfg.out_dtype == "fp32" else torch.bfloat16
+        odt = _torch_dtype(self.cfg.out_dtype)
         if q.dtype != torch.float32 or not q.is_cuda or not q.is_contiguous() or q.dim() != 2 \
                 or q.shape[1] != D:
             raise ValueError("q must be a contiguous [H_q, D] fp32 CUDA tensor")

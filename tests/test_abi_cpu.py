@@ -112,3 +112,27 @@ def test_output_buffers_are_checked_before_any_call():
         _check_out(None, 10, torch.bfloat16, "k_out")
     with pytest.raises(ValueError):
         _check_out(torch.empty(10, dtype=torch.float32), 10, torch.bfloat16, "k_out")
+
+
+def test_write_rows_are_checked_before_any_call():
+    """The rows a write reads: the configured dtype, unit element stride, and every index
+    below the tensor's row count (the library cannot see that count)."""
+    import numpy as np
+    import torch
+    from residual_kv_cache_gb300 import _check_kv_rows
+    kv = torch.zeros(256, 256, dtype=torch.float32)
+    ok = dict(need_cuda=False)
+    _check_kv_rows(kv, 256, torch.float32, 1, None, **ok)                    # rows 0 .. n-1
+    _check_kv_rows(kv, 256, torch.float32, 3, np.array([0, 17, 255], np.int32), **ok)
+    _check_kv_rows(kv.view(-1)[1:1 + 255 * 256].view(255, 256), 256, torch.float32, 1, None, **ok)
+    _check_kv_rows(kv, 256, torch.float32, 1, np.array([-1], np.int32), **ok)  # the library's
+    with pytest.raises(ValueError):
+        _check_kv_rows(kv.to(torch.bfloat16), 256, torch.float32, 1, None, **ok)
+    with pytest.raises(ValueError):
+        _check_kv_rows(kv, 256, torch.float32, 2, np.array([0, 256], np.int32), **ok)
+    with pytest.raises(ValueError):
+        _check_kv_rows(kv, 256, torch.float32, 300, None, **ok)
+    with pytest.raises(ValueError):
+        _check_kv_rows(kv.t(), 256, torch.float32, 1, None, **ok)
+    with pytest.raises(ValueError):
+        _check_kv_rows(kv, 256, torch.float32, 1, None)                      # not on the GPU
