@@ -262,7 +262,10 @@ void rkv_free(rkv_ctx* ctx);
  *   pool_pos   (device, int32) [R]      their positions; INT32_MAX marks an empty slot
  *   out_idx    (device, int32) [n, topk]  output
  *   flags      (device, int32) or NULL: RKV_FLAG_* bits are ORed into it (the caller
- *              clears it); a set RKV_FLAG_TIMEOUT means out_idx is not valid.
+ *              clears it).  If a wait of the kernel gives up (RKV_FLAG_TIMEOUT), every
+ *              slot of out_idx is written as -1.  With NULL, the call uses a status word
+ *              of its own inside the library's scratch, cleared at the start of the
+ *              call, with the same effect on out_idx.
  * d must be a multiple of 64, topk in 1..4, queries and pool 16-byte aligned.
  * Scratch: a fixed 4 MiB device array inside the library (every GPU that loads the
  * library holds it until the process exits), enough for ceil(n/128)*ceil(R/256) <= 1024
@@ -271,8 +274,9 @@ void rkv_free(rkv_ctx* ctx);
  * call writes every entry it later reads.  All calls share the array, so calls whose
  * kernels overlap on the GPU (different streams, no ordering) race and must not be made.
  * The first call on a device looks up the array's device address (cudaGetSymbolAddress
- * with that device current); make that first call before any stream capture.  No call
- * allocates or frees memory.
+ * with that device current); make that first call before any stream capture.  A failed
+ * look-up returns RKV_ECUDA and is tried again by the next call.  No call allocates or
+ * frees memory.
  */
 rkv_status rkv_retrieve_noalloc(const void* queries, const int32_t* q_pos, int32_t n,
                                 const void* pool, const float* pool_norm2,

@@ -228,12 +228,30 @@ def retrieve_noalloc(queries, q_pos, pool, pool_norm2, pool_pos, topk: int = 4, 
                      flags=None, stream=None):
     """Top-k retrieval of one sequence through rkv_retrieve_noalloc (no allocation in the
     library; scratch is a fixed device array).  queries [n, d] bf16, q_pos [n] int32,
-    pool [R, d] bf16, pool_norm2 [R] fp32, pool_pos [R] int32, all CUDA tensors.
-    Returns out [n, topk] int32 (allocated here by torch if not given)."""
+    pool [R, d] bf16, pool_norm2 [R] fp32, pool_pos [R] int32, all contiguous CUDA
+    tensors (the library reads rows of exactly d elements).  Returns out [n, topk] int32
+    (allocated here by torch if not given)."""
+    for t, dt, what in ((queries, torch.bfloat16, "queries"), (pool, torch.bfloat16, "pool"),
+                        (q_pos, torch.int32, "q_pos"), (pool_norm2, torch.float32, "pool_norm2"),
+                        (pool_pos, torch.int32, "pool_pos")):
+        if not isinstance(t, torch.Tensor) or t.dtype != dt or not t.is_cuda \
+                or not t.is_contiguous():
+            raise ValueError(f"{what} must be a contiguous CUDA tensor of {dt}")
+    if queries.dim() != 2 or pool.dim() != 2 or pool.shape[1] != queries.shape[1]:
+        raise ValueError("queries [n, d] and pool [R, d] must share d")
     n, d = queries.shape
     R = pool.shape[0]
+    if q_pos.numel() != n:
+        raise ValueError("q_pos must hold one position per query row")
+    if pool_norm2.numel() < R or pool_pos.numel() < R:
+        raise ValueError("pool_norm2 and pool_pos must hold one entry per pool row")
+    if not 1 <= topk <= 4:
+        raise ValueError("topk must be in 1..4")
     if out is None:
         out = torch.empty((n, topk), dtype=torch.int32, device=queries.device)
+    _check_out(out, n * topk, torch.int32, "out")
+    if flags is not None:
+        _check_out(flags, 1, torch.int32, "flags")
     fp = flags.data_ptr() if flags is not None else None
     _check(lib().rkv_retrieve_noalloc(queries.data_ptr(), q_pos.data_ptr(), n, pool.data_ptr(),
                                       pool_norm2.data_ptr(), pool_pos.data_ptr(), R, d, topk,

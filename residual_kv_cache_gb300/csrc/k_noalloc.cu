@@ -232,11 +232,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // One thread per query: merge its pool tiles' partial lists (increasing slots) and
-// write the final slots.  Every partial it reads was written earlier in this call.
+// write the final slots.  Every partial it reads was written earlier in this call.  If a
+// wait of the retrieval kernel gave up (RKV_FLAG_TIMEOUT in the call's status word), some
+// partial lists may be stale, so every slot of the output is written as -1 instead.
 __global__ void noalloc_merge_kernel(const int2* __restrict__ part, const int32_t* __restrict__ q_pos,
-                                     int n, int n_rt, int topk, int32_t* __restrict__ out_idx) {
+                                     int n, int n_rt, int topk, const int* status,
+                                     int32_t* __restrict__ out_idx) {
   const int q = blockIdx.x * blockDim.x + threadIdx.x;
   if (q >= n) return;
+  if (*reinterpret_cast<const volatile int*>(status) & RKV_FLAG_TIMEOUT) {
+    for (int i = 0; i < topk; ++i) out_idx[(int64_t)q * topk + i] = -1;
+    return;
+  }
   const int t = q / kTileM, r = q % kTileM;
   float bd[4] = {FLT_MAX, FLT_MAX, FLT_MAX, FLT_MAX};
   int bj[4] = {-1, -1, -1, -1};
@@ -254,9 +261,8 @@ __global__ void noalloc_merge_kernel(const int2* __restrict__ part, const int32_
 
 // ---- per-device set-up: the device address of the scratch, and a status word inside it
 struct DeviceSlot {
-  std::once_flag once;
-  cudaError_t err = cudaSuccess;
-  void* scratch = nullptr;
+  std::mutex mu;
+  void* scratch = nullptr;   // set once the look-up has succeeded
 };
 constexpr int kMaxDevices = 64;
 DeviceSlot g_slots[kMaxDevices];
@@ -314,12 +320,22 @@ rkv_status noalloc_retrieve(const void* queries, const int32_t* q_pos, int32_t n
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
     return *why = "no usable current device", RKV_ECUDA;
   DeviceSlot& slot = g_slots[dev];
-  std::call_once(slot.once, [&] {
-    // With this device current: the device address of the scratch array.
-    slot.err = cudaGetSymbolAddress(&slot.scratch, g_noalloc_scratch);
-  });
-  if (slot.err != cudaSuccess || slot.scratch == nullptr)
-    return *why = "cudaGetSymbolAddress of the scratch failed", RKV_ECUDA;
+  void* scratch = nullptr;
+  {
+    // With this device current: the device address of the scratch array.  Only a
+    // successful look-up is kept, so a call that failed (for instance one made during a
+    // stream capture) leaves the next call free to try again.
+    std::lock_guard<std::mutex> lock(slot.mu);
+    if (slot.scratch == nullptr) {
+      void* p = nullptr;
+      if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) {
+        cudaGetLastError();
+        return *why = "cudaGetSymbolAddress of the scratch failed", RKV_ECUDA;
+      }
+      slot.scratch = p;
+    }
+    scratch = slot.scratch;
+  }
   PFN_cuTensorMapEncodeTiled_v12000 enc = na_encoder();
   if (!enc) return *why = "cuTensorMapEncodeTiled is unavailable", RKV_ECUDA;
   CUtensorMap tmQ, tmP;
@@ -335,8 +351,8 @@ rkv_status noalloc_retrieve(const void* queries, const int32_t* q_pos, int32_t n
   a.n_units = (int)units;
   a.norm2 = pool_norm2;
   a.pool_pos = pool_pos;
-  a.part = static_cast<int2*>(slot.scratch);
-  a.status = flags ? flags : static_cast<int*>(slot.scratch) + kStatusOffsetInts;
+  a.part = static_cast<int2*>(scratch);
+  a.status = flags ? flags : static_cast<int*>(scratch) + kStatusOffsetInts;
   const size_t smem = 1024 + (size_t)kNaStages * (kTileABytes + kNaBBytes) + 8 * (2 * kNaStages + 4) + 16;
   if (cudaFuncSetAttribute(noalloc_retrieve_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            (int)smem) != cudaSuccess)
@@ -345,9 +361,14 @@ rkv_status noalloc_retrieve(const void* queries, const int32_t* q_pos, int32_t n
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
     return *why = "cudaDeviceGetAttribute failed", RKV_ECUDA;
   const int grid = units < sms ? (int)units : sms;
+  // without caller flags, the call's status word is the scratch's own: cleared here so
+  // that it holds this call's verdict alone
+  if (!flags && cudaMemsetAsync(a.status, 0, sizeof(int), s) != cudaSuccess)
+    return *why = "clearing the status word failed", RKV_ECUDA;
   noalloc_retrieve_kernel<<<grid, kThreads, smem, s>>>(tmQ, tmP, a);
   if (cudaGetLastError() != cudaSuccess) return *why = "retrieval launch failed", RKV_ECUDA;
-  noalloc_merge_kernel<<<(n + 127) / 128, 128, 0, s>>>(a.part, q_pos, n, n_rt, topk, out_idx);
+  noalloc_merge_kernel<<<(n + 127) / 128, 128, 0, s>>>(a.part, q_pos, n, n_rt, topk, a.status,
+                                                        out_idx);
   if (cudaGetLastError() != cudaSuccess) return *why = "merge launch failed", RKV_ECUDA;
   return RKV_OK;
 }

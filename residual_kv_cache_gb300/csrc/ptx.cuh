@@ -402,8 +402,9 @@ __device__ __forceinline__ void fp8x4_add(uint32_t w, float& s0, float& s1, floa
 }
 
 // Correctly rounded s / 3 for every fp32 s that is a sum of at most three E4M3 values:
-// q = RN(s * RN(1/3)), r = s - 3 q (exact), RN(q + r * RN(1/3)).  Checked against the
-// exact quotient for all 256317 such sums.
+// q = RN(s * RN(1/3)), r = s - 3 q (exact), RN(q + r * RN(1/3)) - Markstein's residual
+// correction of a reciprocal product.  A host test emulates the three roundings exactly
+// and checks the result against the exact quotient for all 256317 such sums.
 __device__ __forceinline__ float div3_rn(float s) {
   const float c = __uint_as_float(0x3EAAAAABu);       // RN(1/3)
   const float q = __fmul_rn(s, c);

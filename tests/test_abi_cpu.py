@@ -136,3 +136,23 @@ def test_write_rows_are_checked_before_any_call():
         _check_kv_rows(kv.t(), 256, torch.float32, 1, None, **ok)
     with pytest.raises(ValueError):
         _check_kv_rows(kv, 256, torch.float32, 1, None)                      # not on the GPU
+
+
+def test_retrieve_noalloc_binding_rejects_bad_arguments():
+    """The binding checks what the library cannot see (dtypes, contiguity, lengths)
+    before any call: CPU tensors, a strided query view, an fp32 pool and short position
+    arrays are refused with ValueError."""
+    import torch
+    import residual_kv_cache_gb300 as rkv
+    n, d, R = 4, 64, 8
+    q = torch.zeros((n, d), dtype=torch.bfloat16)
+    args = dict(q_pos=torch.zeros(n, dtype=torch.int32), pool=torch.zeros((R, d), dtype=torch.bfloat16),
+                pool_norm2=torch.zeros(R), pool_pos=torch.zeros(R, dtype=torch.int32))
+    with pytest.raises(ValueError):
+        rkv.retrieve_noalloc(q, **args)                                  # not CUDA tensors
+    with pytest.raises(ValueError):
+        rkv.retrieve_noalloc(torch.zeros((n, 2 * d), dtype=torch.bfloat16)[:, :d], **args)
+    with pytest.raises(ValueError):
+        rkv.retrieve_noalloc(q, **{**args, "pool": torch.zeros((R, d))})
+    with pytest.raises(ValueError):
+        rkv.retrieve_noalloc(q, **{**args, "q_pos": torch.zeros(n - 1, dtype=torch.int32)})

@@ -160,7 +160,8 @@ def test_retrieval_warmup_k_i():
         slots, _ = C.retrieve(kv[pos], pool.vals, pool.pos, pos, 4)
         n_vis = pos // s + 1
         assert len(slots) == min(4, n_vis)
-    # the survey's walk-through: tokens 1..s-1 see one reference, s+1 sees two
+    # warm-up, k_i = min(k, |T_ref,i|) (ResidualKV notes §2.1): tokens 1..s-1 see one
+    # reference (position 0), token s+1 sees two
     assert len(C.retrieve(kv[1], pool.vals, pool.pos, 1, 4)[0]) == 1
     assert len(C.retrieve(kv[s + 1], pool.vals, pool.pos, s + 1, 4)[0]) == 2
 
