@@ -17,10 +17,9 @@ import torch
 
 import synth
 from oracle import codec as C
-from oracle import formats as F
 
-from _common import (codes_identical_fraction, check_codes_interval, encoder_intervals, gpu_prefill, idx_parity,
-                     make_codec, np64, oracle_shape, rel_fro)
+from _common import (assert_code_parity, gpu_prefill, idx_parity, make_codec, np64, oracle_shape,
+                     rel_fro)
 
 pytestmark = pytest.mark.gpu
 cuda = pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a CUDA GPU")
@@ -45,17 +44,11 @@ def _check_sampled(c, w, kv64, W64, pos, seq=0, bits=None):
     assert not bad, f"retrieval differs beyond near-ties at positions {pos[bad][:5]}"
     same = np.all(gidx == enc["idx"], axis=1)
     rows = pos[same]
-    iv = encoder_intervals(kv64[rows], pool.vals, enc["idx"][same], W64)
-    packed = c.codes[seq].cpu().numpy()[rows]
-    if sh.bits == 16:
-        got = C.unpack_codes(packed, 16, sh.d_c)
-        assert np.all((got >= F.bf16(iv["z"] - iv["w"])) & (got <= F.bf16(iv["z"] + iv["w"])))
-    else:
-        gq = C.unpack_codes(packed, sh.bits, sh.d_c)
-        gm = c.meta[seq].cpu().numpy().astype(np.float64)[rows]
-        assert codes_identical_fraction(gq, gm, enc["q"][same], enc["meta"][same]) >= 0.999
-        viol = check_codes_interval(gq, gm, iv["z"], iv["w"], sh.bits)
-        assert not viol, viol[:3]
+    gq = C.unpack_codes(c.codes[seq].cpu().numpy()[rows], sh.bits, sh.d_c)
+    gm = c.meta[seq].cpu().numpy().astype(np.float64)[rows]
+    assert_code_parity(f"{w.name} T={kv64.shape[0]} sampled", gq, gm, enc["q"][same],
+                       enc["meta"][same], enc["z"][same], kv64[rows], pool.vals,
+                       enc["idx"][same], W64, sh.bits, sh.group)
     return pool, sh
 
 
