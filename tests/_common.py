@@ -119,15 +119,35 @@ U32 = 2.0 ** -24
 
 
 def fp32_chunked_bound(X: np.ndarray, W: np.ndarray, chunk: int = 16) -> np.ndarray:
-    """Bound on |fl32(X W) - X W| for a K-ordered accumulation in 16-wide chunks."""
-    n, K = X.shape
-    S = np.zeros((n, W.shape[1]))
-    acc = np.zeros_like(S)
+    """Bound on |fl32(X W) - X W| for a K-ordered accumulation in 16-wide chunks.  The
+    bound's own sums run in fp32 (torch, all host cores) and are widened by 2^-10 to
+    cover their rounding."""
+    Xt = torch.from_numpy(np.ascontiguousarray(X, dtype=np.float32))
+    Wt = torch.from_numpy(np.ascontiguousarray(W, dtype=np.float32))
+    Xa, Wa = Xt.abs(), Wt.abs()
+    n, K = Xt.shape
+    S = torch.zeros((n, Wt.shape[1]))
+    acc = Xa @ Wa                                      # the in-chunk roundings, all chunks
     for k0 in range(0, K, chunk):
-        xs, ws = X[:, k0:k0 + chunk], W[k0:k0 + chunk]
-        S += xs @ ws
-        acc += np.abs(S) + np.abs(xs) @ np.abs(ws)
-    return 0.5 * U32 * acc
+        S.addmm_(Xt[:, k0:k0 + chunk], Wt[k0:k0 + chunk])
+        acc.add_(S.abs())
+    return (0.5 * U32 * (1.0 + 2.0 ** -10)) * acc.double().numpy()
+
+
+def bf16_near(x: np.ndarray) -> np.ndarray:
+    """Nearest bf16 value of each float64 (ties to even), by the bits of the binary64
+    encoding: exact where the result is a normal bf16, which holds for the values these
+    bounds round; anything else goes through the oracle's general rounding."""
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    b = x.view(np.uint64)
+    lsb = (b >> np.uint64(45)) & np.uint64(1)
+    r = (b + np.uint64((1 << 44) - 1) + lsb) & ~np.uint64((1 << 45) - 1)
+    out = r.view(np.float64)
+    ax = np.abs(x)
+    odd = ~np.isfinite(out) | ((ax < 2.0 ** -126) & (ax != 0)) | (np.abs(out) > 3.3895313892515355e38)
+    if odd.any():
+        out[odd] = F.bf16(x[odd])
+    return out
 
 
 def hidden_bounds(X: np.ndarray, Wc1: np.ndarray, Wc2: np.ndarray):
@@ -143,7 +163,7 @@ def hidden_bounds(X: np.ndarray, Wc1: np.ndarray, Wc2: np.ndarray):
     h = sw * a2
     # Swish and the product in fp32: expf, add, divide, multiply (a few ulps)
     dh = dsw * da1 * np.abs(a2) + np.abs(sw) * da2 + 8 * U32 * np.abs(h) + da1 * da2
-    return h, dh, F.bf16(h - dh), F.bf16(h + dh)
+    return h, dh, bf16_near(h - dh), bf16_near(h + dh)
 
 
 def z_bounds(Hk, Hk_lo, Hk_hi, Hm, Hm_lo, Hm_hi, Wc3):
@@ -208,7 +228,7 @@ def encoder_intervals(kv64_rows, pool_vals, idx_rows, W64):
     xk, xm = oracle_operand_rows(kv64_rows, pool_vals, idx_rows)
     hk, dhk, hk_lo, hk_hi = hidden_bounds(xk, W64["Wc1"], W64["Wc2"])
     hm, dhm, hm_lo, hm_hi = hidden_bounds(xm, W64["Wc1"], W64["Wc2"])
-    Hk, Hm = F.bf16(hk), F.bf16(hm)
+    Hk, Hm = bf16_near(hk), bf16_near(hm)
     z, w = z_bounds(Hk, hk_lo, hk_hi, Hm, hm_lo, hm_hi, W64["Wc3"])
     return dict(Hk=Hk, Hk_lo=hk_lo, Hk_hi=hk_hi, Hm=Hm, Hm_lo=hm_lo, Hm_hi=hm_hi, z=z, w=w)
 

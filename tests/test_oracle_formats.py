@@ -1,4 +1,6 @@
 """Pins of the oracle's number formats against library conversions and brute force."""
+import os
+
 import numpy as np
 import pytest
 import torch
@@ -88,3 +90,17 @@ def test_fp32_is_ieee_single():
     assert F.fp32(x)[0] == 1.0
     assert F.fp32(x)[1] == 1 + 2 ** -22
     assert F.fp32(x)[2] == float(np.float32(0.1))
+
+
+def test_parity_helper_bf16_rounding_matches_the_oracle():
+    """The fast bf16 rounding the parity bounds use equals the oracle's general rounding
+    on random values, exact ties and values next to ties."""
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.abspath(__file__)))
+    from _common import bf16_near
+    rng = np.random.default_rng(5)
+    x = rng.normal(0, 1, 200000) * 10.0 ** rng.uniform(-8, 8, 200000)
+    ties = (np.arange(1, 2000) * 2 + 1) * 2.0 ** -8 * 3.0       # between bf16 neighbours
+    near = np.concatenate([ties * (1 + 2.0 ** -40), ties * (1 - 2.0 ** -40)])
+    for v in (x, ties, near, -ties, np.array([0.0, -0.0, 1.0, 2.0 ** -120])):
+        assert np.array_equal(bf16_near(v), F.bf16(v))
