@@ -1,20 +1,31 @@
 """Benchmark of the ResidualKV cache codec on GB300.
 
-One step = the whole hot path on the Llama-3.1-8B-shaped layer (T = 32768 tokens,
-2d_k = 2048, d_c = 512, d_ff = 1536, stride 16, INT4): the full prefill write
-(pool append of 2048 references + compress of 30720 tokens), then 64 decode steps
-each restoring a fresh seeded random 30 % (9830 tokens).  Inputs are resident in HBM
-before the timed region; L2 is flushed (a 512 MiB write) before every timed step.
+Workloads (`--workload`; the default run measures all of them and prints one line whose
+headline is the first):
 
-value  = (tokens written + tokens restored) per second over the timed steps, summed
-         over ranks (weak scaling: every rank runs its own independent sequence).
-e2e    = the same through the public API with host buffers: every step copies the
-         step's kv rows and selections from pinned host memory and reads the last
-         decode step's K and V back to the host; the copies run on a second stream,
-         double-buffered, so a step's upload overlaps the previous step's compute.
+* qwen7b     the 28-layer Qwen2.5-7B-shaped stack (2d_k = 1024, d_c = 256, d_ff = 768),
+             T = 131072 per layer, stride 16, INT4.  One step = the prefill write of all
+             28 layers, then 64 decode steps, each restoring in every layer 30 % of the
+             tokens as 614 random contiguous 64-token blocks (39296 tokens).
+* llama8b    one Llama-3.1-8B-shaped layer (2d_k = 2048, d_c = 512, d_ff = 1536),
+             T = 32768: the prefill write, then 64 decode steps of 9830 random tokens.
+* batched    the Llama layer shape, 16 sequences prefilled to 16384 tokens.  One step =
+             one decode step: one new token per sequence written (a single-token
+             compress, or a pool append at a reference position), then 30 % of every
+             sequence's history restored in one call; per-step latency p50 / p99.
+* long_int2  the Llama layer shape at T = 262144 with INT2 codes: prefill write, then 16
+             decode steps of 30 % random tokens.
+* long_bf16z the same at T = 65536 with quantisation off (bf16 z).
 
-`--impl reference` times the CPU oracle (test infrastructure) on bounded samples of
-the same workload and prints the same line with "impl": "reference".
+Inputs are resident in HBM before the timed region; L2 is flushed (a 512 MiB write)
+before every timed step.  value = (tokens written + tokens restored) per second over the
+timed steps, summed over ranks (weak scaling: every rank runs its own independent
+sequences).  e2e = the same through the public API with the step's inputs copied from
+pinned host memory inside the timed region and the last restore's K and V read back to
+the host (details in each e2e record).
+
+`--impl reference` times the CPU oracle (test infrastructure) on bounded samples of the
+headline workload and prints the same line with "impl": "reference".
 """
 from __future__ import annotations
 
@@ -32,13 +43,15 @@ if ROOT not in sys.path:
 
 import numpy as np  # noqa: E402
 
-WORKLOAD = "llama8b"
+WORKLOAD_ORDER = ("qwen7b", "llama8b", "batched", "long_int2", "long_bf16z")
+HEADLINE = "qwen7b"
 METRIC = "KV tokens compressed/s + selected tokens reconstructed/s"
 UNIT = "tokens/s"
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 # reference schedule (ResidualKV notes section 2.6): alpha = 0, n_sink = 0 is the fixed
 # stride of the workload; --alpha / --sink time the dynamic stride instead
 SCHEDULE = {"alpha": 0.0, "sink": 0}
+BATCHED_SLACK = 1024          # decode positions a batched run may append after its prefill
 
 
 def schedule_note(w) -> str:
@@ -48,11 +61,12 @@ def schedule_note(w) -> str:
             f"n_sink={SCHEDULE['sink']}")
 
 
-def codec_config(rkv, w, T):
+def codec_config(rkv, w, T, batch=1):
     return rkv.Config(n_kv_heads=w.n_kv_heads, head_dim=w.head_dim, d_c=w.d_c, d_ff=w.d_ff,
                       topk=w.topk, group=w.group, bits=w.bits, ref_stride=w.stride,
                       kv_dtype=w.kv_dtype, out_dtype=w.out_dtype, rope_base=w.rope_base,
-                      max_tokens=T, ref_alpha=SCHEDULE["alpha"], ref_sink=SCHEDULE["sink"])
+                      batch=batch, max_tokens=T, ref_alpha=SCHEDULE["alpha"],
+                      ref_sink=SCHEDULE["sink"])
 
 
 def split_positions(ref_pos, T):
@@ -101,19 +115,26 @@ def reduce_sum(value: float, world: int, device=None) -> float:
 
 
 # ------------------------------------------------------------------ work accounting
-def algorithmic_work(w, n_comp: int, n_sel: int, ref_pos) -> dict:
-    """Flops and bytes the method itself needs, per kernel launch of one step."""
+def per_token_bytes(w) -> dict:
+    code_b = w.d_c * w.bits // 8 if w.bits != 16 else 2 * w.d_c
+    meta_b = 0 if w.bits == 16 else 4 * (w.d_c // 32)
+    return {"code": code_b, "meta": meta_b, "idx": 4 * w.topk,
+            "out": w.d_kv * (4 if w.out_dtype == "fp32" else 2)}
+
+
+def algorithmic_work(w, n_comp: int, n_sel: int, ref_pos, T: int | None = None) -> dict:
+    """Flops and bytes the method itself needs: for the write kernels, summed over one
+    prefill of T tokens of one sequence (n_comp = T); for the restore, one launch of
+    n_sel selected tokens against a pool of len(ref_pos) references."""
+    T = w.T if T is None else T
     dkv, dff, dc = w.d_kv, w.d_ff, w.d_c
     ref_pos = np.asarray(ref_pos, dtype=np.int64)
     n_ref = len(ref_pos)
     n_non = n_comp - n_ref
-    code_b = dc * w.bits // 8 if w.bits != 16 else 2 * dc
-    meta_b = 0 if w.bits == 16 else 4 * (dc // 32)
-    idx_b = 4 * w.topk
-    out_b = 4 if w.out_dtype == "fp32" else 2
+    b = per_token_bytes(w)
     # references visible to each non-reference token (those at earlier positions)
-    before = np.searchsorted(ref_pos, np.arange(w.T), side="left")
-    isref = np.zeros(w.T, dtype=bool)
+    before = np.searchsorted(ref_pos, np.arange(T), side="left")
+    isref = np.zeros(T, dtype=bool)
     isref[ref_pos] = True
     avg_pool = float(before[~isref].sum()) / max(n_non, 1)
     return {
@@ -121,28 +142,28 @@ def algorithmic_work(w, n_comp: int, n_sel: int, ref_pos) -> dict:
                                      "bytes": 2 * n_non * dkv * 2 + 2 * dff * dkv * 2
                                      + 2 * n_non * dff * 2},
         "rkv_gemm3_quant_kernel": {"flops": 2.0 * n_non * dc * (2 * dff),
-                                   "bytes": 2 * n_non * dff * 2 + n_non * (code_b + meta_b)},
+                                   "bytes": 2 * n_non * dff * 2 + n_non * (b["code"] + b["meta"])},
         "rkv_retrieve_kernel": {"flops": 2.0 * n_non * avg_pool * dkv,
-                                "bytes": n_non * dkv * 2 + n_ref * dkv * 2 + n_non * idx_b},
+                                "bytes": n_non * dkv * 2 + n_ref * dkv * 2 + n_non * b["idx"]},
         # per selected token: its code, extremes and slots in, K and V (2 d_k values) out;
         # once per launch: W_d and the FP8 reference pool
         "rkv_reconstruct_kernel": {"flops": 2.0 * n_sel * dc * dkv,
-                                   "bytes": n_sel * (code_b + meta_b + idx_b + dkv * out_b)
+                                   "bytes": n_sel * (b["code"] + b["meta"] + b["idx"] + b["out"])
                                    + dkv * dc * 2 + n_ref * dkv},
     }
 
 
 # ------------------------------------------------------------------ measured DRAM traffic
 # dram__bytes_read.sum + dram__bytes_write.sum of one launch, from the ncu captures
-# summarised under profiles/ (kernel-case workload, same shapes as the bench).  Reported
-# only while the kernel's code is unchanged since the capture (code_sha1 below).
+# summarised under profiles/ (kernel-case runs of the named workload).  Reported only
+# while the kernel's code is unchanged since the capture (code_sha1 below).
 MEASURED_TRAFFIC = {
-    "rkv_reconstruct_kernel": {"file": "k_reconstruct.cu",
-                               "code_sha1": "f980f1e74b50975f308a34b51c121696924766e4",
-                               "bytes": 10745344 + 168704},
-    "rkv_retrieve_kernel": {"file": "k_retrieve.cu",
-                            "code_sha1": "2fa75553f0dcd7f3432ad5a4cd1c4c4a6af2d412",
-                            "bytes": 134557184 + 3536128},
+    ("llama8b", "rkv_reconstruct_kernel"): {"file": "k_reconstruct.cu",
+                                            "code_sha1": "f980f1e74b50975f308a34b51c121696924766e4",
+                                            "bytes": 10745344 + 168704},
+    ("llama8b", "rkv_retrieve_kernel"): {"file": "k_retrieve.cu",
+                                         "code_sha1": "2fa75553f0dcd7f3432ad5a4cd1c4c4a6af2d412",
+                                         "bytes": 134557184 + 3536128},
 }
 
 
@@ -159,18 +180,60 @@ def code_sha1(path: str) -> str:
     return hashlib.sha1("\n".join(lines).encode()).hexdigest()
 
 
-def measured_traffic(kernel: str):
-    rec = MEASURED_TRAFFIC.get(kernel)
+def measured_traffic(workload: str, kernel: str):
+    rec = MEASURED_TRAFFIC.get((workload, kernel))
     if rec is None:
         return None
-    path = os.path.join(os.path.dirname(os.path.abspath(__file__)), "residual_kv_cache_gb300",
-                        "csrc", rec["file"])
+    path = os.path.join(ROOT, "residual_kv_cache_gb300", "csrc", rec["file"])
     try:
         if code_sha1(path) != rec["code_sha1"]:
             return None
     except OSError:
         return None
     return rec["bytes"]
+
+
+def kernel_rows(ktimes: dict, work_per_step: dict, steps: int, peaks: dict) -> dict:
+    """Per kernel: launches, average launch time, share of all launch time, and the
+    rates its algorithmic work per step implies over its event time per step."""
+    total = sum(ms for _, ms in ktimes.values()) or 1.0
+    rows = {}
+    for k, (n, ms) in ktimes.items():
+        r = {"launches": n, "avg_us": ms / max(n, 1) * 1e3, "share": ms / total}
+        if k in work_per_step and ms > 0:
+            t = ms / steps / 1e3
+            wk = work_per_step[k]
+            r["tflops"] = wk["flops"] / t / 1e12
+            r["gbs"] = wk["bytes"] / t / 1e9
+            r["tc_frac"] = r["tflops"] / peaks["bf16_tflops"]
+            r["tc_frac_sustained"] = r["tflops"] / peaks["bf16_tflops_sustained"]
+            r["hbm_frac"] = r["gbs"] / peaks["hbm_gbs"]
+        rows[k] = {kk: (round(v, 4) if isinstance(v, float) else v) for kk, v in r.items()}
+    return rows
+
+
+def roofline_of(rows: dict, work_per_step: dict, peaks: dict, kind: str, workload: str):
+    """The dominant kernel (largest share of launch time) against its binding roof: the
+    tensor peak if its flops per byte exceed the burst ridge point, else HBM.  Per-launch
+    event times, so the burst bf16 peak; the sustained one is shown beside it."""
+    cands = [k for k in rows if k in work_per_step and "tflops" in rows[k]]
+    if not cands:
+        return None
+    dom = max(cands, key=lambda k: rows[k]["share"])
+    r, wk = rows[dom], work_per_step[dom]
+    ridge = peaks["bf16_tflops"] * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    base = {"kernel": dom, "traffic": measured_traffic(workload, dom),
+            "flops_per_byte": round(wk["flops"] / wk["bytes"], 1), "ridge": round(ridge, 1),
+            "tc_frac": r["tc_frac"], "tc_frac_sustained": r["tc_frac_sustained"],
+            "hbm_frac": r["hbm_frac"]}
+    if wk["flops"] / wk["bytes"] > ridge:
+        return {"bound": "tensor", "achieved": round(r["tflops"], 2), "peak": peaks["bf16_tflops"],
+                "unit": "TFLOP/s", "frac": r["tc_frac"],
+                "peak_sustained": peaks["bf16_tflops_sustained"],
+                "frac_sustained": r["tc_frac_sustained"],
+                "peak_kind": f"{kind} bf16 burst (sustained beside it)", **base}
+    return {"bound": "hbm", "achieved": round(r["gbs"], 1), "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": r["hbm_frac"], "peak_kind": f"{kind} copy", **base}
 
 
 # ------------------------------------------------------------------ clocks
@@ -233,188 +296,510 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(sm)}
 
 
-# ------------------------------------------------------------------ CUDA arm
-def run_cuda(args):
-    import torch
-    import residual_kv_cache_gb300 as rkv
-    from residual_kv_cache_gb300 import build as _build
-    import synth
+# ------------------------------------------------------------------ CUDA arm: workloads
+class Ctx:
+    """What every workload runner needs from the process: device, stream, barrier, the
+    L2 flush buffer and the command-line arguments."""
 
-    rank, world, local = dist_env()
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    _build.build()
+    def __init__(self, args, dev, world, rank):
+        import torch
+        self.args, self.dev, self.world, self.rank = args, dev, world, rank
+        self.stream = torch.cuda.current_stream(dev)
+        self.flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
 
-    w = synth.workload(WORKLOAD)
-    T, n_sel, steps_dec = w.T, w.n_sel, w.steps
-    seed = 1000 * (rank + 1)
-    kv = synth.gen_kv(w, seed).to(dev)
-    W = {k: v.to(dev) for k, v in synth.gen_weights(w, seed + 1).items()}
-    cfg = codec_config(rkv, w, T)
-    codec = rkv.Codec(cfg, W, device=dev)
-    ref_pos = rkv.reference_positions(cfg)
-    ref, non = split_positions(ref_pos, T)
-    zeros_ref, zeros_non = np.zeros_like(ref), np.zeros_like(non)
-    sels = [synth.gen_selection(T, n_sel, seed + 10 + s).to(dev) for s in range(steps_dec)]
-    seq0 = torch.zeros(n_sel, dtype=torch.int32, device=dev)
-    k_out = torch.empty((n_sel, w.n_kv_heads, w.head_dim), dtype=torch.bfloat16, device=dev)
-    v_out = torch.empty_like(k_out)
-    flush = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
-    stream = torch.cuda.current_stream(dev)
-
-    def step():
-        codec.reset()
-        codec.pool_append(kv, zeros_ref, ref, src_rows=ref)
-        codec.compress(kv, zeros_non, non, src_rows=non)
-        for s in range(steps_dec):
-            codec.reconstruct(seq0, sels[s], k_out, v_out)
-
-    def barrier():
-        if world > 1:
+    def barrier(self):
+        import torch
+        if self.world > 1:
             import torch.distributed as dist
             dist.barrier()
-        torch.cuda.synchronize(dev)
+        torch.cuda.synchronize(self.dev)
 
-    clocks = ClockSampler(local)           # started now: nvidia-smi takes a while to start
+    def timed(self, step, steps, warmup, launches):
+        """W untimed steps, then K steps each bracketed by events on the launching stream
+        (L2 flushed and the device idle before each).  Returns the step times in ms and
+        the number of library kernels launched inside the K timed intervals (`launches`
+        reads the libraries' launch counters)."""
+        import torch
+        for _ in range(warmup):
+            step()
+        self.barrier()
+        times, n_launch = [], 0
+        for _ in range(steps):
+            self.flush.fill_(1.0)
+            self.barrier()
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            l0 = launches()
+            e0.record(self.stream)
+            step()
+            e1.record(self.stream)
+            n_launch += launches() - l0
+            self.barrier()
+            times.append(e0.elapsed_time(e1))
+        return times, n_launch
+
+    def kernel_times(self, codecs, step, steps):
+        """The same steps again with an event pair around every launch (launches
+        serialised by the events): per kernel (launches, total ms) summed over codecs."""
+        for c in codecs:
+            c.set_timing(True)
+            c.get_timing(reset=True)
+        for _ in range(steps):
+            self.flush.fill_(1.0)
+            self.barrier()
+            step()
+            self.barrier()
+        out = {}
+        for c in codecs:
+            for k, (n, ms) in c.get_timing(reset=True).items():
+                n0, ms0 = out.get(k, (0, 0.0))
+                out[k] = (n0 + n, ms0 + ms)
+            c.set_timing(False)
+        return out
+
+
+def _status(codecs) -> int:
+    s = 0
+    for c in codecs:
+        s |= c.get_status()
+    return s
+
+
+class StackRun:
+    """Prefill + decode-step workloads over L independent layers of one sequence each
+    (qwen7b: 28 layers; llama8b, long_int2, long_bf16z: one)."""
+
+    def __init__(self, name, ctx, seed):
+        import torch
+        import residual_kv_cache_gb300 as rkv
+        import synth
+        w = synth.workload(name)
+        self.name, self.w, self.ctx = name, w, ctx
+        dev = ctx.dev
+        self.L = w.layers
+        cfg = codec_config(rkv, w, w.T)
+        self.ref, self.non = split_positions(rkv.reference_positions(cfg), w.T)
+        self.ref_pos = rkv.reference_positions(cfg)
+        self.zref, self.znon = np.zeros_like(self.ref), np.zeros_like(self.non)
+        # per layer: its own kv rows and codec weights (seeds per layer); full-size stacks
+        # draw on the device (same distribution, see synth.gen_kv)
+        draw_dev = "cpu" if w.T * w.layers <= 65536 else str(dev)
+        self.kv, self.codecs = [], []
+        for l in range(self.L):
+            s = seed + 97 * l
+            self.kv.append(synth.gen_kv(w, s, device=draw_dev).to(dev))
+            W = {k: v.to(dev) for k, v in synth.gen_weights(w, s + 1).items()}
+            self.codecs.append(rkv.Codec(cfg, W, device=dev))
+        # per decode step and layer: the selected positions
+        self.sels = []
+        for st in range(w.steps):
+            row = []
+            for l in range(self.L):
+                sd = seed + 10 + st + 100003 * l
+                if w.sel_block > 1:
+                    row.append(synth.gen_block_selection(w.T, w.sel_block, w.sel_frac, sd).to(dev))
+                else:
+                    row.append(synth.gen_selection(w.T, w.n_sel, sd).to(dev))
+            self.sels.append(row)
+        self.n_sel = int(self.sels[0][0].numel())
+        self.seq0 = torch.zeros(self.n_sel, dtype=torch.int32, device=dev)
+        odt = torch.float32 if w.out_dtype == "fp32" else torch.bfloat16
+        self.k_out = torch.empty((self.n_sel, w.n_kv_heads, w.head_dim), dtype=odt, device=dev)
+        self.v_out = torch.empty_like(self.k_out)
+        self.tokens_written = self.L * w.T
+        self.tokens_read = w.steps * self.L * self.n_sel
+
+    def write(self, kvs):
+        for c, kv in zip(self.codecs, kvs):
+            c.reset()
+            c.pool_append(kv, self.zref, self.ref, src_rows=self.ref)
+            c.compress(kv, self.znon, self.non, src_rows=self.non)
+
+    def read(self, sels, k_out, v_out):
+        for row in sels:
+            for c, sel in zip(self.codecs, row):
+                c.reconstruct(self.seq0, sel, k_out, v_out)
+
+    def step(self):
+        self.write(self.kv)
+        self.read(self.sels, self.k_out, self.v_out)
+
+    def work_per_step(self) -> dict:
+        w = self.w
+        one = algorithmic_work(w, w.T, self.n_sel, self.ref_pos)
+        out = {}
+        for k, v in one.items():
+            mult = self.L * (w.steps if k == "rkv_reconstruct_kernel" else 1)
+            out[k] = {"flops": v["flops"] * mult, "bytes": v["bytes"] * mult}
+        return out
+
+    def describe(self) -> str:
+        w = self.w
+        shape = {"qwen7b": "Qwen2.5-7B-shaped stack of 28 layers",
+                 "llama8b": "Llama-3.1-8B-shaped layer",
+                 "long_int2": "Llama-3.1-8B-shaped layer, long context",
+                 "long_bf16z": "Llama-3.1-8B-shaped layer, quantisation off"}[self.name]
+        q = "bf16 z" if w.bits == 16 else f"INT{w.bits}"
+        sel = (f"{self.n_sel // w.sel_block} random {w.sel_block}-token blocks"
+               if w.sel_block > 1 else f"{self.n_sel} random tokens")
+        per = " per layer" if self.L > 1 else ""
+        return (f"{self.name}: {shape}, T={w.T}{per}, 2d_k={w.d_kv}, d_c={w.d_c}, d_ff={w.d_ff}, "
+                f"{schedule_note(w)}, {q}; prefill write + {w.steps} decode steps x {sel}{per}")
+
+    def e2e(self):
+        """Public-API path with host buffers: every step uploads its inputs (every layer's
+        kv rows and every selection, from pinned host memory) and reads back the last
+        restore's K and V.  Copies run on a second stream and are double-buffered, so a
+        step's upload overlaps the previous step's compute; all K steps, their uploads and
+        their read-backs lie inside one timed interval."""
+        import torch
+        ctx, w = self.ctx, self.w
+        dev, stream = ctx.dev, ctx.stream
+        kv_host = [kv.cpu().pin_memory() for kv in self.kv]
+        sel_host = torch.stack([torch.stack([s.cpu() for s in row]) for row in self.sels]).pin_memory()
+        kv_buf = [[torch.empty_like(kv) for kv in self.kv] for _ in range(2)]
+        sel_buf = [torch.empty(sel_host.shape, dtype=torch.int32, device=dev) for _ in range(2)]
+        k_dev = [torch.empty_like(self.k_out) for _ in range(2)]
+        v_dev = [torch.empty_like(self.k_out) for _ in range(2)]
+        k_host = torch.empty(self.k_out.shape, dtype=self.k_out.dtype).pin_memory()
+        v_host = torch.empty_like(k_host).pin_memory()
+        copy = torch.cuda.Stream(dev)
+        uploaded = [torch.cuda.Event() for _ in range(2)]
+        inputs_free = [torch.cuda.Event() for _ in range(2)]
+        result_ready = [torch.cuda.Event() for _ in range(2)]
+        result_read = [torch.cuda.Event() for _ in range(2)]
+        for b in range(2):
+            inputs_free[b].record(stream)
+            result_read[b].record(stream)
+
+        def upload(i):
+            b = i % 2
+            with torch.cuda.stream(copy):
+                copy.wait_event(inputs_free[b])
+                for dst, src in zip(kv_buf[b], kv_host):
+                    dst.copy_(src, non_blocking=True)
+                sel_buf[b].copy_(sel_host, non_blocking=True)
+                uploaded[b].record(copy)
+
+        def step(i):
+            b = i % 2
+            stream.wait_event(uploaded[b])
+            stream.wait_event(result_read[b])
+            self.write(kv_buf[b])
+            self.read(sel_buf[b], k_dev[b], v_dev[b])
+            inputs_free[b].record(stream)
+            result_ready[b].record(stream)
+            with torch.cuda.stream(copy):
+                copy.wait_event(result_ready[b])
+                k_host.copy_(k_dev[b], non_blocking=True)
+                v_host.copy_(v_dev[b], non_blocking=True)
+                result_read[b].record(copy)
+
+        def run(n):
+            upload(0)
+            for i in range(n):
+                if i + 1 < n:
+                    upload(i + 1)
+                step(i)
+            torch.cuda.synchronize(dev)
+
+        run(max(1, ctx.args.warmup))
+        ctx.barrier()
+        t0 = time.perf_counter()
+        run(ctx.args.steps)
+        t_step = reduce_max((time.perf_counter() - t0) / ctx.args.steps, ctx.world, dev)
+        tokens = reduce_sum(self.tokens_written + self.tokens_read, ctx.world, dev)
+        h2d = sum(k.numel() * k.element_size() for k in kv_host) + sel_host.numel() * 4
+        d2h = 2 * k_host.numel() * k_host.element_size()
+        return {"value": round(tokens / t_step, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h), "ms_per_step": round(t_step * 1e3, 3),
+                "copies": "in: every layer's kv rows and every selection of the step; out: the "
+                          "K and V of the step's last restore (the other restores' K/V stay on "
+                          "the device, where attention would read them); second stream, "
+                          "double-buffered, so a step's upload overlaps the previous step's "
+                          "compute"}
+
+
+class BatchedRun:
+    """Decode steps over B sequences prefilled to T tokens: per step, one new token per
+    sequence written, then 30 % of each sequence's history restored in one call."""
+
+    def __init__(self, name, ctx, seed):
+        import torch
+        import residual_kv_cache_gb300 as rkv
+        import synth
+        w = synth.workload(name)
+        self.name, self.w, self.ctx = name, w, ctx
+        dev = ctx.dev
+        B, T0 = w.batch, w.T
+        self.B, self.T0 = B, T0
+        self.Tcap = T0 + BATCHED_SLACK
+        cfg = codec_config(rkv, w, self.Tcap, batch=B)
+        self.cfg = cfg
+        self.ref_pos_all = rkv.reference_positions(cfg)
+        self.isref = np.zeros(self.Tcap, dtype=bool)
+        self.isref[self.ref_pos_all] = True
+        W = {k: v.to(dev) for k, v in synth.gen_weights(w, seed + 1).items()}
+        self.codec = rkv.Codec(cfg, W, device=dev)
+        self.kv = [synth.gen_kv(w, seed + 50 + b, T=self.Tcap, device=str(dev)) for b in range(B)]
+        self.new_rows = torch.stack([kv for kv in self.kv], dim=1).contiguous()   # [Tcap, B, d_kv]
+        self.seq_ids = np.arange(B, dtype=np.int32)
+        self.pos = T0                                       # next position to append
+        self.sel_cache = {}
+        self.codecs = [self.codec]
+        odt = torch.float32 if w.out_dtype == "fp32" else torch.bfloat16
+        n_max = B * int(round(w.sel_frac * self.Tcap)) + B
+        self.k_out = torch.empty((n_max, w.n_kv_heads, w.head_dim), dtype=odt, device=dev)
+        self.v_out = torch.empty_like(self.k_out)
+        self.prefill()
+
+    def prefill(self):
+        """Every sequence written up to T0 (not timed)."""
+        self.codec.reset()
+        T0 = self.T0
+        pos = np.arange(T0, dtype=np.int32)
+        ref, non = pos[self.isref[:T0]], pos[~self.isref[:T0]]
+        for b in range(self.B):
+            self.codec.pool_append(self.kv[b], np.full(len(ref), b, np.int32), ref, src_rows=ref)
+            self.codec.compress(self.kv[b], np.full(len(non), b, np.int32), non, src_rows=non)
+        self.pos = T0
+        self.ctx.barrier()
+
+    def selection(self, p):
+        """The restore of the step that appends position p: 30 % of each sequence's
+        history [0, p] at seeded random positions (seq ids, positions)."""
+        import torch
+        import synth
+        if p not in self.sel_cache:
+            n = int(round(self.w.sel_frac * (p + 1)))
+            sels = [synth.gen_selection(p + 1, n, 7919 * p + b) for b in range(self.B)]
+            seq = torch.cat([torch.full((n,), b, dtype=torch.int32) for b in range(self.B)])
+            self.sel_cache[p] = (seq.to(self.ctx.dev), torch.cat(sels).to(self.ctx.dev))
+        return self.sel_cache[p]
+
+    def ensure_room(self, steps):
+        if self.pos + steps > self.Tcap:
+            self.prefill()
+
+    def step_at(self, p, rows, seq, pos, k_out, v_out):
+        pp = np.full(self.B, p, dtype=np.int32)
+        if self.isref[p]:
+            self.codec.pool_append(rows, self.seq_ids, pp)
+        else:
+            self.codec.compress(rows, self.seq_ids, pp)
+        n = seq.numel()
+        self.codec.reconstruct(seq, pos, k_out[:n], v_out[:n])
+
+    def step(self):
+        p = self.pos
+        seq, pos = self.selection(p)
+        self.step_at(p, self.new_rows[p], seq, pos, self.k_out, self.v_out)
+        self.pos += 1
+
+    def prepare(self, steps):
+        self.ensure_room(steps)
+        for p in range(self.pos, self.pos + steps):
+            self.selection(p)
+
+    @property
+    def tokens_per_step(self):
+        return self.B + self.B * int(round(self.w.sel_frac * (self.pos + 1)))
+
+    def work_per_step(self) -> dict:
+        w = self.w
+        n_sel = self.B * int(round(w.sel_frac * self.T0))
+        ref_before = int(np.searchsorted(self.ref_pos_all, self.T0))
+        one = algorithmic_work(w, self.T0, n_sel, self.ref_pos_all[:ref_before], T=self.T0)
+        rec = one["rkv_reconstruct_kernel"]
+        # B sequences' pools behind one restore; one token per sequence written
+        rec = {"flops": rec["flops"], "bytes": rec["bytes"] + (self.B - 1) * ref_before * w.d_kv}
+        return {"rkv_reconstruct_kernel": rec}
+
+    def describe(self) -> str:
+        w = self.w
+        return (f"batched: Llama-3.1-8B layer shape, {self.B} sequences prefilled to {self.T0} "
+                f"tokens, {schedule_note(w)}, INT{w.bits}; one decode step = one new token per "
+                f"sequence written + 30 % of every sequence's history restored in one call")
+
+    def e2e(self):
+        """Public-API decode steps with host buffers: each step uploads its 16 new kv rows
+        and its selection (pinned host memory) and reads back the restored K and V.
+        Copies on a second stream, double-buffered."""
+        import torch
+        ctx, w = self.ctx, self.w
+        dev, stream = ctx.dev, ctx.stream
+        K, W_ = ctx.args.steps, max(1, ctx.args.warmup)
+        self.prepare(K + W_)
+        p0 = self.pos
+        rows_host = self.new_rows[p0:p0 + K + W_].cpu().pin_memory()
+        sels = [self.selection(p) for p in range(p0, p0 + K + W_)]
+        seq_host = [s.cpu().pin_memory() for s, _ in sels]
+        pos_host = [q.cpu().pin_memory() for _, q in sels]
+        n_max = max(s.numel() for s, _ in sels)
+        rows_buf = [torch.empty_like(self.new_rows[0]) for _ in range(2)]
+        seq_buf = [torch.empty(n_max, dtype=torch.int32, device=dev) for _ in range(2)]
+        pos_buf = [torch.empty(n_max, dtype=torch.int32, device=dev) for _ in range(2)]
+        k_dev = [torch.empty_like(self.k_out[:n_max]) for _ in range(2)]
+        v_dev = [torch.empty_like(self.k_out[:n_max]) for _ in range(2)]
+        k_host = torch.empty(k_dev[0].shape, dtype=k_dev[0].dtype).pin_memory()
+        v_host = torch.empty_like(k_host).pin_memory()
+        copy = torch.cuda.Stream(dev)
+        ev = {n: [torch.cuda.Event() for _ in range(2)] for n in ("up", "free", "ready", "read")}
+        for b in range(2):
+            ev["free"][b].record(stream)
+            ev["read"][b].record(stream)
+        h2d = d2h = 0
+
+        def upload(i):
+            nonlocal h2d
+            b = i % 2
+            n = seq_host[i].numel()
+            with torch.cuda.stream(copy):
+                copy.wait_event(ev["free"][b])
+                rows_buf[b].copy_(rows_host[i], non_blocking=True)
+                seq_buf[b][:n].copy_(seq_host[i], non_blocking=True)
+                pos_buf[b][:n].copy_(pos_host[i], non_blocking=True)
+                ev["up"][b].record(copy)
+            h2d += rows_host[i].numel() * rows_host.element_size() + 8 * n
+
+        def step(i):
+            nonlocal d2h
+            b = i % 2
+            n = seq_host[i].numel()
+            stream.wait_event(ev["up"][b])
+            stream.wait_event(ev["read"][b])
+            self.step_at(p0 + i, rows_buf[b], seq_buf[b][:n], pos_buf[b][:n], k_dev[b], v_dev[b])
+            ev["free"][b].record(stream)
+            ev["ready"][b].record(stream)
+            with torch.cuda.stream(copy):
+                copy.wait_event(ev["ready"][b])
+                k_host[:n].copy_(k_dev[b][:n], non_blocking=True)
+                v_host[:n].copy_(v_dev[b][:n], non_blocking=True)
+                ev["read"][b].record(copy)
+            d2h += 2 * n * k_host[0].numel() * k_host.element_size()
+
+        def run(first, n):
+            upload(first)
+            for i in range(first, first + n):
+                if i + 1 < first + n:
+                    upload(i + 1)
+                step(i)
+            torch.cuda.synchronize(dev)
+
+        run(0, W_)
+        ctx.barrier()
+        h2d = d2h = 0
+        t0 = time.perf_counter()
+        run(W_, K)
+        t_step = reduce_max((time.perf_counter() - t0) / K, ctx.world, dev)
+        self.pos = p0 + K + W_
+        tokens = sum(self.B + seq_host[i].numel() for i in range(W_, W_ + K)) / K
+        tokens = reduce_sum(tokens, ctx.world, dev)
+        return {"value": round(tokens / t_step, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d / K),
+                "d2h_bytes_per_step": int(d2h / K), "ms_per_step": round(t_step * 1e3, 3),
+                "copies": "in: the step's new kv rows and its selection; out: every restored K "
+                          "and V row of the step; second stream, double-buffered"}
+
+
+def run_workload(name, ctx, seed, with_e2e=True, with_cpu=True):
+    """Measure one workload: device-timed steps, per-kernel event times, roofline of the
+    dominant kernel, storage, end to end, and the oracle baseline."""
+    import torch
+    args = ctx.args
+    peaks, kind = load_peaks()
+    run = BatchedRun(name, ctx, seed) if name == "batched" else StackRun(name, ctx, seed)
+    codecs = run.codecs
+    clocks = ClockSampler(ctx.dev.index or 0)
     clocks.start()
-    for _ in range(args.warmup):
-        step()
-    barrier()
-    if codec.get_status() != 0:
-        raise RuntimeError("device status flags set during warm-up")
-
-    # ---- timed region (device time, CUDA events on the launching stream only at the
-    # step boundaries, so consecutive launches are free to overlap)
-    launches0 = codec.launch_count()
+    if name == "batched":
+        run.prepare(args.warmup + 2 * args.steps)
+    run.step()                                     # first touch (outside every timing)
+    ctx.barrier()
+    if _status(codecs) != 0:
+        raise RuntimeError(f"{name}: device status flags set")
+    count = lambda: sum(c.launch_count() for c in codecs)   # noqa: E731
     clocks.mark_begin()
-    times = []
-    for _ in range(args.steps):
-        flush.fill_(1.0)                       # L2 flush, outside the timed interval
-        barrier()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        step()
-        e1.record(stream)
-        barrier()
-        times.append(e0.elapsed_time(e1))
+    t_tok0 = time.perf_counter()
+    if name == "batched":
+        tokens = []
+
+        def step():
+            tokens.append(run.tokens_per_step)
+            run.step()
+        times, launches_timed = ctx.timed(step, args.steps, args.warmup, count)
+        tokens = tokens[args.warmup:]
+        tok_step = float(np.mean(tokens))
+    else:
+        times, launches_timed = ctx.timed(run.step, args.steps, args.warmup, count)
+        tok_step = run.tokens_written + run.tokens_read
     clocks.mark_end()
     clk = clocks.stop()
-    launches = codec.launch_count() - launches0
-    status = codec.get_status()
-
-    # ---- per-kernel times: the same steps again with an event pair around every launch
-    # (launches serialised by the events; used for the roofline and the kernel table)
-    codec.set_timing(True)
-    codec.get_timing(reset=True)
-    for _ in range(args.steps):
-        flush.fill_(1.0)
-        barrier()
-        step()
-        barrier()
-    ktimes = codec.get_timing(reset=True)
-    codec.set_timing(False)
-    status |= codec.get_status()
-
-    # ---- sparse-layer attention over each decode step's restored rows (not part of the
-    # step above): 32 query heads of the Llama-3.1-8B layer on its 8 key/value heads
-    attn = measure_attention(codec, sels, seq0, k_out, v_out, w, dev, args.steps, flush, barrier)
-    status |= codec.get_status()
-
-    t_step_ms = reduce_max(sum(times) / len(times), world, dev)
-    tokens_step = T + steps_dec * n_sel
-    value = reduce_sum(tokens_step, world, dev) / (t_step_ms / 1e3)
-
-    # split into write and read rates from the kernels' own event times
-    per_k = {k: (n, ms) for k, (n, ms) in ktimes.items()}
-    write_ms = sum(ms for k, (n, ms) in per_k.items() if k != "rkv_reconstruct_kernel") / args.steps
-    read_ms = per_k.get("rkv_reconstruct_kernel", (1, 0.0))[1] / args.steps
-
-    # ---- roofline of the dominant kernel
-    peaks, peaks_kind = load_peaks()
-    work = algorithmic_work(w, T, n_sel, ref_pos)
-    rows = {}
-    for k, (n, ms) in per_k.items():
-        if k not in work or n == 0:
-            continue
-        avg_s = ms / n / 1e3
-        wk = work[k]
-        tc = wk["flops"] / avg_s / 1e12
-        bw = wk["bytes"] / avg_s / 1e9
-        tc_frac = tc / peaks["bf16_tflops_sustained"]
-        bw_frac = bw / peaks["hbm_gbs"]
-        rows[k] = {"avg_us": avg_s * 1e6, "launches": n, "share": ms / sum(m for _, m in per_k.values()),
-                   "tflops": tc, "gbs": bw, "tc_frac": tc_frac, "hbm_frac": bw_frac}
-    dom = max(rows, key=lambda k: rows[k]["share"]) if rows else None
-    roofline = None
-    if dom:
-        r = rows[dom]
-        bound = "tensor" if work[dom]["flops"] / work[dom]["bytes"] > (
-            peaks["bf16_tflops_sustained"] * 1e12) / (peaks["hbm_gbs"] * 1e9) else "hbm"
-        if bound == "tensor":
-            roofline = {"bound": "tensor", "kernel": dom, "achieved": round(r["tflops"], 2),
-                        "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                        "frac": round(r["tc_frac"], 4), "traffic": measured_traffic(dom),
-                        "peak_kind": f"{peaks_kind} bf16 sustained"}
-        else:
-            roofline = {"bound": "hbm", "kernel": dom, "achieved": round(r["gbs"], 1),
-                        "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": round(r["hbm_frac"], 4),
-                        "traffic": measured_traffic(dom), "peak_kind": f"{peaks_kind} copy"}
-
-    # ---- end-to-end through the public API with host buffers
-    e2e = run_e2e(args, codec, kv, sels, w, dev, stream, barrier, world, ref, non)
-
-    out = {
-        "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(t_step_ms, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic",
-        "config": step_config(w, world),
-        "compress_tok_s": round(T / (write_ms / 1e3), 1) if write_ms else None,
-        "reconstruct_tok_s": round(steps_dec * n_sel / (read_ms / 1e3), 1) if read_ms else None,
-        "roofline": roofline,
-        "kernels": {k: {kk: round(vv, 4) for kk, vv in v.items()} for k, v in rows.items()},
-        "e2e": e2e,
-        "sparse_attention": attn,
-        "storage": storage_report(codec, w),
-        "gpu_launches": int(launches),
-        "clocks": clk,
-        "device_status": int(status),
-    }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = cpu_baseline(args.cpu_seconds)
-    if rank == 0:
-        print(json.dumps(out), flush=True)
-    if world > 1:
-        import torch.distributed as dist
-        dist.destroy_process_group()
+    wall = time.perf_counter() - t_tok0
+    if name == "batched":
+        run.prepare(args.steps)
+    ktimes = ctx.kernel_times(codecs, run.step, args.steps)
+    status = _status(codecs)
+    t_ms = reduce_max(sum(times) / len(times), ctx.world, ctx.dev)
+    value = reduce_sum(tok_step, ctx.world, ctx.dev) / (t_ms / 1e3)
+    work = run.work_per_step()
+    rows = kernel_rows(ktimes, work, args.steps, peaks)
+    roof = roofline_of(rows, work, peaks, kind, name)
+    read_ms = ktimes.get("rkv_reconstruct_kernel", (0, 0.0))[1] / args.steps
+    write_ms = sum(ms for k, (n, ms) in ktimes.items() if k != "rkv_reconstruct_kernel") / args.steps
+    out = {"workload": name, "value": round(value, 1), "unit": UNIT, "ms_per_step": round(t_ms, 4),
+           "config": step_config(run, ctx.world), "roofline": roof,
+           "kernels": rows, "gpu_launches": int(launches_timed), "clocks": clk,
+           "device_status": int(status), "timed_region_s": round(wall, 3)}
+    if name == "batched":
+        lat = sorted(times)
+        out["latency_ms"] = {"p50": round(float(np.percentile(lat, 50)), 4),
+                             "p99": round(float(np.percentile(lat, 99)), 4),
+                             "max": round(lat[-1], 4), "steps": len(lat)}
+        out["reconstruct_tok_s"] = round((tok_step - run.B) / (read_ms / 1e3), 1) if read_ms else None
+        out["write_us_per_step"] = round(write_ms * 1e3, 2)
+        out["compress_tok_s"] = round(run.B / (write_ms / 1e3), 1) if write_ms else None
+    else:
+        out["compress_tok_s"] = round(run.tokens_written / (write_ms / 1e3), 1) if write_ms else None
+        out["reconstruct_tok_s"] = round(run.tokens_read / (read_ms / 1e3), 1) if read_ms else None
+    out["storage"] = storage_report(codecs[0], run.w)
+    if with_e2e:
+        out["e2e"] = run.e2e()
+        status |= _status(codecs)
+        out["device_status"] = int(status)
+    if name == "llama8b":
+        out["sparse_attention"] = measure_attention(run, ctx)
+    if with_cpu and ctx.rank == 0 and ctx.world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = cpu_baseline(name, args.cpu_seconds)
+    for c in codecs:
+        c.free()
+    del run
+    torch.cuda.empty_cache()
+    return out
 
 
-def measure_attention(codec, sels, seq0, k_out, v_out, w, dev, steps, flush, barrier):
+def measure_attention(run, ctx):
     """Time rkv_sparse_attention after each decode step's restore (event pairs around
-    its two launches).  Bytes: the K and V rows it reads, q in, o out."""
+    its launches).  Bytes: the K and V rows it reads, q in, o out."""
     import torch
+    w, codec = run.w, run.codecs[0]
     hq = 4 * w.n_kv_heads
     g = torch.Generator().manual_seed(4242)
-    q = torch.randn(hq, w.head_dim, generator=g).to(dev)
-    out = torch.empty(hq, w.head_dim, dtype=torch.float32, device=dev)
+    q = torch.randn(hq, w.head_dim, generator=g).to(ctx.dev)
+    out = torch.empty(hq, w.head_dim, dtype=torch.float32, device=ctx.dev)
     codec.set_timing(True)
     codec.get_timing(reset=True)
-    for _ in range(steps):
-        flush.fill_(1.0)
-        barrier()
-        for s in range(len(sels)):
-            codec.reconstruct(seq0, sels[s], k_out, v_out)
-            codec.sparse_attention(q, k_out, v_out, out)
-        barrier()
+    for _ in range(ctx.args.steps):
+        ctx.flush.fill_(1.0)
+        ctx.barrier()
+        for row in run.sels:
+            codec.reconstruct(run.seq0, row[0], run.k_out, run.v_out)
+            codec.sparse_attention(q, run.k_out, run.v_out, out)
+        ctx.barrier()
     t = codec.get_timing(reset=True)
     codec.set_timing(False)
     calls, ms = t["rkv_attention_kernel"]
     us = ms / calls * 1e3
-    n = w.n_sel
+    n = run.n_sel
     kv_bytes = 2 * n * w.n_kv_heads * w.head_dim * 2
     peaks, kind = load_peaks()
     gbs = (kv_bytes + 2 * hq * w.head_dim * 4) / (us * 1e-6) / 1e9
@@ -422,140 +807,6 @@ def measure_attention(codec, sels, seq0, k_out, v_out, w, dev, steps, flush, bar
             "gbs": round(gbs, 1), "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
             "peak_kind": f"{kind} copy",
             "note": "K/V read right after their restore (L2-resident); o is fp32"}
-
-
-def run_e2e(args, codec, kv_dev, sels_dev, w, dev, stream, barrier, world, ref, non):
-    """Public-API path with host buffers: every step uploads its inputs (kv rows and
-    selections, from pinned host memory) and reads its result (the last restore's K and
-    V) back to the host.  Copies run on a second stream and are double-buffered, so a
-    step's upload overlaps the previous step's compute; all K steps, their uploads and
-    their read-backs lie inside one timed interval."""
-    import torch
-    T, n_sel = w.T, w.n_sel
-    kv_host = kv_dev.cpu().pin_memory()
-    sel_host = torch.stack([s.cpu() for s in sels_dev]).pin_memory()
-    kv_buf = [torch.empty_like(kv_dev) for _ in range(2)]
-    sel_buf = [torch.empty(sel_host.shape, dtype=torch.int32, device=dev) for _ in range(2)]
-    k_dev = [torch.empty((n_sel, w.n_kv_heads, w.head_dim), dtype=torch.bfloat16, device=dev)
-             for _ in range(2)]
-    v_dev = [torch.empty_like(k_dev[0]) for _ in range(2)]
-    k_host = torch.empty((n_sel, w.n_kv_heads, w.head_dim), dtype=torch.bfloat16).pin_memory()
-    v_host = torch.empty_like(k_host).pin_memory()
-    seq0 = torch.zeros(n_sel, dtype=torch.int32, device=dev)
-    copy = torch.cuda.Stream(dev)
-    uploaded = [torch.cuda.Event() for _ in range(2)]
-    inputs_free = [torch.cuda.Event() for _ in range(2)]
-    result_ready = [torch.cuda.Event() for _ in range(2)]
-    result_read = [torch.cuda.Event() for _ in range(2)]
-    for b in range(2):                                  # every buffer starts free
-        inputs_free[b].record(stream)
-        result_read[b].record(stream)
-
-    def upload(i):
-        b = i % 2
-        with torch.cuda.stream(copy):
-            copy.wait_event(inputs_free[b])
-            kv_buf[b].copy_(kv_host, non_blocking=True)
-            sel_buf[b].copy_(sel_host, non_blocking=True)
-            uploaded[b].record(copy)
-
-    def step(i):
-        b = i % 2
-        stream.wait_event(uploaded[b])
-        stream.wait_event(result_read[b])
-        codec.reset()
-        codec.pool_append(kv_buf[b], np.zeros_like(ref), ref, src_rows=ref)
-        codec.compress(kv_buf[b], np.zeros_like(non), non, src_rows=non)
-        for s in range(sel_buf[b].shape[0]):
-            codec.reconstruct(seq0, sel_buf[b][s], k_dev[b], v_dev[b])
-        inputs_free[b].record(stream)
-        result_ready[b].record(stream)
-        with torch.cuda.stream(copy):
-            copy.wait_event(result_ready[b])
-            k_host.copy_(k_dev[b], non_blocking=True)
-            v_host.copy_(v_dev[b], non_blocking=True)
-            result_read[b].record(copy)
-
-    def run(n):
-        upload(0)
-        for i in range(n):
-            if i + 1 < n:
-                upload(i + 1)
-            step(i)
-        torch.cuda.synchronize(dev)
-
-    run(max(1, args.warmup))
-    barrier()
-    t0 = time.perf_counter()
-    run(args.steps)
-    t_step = reduce_max((time.perf_counter() - t0) / args.steps, world, dev)
-    tokens = reduce_sum(T + sel_host.shape[0] * n_sel, world, dev)
-    h2d = kv_host.numel() * kv_host.element_size() + sel_host.numel() * 4
-    d2h = 2 * k_host.numel() * k_host.element_size()
-    return {"value": round(tokens / t_step, 1), "unit": UNIT, "h2d_bytes_per_step": int(h2d),
-            "d2h_bytes_per_step": int(d2h), "ms_per_step": round(t_step * 1e3, 3),
-            "copies": "second stream, double-buffered: a step's upload overlaps the previous "
-                      "step's compute"}
-
-
-# ------------------------------------------------------------------ oracle timing
-def cpu_baseline(budget_s: float = 15.0) -> dict:
-    """Time the CPU oracle (as it stands) on a bounded sample of the workload and
-    scale to the step's token mix."""
-    import torch
-    import synth
-    from oracle import codec as C
-
-    cores = len(os.sched_getaffinity(0))
-    w = synth.workload(WORKLOAD)
-    kv = synth.gen_kv(w, 1000).to(torch.float64).numpy()
-    W = {k: v.to(torch.float64).numpy() for k, v in synth.gen_weights(w, 1001).items()}
-    sh = C.Shape(w.n_kv_heads, w.head_dim, w.d_c, w.d_ff, w.topk, w.group, w.bits, w.stride,
-                 w.rope_base, SCHEDULE["alpha"], SCHEDULE["sink"])
-    t0 = time.perf_counter()
-    pool = C.build_pool(kv, w.T, w.stride, sh.ref_alpha, sh.ref_sink)
-    t_pool = time.perf_counter() - t0
-    rng = np.random.default_rng(0)
-    nonref = np.nonzero(~C.is_reference(np.arange(w.T), w.stride, sh.ref_alpha, sh.ref_sink))[0]
-    # compress sample: batches of 64 tokens until half the budget is used
-    n_c, t_c = 0, 0.0
-    enc_q, enc_meta, enc_idx, enc_pos = [], [], [], []
-    while t_c < budget_s / 2 and n_c < 4096:
-        p = np.sort(rng.choice(nonref, 64, replace=False))
-        t0 = time.perf_counter()
-        e = C.encode_tokens(kv[p], p, pool, W, sh, "operand")
-        t_c += time.perf_counter() - t0
-        n_c += len(p)
-        enc_q.append(e["q"]); enc_meta.append(e["meta"]); enc_idx.append(e["idx"]); enc_pos.append(p)
-    # reconstruct sample over the encoded tokens
-    q = np.concatenate(enc_q); meta = np.concatenate(enc_meta); idx = np.concatenate(enc_idx)
-    pos = np.concatenate(enc_pos)
-    n_r, t_r = 0, 0.0
-    while t_r < budget_s / 2 and n_r < 65536:
-        t0 = time.perf_counter()
-        zt = C.dequantize(q, meta, sh.bits, sh.group)
-        means = np.stack([C.reference_mean(pool.vals, i[i >= 0]) for i in idx])
-        kvh = C.decode(zt, W["Wd"], means)
-        K, V = C.split_kv(kvh, sh.n_kv_heads, sh.head_dim)
-        C.rope(K, pos, sh.rope_base)
-        t_r += time.perf_counter() - t0
-        n_r += len(pos)
-    per_c = (t_c + t_pool * n_c / w.T) / n_c
-    per_r = t_r / n_r
-    tokens = w.T + w.steps * w.n_sel
-    t_step = per_c * w.T + per_r * w.steps * w.n_sel
-    return {"value": round(tokens / t_step, 2), "unit": UNIT, "cores": cores, "kind": "oracle",
-            "sample": f"{n_c} compressed tokens (random non-reference positions, full "
-                      f"{len(pool.pos)}-reference pool, {schedule_note(w)}) and {n_r} restored "
-                      f"tokens of the {WORKLOAD} workload, scaled to the "
-                      f"step mix ({w.T} written + {w.steps}x{w.n_sel} restored)",
-            "compress_tok_s": round(1 / per_c, 2), "reconstruct_tok_s": round(1 / per_r, 2),
-            "seconds": round(t_c + t_r + t_pool, 2)}
-
-
-def _workload():
-    import synth
-    return synth.workload(WORKLOAD)
 
 
 def storage_report(codec, w) -> dict:
@@ -572,33 +823,157 @@ def storage_report(codec, w) -> dict:
             "fraction_without_pool_shadow": round((total - nbytes["pool_bf16"]) / tokens / fp16, 4)}
 
 
-def step_config(w, world: int) -> dict:
+def step_config(run, world: int) -> dict:
     """The workload of one step, the same on both arms of the comparison."""
-    return {"workload": f"{WORKLOAD}: Llama-3.1-8B-shaped layer, T={w.T}, 2d_k={w.d_kv}, "
-                        f"d_c={w.d_c}, d_ff={w.d_ff}, {schedule_note(w)}, INT{w.bits}, "
-                        f"prefill write + {w.steps} decode steps x {w.n_sel} restored",
-            "tokens_per_step": w.T + w.steps * w.n_sel, "l2": "flushed before every timed step",
+    if isinstance(run, BatchedRun):
+        tok = run.B + run.B * int(round(run.w.sel_frac * run.T0))
+    else:
+        tok = run.tokens_written + run.tokens_read
+    return {"workload": run.describe(), "tokens_per_step": tok,
+            "l2": "flushed before every timed step",
             "parallelism": f"replicas x{world} (independent sequences)"}
+
+
+# ------------------------------------------------------------------ CUDA arm: the line
+def run_cuda(args):
+    import torch
+    from residual_kv_cache_gb300 import build as _build
+
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    _build.build()
+    ctx = Ctx(args, dev, world, rank)
+    names = [args.workload] if args.workload else list(WORKLOAD_ORDER)
+    seed = 1000 * (rank + 1)
+    results = {}
+    for i, name in enumerate(names):
+        results[name] = run_workload(name, ctx, seed + 100 * i)
+    head = results[names[0]]
+    out = {"metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world,
+           "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+           "data": "synthetic", "config": head["config"],
+           "compress_tok_s": head.get("compress_tok_s"),
+           "reconstruct_tok_s": head.get("reconstruct_tok_s"),
+           "roofline": head["roofline"], "kernels": head["kernels"], "e2e": head.get("e2e"),
+           "storage": head["storage"], "gpu_launches": head["gpu_launches"],
+           "clocks": head["clocks"], "device_status": head["device_status"]}
+    if "cpu_baseline" in head:
+        out["cpu_baseline"] = head["cpu_baseline"]
+    if len(names) > 1:
+        out["configs"] = {n: results[n] for n in names[1:]}
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+# ------------------------------------------------------------------ oracle timing
+_CPU_INPUTS = {}          # the last workload's sample inputs, drawn once per process
+
+
+def cpu_baseline(name: str, budget_s: float = 16.0) -> dict:
+    """Time the CPU oracle (as it stands) on a bounded sample of one layer of the
+    workload, per token, and scale to the step's token mix."""
+    import torch
+    import synth
+    from oracle import codec as C
+
+    cores = len(os.sched_getaffinity(0))
+    w = synth.workload(name)
+    T = min(w.T, (1 << 27) // w.d_kv)      # the sample's sequence (pool) length
+    if name not in _CPU_INPUTS:
+        kv = synth.gen_kv(w, 1000, T=T).to(torch.float64).numpy()
+        W = {k: v.to(torch.float64).numpy() for k, v in synth.gen_weights(w, 1001).items()}
+        _CPU_INPUTS.clear()
+        _CPU_INPUTS[name] = (kv, W)
+    kv, W = _CPU_INPUTS[name]
+    sh = C.Shape(w.n_kv_heads, w.head_dim, w.d_c, w.d_ff, w.topk, w.group, w.bits, w.stride,
+                 w.rope_base, SCHEDULE["alpha"], SCHEDULE["sink"])
+    t0 = time.perf_counter()
+    pool = C.build_pool(kv, T, w.stride, sh.ref_alpha, sh.ref_sink)
+    t_pool = time.perf_counter() - t0
+    rng = np.random.default_rng(0)
+    nonref = np.nonzero(~C.is_reference(np.arange(T), w.stride, sh.ref_alpha, sh.ref_sink))[0]
+    # compress sample: batches of 64 tokens until half the budget is used
+    n_c, t_c = 0, 0.0
+    enc_q, enc_meta, enc_idx, enc_pos = [], [], [], []
+    while t_c < budget_s / 2 and n_c < 4096:
+        p = np.sort(rng.choice(nonref, 64, replace=False))
+        t0 = time.perf_counter()
+        e = C.encode_tokens(kv[p], p, pool, W, sh, "operand")
+        t_c += time.perf_counter() - t0
+        n_c += len(p)
+        enc_q.append(e["q"]); enc_meta.append(e["meta"]); enc_idx.append(e["idx"]); enc_pos.append(p)
+    q = np.concatenate(enc_q); meta = np.concatenate(enc_meta); idx = np.concatenate(enc_idx)
+    pos = np.concatenate(enc_pos)
+    n_r, t_r = 0, 0.0
+    while t_r < budget_s / 2 and n_r < 65536:
+        t0 = time.perf_counter()
+        zt = C.dequantize(q, meta, sh.bits, sh.group)
+        means = np.stack([C.reference_mean(pool.vals, i[i >= 0]) for i in idx])
+        kvh = C.decode(zt, W["Wd"], means)
+        K, V = C.split_kv(kvh, sh.n_kv_heads, sh.head_dim)
+        C.rope(K, pos, sh.rope_base)
+        t_r += time.perf_counter() - t0
+        n_r += len(pos)
+    per_c = (t_c + t_pool * n_c / T) / n_c
+    per_r = t_r / n_r
+    if name == "batched":
+        n_read = w.batch * int(round(w.sel_frac * w.T))
+        written, read = w.batch, n_read
+    else:
+        n_sel = w.n_sel
+        written, read = w.layers * w.T, w.steps * w.layers * n_sel
+    t_step = per_c * written + per_r * read
+    short = "" if T == w.T else f" (a {T}-token sequence: its pool has {len(pool.pos)} references)"
+    return {"value": round((written + read) / t_step, 2), "unit": UNIT, "cores": cores,
+            "kind": "oracle",
+            "sample": f"{n_c} compressed tokens (random non-reference positions of one layer{short}, "
+                      f"{schedule_note(w)}) and {n_r} restored tokens of the {name} workload, "
+                      f"per token, scaled to the step mix ({written} written + {read} restored)",
+            "compress_tok_s": round(1 / per_c, 2), "reconstruct_tok_s": round(1 / per_r, 2),
+            "seconds": round(t_c + t_r + t_pool, 2)}
 
 
 def run_reference(args):
     rank, world, local = dist_env()
     if rank != 0:
         return
+    name = args.workload or HEADLINE
     vals, last = [], None
     for _ in range(args.warmup):
-        cpu_baseline(args.cpu_seconds / 4)
+        cpu_baseline(name, args.cpu_seconds / 4)
     for _ in range(args.steps):
-        last = cpu_baseline(args.cpu_seconds)
+        last = cpu_baseline(name, args.cpu_seconds)
         vals.append(last["value"])
     v = statistics.mean(vals)
-    w = _workload()
-    tokens = w.T + w.steps * w.n_sel
+    import synth
+    w = synth.workload(name)
+    if name == "batched":
+        tokens = w.batch + w.batch * int(round(w.sel_frac * w.T))
+        desc = (f"batched: Llama-3.1-8B layer shape, {w.batch} sequences prefilled to {w.T} "
+                f"tokens, {schedule_note(w)}, INT{w.bits}; one decode step = one new token per "
+                f"sequence written + 30 % of every sequence's history restored in one call")
+    else:
+        n_sel = (int(round(w.sel_frac * (w.T // w.sel_block))) * w.sel_block
+                 if w.sel_block > 1 else w.n_sel)
+        tokens = w.layers * w.T + w.steps * w.layers * n_sel
+        desc = None
+    cfg = {"workload": desc or _stack_description(name), "tokens_per_step": tokens,
+           "l2": "flushed before every timed step",
+           "parallelism": "replicas x1 (independent sequences)"}
     out = {"metric": METRIC, "value": round(v, 2), "unit": UNIT, "n_gpus": world,
            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(tokens / v * 1e3, 1),
+           "ms_per_step_kind": "extrapolated: each step times a bounded sample of the workload "
+                               "and scales its per-token times to the step's token mix",
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-           "data": "synthetic", "impl": "reference",
-           "config": step_config(w, 1),
+           "data": "synthetic", "impl": "reference", "config": cfg,
            "cpu_baseline": {"value": round(v, 2), "unit": UNIT, "cores": last["cores"],
                             "kind": "oracle", "sample": last["sample"]},
            "e2e": {"value": round(v, 2), "unit": UNIT, "h2d_bytes_per_step": 0,
@@ -606,36 +981,54 @@ def run_reference(args):
     print(json.dumps(out), flush=True)
 
 
+def _stack_description(name: str) -> str:
+    """The description a StackRun gives, without a GPU."""
+    import synth
+    w = synth.workload(name)
+
+    class _R(StackRun):
+        def __init__(self):
+            self.name, self.w, self.L = name, w, w.layers
+            self.n_sel = (int(round(w.sel_frac * (w.T // w.sel_block))) * w.sel_block
+                          if w.sel_block > 1 else w.n_sel)
+    return _R().describe()
+
+
 def run_kernel_case(args):
-    """Minimal case for kernel captures under ncu: one prefill write and two decode-step
-    restores of the workload, each followed by the sparse attention over its rows (no
-    timing, no CPU work)."""
+    """Minimal case for kernel captures under ncu: one layer of the workload, one
+    prefill write and two decode-step restores, each followed by the sparse attention
+    over its rows (no timing, no CPU work)."""
     import torch
     import residual_kv_cache_gb300 as rkv
     from residual_kv_cache_gb300 import build as _build
     import synth
 
     _build.build()
-    w = synth.workload(WORKLOAD)
+    name = args.workload or HEADLINE
+    w = synth.workload(name)
     if args.tokens:
-        w = synth.workload(WORKLOAD, T=args.tokens)
+        w = synth.workload(name, T=args.tokens)
     dev = torch.device("cuda", 0)
-    kv = synth.gen_kv(w, 1000).to(dev)
+    kv = synth.gen_kv(w, 1000, device=str(dev) if w.T > 65536 else "cpu").to(dev)
     W = {k: v.to(dev) for k, v in synth.gen_weights(w, 1001).items()}
     cfg = codec_config(rkv, w, w.T)
     codec = rkv.Codec(cfg, W, device=dev)
     ref, non = split_positions(rkv.reference_positions(cfg), w.T)
     codec.pool_append(kv, np.zeros_like(ref), ref, src_rows=ref)
     codec.compress(kv, np.zeros_like(non), non, src_rows=non)
-    zero = torch.zeros(w.n_sel, dtype=torch.int32, device=dev)
     g = torch.Generator().manual_seed(4242)
     q = torch.randn(4 * w.n_kv_heads, w.head_dim, generator=g).to(dev)
     for s in range(2):
-        K, V = codec.reconstruct(zero, synth.gen_selection(w.T, w.n_sel, 1010 + s).to(dev))
+        if w.sel_block > 1:
+            sel = synth.gen_block_selection(w.T, w.sel_block, w.sel_frac, 1010 + s).to(dev)
+        else:
+            sel = synth.gen_selection(w.T, w.n_sel, 1010 + s).to(dev)
+        zero = torch.zeros(sel.numel(), dtype=torch.int32, device=dev)
+        K, V = codec.reconstruct(zero, sel)
         codec.sparse_attention(q, K, V)             # the sparse layer's attention over them
     torch.cuda.synchronize()
     flags = codec.get_status()
-    print(json.dumps({"kernel_case": WORKLOAD, "T": w.T, "launches": codec.launch_count(),
+    print(json.dumps({"kernel_case": name, "T": w.T, "launches": codec.launch_count(),
                       "status": flags}))
     if flags:
         sys.exit(1)
@@ -644,20 +1037,24 @@ def run_kernel_case(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="cuda", choices=["cuda", "reference"])
+    ap.add_argument("--workload", default=None, choices=list(WORKLOAD_ORDER),
+                    help="measure one workload only (default: all, headline first)")
     ap.add_argument("--alpha", type=float, default=0.0,
                     help="dynamic-stride growth of the reference schedule (0: fixed stride)")
     ap.add_argument("--sink", type=int, default=0, help="sink tokens of the reference schedule")
-    ap.add_argument("--cpu-seconds", type=float, default=16.0)
+    ap.add_argument("--cpu-seconds", type=float, default=8.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--kernel-case", action="store_true",
-                    help="run one prefill and two restores, for kernel captures")
+                    help="run one layer's prefill and two restores, for kernel captures")
     ap.add_argument("--tokens", type=int, default=0, help="override T for --kernel-case")
     args = ap.parse_args()
     if args.alpha < 0 or args.sink < 0:
         ap.error("--alpha and --sink must be >= 0")
+    if args.steps < 1 or args.warmup < 0:
+        ap.error("--steps must be >= 1 and --warmup >= 0")
     SCHEDULE.update(alpha=float(args.alpha), sink=int(args.sink))
     if args.kernel_case:
         run_kernel_case(args)

@@ -102,18 +102,22 @@ def _gen(seed: int) -> torch.Generator:
     return g
 
 
-def gen_kv(w: Workload, seed: int, T: int | None = None) -> torch.Tensor:
+def gen_kv(w: Workload, seed: int, T: int | None = None, device: str = "cpu") -> torch.Tensor:
     """[T, 2d_k] pre-RoPE joint K/V rows: centroid[c_i] + noise * N(0, 1).
 
     Centroids ~ N(0, 1), c_i uniform.  For the Llama/Qwen-shaped workloads the
-    whole tensor is then scaled to unit RMS.  Returned on the CPU in the
-    workload's kv dtype.
+    whole tensor is then scaled to unit RMS.  Returned in the workload's kv dtype.
+    On the CPU (the default) every machine draws the same values; with a CUDA
+    `device` the draws come from that device's generator, seeded the same way: the
+    same distribution, other values (for timing runs of full-size stacks, where
+    drawing gigabytes on the host would take minutes).
     """
     T = w.T if T is None else T
-    g = _gen(seed)
-    cent = torch.randn(w.n_centroids, w.d_kv, generator=g, dtype=torch.float32)
-    c = torch.randint(0, w.n_centroids, (T,), generator=g)
-    kv = cent[c] + w.noise * torch.randn(T, w.d_kv, generator=g, dtype=torch.float32)
+    g = torch.Generator(device=device)
+    g.manual_seed(int(seed))
+    cent = torch.randn(w.n_centroids, w.d_kv, generator=g, dtype=torch.float32, device=device)
+    c = torch.randint(0, w.n_centroids, (T,), generator=g, device=device)
+    kv = cent[c] + w.noise * torch.randn(T, w.d_kv, generator=g, dtype=torch.float32, device=device)
     if w.unit_rms:
         kv = kv / kv.pow(2).mean().sqrt()
     return kv.to(torch.float32 if w.kv_dtype == "fp32" else torch.bfloat16)

@@ -64,11 +64,48 @@ def test_clock_record_keeps_only_the_timed_window():
     assert rec["reasons"] == ["sw_power_cap"]          # the hw_slowdown sample lies outside
 
 
-def test_step_config_names_the_bench_workload():
-    w = synth.workload("llama8b")
-    cfg = bench.step_config(w, 1)
-    assert cfg["tokens_per_step"] == w.T + w.steps * w.n_sel == 32768 + 64 * 9830
+def test_step_config_names_the_bench_workloads():
+    """Token counts per step: the qwen7b stack (28 layers x 131072 written, 64 steps x 28
+    layers x 614 blocks of 64 restored) and the llama8b layer."""
+    w = synth.workload("qwen7b")
+    assert bench._stack_description("qwen7b").startswith("qwen7b: Qwen2.5-7B-shaped stack of 28")
+    sel = synth.gen_block_selection(w.T, w.sel_block, w.sel_frac, 1)
+    assert sel.numel() == 614 * 64
+
+    class _Run(bench.StackRun):
+        def __init__(self, name, n_sel):
+            self.name, self.w = name, synth.workload(name)
+            self.L, self.n_sel = self.w.layers, n_sel
+            self.tokens_written = self.L * self.w.T
+            self.tokens_read = self.w.steps * self.L * n_sel
+
+    cfg = bench.step_config(_Run("qwen7b", 614 * 64), 1)
+    assert cfg["tokens_per_step"] == 28 * 131072 + 64 * 28 * 39296
+    cfg = bench.step_config(_Run("llama8b", 9830), 1)
+    assert cfg["tokens_per_step"] == 32768 + 64 * 9830
     assert cfg["workload"].startswith("llama8b: ")
+
+
+def test_roofline_names_the_binding_roof_against_the_burst_peak():
+    """A restore at the qwen7b shape (236 flop/B) is below the burst ridge point, so HBM
+    binds; at the llama8b shape (413 flop/B) the tensor peak binds, reported against the
+    burst figure with the sustained one beside it."""
+    peaks = {"hbm_gbs": 6785.5, "bf16_tflops": 1871.4, "bf16_tflops_sustained": 1690.7}
+    for name, bound in (("qwen7b", "hbm"), ("llama8b", "tensor")):
+        w = synth.workload(name)
+        ref = np.arange(0, w.T, 16)
+        n_sel = 39296 if name == "qwen7b" else w.n_sel
+        work = bench.algorithmic_work(w, w.T, n_sel, ref)
+        k = "rkv_reconstruct_kernel"
+        rows = bench.kernel_rows({k: (1, 0.05)}, {k: work[k]}, 1, peaks)
+        roof = bench.roofline_of(rows, {k: work[k]}, peaks, "measured", name)
+        assert roof["bound"] == bound and roof["kernel"] == k
+        if bound == "tensor":
+            assert roof["peak"] == 1871.4 and roof["peak_sustained"] == 1690.7
+            assert abs(roof["frac"] - work[k]["flops"] / 50e-6 / 1871.4e12) < 1e-4
+        else:
+            assert roof["peak"] == 6785.5
+            assert abs(roof["frac"] - work[k]["bytes"] / 50e-6 / 6785.5e9) < 1e-4
 
 
 def test_code_hash_ignores_comments_only(tmp_path):
