@@ -304,12 +304,14 @@ int64_t rkv_launch_count(rkv_ctx* ctx);
 
 /*
  * Test hook: device address and size of a scratch tensor of the last
- * compress pass, whose rows are in retrieval order (the pass's rows grouped by
- * sequence, each group padded to a multiple of 128; for a pass over one
- * sequence, row q is the pass's row q):
+ * compress pass.  M and D are in dense order (the pass's rows grouped by
+ * sequence, stably), Q in retrieval order (the same groups, each padded to a
+ * multiple of 128); for a pass over one sequence, row q of each is the pass's
+ * row q:
  *   0 = M, bf16 [rows, 2d_k]: the mean of each row's retrieved references;
- *   1 = H, bf16 [2*rows, d_ff]: SwiGLU hidden rows, 2q of kv_q and 2q+1 of
- *       the mean (negated);
+ *   1 = D, bf16 [rows, 2*d_ff]: row q = [hi | lo], the fp32 difference of the
+ *       SwiGLU hidden rows h(kv_q) - h(mean_q) as two bf16 parts (hi = its bf16
+ *       rounding, lo = the bf16 rounding of the rest);
  *   2 = Q, bf16 [rows, parts*2d_k]: the query rows, whose first 2d_k columns
  *       are bf16(kv) (parts = 1 for bf16 kv, 3 for fp32: hi, mid, lo pieces).
  * Valid until the next call on the context.

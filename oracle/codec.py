@@ -14,12 +14,16 @@ Two arithmetic modes
                    The storage formats the method itself prescribes are kept
                    (FP8 references, FP16 group extremes, b-bit codes).
 ``mode="operand"`` the same steps, but values are rounded where the GPU
-                   library rounds them: bf16 for every tensor-core operand
-                   (kv, reference mean, weights, SwiGLU hidden H, dequantised
-                   code), binary32 for the reference mean and for the code z
-                   before quantisation.  Accumulation stays float64.  The
-                   quantiser's decisions are taken in binary32 (the kernel's
-                   precision) so that integer codes can be compared exactly.
+                   library rounds them: bf16 for the tensor-core operands
+                   kv, reference mean, weights and dequantised code; binary32
+                   for the reference mean and for the code z before
+                   quantisation.  The SwiGLU hidden rows stay exact: the
+                   library forms h(kv) - h(mean) in binary32 and feeds it to
+                   the last GEMM as two bf16 parts (about 16 significant
+                   bits), which W_c3's linearity allows (section 2.3).
+                   Accumulation stays float64.  The quantiser's decisions are
+                   taken in binary32 (the kernel's precision) so that integer
+                   codes can be compared exactly.
 
 Readings of points the page leaves open (each one is also listed in the
 design notes of the repository):
@@ -220,9 +224,9 @@ def swish(x):
 
 
 def swiglu_hidden(x, Wc1, Wc2, mode: str = "operand"):
-    """Swish(x W_c1) (elementwise) x W_c2; bf16-rounded in operand mode."""
-    h = swish(x @ Wc1) * (x @ Wc2)
-    return F.bf16(h) if mode == "operand" else h
+    """Swish(x W_c1) (elementwise) x W_c2, the hidden row of f_c (section 2.3); exact
+    in both modes (the operand mode rounds only x, see the module notes)."""
+    return swish(x @ Wc1) * (x @ Wc2)
 
 
 def f_c(x, Wc1, Wc2, Wc3, mode: str = "operand"):

@@ -215,20 +215,20 @@ __global__ void __launch_bounds__(256)
 }
 
 // ---------------------------------------------------------------- mean rows
-// One warp per retrieval-order row q: M[q] = bf16(mean of the row's retrieved FP8
-// references), zeros for a padding row.  The sum of at most four E4M3 values is exact
-// in fp32; it is divided by k_i once, correctly rounded.  Each lane takes 8-element
-// pieces e = (32 u + lane) * 8, four pieces in flight at a time.  (The row's kv operand
-// is read by the encoder GEMM straight from the query rows.)
+// One warp per dense row j (storage row d_dst[j]): M[j] = bf16(mean of the row's
+// retrieved FP8 references).  The sum of at most four E4M3 values is exact in fp32; it
+// is divided by k_i once, correctly rounded.  Each lane takes 8-element pieces
+// e = (32 u + lane) * 8, four pieces in flight at a time.  (The row's kv operand is read
+// by the encoder GEMM from the query rows, or from their dense copy.)
 __global__ void __launch_bounds__(256)
-    mean_rows_kernel(const int32_t* __restrict__ q_dst, const uint8_t* __restrict__ pool8,
+    mean_rows_kernel(const int32_t* __restrict__ d_dst, const uint8_t* __restrict__ pool8,
                      const int32_t* __restrict__ ref_idx, int topk, int dkv, int T_cap,
-                     int R_cap, int m_pad, __nv_bfloat16* __restrict__ M,
+                     int R_cap, int n_rows, __nv_bfloat16* __restrict__ M,
                      int* __restrict__ status) {
   const int lane = threadIdx.x & 31;
-  for (int64_t q = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); q < m_pad;
+  for (int64_t q = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); q < n_rows;
        q += (int64_t)gridDim.x * 8) {
-    const int64_t dst = q_dst[q];
+    const int64_t dst = d_dst[q];
     __nv_bfloat16* xm = M + q * (int64_t)dkv;
     if (dst < 0) {
       for (int e = lane * 8; e < dkv; e += 256)
@@ -362,13 +362,30 @@ cudaError_t launch_prep_queries(rkv_ctx* c, const void* kv, int64_t stride, cons
   return e;
 }
 
+cudaError_t launch_prep_dense(rkv_ctx* c, const void* kv, int64_t stride, const int32_t* d_src,
+                              int n, cudaStream_t s) {
+  const Dims& d = c->d;
+  cudaEvent_t ev;
+  timing_begin(c, "rkv_prep_queries_kernel", s, &ev);
+  if (d.kv_f32)   // the first of the three bf16 pieces is the bf16 rounding of kv
+    prep_queries_kernel<<<n, 256, 0, s>>>(kv, stride, d.kv_f32, d_src, d.dkv, 1, c->Qd);
+  else
+    prep_queries_bf16_kernel<<<grid_for(n, 8, 16 * c->num_sms), 256, 0, s>>>(
+        static_cast<const __nv_bfloat16*>(kv), stride, d_src, d.dkv, n, c->Qd);
+  cudaError_t e = cudaGetLastError();
+  timing_end(c, "rkv_prep_queries_kernel", s, ev);
+  return e;
+}
+
 cudaError_t launch_mean_rows(rkv_ctx* c, const PassPlan& p, const int32_t* plan, cudaStream_t s) {
   const Dims& d = c->d;
   cudaEvent_t ev;
   timing_begin(c, "rkv_mean_rows_kernel", s, &ev);
-  mean_rows_kernel<<<grid_for(p.m_pad, 8, 16 * c->num_sms), 256, 0, s>>>(
-      plan + p.off_q_dst, static_cast<const uint8_t*>(c->st.pool_fp8), c->st.ref_idx, d.topk,
-      d.dkv, d.T_cap, d.R_cap, p.m_pad, c->M, c->status);
+  // dense rows: with one group the retrieval order's first n_rows rows
+  const int32_t* d_dst = plan + (p.dense ? p.off_d_dst : p.off_q_dst);
+  mean_rows_kernel<<<grid_for(p.n_rows, 8, 16 * c->num_sms), 256, 0, s>>>(
+      d_dst, static_cast<const uint8_t*>(c->st.pool_fp8), c->st.ref_idx, d.topk,
+      d.dkv, d.T_cap, d.R_cap, p.n_rows, c->M, c->status);
   cudaError_t e = cudaGetLastError();
   timing_end(c, "rkv_mean_rows_kernel", s, ev);
   return e;

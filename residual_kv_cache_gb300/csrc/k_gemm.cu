@@ -1,16 +1,23 @@
 // k_gemm.cu - the encoder's two tensor-core GEMMs (ResidualKV notes §2.3, §2.4).
 //
-//   GEMM-1/2:  [kv; mean] rows x [W_c1 | W_c2]  ->  H = Swish(a1) * a2   (bf16)
-//              A tile m (128 rows) = the bf16 kv rows of retrieval rows q = 64 m .. 64 m
-//              + 63 (the first 2d_k columns of the query rows Q) over their bf16 mean rows
-//              (M), two 64-row TMA boxes into one swizzled stage;
+//   GEMM-1/2:  [kv; mean] rows x [W_c1 | W_c2]  ->  h = Swish(a1) * a2, then the
+//              difference h(kv) - h(mean) of each token in fp32, stored as two bf16 parts
+//              D = [d_hi | d_lo] (d_hi = RN_bf16(d), d_lo = RN_bf16(d - d_hi): together
+//              d to about 2^-18 relative).
+//              A tile m (128 rows) = the bf16 kv rows of dense rows q = 64 m .. 64 m + 63
+//              (the first 2d_k columns of the query rows Q, or their dense copy Qd when a
+//              pass holds several sequences) over their bf16 mean rows (M), two 64-row
+//              TMA boxes into one swizzled stage;
 //              B = W12 [2 d_ff, 2d_k] with gate and value columns interleaved per
 //              256-row tile so that one 128x256 accumulator holds a1 and a2 of the same
-//              128 hidden units.  The epilogue applies the SwiGLU gate and stores
-//              h(kv_q) as H row 2q and -h(mean_q) as row 2q + 1 (an exact bf16 sign flip).
-//   GEMM-3:    H viewed as [m, 2 d_ff] (row q = [h(kv_q) | -h(mean_q)]) x W_c3^T
-//              -> z_q = h(kv_q) W_c3 - h(mean_q) W_c3 in one fp32 accumulator: both f_c
-//              outputs are mapped before the subtraction, never f_c of a difference.
+//              128 hidden units.  The epilogue threads of a token's kv row and mean row
+//              swap their fp32 h through shared memory and each forms half of the row's d.
+//   GEMM-3:    D viewed as [m, 2 d_ff] (row q = [d_hi | d_lo]) x [W_c3; W_c3]
+//              -> z_q = d_q W_c3 = h(kv_q) W_c3 - h(mean_q) W_c3.  Each f_c keeps its own
+//              nonlinear map (never f_c of a difference, ResidualKV notes §2.3 boxed z);
+//              W_c3 is linear, so subtracting the mapped rows before or after it is the
+//              same value, and subtracting them first in fp32 keeps the bf16 rounding of
+//              the tensor-core operand off each f_c output.
 //              The epilogue quantises each 32-column group in the thread that owns the
 //              token row (min/max, FP16 extremes rounded outward, Delta, round-half-
 //              even, clamp, nibble/crumb packing) and writes codes and extremes.
@@ -35,12 +42,12 @@ struct GemmShape {
 struct Epi12Args {
   __nv_bfloat16* H;
   int dff;
-  int rows;  // retrieval-order rows (kv and mean row pairs)
+  int rows;  // dense rows (kv and mean row pairs)
 };
 
 struct Epi3Args {
-  const int32_t* q_dst;  // per retrieval row: storage row, -1 for padding
-  int rows;              // retrieval-order rows
+  const int32_t* q_dst;  // per dense row: storage row
+  int rows;              // dense rows
   uint8_t* codes;
   uint32_t* meta;
   int code_bytes, G, bits, BN;
@@ -56,37 +63,70 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
 struct Epi12 {
   using Args = Epi12Args;
   static constexpr bool kSplitA = true;
+  static constexpr uint32_t kExchangeBytes = kTileM * 32 * 4;   // 128 rows x 32 fp32
+  // Tile row i holds the kv (i < 64) or mean (i >= 64) row of dense row 64 m + i % 64.
+  // Per 32-column chunk: every thread writes its row's fp32 h to the exchange buffer,
+  // then the kv thread of token t forms d = h(kv) - h(mean) for the chunk's first 16
+  // columns and the mean thread of t for the last 16, and stores d_hi and d_lo.
   __device__ static void run(const Args& a, uint32_t tacc, int m, int n, int row_in_tile,
-                             int* status) {
-    // tile row i holds the kv (i < 64) or mean (i >= 64) row of retrieval row 64 m + i % 64
+                             int* status, float* xch) {
     const int half = row_in_tile >= kTileM / 2 ? 1 : 0;
-    const int64_t q = (int64_t)m * (kTileM / 2) + (row_in_tile & (kTileM / 2 - 1));
-    const int64_t row = 2 * q + half;
+    const int tok = row_in_tile & (kTileM / 2 - 1);
+    const int64_t q = (int64_t)m * (kTileM / 2) + tok;
     const bool valid = q < a.rows;
-    const float sign = half ? -1.0f : 1.0f;
+    // exchange rows of 32 floats; the 16-byte chunks of row r sit at chunk ^ (r & 7) so
+    // that a warp's 16-byte accesses to 32 consecutive rows spread over the banks
+    float4* my_row = reinterpret_cast<float4*>(xch) + row_in_tile * 8;
+    const float4* kv_row = reinterpret_cast<const float4*>(xch) + tok * 8;
+    const float4* mn_row = reinterpret_cast<const float4*>(xch) + (tok + kTileM / 2) * 8;
+    const int sw_me = row_in_tile & 7, sw_tok = tok & 7;   // (tok + 64) & 7 == tok & 7
 #pragma unroll 1
     for (int c = 0; c < 4; ++c) {
       uint32_t g[32], v[32];
       tmem_ld32(tacc + c * 32, g);
       tmem_ld32(tacc + 128 + c * 32, v);
       tmem_ld_wait();
-      if (!valid) continue;
-      uint32_t w[16];
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        float h[2];
+      for (int i = 0; i < 8; ++i) {
+        float h[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const float a1 = __uint_as_float(g[4 * i + j]);
+          const float a2 = __uint_as_float(v[4 * i + j]);
+          h[j] = __fdividef(a1, 1.0f + __expf(-a1)) * a2;   // Swish (beta = 1) times a2
+        }
+        my_row[i ^ sw_me] = make_float4(h[0], h[1], h[2], h[3]);
+      }
+      bar_sync(1, 128);
+      uint32_t whi[8], wlo[8];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int ch = 4 * half + i;                  // this thread's 16-byte chunks
+        const float4 hk = kv_row[ch ^ sw_tok], hm = mn_row[ch ^ sw_tok];
+        const float d[4] = {hk.x - hm.x, hk.y - hm.y, hk.z - hm.z, hk.w - hm.w};
+        float lo[4];
+        uint32_t hb[2];
 #pragma unroll
         for (int j = 0; j < 2; ++j) {
-          const float a1 = __uint_as_float(g[2 * i + j]);
-          const float a2 = __uint_as_float(v[2 * i + j]);
-          const float sw = a1 / (1.0f + expf(-a1));   // Swish, beta = 1
-          h[j] = sign * (sw * a2);
+          hb[j] = pack_bf16x2(d[2 * j], d[2 * j + 1]);
+          lo[2 * j] = d[2 * j] - __uint_as_float(hb[j] << 16);
+          lo[2 * j + 1] = d[2 * j + 1] - __uint_as_float(hb[j] & 0xFFFF0000u);
         }
-        w[i] = pack_bf16x2(h[0], h[1]);
+        whi[2 * i] = hb[0];
+        whi[2 * i + 1] = hb[1];
+        wlo[2 * i] = pack_bf16x2(lo[0], lo[1]);
+        wlo[2 * i + 1] = pack_bf16x2(lo[2], lo[3]);
       }
-      uint4* dst = reinterpret_cast<uint4*>(a.H + row * a.dff + (int64_t)n * 128 + c * 32);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) dst[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+      if (valid) {
+        __nv_bfloat16* dst = a.H + q * (2 * (int64_t)a.dff) + (int64_t)n * 128 + c * 32 + half * 16;
+        uint4* dh = reinterpret_cast<uint4*>(dst);
+        uint4* dl = reinterpret_cast<uint4*>(dst + a.dff);
+        dh[0] = make_uint4(whi[0], whi[1], whi[2], whi[3]);
+        dh[1] = make_uint4(whi[4], whi[5], whi[6], whi[7]);
+        dl[0] = make_uint4(wlo[0], wlo[1], wlo[2], wlo[3]);
+        dl[1] = make_uint4(wlo[4], wlo[5], wlo[6], wlo[7]);
+      }
+      bar_sync(1, 128);                                // the buffer is reused next chunk
     }
   }
 };
@@ -158,8 +198,9 @@ __device__ __forceinline__ void quant_group(const float* z, int bits, uint8_t* c
 struct Epi3 {
   using Args = Epi3Args;
   static constexpr bool kSplitA = false;
+  static constexpr uint32_t kExchangeBytes = 0;
   __device__ static void run(const Args& a, uint32_t tacc, int m, int n, int row_in_tile,
-                             int* status) {
+                             int* status, float*) {
     const int64_t row = (int64_t)m * kTileM + row_in_tile;
     const int64_t dst = row < a.rows ? (int64_t)a.q_dst[row] : -1;
     const bool valid = dst >= 0;                     // padding rows are not stored
@@ -192,7 +233,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* smem = align1024(smem_raw);
   uint8_t* sA = smem;
   uint8_t* sB = smem + STAGES * kTileABytes;
-  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * kBBytes);
+  float* xch = reinterpret_cast<float*>(sB + STAGES * kBBytes);   // epilogue exchange
+  uint64_t* full = reinterpret_cast<uint64_t*>(sB + STAGES * kBBytes + Epi::kExchangeBytes);
   uint64_t* empty = full + STAGES;
   uint64_t* tfull = empty + STAGES;
   uint64_t* tempty = tfull + 2;
@@ -321,10 +363,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < n_tiles_total; t += gridDim.x) {
       const int m = t / g.n_tiles, n = t % g.n_tiles;
-      if (!warp_wait(&tfull[acc], acc_phase, abort_flag, g.status)) break;
+      // An epilogue that swaps rows between its warps (named barriers inside) goes on
+      // only if all four warps' waits succeeded, so no warp is left alone at a barrier.
+      bool ok = warp_wait(&tfull[acc], acc_phase, abort_flag, g.status);
+      if (Epi::kExchangeBytes > 0) ok = bar_red_and(2, 128, ok);
+      if (!ok) break;
       tc_fence_after();
       const uint32_t tacc = tmem + ((uint32_t)(ew * 32) << 16) + (uint32_t)(acc * BN);
-      Epi::run(ea, tacc, m, n, row_in_tile, g.status);
+      Epi::run(ea, tacc, m, n, row_in_tile, g.status, xch);
       tc_fence_before();
       __syncwarp();
       if (lane_id() == 0) mbar_arrive(&tempty[acc]);
@@ -343,15 +389,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int BN, int STAGES>
+template <int BN, int STAGES, typename Epi>
 constexpr size_t gemm_smem_bytes() {
-  return 1024 + (size_t)STAGES * (kTileABytes + BN * 128) + 8 * (2 * STAGES + 4) + 16;
+  return 1024 + (size_t)STAGES * (kTileABytes + BN * 128) + Epi::kExchangeBytes +
+         8 * (2 * STAGES + 4) + 16;
 }
 
 template <int BN, int STAGES, typename Epi>
 cudaError_t run_gemm(rkv_ctx* c, const CUtensorMap& tA, const CUtensorMap& tA2, const CUtensorMap& tB,
                      GemmShape g, typename Epi::Args ea, const char* name, cudaStream_t s) {
-  const size_t smem = gemm_smem_bytes<BN, STAGES>();
+  const size_t smem = gemm_smem_bytes<BN, STAGES, Epi>();
   auto kern = tc_gemm_kernel<BN, STAGES, Epi>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
@@ -368,16 +415,17 @@ cudaError_t run_gemm(rkv_ctx* c, const CUtensorMap& tA, const CUtensorMap& tA2, 
 
 }  // namespace
 
-cudaError_t launch_gemm12(rkv_ctx* c, int m_pad, cudaStream_t s) {
+cudaError_t launch_gemm12(rkv_ctx* c, const PassPlan& p, cudaStream_t s) {
   const Dims& d = c->d;
+  const int rows = p.n_rows;                    // dense rows
   GemmShape g;
-  g.m_tiles = (m_pad + kTileM / 2 - 1) / (kTileM / 2);
+  g.m_tiles = (rows + kTileM / 2 - 1) / (kTileM / 2);
   g.n_tiles = (2 * d.dff) / kEncN;
   g.nkb = d.dkv / kTileK;
   g.b_kwrap = g.nkb;
   g.status = c->status;
-  Epi12Args ea{c->H, d.dff, m_pad};
-  return run_gemm<kEncN, 4, Epi12>(c, c->tm_qa, c->tm_m, c->tm_w12, g, ea,
+  Epi12Args ea{c->H, d.dff, rows};
+  return run_gemm<kEncN, 4, Epi12>(c, p.dense ? c->tm_qd : c->tm_qa, c->tm_m, c->tm_w12, g, ea,
                                    "rkv_gemm12_swiglu_kernel", s);
 }
 
@@ -385,12 +433,13 @@ cudaError_t launch_gemm3_quant(rkv_ctx* c, const PassPlan& p, const int32_t* pla
                                cudaStream_t s) {
   const Dims& d = c->d;
   GemmShape g;
-  g.m_tiles = (p.m_pad + kTileM - 1) / kTileM;
+  g.m_tiles = (p.n_rows + kTileM - 1) / kTileM;  // dense rows
   g.nkb = (2 * d.dff) / kTileK;
   g.b_kwrap = d.dff / kTileK;
   g.status = c->status;
-  Epi3Args ea{plan + p.off_q_dst, p.m_pad, static_cast<uint8_t*>(c->st.codes),
-              static_cast<uint32_t*>(c->st.meta), d.code_bytes, d.G, d.bits, 0};
+  Epi3Args ea{plan + (p.dense ? p.off_d_dst : p.off_q_dst), p.n_rows,
+              static_cast<uint8_t*>(c->st.codes), static_cast<uint32_t*>(c->st.meta),
+              d.code_bytes, d.G, d.bits, 0};
   const char* name = "rkv_gemm3_quant_kernel";
   // Tile width: the one whose whole waves of one-tile-per-SM finish first (a tile's
   // main loop costs in proportion to its width).

@@ -409,7 +409,8 @@ rkv_status rkv_create(const rkv_config* cfg, const void* Wc1, const void* Wc2, c
   c->m_cap = c->max_rows + kTileM * std::min(d.B, c->max_rows);
   c->tiles_cap = c->m_cap / kTileM;
   c->units_cap = c->tiles_cap * ((d.R_cap + kRefTile - 1) / kRefTile);
-  c->plan_ints = std::max(3 * c->m_cap + 4 * c->tiles_cap + 2 * c->units_cap, 4 * c->max_rows);
+  c->plan_ints = std::max(4 * c->m_cap + 4 * c->tiles_cap + 2 * c->units_cap + 2 * c->max_rows,
+                          4 * c->max_rows);
   c->pool_count.assign(d.B, 0);
   c->ref_before.assign((size_t)d.T_cap + 1, 0);
   walk_schedule(d.T_cap, d.stride, d.alpha, d.sink, [&](int p) { c->ref_before[p + 1] = 1; });
@@ -428,6 +429,7 @@ rkv_status rkv_create(const rkv_config* cfg, const void* Wc1, const void* Wc2, c
   ALLOC(c->ref_before_dev, ((size_t)d.T_cap + 1) * sizeof(int32_t));
   ALLOC(c->Q, (size_t)c->m_cap * d.parts * d.dkv * 2);
   ALLOC(c->M, (size_t)c->m_cap * d.dkv * 2);
+  if (d.B > 1) ALLOC(c->Qd, (size_t)c->max_rows * d.dkv * 2);
   ALLOC(c->H, (size_t)2 * c->m_cap * d.dff * 2);
   ALLOC(c->part, (size_t)c->units_cap * kTileM * 4 * sizeof(int2));
   ALLOC(c->attn_ws, sizeof(float) * kAttnMaxChunks * kAttnMaxGroup * d.N * (2 + d.D));
@@ -481,6 +483,7 @@ rkv_status rkv_create(const rkv_config* cfg, const void* Wc1, const void* Wc2, c
   ok &= make_map(&c->tm_pool, st->pool_bf16, dkv, (uint64_t)d.B * d.R_cap, dkv * 2, kRefTile);
   ok &= make_map(&c->tm_qa, c->Q, dkv, c->m_cap, (uint64_t)d.parts * dkv * 2, kTileM / 2);
   ok &= make_map(&c->tm_m, c->M, dkv, c->m_cap, dkv * 2, kTileM / 2);
+  if (c->Qd) ok &= make_map(&c->tm_qd, c->Qd, dkv, c->max_rows, dkv * 2, kTileM / 2);
   ok &= make_map(&c->tm_w12, c->w12, dkv, (uint64_t)2 * d.dff, dkv * 2, kEncN);
   ok &= make_map(&c->tm_h3, c->H, (uint64_t)2 * d.dff, c->m_cap, (uint64_t)2 * d.dff * 2, kTileM);
   const uint32_t bn3 = d.dc % 256 == 0 ? 256u : (d.dc % 128 == 0 ? 128u : 64u);
@@ -682,8 +685,33 @@ rkv_status rkv_compress(rkv_ctx* c, const void* kv, int64_t kv_row_stride, const
     p.n_units = n_units;
     p.off_u_rt = p.off_u_tile + n_units;
     p.total_ints = p.off_u_rt + n_units;
-    if (n_units > c->units_cap || p.total_ints > c->plan_ints)
+    // several sequences in the pass: the encoder GEMMs take its rows densely packed
+    p.dense = gbeg.size() > 2;
+    if (p.dense) {
+      p.off_q_comp = p.total_ints;
+      p.off_d_src = p.off_q_comp + m_pad;
+      p.off_d_dst = p.off_d_src + m;
+      p.total_ints = p.off_d_dst + m;
+    }
+    if (n_units > c->units_cap || p.total_ints > c->plan_ints || (p.dense && !c->Qd))
       return fail(RKV_ECAPACITY, "compress pass exceeds the planned retrieval scratch");
+    if (p.dense) {
+      // dense row j = the j-th row in group order; retrieval row q of group g sits at
+      // the group's padded offset
+      for (size_t g = 0, q = 0; g + 1 < gbeg.size(); ++g) {
+        const int i = gbeg[g], j = gbeg[g + 1];
+        const int padded = (j - i + kTileM - 1) / kTileM * kTileM;
+        for (int k = 0; k < padded; ++k) {
+          const bool real = k < j - i;
+          h[p.off_q_comp + q + k] = real ? i + k : -1;
+          if (real) {
+            h[p.off_d_src + i + k] = h[p.off_q_src + q + k];
+            h[p.off_d_dst + i + k] = h[p.off_q_dst + q + k];
+          }
+        }
+        q += padded;
+      }
+    }
     // tiles in order; units tile-major, pool tiles in increasing slot order
     int u = 0;
     for (int i = 0; i < ntiles; ++i) {
@@ -697,10 +725,11 @@ rkv_status rkv_compress(rkv_ctx* c, const void* kv, int64_t kv_row_stride, const
       }
     }
     CUDA_OK(staging_upload(c, b, p.off_q_pos, p.total_ints - p.off_q_pos, st));
+    if (p.dense) CUDA_OK(launch_prep_dense(c, kv, kv_row_stride, plan + p.off_d_src, m, st));
     CUDA_OK(launch_retrieve(c, p, plan, st));
     CUDA_OK(launch_retrieve_merge(c, p, plan, st));
     CUDA_OK(launch_mean_rows(c, p, plan, st));
-    CUDA_OK(launch_gemm12(c, p.m_pad, st));
+    CUDA_OK(launch_gemm12(c, p, st));
     CUDA_OK(launch_gemm3_quant(c, p, plan, st));
   }
   return RKV_OK;
@@ -774,6 +803,7 @@ void rkv_free(rkv_ctx* c) {
   cudaFree(c->ref_before_dev);
   cudaFree(c->Q);
   cudaFree(c->M);
+  cudaFree(c->Qd);
   cudaFree(c->H);
   cudaFree(c->part);
   cudaFree(c->status);

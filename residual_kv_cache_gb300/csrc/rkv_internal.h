@@ -42,15 +42,23 @@ struct TimingSlot {
   std::vector<cudaEvent_t> pending;  // start/stop pairs not yet read
 };
 
-// Device plan of one compress pass (int32 arrays inside one buffer).
+// Device plan of one compress pass (int32 arrays inside one buffer).  Retrieval works
+// in retrieval order (the pass's rows grouped by sequence, each group padded to 128
+// rows, so a tile queries one pool); the encoder GEMMs work on the pass's rows packed
+// densely (row j = the j-th row in group order).  With one group the two orders agree
+// on the first n_rows rows and the dense arrays are not used.
 struct PassPlan {
   int n_rows = 0;      // compact rows (this pass)
   int m_pad = 0;       // retrieval-order rows, padded per sequence to 128
   int n_tiles = 0;     // retrieval tiles (128 query rows of one sequence)
   int n_units = 0;     // retrieval units: (tile, 256-reference pool tile)
+  bool dense = false;  // several groups: the encoder reads the dense arrays below
   // offsets (in int32 elements) inside the plan buffer
   int off_q_src, off_q_pos, off_q_dst, off_t_seq, off_t_row0, off_t_nrt, off_t_u0, off_u_tile,
       off_u_rt;
+  int off_q_comp = 0;  // [m_pad] dense row of each retrieval row, -1 for padding
+  int off_d_src = 0;   // [n_rows] source kv row of each dense row
+  int off_d_dst = 0;   // [n_rows] storage row of each dense row
   int total_ints = 0;
 };
 
@@ -74,9 +82,11 @@ struct rkv_ctx {
   float2* rope_hi = nullptr;      // [n_hi][D/2] (cos, sin)(h * 512 * theta_j)
   int32_t* ref_before_dev = nullptr;   // [T_cap + 1] device copy of ref_before
   __nv_bfloat16* Q = nullptr;     // [m_cap, parts * 2d_k] retrieval-order queries
-  __nv_bfloat16* M = nullptr;     // [m_cap, 2d_k] bf16 reference means, retrieval order
-  __nv_bfloat16* H = nullptr;     // [2 m_cap, d_ff] SwiGLU rows: 2q from kv, 2q + 1 from the
-                                  // mean (negated)
+  __nv_bfloat16* M = nullptr;     // [m_cap, 2d_k] bf16 reference means, dense order
+  __nv_bfloat16* Qd = nullptr;    // [max_rows, 2d_k] bf16 kv rows in dense order (B > 1 only;
+                                  // with one sequence the query rows serve)
+  __nv_bfloat16* H = nullptr;     // [m_cap, 2 d_ff] row q: [hi | lo] bf16 parts of the fp32
+                                  // hidden difference h(kv_q) - h(mean_q)
   int2* part = nullptr;           // [units_cap, 128, 4] partial top-k (distance bits, slot)
   float* attn_ws = nullptr;       // sparse attention chunk partials (m, l, acc), kAttnMaxChunks
                                   // x kAttnMaxGroup N query heads
@@ -93,6 +103,7 @@ struct rkv_ctx {
   // TMA descriptors (fixed addresses, built once)
   CUtensorMap tm_q, tm_pool, tm_w12, tm_h3, tm_w3, tm_w3_128, tm_wd;
   CUtensorMap tm_qa, tm_m;        // GEMM-1/2 A halves: the bf16 kv piece of Q, and M (64 rows)
+  CUtensorMap tm_qd;              // GEMM-1/2 kv half from Qd (dense passes)
 
   // host mirror of each sequence's pool fill
   std::vector<int32_t> pool_count;
@@ -116,11 +127,14 @@ cudaError_t launch_pool_append(rkv_ctx* c, const void* kv, int64_t stride, const
                                int n, cudaStream_t s);
 cudaError_t launch_prep_queries(rkv_ctx* c, const void* kv, int64_t stride, const int32_t* q_src,
                                 int m_pad, cudaStream_t s);
+// bf16 kv rows of the dense order into Qd (n rows, sources d_src)
+cudaError_t launch_prep_dense(rkv_ctx* c, const void* kv, int64_t stride, const int32_t* d_src,
+                              int n, cudaStream_t s);
 cudaError_t launch_retrieve(rkv_ctx* c, const PassPlan& p, const int32_t* plan, cudaStream_t s);
 cudaError_t launch_retrieve_merge(rkv_ctx* c, const PassPlan& p, const int32_t* plan,
                                   cudaStream_t s);
 cudaError_t launch_mean_rows(rkv_ctx* c, const PassPlan& p, const int32_t* plan, cudaStream_t s);
-cudaError_t launch_gemm12(rkv_ctx* c, int m_pad, cudaStream_t s);
+cudaError_t launch_gemm12(rkv_ctx* c, const PassPlan& p, cudaStream_t s);
 cudaError_t launch_gemm3_quant(rkv_ctx* c, const PassPlan& p, const int32_t* plan,
                                cudaStream_t s);
 cudaError_t launch_reconstruct(rkv_ctx* c, const int32_t* seq, const int32_t* pos, int n_sel,
