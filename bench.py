@@ -810,17 +810,21 @@ def measure_attention(run, ctx):
 
 
 def storage_report(codec, w) -> dict:
-    """Bytes the codec keeps per token (its storage tensors over B x T tokens) against FP16
-    K and V (2 bytes per value of the 2d_k-wide row).  The bf16 shadow of the FP8 pool is
-    the retrieval's tensor-core operand, shown separately."""
-    names = ["pool_fp8", "pool_bf16", "pool_norm2", "pool_pos", "codes", "meta", "ref_idx"]
+    """Bytes the codec's storage keeps per token (the caller's storage tensors over B x T
+    tokens: FP8 references with their norms and positions, codes, extremes, slots)
+    against FP16 K and V (2 bytes per value of the 2d_k-wide row).  The library's bf16
+    copy of the pool (the retrieval's tensor-core operand, a compute cache derived from
+    the FP8 references) is shown beside it."""
+    names = ["pool_fp8", "pool_norm2", "pool_pos", "codes", "meta", "ref_idx"]
     nbytes = {n: getattr(codec, n).numel() * getattr(codec, n).element_size() for n in names}
     tokens = codec.codes.shape[0] * codec.codes.shape[1]
     fp16 = 2 * w.d_kv
     total = sum(nbytes.values())
+    cache = codec.pool_cache_bytes()
     return {"bytes_per_token": round(total / tokens, 1),
             "fraction_of_fp16_kv": round(total / tokens / fp16, 4),
-            "fraction_without_pool_shadow": round((total - nbytes["pool_bf16"]) / tokens / fp16, 4)}
+            "compute_cache_bytes_per_token": round(cache / tokens, 1),
+            "fraction_with_compute_cache": round((total + cache) / tokens / fp16, 4)}
 
 
 def step_config(run, world: int) -> dict:

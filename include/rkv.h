@@ -107,8 +107,6 @@ typedef struct {
  * rkv_storage_bytes.  All row-major; "row" = seq * T_cap + pos for token
  * tables and seq * R_cap + slot for pool tables.
  *   pool_fp8   [B, R_cap, 2d_k]  E4M3 references (ResidualKV notes §2.4, §3.3)
- *   pool_bf16  [B, R_cap, 2d_k]  the same values in bf16: the tensor-core
- *                                operand of retrieval (a compute copy)
  *   pool_norm2 [B, R_cap]  fp32  squared norm of each decoded reference
  *   pool_pos   [B, R_cap]  int32 position of each reference, INT32_MAX = empty
  *   codes      [B, T_cap, code_bytes]  packed codes (d_c*b/8 bytes; 2*d_c
@@ -120,7 +118,6 @@ typedef struct {
  */
 typedef struct {
   void* pool_fp8;
-  void* pool_bf16;
   float* pool_norm2;
   int32_t* pool_pos;
   void* codes;
@@ -128,8 +125,8 @@ typedef struct {
   int32_t* ref_idx;
 } rkv_storage;
 
-/* Byte sizes of the seven storage tensors, in the order of rkv_storage. */
-rkv_status rkv_storage_bytes(const rkv_config* cfg, size_t sizes[7]);
+/* Byte sizes of the six storage tensors, in the order of rkv_storage. */
+rkv_status rkv_storage_bytes(const rkv_config* cfg, size_t sizes[6]);
 
 /*
  * The reference positions of cfg's schedule below max_tokens (ResidualKV notes
@@ -169,7 +166,8 @@ rkv_status rkv_create(const rkv_config* cfg, const void* Wc1, const void* Wc2,
  *   src_rows, seq, pos (host) [n]; every pos must be a position of the
  *     schedule (see rkv_config), and per sequence the positions must continue
  *     the sequence's references in order (slot m = the m-th schedule position).
- * Writes pool_fp8/pool_bf16/pool_norm2/pool_pos at the position's slot and the
+ * Writes pool_fp8/pool_norm2/pool_pos at the position's slot (and the context's
+ * bf16 copy of the reference, see rkv_pool_cache) and the
  * token's own row: ref_idx = [slot, -1, ...], codes = 0, meta = 0.
  * Errors (nothing launched): RKV_EINVAL (range, not a reference position,
  * out of order), RKV_ECAPACITY (slot >= R_cap).
@@ -224,6 +222,17 @@ rkv_status rkv_sparse_attention(rkv_ctx* ctx, const float* q, int32_t n_q_heads,
                                 void* stream);
 
 /*
+ * The context's bf16 copy of the reference pool: [B, R_cap, 2d_k], row
+ * s * R_cap + slot holding the decoded E4M3 reference of that slot exactly (every E4M3
+ * value is a bf16 value).  It is the tensor-core operand of retrieval, a compute cache
+ * that rkv_pool_append keeps in step with pool_fp8, not part of the cache's storage;
+ * the context owns it and rkv_free releases it.  *ptr (device) and *bytes receive its
+ * address and size; read it only in stream order after the appends that wrote it.
+ * Errors: RKV_EINVAL (NULL argument).
+ */
+rkv_status rkv_pool_cache(rkv_ctx* ctx, void** ptr, size_t* bytes);
+
+/*
  * Forget everything written for one sequence (seq >= 0) or for all (seq = -1):
  * its pool slots become empty and its token rows unwritten, so the slot can
  * hold a new sequence (stream-ordered; codes and extremes are overwritten by
@@ -257,7 +266,8 @@ void rkv_free(rkv_ctx* ctx);
  * nearest in squared L2 distance, nearest first, ties to the smaller slot, -1 padded.
  *   queries    (device, bf16)  [n, d]   the query rows (bf16 joint K/V rows)
  *   q_pos      (device, int32) [n]      their positions
- *   pool       (device, bf16)  [R, d]   the decoded reference rows (rkv_storage.pool_bf16)
+ *   pool       (device, bf16)  [R, d]   the decoded reference rows (for a context's
+ *                                      sequence s: rkv_pool_cache rows s * R_cap ..)
  *   pool_norm2 (device, fp32)  [R]      their squared norms (rkv_storage.pool_norm2)
  *   pool_pos   (device, int32) [R]      their positions; INT32_MAX marks an empty slot
  *   out_idx    (device, int32) [n, topk]  output

@@ -48,10 +48,9 @@ class _Config(ctypes.Structure):
 
 
 class _Storage(ctypes.Structure):
-    _fields_ = [("pool_fp8", ctypes.c_void_p), ("pool_bf16", ctypes.c_void_p),
-                ("pool_norm2", ctypes.c_void_p), ("pool_pos", ctypes.c_void_p),
-                ("codes", ctypes.c_void_p), ("meta", ctypes.c_void_p),
-                ("ref_idx", ctypes.c_void_p)]
+    _fields_ = [("pool_fp8", ctypes.c_void_p), ("pool_norm2", ctypes.c_void_p),
+                ("pool_pos", ctypes.c_void_p), ("codes", ctypes.c_void_p),
+                ("meta", ctypes.c_void_p), ("ref_idx", ctypes.c_void_p)]
 
 
 class _Timing(ctypes.Structure):
@@ -73,6 +72,7 @@ ABI_FUNCTIONS = {
     "rkv_sparse_attention": (_I32, [_P, _P, _I32, _P, _P, _I32, _P, _P]),
     "rkv_get_status": (_I32, [_P, ctypes.POINTER(_I32), _P]),
     "rkv_reset": (_I32, [_P, _I32, _P]),
+    "rkv_pool_cache": (_I32, [_P, ctypes.POINTER(_P), ctypes.POINTER(ctypes.c_size_t)]),
     "rkv_last_error": (ctypes.c_char_p, []),
     "rkv_free": (None, [_P]),
     "rkv_set_timing": (_I32, [_P, _I32]),
@@ -206,7 +206,7 @@ class Config:
 
 
 def storage_bytes(cfg: Config):
-    sizes = (ctypes.c_size_t * 7)()
+    sizes = (ctypes.c_size_t * 6)()
     c = cfg.to_c()
     _check(lib().rkv_storage_bytes(ctypes.byref(c), sizes))
     return list(sizes)
@@ -262,22 +262,22 @@ def retrieve_noalloc(queries, q_pos, pool, pool_norm2, pool_pos, topk: int = 4, 
 class Codec:
     """One codec layer: caller-side storage tensors plus the library context."""
 
-    STORAGE = ("pool_fp8", "pool_bf16", "pool_norm2", "pool_pos", "codes", "meta", "ref_idx")
+    STORAGE = ("pool_fp8", "pool_norm2", "pool_pos", "codes", "meta", "ref_idx")
 
     def __init__(self, cfg: Config, weights: dict, device=None, stream=None):
         self.cfg = cfg
         self.device = torch.device(device or "cuda")
         c = cfg.to_c()
         self._c = c
-        sizes = (ctypes.c_size_t * 7)()
+        sizes = (ctypes.c_size_t * 6)()
         _check(lib().rkv_storage_bytes(ctypes.byref(c), sizes))
         B, T = c.batch, c.max_tokens
         dkv, G = cfg.d_kv, cfg.d_c // cfg.group
         R = sizes[0] // (B * dkv)                      # pool slots per sequence
-        cb = sizes[4] // (B * T)
+        cb = sizes[3] // (B * T)
         dev = self.device
+        self._shape = (B, R, dkv)
         self.pool_fp8 = torch.empty((B, R, dkv), dtype=torch.uint8, device=dev)
-        self.pool_bf16 = torch.empty((B, R, dkv), dtype=torch.bfloat16, device=dev)
         self.pool_norm2 = torch.empty((B, R), dtype=torch.float32, device=dev)
         self.pool_pos = torch.empty((B, R), dtype=torch.int32, device=dev)
         self.codes = torch.zeros((B, T, cb), dtype=torch.uint8, device=dev)
@@ -292,6 +292,24 @@ class Codec:
         _check(lib().rkv_create(ctypes.byref(c), *(t.data_ptr() for t in w), ctypes.byref(st),
                                 _stream_ptr(stream), ctypes.byref(ctx)))
         self._ctx = ctx
+
+    @property
+    def pool_bf16(self) -> torch.Tensor:
+        """The context's bf16 copy of the pool ([B, R_cap, 2d_k], the retrieval's
+        tensor-core operand; library memory, valid while the codec lives): a view, not a
+        copy."""
+        p, b = ctypes.c_void_p(), ctypes.c_size_t()
+        _check(lib().rkv_pool_cache(self._ctx, ctypes.byref(p), ctypes.byref(b)))
+        B, R, dkv = self._shape
+        cai = type("_Dev", (), {})()
+        cai.__cuda_array_interface__ = {"shape": (B, R, dkv), "typestr": "<u2",
+                                        "data": (p.value, False), "version": 3}
+        return torch.as_tensor(cai, device=self.device).view(torch.bfloat16)
+
+    def pool_cache_bytes(self) -> int:
+        p, b = ctypes.c_void_p(), ctypes.c_size_t()
+        _check(lib().rkv_pool_cache(self._ctx, ctypes.byref(p), ctypes.byref(b)))
+        return int(b.value)
 
     # -- ABI calls -------------------------------------------------------------------
     def _rows_call(self, fn, kv, seq, pos, src_rows, stream):

@@ -338,7 +338,7 @@ cudaError_t launch_pool_append(rkv_ctx* c, const void* kv, int64_t stride, const
   auto kern = d.kv_f32 ? pool_append_kernel<true> : pool_append_kernel<false>;
   kern<<<(n + 7) / 8, 256, 0, s>>>(kv, stride, plan, n, d.dkv, d.R_cap,
                                    static_cast<uint8_t*>(c->st.pool_fp8),
-                                   static_cast<__nv_bfloat16*>(c->st.pool_bf16), c->st.pool_norm2,
+                                   c->pool_bf16, c->st.pool_norm2,
                                    c->st.pool_pos, c->st.ref_idx, d.topk,
                                    static_cast<uint8_t*>(c->st.codes), d.code_bytes,
                                    static_cast<uint32_t*>(c->st.meta), d.G);

@@ -366,18 +366,17 @@ rkv_status rkv_reference_positions(const rkv_config* cfg, int32_t* pos, int32_t 
   return RKV_OK;
 }
 
-rkv_status rkv_storage_bytes(const rkv_config* cfg, size_t sizes[7]) {
+rkv_status rkv_storage_bytes(const rkv_config* cfg, size_t sizes[6]) {
   Dims d;
   rkv_status st = derive(cfg, &d);
   if (st != RKV_OK) return st;
   const size_t pool_rows = (size_t)d.B * d.R_cap, tok_rows = (size_t)d.B * d.T_cap;
   sizes[0] = pool_rows * d.dkv;                 // pool_fp8
-  sizes[1] = pool_rows * d.dkv * 2;             // pool_bf16
-  sizes[2] = pool_rows * 4;                     // pool_norm2
-  sizes[3] = pool_rows * 4;                     // pool_pos
-  sizes[4] = tok_rows * d.code_bytes;           // codes
-  sizes[5] = tok_rows * d.G * 4;                // meta
-  sizes[6] = tok_rows * d.topk * 4;             // ref_idx
+  sizes[1] = pool_rows * 4;                     // pool_norm2
+  sizes[2] = pool_rows * 4;                     // pool_pos
+  sizes[3] = tok_rows * d.code_bytes;           // codes
+  sizes[4] = tok_rows * d.G * 4;                // meta
+  sizes[5] = tok_rows * d.topk * 4;             // ref_idx
   return RKV_OK;
 }
 
@@ -389,7 +388,7 @@ rkv_status rkv_create(const rkv_config* cfg, const void* Wc1, const void* Wc2, c
   rkv_status r = derive(cfg, &d);
   if (r != RKV_OK) return r;
   if (!st || !Wc1 || !Wc2 || !Wc3 || !Wd) return fail(RKV_EINVAL, "NULL weight or storage");
-  const void* ptrs[] = {Wc1, Wc2, Wc3, Wd, st->pool_fp8, st->pool_bf16, st->pool_norm2,
+  const void* ptrs[] = {Wc1, Wc2, Wc3, Wd, st->pool_fp8, st->pool_norm2,
                         st->pool_pos, st->codes, st->meta, st->ref_idx};
   for (const void* p : ptrs) {
     if (!p) return fail(RKV_EINVAL, "NULL storage pointer");
@@ -421,6 +420,7 @@ rkv_status rkv_create(const rkv_config* cfg, const void* Wc1, const void* Wc2, c
 #define ALLOC(ptr, bytes)                                                                 \
   if (fail_status == RKV_OK && alloc(reinterpret_cast<void**>(&(ptr)), (bytes)) != cudaSuccess) \
     fail_status = fail(RKV_ECUDA, "cudaMalloc of %zu bytes failed", (size_t)(bytes));
+  ALLOC(c->pool_bf16, (size_t)d.B * d.R_cap * d.dkv * 2);
   ALLOC(c->w12, (size_t)2 * d.dff * d.dkv * 2);
   ALLOC(c->w3, (size_t)d.dc * d.dff * 2);
   ALLOC(c->wd, (size_t)d.dkv * d.dc * 2);
@@ -480,7 +480,7 @@ rkv_status rkv_create(const rkv_config* cfg, const void* Wc1, const void* Wc2, c
   const uint64_t dkv = d.dkv;
   bool ok = true;
   ok &= make_map(&c->tm_q, c->Q, (uint64_t)d.parts * dkv, c->m_cap, (uint64_t)d.parts * dkv * 2, kTileM);
-  ok &= make_map(&c->tm_pool, st->pool_bf16, dkv, (uint64_t)d.B * d.R_cap, dkv * 2, kRefTile);
+  ok &= make_map(&c->tm_pool, c->pool_bf16, dkv, (uint64_t)d.B * d.R_cap, dkv * 2, kRefTile);
   ok &= make_map(&c->tm_qa, c->Q, dkv, c->m_cap, (uint64_t)d.parts * dkv * 2, kTileM / 2);
   ok &= make_map(&c->tm_m, c->M, dkv, c->m_cap, dkv * 2, kTileM / 2);
   if (c->Qd) ok &= make_map(&c->tm_qd, c->Qd, dkv, c->max_rows, dkv * 2, kTileM / 2);
@@ -500,6 +500,7 @@ rkv_status rkv_create(const rkv_config* cfg, const void* Wc1, const void* Wc2, c
   cudaError_t e = cudaMemsetAsync(c->status, 0, 512, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(c->Q, 0, (size_t)c->m_cap * d.parts * d.dkv * 2, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(c->M, 0, (size_t)c->m_cap * d.dkv * 2, s);
+  if (e == cudaSuccess) e = cudaMemsetAsync(c->pool_bf16, 0, (size_t)d.B * d.R_cap * d.dkv * 2, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(c->H, 0, (size_t)2 * c->m_cap * d.dff * 2, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(c->attn_count, 0, sizeof(int) * d.N, s);
   if (e == cudaSuccess) e = launch_init_storage(c, s);
@@ -767,6 +768,13 @@ rkv_status rkv_sparse_attention(rkv_ctx* c, const float* q, int32_t n_q_heads, c
   return RKV_OK;
 }
 
+rkv_status rkv_pool_cache(rkv_ctx* c, void** ptr, size_t* bytes) {
+  if (!c || !ptr || !bytes) return fail(RKV_EINVAL, "NULL argument");
+  *ptr = c->pool_bf16;
+  *bytes = (size_t)c->d.B * c->d.R_cap * c->d.dkv * 2;
+  return RKV_OK;
+}
+
 rkv_status rkv_reset(rkv_ctx* c, int32_t seq, void* stream) {
   if (!c) return fail(RKV_EINVAL, "ctx is NULL");
   if (seq < -1 || seq >= c->d.B) return fail(RKV_EINVAL, "seq %d out of range", seq);
@@ -793,6 +801,7 @@ rkv_status rkv_get_status(rkv_ctx* c, int32_t* flags, void* stream) {
 
 void rkv_free(rkv_ctx* c) {
   if (!c) return;
+  cudaFree(c->pool_bf16);
   cudaFree(c->w12);
   cudaFree(c->attn_ws);
   cudaFree(c->attn_count);

@@ -75,6 +75,8 @@ struct rkv_ctx {
   int tiles_cap = 0;
 
   // library-owned device memory
+  __nv_bfloat16* pool_bf16 = nullptr;  // [B, R_cap, 2d_k] bf16 copy of the FP8 pool (retrieval
+                                       // operand, kept in step by pool_append)
   __nv_bfloat16* w12 = nullptr;   // [2 d_ff, 2d_k]: per 256-row tile, 128 W_c1^T rows then 128 W_c2^T rows
   __nv_bfloat16* w3 = nullptr;    // [d_c, d_ff] = W_c3^T
   __nv_bfloat16* wd = nullptr;    // [2d_k, d_c] = W_d^T

@@ -41,8 +41,8 @@ def test_storage_bytes_and_config_validation(built):
     cfg = rkv.Config(n_kv_heads=8, head_dim=128, d_c=512, d_ff=1536, bits=4, ref_stride=16,
                      max_tokens=32768)
     s = rkv.storage_bytes(cfg)
-    assert s[0] == 2048 * 2048 and s[1] == 2048 * 2048 * 2
-    assert s[4] == 32768 * 256 and s[5] == 32768 * 16 * 4 and s[6] == 32768 * 4 * 4
+    assert len(s) == 6 and s[0] == 2048 * 2048 and s[1] == 2048 * 4 and s[2] == 2048 * 4
+    assert s[3] == 32768 * 256 and s[4] == 32768 * 16 * 4 and s[5] == 32768 * 4 * 4
     for bad in (dict(head_dim=96), dict(d_c=100), dict(d_c=576), dict(bits=3), dict(topk=5), dict(d_ff=200),
                 dict(group=16), dict(max_refs=10), dict(ref_alpha=-0.1), dict(ref_sink=-1),
                 dict(ref_alpha=float("nan")), dict(ref_alpha=0.02, ref_sink=4, max_refs=100)):

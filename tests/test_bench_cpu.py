@@ -121,24 +121,28 @@ def test_code_hash_ignores_comments_only(tmp_path):
 
 def test_storage_report_of_the_llama8b_layer():
     """codes 256 + extremes 64 + slots 16 B per token, FP8 pool 2048 B per reference (one
-    token in 16) plus its bf16 shadow and 8 B of norm and position per slot."""
+    token in 16) with 8 B of norm and position per slot; the library's bf16 copy of the
+    pool (4096 B per reference) shown beside it."""
     import torch
     w = synth.workload("llama8b")
     B, T, R = 1, w.T, w.T // 16
 
     class _Codec:
         pool_fp8 = torch.empty((B, R, w.d_kv), dtype=torch.uint8)
-        pool_bf16 = torch.empty((B, R, w.d_kv), dtype=torch.bfloat16)
         pool_norm2 = torch.empty((B, R), dtype=torch.float32)
         pool_pos = torch.empty((B, R), dtype=torch.int32)
         codes = torch.empty((B, T, 256), dtype=torch.uint8)
         meta = torch.empty((B, T, 16, 2), dtype=torch.float16)
         ref_idx = torch.empty((B, T, 4), dtype=torch.int32)
 
+        def pool_cache_bytes(self):
+            return B * R * w.d_kv * 2
+
     rep = bench.storage_report(_Codec(), w)
-    per_tok = 256 + 64 + 16 + (2048 + 4096 + 8) / 16
+    per_tok = 256 + 64 + 16 + (2048 + 8) / 16
     assert rep["bytes_per_token"] == round(per_tok, 1)
-    assert rep["fraction_of_fp16_kv"] == round(per_tok / 4096, 4)
-    # without the shadow: the page's INT4 formula with the slots added (11.33 %), plus the
-    # 8-byte norm and position of each pool slot
-    assert rep["fraction_without_pool_shadow"] == round((256 + 64 + 16 + 2056 / 16) / 4096, 4) == 0.1134
+    # the page's INT4 formula with the slots added (11.33 %), plus the 8-byte norm and
+    # position of each pool slot
+    assert rep["fraction_of_fp16_kv"] == round(per_tok / 4096, 4) == 0.1134
+    assert rep["compute_cache_bytes_per_token"] == 256.0
+    assert rep["fraction_with_compute_cache"] == round((per_tok + 256) / 4096, 4)
