@@ -20,10 +20,9 @@
 // sectors and the other the y sectors, and meet at a named barrier per reference.  Each
 // epilogue thread then sums its row's references (exact in fp32), adds the sum / k_i to
 // its accumulator row (one fma for k_i = 1, 2, 4, where the scaling is exact; the
-// correctly rounded s / 3 for k_i = 3), rotates the K columns and writes its 16 + 16 K
-// or V values into its warp's two shared-memory boxes (32 rows x 16 columns each),
-// which one lane of the warp stores by TMA; the tensor map clips the rows past the
-// selection.
+// correctly rounded s / 3 for k_i = 3), rotates the K columns and stores its 16 + 16 K
+// or V values straight from registers, one 32-byte store per 16 bf16 values (a whole
+// sector of the row); rows past the selection are not stored.
 //
 // Back-to-back launches overlap: every CTA lets the next launch of the stream start its
 // CTAs as SMs free up, and a thread waits for the previous grid to complete only before
@@ -48,7 +47,6 @@ namespace {
 // cap a thread at 96 registers.
 constexpr int kReconThreads = 640;
 constexpr int kEpiWarpR = 4;                 // first epilogue warp
-constexpr int kEpiWarps = 16;
 constexpr int kNT = 128;                     // output columns per unit
 constexpr uint32_t kBBytes = kNT * 128;      // one 64-wide k-block of W_d^T rows
 constexpr uint32_t kPlaneBytes = kTileM * 32;            // one 32-byte sector per tile row
@@ -84,6 +82,13 @@ struct ReconArgs {
   int B, T_cap, R_cap, topk, dkv, dk, dc, D, G, bits, code_bytes;
   int* status;
 };
+
+// One 32-byte store (eight 32-bit words) to a 32-byte aligned global address.
+__device__ __forceinline__ void st_global_v8(void* p, const uint32_t* w) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(p), "r"(w[0]),
+               "r"(w[1]), "r"(w[2]), "r"(w[3]), "r"(w[4]), "r"(w[5]), "r"(w[6]), "r"(w[7])
+               : "memory");
+}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   __nv_bfloat16 lo = __float2bfloat16_rn(a), hi = __float2bfloat16_rn(b);
@@ -273,17 +278,14 @@ __device__ __forceinline__ int range_start(int b, int grid, int units, int n_til
 }
 
 __global__ void __launch_bounds__(kReconThreads, 1)
-    reconstruct_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmK,
-                       const __grid_constant__ CUtensorMap tmV, const __grid_constant__ ReconArgs a) {
+    reconstruct_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ ReconArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int nkb = a.dc / kTileK;
   uint8_t* sB = smem;                                       // b_stages x W_d^T k-block
   uint8_t* sG = sB + a.b_stages * kBBytes;                  // per-warp reference slots
   float4* sCS = reinterpret_cast<float4*>(sG + kGBytes);
-  const uint32_t ob = a.out_f32 ? 64u : 32u;                // bytes of one output box row
-  uint8_t* sO = reinterpret_cast<uint8_t*>(sCS) + kCSBytes; // per-warp output boxes
-  uint64_t* full = reinterpret_cast<uint64_t*>(sO + kEpiWarps * 2 * 32 * ob);
+  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sCS) + kCSBytes);
   uint64_t* empty = full + a.b_stages;
   uint64_t* tfull = empty + a.b_stages;
   uint64_t* tempty = tfull + 2;
@@ -311,8 +313,6 @@ __global__ void __launch_bounds__(kReconThreads, 1)
     *abort_flag = 0;
     fence_barrier_init();
     tma_prefetch(&tmW);
-    tma_prefetch(&tmK);
-    tma_prefetch(&tmV);
   }
   if (warp == 0) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -593,58 +593,37 @@ __global__ void __launch_bounds__(kReconThreads, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i) mx[i] = 0.f, my[i] = 0.f;
       }
-      // ---- output: stage this warp's two boxes, then one lane stores them by TMA (rows
-      // past the selection are clipped by the tensor map)
-      if (lane_id() == 0) bulk_wait_read0();           // the previous boxes have been read
-      __syncwarp();
-      // this warp's boxes (32 rows x 16 columns of x, then of y); lane r writes box row r,
-      // its 16-byte chunk c at chunk c ^ (bits of r), the tensor map's swizzle
-      uint8_t* so = sO + (uint32_t)(warp - kEpiWarpR) * (2 * 32 * ob);
-      const uint32_t so_row = (uint32_t)lane_id() * ob;
-      const uint32_t so_sw = a.out_f32 ? ((lane_id() >> 1) & 3u) : ((lane_id() >> 2) & 1u);
-      if (a.out_f32) {
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint32_t off = so_row + (((uint32_t)c ^ so_sw) << 4);
-          *reinterpret_cast<float4*>(so + off) =
-              make_float4(mx[4 * c], mx[4 * c + 1], mx[4 * c + 2], mx[4 * c + 3]);
-          *reinterpret_cast<float4*>(so + 32 * ob + off) =
-              make_float4(my[4 * c], my[4 * c + 1], my[4 * c + 2], my[4 * c + 3]);
-        }
-      } else {
-#pragma unroll
-        for (int c = 0; c < 2; ++c) {
-          const uint32_t off = so_row + (((uint32_t)c ^ so_sw) << 4);
-          uint4 vx, vy;
-          vx.x = pack_bf16x2(mx[8 * c], mx[8 * c + 1]);
-          vx.y = pack_bf16x2(mx[8 * c + 2], mx[8 * c + 3]);
-          vx.z = pack_bf16x2(mx[8 * c + 4], mx[8 * c + 5]);
-          vx.w = pack_bf16x2(mx[8 * c + 6], mx[8 * c + 7]);
-          vy.x = pack_bf16x2(my[8 * c], my[8 * c + 1]);
-          vy.y = pack_bf16x2(my[8 * c + 2], my[8 * c + 3]);
-          vy.z = pack_bf16x2(my[8 * c + 4], my[8 * c + 5]);
-          vy.w = pack_bf16x2(my[8 * c + 6], my[8 * c + 7]);
-          *reinterpret_cast<uint4*>(so + off) = vx;
-          *reinterpret_cast<uint4*>(so + 32 * ob + off) = vy;
-        }
+      // ---- output: 32-byte stores straight from registers (the row's 16 x values, then
+      // its 16 y values); K/V may be the previous launch's outputs, so each thread waits
+      // for the previous grid before its first store
+      if (!waited) {
+        pdl_wait_previous_grid();
+        waited = true;
       }
-      fence_proxy_async_smem();
-      __syncwarp();
-      const int y0 = m * kTileM + ew * 32;
-      if (lane_id() == 0 && y0 < a.n_sel) {
-        if (!waited) {
-          pdl_wait_previous_grid();                    // K/V may be the previous launch's outputs
-          waited = true;
+      const int64_t grow = (int64_t)m * kTileM + row;
+      if (grow < a.n_sel) {
+        const int64_t o0 = grow * a.dk + (is_k ? c0 : c0 - a.dk) + j0;
+        void* base = is_k ? a.k_out : a.v_out;
+        if (a.out_f32) {
+          float* o = static_cast<float*>(base) + o0;
+          st_global_v8(o, reinterpret_cast<const uint32_t*>(mx));
+          st_global_v8(o + 8, reinterpret_cast<const uint32_t*>(mx + 8));
+          st_global_v8(o + P, reinterpret_cast<const uint32_t*>(my));
+          st_global_v8(o + P + 8, reinterpret_cast<const uint32_t*>(my + 8));
+        } else {
+          uint32_t wx[8], wy[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            wx[i] = pack_bf16x2(mx[2 * i], mx[2 * i + 1]);
+            wy[i] = pack_bf16x2(my[2 * i], my[2 * i + 1]);
+          }
+          __nv_bfloat16* o = static_cast<__nv_bfloat16*>(base) + o0;
+          st_global_v8(o, wx);
+          st_global_v8(o + P, wy);
         }
-        const CUtensorMap* om = is_k ? &tmK : &tmV;
-        const int x0 = (is_k ? c0 : c0 - a.dk) + j0;
-        tma_store_2d(om, so, x0, y0);
-        tma_store_2d(om, so + 32 * ob, x0 + P, y0);
-        bulk_commit();
       }
     }
     cp_async_wait<0>();                                // no copy may outlive the CTA
-    if (lane_id() == 0) bulk_wait0();                  // nor any output store
   }
 
   tc_fence_before();
@@ -661,15 +640,18 @@ cudaError_t launch_reconstruct(rkv_ctx* c, const int32_t* seq, const int32_t* po
                                void* k_out, void* v_out, cudaStream_t s) {
   const Dims& d = c->d;
   if (n_sel <= 0) return cudaSuccess;
-  const size_t obytes = (size_t)kEpiWarps * 2 * 32 * (d.out_f32 ? 64 : 32);
-  const size_t fixed = 1024 + kCSBytes + kGBytes + obytes + kBarBytes;
+  const size_t fixed = 1024 + kCSBytes + kGBytes + kBarBytes;
   int b_stages = (int)((232448 - fixed) / kBBytes);
   if (b_stages > kMaxStages) b_stages = kMaxStages;
   if (b_stages < 2) return cudaErrorInvalidConfiguration;
   const size_t smem = fixed + (size_t)b_stages * kBBytes;
-  cudaError_t e = cudaFuncSetAttribute(reconstruct_kernel,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
+  // the kernel's shared-memory limit is raised once per context (on its device)
+  cudaError_t e = cudaSuccess;
+  if (c->recon_smem < (int)smem) {
+    e = cudaFuncSetAttribute(reconstruct_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    c->recon_smem = (int)smem;
+  }
   ReconArgs a;
   a.seq = seq;
   a.pos = pos;
@@ -699,10 +681,6 @@ cudaError_t launch_reconstruct(rkv_ctx* c, const int32_t* seq, const int32_t* po
   a.bits = d.bits;
   a.code_bytes = d.code_bytes;
   a.status = c->status;
-  CUtensorMap tmK, tmV;
-  if (!make_out_map(&tmK, k_out, d.dk, n_sel, d.out_f32) ||
-      !make_out_map(&tmV, v_out, d.dk, n_sel, d.out_f32))
-    return cudaErrorInvalidValue;
   const int grid = a.units < c->num_sms ? a.units : c->num_sms;
   cudaEvent_t ev;
   timing_begin(c, "rkv_reconstruct_kernel", s, &ev);
@@ -716,7 +694,7 @@ cudaError_t launch_reconstruct(rkv_ctx* c, const int32_t* seq, const int32_t* po
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  e = cudaLaunchKernelEx(&lc, reconstruct_kernel, c->tm_wd, tmK, tmV, a);
+  e = cudaLaunchKernelEx(&lc, reconstruct_kernel, c->tm_wd, a);
   if (e == cudaSuccess) e = cudaGetLastError();
   timing_end(c, "rkv_reconstruct_kernel", s, ev);
   return e;

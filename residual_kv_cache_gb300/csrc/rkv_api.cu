@@ -163,19 +163,6 @@ namespace rkv {
 
 void set_error(const char* msg) { g_err = msg ? msg : ""; }
 
-bool make_out_map(CUtensorMap* m, void* base, int64_t cols, int64_t rows, bool f32) {
-  const uint32_t es = f32 ? 4u : 2u;
-  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)cols * es};
-  cuuint32_t box[2] = {16u, 32u};
-  cuuint32_t estr[2] = {1u, 1u};
-  CUresult r = g_encode(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                        2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        f32 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_32B,
-                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  return r == CUDA_SUCCESS;
-}
-
 void timing_begin(rkv_ctx* c, const char* name, cudaStream_t s, cudaEvent_t* start) {
   c->launches++;
   *start = nullptr;

@@ -70,6 +70,7 @@ struct rkv_ctx {
   rkv_storage st;
   int device = 0;
   int num_sms = 0;
+  int recon_smem = 0;          // dynamic shared memory the restore kernel is set up for
   int max_rows = 0;    // compact rows per pass
   int m_cap = 0;       // retrieval-order rows per pass (with padding)
   int tiles_cap = 0;
@@ -156,7 +157,6 @@ cudaError_t launch_attention(rkv_ctx* c, const float* q, int n_q_heads, const vo
 // Tensor map of a row-major [rows, cols] output matrix (bf16 or fp32) for 2-D tiled
 // stores: box = {16 columns, 32 rows}, swizzled over the box's row bytes (32 or 64), so
 // that a warp writing one box row per lane in 16-byte chunks hits distinct banks.
-bool make_out_map(CUtensorMap* m, void* base, int64_t cols, int64_t rows, bool f32);
 
 // Record the message rkv_last_error returns on this thread.
 void set_error(const char* msg);
