@@ -5,11 +5,15 @@
 //
 // Work unit = (tile of 128 selected tokens, 128 output columns = one head for D = 128,
 // two for D = 64).  A CTA owns a contiguous range of units, so consecutive units share
-// the token tile.  Per token tile, the 512 epilogue threads (four warpgroups; the
+// the token tile.  Two loader warps stage each later token tile of the range in shared
+// memory while the previous tile is restored: per row its record (validity, k_i,
+// position, pool rows of its references), its extremes and, for code rows of at most
+// 128 bytes, its codes.  Per token tile, the 512 epilogue threads (four warpgroups; the
 // threads of TMEM lane r own token row r):
 //   1. dequantise the row's codes in fp32 (z~ = q * Delta + min, Delta = (max - min) /
 //      (2^b - 1)) and store bf16 z~ straight into tensor memory, where the tensor core
-//      reads the A operand (two bf16 per 32-bit column);
+//      reads the A operand (two bf16 per 32-bit column); with d_c <= 256 z~ has two
+//      buffers, so the next tile's goes in while the tensor core still reads this one's;
 //   2. build the row's RoPE cos/sin for its 16 column pairs (float64-built two-level
 //      tables, angle addition in fp32) into shared memory.
 // Per unit, a TMA ring streams W_d^T tiles (the B operand) and one thread issues
@@ -26,14 +30,14 @@
 //
 // Back-to-back launches overlap: every CTA lets the next launch of the stream start its
 // CTAs as SMs free up, and a thread waits for the previous grid to complete only before
-// its first output store, so one launch's setup (dependent loads of selections, slots
-// and codes, dequantisation) hides behind the previous launch's last CTAs.  Nothing else
-// this kernel reads is written by it.
+// its first output store, so one launch's first-tile setup (dependent loads of
+// selections, slots and codes, dequantisation) hides behind the previous launch's last
+// CTAs.  Nothing else this kernel reads is written by it.
 //
-// Per unit an SM pulls 128 KB of W_d^T and up to 64 KB of reference rows from L2; the
-// tensor core finishes a unit's MMAs well within the epilogue's time, so the kernel is
-// bound by the epilogue's dependent chains and the per-tile setup, not by the tensor
-// core or by HBM.
+// Per unit an SM pulls 256 d_c bytes of W_d^T and up to 64 KB of reference rows from L2;
+// the tensor core finishes a unit's MMAs well within the epilogue's time, so the kernel
+// is bound by the epilogue's dependent chains and the first tile's setup, not by the
+// tensor core or by HBM.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -42,7 +46,7 @@
 namespace rkv {
 namespace {
 
-// 20 warps: 0 TMEM + W_d^T producer, 1 MMA, 2..3 idle, 4..19 epilogue.
+// 20 warps: 0 TMEM + W_d^T producer, 1 MMA, 2..3 loaders, 4..19 epilogue.
 // The register file is split over the four SM sub-partitions, so 18 or 20 warps both
 // cap a thread at 96 registers.
 constexpr int kReconThreads = 640;
@@ -53,6 +57,8 @@ constexpr uint32_t kPlaneBytes = kTileM * 32;            // one 32-byte sector p
 constexpr uint32_t kGBytes = 2 * 4 * 2 * kPlaneBytes;    // [group pair][ref][x|y] planes
 constexpr uint32_t kCSBytes = 4 * 8 * kTileM * 16;   // cos/sin: 4 groups x 8 float4 x 128 rows
 constexpr uint32_t kBarBytes = 512;
+constexpr int kRecInts = 8;                  // staged row record: flags, pos, pool rows 0..3, seq
+constexpr int kLoadWarp0 = 2;                // warps 2..3 stage the CTA's later tiles
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kACol = 2 * kNT;          // z~ after the two accumulators
 constexpr int kMaxStages = 8;
@@ -80,6 +86,9 @@ struct ReconArgs {
   void* v_out;
   int out_f32;
   int B, T_cap, R_cap, topk, dkv, dk, dc, D, G, bits, code_bytes;
+  int zbufs;          // z~ buffers in TMEM: 2 when d_c <= 256, else 1
+  int stage_codes;    // later tiles' codes are staged in shared memory (code_bytes <= 256)
+  int chunk_mask;     // swizzle of a staged code row's 16-byte chunks: chunk c ^ (row & mask)
   int* status;
 };
 
@@ -103,6 +112,53 @@ __device__ __forceinline__ void fp8x16_add(uint4 v, float* s) {
   fp8x4_add(v.y, s[4], s[5], s[6], s[7]);
   fp8x4_add(v.z, s[8], s[9], s[10], s[11]);
   fp8x4_add(v.w, s[12], s[13], s[14], s[15]);
+}
+
+// z~ = q * Delta + min of code groups g0 .. g0 + g_per - 1 (at most four) of one row into
+// TMEM at zaddr + 16 g; mt[i] holds the group's (min, max) as two f16, cw[i] its packed
+// codes.  An invalid row decodes to zeros.
+__device__ __forceinline__ void dequant_groups(const ReconArgs& a, bool valid, const uint32_t* mt,
+                                               const uint4* cw, int g0, int g_per, uint32_t zaddr) {
+  // Codes become floats without integer-to-float conversions: a code q placed in the
+  // low mantissa bits under the exponent of 2^23 reads as the float 2^23 + q exactly,
+  // and one subtraction leaves q.  z~ = RN(RN(q * Delta) + min), two columns at a time.
+  const int levels = (1 << a.bits) - 1;
+  const uint64_t two23 = f32x2_pack(8388608.0f, 8388608.0f);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (i >= g_per) break;
+    const int g = g0 + i;
+    float lo = __half2float(__ushort_as_half((unsigned short)(mt[i] & 0xFFFFu)));
+    const float hi = __half2float(__ushort_as_half((unsigned short)(mt[i] >> 16)));
+    float delta = __fdiv_rn(__fsub_rn(hi, lo), (float)levels);
+    if (!valid) lo = 0.f, delta = 0.f;              // an invalid row decodes to zeros
+    const uint64_t dd = f32x2_pack(delta, delta);
+    const uint32_t w4[4] = {cw[i].x, cw[i].y, cw[i].z, cw[i].w};
+    uint32_t o[16];
+#pragma unroll
+    for (int e = 0; e < 16; ++e) {
+      uint32_t t0, t1;                               // 2^23 + q of coordinates 2e, 2e + 1
+      if (a.bits == 4) {
+        // word e/4 holds coordinates 8 (e/4) + n in nibble n: the even nibbles of a
+        // word are its bytes' low halves, the odd nibbles their high halves
+        const uint32_t w = w4[e >> 2];
+        const uint32_t sel = 0x7650u + (uint32_t)(e & 3);
+        t0 = __byte_perm(w & 0x0F0F0F0Fu, 0x4B000000u, sel);
+        t1 = __byte_perm((w >> 4) & 0x0F0F0F0Fu, 0x4B000000u, sel);
+      } else {
+        const int k = 2 * e;
+        t0 = ((w4[k >> 4] >> (2 * (k & 15))) & 3u) | 0x4B000000u;
+        t1 = ((w4[k >> 4] >> (2 * (k & 15) + 2)) & 3u) | 0x4B000000u;
+      }
+      const uint64_t q = f32x2_sub(f32x2_pack(__uint_as_float(t0), __uint_as_float(t1)), two23);
+      // the addition stays scalar: ptxas contracts a packed multiply followed by a
+      // packed add into one fused multiply-add, which rounds once instead of twice
+      float m0, m1;
+      f32x2_unpack(f32x2_mul(q, dd), m0, m1);
+      o[e] = pack_bf16x2(__fadd_rn(m0, lo), __fadd_rn(m1, lo));
+    }
+    tmem_st16(zaddr + 16u * (uint32_t)g, o);
+  }
 }
 
 // Per-tile state of one epilogue thread's token row, packed into two registers.
@@ -218,49 +274,72 @@ __device__ __forceinline__ TileRow tile_setup(const ReconArgs& a, int m, int row
       tmem_st16(zaddr + 16u * (uint32_t)g, o);
     }
   } else {
-    // Codes become floats without integer-to-float conversions: a code q placed in the
-    // low mantissa bits under the exponent of 2^23 reads as the float 2^23 + q exactly,
-    // and one subtraction leaves q.  z~ = RN(RN(q * Delta) + min), two columns at a time.
-    const int levels = (1 << a.bits) - 1;
-    const uint64_t two23 = f32x2_pack(8388608.0f, 8388608.0f);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      if (i >= g_per) break;
-      const int g = g0 + i;
-      float lo = __half2float(__ushort_as_half((unsigned short)(mt[i] & 0xFFFFu)));
-      const float hi = __half2float(__ushort_as_half((unsigned short)(mt[i] >> 16)));
-      float delta = __fdiv_rn(__fsub_rn(hi, lo), (float)levels);
-      if (!valid) lo = 0.f, delta = 0.f;              // an invalid row decodes to zeros
-      const uint64_t dd = f32x2_pack(delta, delta);
-      const uint32_t w4[4] = {cw[i].x, cw[i].y, cw[i].z, cw[i].w};
-      uint32_t o[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) {
-        uint32_t t0, t1;                               // 2^23 + q of coordinates 2e, 2e + 1
-        if (a.bits == 4) {
-          // word e/4 holds coordinates 8 (e/4) + n in nibble n: the even nibbles of a
-          // word are its bytes' low halves, the odd nibbles their high halves
-          const uint32_t w = w4[e >> 2];
-          const uint32_t sel = 0x7650u + (uint32_t)(e & 3);
-          t0 = __byte_perm(w & 0x0F0F0F0Fu, 0x4B000000u, sel);
-          t1 = __byte_perm((w >> 4) & 0x0F0F0F0Fu, 0x4B000000u, sel);
-        } else {
-          const int k = 2 * e;
-          t0 = ((w4[k >> 4] >> (2 * (k & 15))) & 3u) | 0x4B000000u;
-          t1 = ((w4[k >> 4] >> (2 * (k & 15) + 2)) & 3u) | 0x4B000000u;
-        }
-        const uint64_t q = f32x2_sub(f32x2_pack(__uint_as_float(t0), __uint_as_float(t1)), two23);
-        // the addition stays scalar: ptxas contracts a packed multiply followed by a
-        // packed add into one fused multiply-add, which rounds once instead of twice
-        float m0, m1;
-        f32x2_unpack(f32x2_mul(q, dd), m0, m1);
-        o[e] = pack_bf16x2(__fadd_rn(m0, lo), __fadd_rn(m1, lo));
-      }
-      tmem_st16(zaddr + 16u * (uint32_t)g, o);
-    }
+    dequant_groups(a, valid, mt, cw, g0, g_per, zaddr);
   }
   tmem_st_wait();
   return tr;
+}
+
+// Row `row` of token tile m staged for the epilogue by a loader thread: its record
+// (flags as in RowState, position, pool rows of references 0..3 or -1, sequence), its
+// extremes and, with a.stage_codes, its packed codes (16-byte chunks, chunk c stored at
+// c ^ (row & a.chunk_mask)).  Raises the device flags for bad selections.
+__device__ __forceinline__ void stage_row(const ReconArgs& a, int m, int row, int* rec,
+                                          uint32_t* smeta, uint8_t* scodes) {
+  const int64_t gi = (int64_t)m * kTileM + row;
+  const bool in_sel = gi < a.n_sel;
+  const int s_ = in_sel ? a.seq[gi] : -1;
+  const int p_ = in_sel ? a.pos[gi] : -1;
+  bool in_range = false;
+  int64_t dst = 0;
+  if (in_sel) {
+    if (s_ < 0 || s_ >= a.B || p_ < 0 || p_ >= a.T_cap) {
+      atomicOr(a.status, RKV_FLAG_BAD_INDEX);
+    } else {
+      in_range = true;
+      dst = (int64_t)s_ * a.T_cap + p_;
+    }
+  }
+  int32_t sl[4] = {-1, -1, -1, -1};
+  if (in_range) {
+#pragma unroll
+    for (int t = 0; t < 4; ++t)
+      if (t < a.topk) sl[t] = a.ref_idx[dst * a.topk + t];
+  }
+  int r[4] = {-1, -1, -1, -1};
+  int kcnt = 0;
+  if (in_range) {
+    if (sl[0] < 0) atomicOr(a.status, RKV_FLAG_UNWRITTEN);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      if (sl[t] >= a.R_cap) atomicOr(a.status, RKV_FLAG_BAD_SLOT);
+      if (sl[t] >= 0 && sl[t] < a.R_cap) {
+        r[t] = s_ * a.R_cap + sl[t];
+        ++kcnt;
+      }
+    }
+  }
+  const bool valid = in_range && r[0] >= 0 && kcnt > 0;
+  if (!valid) {
+    kcnt = 0;
+#pragma unroll
+    for (int t = 0; t < 4; ++t) r[t] = -1;
+  }
+  int flags = (valid ? 1 : 0) | (kcnt << 5);
+#pragma unroll
+  for (int t = 0; t < 4; ++t) flags |= (r[t] >= 0 ? 1 : 0) << (1 + t);
+  if (valid) {
+    if (a.bits != 16)
+      for (int g = 0; g < a.G; ++g) smeta[row * a.G + g] = a.meta[dst * a.G + g];
+    if (a.stage_codes) {
+      const uint8_t* crow = a.codes + dst * a.code_bytes;
+      uint8_t* srow = scodes + row * a.code_bytes;
+      for (int c = 0; c < a.code_bytes / 16; ++c)
+        cp_async16(srow + ((c ^ (row & a.chunk_mask)) << 4), crow + 16 * c);
+    }
+  }
+  reinterpret_cast<int4*>(rec)[0] = make_int4(flags, in_range ? p_ : 0, r[0], r[1]);
+  reinterpret_cast<int4*>(rec)[1] = make_int4(r[2], r[3], in_range ? s_ : 0, 0);
 }
 
 // First unit of CTA b's contiguous range (b = grid gives `units`).  The ranges split a
@@ -285,13 +364,19 @@ __global__ void __launch_bounds__(kReconThreads, 1)
   uint8_t* sB = smem;                                       // b_stages x W_d^T k-block
   uint8_t* sG = sB + a.b_stages * kBBytes;                  // per-warp reference slots
   float4* sCS = reinterpret_cast<float4*>(sG + kGBytes);
-  uint64_t* full = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(sCS) + kCSBytes);
+  int* sRec = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(sCS) + kCSBytes);  // staged tile
+  uint32_t* sMeta = reinterpret_cast<uint32_t*>(sRec + kTileM * kRecInts);
+  uint8_t* sCodes = reinterpret_cast<uint8_t*>(sMeta + kTileM * a.G);
+  uint64_t* full = reinterpret_cast<uint64_t*>(
+      sCodes + (a.stage_codes ? ((kTileM * a.code_bytes + 127) & ~127) : 0));
   uint64_t* empty = full + a.b_stages;
   uint64_t* tfull = empty + a.b_stages;
   uint64_t* tempty = tfull + 2;
   uint64_t* afull = tempty + 2;                             // z~ of a tile is in TMEM
   uint64_t* afree = afull + 1;                              // the MMAs of a tile are done
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(afree + 1);
+  uint64_t* staged = afree + 1;                             // the next tile is staged
+  uint64_t* sfree = staged + 1;                             // the staged tile has been read
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sfree + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -310,6 +395,8 @@ __global__ void __launch_bounds__(kReconThreads, 1)
     }
     mbar_init(afull, 16);
     mbar_init(afree, 1);
+    mbar_init(staged, 2 * 64);       // 64 loader threads: a plain and a copy-completion arrival
+    mbar_init(sfree, 16);
     *abort_flag = 0;
     fence_barrier_init();
     tma_prefetch(&tmW);
@@ -354,15 +441,19 @@ __global__ void __launch_bounds__(kReconThreads, 1)
       Ring ring;
       int acc = 0;
       uint32_t acc_phase = 0, a_phase = 0;
-      int cur_m = -1;
+      int cur_m = -1, tt = -1;
+      uint32_t zoff = 0;
       bool ok = true, any = false;
       int last_stage = 0;
       uint32_t last_phase = 0;
       for (int u = u_begin; u < u_end && ok; ++u) {
         const int m = u / a.n_tiles;
         if (m != cur_m) {
-          // the previous tile's z~ may be overwritten once its MMAs are done
-          if (cur_m >= 0) umma_commit(afree);
+          // with one z~ buffer, the previous tile's z~ may be overwritten once its MMAs
+          // are done
+          if (cur_m >= 0 && a.zbufs == 1) umma_commit(afree);
+          ++tt;
+          zoff = (uint32_t)((tt % a.zbufs) * (a.dc / 2));
           if (!mbar_wait(afull, a_phase, abort_flag, a.status)) {
             ok = false;
             break;
@@ -385,7 +476,7 @@ __global__ void __launch_bounds__(kReconThreads, 1)
           const uint32_t b0 = smem_u32(sB + ring.stage * kBBytes);
 #pragma unroll
           for (int k = 0; k < kTileK / 16; ++k)
-            umma_bf16_ta(d, tmem + kACol + (uint32_t)(kb * (kTileK / 2) + k * 8),
+            umma_bf16_ta(d, tmem + kACol + zoff + (uint32_t)(kb * (kTileK / 2) + k * 8),
                          sdesc_sw128(b0 + k * 32), idesc, (kb | k) != 0 ? 1u : 0u);
           umma_commit(&empty[ring.stage]);
           any = true;
@@ -402,7 +493,27 @@ __global__ void __launch_bounds__(kReconThreads, 1)
       }
       if (!ok && any) drain_wait(&empty[last_stage], last_phase);
     }
-  } else if (warp >= kEpiWarpR) {
+  } else if (warp < kEpiWarpR) {
+    // ------------------------------------------------ loaders: the CTA's later tiles
+    // (records, extremes, codes) staged in shared memory one tile ahead, so that a tile
+    // change costs the epilogue no global round trip
+    const int l = (int)threadIdx.x - 32 * kLoadWarp0;
+    if (u_begin < u_end) {
+      const int m_first = u_begin / a.n_tiles, m_last = (u_end - 1) / a.n_tiles;
+      uint32_t free_phase = 0;
+      for (int m = m_first + 1; m <= m_last; ++m) {
+        if (m > m_first + 1) {
+          if (!mbar_wait(sfree, free_phase, abort_flag, a.status)) break;
+          free_phase ^= 1u;
+        }
+        stage_row(a, m, l, sRec + l * kRecInts, sMeta, sCodes);
+        stage_row(a, m, l + 64, sRec + (l + 64) * kRecInts, sMeta, sCodes);
+        cp_async_arrive_noinc(staged);
+        mbar_arrive(staged);
+      }
+    }
+    cp_async_wait_all();                               // no copy may outlive the CTA
+  } else {
     // Four groups of four consecutive warps (warps 4..19).  Warp w reads TMEM lanes
     // [32 (w % 4), +32), so every group owns the same 128 rows; group g takes 16 of each
     // unit's 64 column pairs and a quarter of each row's code groups.
@@ -431,7 +542,7 @@ __global__ void __launch_bounds__(kReconThreads, 1)
     uint8_t* cp_dst0 = pslots + half * kPlaneBytes + (uint32_t)cp_r0 * 32 +
                        (uint32_t)(((cl & 1) ^ ((cp_r0 >> 2) & 1)) * 16);
     const uint8_t* cp_src0 = a.pool8 + (half ? xsec + P : xsec) + 16 * (cl & 1);
-    const uint32_t zaddr = tmem + lane_base + kACol;  // this thread's z~ columns
+    const uint32_t zaddr = tmem + lane_base + kACol;  // this thread's z~ columns (buffer 0)
     const int g0 = wg * a.G / 4;                     // this group's code groups [g0, g0+g_per)
     const int g_per = (wg + 1) * a.G / 4 - g0;
     float4* cs_row = sCS + wg * 8 * kTileM + row;    // entry i at cs_row[i * kTileM]
@@ -441,10 +552,7 @@ __global__ void __launch_bounds__(kReconThreads, 1)
     int cp0[4], cp1[4];                               // pool rows this lane copies (per tile)
     int nx_s = -1, nx_p = -1;                         // the row of the next tile
     auto setup_a = [&](int m) -> RowState {
-      const TileRow tr = tile_setup(a, m, row, wg, g0, g_per, zaddr, nx_s, nx_p,
-                                    (m + 1) * a.n_tiles < u_end);
-      nx_s = tr.nx_s;
-      nx_p = tr.nx_p;
+      const TileRow tr = tile_setup(a, m, row, wg, g0, g_per, zaddr, nx_s, nx_p, false);
       tc_fence_before();
       __syncwarp();
       if (lane_id() == 0) mbar_arrive(afull);
@@ -454,6 +562,75 @@ __global__ void __launch_bounds__(kReconThreads, 1)
         cp1[t] = __shfl_sync(0xffffffffu, tr.r[t], (cl >> 1) + 16);
       }
       return tr.st;
+    };
+
+    // z~ of the staged tile into z~ buffer zb (its previous tile's MMAs are done), the
+    // row state and this lane's copy rows from the records, then one arrival per warp on
+    // afull (the tensor core may start the tile) and on sfree (the loaders may restage).
+    uint32_t staged_phase = 0;
+    auto setup_s = [&](int zb, RowState& st) -> bool {
+      const bool w = mbar_wait(staged, staged_phase, abort_flag, a.status);
+      if (!__all_sync(0xffffffffu, w)) return false;
+      staged_phase ^= 1u;
+      const int* rec = sRec + row * kRecInts;
+      st.flags = rec[0];
+      st.pos = rec[1];
+      const bool valid = st.valid();
+      const uint32_t za = zaddr + (uint32_t)(zb * (a.dc / 2));
+      const uint8_t* srow = sCodes + row * a.code_bytes;
+      if (a.bits == 16) {
+        const uint8_t* crow = a.codes + ((int64_t)rec[6] * a.T_cap + rec[1]) * a.code_bytes;
+        for (int g = g0; g < g0 + g_per; ++g) {
+          uint32_t o[16];
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (valid)
+              v = a.stage_codes
+                      ? *reinterpret_cast<const uint4*>(srow + (((4 * g + q) ^ (row & a.chunk_mask)) << 4))
+                      : reinterpret_cast<const uint4*>(crow + (int64_t)g * 64)[q];
+            o[4 * q] = v.x, o[4 * q + 1] = v.y, o[4 * q + 2] = v.z, o[4 * q + 3] = v.w;
+          }
+          tmem_st16(za + 16u * (uint32_t)g, o);
+        }
+      } else {
+        const uint8_t* crow = a.codes + ((int64_t)rec[6] * a.T_cap + rec[1]) * a.code_bytes;
+        uint32_t mt[4] = {0u, 0u, 0u, 0u};
+        uint4 cw[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          cw[i] = make_uint4(0u, 0u, 0u, 0u);
+          if (i < g_per && valid) {
+            const int g = g0 + i;
+            mt[i] = sMeta[row * a.G + g];
+            if (a.bits == 4) {
+              cw[i] = a.stage_codes
+                          ? *reinterpret_cast<const uint4*>(srow + ((g ^ (row & a.chunk_mask)) << 4))
+                          : *reinterpret_cast<const uint4*>(crow + (int64_t)g * 16);
+            } else {
+              const uint2 v = a.stage_codes
+                                  ? *reinterpret_cast<const uint2*>(
+                                        srow + (((g >> 1) ^ (row & a.chunk_mask)) << 4) + 8 * (g & 1))
+                                  : *reinterpret_cast<const uint2*>(crow + (int64_t)g * 8);
+              cw[i] = make_uint4(v.x, v.y, 0u, 0u);
+            }
+          }
+        }
+        dequant_groups(a, valid, mt, cw, g0, g_per, za);
+      }
+      tmem_st_wait();
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        cp0[t] = sRec[cp_r0 * kRecInts + 2 + t];
+        cp1[t] = sRec[(cp_r0 + 16) * kRecInts + 2 + t];
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane_id() == 0) {
+        mbar_arrive(afull);
+        mbar_arrive(sfree);
+      }
+      return true;
     };
 
     // cos/sin of the row's 16 pairs at its own position, into shared memory
@@ -491,7 +668,7 @@ __global__ void __launch_bounds__(kReconThreads, 1)
     bool waited = false;                               // previous grid complete (first store)
     int acc = 0;
     uint32_t acc_phase = 0, afree_phase = 0;
-    int cur_m = -1;
+    int cur_m = -1, tt = 0;
     bool ok = true;
     for (int u = u_begin; u < u_end && ok; ++u) {
       const int m = u / a.n_tiles, n = u % a.n_tiles;
@@ -504,19 +681,23 @@ __global__ void __launch_bounds__(kReconThreads, 1)
 #pragma unroll
           for (int t = 0; t < 4; ++t) issue_ref(n, true, t);   // the first unit's copies
         } else {
-          cur = nxt;                                   // z~ already staged before the last unit
+          cur = nxt;                                   // z~ already set up before the last unit
+          ++tt;
         }
         cur_m = m;
         setup_cs(cur.pos);
       }
-      // Last unit of its tile: as soon as the tensor core is done with this tile, stage
-      // the next tile's z~ so the MMAs resume while this unit's epilogue runs; from here
-      // on every copy this thread issues is for the next tile.
+      // Last unit of its tile: set up the next tile (staged by the loaders) so the MMAs
+      // go on while this unit's epilogue runs; with one z~ buffer, once the tensor core
+      // is done with this tile.  From here on every copy this thread issues is for the
+      // next tile.
       if (u + 1 < u_end && (u + 1) / a.n_tiles != m) {
-        // both warps of the pair leave together, so neither waits at a barrier alone
-        if (!bar_red_and(bar_id, 64, warp_wait(afree, afree_phase, abort_flag, a.status))) break;
-        afree_phase ^= 1u;
-        nxt = setup_a(m + 1);
+        if (a.zbufs == 1) {
+          // both warps of the pair leave together, so neither waits at a barrier alone
+          if (!bar_red_and(bar_id, 64, warp_wait(afree, afree_phase, abort_flag, a.status))) break;
+          afree_phase ^= 1u;
+        }
+        if (!setup_s((tt + 1) % a.zbufs, nxt)) break;
       }
       const bool more = u + 1 < u_end;
       const int n_next = (u + 1) % a.n_tiles;
@@ -640,7 +821,11 @@ cudaError_t launch_reconstruct(rkv_ctx* c, const int32_t* seq, const int32_t* po
                                void* k_out, void* v_out, cudaStream_t s) {
   const Dims& d = c->d;
   if (n_sel <= 0) return cudaSuccess;
-  const size_t fixed = 1024 + kCSBytes + kGBytes + kBarBytes;
+  // staged tile: records, extremes and (rows of at most 128 bytes) codes
+  const bool stage_codes = d.code_bytes <= 128;
+  const size_t stage = (size_t)kTileM * kRecInts * 4 + (size_t)kTileM * d.G * 4 +
+                       (stage_codes ? (((size_t)kTileM * d.code_bytes + 127) & ~(size_t)127) : 0);
+  const size_t fixed = 1024 + kCSBytes + kGBytes + stage + kBarBytes;
   int b_stages = (int)((232448 - fixed) / kBBytes);
   if (b_stages > kMaxStages) b_stages = kMaxStages;
   if (b_stages < 2) return cudaErrorInvalidConfiguration;
@@ -680,6 +865,13 @@ cudaError_t launch_reconstruct(rkv_ctx* c, const int32_t* seq, const int32_t* po
   a.G = d.G;
   a.bits = d.bits;
   a.code_bytes = d.code_bytes;
+  a.zbufs = 2 * kNT + d.dc <= (int)kTmemCols ? 2 : 1;     // d_c / 2 TMEM columns per buffer
+  a.stage_codes = stage_codes ? 1 : 0;
+  {
+    const int chunks = d.code_bytes / 16;
+    const int low = chunks & -chunks;                         // largest power of two dividing it
+    a.chunk_mask = (low < 8 ? low : 8) - 1;
+  }
   a.status = c->status;
   const int grid = a.units < c->num_sms ? a.units : c->num_sms;
   cudaEvent_t ev;
