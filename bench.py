@@ -159,11 +159,11 @@ def algorithmic_work(w, n_comp: int, n_sel: int, ref_pos, T: int | None = None) 
 # while the kernel's code is unchanged since the capture (code_sha1 below).
 MEASURED_TRAFFIC = {
     ("llama8b", "rkv_reconstruct_kernel"): {"file": "k_reconstruct.cu",
-                                            "code_sha1": "f980f1e74b50975f308a34b51c121696924766e4",
-                                            "bytes": 10745344 + 168704},
+                                            "code_sha1": "04ba157c4bcef39262c86cfe863d8d5864d004bc",
+                                            "bytes": 10470400 + 86016},
     ("qwen7b", "rkv_reconstruct_kernel"): {"file": "k_reconstruct.cu",
-                                           "code_sha1": "f980f1e74b50975f308a34b51c121696924766e4",
-                                           "bytes": 16630016 + 26752512},
+                                           "code_sha1": "04ba157c4bcef39262c86cfe863d8d5864d004bc",
+                                           "bytes": 15946240 + 25549312},
     ("llama8b", "rkv_retrieve_kernel"): {"file": "k_retrieve.cu",
                                          "code_sha1": "2fa75553f0dcd7f3432ad5a4cd1c4c4a6af2d412",
                                          "bytes": 134557184 + 3536128},
