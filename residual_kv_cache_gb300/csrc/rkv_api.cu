@@ -147,11 +147,38 @@ int32_t* staging_acquire(rkv_ctx* c, int* which) {
   return c->plan_host[b];
 }
 
+// The device pulls a staged plan straight from the mapped pinned buffer with loads, so
+// that the upload never queues behind a large host-to-device transfer that the caller
+// runs on the copy engines at the same time (a copy-engine memcpy would).
+__global__ void stage_pull_kernel(const int32_t* __restrict__ src, int32_t* __restrict__ dst, int n) {
+  const int stride = gridDim.x * blockDim.x;
+  const int n4 = n >> 2;
+  const int4* s4 = reinterpret_cast<const int4*>(src);
+  int4* d4 = reinterpret_cast<int4*>(dst);
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n4; i += stride) d4[i] = s4[i];
+  for (int i = 4 * n4 + blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) dst[i] = src[i];
+}
+
 // Upload ints [first, first + n_ints) of staging buffer b; the buffer is free again once
 // the event recorded after its last upload has completed.
 cudaError_t staging_upload(rkv_ctx* c, int b, int first, int n_ints, cudaStream_t s) {
-  cudaError_t e = cudaMemcpyAsync(c->plan_dev[b] + first, c->plan_host[b] + first,
-                                  sizeof(int32_t) * n_ints, cudaMemcpyHostToDevice, s);
+  cudaError_t e = cudaSuccess;
+  if (n_ints <= 0) return cudaEventRecord(c->plan_copied[b], s);
+  if (c->plan_host_dev[b] != nullptr && (first & 3) == 0) {
+    // 16-byte aligned start (both buffers are): 256 threads per block, enough blocks
+    // for the size (at most one wave)
+    int blocks = (n_ints / 4 + 255) / 256;
+    if (blocks < 1) blocks = 1;
+    if (blocks > c->num_sms) blocks = c->num_sms;
+    cudaEvent_t ev;
+    timing_begin(c, "rkv_stage_pull_kernel", s, &ev);
+    stage_pull_kernel<<<blocks, 256, 0, s>>>(c->plan_host_dev[b] + first, c->plan_dev[b] + first, n_ints);
+    e = cudaGetLastError();
+    timing_end(c, "rkv_stage_pull_kernel", s, ev);
+  } else {
+    e = cudaMemcpyAsync(c->plan_dev[b] + first, c->plan_host[b] + first, sizeof(int32_t) * n_ints,
+                        cudaMemcpyHostToDevice, s);
+  }
   if (e != cudaSuccess) return e;
   return cudaEventRecord(c->plan_copied[b], s);
 }
@@ -431,11 +458,18 @@ rkv_status rkv_create(const rkv_config* cfg, const void* Wc1, const void* Wc2, c
   }
   for (int b = 0; b < 2; ++b) {
     if (cudaHostAlloc(reinterpret_cast<void**>(&c->plan_host[b]), (size_t)c->plan_ints * 4,
-                      cudaHostAllocDefault) != cudaSuccess ||
+                      cudaHostAllocMapped) != cudaSuccess ||
         cudaEventCreateWithFlags(&c->plan_copied[b], cudaEventDisableTiming) != cudaSuccess) {
       rkv_free(c);
       return fail(RKV_ECUDA, "pinned staging allocation failed");
     }
+    // the device-side address of the mapped buffer; without one, uploads use memcpy
+    void* dp = nullptr;
+    if (cudaHostGetDevicePointer(&dp, c->plan_host[b], 0) == cudaSuccess && dp != nullptr &&
+        (reinterpret_cast<uintptr_t>(dp) & 15u) == 0)
+      c->plan_host_dev[b] = static_cast<const int32_t*>(dp);
+    else
+      cudaGetLastError();
   }
 
   // RoPE tables in float64, rounded once to fp32: (cos, sin) of l*theta_j and of

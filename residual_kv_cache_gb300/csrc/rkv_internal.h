@@ -97,6 +97,7 @@ struct rkv_ctx {
   int units_cap = 0;
   int32_t* plan_dev[2] = {nullptr, nullptr};
   int32_t* plan_host[2] = {nullptr, nullptr};   // pinned staging
+  const int32_t* plan_host_dev[2] = {nullptr, nullptr};   // its device-side address (mapped)
   cudaEvent_t plan_copied[2] = {nullptr, nullptr};
   int plan_ints = 0;
   int plan_flip = 0;
