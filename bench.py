@@ -452,9 +452,11 @@ class StackRun:
     def e2e(self):
         """Public-API path with host buffers: every step uploads its inputs (every layer's
         kv rows and every selection, from pinned host memory) and reads back the last
-        restore's K and V.  Copies run on a second stream and are double-buffered, so a
-        step's upload overlaps the previous step's compute; all K steps, their uploads and
-        their read-backs lie inside one timed interval."""
+        restore's K and V.  Copies run on a second stream, double-buffered: the next step's
+        kv rows go up while this step's write phase runs (their buffer was last read by the
+        previous step's write phase), its selections once the previous step's restores
+        are done, and a step's results come back while the next step computes; all K
+        steps, their uploads and their read-backs lie inside one timed interval."""
         import torch
         ctx, w = self.ctx, self.w
         dev, stream = ctx.dev, ctx.stream
@@ -468,29 +470,39 @@ class StackRun:
         v_host = torch.empty_like(k_host).pin_memory()
         copy = torch.cuda.Stream(dev)
         uploaded = [torch.cuda.Event() for _ in range(2)]
-        inputs_free = [torch.cuda.Event() for _ in range(2)]
+        kv_free = [torch.cuda.Event() for _ in range(2)]
+        sel_free = [torch.cuda.Event() for _ in range(2)]
         result_ready = [torch.cuda.Event() for _ in range(2)]
         result_read = [torch.cuda.Event() for _ in range(2)]
         for b in range(2):
-            inputs_free[b].record(stream)
+            kv_free[b].record(stream)
+            sel_free[b].record(stream)
             result_read[b].record(stream)
 
-        def upload(i):
+        def upload(i, write_start):
             b = i % 2
             with torch.cuda.stream(copy):
-                copy.wait_event(inputs_free[b])
+                copy.wait_event(kv_free[b])
+                if write_start is not None:
+                    copy.wait_event(write_start)
                 for dst, src in zip(kv_buf[b], kv_host):
                     dst.copy_(src, non_blocking=True)
+                copy.wait_event(sel_free[b])
                 sel_buf[b].copy_(sel_host, non_blocking=True)
                 uploaded[b].record(copy)
 
-        def step(i):
+        def step(i, n):
             b = i % 2
             stream.wait_event(uploaded[b])
             stream.wait_event(result_read[b])
+            write_start = torch.cuda.Event()
+            write_start.record(stream)
+            if i + 1 < n:
+                upload(i + 1, write_start)
             self.write(kv_buf[b])
+            kv_free[b].record(stream)
             self.read(sel_buf[b], k_dev[b], v_dev[b])
-            inputs_free[b].record(stream)
+            sel_free[b].record(stream)
             result_ready[b].record(stream)
             with torch.cuda.stream(copy):
                 copy.wait_event(result_ready[b])
@@ -499,11 +511,9 @@ class StackRun:
                 result_read[b].record(copy)
 
         def run(n):
-            upload(0)
+            upload(0, None)
             for i in range(n):
-                if i + 1 < n:
-                    upload(i + 1)
-                step(i)
+                step(i, n)
             torch.cuda.synchronize(dev)
 
         run(max(1, ctx.args.warmup))
@@ -519,8 +529,8 @@ class StackRun:
                 "copies": "in: every layer's kv rows and every selection of the step; out: the "
                           "K and V of the step's last restore (the other restores' K/V stay on "
                           "the device, where attention would read them); second stream, "
-                          "double-buffered, so a step's upload overlaps the previous step's "
-                          "compute"}
+                          "double-buffered: the next step's kv rows go up during this step's "
+                          "write phase, results come back during the next step"}
 
 
 class BatchedRun:
