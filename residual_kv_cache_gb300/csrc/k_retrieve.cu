@@ -83,6 +83,29 @@ __device__ __forceinline__ void topk_insert(float d, int j, float* bd, int* bj) 
   }
 }
 
+// The same insertion without branches: (d, j) goes in at the first place k where
+// d < bd[k] (strict, so an equal score keeps the earlier, smaller slot), the entries from
+// k on move down one, and the last falls out; nothing changes when d >= bd[3].  The four
+// compares and the selects run on every lane alike, so a warp whose lanes insert at
+// different places (or not at all) never splits.
+__device__ __forceinline__ void topk_insert_nb(float d, int j, float* bd, int* bj) {
+  const bool c0 = d < bd[0], c1 = d < bd[1], c2 = d < bd[2], c3 = d < bd[3];
+  const float n3 = c2 ? bd[2] : (c3 ? d : bd[3]);
+  const int m3 = c2 ? bj[2] : (c3 ? j : bj[3]);
+  const float n2 = c1 ? bd[1] : (c2 ? d : bd[2]);
+  const int m2 = c1 ? bj[1] : (c2 ? j : bj[2]);
+  const float n1 = c0 ? bd[0] : (c1 ? d : bd[1]);
+  const int m1 = c0 ? bj[0] : (c1 ? j : bj[1]);
+  bd[0] = c0 ? d : bd[0];
+  bj[0] = c0 ? j : bj[0];
+  bd[1] = n1;
+  bj[1] = m1;
+  bd[2] = n2;
+  bj[2] = m2;
+  bd[3] = n3;
+  bj[3] = m3;
+}
+
 __global__ void __launch_bounds__(kRetrThreads, 1)
     retrieve_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmP,
                     RetrieveArgs a) {
@@ -244,8 +267,9 @@ __global__ void __launch_bounds__(kRetrThreads, 1)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
             const int i = 4 * q + e;
-            const float dist = fmaf(-2.0f, __uint_as_float(r[i]), nn[e]);
-            if (j0 + i < nref) topk_insert(dist, j0 + i, bd, bj);
+            // slots at or after nref (references not before the token) never enter
+            const float dist = j0 + i < nref ? fmaf(-2.0f, __uint_as_float(r[i]), nn[e]) : INFINITY;
+            topk_insert_nb(dist, j0 + i, bd, bj);
           }
         }
       }
