@@ -165,10 +165,14 @@ __device__ __forceinline__ void quant_group(const float* z, int bits, uint8_t* c
   const int levels = (1 << bits) - 1;
   const float delta = __fdiv_rn(__fsub_rn(hi, lo), (float)levels);
   const bool zero = constant || (delta == 0.0f);
+  // (z - min) / Delta as a product with the correctly rounded reciprocal: the pre-round
+  // value moves by at most ~2 ulp, which can change a code only within ~1e-6 of a .5
+  // boundary (the method's code tolerance allows +-1 within 1e-3 of one)
+  const float rdelta = zero ? 0.0f : __frcp_rn(delta);
   int q[32];
 #pragma unroll
   for (int i = 0; i < 32; ++i) {
-    int v = zero ? 0 : __float2int_rn(__fdiv_rn(__fsub_rn(z[i], lo), delta));
+    int v = zero ? 0 : __float2int_rn(__fmul_rn(__fsub_rn(z[i], lo), rdelta));
     q[i] = v < 0 ? 0 : (v > levels ? levels : v);
   }
   if (bits == 4) {
