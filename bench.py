@@ -165,8 +165,8 @@ MEASURED_TRAFFIC = {
                                            "code_sha1": "04ba157c4bcef39262c86cfe863d8d5864d004bc",
                                            "bytes": 15946240 + 25549312},
     ("llama8b", "rkv_retrieve_kernel"): {"file": "k_retrieve.cu",
-                                         "code_sha1": "2fa75553f0dcd7f3432ad5a4cd1c4c4a6af2d412",
-                                         "bytes": 134557184 + 3536128},
+                                         "code_sha1": "aa7c494b08aad67b44f721081daffd90bc65a63e",
+                                         "bytes": 134541056 + 3821568},
 }
 
 
