@@ -222,6 +222,28 @@ rkv_status rkv_sparse_attention(rkv_ctx* ctx, const float* q, int32_t n_q_heads,
                                 void* stream);
 
 /*
+ * Restore fused into the sparse layer's attention (ResidualKV notes §2.7, Fig. 7: the
+ * selected tokens I_t are restored and attended in one pass, o = softmax(q K_hat^T /
+ * sqrt(D)) V_hat); the same result as rkv_reconstruct followed by rkv_sparse_attention,
+ * without writing K_hat / V_hat to memory.
+ *   seq, pos (device, int32) [n_sel]: the selected tokens (as for rkv_reconstruct).
+ *   q (device, fp32) [n_q_heads, D]: the decode query, already rotated; query head h
+ *     reads key/value head h / (n_q_heads / N).  8-byte aligned.
+ *   out (device, fp32) [n_q_heads, D].
+ *   n_q_heads: a multiple of N, at most 8 N;  n_sel in [1, min(262144, B * max_tokens)].
+ * Needs head_dim = 128 and out_dtype = bf16: K_hat and V_hat are rounded to bf16 where
+ * rkv_reconstruct would store them, the scores and the weights reach the tensor core as
+ * bf16 high + low parts (relative error below 2^-16), sums are fp32.  The library's
+ * workspace holds per-tile partials, so calls on one context must not run concurrently.
+ * Bad selections raise the same status bits as rkv_reconstruct (their rows count as
+ * zero K_hat / V_hat rows).
+ * Errors (nothing launched): RKV_EINVAL (shape, dtype, sizes, NULL), RKV_EALIGN; RKV_ECUDA.
+ */
+rkv_status rkv_restore_attend(rkv_ctx* ctx, const int32_t* seq, const int32_t* pos,
+                              int32_t n_sel, const float* q, int32_t n_q_heads, float* out,
+                              void* stream);
+
+/*
  * The context's bf16 copy of the reference pool: [B, R_cap, 2d_k], row
  * s * R_cap + slot holding the decoded E4M3 reference of that slot exactly (every E4M3
  * value is a bf16 value).  It is the tensor-core operand of retrieval, a compute cache

@@ -22,7 +22,9 @@ from __future__ import annotations
 
 import numpy as np
 
-__all__ = ["sparse_attention"]
+from . import formats as F
+
+__all__ = ["sparse_attention", "attend_restored"]
 
 
 def sparse_attention(q, K, V):
@@ -48,3 +50,21 @@ def sparse_attention(q, K, V):
         w = np.exp(s - s.max())
         out[h] = (w / w.sum()) @ V[:, g, :]
     return out
+
+
+def attend_restored(q, K_hat, V_hat, rows: str = "bf16"):
+    """The sparse layer's read as one pass (ResidualKV notes section 2.7, Fig. 7: the
+    selected tokens are restored and attended without a stored K/V copy): the output
+    equation over the restored rows as the read consumes them.
+
+    K_hat, V_hat [n, N, D] are the restored rows in float64 (``codec.reconstruct``);
+    ``rows`` names the format they are handed to the attention in: "bf16" rounds them
+    (nearest-even) as a bf16 restore output is rounded, "f64" keeps them.  Reading of
+    the page: it fixes no format for the restored rows, and a fused read rounds them
+    where an unfused one would store them.
+    """
+    if rows == "bf16":
+        K_hat, V_hat = F.bf16(K_hat), F.bf16(V_hat)
+    elif rows != "f64":
+        raise ValueError("rows must be 'bf16' or 'f64'")
+    return sparse_attention(q, K_hat, V_hat)

@@ -70,6 +70,7 @@ ABI_FUNCTIONS = {
     "rkv_compress": (_I32, [_P, _P, _I64, _P, _P, _P, _I32, _P]),
     "rkv_reconstruct": (_I32, [_P, _P, _P, _I32, _P, _P, _P]),
     "rkv_sparse_attention": (_I32, [_P, _P, _I32, _P, _P, _I32, _P, _P]),
+    "rkv_restore_attend": (_I32, [_P, _P, _P, _I32, _P, _I32, _P, _P]),
     "rkv_get_status": (_I32, [_P, ctypes.POINTER(_I32), _P]),
     "rkv_reset": (_I32, [_P, _I32, _P]),
     "rkv_pool_cache": (_I32, [_P, ctypes.POINTER(_P), ctypes.POINTER(ctypes.c_size_t)]),
@@ -370,6 +371,28 @@ class Codec:
         _check(lib().rkv_sparse_attention(self._ctx, q.data_ptr(), q.shape[0], k.data_ptr(),
                                           v.data_ptr(), k.shape[0], out.data_ptr(),
                                           _stream_ptr(stream)))
+        return out
+
+    def restore_attend(self, seq, pos, q, out=None, stream=None):
+        """softmax(q K_hat^T / sqrt(D)) V_hat over the selected tokens, restored on chip
+        (nothing of K_hat / V_hat is written).  seq, pos: int32 CUDA tensors; q: [H_q, D]
+        fp32 CUDA tensor; returns out [H_q, D] fp32."""
+        D = self.cfg.head_dim
+        n = int(pos.numel())
+        for t in (seq, pos):
+            if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+                raise ValueError("seq and pos must be contiguous int32 CUDA tensors")
+        if int(seq.numel()) != n:
+            raise ValueError("seq and pos must have the same length")
+        if q.dtype != torch.float32 or not q.is_cuda or not q.is_contiguous() or q.dim() != 2 \
+                or q.shape[1] != D:
+            raise ValueError("q must be a contiguous [H_q, D] fp32 CUDA tensor")
+        if out is None:
+            out = torch.empty((q.shape[0], D), dtype=torch.float32, device=q.device)
+        _check_out(out, q.shape[0] * D, torch.float32, "out")
+        _check(lib().rkv_restore_attend(self._ctx, seq.data_ptr(), pos.data_ptr(), n,
+                                        q.data_ptr(), q.shape[0], out.data_ptr(),
+                                        _stream_ptr(stream)))
         return out
 
     def reset(self, seq: int = -1, stream=None):

@@ -266,7 +266,67 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
   if (threadIdx.x == 0) count[g] = 0;                // ready for the next call
 }
 
+// Merge of the fused restore + attention's partials (one per 128-token tile and query
+// head): one CTA per query head, thread d for output dimension d (D = 128).
+constexpr int kMergeMaxTiles = kAttnMaxTokens / kTileM;
+
+__global__ void __launch_bounds__(128)
+    attend_merge_kernel(const float* __restrict__ pm, const float* __restrict__ pl,
+                        const float* __restrict__ po, int tiles, int Hq, float* __restrict__ out) {
+  __shared__ float fac[kMergeMaxTiles];
+  __shared__ float red[4];
+  pdl_launch_dependents();
+  pdl_wait_previous_grid();                        // the partials of the fused launch
+  const int h = blockIdx.x, w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  float mx = -FLT_MAX;
+  for (int t = threadIdx.x; t < tiles; t += 128) mx = fmaxf(mx, __ldcg(pm + (size_t)t * Hq + h));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (l == 0) red[w] = mx;
+  __syncthreads();
+  mx = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  float L = 0.f;
+  for (int t = threadIdx.x; t < tiles; t += 128) {
+    const float f = expf(__ldcg(pm + (size_t)t * Hq + h) - mx);
+    fac[t] = f;
+    L = fmaf(__ldcg(pl + (size_t)t * Hq + h), f, L);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
+  __syncthreads();                                 // every thread has read red (the maximum)
+  if (l == 0) red[w] = L;
+  __syncthreads();
+  L = (red[0] + red[1]) + (red[2] + red[3]);
+  const float* p = po + (size_t)h * 128 + threadIdx.x;
+  const size_t stride = (size_t)Hq * 128;
+  float o = 0.f;
+#pragma unroll 8
+  for (int t = 0; t < tiles; ++t) o = fmaf(__ldcg(p + (size_t)t * stride), fac[t], o);
+  out[(size_t)h * 128 + threadIdx.x] = o / L;
+}
+
 }  // namespace
+
+cudaError_t launch_attend_merge(rkv_ctx* c, const float* pm, const float* pl, const float* po,
+                                int tiles, int n_q_heads, float* out, cudaStream_t s) {
+  if (tiles < 1 || tiles > kMergeMaxTiles) return cudaErrorInvalidValue;
+  cudaEvent_t ev;
+  timing_begin(c, "rkv_attend_merge_kernel", s, &ev);
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(n_q_heads);
+  lc.blockDim = dim3(128);
+  lc.dynamicSmemBytes = 0;
+  lc.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  cudaError_t e = cudaLaunchKernelEx(&lc, attend_merge_kernel, pm, pl, po, tiles, n_q_heads, out);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  timing_end(c, "rkv_attend_merge_kernel", s, ev);
+  return e;
+}
 
 // Tokens per chunk: enough chunks for one resident wave of CTAs over the N key/value
 // heads (kAttnCtasPerSm per SM), at most 1024 tokens (the weights' shared memory) and

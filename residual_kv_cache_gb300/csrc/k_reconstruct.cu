@@ -38,6 +38,26 @@
 // the tensor core finishes a unit's MMAs well within the epilogue's time, so the kernel
 // is bound by the epilogue's dependent chains and the first tile's setup, not by the
 // tensor core or by HBM.
+//
+// Restore fused into the sparse layer's attention (§2.7: o = softmax(q K_hat^T / sqrt(D))
+// V_hat over the selected tokens; D = 128, bf16 K_hat / V_hat).  The same kernel,
+// instantiated with kAttend, orders its units as (K head h, V head h) pairs of a token
+// tile and keeps the restored rows on chip:
+//   * the K unit's epilogue writes its bf16 K_hat rows into a shared-memory tile
+//     (token-major, 128-byte swizzle), and the MMA thread computes the tile's scores
+//     S = K_hat Q^T into the K accumulator's first 16 columns, Q holding the scaled query
+//     rows of the head's group as bf16 high and low parts (q / sqrt(D) = hi + lo to
+//     within 2^-16 relative), so that the tensor core's products stay exact;
+//   * the epilogue reads each row's scores, takes the tile's maximum m and the weights
+//     p = exp(s - m) per query head (rows past the selection weigh nothing), writes m and
+//     l = sum p per (tile, query head) to global memory, and puts p into a second tile
+//     as bf16 high and low parts;
+//   * the V unit's epilogue writes its V_hat rows transposed (dimension-major) into the
+//     first tile, and the MMA thread computes V_hat^T P into the V accumulator's first
+//     16 columns: per dimension d and query head, sum over the tile's tokens of p v_d;
+//   * a merge kernel combines the tiles of each query head: M = max m, L = sum l e^(m-M),
+//     o = sum o_tile e^(m - M) / L.
+// No restored row is written to global memory.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -56,7 +76,8 @@ constexpr uint32_t kBBytes = kNT * 128;      // one 64-wide k-block of W_d^T row
 constexpr uint32_t kPlaneBytes = kTileM * 32;            // one 32-byte sector per tile row
 constexpr uint32_t kGBytes = 2 * 4 * 2 * kPlaneBytes;    // [group pair][ref][x|y] planes
 constexpr uint32_t kCSBytes = 4 * 8 * kTileM * 16;   // cos/sin: 4 groups x 8 float4 x 128 rows
-constexpr uint32_t kBarBytes = 512;
+constexpr uint32_t kBarBytes = 1024;            // mbarriers, TMEM slot; from +512 the
+                                               // fused read's reduction slots
 constexpr int kRecInts = 8;                  // staged row record: flags, pos, pool rows 0..3, seq
 constexpr int kLoadWarp0 = 2;                // warps 2..3 stage the CTA's later tiles
 constexpr uint32_t kTmemCols = 512;
@@ -68,6 +89,12 @@ constexpr int kMaxStages = 8;
 #define RKV_TILE_CHANGE_COST4 10
 #endif
 constexpr int kTileChangeCost4 = RKV_TILE_CHANGE_COST4;
+// restore + attention: K_hat / V_hat^T tile (two 64-column swizzle atoms of 128 rows),
+// the weight tile P and the pair's query tile (16 rows x 128 bf16 each)
+constexpr uint32_t kKVBytes = 2 * kTileM * 128;
+constexpr uint32_t kRowTile16 = 16 * 128;            // one swizzle atom of a 16-row tile
+constexpr uint32_t kPBytes = 2 * kRowTile16;
+constexpr uint32_t kAttendBytes = kKVBytes + 2 * kPBytes;
 
 struct ReconArgs {
   const int32_t* seq;
@@ -90,6 +117,13 @@ struct ReconArgs {
   int stage_codes;    // later tiles' codes are staged in shared memory (code_bytes <= 256)
   int chunk_mask;     // swizzle of a staged code row's 16-byte chunks: chunk c ^ (row & mask)
   int* status;
+  // restore + attention only
+  const float* q;     // [N gq][D] fp32 decode queries; query head h gq + g reads head h
+  int gq;             // query heads per key/value head (<= 8)
+  float q_scale;      // 1 / sqrt(D)
+  float* part_m;      // [tiles][N gq] each token tile's maximum score
+  float* part_l;      // [tiles][N gq] sum of exp(s - m) over the tile
+  float* part_o;      // [tiles][N gq][D] sum of exp(s - m) v over the tile
 };
 
 // One 32-byte store (eight 32-bit words) to a 32-byte aligned global address.
@@ -103,6 +137,14 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   __nv_bfloat16 lo = __float2bfloat16_rn(a), hi = __float2bfloat16_rn(b);
   return static_cast<uint32_t>(__bfloat16_as_ushort(lo)) |
          (static_cast<uint32_t>(__bfloat16_as_ushort(hi)) << 16);
+}
+
+// Byte offset of bf16 element (r, c) in a K-major tile stored with the 128-byte swizzle:
+// 64-column atoms `atom` bytes apart, 128-byte rows, 16-byte chunk (c % 64) / 8 of row r
+// at position chunk ^ (r % 8).
+__device__ __forceinline__ uint32_t sw128_off(int r, int c, uint32_t atom) {
+  return (uint32_t)(c >> 6) * atom + (uint32_t)r * 128u +
+         ((uint32_t)(((c & 63) >> 3) ^ (r & 7)) << 4) + (uint32_t)(c & 7) * 2u;
 }
 
 // s[i] += value of FP8 byte i of v (16 bytes); exact in fp32 for <= 4 addends (their
@@ -343,26 +385,39 @@ __device__ __forceinline__ void stage_row(const ReconArgs& a, int m, int row, in
 }
 
 // First unit of CTA b's contiguous range (b = grid gives `units`).  The ranges split a
-// cost of one per unit plus kTileChangeCost4 / 4 per token-tile boundary crossed inside
+// cost of one per unit plus cost4 / 4 per token-tile boundary crossed inside
 // a range evenly over the grid: each tile after the first carries that extra cost ahead
 // of its first unit, and a cut falling there starts the next range on the tile.
-__device__ __forceinline__ int range_start(int b, int grid, int units, int n_tiles) {
-  const int64_t tc = 4 * (int64_t)n_tiles + kTileChangeCost4;
-  const int64_t total = (int64_t)(units / n_tiles) * tc - kTileChangeCost4;
-  const int64_t c = (int64_t)b * total / grid + kTileChangeCost4;
+__device__ __forceinline__ int range_start(int b, int grid, int units, int n_tiles, int cost4) {
+  const int64_t tc = 4 * (int64_t)n_tiles + cost4;
+  const int64_t total = (int64_t)(units / n_tiles) * tc - cost4;
+  const int64_t c = (int64_t)b * total / grid + cost4;
   const int64_t t = c / tc;
-  const int64_t off4 = c - t * tc - kTileChangeCost4;
+  const int64_t off4 = c - t * tc - cost4;
   const int64_t u = t * n_tiles + (off4 <= 0 ? 0 : off4 / 4);
   return (int)(u < units ? u : units);
 }
 
+// Output column tile of unit j of a token tile: j itself, or with kAttend the pairs
+// (K head j / 2, V head j / 2).
+template <bool kAttend>
+__device__ __forceinline__ int unit_col(int j, int n_tiles) {
+  if constexpr (kAttend) return (j & 1) ? (n_tiles >> 1) + (j >> 1) : (j >> 1);
+  return j;
+}
+
+template <bool kAttend>
 __global__ void __launch_bounds__(kReconThreads, 1)
     reconstruct_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ ReconArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = align1024(smem_raw);
   const int nkb = a.dc / kTileK;
   uint8_t* sB = smem;                                       // b_stages x W_d^T k-block
-  uint8_t* sG = sB + a.b_stages * kBBytes;                  // per-warp reference slots
+  // restore + attention: K_hat / V_hat^T tile, weight tile, query tile
+  uint8_t* sKV = sB + a.b_stages * kBBytes;
+  uint8_t* sP = sKV + kKVBytes;
+  uint8_t* sQ = sP + kPBytes;
+  uint8_t* sG = kAttend ? sQ + kPBytes : sKV;               // per-warp reference slots
   float4* sCS = reinterpret_cast<float4*>(sG + kGBytes);
   int* sRec = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(sCS) + kCSBytes);  // staged tile
   uint32_t* sMeta = reinterpret_cast<uint32_t*>(sRec + kTileM * kRecInts);
@@ -376,13 +431,23 @@ __global__ void __launch_bounds__(kReconThreads, 1)
   uint64_t* afree = afull + 1;                              // the MMAs of a tile are done
   uint64_t* staged = afree + 1;                             // the next tile is staged
   uint64_t* sfree = staged + 1;                             // the staged tile has been read
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(sfree + 1);
+  uint64_t* kready = sfree + 1;       // restore + attention: K_hat (and the queries) staged
+  uint64_t* sdone = kready + 1;       //   the scores are in TMEM
+  uint64_t* vready = sdone + 1;       //   V_hat^T and the weights staged
+  uint64_t* odone = vready + 1;       //   V_hat^T P is in TMEM
+  uint64_t* gsum = odone + 1;         //   [4] a warp group's per-warp maxima / sums written
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gsum + 4);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* sRed = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 512);  // [4][16]
 
   const int warp = threadIdx.x >> 5;
   pdl_launch_dependents();
-  const int u_begin = range_start(blockIdx.x, gridDim.x, a.units, a.n_tiles);
-  const int u_end = range_start(blockIdx.x + 1, gridDim.x, a.units, a.n_tiles);
+  // with kAttend the ranges are cut between pairs
+  constexpr int kSpan = kAttend ? 2 : 1;
+  const int u_begin = kSpan * range_start(blockIdx.x, gridDim.x, a.units / kSpan,
+                                          a.n_tiles / kSpan, kTileChangeCost4 / kSpan);
+  const int u_end = kSpan * range_start(blockIdx.x + 1, gridDim.x, a.units / kSpan,
+                                        a.n_tiles / kSpan, kTileChangeCost4 / kSpan);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < a.b_stages; ++s) {
@@ -397,6 +462,11 @@ __global__ void __launch_bounds__(kReconThreads, 1)
     mbar_init(afree, 1);
     mbar_init(staged, 2 * 64);       // 64 loader threads: a plain and a copy-completion arrival
     mbar_init(sfree, 16);
+    mbar_init(kready, 16);
+    mbar_init(sdone, 1);
+    mbar_init(vready, 16);
+    mbar_init(odone, 1);
+    for (int g = 0; g < 4; ++g) mbar_init(&gsum[g], 4);
     *abort_flag = 0;
     fence_barrier_init();
     tma_prefetch(&tmW);
@@ -417,7 +487,7 @@ __global__ void __launch_bounds__(kReconThreads, 1)
       uint32_t issued = 0, issued_phase = 0;             // bit s: stage s used / its phase
       bool ok = true;
       for (int u = u_begin; u < u_end && ok; ++u) {
-        const int n = u % a.n_tiles;
+        const int n = unit_col<kAttend>(u % a.n_tiles, a.n_tiles);
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&empty[ring.stage], ring.phase ^ 1u, abort_flag, a.status)) {
             ok = false;
@@ -446,6 +516,21 @@ __global__ void __launch_bounds__(kReconThreads, 1)
       bool ok = true, any = false;
       int last_stage = 0;
       uint32_t last_phase = 0;
+      // restore + attention: a pair's products of two 128 x 128 shared-memory tiles with a
+      // 16-row tile (scores K_hat Q^T, then V_hat^T P), 16 accumulator columns each
+      bool pend_o = false, small_last = false;
+      uint32_t s_phase = 0, o_phase = 0, small_par = 0;
+      uint64_t* small_bar = sdone;
+      auto pair_mma = [&](uint32_t d, const uint8_t* A, const uint8_t* B) {
+        constexpr uint32_t idesc16 = idesc_bf16_f32(kTileM, 16);
+        const uint32_t a0 = smem_u32(A), b0 = smem_u32(B);
+#pragma unroll
+        for (int kb = 0; kb < 2; ++kb)
+#pragma unroll
+          for (int k = 0; k < kTileK / 16; ++k)
+            umma_bf16(d, sdesc_sw128(a0 + kb * (kTileM * 128) + k * 32),
+                      sdesc_sw128(b0 + kb * kRowTile16 + k * 32), idesc16, (kb | k) != 0 ? 1u : 0u);
+      };
       for (int u = u_begin; u < u_end && ok; ++u) {
         const int m = u / a.n_tiles;
         if (m != cur_m) {
@@ -486,12 +571,60 @@ __global__ void __launch_bounds__(kReconThreads, 1)
         }
         if (!ok) break;
         umma_commit(&tfull[acc]);
+        small_last = false;
+        if constexpr (kAttend) {
+          if (acc == 0) {
+            // the next pair's K unit is issued: the previous pair's V_hat^T P next
+            if (pend_o) {
+              if (!mbar_wait(vready, o_phase, abort_flag, a.status)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+              pair_mma(tmem + kNT, sKV, sP);
+              umma_commit(odone);
+              small_bar = odone, small_par = o_phase, small_last = true;
+              o_phase ^= 1u;
+              pend_o = false;
+            }
+          } else {
+            // the pair's scores, once its K_hat rows (and the queries) are staged
+            if (!mbar_wait(kready, s_phase, abort_flag, a.status)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            pair_mma(tmem, sKV, sQ);
+            umma_commit(sdone);
+            small_bar = sdone, small_par = s_phase, small_last = true;
+            s_phase ^= 1u;
+            pend_o = true;
+          }
+        }
         if (++acc == 2) {
           acc = 0;
           acc_phase ^= 1u;
         }
       }
-      if (!ok && any) drain_wait(&empty[last_stage], last_phase);
+      if constexpr (kAttend) {
+        if (ok && pend_o) {
+          if (mbar_wait(vready, o_phase, abort_flag, a.status)) {
+            tc_fence_after();
+            pair_mma(tmem + kNT, sKV, sP);
+            umma_commit(odone);
+            small_bar = odone, small_par = o_phase, small_last = true;
+          } else {
+            ok = false;
+          }
+        }
+      }
+      // MMAs complete in issue order: waiting for the last commit drains them all
+      if (!ok && any) {
+        if (small_last)
+          drain_wait(small_bar, small_par);
+        else
+          drain_wait(&empty[last_stage], last_phase);
+      }
     }
   } else if (warp < kEpiWarpR) {
     // ------------------------------------------------ loaders: the CTA's later tiles
@@ -670,8 +803,19 @@ __global__ void __launch_bounds__(kReconThreads, 1)
     uint32_t acc_phase = 0, afree_phase = 0;
     int cur_m = -1, tt = 0;
     bool ok = true;
+    uint32_t s_phase = 0, o_phase = 0, g_phase = 0;   // restore + attention
+    // The four warps of a group exchange their rows' maxima and sums through shared
+    // memory: each warp's lane 0 writes and arrives, then all wait (bounded).
+    auto group_exchange = [&]() -> bool {
+      __syncwarp();
+      if (lane_id() == 0) mbar_arrive(&gsum[wg]);
+      const bool w = warp_wait(&gsum[wg], g_phase, abort_flag, a.status);
+      g_phase ^= 1u;
+      __syncwarp();
+      return w;
+    };
     for (int u = u_begin; u < u_end && ok; ++u) {
-      const int m = u / a.n_tiles, n = u % a.n_tiles;
+      const int m = u / a.n_tiles, n = unit_col<kAttend>(u % a.n_tiles, a.n_tiles);
       if (m != cur_m) {
         if (cur_m < 0) {
           const int64_t gi = (int64_t)m * kTileM + row;
@@ -700,7 +844,7 @@ __global__ void __launch_bounds__(kReconThreads, 1)
         if (!setup_s((tt + 1) % a.zbufs, nxt)) break;
       }
       const bool more = u + 1 < u_end;
-      const int n_next = (u + 1) % a.n_tiles;
+      const int n_next = unit_col<kAttend>((u + 1) % a.n_tiles, a.n_tiles);
       const int c0 = n * kNT + hl * a.D;               // first KV_hat column of the head
       const bool is_k = c0 < a.dk;
       // ---- mean of the references: wait for this unit's copies of reference t (both
@@ -751,10 +895,13 @@ __global__ void __launch_bounds__(kReconThreads, 1)
           my[i] = __fmaf_rn(my[i], kinv, __uint_as_float(yr[i]));
         }
       }
-      // the accumulator is free as soon as it has been read
-      tc_fence_before();
-      __syncwarp();
-      if (lane_id() == 0) mbar_arrive(&tempty[acc]);
+      // the accumulator is free as soon as it has been read (with kAttend, once the
+      // pair's product in its first columns has been read)
+      if constexpr (!kAttend) {
+        tc_fence_before();
+        __syncwarp();
+        if (lane_id() == 0) mbar_arrive(&tempty[acc]);
+      }
       if (++acc == 2) {
         acc = 0;
         acc_phase ^= 1u;
@@ -773,6 +920,159 @@ __global__ void __launch_bounds__(kReconThreads, 1)
       if (!cur.valid()) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) mx[i] = 0.f, my[i] = 0.f;
+      }
+      if constexpr (kAttend) {
+        // ---- attention over the tile (ResidualKV notes §2.7 output equation)
+        const int NH = a.dk / a.D;
+        const int h = (u % a.n_tiles) >> 1;             // key/value head of the pair
+        const int et = (int)threadIdx.x - 32 * kEpiWarpR;
+        if (!waited) {
+          // the queries and the partial sums may belong to the previous launch's merge
+          pdl_wait_previous_grid();
+          waited = true;
+          // the weight tile's rows past 2 gq stay zero
+          for (int i = et; i < (int)(kPBytes / 16); i += 512)
+            reinterpret_cast<uint4*>(sP)[i] = make_uint4(0u, 0u, 0u, 0u);
+        }
+        const int gA = wg, gB = wg + 4;                 // this group's query heads
+        const bool hasA = gA < a.gq, hasB = gB < a.gq;  // uniform over the group
+        const bool live = (int64_t)m * kTileM + row < a.n_sel;
+        const int64_t qh0 = ((int64_t)m * NH + h) * a.gq;   // partial slot of (tile, head h gq)
+        if (is_k) {
+          // the head's query tile (the previous pair's scores are done with it): row g < gq
+          // the bf16 high part of q_g / sqrt(D), row gq + g the low part (the exact
+          // remainder, rounded), other rows zero
+          for (int i = et; i < 16 * 64; i += 512) {
+            const int r16 = i >> 6, d = 2 * (i & 63);
+            uint32_t wv = 0u;
+            if (r16 < 2 * a.gq) {
+              const int g = r16 < a.gq ? r16 : r16 - a.gq;
+              const float2 qv =
+                  *reinterpret_cast<const float2*>(a.q + ((int64_t)h * a.gq + g) * a.D + d);
+              const float q0 = qv.x * a.q_scale, q1 = qv.y * a.q_scale;
+              const float h0 = __bfloat162float(__float2bfloat16_rn(q0));
+              const float h1 = __bfloat162float(__float2bfloat16_rn(q1));
+              wv = r16 < a.gq ? pack_bf16x2(h0, h1) : pack_bf16x2(q0 - h0, q1 - h1);
+            }
+            *reinterpret_cast<uint32_t*>(sQ + sw128_off(r16, d, kRowTile16)) = wv;
+          }
+          // K_hat row into the token-major tile: x values (dimensions j0 ..) in the first
+          // 64-column atom, y values (j0 + 64 ..) in the second
+          {
+            uint32_t wx[8], wy[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              wx[i] = pack_bf16x2(mx[2 * i], mx[2 * i + 1]);
+              wy[i] = pack_bf16x2(my[2 * i], my[2 * i + 1]);
+            }
+            const int cx = j0 >> 3, sw = row & 7;
+            uint8_t* k0 = sKV + (uint32_t)row * 128u;
+            uint8_t* k1 = k0 + kTileM * 128;
+            *reinterpret_cast<uint4*>(k0 + ((cx ^ sw) << 4)) = make_uint4(wx[0], wx[1], wx[2], wx[3]);
+            *reinterpret_cast<uint4*>(k0 + (((cx + 1) ^ sw) << 4)) = make_uint4(wx[4], wx[5], wx[6], wx[7]);
+            *reinterpret_cast<uint4*>(k1 + ((cx ^ sw) << 4)) = make_uint4(wy[0], wy[1], wy[2], wy[3]);
+            *reinterpret_cast<uint4*>(k1 + (((cx + 1) ^ sw) << 4)) = make_uint4(wy[4], wy[5], wy[6], wy[7]);
+          }
+          tc_fence_before();                            // the K accumulator has been read
+          fence_proxy_async_smem();                     // the rows are visible to the MMA
+          __syncwarp();
+          if (lane_id() == 0) mbar_arrive(kready);
+          // every wait that can give up is followed by a vote of the warp pair that shares
+          // reference slots, so that the two always leave together
+          if (!bar_red_and(bar_id, 64, warp_wait(sdone, s_phase, abort_flag, a.status))) break;
+          s_phase ^= 1u;
+          tc_fence_after();
+          // row's scores: S[:, g] + S[:, gq + g] = K_hat (q_hi + q_lo) / sqrt(D)
+          const uint32_t tS = tmem + lane_base;
+          uint32_t sa = 0u, sa2 = 0u, sb = 0u, sb2 = 0u;
+          if (hasA) sa = tmem_ld1(tS + gA), sa2 = tmem_ld1(tS + a.gq + gA);
+          if (hasB) sb = tmem_ld1(tS + gB), sb2 = tmem_ld1(tS + a.gq + gB);
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane_id() == 0) mbar_arrive(&tempty[0]);
+          bool gok = true;
+          if (hasA) {
+            const float s0 = live ? __uint_as_float(sa) + __uint_as_float(sa2) : -INFINITY;
+            const float s1 = live && hasB ? __uint_as_float(sb) + __uint_as_float(sb2) : -INFINITY;
+            float* red = sRed + wg * 16;                // [max A | max B | sum A | sum B][4 warps]
+            float m0 = s0, m1 = s1;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+              m0 = fmaxf(m0, __shfl_xor_sync(0xffffffffu, m0, o));
+              m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
+            }
+            if (lane_id() == 0) red[ew] = m0, red[4 + ew] = m1;
+            gok = group_exchange();
+            m0 = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+            m1 = fmaxf(fmaxf(red[4], red[5]), fmaxf(red[6], red[7]));
+            const float p0 = live ? expf(s0 - m0) : 0.f;
+            const float p1 = live && hasB ? expf(s1 - m1) : 0.f;
+            float l0 = p0, l1 = p1;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+              l0 += __shfl_xor_sync(0xffffffffu, l0, o);
+              l1 += __shfl_xor_sync(0xffffffffu, l1, o);
+            }
+            if (lane_id() == 0) red[8 + ew] = l0, red[12 + ew] = l1;
+            // weights as bf16 high + low parts: rows g and gq + g of P, column = token
+            const float pa = __bfloat162float(__float2bfloat16_rn(p0));
+            const float pb = __bfloat162float(__float2bfloat16_rn(p1));
+            *reinterpret_cast<__nv_bfloat16*>(sP + sw128_off(gA, row, kRowTile16)) = __float2bfloat16_rn(pa);
+            *reinterpret_cast<__nv_bfloat16*>(sP + sw128_off(a.gq + gA, row, kRowTile16)) =
+                __float2bfloat16_rn(p0 - pa);
+            if (hasB) {
+              *reinterpret_cast<__nv_bfloat16*>(sP + sw128_off(gB, row, kRowTile16)) = __float2bfloat16_rn(pb);
+              *reinterpret_cast<__nv_bfloat16*>(sP + sw128_off(a.gq + gB, row, kRowTile16)) =
+                  __float2bfloat16_rn(p1 - pb);
+            }
+            gok = group_exchange() && gok;
+            if (gok && ew == 0 && lane_id() == 0) {
+              a.part_m[qh0 + gA] = m0;
+              a.part_l[qh0 + gA] = (red[8] + red[9]) + (red[10] + red[11]);
+              if (hasB) {
+                a.part_m[qh0 + gB] = m1;
+                a.part_l[qh0 + gB] = (red[12] + red[13]) + (red[14] + red[15]);
+              }
+            }
+          }
+          if (!bar_red_and(bar_id, 64, gok)) break;
+        } else {
+          // V_hat row transposed into the dimension-major tile: element (d, token) at row d,
+          // token chunk (token & 63) / 8 swizzled with d, atom token / 64
+          {
+            const int e = row & 63, c = e >> 3;
+            uint8_t* vb = sKV + (uint32_t)(row >> 6) * (kTileM * 128) + (uint32_t)(e & 7) * 2;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int dx = xcol + i, dy = ycol + i;
+              *reinterpret_cast<__nv_bfloat16*>(vb + dx * 128 + ((c ^ (dx & 7)) << 4)) =
+                  __float2bfloat16_rn(mx[i]);
+              *reinterpret_cast<__nv_bfloat16*>(vb + dy * 128 + ((c ^ (dy & 7)) << 4)) =
+                  __float2bfloat16_rn(my[i]);
+            }
+          }
+          tc_fence_before();
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane_id() == 0) mbar_arrive(vready);
+          if (!bar_red_and(bar_id, 64, warp_wait(odone, o_phase, abort_flag, a.status))) break;
+          o_phase ^= 1u;
+          tc_fence_after();
+          // lane d of the V accumulator: column g + column gq + g = sum_t p_t v_t[d]
+          const uint32_t tO = tmem + lane_base + kNT;
+          uint32_t oa = 0u, oa2 = 0u, ob = 0u, ob2 = 0u;
+          if (hasA) oa = tmem_ld1(tO + gA), oa2 = tmem_ld1(tO + a.gq + gA);
+          if (hasB) ob = tmem_ld1(tO + gB), ob2 = tmem_ld1(tO + a.gq + gB);
+          tmem_ld_wait();
+          tc_fence_before();
+          __syncwarp();
+          if (lane_id() == 0) mbar_arrive(&tempty[1]);
+          float* po = a.part_o + qh0 * a.D + row;
+          if (hasA) po[(int64_t)gA * a.D] = __uint_as_float(oa) + __uint_as_float(oa2);
+          if (hasB) po[(int64_t)gB * a.D] = __uint_as_float(ob) + __uint_as_float(ob2);
+        }
+        continue;
       }
       // ---- output: 32-byte stores straight from registers (the row's 16 x values, then
       // its 16 y values); K/V may be the previous launch's outputs, so each thread waits
@@ -817,27 +1117,22 @@ __global__ void __launch_bounds__(kReconThreads, 1)
 
 }  // namespace
 
-cudaError_t launch_reconstruct(rkv_ctx* c, const int32_t* seq, const int32_t* pos, int n_sel,
-                               void* k_out, void* v_out, cudaStream_t s) {
+// The restore's arguments and shared-memory size for a selection of n_sel >= 1 tokens;
+// `attend_bytes` of shared memory are set aside before the reference slots.
+static cudaError_t recon_setup(rkv_ctx* c, const int32_t* seq, const int32_t* pos, int n_sel,
+                               size_t attend_bytes, ReconArgs* ap, size_t* smem_out) {
   const Dims& d = c->d;
-  if (n_sel <= 0) return cudaSuccess;
   // staged tile: records, extremes and (rows of at most 128 bytes) codes
   const bool stage_codes = d.code_bytes <= 128;
   const size_t stage = (size_t)kTileM * kRecInts * 4 + (size_t)kTileM * d.G * 4 +
                        (stage_codes ? (((size_t)kTileM * d.code_bytes + 127) & ~(size_t)127) : 0);
-  const size_t fixed = 1024 + kCSBytes + kGBytes + stage + kBarBytes;
+  const size_t fixed = 1024 + attend_bytes + kCSBytes + kGBytes + stage + kBarBytes;
   int b_stages = (int)((232448 - fixed) / kBBytes);
   if (b_stages > kMaxStages) b_stages = kMaxStages;
   if (b_stages < 2) return cudaErrorInvalidConfiguration;
-  const size_t smem = fixed + (size_t)b_stages * kBBytes;
-  // the kernel's shared-memory limit is raised once per context (on its device)
-  cudaError_t e = cudaSuccess;
-  if (c->recon_smem < (int)smem) {
-    e = cudaFuncSetAttribute(reconstruct_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    c->recon_smem = (int)smem;
-  }
-  ReconArgs a;
+  *smem_out = fixed + (size_t)b_stages * kBBytes;
+  ReconArgs& a = *ap;
+  a = ReconArgs{};
   a.seq = seq;
   a.pos = pos;
   a.n_sel = n_sel;
@@ -851,8 +1146,6 @@ cudaError_t launch_reconstruct(rkv_ctx* c, const int32_t* seq, const int32_t* po
   a.pool8 = static_cast<const uint8_t*>(c->st.pool_fp8);
   a.rope_lo = c->rope_lo;
   a.rope_hi = c->rope_hi;
-  a.k_out = k_out;
-  a.v_out = v_out;
   a.out_f32 = d.out_f32;
   a.B = d.B;
   a.T_cap = d.T_cap;
@@ -873,9 +1166,22 @@ cudaError_t launch_reconstruct(rkv_ctx* c, const int32_t* seq, const int32_t* po
     a.chunk_mask = (low < 8 ? low : 8) - 1;
   }
   a.status = c->status;
-  const int grid = a.units < c->num_sms ? a.units : c->num_sms;
+  return cudaSuccess;
+}
+
+template <bool kAttend>
+static cudaError_t recon_launch(rkv_ctx* c, const ReconArgs& a, size_t smem, int grid,
+                                int* smem_set, const char* name, cudaStream_t s) {
+  // the kernel's shared-memory limit is raised once per context (on its device)
+  cudaError_t e = cudaSuccess;
+  if (*smem_set < (int)smem) {
+    e = cudaFuncSetAttribute(reconstruct_kernel<kAttend>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e != cudaSuccess) return e;
+    *smem_set = (int)smem;
+  }
   cudaEvent_t ev;
-  timing_begin(c, "rkv_reconstruct_kernel", s, &ev);
+  timing_begin(c, name, s, &ev);
   cudaLaunchConfig_t lc = {};
   lc.gridDim = dim3(grid);
   lc.blockDim = dim3(kReconThreads);
@@ -886,10 +1192,47 @@ cudaError_t launch_reconstruct(rkv_ctx* c, const int32_t* seq, const int32_t* po
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   lc.attrs = attr;
   lc.numAttrs = 1;
-  e = cudaLaunchKernelEx(&lc, reconstruct_kernel, c->tm_wd, a);
+  e = cudaLaunchKernelEx(&lc, reconstruct_kernel<kAttend>, c->tm_wd, a);
   if (e == cudaSuccess) e = cudaGetLastError();
-  timing_end(c, "rkv_reconstruct_kernel", s, ev);
+  timing_end(c, name, s, ev);
   return e;
+}
+
+cudaError_t launch_reconstruct(rkv_ctx* c, const int32_t* seq, const int32_t* pos, int n_sel,
+                               void* k_out, void* v_out, cudaStream_t s) {
+  if (n_sel <= 0) return cudaSuccess;
+  ReconArgs a;
+  size_t smem = 0;
+  cudaError_t e = recon_setup(c, seq, pos, n_sel, 0, &a, &smem);
+  if (e != cudaSuccess) return e;
+  a.k_out = k_out;
+  a.v_out = v_out;
+  const int grid = a.units < c->num_sms ? a.units : c->num_sms;
+  return recon_launch<false>(c, a, smem, grid, &c->recon_smem, "rkv_reconstruct_kernel", s);
+}
+
+cudaError_t launch_restore_attend(rkv_ctx* c, const int32_t* seq, const int32_t* pos, int n_sel,
+                                  const float* q, int n_q_heads, float* out, cudaStream_t s) {
+  const Dims& d = c->d;
+  if (n_sel <= 0) return cudaSuccess;
+  const size_t attend = kAttendBytes;
+  ReconArgs a;
+  size_t smem = 0;
+  cudaError_t e = recon_setup(c, seq, pos, n_sel, attend, &a, &smem);
+  if (e != cudaSuccess) return e;
+  const int gq = n_q_heads / d.N;
+  const int m_tiles = (n_sel + kTileM - 1) / kTileM;
+  a.q = q;
+  a.gq = gq;
+  a.q_scale = (float)(1.0 / sqrt((double)d.D));
+  a.part_m = c->fa_ws;
+  a.part_l = a.part_m + (size_t)m_tiles * n_q_heads;
+  a.part_o = a.part_l + (size_t)m_tiles * n_q_heads;
+  const int pairs = a.units / 2;
+  const int grid = pairs < c->num_sms ? pairs : c->num_sms;
+  e = recon_launch<true>(c, a, smem, grid, &c->fused_smem, "rkv_restore_attend_kernel", s);
+  if (e != cudaSuccess) return e;
+  return launch_attend_merge(c, a.part_m, a.part_l, a.part_o, m_tiles, n_q_heads, out, s);
 }
 
 }  // namespace rkv

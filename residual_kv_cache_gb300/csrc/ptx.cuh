@@ -289,7 +289,14 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
   return d;
 }
 
-// 32 lanes x 32-bit, 8 / 16 / 32 consecutive columns per thread (thread t <- lane base+t).
+// 32 lanes x 32-bit, 1 / 8 / 16 / 32 consecutive columns per thread (thread t <- lane
+// base + t); the address is the same for the whole warp.
+__device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
+  uint32_t r;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(r) : "r"(taddr));
+  return r;
+}
+
 __device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t* r) {
   asm volatile(
       "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"

@@ -448,6 +448,11 @@ rkv_status rkv_create(const rkv_config* cfg, const void* Wc1, const void* Wc2, c
   ALLOC(c->part, (size_t)c->units_cap * kTileM * 4 * sizeof(int2));
   ALLOC(c->attn_ws, sizeof(float) * kAttnMaxChunks * kAttnMaxGroup * d.N * (2 + d.D));
   ALLOC(c->attn_count, sizeof(int) * d.N);
+  {
+    const int64_t toks = (int64_t)d.B * d.T_cap < kAttnMaxTokens ? (int64_t)d.B * d.T_cap : kAttnMaxTokens;
+    const int64_t tiles = (toks + kTileM - 1) / kTileM;
+    ALLOC(c->fa_ws, sizeof(float) * (size_t)tiles * kAttnMaxGroup * d.N * (2 + d.D));
+  }
   ALLOC(c->plan_dev[0], (size_t)c->plan_ints * 4);
   ALLOC(c->plan_dev[1], (size_t)c->plan_ints * 4);
   ALLOC(c->status, 512);
@@ -789,6 +794,26 @@ rkv_status rkv_sparse_attention(rkv_ctx* c, const float* q, int32_t n_q_heads, c
   return RKV_OK;
 }
 
+rkv_status rkv_restore_attend(rkv_ctx* c, const int32_t* seq, const int32_t* pos, int32_t n_sel,
+                              const float* q, int32_t n_q_heads, float* out, void* stream) {
+  if (!c) return fail(RKV_EINVAL, "ctx is NULL");
+  if (!seq || !pos || !q || !out) return fail(RKV_EINVAL, "NULL seq, pos, q or out");
+  const Dims& d = c->d;
+  if (d.D != 128 || d.out_f32)
+    return fail(RKV_EINVAL, "the fused restore + attention needs head_dim 128 and bf16 outputs");
+  if (n_q_heads < d.N || n_q_heads % d.N != 0 || n_q_heads / d.N > kAttnMaxGroup)
+    return fail(RKV_EINVAL, "n_q_heads must be a multiple of n_kv_heads, at most %d times it",
+                kAttnMaxGroup);
+  if (n_sel < 1 || n_sel > kAttnMaxTokens || (int64_t)n_sel > (int64_t)d.B * d.T_cap)
+    return fail(RKV_EINVAL, "n_sel must be in [1, min(%d, B * max_tokens)]", kAttnMaxTokens);
+  if ((reinterpret_cast<uintptr_t>(q) & 7u) || (reinterpret_cast<uintptr_t>(out) & 3u) ||
+      (reinterpret_cast<uintptr_t>(seq) & 3u) || (reinterpret_cast<uintptr_t>(pos) & 3u))
+    return fail(RKV_EALIGN, "q must be 8-byte aligned, out, seq and pos 4-byte aligned");
+  CUDA_OK(launch_restore_attend(c, seq, pos, n_sel, q, n_q_heads, out,
+                                static_cast<cudaStream_t>(stream)));
+  return RKV_OK;
+}
+
 rkv_status rkv_pool_cache(rkv_ctx* c, void** ptr, size_t* bytes) {
   if (!c || !ptr || !bytes) return fail(RKV_EINVAL, "NULL argument");
   *ptr = c->pool_bf16;
@@ -826,6 +851,7 @@ void rkv_free(rkv_ctx* c) {
   cudaFree(c->w12);
   cudaFree(c->attn_ws);
   cudaFree(c->attn_count);
+  cudaFree(c->fa_ws);
   cudaFree(c->w3);
   cudaFree(c->wd);
   cudaFree(c->rope_lo);

@@ -94,6 +94,9 @@ struct rkv_ctx {
   float* attn_ws = nullptr;       // sparse attention chunk partials (m, l, acc), kAttnMaxChunks
                                   // x kAttnMaxGroup N query heads
   int* attn_count = nullptr;      // [N] finished chunks per key/value head (zero between calls)
+  float* fa_ws = nullptr;         // restore + attention partials (m, l, o) per token tile and
+                                  // query head: up to kAttnMaxTokens / 128 tiles x 8 N heads
+  int fused_smem = 0;             // dynamic shared memory the fused kernel is set up for
   int units_cap = 0;
   int32_t* plan_dev[2] = {nullptr, nullptr};
   int32_t* plan_host[2] = {nullptr, nullptr};   // pinned staging
@@ -155,9 +158,15 @@ int attention_chunk(int n, int N, int num_sms);
 cudaError_t launch_attention(rkv_ctx* c, const float* q, int n_q_heads, const void* k,
                              const void* v, int n, float* out, cudaStream_t s);
 
-// Tensor map of a row-major [rows, cols] output matrix (bf16 or fp32) for 2-D tiled
-// stores: box = {16 columns, 32 rows}, swizzled over the box's row bytes (32 or 64), so
-// that a warp writing one box row per lane in 16-byte chunks hits distinct banks.
+// Restore fused into the sparse attention (D = 128, bf16 K_hat / V_hat, n_q_heads / N <=
+// kAttnMaxGroup, n_sel <= kAttnMaxTokens): per (token tile, query head) softmax partials
+// in the context's workspace, then launch_attend_merge.
+cudaError_t launch_restore_attend(rkv_ctx* c, const int32_t* seq, const int32_t* pos, int n_sel,
+                                  const float* q, int n_q_heads, float* out, cudaStream_t s);
+// out[h] = sum_t o_t[h] e^(m_t[h] - M) / sum_t l_t[h] e^(m_t[h] - M), M = max_t m_t[h], over
+// `tiles` partials [tiles][n_q_heads] (o: [tiles][n_q_heads][128]).
+cudaError_t launch_attend_merge(rkv_ctx* c, const float* pm, const float* pl, const float* po,
+                                int tiles, int n_q_heads, float* out, cudaStream_t s);
 
 // Record the message rkv_last_error returns on this thread.
 void set_error(const char* msg);

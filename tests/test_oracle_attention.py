@@ -66,3 +66,25 @@ def test_rejects_empty_selection_and_bad_groups():
         A.sparse_attention(np.zeros((2, 4)), np.zeros((0, 1, 4)), np.zeros((0, 1, 4)))
     with pytest.raises(ValueError):
         A.sparse_attention(np.zeros((3, 4)), np.zeros((2, 2, 4)), np.zeros((2, 2, 4)))
+
+
+def test_attend_restored_rounds_rows_as_torch_bf16():
+    """The one-pass read (ResidualKV notes section 2.7, Fig. 7) attends over the restored
+    rows rounded to bf16: the same as torch's scaled dot-product attention over the rows
+    converted by torch to bfloat16 (nearest-even) and back; one token returns its value
+    rounded to bf16; with rows="f64" nothing is rounded."""
+    rng = np.random.default_rng(4)
+    n, N, D = 200, 2, 128
+    q, K, V = _rand(rng, N, D), _rand(rng, n, N, D) * 3.0, _rand(rng, n, N, D)
+    Kb = torch.tensor(K).to(torch.bfloat16).double()
+    Vb = torch.tensor(V).to(torch.bfloat16).double()
+    ref = torch.nn.functional.scaled_dot_product_attention(
+        torch.tensor(q)[:, None, :], Kb.permute(1, 0, 2), Vb.permute(1, 0, 2))[:, 0, :].numpy()
+    got = A.attend_restored(q, K, V)
+    assert np.allclose(got, ref, rtol=1e-12, atol=1e-12)
+    assert not np.allclose(got, A.sparse_attention(q, K, V), rtol=1e-6, atol=0)
+    assert np.array_equal(A.attend_restored(q, K, V, rows="f64"), A.sparse_attention(q, K, V))
+    one = A.attend_restored(q[:1], K[:1, :1], V[:1, :1])
+    assert np.array_equal(one[0], torch.tensor(V[0, 0]).to(torch.bfloat16).double().numpy())
+    with pytest.raises(ValueError):
+        A.attend_restored(q, K, V, rows="fp8")
