@@ -779,7 +779,7 @@ def run_workload(name, ctx, seed, with_e2e=True, with_cpu=True):
         out["e2e"] = run.e2e()
         status |= _status(codecs)
         out["device_status"] = int(status)
-    if name == "llama8b":
+    if name in Q_HEADS:
         out["sparse_attention"] = measure_attention(run, ctx)
     if with_cpu and ctx.rank == 0 and ctx.world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = cpu_baseline(name, args.cpu_seconds)
@@ -790,36 +790,81 @@ def run_workload(name, ctx, seed, with_e2e=True, with_cpu=True):
     return out
 
 
+# query heads of the models the stacks are shaped after (Llama-3-8B: 32 over 8 key/value
+# heads; Qwen2.5-7B: 28 over 4)
+Q_HEADS = {"llama8b": 32, "qwen7b": 28}
+
+
 def measure_attention(run, ctx):
-    """Time rkv_sparse_attention after each decode step's restore (event pairs around
-    its launches).  Bytes: the K and V rows it reads, q in, o out."""
+    """The sparse layer's read after each decode step (layer 0's selection), two ways:
+    rkv_reconstruct then rkv_sparse_attention (K/V written, then read back while still in
+    L2), and rkv_restore_attend (K/V kept on chip, then the per-tile merge).  Each is
+    timed back to back over the steps (events around the whole sequence of calls) and
+    per kernel (event pairs around each launch).  Attention bytes: the K and V rows it
+    reads, q in, o out."""
     import torch
     w, codec = run.w, run.codecs[0]
-    hq = 4 * w.n_kv_heads
+    hq = Q_HEADS.get(run.name, 4 * w.n_kv_heads)
     g = torch.Generator().manual_seed(4242)
     q = torch.randn(hq, w.head_dim, generator=g).to(ctx.dev)
     out = torch.empty(hq, w.head_dim, dtype=torch.float32, device=ctx.dev)
-    codec.set_timing(True)
-    codec.get_timing(reset=True)
-    for _ in range(ctx.args.steps):
-        ctx.flush.fill_(1.0)
-        ctx.barrier()
-        for row in run.sels:
-            codec.reconstruct(run.seq0, row[0], run.k_out, run.v_out)
-            codec.sparse_attention(q, run.k_out, run.v_out, out)
-        ctx.barrier()
-    t = codec.get_timing(reset=True)
-    codec.set_timing(False)
-    calls, ms = t["rkv_attention_kernel"]
-    us = ms / calls * 1e3
+    out_f = torch.empty_like(out)
+    rows = [row[0] for row in run.sels]
+    unfused = lambda sel: (codec.reconstruct(run.seq0, sel, run.k_out, run.v_out),
+                           codec.sparse_attention(q, run.k_out, run.v_out, out))
+    fused = lambda sel: codec.restore_attend(run.seq0, sel, q, out_f)
+
+    def back_to_back(fn):
+        per = []
+        for _ in range(ctx.args.steps):
+            ctx.flush.fill_(1.0)
+            ctx.barrier()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for sel in rows:
+                fn(sel)
+            e1.record()
+            torch.cuda.synchronize()
+            per.append(e0.elapsed_time(e1) / len(rows))
+        return float(np.median(per)) * 1e3
+
+    def per_kernel(fn):
+        codec.set_timing(True)
+        codec.get_timing(reset=True)
+        for _ in range(ctx.args.steps):
+            ctx.flush.fill_(1.0)
+            ctx.barrier()
+            for sel in rows:
+                fn(sel)
+            ctx.barrier()
+        t = codec.get_timing(reset=True)
+        codec.set_timing(False)
+        return {k: ms / n * 1e3 for k, (n, ms) in t.items() if n}
+
+    for fn in (unfused, fused):                      # warm-up
+        for sel in rows[:4]:
+            fn(sel)
+    torch.cuda.synchronize()
+    b2b_unfused, b2b_fused = back_to_back(unfused), back_to_back(fused)
+    k_unfused, k_fused = per_kernel(unfused), per_kernel(fused)
+    us = k_unfused["rkv_attention_kernel"]
     n = run.n_sel
     kv_bytes = 2 * n * w.n_kv_heads * w.head_dim * 2
     peaks, kind = load_peaks()
     gbs = (kv_bytes + 2 * hq * w.head_dim * 4) / (us * 1e-6) / 1e9
+    d = (out - out_f).abs().max().item() / max(out.abs().max().item(), 1e-30)
     return {"tokens": n, "q_heads": hq, "kv_heads": w.n_kv_heads, "us_per_call": round(us, 2),
             "gbs": round(gbs, 1), "hbm_frac": round(gbs / peaks["hbm_gbs"], 4),
             "peak_kind": f"{kind} copy",
-            "note": "K/V read right after their restore (L2-resident); o is fp32"}
+            "note": "K/V read right after their restore (L2-resident); o is fp32",
+            "restore_then_attention_us": round(b2b_unfused, 2),
+            "restore_attend_us": round(b2b_fused, 2),
+            "fused_speedup": round(b2b_unfused / b2b_fused, 3),
+            "per_kernel_us": {k: round(v, 2) for k, v in {**k_unfused, **k_fused}.items()},
+            "fused_vs_unfused_max_rel_diff": float(f"{d:.3e}"),
+            "timing": "per step: one restore + attention of layer 0's selection; median over "
+                      "steps of (events around all decode steps' calls) / calls; per_kernel: "
+                      "event pairs around each launch"}
 
 
 def storage_report(codec, w) -> dict:
@@ -881,6 +926,8 @@ def run_cuda(args):
            "clocks": head["clocks"], "device_status": head["device_status"]}
     if "cpu_baseline" in head:
         out["cpu_baseline"] = head["cpu_baseline"]
+    if "sparse_attention" in head:
+        out["sparse_attention"] = head["sparse_attention"]
     if len(names) > 1:
         out["configs"] = {n: results[n] for n in names[1:]}
     if rank == 0:
@@ -1014,7 +1061,8 @@ def _stack_description(name: str) -> str:
 def run_kernel_case(args):
     """Minimal case for kernel captures under ncu: one layer of the workload, one
     prefill write and two decode-step restores, each followed by the sparse attention
-    over its rows (no timing, no CPU work)."""
+    over its rows and by the fused restore + attention of the same selection (no timing,
+    no CPU work)."""
     import torch
     import residual_kv_cache_gb300 as rkv
     from residual_kv_cache_gb300 import build as _build
@@ -1034,7 +1082,8 @@ def run_kernel_case(args):
     codec.pool_append(kv, np.zeros_like(ref), ref, src_rows=ref)
     codec.compress(kv, np.zeros_like(non), non, src_rows=non)
     g = torch.Generator().manual_seed(4242)
-    q = torch.randn(4 * w.n_kv_heads, w.head_dim, generator=g).to(dev)
+    q = torch.randn(Q_HEADS.get(name, 4 * w.n_kv_heads), w.head_dim, generator=g).to(dev)
+    fuse = w.head_dim == 128 and cfg.out_dtype == "bf16"
     for s in range(2):
         if w.sel_block > 1:
             sel = synth.gen_block_selection(w.T, w.sel_block, w.sel_frac, 1010 + s).to(dev)
@@ -1043,6 +1092,8 @@ def run_kernel_case(args):
         zero = torch.zeros(sel.numel(), dtype=torch.int32, device=dev)
         K, V = codec.reconstruct(zero, sel)
         codec.sparse_attention(q, K, V)             # the sparse layer's attention over them
+        if fuse:
+            codec.restore_attend(zero, sel, q)          # the same read, restored on chip
     torch.cuda.synchronize()
     flags = codec.get_status()
     print(json.dumps({"kernel_case": name, "T": w.T, "launches": codec.launch_count(),

@@ -267,26 +267,34 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
 }
 
 // Merge of the fused restore + attention's partials (one per 128-token tile and query
-// head): one CTA per query head, thread d for output dimension d (D = 128).
+// head).  CTA (h, c) produces dimensions [32 c, 32 c + 32) of query head h: every CTA of
+// the head takes M = max m_t and the factors e^(m_t - M) over all tiles, then warp w sums
+// tiles w, w + 8, ... (lane = dimension, one 128-byte row per tile) and the eight warps'
+// sums are added.
 constexpr int kMergeMaxTiles = kAttnMaxTokens / kTileM;
+constexpr int kMergeThreads = 256;
 
-__global__ void __launch_bounds__(128)
+__global__ void __launch_bounds__(kMergeThreads)
     attend_merge_kernel(const float* __restrict__ pm, const float* __restrict__ pl,
                         const float* __restrict__ po, int tiles, int Hq, float* __restrict__ out) {
   __shared__ float fac[kMergeMaxTiles];
-  __shared__ float red[4];
+  __shared__ float red[8];
+  __shared__ float part[8][32];
   pdl_launch_dependents();
   pdl_wait_previous_grid();                        // the partials of the fused launch
-  const int h = blockIdx.x, w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  const int h = blockIdx.x, c = blockIdx.y, w = threadIdx.x >> 5, l = threadIdx.x & 31;
   float mx = -FLT_MAX;
-  for (int t = threadIdx.x; t < tiles; t += 128) mx = fmaxf(mx, __ldcg(pm + (size_t)t * Hq + h));
+  for (int t = threadIdx.x; t < tiles; t += kMergeThreads)
+    mx = fmaxf(mx, __ldcg(pm + (size_t)t * Hq + h));
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   if (l == 0) red[w] = mx;
   __syncthreads();
-  mx = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
+  mx = red[0];
+#pragma unroll
+  for (int i = 1; i < 8; ++i) mx = fmaxf(mx, red[i]);
   float L = 0.f;
-  for (int t = threadIdx.x; t < tiles; t += 128) {
+  for (int t = threadIdx.x; t < tiles; t += kMergeThreads) {
     const float f = expf(__ldcg(pm + (size_t)t * Hq + h) - mx);
     fac[t] = f;
     L = fmaf(__ldcg(pl + (size_t)t * Hq + h), f, L);
@@ -295,14 +303,21 @@ __global__ void __launch_bounds__(128)
   for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
   __syncthreads();                                 // every thread has read red (the maximum)
   if (l == 0) red[w] = L;
-  __syncthreads();
-  L = (red[0] + red[1]) + (red[2] + red[3]);
-  const float* p = po + (size_t)h * 128 + threadIdx.x;
+  __syncthreads();                                 // and fac is complete
+  L = ((red[0] + red[1]) + (red[2] + red[3])) + ((red[4] + red[5]) + (red[6] + red[7]));
+  const float* p = po + (size_t)h * 128 + c * 32 + l;
   const size_t stride = (size_t)Hq * 128;
   float o = 0.f;
-#pragma unroll 8
-  for (int t = 0; t < tiles; ++t) o = fmaf(__ldcg(p + (size_t)t * stride), fac[t], o);
-  out[(size_t)h * 128 + threadIdx.x] = o / L;
+#pragma unroll 4
+  for (int t = w; t < tiles; t += 8) o = fmaf(__ldcg(p + (size_t)t * stride), fac[t], o);
+  part[w][l] = o;
+  __syncthreads();
+  if (w == 0) {
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s += part[i][l];
+    out[(size_t)h * 128 + c * 32 + l] = s / L;
+  }
 }
 
 }  // namespace
@@ -313,8 +328,8 @@ cudaError_t launch_attend_merge(rkv_ctx* c, const float* pm, const float* pl, co
   cudaEvent_t ev;
   timing_begin(c, "rkv_attend_merge_kernel", s, &ev);
   cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3(n_q_heads);
-  lc.blockDim = dim3(128);
+  lc.gridDim = dim3(n_q_heads, 4);
+  lc.blockDim = dim3(kMergeThreads);
   lc.dynamicSmemBytes = 0;
   lc.stream = s;
   cudaLaunchAttribute attr[1];

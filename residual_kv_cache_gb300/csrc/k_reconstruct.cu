@@ -95,6 +95,8 @@ constexpr uint32_t kKVBytes = 2 * kTileM * 128;
 constexpr uint32_t kRowTile16 = 16 * 128;            // one swizzle atom of a 16-row tile
 constexpr uint32_t kPBytes = 2 * kRowTile16;
 constexpr uint32_t kAttendBytes = kKVBytes + 2 * kPBytes;
+constexpr int kGroupBar0 = 9;     // named barriers 9..12: the four warps of one epilogue group
+constexpr int kVoteBar = 13;      // all 16 epilogue warps
 
 struct ReconArgs {
   const int32_t* seq;
@@ -435,8 +437,7 @@ __global__ void __launch_bounds__(kReconThreads, 1)
   uint64_t* sdone = kready + 1;       //   the scores are in TMEM
   uint64_t* vready = sdone + 1;       //   V_hat^T and the weights staged
   uint64_t* odone = vready + 1;       //   V_hat^T P is in TMEM
-  uint64_t* gsum = odone + 1;         //   [4] a warp group's per-warp maxima / sums written
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(gsum + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(odone + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   float* sRed = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(full) + 512);  // [4][16]
 
@@ -466,7 +467,6 @@ __global__ void __launch_bounds__(kReconThreads, 1)
     mbar_init(sdone, 1);
     mbar_init(vready, 16);
     mbar_init(odone, 1);
-    for (int g = 0; g < 4; ++g) mbar_init(&gsum[g], 4);
     *abort_flag = 0;
     fence_barrier_init();
     tma_prefetch(&tmW);
@@ -703,7 +703,9 @@ __global__ void __launch_bounds__(kReconThreads, 1)
     uint32_t staged_phase = 0;
     auto setup_s = [&](int zb, RowState& st) -> bool {
       const bool w = mbar_wait(staged, staged_phase, abort_flag, a.status);
-      if (!__all_sync(0xffffffffu, w)) return false;
+      bool wa = __all_sync(0xffffffffu, w);
+      if constexpr (kAttend) wa = bar_red_and(kVoteBar, 512, wa);
+      if (!wa) return false;
       staged_phase ^= 1u;
       const int* rec = sRec + row * kRecInts;
       st.flags = rec[0];
@@ -803,18 +805,39 @@ __global__ void __launch_bounds__(kReconThreads, 1)
     uint32_t acc_phase = 0, afree_phase = 0;
     int cur_m = -1, tt = 0;
     bool ok = true;
-    uint32_t s_phase = 0, o_phase = 0, g_phase = 0;   // restore + attention
-    // The four warps of a group exchange their rows' maxima and sums through shared
-    // memory: each warp's lane 0 writes and arrives, then all wait (bounded).
-    auto group_exchange = [&]() -> bool {
+    uint32_t s_phase = 0, o_phase = 0;                // restore + attention
+    // A wait that gives up makes the warp leave the unit loop.  Without kAttend the two
+    // warps of a pair (sharing reference slots and a named barrier) vote together; with
+    // kAttend all 16 epilogue warps do, since the four warps of a group also meet at a
+    // named barrier in the softmax: every warp then leaves at the same wait.
+    const int vote_id = kAttend ? kVoteBar : bar_id;
+    const int vote_n = kAttend ? 512 : 64;
+    // V_hat^T P of the pair whose V unit is uv: lane d of the V accumulator, column g +
+    // column gq + g = sum over the tile's tokens of p v_d; then the accumulator is free.
+    auto finish_o = [&](int uv) -> bool {
+      if (!bar_red_and(vote_id, vote_n, warp_wait(odone, o_phase, abort_flag, a.status))) return false;
+      o_phase ^= 1u;
+      tc_fence_after();
+      const int gA = wg, gB = wg + 4;
+      const bool hasA = gA < a.gq, hasB = gB < a.gq;
+      const uint32_t tO = tmem + lane_base + kNT;
+      uint32_t oa = 0u, oa2 = 0u, ob = 0u, ob2 = 0u;
+      if (hasA) oa = tmem_ld1(tO + gA), oa2 = tmem_ld1(tO + a.gq + gA);
+      if (hasB) ob = tmem_ld1(tO + gB), ob2 = tmem_ld1(tO + a.gq + gB);
+      tmem_ld_wait();
+      tc_fence_before();
       __syncwarp();
-      if (lane_id() == 0) mbar_arrive(&gsum[wg]);
-      const bool w = warp_wait(&gsum[wg], g_phase, abort_flag, a.status);
-      g_phase ^= 1u;
-      __syncwarp();
-      return w;
+      if (lane_id() == 0) mbar_arrive(&tempty[1]);
+      const int64_t qh0 =
+          ((int64_t)(uv / a.n_tiles) * (a.dk / a.D) + ((uv % a.n_tiles) >> 1)) * a.gq;
+      float* po = a.part_o + qh0 * a.D + row;
+      if (hasA) po[(int64_t)gA * a.D] = __uint_as_float(oa) + __uint_as_float(oa2);
+      if (hasB) po[(int64_t)gB * a.D] = __uint_as_float(ob) + __uint_as_float(ob2);
+      return true;
     };
-    for (int u = u_begin; u < u_end && ok; ++u) {
+    int u_done = u_begin;                              // == u_end unless the loop broke off
+    for (; u_done < u_end && ok; ++u_done) {
+      const int u = u_done;
       const int m = u / a.n_tiles, n = unit_col<kAttend>(u % a.n_tiles, a.n_tiles);
       if (m != cur_m) {
         if (cur_m < 0) {
@@ -838,7 +861,7 @@ __global__ void __launch_bounds__(kReconThreads, 1)
       if (u + 1 < u_end && (u + 1) / a.n_tiles != m) {
         if (a.zbufs == 1) {
           // both warps of the pair leave together, so neither waits at a barrier alone
-          if (!bar_red_and(bar_id, 64, warp_wait(afree, afree_phase, abort_flag, a.status))) break;
+          if (!bar_red_and(vote_id, vote_n, warp_wait(afree, afree_phase, abort_flag, a.status))) break;
           afree_phase ^= 1u;
         }
         if (!setup_s((tt + 1) % a.zbufs, nxt)) break;
@@ -880,7 +903,7 @@ __global__ void __launch_bounds__(kReconThreads, 1)
       }
       // ---- accumulator row; the pair's vote also tells that both warps have read
       // reference 3, whose plane then takes the next unit's copy
-      if (!bar_red_and(bar_id, 64, warp_wait(&tfull[acc], acc_phase, abort_flag, a.status))) break;
+      if (!bar_red_and(vote_id, vote_n, warp_wait(&tfull[acc], acc_phase, abort_flag, a.status))) break;
       issue_ref(n_next, more && 3 < a.topk, 3);
       tc_fence_after();
       {
@@ -922,38 +945,44 @@ __global__ void __launch_bounds__(kReconThreads, 1)
         for (int i = 0; i < 16; ++i) mx[i] = 0.f, my[i] = 0.f;
       }
       if constexpr (kAttend) {
-        // ---- attention over the tile (ResidualKV notes §2.7 output equation)
-        const int NH = a.dk / a.D;
-        const int h = (u % a.n_tiles) >> 1;             // key/value head of the pair
+        // ---- attention over the tile (ResidualKV notes §2.7 output equation).  Each
+        // tensor-core round trip overlaps the epilogue's next piece of restore work: the
+        // scores of pair p run while its V_hat rows are built, its V_hat^T P while the
+        // next pair's K_hat rows are built.
         const int et = (int)threadIdx.x - 32 * kEpiWarpR;
-        if (!waited) {
-          // the queries and the partial sums may belong to the previous launch's merge
-          pdl_wait_previous_grid();
-          waited = true;
-          // the weight tile's rows past 2 gq stay zero
-          for (int i = et; i < (int)(kPBytes / 16); i += 512)
-            reinterpret_cast<uint4*>(sP)[i] = make_uint4(0u, 0u, 0u, 0u);
-        }
-        const int gA = wg, gB = wg + 4;                 // this group's query heads
-        const bool hasA = gA < a.gq, hasB = gB < a.gq;  // uniform over the group
+        const int h = (u % a.n_tiles) >> 1;             // key/value head of the pair
         const bool live = (int64_t)m * kTileM + row < a.n_sel;
-        const int64_t qh0 = ((int64_t)m * NH + h) * a.gq;   // partial slot of (tile, head h gq)
         if (is_k) {
-          // the head's query tile (the previous pair's scores are done with it): row g < gq
-          // the bf16 high part of q_g / sqrt(D), row gq + g the low part (the exact
-          // remainder, rounded), other rows zero
-          for (int i = et; i < 16 * 64; i += 512) {
-            const int r16 = i >> 6, d = 2 * (i & 63);
-            uint32_t wv = 0u;
+          // the head's query rows (loads in flight while the previous pair is finished)
+          float2 qv[2];
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int i = et + 512 * j, r16 = i >> 6, d = 2 * (i & 63);
+            qv[j] = make_float2(0.f, 0.f);
             if (r16 < 2 * a.gq) {
               const int g = r16 < a.gq ? r16 : r16 - a.gq;
-              const float2 qv =
-                  *reinterpret_cast<const float2*>(a.q + ((int64_t)h * a.gq + g) * a.D + d);
-              const float q0 = qv.x * a.q_scale, q1 = qv.y * a.q_scale;
-              const float h0 = __bfloat162float(__float2bfloat16_rn(q0));
-              const float h1 = __bfloat162float(__float2bfloat16_rn(q1));
-              wv = r16 < a.gq ? pack_bf16x2(h0, h1) : pack_bf16x2(q0 - h0, q1 - h1);
+              qv[j] = *reinterpret_cast<const float2*>(a.q + ((int64_t)h * a.gq + g) * a.D + d);
             }
+          }
+          if (!waited) {
+            // the queries and the partial sums may belong to the previous launch's merge
+            pdl_wait_previous_grid();
+            waited = true;
+            // the weight tile's rows past 2 gq stay zero
+            for (int i = et; i < (int)(kPBytes / 16); i += 512)
+              reinterpret_cast<uint4*>(sP)[i] = make_uint4(0u, 0u, 0u, 0u);
+          } else if (!finish_o(u - 1)) {
+            break;                                      // the previous pair's V_hat^T P
+          }
+          // query tile: row g < gq the bf16 high part of q_g / sqrt(D), row gq + g the low
+          // part (the exact remainder, rounded), other rows zero
+#pragma unroll
+          for (int j = 0; j < 2; ++j) {
+            const int i = et + 512 * j, r16 = i >> 6, d = 2 * (i & 63);
+            const float q0 = qv[j].x * a.q_scale, q1 = qv[j].y * a.q_scale;
+            const float h0 = __bfloat162float(__float2bfloat16_rn(q0));
+            const float h1 = __bfloat162float(__float2bfloat16_rn(q1));
+            const uint32_t wv = r16 < a.gq ? pack_bf16x2(h0, h1) : pack_bf16x2(q0 - h0, q1 - h1);
             *reinterpret_cast<uint32_t*>(sQ + sw128_off(r16, d, kRowTile16)) = wv;
           }
           // K_hat row into the token-major tile: x values (dimensions j0 ..) in the first
@@ -974,15 +1003,16 @@ __global__ void __launch_bounds__(kReconThreads, 1)
             *reinterpret_cast<uint4*>(k1 + (((cx + 1) ^ sw) << 4)) = make_uint4(wy[4], wy[5], wy[6], wy[7]);
           }
           tc_fence_before();                            // the K accumulator has been read
-          fence_proxy_async_smem();                     // the rows are visible to the MMA
+          fence_proxy_async_smem();                     // the tiles are visible to the MMA
           __syncwarp();
           if (lane_id() == 0) mbar_arrive(kready);
-          // every wait that can give up is followed by a vote of the warp pair that shares
-          // reference slots, so that the two always leave together
-          if (!bar_red_and(bar_id, 64, warp_wait(sdone, s_phase, abort_flag, a.status))) break;
+        } else {
+          // the pair's scores: S[:, g] + S[:, gq + g] = K_hat (q_hi + q_lo) / sqrt(D)
+          if (!bar_red_and(vote_id, vote_n, warp_wait(sdone, s_phase, abort_flag, a.status))) break;
           s_phase ^= 1u;
           tc_fence_after();
-          // row's scores: S[:, g] + S[:, gq + g] = K_hat (q_hi + q_lo) / sqrt(D)
+          const int gA = wg, gB = wg + 4;               // this group's query heads
+          const bool hasA = gA < a.gq, hasB = gB < a.gq;  // uniform over the group
           const uint32_t tS = tmem + lane_base;
           uint32_t sa = 0u, sa2 = 0u, sb = 0u, sb2 = 0u;
           if (hasA) sa = tmem_ld1(tS + gA), sa2 = tmem_ld1(tS + a.gq + gA);
@@ -991,8 +1021,8 @@ __global__ void __launch_bounds__(kReconThreads, 1)
           tc_fence_before();
           __syncwarp();
           if (lane_id() == 0) mbar_arrive(&tempty[0]);
-          bool gok = true;
           if (hasA) {
+            const int64_t qh0 = ((int64_t)m * (a.dk / a.D) + h) * a.gq;  // (tile, head h gq)
             const float s0 = live ? __uint_as_float(sa) + __uint_as_float(sa2) : -INFINITY;
             const float s1 = live && hasB ? __uint_as_float(sb) + __uint_as_float(sb2) : -INFINITY;
             float* red = sRed + wg * 16;                // [max A | max B | sum A | sum B][4 warps]
@@ -1003,7 +1033,7 @@ __global__ void __launch_bounds__(kReconThreads, 1)
               m1 = fmaxf(m1, __shfl_xor_sync(0xffffffffu, m1, o));
             }
             if (lane_id() == 0) red[ew] = m0, red[4 + ew] = m1;
-            gok = group_exchange();
+            bar_sync(kGroupBar0 + wg, 128);
             m0 = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
             m1 = fmaxf(fmaxf(red[4], red[5]), fmaxf(red[6], red[7]));
             const float p0 = live ? expf(s0 - m0) : 0.f;
@@ -1026,8 +1056,8 @@ __global__ void __launch_bounds__(kReconThreads, 1)
               *reinterpret_cast<__nv_bfloat16*>(sP + sw128_off(a.gq + gB, row, kRowTile16)) =
                   __float2bfloat16_rn(p1 - pb);
             }
-            gok = group_exchange() && gok;
-            if (gok && ew == 0 && lane_id() == 0) {
+            bar_sync(kGroupBar0 + wg, 128);
+            if (ew == 0 && lane_id() == 0) {
               a.part_m[qh0 + gA] = m0;
               a.part_l[qh0 + gA] = (red[8] + red[9]) + (red[10] + red[11]);
               if (hasB) {
@@ -1036,10 +1066,9 @@ __global__ void __launch_bounds__(kReconThreads, 1)
               }
             }
           }
-          if (!bar_red_and(bar_id, 64, gok)) break;
-        } else {
-          // V_hat row transposed into the dimension-major tile: element (d, token) at row d,
-          // token chunk (token & 63) / 8 swizzled with d, atom token / 64
+          // V_hat row transposed into the dimension-major tile (the scores are done with
+          // the K_hat rows): element (d, token) at row d, token chunk (token & 63) / 8
+          // swizzled with d, atom token / 64
           {
             const int e = row & 63, c = e >> 3;
             uint8_t* vb = sKV + (uint32_t)(row >> 6) * (kTileM * 128) + (uint32_t)(e & 7) * 2;
@@ -1056,21 +1085,6 @@ __global__ void __launch_bounds__(kReconThreads, 1)
           fence_proxy_async_smem();
           __syncwarp();
           if (lane_id() == 0) mbar_arrive(vready);
-          if (!bar_red_and(bar_id, 64, warp_wait(odone, o_phase, abort_flag, a.status))) break;
-          o_phase ^= 1u;
-          tc_fence_after();
-          // lane d of the V accumulator: column g + column gq + g = sum_t p_t v_t[d]
-          const uint32_t tO = tmem + lane_base + kNT;
-          uint32_t oa = 0u, oa2 = 0u, ob = 0u, ob2 = 0u;
-          if (hasA) oa = tmem_ld1(tO + gA), oa2 = tmem_ld1(tO + a.gq + gA);
-          if (hasB) ob = tmem_ld1(tO + gB), ob2 = tmem_ld1(tO + a.gq + gB);
-          tmem_ld_wait();
-          tc_fence_before();
-          __syncwarp();
-          if (lane_id() == 0) mbar_arrive(&tempty[1]);
-          float* po = a.part_o + qh0 * a.D + row;
-          if (hasA) po[(int64_t)gA * a.D] = __uint_as_float(oa) + __uint_as_float(oa2);
-          if (hasB) po[(int64_t)gB * a.D] = __uint_as_float(ob) + __uint_as_float(ob2);
         }
         continue;
       }
@@ -1103,6 +1117,9 @@ __global__ void __launch_bounds__(kReconThreads, 1)
           st_global_v8(o + P, wy);
         }
       }
+    }
+    if constexpr (kAttend) {
+      if (ok && u_done == u_end && u_end > u_begin) finish_o(u_end - 1);
     }
     cp_async_wait<0>();                                // no copy may outlive the CTA
   }
