@@ -14,10 +14,13 @@
 
 #include <cfloat>
 
+#include <cooperative_groups.h>
+
 #include "ptx.cuh"
 #include "rkv_internal.h"
 
 namespace rkv {
+namespace cg = cooperative_groups;
 namespace {
 
 constexpr int kAttnThreads = 256;
@@ -267,57 +270,65 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
 }
 
 // Merge of the fused restore + attention's partials (one per 128-token tile and query
-// head).  CTA (h, c) produces dimensions [32 c, 32 c + 32) of query head h: every CTA of
-// the head takes M = max m_t and the factors e^(m_t - M) over all tiles, then warp w sums
-// tiles w, w + 8, ... (lane = dimension, one 128-byte row per tile) and the eight warps'
-// sums are added.
-constexpr int kMergeMaxTiles = kAttnMaxTokens / kTileM;
+// head; maxima in base-2 units).  A cluster of kMergeSlices CTAs produces dimensions
+// [32 c, 32 c + 32) of query head h.  Warp w of CTA s takes tiles s + S (w + 8 j) in one
+// pass, keeping a running (M, L, o) (lane = dimension): per tile, M' = max(M, m_t), then
+// L = L 2^(M - M') + l_t 2^(m_t - M') and o likewise, so every load is independent of the
+// others.  The eight warps' triples are combined the same way in shared memory, and CTA 0
+// combines the slices' triples from the other CTAs' shared memory.
+constexpr int kMergeSlices = 8;
 constexpr int kMergeThreads = 256;
+constexpr int kMergeMaxTiles = kAttnMaxTokens / kTileM;
+
+struct Triple {
+  float M, L, o;
+};
+
+__device__ __forceinline__ void merge_into(Triple& a, float m, float l, float o) {
+  const float M = fmaxf(a.M, m);
+  const float fa = ex2_approx(a.M - M), fb = ex2_approx(m - M);   // 0 for -FLT_MAX terms
+  a.L = fmaf(a.L, fa, l * fb);
+  a.o = fmaf(a.o, fa, o * fb);
+  a.M = M;
+}
 
 __global__ void __launch_bounds__(kMergeThreads)
     attend_merge_kernel(const float* __restrict__ pm, const float* __restrict__ pl,
                         const float* __restrict__ po, int tiles, int Hq, float* __restrict__ out) {
-  __shared__ float fac[kMergeMaxTiles];
-  __shared__ float red[8];
-  __shared__ float part[8][32];
+  __shared__ float wm[8], wl[8], wo[8][32];
+  __shared__ float slice[34];                      // M_s, L_s, o_s[32]
+  cg::cluster_group cluster = cg::this_cluster();
   pdl_launch_dependents();
   pdl_wait_previous_grid();                        // the partials of the fused launch
-  const int h = blockIdx.x, c = blockIdx.y, w = threadIdx.x >> 5, l = threadIdx.x & 31;
-  float mx = -FLT_MAX;
-  for (int t = threadIdx.x; t < tiles; t += kMergeThreads)
-    mx = fmaxf(mx, __ldcg(pm + (size_t)t * Hq + h));
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  if (l == 0) red[w] = mx;
-  __syncthreads();
-  mx = red[0];
-#pragma unroll
-  for (int i = 1; i < 8; ++i) mx = fmaxf(mx, red[i]);
-  float L = 0.f;
-  for (int t = threadIdx.x; t < tiles; t += kMergeThreads) {
-    const float f = expf(__ldcg(pm + (size_t)t * Hq + h) - mx);
-    fac[t] = f;
-    L = fmaf(__ldcg(pl + (size_t)t * Hq + h), f, L);
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) L += __shfl_xor_sync(0xffffffffu, L, o);
-  __syncthreads();                                 // every thread has read red (the maximum)
-  if (l == 0) red[w] = L;
-  __syncthreads();                                 // and fac is complete
-  L = ((red[0] + red[1]) + (red[2] + red[3])) + ((red[4] + red[5]) + (red[6] + red[7]));
-  const float* p = po + (size_t)h * 128 + c * 32 + l;
-  const size_t stride = (size_t)Hq * 128;
-  float o = 0.f;
+  const int s = blockIdx.x, c = blockIdx.y, h = blockIdx.z;
+  const int w = threadIdx.x >> 5, l = threadIdx.x & 31;
+  Triple acc{-FLT_MAX, 0.f, 0.f};
 #pragma unroll 4
-  for (int t = w; t < tiles; t += 8) o = fmaf(__ldcg(p + (size_t)t * stride), fac[t], o);
-  part[w][l] = o;
+  for (int t = s + kMergeSlices * w; t < tiles; t += kMergeSlices * 8) {
+    const size_t i = (size_t)t * Hq + h;
+    merge_into(acc, __ldcg(pm + i), __ldcg(pl + i), __ldcg(po + i * 128 + c * 32 + l));
+  }
+  if (l == 0) wm[w] = acc.M, wl[w] = acc.L;
+  wo[w][l] = acc.o;
   __syncthreads();
   if (w == 0) {
-    float s = 0.f;
+    Triple t{-FLT_MAX, 0.f, 0.f};
 #pragma unroll
-    for (int i = 0; i < 8; ++i) s += part[i][l];
-    out[(size_t)h * 128 + c * 32 + l] = s / L;
+    for (int i = 0; i < 8; ++i) merge_into(t, wm[i], wl[i], wo[i][l]);
+    slice[2 + l] = t.o;
+    if (l == 0) slice[0] = t.M, slice[1] = t.L;
   }
+  cluster.sync();                                  // every slice is in its CTA's memory
+  if (s == 0 && w == 0) {
+    Triple t{-FLT_MAX, 0.f, 0.f};
+#pragma unroll
+    for (int r = 0; r < kMergeSlices; ++r) {
+      const float* sr = cluster.map_shared_rank(slice, r);
+      merge_into(t, sr[0], sr[1], sr[2 + l]);
+    }
+    out[(size_t)h * 128 + c * 32 + l] = t.o / t.L;
+  }
+  cluster.sync();                                  // CTA 0 has read every slice
 }
 
 }  // namespace
@@ -328,15 +339,19 @@ cudaError_t launch_attend_merge(rkv_ctx* c, const float* pm, const float* pl, co
   cudaEvent_t ev;
   timing_begin(c, "rkv_attend_merge_kernel", s, &ev);
   cudaLaunchConfig_t lc = {};
-  lc.gridDim = dim3(n_q_heads, 4);
+  lc.gridDim = dim3(kMergeSlices, 4, n_q_heads);
   lc.blockDim = dim3(kMergeThreads);
   lc.dynamicSmemBytes = 0;
   lc.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = kMergeSlices;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
   lc.attrs = attr;
-  lc.numAttrs = 1;
+  lc.numAttrs = 2;
   cudaError_t e = cudaLaunchKernelEx(&lc, attend_merge_kernel, pm, pl, po, tiles, n_q_heads, out);
   if (e == cudaSuccess) e = cudaGetLastError();
   timing_end(c, "rkv_attend_merge_kernel", s, ev);

@@ -49,14 +49,15 @@
 //     rows of the head's group as bf16 high and low parts (q / sqrt(D) = hi + lo to
 //     within 2^-16 relative), so that the tensor core's products stay exact;
 //   * the epilogue reads each row's scores, takes the tile's maximum m and the weights
-//     p = exp(s - m) per query head (rows past the selection weigh nothing), writes m and
-//     l = sum p per (tile, query head) to global memory, and puts p into a second tile
-//     as bf16 high and low parts;
+//     p = exp(s - m) per query head (rows past the selection weigh nothing; computed in
+//     base 2, log2(e) folded into the query scale), writes m and l = sum p per (tile,
+//     query head) to global memory, and puts p into a second tile as bf16 high and low
+//     parts;
 //   * the V unit's epilogue writes its V_hat rows transposed (dimension-major) into the
 //     first tile, and the MMA thread computes V_hat^T P into the V accumulator's first
 //     16 columns: per dimension d and query head, sum over the tile's tokens of p v_d;
-//   * a merge kernel combines the tiles of each query head: M = max m, L = sum l e^(m-M),
-//     o = sum o_tile e^(m - M) / L.
+//   * a merge kernel combines the tiles of each query head: M = max m, L = sum l 2^(m-M),
+//     o = sum o_tile 2^(m - M) / L.
 // No restored row is written to global memory.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -122,10 +123,10 @@ struct ReconArgs {
   // restore + attention only
   const float* q;     // [N gq][D] fp32 decode queries; query head h gq + g reads head h
   int gq;             // query heads per key/value head (<= 8)
-  float q_scale;      // 1 / sqrt(D)
-  float* part_m;      // [tiles][N gq] each token tile's maximum score
-  float* part_l;      // [tiles][N gq] sum of exp(s - m) over the tile
-  float* part_o;      // [tiles][N gq][D] sum of exp(s - m) v over the tile
+  float q_scale;      // log2(e) / sqrt(D): scores in base-2 units, s' = s log2(e)
+  float* part_m;      // [tiles][N gq] each token tile's maximum score s'
+  float* part_l;      // [tiles][N gq] sum of 2^(s' - m) over the tile
+  float* part_o;      // [tiles][N gq][D] sum of 2^(s' - m) v over the tile
 };
 
 // One 32-byte store (eight 32-bit words) to a 32-byte aligned global address.
@@ -1036,8 +1037,9 @@ __global__ void __launch_bounds__(kReconThreads, 1)
             bar_sync(kGroupBar0 + wg, 128);
             m0 = fmaxf(fmaxf(red[0], red[1]), fmaxf(red[2], red[3]));
             m1 = fmaxf(fmaxf(red[4], red[5]), fmaxf(red[6], red[7]));
-            const float p0 = live ? expf(s0 - m0) : 0.f;
-            const float p1 = live && hasB ? expf(s1 - m1) : 0.f;
+            // exp(s - m) in base 2: 2^(s' - m') with s' = s log2(e) (folded into q)
+            const float p0 = live ? ex2_approx(s0 - m0) : 0.f;
+            const float p1 = live && hasB ? ex2_approx(s1 - m1) : 0.f;
             float l0 = p0, l1 = p1;
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) {
@@ -1241,7 +1243,7 @@ cudaError_t launch_restore_attend(rkv_ctx* c, const int32_t* seq, const int32_t*
   const int m_tiles = (n_sel + kTileM - 1) / kTileM;
   a.q = q;
   a.gq = gq;
-  a.q_scale = (float)(1.0 / sqrt((double)d.D));
+  a.q_scale = (float)(1.4426950408889634 / sqrt((double)d.D));   // log2(e) / sqrt(D)
   a.part_m = c->fa_ws;
   a.part_l = a.part_m + (size_t)m_tiles * n_q_heads;
   a.part_o = a.part_l + (size_t)m_tiles * n_q_heads;

@@ -289,6 +289,14 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t saddr) {
   return d;
 }
 
+// 2^x by the special-function unit (ex2.approx, relative error ~2^-22; results below
+// 2^-126 flush to zero).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // 32 lanes x 32-bit, 1 / 8 / 16 / 32 consecutive columns per thread (thread t <- lane
 // base + t); the address is the same for the whole warp.
 __device__ __forceinline__ uint32_t tmem_ld1(uint32_t taddr) {
