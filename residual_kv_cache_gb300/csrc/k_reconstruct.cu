@@ -97,7 +97,7 @@ constexpr uint32_t kRowTile16 = 16 * 128;            // one swizzle atom of a 16
 constexpr uint32_t kPBytes = 2 * kRowTile16;
 constexpr uint32_t kAttendBytes = kKVBytes + 2 * kPBytes;
 constexpr int kGroupBar0 = 9;     // named barriers 9..12: the four warps of one epilogue group
-constexpr int kVoteBar = 13;      // all 16 epilogue warps
+constexpr int kHalfBar0 = 13;     // 13, 14: the eight warps of groups 0-1, 2-3
 
 struct ReconArgs {
   const int32_t* seq;
@@ -705,7 +705,7 @@ __global__ void __launch_bounds__(kReconThreads, 1)
     auto setup_s = [&](int zb, RowState& st) -> bool {
       const bool w = mbar_wait(staged, staged_phase, abort_flag, a.status);
       bool wa = __all_sync(0xffffffffu, w);
-      if constexpr (kAttend) wa = bar_red_and(kVoteBar, 512, wa);
+      if constexpr (kAttend) wa = bar_red_and(kHalfBar0 + (wg >> 1), 256, wa);
       if (!wa) return false;
       staged_phase ^= 1u;
       const int* rec = sRec + row * kRecInts;
@@ -807,12 +807,13 @@ __global__ void __launch_bounds__(kReconThreads, 1)
     int cur_m = -1, tt = 0;
     bool ok = true;
     uint32_t s_phase = 0, o_phase = 0;                // restore + attention
-    // A wait that gives up makes the warp leave the unit loop.  Without kAttend the two
-    // warps of a pair (sharing reference slots and a named barrier) vote together; with
-    // kAttend all 16 epilogue warps do, since the four warps of a group also meet at a
-    // named barrier in the softmax: every warp then leaves at the same wait.
-    const int vote_id = kAttend ? kVoteBar : bar_id;
-    const int vote_n = kAttend ? 512 : 64;
+    // A wait that gives up makes the warp leave the unit loop, together with every warp
+    // it meets at a named barrier.  Without kAttend that is the pair sharing reference
+    // slots: the two vote.  With kAttend the four warps of a group also meet in the
+    // softmax, which joins groups 0 and 1 (and 2 and 3) through their pairs: the eight
+    // warps of each half vote together.  The two halves share no barrier.
+    const int vote_id = kAttend ? kHalfBar0 + (wg >> 1) : bar_id;
+    const int vote_n = kAttend ? 256 : 64;
     // V_hat^T P of the pair whose V unit is uv: lane d of the V accumulator, column g +
     // column gq + g = sum over the tile's tokens of p v_d; then the accumulator is free.
     auto finish_o = [&](int uv) -> bool {
