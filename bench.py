@@ -159,11 +159,11 @@ def algorithmic_work(w, n_comp: int, n_sel: int, ref_pos, T: int | None = None) 
 # while the kernel's code is unchanged since the capture (code_sha1 below).
 MEASURED_TRAFFIC = {
     ("llama8b", "rkv_reconstruct_kernel"): {"file": "k_reconstruct.cu",
-                                            "code_sha1": "04ba157c4bcef39262c86cfe863d8d5864d004bc",
-                                            "bytes": 10470400 + 86016},
+                                            "code_sha1": "5198262cc641e670ca2a24f8616c6b236a0804fa",
+                                            "bytes": 10437376 + 52480},
     ("qwen7b", "rkv_reconstruct_kernel"): {"file": "k_reconstruct.cu",
-                                           "code_sha1": "04ba157c4bcef39262c86cfe863d8d5864d004bc",
-                                           "bytes": 15946240 + 25549312},
+                                           "code_sha1": "5198262cc641e670ca2a24f8616c6b236a0804fa",
+                                           "bytes": 15855104 + 24869888},
     ("llama8b", "rkv_retrieve_kernel"): {"file": "k_retrieve.cu",
                                          "code_sha1": "aa7c494b08aad67b44f721081daffd90bc65a63e",
                                          "bytes": 134541056 + 3821568},
