@@ -229,6 +229,22 @@ def swiglu_hidden(x, Wc1, Wc2, mode: str = "operand"):
     return swish(x @ Wc1) * (x @ Wc2)
 
 
+def mean_hidden_from_refs(pool_vals, slots, Wc1, Wc2):
+    """The hidden row of f_c at the reference mean, with the mean's pre-activations
+    taken from the references' own: mean_i W = (1/k_i) sum_j (kv_j W) for j in R_i,
+    since x W is linear in x (section 2.3 maps the mean, which section 2.2 averages in
+    KV space).  The references are the FP8-decoded pool rows, exact in bf16, so no
+    operand is rounded; accumulation is float64.  This is the weight-stationary form of
+    the mean half of the encoder: the products kv_j W_c1 / W_c2 are fixed per reference
+    and can be kept beside the pool.
+    """
+    R = pool_vals[np.asarray(slots)]
+    k = len(slots)
+    a1 = (R @ Wc1).sum(axis=0) / k
+    a2 = (R @ Wc2).sum(axis=0) / k
+    return swish(a1) * a2
+
+
 def f_c(x, Wc1, Wc2, Wc3, mode: str = "operand"):
     """f_c(x) = (Swish(x W_c1) * x W_c2) W_c3 (row-vector convention)."""
     if mode == "operand":
@@ -435,20 +451,39 @@ def encode_token(kv_i, pos: int, pool: Pool, W, shape: Shape, mode: str = "opera
             "meta": meta[0], "overflow": bool(ovf[0])}
 
 
-def encode_tokens(kv, positions, pool: Pool, W, shape: Shape, mode: str = "operand"):
-    """encode_token over many tokens, batching the f_c products."""
+def encode_tokens(kv, positions, pool: Pool, W, shape: Shape, mode: str = "operand",
+                  mean_from: str = "row"):
+    """encode_token over many tokens, batching the f_c products.
+
+    mean_from="row" maps the mean row itself (f_c(mean), as written in section 2.3);
+    "refs" takes the mean's hidden row from the references' pre-activations
+    (``mean_hidden_from_refs``), the same value in exact arithmetic, rounded
+    differently: the mean is then never rounded to a tensor-core operand.
+    """
+    if mean_from not in ("row", "refs"):
+        raise ValueError("mean_from must be 'row' or 'refs'")
     kv = np.asarray(kv, np.float64)
     positions = np.asarray(positions, dtype=np.int64)
     n = len(positions)
     idx = np.full((n, shape.topk), -1, dtype=np.int64)
     dist = np.full((n, shape.topk), np.nan)
     means = np.zeros((n, shape.d_kv))
+    h_mean = np.zeros((n, shape.d_ff)) if mean_from == "refs" else None
     for r, p in enumerate(positions):
         slots, d = retrieve(kv[r], pool.vals, pool.pos, int(p), shape.topk)
         idx[r, : len(slots)] = slots
         dist[r, : len(slots)] = d
         means[r] = reference_mean(pool.vals, slots, mode)
-    z = residual_code(kv, means, W, mode) if n else np.zeros((0, shape.d_c))
+        if h_mean is not None:
+            h_mean[r] = mean_hidden_from_refs(pool.vals, slots, W["Wc1"], W["Wc2"])
+    if not n:
+        z = np.zeros((0, shape.d_c))
+    elif h_mean is None:
+        z = residual_code(kv, means, W, mode)
+    else:
+        x = F.bf16(kv) if mode == "operand" else kv
+        z = (swiglu_hidden(x, W["Wc1"], W["Wc2"], mode) - h_mean) @ W["Wc3"]
+        z = F.fp32(z) if mode == "operand" else z
     q, meta, ovf = quantize(z, shape.bits, shape.group, mode)
     return {"idx": idx, "dist": dist, "mean": means, "z": z, "q": q,
             "meta": meta, "overflow": ovf}
@@ -471,7 +506,8 @@ class Store:
         return pack_codes(self.q, self.shape.bits)
 
 
-def compress_sequence(kv, W, shape: Shape, mode: str = "operand") -> Store:
+def compress_sequence(kv, W, shape: Shape, mode: str = "operand",
+                      mean_from: str = "row") -> Store:
     """Write all T tokens: references go to the pool, the rest are encoded.
 
     A reference's own row gets idx [slot, -1, ...] and an all-zero code with
@@ -488,7 +524,7 @@ def compress_sequence(kv, W, shape: Shape, mode: str = "operand") -> Store:
     idx[pool.pos, 0] = np.arange(len(pool.pos))
     nonref = np.nonzero(~is_reference(np.arange(T), shape.stride, shape.ref_alpha,
                                       shape.ref_sink))[0]
-    enc = encode_tokens(kv[nonref], nonref, pool, W, shape, mode)
+    enc = encode_tokens(kv[nonref], nonref, pool, W, shape, mode, mean_from)
     idx[nonref] = enc["idx"]
     q[nonref] = enc["q"]
     meta[nonref] = enc["meta"]

@@ -448,3 +448,57 @@ def test_operand_and_fp64_modes_agree_loosely():
     Kb, Vb, _ = C.reconstruct(b, pos, W, "fp64")
     rel = np.linalg.norm(np.concatenate([Ka - Kb, Va - Vb])) / np.linalg.norm(np.concatenate([Kb, Vb]))
     assert rel < 5e-2
+
+
+def test_mean_hidden_from_reference_preactivations():
+    """The weight-stationary form of the mean's hidden row (ResidualKV notes §2.3, f_c at
+    the §2.2 mean): (1/k) sum_j r_j W taken per reference equals torch's
+    silu(mean W_c1) * (mean W_c2) at the exact float64 mean; one reference gives the
+    hidden row at that reference; repeating a reference or permuting the slots changes
+    nothing."""
+    import torch
+    rng = np.random.default_rng(11)
+    d_kv, d_ff = 64, 48
+    pool = rng.normal(size=(9, d_kv))
+    W1, W2 = rng.normal(size=(d_kv, d_ff)) / 8, rng.normal(size=(d_kv, d_ff)) / 8
+
+    def torch_hidden(x):
+        xt = torch.tensor(x)
+        return (torch.nn.functional.silu(xt @ torch.tensor(W1)) * (xt @ torch.tensor(W2))).numpy()
+
+    for slots in ([3], [0, 5], [1, 2, 7], [8, 4, 6, 0]):
+        got = C.mean_hidden_from_refs(pool, slots, W1, W2)
+        want = torch_hidden(pool[slots].mean(axis=0))
+        assert np.allclose(got, want, rtol=1e-11, atol=1e-12), slots
+    assert np.allclose(C.mean_hidden_from_refs(pool, [5], W1, W2), torch_hidden(pool[5]),
+                       rtol=1e-12, atol=1e-13)
+    assert np.allclose(C.mean_hidden_from_refs(pool, [5, 5], W1, W2),
+                       C.mean_hidden_from_refs(pool, [5], W1, W2), rtol=1e-13, atol=1e-14)
+    assert np.allclose(C.mean_hidden_from_refs(pool, [2, 7, 1], W1, W2),
+                       C.mean_hidden_from_refs(pool, [1, 2, 7], W1, W2), rtol=1e-13, atol=1e-14)
+
+
+def test_encoding_from_reference_preactivations():
+    """encode_tokens with the mean's hidden row from the references: in fp64 the same z
+    as mapping the mean row (linearity); in operand mode it differs only by the bf16
+    rounding the mean row gets as a tensor-core operand (well under 1 % of z here), and
+    the slots are the same."""
+    import synth
+    w = synth.workload("tiny")
+    kv = synth.gen_kv(w, 21).double().numpy()
+    W = {k: v.double().numpy() for k, v in synth.gen_weights(w, 22).items()}
+    sh = C.Shape(w.n_kv_heads, w.head_dim, w.d_c, w.d_ff, w.topk, w.group, w.bits, w.stride,
+                 w.rope_base)
+    pool = C.build_pool(kv, w.T, w.stride)
+    pos = np.array([9, 33, 100, 201, 255])
+    a = C.encode_tokens(kv[pos], pos, pool, W, sh, "fp64", "row")
+    b = C.encode_tokens(kv[pos], pos, pool, W, sh, "fp64", "refs")
+    assert np.array_equal(a["idx"], b["idx"])
+    assert np.allclose(a["z"], b["z"], rtol=1e-10, atol=1e-12)
+    c = C.encode_tokens(kv[pos], pos, pool, W, sh, "operand", "row")
+    e = C.encode_tokens(kv[pos], pos, pool, W, sh, "operand", "refs")
+    assert np.array_equal(c["idx"], e["idx"])
+    rel = np.linalg.norm(c["z"] - e["z"]) / np.linalg.norm(c["z"])
+    assert 0 < rel < 1e-2
+    with pytest.raises(ValueError):
+        C.encode_tokens(kv[pos], pos, pool, W, sh, "fp64", "mean")
