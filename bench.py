@@ -51,6 +51,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # reference schedule (ResidualKV notes section 2.6): alpha = 0, n_sink = 0 is the fixed
 # stride of the workload; --alpha / --sink time the dynamic stride instead
 SCHEDULE = {"alpha": 0.0, "sink": 0}
+# 1: the encoder takes the mean's pre-activations from per-reference products kept beside
+# the pool (the library's mean_precompute mode) instead of mapping the mean row
+ENCODER = {"mean_precompute": 0}
 BATCHED_SLACK = 1024          # decode positions a batched run may append after its prefill
 
 
@@ -66,7 +69,7 @@ def codec_config(rkv, w, T, batch=1):
                       topk=w.topk, group=w.group, bits=w.bits, ref_stride=w.stride,
                       kv_dtype=w.kv_dtype, out_dtype=w.out_dtype, rope_base=w.rope_base,
                       batch=batch, max_tokens=T, ref_alpha=SCHEDULE["alpha"],
-                      ref_sink=SCHEDULE["sink"])
+                      ref_sink=SCHEDULE["sink"], mean_precompute=ENCODER["mean_precompute"])
 
 
 def split_positions(ref_pos, T):
@@ -891,9 +894,12 @@ def step_config(run, world: int) -> dict:
         tok = run.B + run.B * int(round(run.w.sel_frac * run.T0))
     else:
         tok = run.tokens_written + run.tokens_read
-    return {"workload": run.describe(), "tokens_per_step": tok,
-            "l2": "flushed before every timed step",
-            "parallelism": f"replicas x{world} (independent sequences)"}
+    cfg = {"workload": run.describe(), "tokens_per_step": tok,
+           "l2": "flushed before every timed step",
+           "parallelism": f"replicas x{world} (independent sequences)"}
+    if ENCODER["mean_precompute"]:
+        cfg["encoder_mean"] = "per-reference pre-activations (mean_precompute=1)"
+    return cfg
 
 
 # ------------------------------------------------------------------ CUDA arm: the line
@@ -1118,12 +1124,15 @@ def main():
     ap.add_argument("--kernel-case", action="store_true",
                     help="run one layer's prefill and two restores, for kernel captures")
     ap.add_argument("--tokens", type=int, default=0, help="override T for --kernel-case")
+    ap.add_argument("--mean-precompute", action="store_true",
+                    help="encoder mean from per-reference pre-activations (mean_precompute=1)")
     args = ap.parse_args()
     if args.alpha < 0 or args.sink < 0:
         ap.error("--alpha and --sink must be >= 0")
     if args.steps < 1 or args.warmup < 0:
         ap.error("--steps must be >= 1 and --warmup >= 0")
     SCHEDULE.update(alpha=float(args.alpha), sink=int(args.sink))
+    ENCODER.update(mean_precompute=1 if args.mean_precompute else 0)
     if args.kernel_case:
         run_kernel_case(args)
     elif args.impl == "reference":

@@ -92,6 +92,17 @@ typedef struct {
   double ref_alpha;          /* alpha >= 0: growth of the dynamic stride (0 =
                                 fixed stride)                                 */
   int32_t ref_sink;          /* n_sink >= 0: sink tokens                       */
+  int32_t mean_precompute;   /* 0: the encoder maps each token's reference mean
+                                row (GEMM-1/2 over kv and mean rows); 1: it takes
+                                the mean's pre-activations from the references'
+                                own, kept beside the pool (mean W = (1/k) sum
+                                r_j W, §2.3): rkv_pool_append computes
+                                r [W_c1 | W_c2] in fp32 for each appended
+                                reference (a context-owned table, 8 d_ff bytes
+                                per pool slot), and rkv_compress's GEMM-1/2 runs
+                                on kv rows only.  The mean is then never rounded
+                                to a bf16 operand, so codes can differ from mode
+                                0 by one near rounding boundaries.            */
 } rkv_config;
 /*
  * Reference schedule (ResidualKV notes §2.6): a position is a reference iff it
@@ -345,7 +356,11 @@ int64_t rkv_launch_count(rkv_ctx* ctx);
  *       SwiGLU hidden rows h(kv_q) - h(mean_q) as two bf16 parts (hi = its bf16
  *       rounding, lo = the bf16 rounding of the rest);
  *   2 = Q, bf16 [rows, parts*2d_k]: the query rows, whose first 2d_k columns
- *       are bf16(kv) (parts = 1 for bf16 kv, 3 for fp32: hi, mid, lo pieces).
+ *       are bf16(kv) (parts = 1 for bf16 kv, 3 for fp32: hi, mid, lo pieces);
+ *   3 = P (mean_precompute only), fp32 [B R_cap rounded up to 128, 2*d_ff]:
+ *       row s R_cap + slot = r [W_c1 | W_c2] of that reference r, the columns
+ *       of each 256-column block being 128 W_c1 columns then the same 128 W_c2
+ *       columns (block n: hidden units 128 n .. 128 n + 127).
  * Valid until the next call on the context.
  */
 rkv_status rkv_debug_scratch(rkv_ctx* ctx, int32_t which, void** ptr, size_t* bytes);

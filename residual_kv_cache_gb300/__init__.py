@@ -44,7 +44,8 @@ class _Config(ctypes.Structure):
                 ("out_dtype", ctypes.c_int32), ("rope_base", ctypes.c_double),
                 ("batch", ctypes.c_int32), ("max_tokens", ctypes.c_int32),
                 ("max_refs", ctypes.c_int32), ("max_rows", ctypes.c_int32),
-                ("ref_alpha", ctypes.c_double), ("ref_sink", ctypes.c_int32)]
+                ("ref_alpha", ctypes.c_double), ("ref_sink", ctypes.c_int32),
+                ("mean_precompute", ctypes.c_int32)]
 
 
 class _Storage(ctypes.Structure):
@@ -193,13 +194,14 @@ class Config:
     max_rows: int = 0
     ref_alpha: float = 0.0     # dynamic-stride growth; 0 = fixed stride
     ref_sink: int = 0          # sink tokens kept as references ahead of the schedule
+    mean_precompute: int = 0   # 1: the mean's pre-activations from the references' own
 
     def to_c(self) -> _Config:
         return _Config(self.n_kv_heads, self.head_dim, self.d_c, self.d_ff, self.topk,
                        self.group, self.bits, self.ref_stride, _dtype_code(self.kv_dtype),
                        _dtype_code(self.out_dtype), float(self.rope_base), self.batch,
                        self.max_tokens, self.max_refs, self.max_rows, float(self.ref_alpha),
-                       self.ref_sink)
+                       self.ref_sink, self.mean_precompute)
 
     @property
     def d_kv(self) -> int:

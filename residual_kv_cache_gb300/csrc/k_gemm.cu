@@ -37,12 +37,35 @@ struct GemmShape {
   int m_tiles, n_tiles, nkb;  // tiles of 128 rows, tiles of BN columns, 64-wide k-blocks
   int b_kwrap;                // B's k-block coordinate is kb % b_kwrap
   int* status;
+  const int32_t* m_list;      // if set, row tile i is m_list[i] (device), else i
 };
+
+__device__ __forceinline__ int row_tile(const GemmShape& g, int i) {
+  return g.m_list ? g.m_list[i] : i;
+}
 
 struct Epi12Args {
   __nv_bfloat16* H;
   int dff;
   int rows;  // dense rows (kv and mean row pairs)
+};
+
+// mean_precompute, reference pre-activations: P[row] = r [W_c1 | W_c2] in fp32
+struct EpiPArgs {
+  float* P;
+  int64_t rows;  // B R_cap pool rows
+  int ld;        // 2 d_ff
+};
+
+// mean_precompute, GEMM-1/2 over kv rows only
+struct Epi12RArgs {
+  __nv_bfloat16* H;
+  int dff;
+  int rows;                // dense rows
+  const int32_t* q_dst;    // per dense row: storage row (seq T_cap + pos)
+  const int32_t* ref_idx;  // [B T_cap, topk] pool slots of each token
+  int topk, R_cap, T_cap;
+  const float* P;
 };
 
 struct Epi3Args {
@@ -127,6 +150,141 @@ struct Epi12 {
         dl[1] = make_uint4(wlo[4], wlo[5], wlo[6], wlo[7]);
       }
       bar_sync(1, 128);                                // the buffer is reused next chunk
+    }
+  }
+};
+
+// The fp32 accumulators of 128 pool rows x 256 columns (one W12 tile: 128 W_c1 then 128
+// W_c2 columns) stored as they are: row r of tile m is pool row 128 m + r.
+struct EpiP {
+  using Args = EpiPArgs;
+  static constexpr bool kSplitA = false;
+  static constexpr uint32_t kExchangeBytes = 0;
+  __device__ static void run(const Args& a, uint32_t tacc, int m, int n, int row_in_tile,
+                             int*, float*) {
+    const int64_t row = (int64_t)m * kTileM + row_in_tile;
+    const bool valid = row < a.rows;
+    float* dst = a.P + row * a.ld + (int64_t)n * 256;
+#pragma unroll 1
+    for (int c = 0; c < 8; ++c) {
+      uint32_t r[32];
+      tmem_ld32(tacc + c * 32, r);
+      tmem_ld_wait();
+      if (!valid) continue;
+      float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        d4[i] = make_float4(__uint_as_float(r[4 * i]), __uint_as_float(r[4 * i + 1]),
+                            __uint_as_float(r[4 * i + 2]), __uint_as_float(r[4 * i + 3]));
+    }
+  }
+};
+
+// GEMM-1/2 of 128 kv rows with the mean's hidden row taken from the references'
+// pre-activations: per token, the k_i pool slots' P rows summed over the tile's 128 hidden
+// units (gate and value columns), scaled by 1 / k_i (exact for k_i = 1, 2, 4; a correctly
+// rounded division for 3), and put through the same SwiGLU as the kv row; the thread of
+// token row q stores d = h(kv) - h(mean) as [d_hi | d_lo].
+// The gathers are cooperative: per 32-column chunk, a warp reads the P slices of its 32
+// tokens as whole 128-byte rows (lane l: token 4 i + l / 8, columns 4 (l % 8) ..), four
+// tokens per 16-byte load instruction, forms h(mean) column-wise into shared memory
+// (rows padded to 36 floats), and each thread then reads its own row back.
+struct Epi12R {
+  using Args = Epi12RArgs;
+  static constexpr bool kSplitA = false;
+  static constexpr int kRowF = 36;                           // padded h(mean) row, floats
+  static constexpr uint32_t kWarpBytes = 32 * kRowF * 4 + 32 * 4 * 4 + 32 * 4;
+  static constexpr uint32_t kExchangeBytes = 4 * kWarpBytes;
+  __device__ static void run(const Args& a, uint32_t tacc, int m, int n, int row_in_tile,
+                             int*, float* xch) {
+    const int ew = row_in_tile >> 5, l = row_in_tile & 31;
+    float* hm_s = xch + ew * (kWarpBytes / 4);               // [32][kRowF]
+    int* prow_s = reinterpret_cast<int*>(hm_s + 32 * kRowF);  // [32][4] P rows, -1 if none
+    float* kinv_s = reinterpret_cast<float*>(prow_s + 32 * 4);  // [32]: 1/k, or -3 for k = 3
+    const int64_t q = (int64_t)m * kTileM + row_in_tile;
+    const bool valid = q < a.rows;
+    {
+      int pr[4] = {-1, -1, -1, -1};
+      int k = 0;
+      if (valid) {
+        const int64_t dst = a.q_dst[q];
+        const int base = (int)(dst / a.T_cap) * a.R_cap;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const int slot = t < a.topk ? a.ref_idx[dst * a.topk + t] : -1;
+          if (slot >= 0 && slot < a.R_cap) pr[k++] = base + slot;
+        }
+      }
+      reinterpret_cast<int4*>(prow_s)[l] = make_int4(pr[0], pr[1], pr[2], pr[3]);
+      kinv_s[l] = k == 3 ? -3.0f : (k == 2 ? 0.5f : (k == 4 ? 0.25f : 1.0f));
+    }
+    __syncwarp();
+    const int sub = l >> 3, c4 = (l & 7) * 4;                // token within a group of 4, column
+    const int64_t ld = 2 * (int64_t)a.dff;
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      uint32_t g[32], v[32];
+      tmem_ld32(tacc + c * 32, g);
+      tmem_ld32(tacc + 128 + c * 32, v);
+      // h(mean) of the warp's 32 tokens, columns c4 .. c4 + 3 of this chunk
+      const int64_t col = (int64_t)n * 256 + c * 32 + c4;
+#pragma unroll 2
+      for (int i = 0; i < 8; ++i) {
+        const int j = 4 * i + sub;
+        const int4 pr = reinterpret_cast<const int4*>(prow_s)[j];
+        const int prs[4] = {pr.x, pr.y, pr.z, pr.w};
+        float4 sg = make_float4(0.f, 0.f, 0.f, 0.f), sv = sg;
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          if (prs[t] < 0) continue;
+          const float* base = a.P + (int64_t)prs[t] * ld + col;
+          const float4 x = __ldg(reinterpret_cast<const float4*>(base));
+          const float4 y = __ldg(reinterpret_cast<const float4*>(base + 128));
+          sg.x += x.x, sg.y += x.y, sg.z += x.z, sg.w += x.w;
+          sv.x += y.x, sv.y += y.y, sv.z += y.z, sv.w += y.w;
+        }
+        const float kv = kinv_s[j];
+        const float s1[4] = {sg.x, sg.y, sg.z, sg.w}, s2[4] = {sv.x, sv.y, sv.z, sv.w};
+        float h[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float m1 = kv < 0.f ? __fdiv_rn(s1[e], 3.0f) : s1[e] * kv;
+          const float m2 = kv < 0.f ? __fdiv_rn(s2[e], 3.0f) : s2[e] * kv;
+          h[e] = __fdividef(m1, 1.0f + __expf(-m1)) * m2;
+        }
+        *reinterpret_cast<float4*>(hm_s + j * kRowF + c4) = make_float4(h[0], h[1], h[2], h[3]);
+      }
+      __syncwarp();
+      tmem_ld_wait();
+      uint32_t whi[16], wlo[16];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 hm = *reinterpret_cast<const float4*>(hm_s + l * kRowF + 4 * i);
+        const float hms[4] = {hm.x, hm.y, hm.z, hm.w};
+        float d[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float a1 = __uint_as_float(g[4 * i + e]), a2 = __uint_as_float(v[4 * i + e]);
+          d[e] = __fdividef(a1, 1.0f + __expf(-a1)) * a2 - hms[e];
+        }
+#pragma unroll
+        for (int e = 0; e < 4; e += 2) {
+          const uint32_t hb = pack_bf16x2(d[e], d[e + 1]);
+          whi[2 * i + e / 2] = hb;
+          wlo[2 * i + e / 2] = pack_bf16x2(d[e] - __uint_as_float(hb << 16),
+                                           d[e + 1] - __uint_as_float(hb & 0xFFFF0000u));
+        }
+      }
+      __syncwarp();                                    // hm_s is rewritten next chunk
+      if (!valid) continue;
+      __nv_bfloat16* dst = a.H + q * (2 * (int64_t)a.dff) + (int64_t)n * 128 + c * 32;
+      uint4* dh = reinterpret_cast<uint4*>(dst);
+      uint4* dl = reinterpret_cast<uint4*>(dst + a.dff);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        dh[i] = make_uint4(whi[4 * i], whi[4 * i + 1], whi[4 * i + 2], whi[4 * i + 3]);
+        dl[i] = make_uint4(wlo[4 * i], wlo[4 * i + 1], wlo[4 * i + 2], wlo[4 * i + 3]);
+      }
     }
   }
 };
@@ -281,7 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int s = 0; s < STAGES; ++s) issued[s] = 0, issued_phase[s] = 0;
       bool ok = true;
       for (int t = blockIdx.x; t < n_tiles_total && ok; t += gridDim.x) {
-        const int m = t / g.n_tiles, n = t % g.n_tiles;
+        const int m = row_tile(g, t / g.n_tiles), n = t % g.n_tiles;
         for (int kb = 0; kb < g.nkb; ++kb) {
           if (!mbar_wait(&empty[ring.stage], ring.phase ^ 1u, abort_flag, g.status)) {
             ok = false;
@@ -366,7 +524,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     for (int t = blockIdx.x; t < n_tiles_total; t += gridDim.x) {
-      const int m = t / g.n_tiles, n = t % g.n_tiles;
+      const int m = row_tile(g, t / g.n_tiles), n = t % g.n_tiles;
       // An epilogue that swaps rows between its warps (named barriers inside) goes on
       // only if all four warps' waits succeeded, so no warp is left alone at a barrier.
       bool ok = warp_wait(&tfull[acc], acc_phase, abort_flag, g.status);
@@ -419,10 +577,21 @@ cudaError_t run_gemm(rkv_ctx* c, const CUtensorMap& tA, const CUtensorMap& tA2, 
 
 }  // namespace
 
-cudaError_t launch_gemm12(rkv_ctx* c, const PassPlan& p, cudaStream_t s) {
+cudaError_t launch_gemm12(rkv_ctx* c, const PassPlan& p, const int32_t* plan, cudaStream_t s) {
   const Dims& d = c->d;
   const int rows = p.n_rows;                    // dense rows
-  GemmShape g;
+  GemmShape g{};
+  if (d.mean_pre) {
+    g.m_tiles = (rows + kTileM - 1) / kTileM;
+    g.n_tiles = (2 * d.dff) / kEncN;
+    g.nkb = d.dkv / kTileK;
+    g.b_kwrap = g.nkb;
+    g.status = c->status;
+    Epi12RArgs ea{c->H, d.dff, rows, plan + (p.dense ? p.off_d_dst : p.off_q_dst),
+                  c->st.ref_idx, d.topk, d.R_cap, d.T_cap, c->P};
+    const CUtensorMap& tA = p.dense ? c->tm_qd128 : c->tm_qa128;
+    return run_gemm<kEncN, 4, Epi12R>(c, tA, tA, c->tm_w12, g, ea, "rkv_gemm12_refpre_kernel", s);
+  }
   g.m_tiles = (rows + kTileM / 2 - 1) / (kTileM / 2);
   g.n_tiles = (2 * d.dff) / kEncN;
   g.nkb = d.dkv / kTileK;
@@ -433,10 +602,24 @@ cudaError_t launch_gemm12(rkv_ctx* c, const PassPlan& p, cudaStream_t s) {
                                    "rkv_gemm12_swiglu_kernel", s);
 }
 
+cudaError_t launch_pool_preact(rkv_ctx* c, const int32_t* tiles, int n_tiles, cudaStream_t s) {
+  const Dims& d = c->d;
+  GemmShape g{};
+  g.m_tiles = n_tiles;
+  g.n_tiles = (2 * d.dff) / kEncN;
+  g.nkb = d.dkv / kTileK;
+  g.b_kwrap = g.nkb;
+  g.status = c->status;
+  g.m_list = tiles;
+  EpiPArgs ea{c->P, (int64_t)d.B * d.R_cap, 2 * d.dff};
+  return run_gemm<kEncN, 4, EpiP>(c, c->tm_pool128, c->tm_pool128, c->tm_w12, g, ea,
+                                  "rkv_pool_preact_kernel", s);
+}
+
 cudaError_t launch_gemm3_quant(rkv_ctx* c, const PassPlan& p, const int32_t* plan,
                                cudaStream_t s) {
   const Dims& d = c->d;
-  GemmShape g;
+  GemmShape g{};
   g.m_tiles = (p.n_rows + kTileM - 1) / kTileM;  // dense rows
   g.nkb = (2 * d.dff) / kTileK;
   g.b_kwrap = d.dff / kTileK;

@@ -114,6 +114,9 @@ rkv_status derive(const rkv_config* c, Dims* d) {
   if (!(c->ref_alpha >= 0.0 && c->ref_alpha <= 1e6))
     return fail(RKV_EINVAL, "ref_alpha must be in [0, 1e6]");
   if (c->ref_sink < 0) return fail(RKV_EINVAL, "ref_sink must be >= 0");
+  if (!(c->mean_precompute == 0 || c->mean_precompute == 1))
+    return fail(RKV_EINVAL, "mean_precompute must be 0 or 1");
+  d->mean_pre = c->mean_precompute;
   d->alpha = c->ref_alpha;
   d->sink = c->ref_sink;
   d->fixed = c->ref_alpha == 0.0 && c->ref_sink == 0;
@@ -455,6 +458,8 @@ rkv_status rkv_create(const rkv_config* cfg, const void* Wc1, const void* Wc2, c
   }
   ALLOC(c->plan_dev[0], (size_t)c->plan_ints * 4);
   ALLOC(c->plan_dev[1], (size_t)c->plan_ints * 4);
+  if (d.mean_pre)
+    ALLOC(c->P, (((size_t)d.B * d.R_cap + kTileM - 1) / kTileM * kTileM) * 2 * d.dff * sizeof(float));
   ALLOC(c->status, 512);
 #undef ALLOC
   if (fail_status != RKV_OK) {
@@ -517,6 +522,11 @@ rkv_status rkv_create(const rkv_config* cfg, const void* Wc1, const void* Wc2, c
   if (d.dc % 128 == 0)
     ok &= make_map(&c->tm_w3_128, c->w3, d.dff, d.dc, (uint64_t)d.dff * 2, 128u);
   ok &= make_map(&c->tm_wd, c->wd, d.dc, dkv, (uint64_t)d.dc * 2, kDecN);
+  if (d.mean_pre) {
+    ok &= make_map(&c->tm_pool128, c->pool_bf16, dkv, (uint64_t)d.B * d.R_cap, dkv * 2, kTileM);
+    ok &= make_map(&c->tm_qa128, c->Q, dkv, c->m_cap, (uint64_t)d.parts * dkv * 2, kTileM);
+    if (c->Qd) ok &= make_map(&c->tm_qd128, c->Qd, dkv, c->max_rows, dkv * 2, kTileM);
+  }
   if (!ok) {
     rkv_free(c);
     return fail(RKV_ECUDA, "cuTensorMapEncodeTiled rejected a tensor map");
@@ -588,8 +598,28 @@ rkv_status rkv_pool_append(rkv_ctx* c, const void* kv, int64_t kv_row_stride,
       h[4 * i + 2] = p;
       h[4 * i + 3] = s * d.T_cap + p;
     }
-    CUDA_OK(staging_upload(c, b, 0, 4 * m, st));
+    // with mean_precompute, the pool tiles (128 slots) these references fall in, in
+    // increasing order, follow the rows in the plan
+    int n_pt = 0;
+    if (d.mean_pre) {
+      int last = -1;
+      bool sorted = true;
+      for (int i = 0; i < m; ++i) {
+        const int t = h[4 * i + 1] / kTileM;
+        if (t != last) {
+          if (t < last) sorted = false;
+          h[4 * m + n_pt++] = t;
+          last = t;
+        }
+      }
+      if (!sorted) {
+        std::sort(h + 4 * m, h + 4 * m + n_pt);
+        n_pt = (int)(std::unique(h + 4 * m, h + 4 * m + n_pt) - (h + 4 * m));
+      }
+    }
+    CUDA_OK(staging_upload(c, b, 0, 4 * m + n_pt, st));
     CUDA_OK(launch_pool_append(c, kv, kv_row_stride, c->plan_dev[b], m, st));
+    if (n_pt) CUDA_OK(launch_pool_preact(c, c->plan_dev[b] + 4 * m, n_pt, st));
   }
   c->pool_count = next;
   return RKV_OK;
@@ -755,8 +785,8 @@ rkv_status rkv_compress(rkv_ctx* c, const void* kv, int64_t kv_row_stride, const
     if (p.dense) CUDA_OK(launch_prep_dense(c, kv, kv_row_stride, plan + p.off_d_src, m, st));
     CUDA_OK(launch_retrieve(c, p, plan, st));
     CUDA_OK(launch_retrieve_merge(c, p, plan, st));
-    CUDA_OK(launch_mean_rows(c, p, plan, st));
-    CUDA_OK(launch_gemm12(c, p, st));
+    if (!d.mean_pre) CUDA_OK(launch_mean_rows(c, p, plan, st));
+    CUDA_OK(launch_gemm12(c, p, plan, st));
     CUDA_OK(launch_gemm3_quant(c, p, plan, st));
   }
   return RKV_OK;
@@ -852,6 +882,7 @@ void rkv_free(rkv_ctx* c) {
   cudaFree(c->attn_ws);
   cudaFree(c->attn_count);
   cudaFree(c->fa_ws);
+  cudaFree(c->P);
   cudaFree(c->w3);
   cudaFree(c->wd);
   cudaFree(c->rope_lo);
@@ -922,8 +953,11 @@ rkv_status rkv_debug_scratch(rkv_ctx* c, int32_t which, void** ptr, size_t* byte
   } else if (which == 2) {
     *ptr = c->Q;
     *bytes = (size_t)c->m_cap * c->d.parts * c->d.dkv * 2;
+  } else if (which == 3 && c->P) {
+    *ptr = c->P;
+    *bytes = (((size_t)c->d.B * c->d.R_cap + kTileM - 1) / kTileM * kTileM) * 2 * c->d.dff * 4;
   } else {
-    return fail(RKV_EINVAL, "which must be 0, 1 or 2");
+    return fail(RKV_EINVAL, "which must be 0, 1, 2 (or 3 with mean_precompute)");
   }
   return RKV_OK;
 }

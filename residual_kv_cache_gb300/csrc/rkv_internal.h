@@ -30,6 +30,7 @@ struct Dims {
   int fixed;       // the schedule is pos % stride == 0
   int n_sched;     // schedule positions below T_cap
   int kv_f32, out_f32;
+  int mean_pre;    // the mean's pre-activations from the references' (table P)
   int parts;       // 3 bf16 pieces per fp32 query element, 1 for bf16
   int n_hi;        // rows of the high RoPE table
 };
@@ -104,6 +105,8 @@ struct rkv_ctx {
   cudaEvent_t plan_copied[2] = {nullptr, nullptr};
   int plan_ints = 0;
   int plan_flip = 0;
+  float* P = nullptr;             // mean_precompute: [B R_cap rounded up to 128, 2 d_ff] fp32
+                                  // r [W_c1 | W_c2] of each pool slot, columns in W12's order
   int* status = nullptr;          // device status word (first 64 bytes of a 512-byte block)
   const uint8_t* zero_line = nullptr;   // 256 zero bytes in the same block (gather source)
 
@@ -111,6 +114,7 @@ struct rkv_ctx {
   CUtensorMap tm_q, tm_pool, tm_w12, tm_h3, tm_w3, tm_w3_128, tm_wd;
   CUtensorMap tm_qa, tm_m;        // GEMM-1/2 A halves: the bf16 kv piece of Q, and M (64 rows)
   CUtensorMap tm_qd;              // GEMM-1/2 kv half from Qd (dense passes)
+  CUtensorMap tm_pool128, tm_qa128, tm_qd128;   // 128-row boxes: mean_precompute GEMMs
 
   // host mirror of each sequence's pool fill
   std::vector<int32_t> pool_count;
@@ -141,9 +145,14 @@ cudaError_t launch_retrieve(rkv_ctx* c, const PassPlan& p, const int32_t* plan, 
 cudaError_t launch_retrieve_merge(rkv_ctx* c, const PassPlan& p, const int32_t* plan,
                                   cudaStream_t s);
 cudaError_t launch_mean_rows(rkv_ctx* c, const PassPlan& p, const int32_t* plan, cudaStream_t s);
-cudaError_t launch_gemm12(rkv_ctx* c, const PassPlan& p, cudaStream_t s);
+// GEMM-1/2 and the hidden difference; with mean_precompute over kv rows only, the mean's
+// hidden row from P (plan: the pass's plan, for each dense row's storage row)
+cudaError_t launch_gemm12(rkv_ctx* c, const PassPlan& p, const int32_t* plan, cudaStream_t s);
 cudaError_t launch_gemm3_quant(rkv_ctx* c, const PassPlan& p, const int32_t* plan,
                                cudaStream_t s);
+// mean_precompute: P rows of the pool tiles listed in `tiles` (128 slots each, indices
+// into [B R_cap] rows), from the bf16 pool copy
+cudaError_t launch_pool_preact(rkv_ctx* c, const int32_t* tiles, int n_tiles, cudaStream_t s);
 cudaError_t launch_reconstruct(rkv_ctx* c, const int32_t* seq, const int32_t* pos, int n_sel,
                                void* k_out, void* v_out, cudaStream_t s);
 

@@ -32,13 +32,14 @@ def device_bytes(ptr: int, nbytes: int) -> torch.Tensor:
 
 def make_codec(w: synth.Workload, W: dict, T: int, batch: int = 1, max_rows: int = 0,
                out_dtype: str | None = None, bits: int | None = None, alpha: float = 0.0,
-               sink: int = 0):
+               sink: int = 0, mean_precompute: int = 0):
     from residual_kv_cache_gb300 import Codec, Config
     cfg = Config(n_kv_heads=w.n_kv_heads, head_dim=w.head_dim, d_c=w.d_c, d_ff=w.d_ff,
                  topk=w.topk, group=w.group, bits=w.bits if bits is None else bits,
                  ref_stride=w.stride, kv_dtype=w.kv_dtype,
                  out_dtype=out_dtype or w.out_dtype, rope_base=w.rope_base, batch=batch,
-                 max_tokens=T, max_rows=max_rows, ref_alpha=alpha, ref_sink=sink)
+                 max_tokens=T, max_rows=max_rows, ref_alpha=alpha, ref_sink=sink,
+                 mean_precompute=mean_precompute)
     Wd = {k: v.cuda().contiguous() for k, v in W.items()}
     return Codec(cfg, Wd)
 
@@ -159,6 +160,13 @@ def hidden_bounds(X: np.ndarray, Wc1: np.ndarray, Wc2: np.ndarray):
     a1, a2 = X @ Wc1, X @ Wc2
     da1 = fp32_chunked_bound(X, Wc1)
     da2 = fp32_chunked_bound(X, Wc2)
+    return swiglu_bounds(a1, a2, da1, da2)
+
+
+def swiglu_bounds(a1, a2, da1, da2):
+    """h = Swish(a1) * a2 for exact pre-activations, and the bound dh on a fp32
+    evaluation from pre-activations within da1, da2 of them (Swish with a fast
+    exponential and division, relative error <= |a1| 2^-22 + 2^-19, then the product)."""
     with np.errstate(over="ignore"):
         sig = 1.0 / (1.0 + np.exp(-a1))
     sw = a1 * sig
@@ -233,6 +241,34 @@ def encoder_intervals(kv64_rows, pool_vals, idx_rows, W64):
     hm, dhm = hidden_bounds(xm, W64["Wc1"], W64["Wc2"])
     d = hk - hm
     dd = dhk + dhm + 2.0 ** -23 * np.abs(d)          # + the fp32 subtraction
+    z, w = z_bounds(d, dd, W64["Wc3"])
+    return dict(d=d, dd=dd, z=z, w=w)
+
+
+def encoder_intervals_refs(kv64_rows, pool_vals, idx_rows, W64):
+    """encoder_intervals for the mean's pre-activations taken from the references' own
+    (mean_precompute): per slot P = fl32(r [W_c1 | W_c2]) within the chunked fp32 bound,
+    the fp32 sum of the token's k <= 4 P rows (<= 3 additions, 2^-23 of the running sum
+    each), the scaling by 1/k (exact for k = 1, 2, 4; one rounding for 3), then the same
+    Swish, subtraction and GEMM-3 bounds."""
+    xk = F.bf16(kv64_rows)
+    hk, dhk = hidden_bounds(xk, W64["Wc1"], W64["Wc2"])
+    P1, P2 = pool_vals @ W64["Wc1"], pool_vals @ W64["Wc2"]
+    dP1, dP2 = fp32_chunked_bound(pool_vals, W64["Wc1"]), fp32_chunked_bound(pool_vals, W64["Wc2"])
+    n = len(idx_rows)
+    a1 = np.zeros((n, P1.shape[1]))
+    a2, da1, da2 = np.zeros_like(a1), np.zeros_like(a1), np.zeros_like(a1)
+    for r, i in enumerate(idx_rows):
+        s = i[i >= 0]
+        k = len(s)
+        a1[r], a2[r] = P1[s].sum(0) / k, P2[s].sum(0) / k
+        sum_err = 3 * 2.0 ** -23 * (np.abs(P1[s]).sum(0) + dP1[s].sum(0))
+        da1[r] = (dP1[s].sum(0) + sum_err) / k + 2.0 ** -24 * np.abs(a1[r])
+        sum_err = 3 * 2.0 ** -23 * (np.abs(P2[s]).sum(0) + dP2[s].sum(0))
+        da2[r] = (dP2[s].sum(0) + sum_err) / k + 2.0 ** -24 * np.abs(a2[r])
+    hm, dhm = swiglu_bounds(a1, a2, da1, da2)
+    d = hk - hm
+    dd = dhk + dhm + 2.0 ** -23 * np.abs(d)
     z, w = z_bounds(d, dd, W64["Wc3"])
     return dict(d=d, dd=dd, z=z, w=w)
 
