@@ -66,6 +66,7 @@ struct Epi12RArgs {
   const int32_t* ref_idx;  // [B T_cap, topk] pool slots of each token
   int topk, R_cap, T_cap;
   const float* P;
+  int zero_row;            // a row of P that holds zeros (stands in for a missing slot)
 };
 
 struct Epi3Args {
@@ -199,12 +200,12 @@ struct Epi12R {
                              int*, float* xch) {
     const int ew = row_in_tile >> 5, l = row_in_tile & 31;
     float* hm_s = xch + ew * (kWarpBytes / 4);               // [32][kRowF]
-    int* prow_s = reinterpret_cast<int*>(hm_s + 32 * kRowF);  // [32][4] P rows, -1 if none
+    int* prow_s = reinterpret_cast<int*>(hm_s + 32 * kRowF);  // [32][4] P rows (zero row if none)
     float* kinv_s = reinterpret_cast<float*>(prow_s + 32 * 4);  // [32]: 1/k, or -3 for k = 3
     const int64_t q = (int64_t)m * kTileM + row_in_tile;
     const bool valid = q < a.rows;
     {
-      int pr[4] = {-1, -1, -1, -1};
+      int pr[4] = {a.zero_row, a.zero_row, a.zero_row, a.zero_row};
       int k = 0;
       if (valid) {
         const int64_t dst = a.q_dst[q];
@@ -228,15 +229,14 @@ struct Epi12R {
       tmem_ld32(tacc + 128 + c * 32, v);
       // h(mean) of the warp's 32 tokens, columns c4 .. c4 + 3 of this chunk
       const int64_t col = (int64_t)n * 256 + c * 32 + c4;
-#pragma unroll 2
+#pragma unroll 4
       for (int i = 0; i < 8; ++i) {
         const int j = 4 * i + sub;
         const int4 pr = reinterpret_cast<const int4*>(prow_s)[j];
         const int prs[4] = {pr.x, pr.y, pr.z, pr.w};
         float4 sg = make_float4(0.f, 0.f, 0.f, 0.f), sv = sg;
 #pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          if (prs[t] < 0) continue;
+        for (int t = 0; t < 4; ++t) {              // missing slots read the zero row
           const float* base = a.P + (int64_t)prs[t] * ld + col;
           const float4 x = __ldg(reinterpret_cast<const float4*>(base));
           const float4 y = __ldg(reinterpret_cast<const float4*>(base + 128));
@@ -587,8 +587,9 @@ cudaError_t launch_gemm12(rkv_ctx* c, const PassPlan& p, const int32_t* plan, cu
     g.nkb = d.dkv / kTileK;
     g.b_kwrap = g.nkb;
     g.status = c->status;
+    const int zero_row = (d.B * d.R_cap + kTileM - 1) / kTileM * kTileM;   // past the tiles
     Epi12RArgs ea{c->H, d.dff, rows, plan + (p.dense ? p.off_d_dst : p.off_q_dst),
-                  c->st.ref_idx, d.topk, d.R_cap, d.T_cap, c->P};
+                  c->st.ref_idx, d.topk, d.R_cap, d.T_cap, c->P, zero_row};
     const CUtensorMap& tA = p.dense ? c->tm_qd128 : c->tm_qa128;
     return run_gemm<kEncN, 4, Epi12R>(c, tA, tA, c->tm_w12, g, ea, "rkv_gemm12_refpre_kernel", s);
   }

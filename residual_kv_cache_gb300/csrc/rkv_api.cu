@@ -458,8 +458,9 @@ rkv_status rkv_create(const rkv_config* cfg, const void* Wc1, const void* Wc2, c
   }
   ALLOC(c->plan_dev[0], (size_t)c->plan_ints * 4);
   ALLOC(c->plan_dev[1], (size_t)c->plan_ints * 4);
-  if (d.mean_pre)
-    ALLOC(c->P, (((size_t)d.B * d.R_cap + kTileM - 1) / kTileM * kTileM) * 2 * d.dff * sizeof(float));
+  // P: the pool's rows rounded up to whole 128-row tiles, then one zero row
+  const size_t p_rows = ((size_t)d.B * d.R_cap + kTileM - 1) / kTileM * kTileM + 1;
+  if (d.mean_pre) ALLOC(c->P, p_rows * 2 * d.dff * sizeof(float));
   ALLOC(c->status, 512);
 #undef ALLOC
   if (fail_status != RKV_OK) {
@@ -539,6 +540,7 @@ rkv_status rkv_create(const rkv_config* cfg, const void* Wc1, const void* Wc2, c
   if (e == cudaSuccess) e = cudaMemsetAsync(c->pool_bf16, 0, (size_t)d.B * d.R_cap * d.dkv * 2, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(c->H, 0, (size_t)2 * c->m_cap * d.dff * 2, s);
   if (e == cudaSuccess) e = cudaMemsetAsync(c->attn_count, 0, sizeof(int) * d.N, s);
+  if (e == cudaSuccess && c->P) e = cudaMemsetAsync(c->P, 0, p_rows * 2 * d.dff * sizeof(float), s);
   if (e == cudaSuccess) e = launch_init_storage(c, s);
   if (e == cudaSuccess)
     e = launch_repack_weights(c, static_cast<const __nv_bfloat16*>(Wc1),
