@@ -619,6 +619,7 @@ rkv_status rkv_pool_append(rkv_ctx* c, const void* kv, int64_t kv_row_stride,
         n_pt = (int)(std::unique(h + 4 * m, h + 4 * m + n_pt) - (h + 4 * m));
       }
     }
+    if (4 * m + n_pt > c->plan_ints) return fail(RKV_ECAPACITY, "append plan exceeds the staging buffer");
     CUDA_OK(staging_upload(c, b, 0, 4 * m + n_pt, st));
     CUDA_OK(launch_pool_append(c, kv, kv_row_stride, c->plan_dev[b], m, st));
     if (n_pt) CUDA_OK(launch_pool_preact(c, c->plan_dev[b] + 4 * m, n_pt, st));
