@@ -206,3 +206,22 @@ def test_mode_is_validated():
     c = make_codec(w, synth.gen_weights(w, 71), T=256)
     with pytest.raises(rkv.RkvError):
         c.debug_scratch(3)                       # no table without the mode
+
+
+@cuda
+def test_dynamic_schedule_and_int2():
+    """The dynamic-stride schedule (alpha = 0.1, two sink tokens) with INT2 codes: the pool
+    tiles a call touches follow the schedule's slots."""
+    w = synth.workload("llama8b")
+    T = 1024
+    kv = synth.gen_kv(w, 80, T=T)
+    W = synth.gen_weights(w, 81)
+    c = make_codec(w, W, T=T, bits=2, alpha=0.1, sink=2, mean_precompute=1)
+    ref, non = gpu_prefill(c, kv.cuda(), w.stride, alpha=0.1, sink=2)
+    torch.cuda.synchronize()
+    assert c.get_status() == 0
+    sh = C.Shape(**{**oracle_shape(w, 0.1, 2).__dict__, "bits": 2})
+    st = C.compress_sequence(np64(kv), _weights64(W), sh, "operand", mean_from="refs")
+    rows = _same_idx_rows(c, st, non)
+    assert len(rows) >= 0.99 * len(non)
+    _codes_rule(c, st, sh, rows, "dyn int2", np64(kv), _weights64(W))

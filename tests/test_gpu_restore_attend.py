@@ -243,3 +243,27 @@ def test_fused_rejects_unsupported_shapes(llama_store):
     f = make_codec(wl, synth.gen_weights(wl, 1411), T=256, out_dtype="fp32")
     with pytest.raises(rkv.RkvError):
         f.restore_attend(zero, sel, torch.zeros(8, 128, device="cuda"))
+
+
+@cuda
+def test_fused_selection_over_two_sequences():
+    """A selection drawn from two sequences of one context: one softmax over all its rows,
+    the same as restoring them and attending over the restored rows."""
+    w = synth.workload("llama8b")
+    T = 1024
+    kvs = [synth.gen_kv(w, 1420 + s, T=T) for s in range(2)]
+    c = make_codec(w, synth.gen_weights(w, 1422), T=T, batch=2, out_dtype="bf16")
+    for s in range(2):
+        gpu_prefill(c, kvs[s].cuda(), w.stride, seq_id=s)
+    torch.cuda.synchronize()
+    assert c.get_status() == 0
+    g = torch.Generator().manual_seed(1423)
+    seq = torch.randint(0, 2, (900,), generator=g, dtype=torch.int32).cuda()
+    pos = torch.randint(0, T, (900,), generator=g, dtype=torch.int32).cuda()
+    q = _q(32, 128, 1424).cuda()
+    out = c.restore_attend(seq, pos, q)
+    K, V = c.reconstruct(seq, pos)
+    torch.cuda.synchronize()
+    assert c.get_status() == 0
+    ref = A.sparse_attention(q.double().cpu().numpy(), np64(K), np64(V))
+    assert rel_fro(np64(out), ref) <= TOL_SAME_ROWS
