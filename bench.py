@@ -412,8 +412,13 @@ class StackRun:
         odt = torch.float32 if w.out_dtype == "fp32" else torch.bfloat16
         self.k_out = torch.empty((self.n_sel, w.n_kv_heads, w.head_dim), dtype=odt, device=dev)
         self.v_out = torch.empty_like(self.k_out)
+        # a decode step restores every layer's selection in one launch, each layer into its
+        # own K and V (rkv_reconstruct_multi); one layer uses the single restore
+        self.k_outs = [self.k_out] + [torch.empty_like(self.k_out) for _ in range(self.L - 1)]
+        self.v_outs = [self.v_out] + [torch.empty_like(self.k_out) for _ in range(self.L - 1)]
         self.tokens_written = self.L * w.T
         self.tokens_read = w.steps * self.L * self.n_sel
+        self.read_kernel = "rkv_reconstruct_multi_kernel" if self.L > 1 else "rkv_reconstruct_kernel"
 
     def write(self, kvs):
         for c, kv in zip(self.codecs, kvs):
@@ -421,14 +426,17 @@ class StackRun:
             c.pool_append(kv, self.zref, self.ref, src_rows=self.ref)
             c.compress(kv, self.znon, self.non, src_rows=self.non)
 
-    def read(self, sels, k_out, v_out):
+    def read(self, sels, k_outs, v_outs):
+        import residual_kv_cache_gb300 as rkv
         for row in sels:
-            for c, sel in zip(self.codecs, row):
-                c.reconstruct(self.seq0, sel, k_out, v_out)
+            if self.L > 1:
+                rkv.reconstruct_multi(self.codecs, [self.seq0] * self.L, list(row), k_outs, v_outs)
+            else:
+                self.codecs[0].reconstruct(self.seq0, row[0], k_outs[0], v_outs[0])
 
     def step(self):
         self.write(self.kv)
-        self.read(self.sels, self.k_out, self.v_out)
+        self.read(self.sels, self.k_outs, self.v_outs)
 
     def work_per_step(self) -> dict:
         w = self.w
@@ -436,7 +444,8 @@ class StackRun:
         out = {}
         for k, v in one.items():
             mult = self.L * (w.steps if k == "rkv_reconstruct_kernel" else 1)
-            out[k] = {"flops": v["flops"] * mult, "bytes": v["bytes"] * mult}
+            out[self.read_kernel if k == "rkv_reconstruct_kernel" else k] = {
+                "flops": v["flops"] * mult, "bytes": v["bytes"] * mult}
         return out
 
     def describe(self) -> str:
@@ -467,8 +476,9 @@ class StackRun:
         sel_host = torch.stack([torch.stack([s.cpu() for s in row]) for row in self.sels]).pin_memory()
         kv_buf = [[torch.empty_like(kv) for kv in self.kv] for _ in range(2)]
         sel_buf = [torch.empty(sel_host.shape, dtype=torch.int32, device=dev) for _ in range(2)]
-        k_dev = [torch.empty_like(self.k_out) for _ in range(2)]
-        v_dev = [torch.empty_like(self.k_out) for _ in range(2)]
+        # per layer its own K and V; the last layer's (the one read back) double-buffered
+        k_dev = [self.k_outs[:-1] + [torch.empty_like(self.k_out)] for _ in range(2)]
+        v_dev = [self.v_outs[:-1] + [torch.empty_like(self.k_out)] for _ in range(2)]
         k_host = torch.empty(self.k_out.shape, dtype=self.k_out.dtype).pin_memory()
         v_host = torch.empty_like(k_host).pin_memory()
         copy = torch.cuda.Stream(dev)
@@ -509,8 +519,8 @@ class StackRun:
             result_ready[b].record(stream)
             with torch.cuda.stream(copy):
                 copy.wait_event(result_ready[b])
-                k_host.copy_(k_dev[b], non_blocking=True)
-                v_host.copy_(v_dev[b], non_blocking=True)
+                k_host.copy_(k_dev[b][-1], non_blocking=True)
+                v_host.copy_(v_dev[b][-1], non_blocking=True)
                 result_read[b].record(copy)
 
         def run(n):
@@ -760,8 +770,9 @@ def run_workload(name, ctx, seed, with_e2e=True, with_cpu=True):
     work = run.work_per_step()
     rows = kernel_rows(ktimes, work, args.steps, peaks)
     roof = roofline_of(rows, work, peaks, kind, name)
-    read_ms = ktimes.get("rkv_reconstruct_kernel", (0, 0.0))[1] / args.steps
-    write_ms = sum(ms for k, (n, ms) in ktimes.items() if k != "rkv_reconstruct_kernel") / args.steps
+    read_k = ("rkv_reconstruct_kernel", "rkv_reconstruct_multi_kernel")
+    read_ms = sum(ms for k, (n, ms) in ktimes.items() if k in read_k) / args.steps
+    write_ms = sum(ms for k, (n, ms) in ktimes.items() if k not in read_k) / args.steps
     out = {"workload": name, "value": round(value, 1), "unit": UNIT, "ms_per_step": round(t_ms, 4),
            "config": step_config(run, ctx.world), "roofline": roof,
            "kernels": rows, "gpu_launches": int(launches_timed), "clocks": clk,
@@ -1100,10 +1111,29 @@ def run_kernel_case(args):
         codec.sparse_attention(q, K, V)             # the sparse layer's attention over them
         if fuse:
             codec.restore_attend(zero, sel, q)          # the same read, restored on chip
+    # with --layers L > 1: L - 1 more layers prefilled the same way, then two decode steps
+    # restoring all L layers' selections in one launch each (rkv_reconstruct_multi)
+    codecs = [codec]
+    for l in range(1, args.layers):
+        kvl = synth.gen_kv(w, 1000 + 7 * l, device=str(dev) if w.T > 65536 else "cpu").to(dev)
+        Wl = {k: v.to(dev) for k, v in synth.gen_weights(w, 1001 + 7 * l).items()}
+        cl = rkv.Codec(cfg, Wl, device=dev)
+        cl.pool_append(kvl, np.zeros_like(ref), ref, src_rows=ref)
+        cl.compress(kvl, np.zeros_like(non), non, src_rows=non)
+        codecs.append(cl)
+        del kvl
+    if args.layers > 1:
+        for s in range(2):
+            sels = [(synth.gen_block_selection(w.T, w.sel_block, w.sel_frac, 1020 + 31 * s + l)
+                     if w.sel_block > 1 else synth.gen_selection(w.T, w.n_sel, 1020 + 31 * s + l)).to(dev)
+                    for l in range(args.layers)]
+            rkv.reconstruct_multi(codecs, [torch.zeros_like(x) for x in sels], sels)
     torch.cuda.synchronize()
-    flags = codec.get_status()
-    print(json.dumps({"kernel_case": name, "T": w.T, "launches": codec.launch_count(),
-                      "status": flags}))
+    flags = 0
+    for c in codecs:
+        flags |= c.get_status()
+    print(json.dumps({"kernel_case": name, "T": w.T, "layers": args.layers,
+                      "launches": sum(c.launch_count() for c in codecs), "status": flags}))
     if flags:
         sys.exit(1)
 
@@ -1124,6 +1154,8 @@ def main():
     ap.add_argument("--kernel-case", action="store_true",
                     help="run one layer's prefill and two restores, for kernel captures")
     ap.add_argument("--tokens", type=int, default=0, help="override T for --kernel-case")
+    ap.add_argument("--layers", type=int, default=1,
+                    help="--kernel-case: layers restored together by one multi-context launch")
     ap.add_argument("--mean-precompute", action="store_true",
                     help="encoder mean from per-reference pre-activations (mean_precompute=1)")
     args = ap.parse_args()

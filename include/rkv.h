@@ -216,6 +216,29 @@ rkv_status rkv_reconstruct(rkv_ctx* ctx, const int32_t* seq, const int32_t* pos,
                            int32_t n_sel, void* k_out, void* v_out, void* stream);
 
 /*
+ * Restore the selections of several contexts in one launch (ResidualKV notes §2.5,
+ * §2.7: the same computation as one rkv_reconstruct per context).  Meant for the
+ * layers of one decode step whose selections are all known before their restores
+ * run (an index set chosen once per step for a group of sparse layers, as in the
+ * OmniKV combination, or independent selections); a layer whose selection depends
+ * on an earlier layer's attention must be restored by its own call.  One launch
+ * saves each further restore its own start-up and tail.
+ *   ctxs [n]: contexts of equal shape (N, D, d_c, topk, bits, batch, max_tokens,
+ *     max_refs, out_dtype, rope_base) on one device; each restores from its own
+ *     storage and W_d.  1 <= n <= 32.
+ *   seq[i], pos[i] (device, int32) [n_sel[i]], k_out[i], v_out[i] (device)
+ *     [n_sel[i], N, D]: as for rkv_reconstruct; n_sel[i] = 0 skips problem i.
+ * Bad selections raise the status bits of their own context; a kernel wait that
+ * times out is reported on ctxs[0].  The launch's timing is ctxs[0]'s; a call with
+ * one non-empty problem runs rkv_reconstruct's kernel on that context.
+ * Errors (nothing launched): RKV_EINVAL (NULL, n, mismatched contexts), RKV_EALIGN;
+ * RKV_ECUDA.
+ */
+rkv_status rkv_reconstruct_multi(rkv_ctx* const* ctxs, int32_t n, const int32_t* const* seq,
+                                 const int32_t* const* pos, const int32_t* n_sel,
+                                 void* const* k_out, void* const* v_out, void* stream);
+
+/*
  * Sparse-layer attention over restored K/V (ResidualKV notes §2.7, the output
  * equation o = softmax(q K_hat^T / sqrt(D)) V_hat over the selected tokens I_t).
  *   q (device, fp32) [n_q_heads, D]: the decode query, already rotated at its own

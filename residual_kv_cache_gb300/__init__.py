@@ -16,7 +16,7 @@ import torch
 
 __all__ = ["RkvError", "RkvLibraryMissing", "Config", "Codec", "lib", "LIB_PATH", "retrieve_noalloc",
            "FLAG_TIMEOUT", "FLAG_BAD_INDEX", "FLAG_UNWRITTEN", "FLAG_FP16_SAT", "FLAG_BAD_SLOT",
-           "ABI_FUNCTIONS"]
+           "ABI_FUNCTIONS", "reconstruct_multi"]
 
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "librkv.so")
 
@@ -72,6 +72,7 @@ ABI_FUNCTIONS = {
     "rkv_reconstruct": (_I32, [_P, _P, _P, _I32, _P, _P, _P]),
     "rkv_sparse_attention": (_I32, [_P, _P, _I32, _P, _P, _I32, _P, _P]),
     "rkv_restore_attend": (_I32, [_P, _P, _P, _I32, _P, _I32, _P, _P]),
+    "rkv_reconstruct_multi": (_I32, [_P, _I32, _P, _P, _P, _P, _P, _P]),
     "rkv_get_status": (_I32, [_P, ctypes.POINTER(_I32), _P]),
     "rkv_reset": (_I32, [_P, _I32, _P]),
     "rkv_pool_cache": (_I32, [_P, ctypes.POINTER(_P), ctypes.POINTER(ctypes.c_size_t)]),
@@ -260,6 +261,40 @@ def retrieve_noalloc(queries, q_pos, pool, pool_norm2, pool_pos, topk: int = 4, 
                                       pool_norm2.data_ptr(), pool_pos.data_ptr(), R, d, topk,
                                       out.data_ptr(), fp, _stream_ptr(stream)))
     return out
+
+
+def reconstruct_multi(codecs, seqs, poss, k_outs=None, v_outs=None, stream=None):
+    """Restore each codec's selection (seqs[i], poss[i]: int32 CUDA tensors) in one launch
+    (codecs of equal shape on one device).  Returns the lists (K_i, V_i)."""
+    n = len(codecs)
+    if n == 0 or len(seqs) != n or len(poss) != n:
+        raise ValueError("one seq and pos tensor per codec")
+    k_outs = list(k_outs) if k_outs is not None else [None] * n
+    v_outs = list(v_outs) if v_outs is not None else [None] * n
+    ns = []
+    for i, (c, sq, ps) in enumerate(zip(codecs, seqs, poss)):
+        for t in (sq, ps):
+            if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+                raise ValueError("seq and pos must be contiguous int32 CUDA tensors")
+        m = int(ps.numel())
+        if int(sq.numel()) != m:
+            raise ValueError("seq and pos must have the same length")
+        N, D = c.cfg.n_kv_heads, c.cfg.head_dim
+        odt = _torch_dtype(c.cfg.out_dtype)
+        if k_outs[i] is None:
+            k_outs[i] = torch.empty((m, N, D), dtype=odt, device=c.device)
+        if v_outs[i] is None:
+            v_outs[i] = torch.empty((m, N, D), dtype=odt, device=c.device)
+        _check_out(k_outs[i], m * N * D, odt, "k_out")
+        _check_out(v_outs[i], m * N * D, odt, "v_out")
+        ns.append(m)
+    P = ctypes.c_void_p * n
+    ctxs = P(*[c._ctx for c in codecs])
+    sp, pp_ = P(*[t.data_ptr() for t in seqs]), P(*[t.data_ptr() for t in poss])
+    kp, vp = P(*[t.data_ptr() for t in k_outs]), P(*[t.data_ptr() for t in v_outs])
+    nsel = (_I32 * n)(*ns)
+    _check(lib().rkv_reconstruct_multi(ctxs, n, sp, pp_, nsel, kp, vp, _stream_ptr(stream)))
+    return k_outs, v_outs
 
 
 class Codec:

@@ -206,6 +206,45 @@ __device__ __forceinline__ void dequant_groups(const ReconArgs& a, bool valid, c
   }
 }
 
+// The inputs that belong to one restore problem: its selection, storage and status
+// word.  A launch restores one problem, or several contexts' selections at once
+// (reconstruct_multi_kernel), whose token tiles it numbers one after the other.
+struct ProbView {
+  const int32_t* seq;
+  const int32_t* pos;
+  int n_sel;
+  const uint8_t* codes;
+  const uint32_t* meta;
+  const int32_t* ref_idx;
+  int* status;
+};
+
+struct ReconProblems {
+  int n;
+  int tile0[kReconMaxProblems + 1];   // first token tile of each problem; [n] = all tiles
+  const int32_t* seq[kReconMaxProblems];
+  const int32_t* pos[kReconMaxProblems];
+  int n_sel[kReconMaxProblems];
+  const uint8_t* codes[kReconMaxProblems];
+  const uint32_t* meta[kReconMaxProblems];
+  const int32_t* ref_idx[kReconMaxProblems];
+  const uint8_t* pool8[kReconMaxProblems];
+  void* k_out[kReconMaxProblems];
+  void* v_out[kReconMaxProblems];
+  int* status[kReconMaxProblems];
+};
+
+struct ReconMaps {
+  CUtensorMap tmW[kReconMaxProblems];   // each problem's W_d^T
+};
+
+// Problem of token tile T (tiles of problem i are [tile0[i], tile0[i + 1])).
+__device__ __forceinline__ int problem_of(const ReconProblems& mp, int T) {
+  int i = 0;
+  while (i + 1 < mp.n && T >= mp.tile0[i + 1]) ++i;
+  return i;
+}
+
 // Per-tile state of one epilogue thread's token row, packed into two registers.
 struct RowState {
   int flags;    // bit 0: the row has a readable code and a first reference; bits 1..4:
@@ -230,19 +269,19 @@ struct TileRow {
 // zaddr + 16 g; zeros for an invalid row).  Raises the device flags for bad selections.
 // With `next`, also loads the next tile's sequence and position of the row, so that the
 // next call starts with independent loads.
-__device__ __forceinline__ TileRow tile_setup(const ReconArgs& a, int m, int row, int wg,
-                                              int g0, int g_per, uint32_t zaddr, int s_,
-                                              int p_, bool next) {
+__device__ __forceinline__ TileRow tile_setup(const ReconArgs& a, const ProbView& v, int m,
+                                              int row, int wg, int g0, int g_per,
+                                              uint32_t zaddr, int s_, int p_, bool next) {
   TileRow tr;
   RowState& st = tr.st;
   const int64_t gi = (int64_t)m * kTileM + row;
-  const bool in_sel = gi < a.n_sel;
+  const bool in_sel = gi < v.n_sel;
   st.pos = 0;
   bool in_range = false;
   int64_t dst = 0;
   if (in_sel) {
     if (s_ < 0 || s_ >= a.B || p_ < 0 || p_ >= a.T_cap) {
-      if (wg == 0) atomicOr(a.status, RKV_FLAG_BAD_INDEX);
+      if (wg == 0) atomicOr(v.status, RKV_FLAG_BAD_INDEX);
     } else {
       in_range = true;
       dst = (int64_t)s_ * a.T_cap + p_;
@@ -255,17 +294,17 @@ __device__ __forceinline__ TileRow tile_setup(const ReconArgs& a, int m, int row
   uint4 cw[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) cw[i] = make_uint4(0u, 0u, 0u, 0u);
-  const uint8_t* crow = a.codes + dst * a.code_bytes;
+  const uint8_t* crow = v.codes + dst * a.code_bytes;
   if (in_range) {
 #pragma unroll
     for (int t = 0; t < 4; ++t)
-      if (t < a.topk) sl[t] = a.ref_idx[dst * a.topk + t];
+      if (t < a.topk) sl[t] = v.ref_idx[dst * a.topk + t];
     if (a.bits != 16) {
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         if (i < g_per) {
           const int g = g0 + i;
-          mt[i] = a.meta[dst * a.G + g];
+          mt[i] = v.meta[dst * a.G + g];
           if (a.bits == 4) {
             cw[i] = *reinterpret_cast<const uint4*>(crow + (int64_t)g * 16);
           } else {
@@ -278,19 +317,19 @@ __device__ __forceinline__ TileRow tile_setup(const ReconArgs& a, int m, int row
   }
   {
     const int64_t gn = gi + kTileM;
-    const bool nx = next && gn < a.n_sel;
-    tr.nx_s = nx ? a.seq[gn] : -1;
-    tr.nx_p = nx ? a.pos[gn] : -1;
+    const bool nx = next && gn < v.n_sel;
+    tr.nx_s = nx ? v.seq[gn] : -1;
+    tr.nx_p = nx ? v.pos[gn] : -1;
   }
   int kcnt = 0;
   bool valid = false;
 #pragma unroll
   for (int t = 0; t < 4; ++t) tr.r[t] = -1;
   if (in_range) {
-    if (sl[0] < 0 && wg == 0) atomicOr(a.status, RKV_FLAG_UNWRITTEN);
+    if (sl[0] < 0 && wg == 0) atomicOr(v.status, RKV_FLAG_UNWRITTEN);
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
-      if (sl[t] >= a.R_cap && wg == 0) atomicOr(a.status, RKV_FLAG_BAD_SLOT);
+      if (sl[t] >= a.R_cap && wg == 0) atomicOr(v.status, RKV_FLAG_BAD_SLOT);
       if (sl[t] >= 0 && sl[t] < a.R_cap) {
         tr.r[t] = s_ * a.R_cap + sl[t];
         ++kcnt;
@@ -329,17 +368,17 @@ __device__ __forceinline__ TileRow tile_setup(const ReconArgs& a, int m, int row
 // (flags as in RowState, position, pool rows of references 0..3 or -1, sequence), its
 // extremes and, with a.stage_codes, its packed codes (16-byte chunks, chunk c stored at
 // c ^ (row & a.chunk_mask)).  Raises the device flags for bad selections.
-__device__ __forceinline__ void stage_row(const ReconArgs& a, int m, int row, int* rec,
-                                          uint32_t* smeta, uint8_t* scodes) {
+__device__ __forceinline__ void stage_row(const ReconArgs& a, const ProbView& v, int m, int row,
+                                          int* rec, uint32_t* smeta, uint8_t* scodes) {
   const int64_t gi = (int64_t)m * kTileM + row;
-  const bool in_sel = gi < a.n_sel;
-  const int s_ = in_sel ? a.seq[gi] : -1;
-  const int p_ = in_sel ? a.pos[gi] : -1;
+  const bool in_sel = gi < v.n_sel;
+  const int s_ = in_sel ? v.seq[gi] : -1;
+  const int p_ = in_sel ? v.pos[gi] : -1;
   bool in_range = false;
   int64_t dst = 0;
   if (in_sel) {
     if (s_ < 0 || s_ >= a.B || p_ < 0 || p_ >= a.T_cap) {
-      atomicOr(a.status, RKV_FLAG_BAD_INDEX);
+      atomicOr(v.status, RKV_FLAG_BAD_INDEX);
     } else {
       in_range = true;
       dst = (int64_t)s_ * a.T_cap + p_;
@@ -349,15 +388,15 @@ __device__ __forceinline__ void stage_row(const ReconArgs& a, int m, int row, in
   if (in_range) {
 #pragma unroll
     for (int t = 0; t < 4; ++t)
-      if (t < a.topk) sl[t] = a.ref_idx[dst * a.topk + t];
+      if (t < a.topk) sl[t] = v.ref_idx[dst * a.topk + t];
   }
   int r[4] = {-1, -1, -1, -1};
   int kcnt = 0;
   if (in_range) {
-    if (sl[0] < 0) atomicOr(a.status, RKV_FLAG_UNWRITTEN);
+    if (sl[0] < 0) atomicOr(v.status, RKV_FLAG_UNWRITTEN);
 #pragma unroll
     for (int t = 0; t < 4; ++t) {
-      if (sl[t] >= a.R_cap) atomicOr(a.status, RKV_FLAG_BAD_SLOT);
+      if (sl[t] >= a.R_cap) atomicOr(v.status, RKV_FLAG_BAD_SLOT);
       if (sl[t] >= 0 && sl[t] < a.R_cap) {
         r[t] = s_ * a.R_cap + sl[t];
         ++kcnt;
@@ -375,9 +414,9 @@ __device__ __forceinline__ void stage_row(const ReconArgs& a, int m, int row, in
   for (int t = 0; t < 4; ++t) flags |= (r[t] >= 0 ? 1 : 0) << (1 + t);
   if (valid) {
     if (a.bits != 16)
-      for (int g = 0; g < a.G; ++g) smeta[row * a.G + g] = a.meta[dst * a.G + g];
+      for (int g = 0; g < a.G; ++g) smeta[row * a.G + g] = v.meta[dst * a.G + g];
     if (a.stage_codes) {
-      const uint8_t* crow = a.codes + dst * a.code_bytes;
+      const uint8_t* crow = v.codes + dst * a.code_bytes;
       uint8_t* srow = scodes + row * a.code_bytes;
       for (int c = 0; c < a.code_bytes / 16; ++c)
         cp_async16(srow + ((c ^ (row & a.chunk_mask)) << 4), crow + 16 * c);
@@ -409,10 +448,29 @@ __device__ __forceinline__ int unit_col(int j, int n_tiles) {
   return j;
 }
 
-template <bool kAttend>
-__global__ void __launch_bounds__(kReconThreads, 1)
-    reconstruct_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ ReconArgs a) {
+// The kernel body.  tmWs: W_d^T's tensor map (one per problem with kMulti); mp: the
+// problems of a multi-problem launch (unused otherwise: a's pointers are the problem).
+template <bool kAttend, bool kMulti>
+__device__ __forceinline__ void restore_body(const CUtensorMap* tmWs, const ReconArgs& a,
+                                             const ReconProblems* mp) {
   extern __shared__ uint8_t smem_raw[];
+  // problem of a token tile, its inputs, and the tile's index within the problem
+  auto view = [&](int pi) -> ProbView {
+    if constexpr (kMulti)
+      return ProbView{mp->seq[pi], mp->pos[pi], mp->n_sel[pi], mp->codes[pi],
+                      mp->meta[pi], mp->ref_idx[pi], mp->status[pi]};
+    else
+      return ProbView{a.seq, a.pos, a.n_sel, a.codes, a.meta, a.ref_idx, a.status};
+  };
+  auto tile_local = [&](int T, int& pi) -> int {
+    if constexpr (kMulti) {
+      pi = problem_of(*mp, T);
+      return T - mp->tile0[pi];
+    } else {
+      pi = 0;
+      return T;
+    }
+  };
   uint8_t* smem = align1024(smem_raw);
   const int nkb = a.dc / kTileK;
   uint8_t* sB = smem;                                       // b_stages x W_d^T k-block
@@ -444,12 +502,36 @@ __global__ void __launch_bounds__(kReconThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   pdl_launch_dependents();
-  // with kAttend the ranges are cut between pairs
+  // The CTA's units, in order.  One problem: a contiguous range, cost-balanced (with
+  // kAttend cut between pairs).  Several problems (kMulti): every gridDim-th token tile,
+  // each tile's units in a row, so that the CTAs work through the problems together and
+  // the L2 holds one or two problems' pools and weights at a time rather than all.
   constexpr int kSpan = kAttend ? 2 : 1;
-  const int u_begin = kSpan * range_start(blockIdx.x, gridDim.x, a.units / kSpan,
-                                          a.n_tiles / kSpan, kTileChangeCost4 / kSpan);
-  const int u_end = kSpan * range_start(blockIdx.x + 1, gridDim.x, a.units / kSpan,
-                                        a.n_tiles / kSpan, kTileChangeCost4 / kSpan);
+  int u_first = 0, u_count = 0, t_count = 0;          // first unit; units and tiles
+  if constexpr (kMulti) {
+    const int tiles = a.units / a.n_tiles, b = (int)blockIdx.x, gs = (int)gridDim.x;
+    t_count = tiles > b ? (tiles - b + gs - 1) / gs : 0;
+    u_count = t_count * a.n_tiles;
+  } else {
+    u_first = kSpan * range_start(blockIdx.x, gridDim.x, a.units / kSpan, a.n_tiles / kSpan,
+                                  kTileChangeCost4 / kSpan);
+    const int u_last = kSpan * range_start(blockIdx.x + 1, gridDim.x, a.units / kSpan,
+                                           a.n_tiles / kSpan, kTileChangeCost4 / kSpan);
+    u_count = u_last - u_first;
+    t_count = u_count > 0 ? (u_last - 1) / a.n_tiles - u_first / a.n_tiles + 1 : 0;
+  }
+  auto unit_at = [&](int k) -> int {                  // the CTA's k-th unit
+    if constexpr (kMulti)
+      return ((int)blockIdx.x + (k / a.n_tiles) * (int)gridDim.x) * a.n_tiles + k % a.n_tiles;
+    else
+      return u_first + k;
+  };
+  auto tile_at = [&](int j) -> int {                  // the CTA's j-th token tile
+    if constexpr (kMulti)
+      return (int)blockIdx.x + j * (int)gridDim.x;
+    else
+      return u_first / a.n_tiles + j;
+  };
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < a.b_stages; ++s) {
@@ -470,7 +552,7 @@ __global__ void __launch_bounds__(kReconThreads, 1)
     mbar_init(odone, 1);
     *abort_flag = 0;
     fence_barrier_init();
-    tma_prefetch(&tmW);
+    tma_prefetch(tmWs);
   }
   if (warp == 0) {
     tmem_alloc(tmem_slot, kTmemCols);
@@ -487,15 +569,19 @@ __global__ void __launch_bounds__(kReconThreads, 1)
       Ring ring;
       uint32_t issued = 0, issued_phase = 0;             // bit s: stage s used / its phase
       bool ok = true;
-      for (int u = u_begin; u < u_end && ok; ++u) {
+      int pw = 0;                                        // problem of unit u
+      for (int k = 0; k < u_count && ok; ++k) {
+        const int u = unit_at(k);
         const int n = unit_col<kAttend>(u % a.n_tiles, a.n_tiles);
+        if constexpr (kMulti)
+          while (pw + 1 < mp->n && u / a.n_tiles >= mp->tile0[pw + 1]) ++pw;
         for (int kb = 0; kb < nkb; ++kb) {
           if (!mbar_wait(&empty[ring.stage], ring.phase ^ 1u, abort_flag, a.status)) {
             ok = false;
             break;
           }
           mbar_arrive_expect_tx(&full[ring.stage], kBBytes);
-          tma_load_2d(sB + ring.stage * kBBytes, &tmW, &full[ring.stage], kb * kTileK, n * kNT);
+          tma_load_2d(sB + ring.stage * kBBytes, tmWs + pw, &full[ring.stage], kb * kTileK, n * kNT);
           issued |= 1u << ring.stage;
           issued_phase = (issued_phase & ~(1u << ring.stage)) | (ring.phase << ring.stage);
           ring.next(a.b_stages);
@@ -532,7 +618,8 @@ __global__ void __launch_bounds__(kReconThreads, 1)
             umma_bf16(d, sdesc_sw128(a0 + kb * (kTileM * 128) + k * 32),
                       sdesc_sw128(b0 + kb * kRowTile16 + k * 32), idesc16, (kb | k) != 0 ? 1u : 0u);
       };
-      for (int u = u_begin; u < u_end && ok; ++u) {
+      for (int k = 0; k < u_count && ok; ++k) {
+        const int u = unit_at(k);
         const int m = u / a.n_tiles;
         if (m != cur_m) {
           // with one z~ buffer, the previous tile's z~ may be overwritten once its MMAs
@@ -632,16 +719,19 @@ __global__ void __launch_bounds__(kReconThreads, 1)
     // (records, extremes, codes) staged in shared memory one tile ahead, so that a tile
     // change costs the epilogue no global round trip
     const int l = (int)threadIdx.x - 32 * kLoadWarp0;
-    if (u_begin < u_end) {
-      const int m_first = u_begin / a.n_tiles, m_last = (u_end - 1) / a.n_tiles;
+    {
       uint32_t free_phase = 0;
-      for (int m = m_first + 1; m <= m_last; ++m) {
-        if (m > m_first + 1) {
+      for (int j = 1; j < t_count; ++j) {
+        const int m = tile_at(j);
+        if (j > 1) {
           if (!mbar_wait(sfree, free_phase, abort_flag, a.status)) break;
           free_phase ^= 1u;
         }
-        stage_row(a, m, l, sRec + l * kRecInts, sMeta, sCodes);
-        stage_row(a, m, l + 64, sRec + (l + 64) * kRecInts, sMeta, sCodes);
+        int pl;
+        const int ml = tile_local(m, pl);
+        const ProbView v = view(pl);
+        stage_row(a, v, ml, l, sRec + l * kRecInts, sMeta, sCodes);
+        stage_row(a, v, ml, l + 64, sRec + (l + 64) * kRecInts, sMeta, sCodes);
         cp_async_arrive_noinc(staged);
         mbar_arrive(staged);
       }
@@ -675,7 +765,10 @@ __global__ void __launch_bounds__(kReconThreads, 1)
     const int cp_r0 = ew * 32 + (cl >> 1);             // copies rows cp_r0 and cp_r0 + 16
     uint8_t* cp_dst0 = pslots + half * kPlaneBytes + (uint32_t)cp_r0 * 32 +
                        (uint32_t)(((cl & 1) ^ ((cp_r0 >> 2) & 1)) * 16);
-    const uint8_t* cp_src0 = a.pool8 + (half ? xsec + P : xsec) + 16 * (cl & 1);
+    const int cp_off = (half ? xsec + P : xsec) + 16 * (cl & 1);
+    // kMulti: bits 0..7 the problem of the current tile, bits 8..15 the problem the
+    // thread's reference copies in flight are for (the next tile's, from its set-up on)
+    int pp = 0;
     const uint32_t zaddr = tmem + lane_base + kACol;  // this thread's z~ columns (buffer 0)
     const int g0 = wg * a.G / 4;                     // this group's code groups [g0, g0+g_per)
     const int g_per = (wg + 1) * a.G / 4 - g0;
@@ -685,8 +778,8 @@ __global__ void __launch_bounds__(kReconThreads, 1)
     // previous tile), then one arrival per warp on afull.
     int cp0[4], cp1[4];                               // pool rows this lane copies (per tile)
     int nx_s = -1, nx_p = -1;                         // the row of the next tile
-    auto setup_a = [&](int m) -> RowState {
-      const TileRow tr = tile_setup(a, m, row, wg, g0, g_per, zaddr, nx_s, nx_p, false);
+    auto setup_a = [&](int m, const ProbView& v) -> RowState {
+      const TileRow tr = tile_setup(a, v, m, row, wg, g0, g_per, zaddr, nx_s, nx_p, false);
       tc_fence_before();
       __syncwarp();
       if (lane_id() == 0) mbar_arrive(afull);
@@ -702,7 +795,9 @@ __global__ void __launch_bounds__(kReconThreads, 1)
     // row state and this lane's copy rows from the records, then one arrival per warp on
     // afull (the tensor core may start the tile) and on sfree (the loaders may restage).
     uint32_t staged_phase = 0;
-    auto setup_s = [&](int zb, RowState& st) -> bool {
+    auto setup_s = [&](int zb, RowState& st, int ps) -> bool {
+      const uint8_t* codes_s = a.codes;                // the staged tile's problem's codes
+      if constexpr (kMulti) codes_s = mp->codes[ps];
       const bool w = mbar_wait(staged, staged_phase, abort_flag, a.status);
       bool wa = __all_sync(0xffffffffu, w);
       if constexpr (kAttend) wa = bar_red_and(kHalfBar0 + (wg >> 1), 256, wa);
@@ -715,7 +810,7 @@ __global__ void __launch_bounds__(kReconThreads, 1)
       const uint32_t za = zaddr + (uint32_t)(zb * (a.dc / 2));
       const uint8_t* srow = sCodes + row * a.code_bytes;
       if (a.bits == 16) {
-        const uint8_t* crow = a.codes + ((int64_t)rec[6] * a.T_cap + rec[1]) * a.code_bytes;
+        const uint8_t* crow = codes_s + ((int64_t)rec[6] * a.T_cap + rec[1]) * a.code_bytes;
         for (int g = g0; g < g0 + g_per; ++g) {
           uint32_t o[16];
 #pragma unroll
@@ -730,7 +825,7 @@ __global__ void __launch_bounds__(kReconThreads, 1)
           tmem_st16(za + 16u * (uint32_t)g, o);
         }
       } else {
-        const uint8_t* crow = a.codes + ((int64_t)rec[6] * a.T_cap + rec[1]) * a.code_bytes;
+        const uint8_t* crow = codes_s + ((int64_t)rec[6] * a.T_cap + rec[1]) * a.code_bytes;
         uint32_t mt[4] = {0u, 0u, 0u, 0u};
         uint4 cw[4];
 #pragma unroll
@@ -793,7 +888,9 @@ __global__ void __launch_bounds__(kReconThreads, 1)
       if (active) {
         const int p0 = cp0[t], p1 = cp1[t];
         uint8_t* dst = cp_dst0 + (uint32_t)(t * 2) * kPlaneBytes;
-        const uint8_t* src = cp_src0 + n_next * kNT;
+        const uint8_t* pool = a.pool8;
+        if constexpr (kMulti) pool = mp->pool8[(pp >> 8) & 0xff];
+        const uint8_t* src = pool + cp_off + n_next * kNT;
         if (p0 >= 0) cp_async16(dst, src + (int64_t)p0 * a.dkv);
         if (p1 >= 0) cp_async16(dst + 16 * 32, src + (int64_t)p1 * a.dkv);
       }
@@ -837,20 +934,29 @@ __global__ void __launch_bounds__(kReconThreads, 1)
       if (hasB) po[(int64_t)gB * a.D] = __uint_as_float(ob) + __uint_as_float(ob2);
       return true;
     };
-    int u_done = u_begin;                              // == u_end unless the loop broke off
-    for (; u_done < u_end && ok; ++u_done) {
-      const int u = u_done;
+    int k_done = 0;                                    // == u_count unless the loop broke off
+    for (; k_done < u_count && ok; ++k_done) {
+      const int u = unit_at(k_done);
+      // the next unit (meaningful while k_done + 1 < u_count)
+      const int u_next = kMulti ? unit_at(k_done + 1) : u + 1;
       const int m = u / a.n_tiles, n = unit_col<kAttend>(u % a.n_tiles, a.n_tiles);
       if (m != cur_m) {
         if (cur_m < 0) {
-          const int64_t gi = (int64_t)m * kTileM + row;
-          nx_s = gi < a.n_sel ? a.seq[gi] : -1;
-          nx_p = gi < a.n_sel ? a.pos[gi] : -1;
-          cur = setup_a(m);
+          int p0 = 0, ml = m;
+          if constexpr (kMulti) {
+            ml = tile_local(m, p0);
+            pp = p0 | (p0 << 8);
+          }
+          const ProbView v = view(p0);
+          const int64_t gi = (int64_t)ml * kTileM + row;
+          nx_s = gi < v.n_sel ? v.seq[gi] : -1;
+          nx_p = gi < v.n_sel ? v.pos[gi] : -1;
+          cur = setup_a(ml, v);
 #pragma unroll
           for (int t = 0; t < 4; ++t) issue_ref(n, true, t);   // the first unit's copies
         } else {
           cur = nxt;                                   // z~ already set up before the last unit
+          if constexpr (kMulti) pp = ((pp >> 8) & 0xff) * 0x101;
           ++tt;
         }
         cur_m = m;
@@ -860,16 +966,19 @@ __global__ void __launch_bounds__(kReconThreads, 1)
       // go on while this unit's epilogue runs; with one z~ buffer, once the tensor core
       // is done with this tile.  From here on every copy this thread issues is for the
       // next tile.
-      if (u + 1 < u_end && (u + 1) / a.n_tiles != m) {
+      if (k_done + 1 < u_count && u_next / a.n_tiles != m) {
         if (a.zbufs == 1) {
           // both warps of the pair leave together, so neither waits at a barrier alone
           if (!bar_red_and(vote_id, vote_n, warp_wait(afree, afree_phase, abort_flag, a.status))) break;
           afree_phase ^= 1u;
         }
-        if (!setup_s((tt + 1) % a.zbufs, nxt)) break;
+        int pn = 0;
+        if constexpr (kMulti) pn = problem_of(*mp, u_next / a.n_tiles);
+        if (!setup_s((tt + 1) % a.zbufs, nxt, pn)) break;
+        if constexpr (kMulti) pp = (pp & 0xff) | (pn << 8);   // this unit's copies are the next tile's
       }
-      const bool more = u + 1 < u_end;
-      const int n_next = unit_col<kAttend>((u + 1) % a.n_tiles, a.n_tiles);
+      const bool more = k_done + 1 < u_count;
+      const int n_next = unit_col<kAttend>(u_next % a.n_tiles, a.n_tiles);
       const int c0 = n * kNT + hl * a.D;               // first KV_hat column of the head
       const bool is_k = c0 < a.dk;
       // ---- mean of the references: wait for this unit's copies of reference t (both
@@ -1098,10 +1207,18 @@ __global__ void __launch_bounds__(kReconThreads, 1)
         pdl_wait_previous_grid();
         waited = true;
       }
-      const int64_t grow = (int64_t)m * kTileM + row;
-      if (grow < a.n_sel) {
+      int64_t grow = (int64_t)m * kTileM + row;
+      int nsel_cur = a.n_sel;
+      void* kb_cur = a.k_out;
+      void* vb_cur = a.v_out;
+      if constexpr (kMulti) {
+        const int pc = pp & 0xff;
+        grow -= (int64_t)mp->tile0[pc] * kTileM;
+        nsel_cur = mp->n_sel[pc], kb_cur = mp->k_out[pc], vb_cur = mp->v_out[pc];
+      }
+      if (grow < nsel_cur) {
         const int64_t o0 = grow * a.dk + (is_k ? c0 : c0 - a.dk) + j0;
-        void* base = is_k ? a.k_out : a.v_out;
+        void* base = is_k ? kb_cur : vb_cur;
         if (a.out_f32) {
           float* o = static_cast<float*>(base) + o0;
           st_global_v8(o, reinterpret_cast<const uint32_t*>(mx));
@@ -1122,7 +1239,7 @@ __global__ void __launch_bounds__(kReconThreads, 1)
       }
     }
     if constexpr (kAttend) {
-      if (ok && u_done == u_end && u_end > u_begin) finish_o(u_end - 1);
+      if (ok && k_done == u_count && u_count > 0) finish_o(unit_at(u_count - 1));
     }
     cp_async_wait<0>();                                // no copy may outlive the CTA
   }
@@ -1133,6 +1250,20 @@ __global__ void __launch_bounds__(kReconThreads, 1)
     tc_fence_after();
     tmem_dealloc(tmem, kTmemCols);
   }
+}
+
+template <bool kAttend>
+__global__ void __launch_bounds__(kReconThreads, 1)
+    reconstruct_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ ReconArgs a) {
+  restore_body<kAttend, false>(&tmW, a, nullptr);
+}
+
+// Several contexts' selections in one launch: a's dimensions, tables and wait status
+// are shared, mp holds each problem's inputs and outputs, mm its W_d^T map.
+__global__ void __launch_bounds__(kReconThreads, 1)
+    reconstruct_multi_kernel(const __grid_constant__ ReconMaps mm, const __grid_constant__ ReconArgs a,
+                             const __grid_constant__ ReconProblems mp) {
+  restore_body<false, true>(mm.tmW, a, &mp);
 }
 
 }  // namespace
@@ -1229,6 +1360,64 @@ cudaError_t launch_reconstruct(rkv_ctx* c, const int32_t* seq, const int32_t* po
   a.v_out = v_out;
   const int grid = a.units < c->num_sms ? a.units : c->num_sms;
   return recon_launch<false>(c, a, smem, grid, &c->recon_smem, "rkv_reconstruct_kernel", s);
+}
+
+cudaError_t launch_reconstruct_multi(rkv_ctx* const* cs, int n, const int32_t* const* seqs,
+                                     const int32_t* const* poss, const int32_t* n_sels,
+                                     void* const* k_outs, void* const* v_outs, cudaStream_t s) {
+  ReconProblems mp{};                 // launch parameters (copied when the kernel is launched)
+  ReconMaps mm;
+  rkv_ctx* c0 = cs[0];
+  mp.n = n;
+  int tiles = 0, first = -1;
+  for (int i = 0; i < n; ++i) {
+    mp.tile0[i] = tiles;
+    tiles += (n_sels[i] + kTileM - 1) / kTileM;
+    mp.seq[i] = seqs[i];
+    mp.pos[i] = poss[i];
+    mp.n_sel[i] = n_sels[i];
+    mp.codes[i] = static_cast<const uint8_t*>(cs[i]->st.codes);
+    mp.meta[i] = static_cast<const uint32_t*>(cs[i]->st.meta);
+    mp.ref_idx[i] = cs[i]->st.ref_idx;
+    mp.pool8[i] = static_cast<const uint8_t*>(cs[i]->st.pool_fp8);
+    mp.k_out[i] = k_outs[i];
+    mp.v_out[i] = v_outs[i];
+    mp.status[i] = cs[i]->status;
+    mm.tmW[i] = cs[i]->tm_wd;
+    if (first < 0 && n_sels[i] > 0) first = i;
+  }
+  mp.tile0[n] = tiles;
+  if (tiles == 0) return cudaSuccess;
+  ReconArgs a;
+  size_t smem = 0;
+  cudaError_t e = recon_setup(c0, seqs[first], poss[first], n_sels[first], 0, &a, &smem);
+  if (e != cudaSuccess) return e;
+  a.units = tiles * a.n_tiles;
+  a.k_out = k_outs[first];
+  a.v_out = v_outs[first];
+  if (c0->multi_smem < (int)smem) {
+    e = cudaFuncSetAttribute(reconstruct_multi_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)smem);
+    if (e != cudaSuccess) return e;
+    c0->multi_smem = (int)smem;
+  }
+  const int grid = a.units < c0->num_sms ? a.units : c0->num_sms;
+  cudaEvent_t ev;
+  timing_begin(c0, "rkv_reconstruct_multi_kernel", s, &ev);
+  cudaLaunchConfig_t lc = {};
+  lc.gridDim = dim3(grid);
+  lc.blockDim = dim3(kReconThreads);
+  lc.dynamicSmemBytes = smem;
+  lc.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  e = cudaLaunchKernelEx(&lc, reconstruct_multi_kernel, mm, a, mp);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  timing_end(c0, "rkv_reconstruct_multi_kernel", s, ev);
+  return e;
 }
 
 cudaError_t launch_restore_attend(rkv_ctx* c, const int32_t* seq, const int32_t* pos, int n_sel,

@@ -809,6 +809,48 @@ rkv_status rkv_reconstruct(rkv_ctx* c, const int32_t* seq, const int32_t* pos, i
   return RKV_OK;
 }
 
+rkv_status rkv_reconstruct_multi(rkv_ctx* const* ctxs, int32_t n, const int32_t* const* seq,
+                                 const int32_t* const* pos, const int32_t* n_sel,
+                                 void* const* k_out, void* const* v_out, void* stream) {
+  if (!ctxs || !seq || !pos || !n_sel || !k_out || !v_out)
+    return fail(RKV_EINVAL, "NULL argument array");
+  if (n < 1 || n > kReconMaxProblems)
+    return fail(RKV_EINVAL, "n must be in [1, %d]", kReconMaxProblems);
+  const rkv_ctx* c0 = ctxs[0];
+  if (!c0) return fail(RKV_EINVAL, "ctxs[0] is NULL");
+  const Dims& d = c0->d;
+  for (int i = 0; i < n; ++i) {
+    const rkv_ctx* c = ctxs[i];
+    if (!c) return fail(RKV_EINVAL, "ctxs[%d] is NULL", i);
+    const Dims& e = c->d;
+    // one kernel serves all: every dimension, format and table must agree
+    if (c->device != c0->device || e.N != d.N || e.D != d.D || e.dc != d.dc || e.topk != d.topk ||
+        e.bits != d.bits || e.B != d.B || e.T_cap != d.T_cap || e.R_cap != d.R_cap ||
+        e.out_f32 != d.out_f32 || c->cfg.rope_base != c0->cfg.rope_base)
+      return fail(RKV_EINVAL, "ctxs[%d] differs from ctxs[0] in device, shape, format or tables", i);
+    if (n_sel[i] < 0) return fail(RKV_EINVAL, "n_sel[%d] < 0", i);
+    if (n_sel[i] == 0) continue;
+    if (!seq[i] || !pos[i] || !k_out[i] || !v_out[i])
+      return fail(RKV_EINVAL, "NULL seq, pos or output of problem %d", i);
+    if ((reinterpret_cast<uintptr_t>(k_out[i]) & 31u) || (reinterpret_cast<uintptr_t>(v_out[i]) & 31u) ||
+        (reinterpret_cast<uintptr_t>(seq[i]) & 3u) || (reinterpret_cast<uintptr_t>(pos[i]) & 3u))
+      return fail(RKV_EALIGN, "problem %d: outputs must be 32-byte aligned, seq/pos 4-byte aligned", i);
+  }
+  // one problem with tokens: the single restore (its ranges are balanced for one problem)
+  int live = 0, only = -1;
+  for (int i = 0; i < n; ++i)
+    if (n_sel[i] > 0) ++live, only = i;
+  if (live == 0) return RKV_OK;
+  if (live == 1) {
+    CUDA_OK(launch_reconstruct(const_cast<rkv_ctx*>(ctxs[only]), seq[only], pos[only], n_sel[only],
+                               k_out[only], v_out[only], static_cast<cudaStream_t>(stream)));
+    return RKV_OK;
+  }
+  CUDA_OK(launch_reconstruct_multi(const_cast<rkv_ctx* const*>(ctxs), n, seq, pos, n_sel, k_out,
+                                   v_out, static_cast<cudaStream_t>(stream)));
+  return RKV_OK;
+}
+
 rkv_status rkv_sparse_attention(rkv_ctx* c, const float* q, int32_t n_q_heads, const void* k,
                                 const void* v, int32_t n, float* out, void* stream) {
   if (!c) return fail(RKV_EINVAL, "ctx is NULL");

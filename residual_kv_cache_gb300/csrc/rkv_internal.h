@@ -18,6 +18,7 @@ constexpr int kRefTile = 256;      // references per retrieval tile
 constexpr int kEncN = 256;         // GEMM-1/2 N tile: 128 W_c1 + 128 W_c2 columns
 constexpr int kDecN = 128;         // decoder N tile (one head of D = 128)
 constexpr int kRopeLo = 512;       // positions per low RoPE table
+constexpr int kReconMaxProblems = 32;   // contexts one rkv_reconstruct_multi launch restores
 
 // Derived sizes of a configuration.
 struct Dims {
@@ -98,6 +99,7 @@ struct rkv_ctx {
   float* fa_ws = nullptr;         // restore + attention partials (m, l, o) per token tile and
                                   // query head: up to kAttnMaxTokens / 128 tiles x 8 N heads
   int fused_smem = 0;             // dynamic shared memory the fused kernel is set up for
+  int multi_smem = 0;             // ... and the multi-context restore kernel
   int units_cap = 0;
   int32_t* plan_dev[2] = {nullptr, nullptr};
   int32_t* plan_host[2] = {nullptr, nullptr};   // pinned staging
@@ -155,6 +157,11 @@ cudaError_t launch_gemm3_quant(rkv_ctx* c, const PassPlan& p, const int32_t* pla
 cudaError_t launch_pool_preact(rkv_ctx* c, const int32_t* tiles, int n_tiles, cudaStream_t s);
 cudaError_t launch_reconstruct(rkv_ctx* c, const int32_t* seq, const int32_t* pos, int n_sel,
                                void* k_out, void* v_out, cudaStream_t s);
+// One launch restoring the selections of n <= kReconMaxProblems contexts of equal
+// dimensions (validated by the caller); the timing slot is the first context's.
+cudaError_t launch_reconstruct_multi(rkv_ctx* const* cs, int n, const int32_t* const* seqs,
+                                     const int32_t* const* poss, const int32_t* n_sels,
+                                     void* const* k_outs, void* const* v_outs, cudaStream_t s);
 
 cudaError_t launch_timeout_probe(rkv_ctx* c, cudaStream_t s);
 
