@@ -167,6 +167,12 @@ MEASURED_TRAFFIC = {
     ("qwen7b", "rkv_reconstruct_kernel"): {"file": "k_reconstruct.cu",
                                            "code_sha1": "5198262cc641e670ca2a24f8616c6b236a0804fa",
                                            "bytes": 15855104 + 24869888},
+    # one launch over the 28 layers: a capture of the same kernel over 4 layers (157184
+    # tokens, dram read 62619904 + write 266115584 bytes), scaled by 28 / 4 (every term of
+    # its traffic, pools, codes and outputs, is per problem)
+    ("qwen7b", "rkv_reconstruct_multi_kernel"): {"file": "k_reconstruct.cu",
+                                                 "code_sha1": "5f712fbabd15b4ae5b185c817fc77fbd5cd0b90b",
+                                                 "bytes": (62619904 + 266115584) * 7},
     ("llama8b", "rkv_retrieve_kernel"): {"file": "k_retrieve.cu",
                                          "code_sha1": "aa7c494b08aad67b44f721081daffd90bc65a63e",
                                          "bytes": 134541056 + 3821568},
