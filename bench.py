@@ -162,11 +162,11 @@ def algorithmic_work(w, n_comp: int, n_sel: int, ref_pos, T: int | None = None) 
 # while the kernel's code is unchanged since the capture (code_sha1 below).
 MEASURED_TRAFFIC = {
     ("llama8b", "rkv_reconstruct_kernel"): {"file": "k_reconstruct.cu",
-                                            "code_sha1": "5198262cc641e670ca2a24f8616c6b236a0804fa",
-                                            "bytes": 10437376 + 52480},
+                                            "code_sha1": "5f712fbabd15b4ae5b185c817fc77fbd5cd0b90b",
+                                            "bytes": 10437888 + 68096},
     ("qwen7b", "rkv_reconstruct_kernel"): {"file": "k_reconstruct.cu",
-                                           "code_sha1": "5198262cc641e670ca2a24f8616c6b236a0804fa",
-                                           "bytes": 15855104 + 24869888},
+                                           "code_sha1": "5f712fbabd15b4ae5b185c817fc77fbd5cd0b90b",
+                                           "bytes": 15861760 + 25484032},
     # one launch over the 28 layers: a capture of the same kernel over 4 layers (157184
     # tokens, dram read 62619904 + write 266115584 bytes), scaled by 28 / 4 (every term of
     # its traffic, pools, codes and outputs, is per problem)
