@@ -4,8 +4,9 @@
 // tokens are restored).
 //
 // Work unit = (tile of 128 selected tokens, 128 output columns = one head for D = 128,
-// two for D = 64).  A CTA owns a contiguous range of units, so consecutive units share
-// the token tile.  Two loader warps stage each later token tile of the range in shared
+// two for D = 64).  A CTA owns a contiguous range of units (with several problems in one
+// launch: every gridDim-th token tile, each with all its units), so consecutive units
+// share the token tile.  Two loader warps stage each later token tile of the CTA in shared
 // memory while the previous tile is restored: per row its record (validity, k_i,
 // position, pool rows of its references), its extremes and, for code rows of at most
 // 128 bytes, its codes.  Per token tile, the 512 epilogue threads (four warpgroups; the

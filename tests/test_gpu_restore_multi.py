@@ -2,8 +2,9 @@
 computation as one rkv_reconstruct per context (ResidualKV notes §2.5 decode and mean,
 §2.1 RoPE at the token's own position, §2.7 only the selected tokens), so the outputs
 must be identical bit for bit.  The token tiles of all problems are numbered one after
-the other and cut into one range per CTA, so ranges cross problems (a CTA switches
-storage, pool and W_d between two tiles); covered with INT4 code rows read from global
+the other and dealt to the CTAs in a stride (CTA b takes tiles b, b + G, ...), so a CTA
+works on several problems (it switches storage, pool and W_d between two tiles, and
+prefetches the next tile's W_d while the current one runs); covered with INT4 code rows read from global
 memory (Llama shape, one z~ buffer) and staged (Qwen shape, two z~ buffers), fp32
 outputs (the tiny shape), empty and one-token problems, two sequences per context."""
 import numpy as np
